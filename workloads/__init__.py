@@ -1,0 +1,262 @@
+"""Seeded synthetic inputs for the packed CTC loss.
+
+This module only draws inputs: utterance lengths, target sequences and
+log-softmax log probabilities laid out token-flat.  It holds none of the
+CTC arithmetic, so both the fp64 oracle and the CUDA path can be fed the
+very same batch.
+
+The five named workloads follow the shapes, sizes and value distributions
+of the packed-CTC benchmark configurations:
+
+* ``tiny``      -- 4 utterances, T=[50,37,64,20], D=32, U=[10,8,12,4], fp32
+* ``conformer`` -- 32 utterances, T~U[200,400], D=1025, U~U[T/6,T/4],
+                   10% forced adjacent repeats, N(0,3^2) logits, bf16, mean
+* ``longform``  -- 8 utterances, T~U[1500,2000], D=1025, U~U[T/4,T/3], fp32,
+                   plus one infeasible all-repeat utterance, zero_infinity, sum
+* ``char``      -- 256 utterances, T~U[100,1000], D=29, U~U[T/8,T/3],
+                   20% forced adjacent repeats, fp16, mean
+* ``largevocab``-- 64 utterances, T~U[400,800], D=8193, U~U[T/8,T/4],
+                   N(0,3^2) logits, bf16, none
+
+Readings of the distribution wording (the same for every workload):
+"uniform in [a, b]" draws integers with both ends included; ``U ~ U[T/k, T/m]``
+draws from ``[ceil(T/k), floor(T/m)]``; "x% forced adjacent repeats" lets each
+target position i >= 1 copy position i-1 with probability x, and a sequence
+that this makes infeasible (T < U + repeats) is drawn again.  Logits are
+float32 N(0, sigma^2), the log-softmax is taken in float32 and then cast.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence
+
+import torch
+
+__all__ = ["Batch", "WORKLOADS", "make_batch", "workload", "padded_targets", "select_utterances"]
+
+
+@dataclasses.dataclass
+class Batch:
+    """One packed batch, all tensors on the CPU.
+
+    ``log_probs`` is ``(T_total, D)``; utterance ``b`` owns rows
+    ``[cu_seqlens[b], cu_seqlens[b] + lengths[b])``.  ``targets`` holds the
+    target sequences concatenated (``sum(target_lengths)`` int32 entries).
+    """
+
+    name: str
+    log_probs: torch.Tensor
+    cu_seqlens: torch.Tensor
+    lengths: torch.Tensor
+    targets: torch.Tensor
+    target_lengths: torch.Tensor
+    blank: int
+    zero_infinity: bool
+    reduction: str
+    max_target_len: int
+
+    @property
+    def B(self) -> int:
+        return int(self.lengths.numel())
+
+    @property
+    def D(self) -> int:
+        return int(self.log_probs.shape[1])
+
+    @property
+    def T_total(self) -> int:
+        return int(self.log_probs.shape[0])
+
+    @property
+    def frames(self) -> int:
+        return int(self.lengths.sum())
+
+
+def _uniform_int(gen: torch.Generator, lo: int, hi: int) -> int:
+    """Integer uniform on [lo, hi], both ends included."""
+    return int(torch.randint(lo, hi + 1, (1,), generator=gen).item())
+
+
+def _draw_targets(gen, length, lo, hi, repeat_prob):
+    labels = torch.randint(lo, hi + 1, (length,), generator=gen)
+    if repeat_prob > 0 and length > 1:
+        copy = torch.rand(length, generator=gen) < repeat_prob
+        for i in range(1, length):
+            if copy[i]:
+                labels[i] = labels[i - 1]
+    return labels
+
+
+def _adjacent_repeats(labels: torch.Tensor) -> int:
+    if labels.numel() < 2:
+        return 0
+    return int((labels[1:] == labels[:-1]).sum())
+
+
+def make_batch(
+    lengths: Sequence[int],
+    target_lengths: Sequence[int],
+    num_classes: int,
+    *,
+    dtype: torch.dtype = torch.float32,
+    seed: int = 0,
+    sigma: float = 2.0,
+    label_low: int = 1,
+    label_high: Optional[int] = None,
+    repeat_prob: float = 0.0,
+    blank: int = 0,
+    zero_infinity: bool = False,
+    reduction: str = "none",
+    targets: Optional[Sequence[Sequence[int]]] = None,
+    max_target_len: Optional[int] = None,
+    gaps: Optional[Sequence[int]] = None,
+    redraw_infeasible: bool = False,
+    name: str = "custom",
+) -> Batch:
+    """Build a packed batch with the given per-utterance frame and target counts.
+
+    ``gaps[b]`` extra rows may follow utterance ``b`` inside its cu_seqlens
+    span (a gapped layout); those rows hold log probabilities too but belong
+    to no utterance.
+    """
+    gen = torch.Generator().manual_seed(seed)
+    B = len(lengths)
+    label_high = num_classes - 1 if label_high is None else label_high
+    gaps = [0] * B if gaps is None else list(gaps)
+    seqs: List[torch.Tensor] = []
+    for b in range(B):
+        if targets is not None:
+            seq = torch.as_tensor(list(targets[b])[: target_lengths[b]], dtype=torch.int64)
+        else:
+            for _ in range(1000):
+                seq = _draw_targets(gen, int(target_lengths[b]), label_low, label_high, repeat_prob)
+                if not redraw_infeasible or lengths[b] >= seq.numel() + _adjacent_repeats(seq):
+                    break
+        seqs.append(seq)
+    spans = [int(lengths[b]) + int(gaps[b]) for b in range(B)]
+    cu = [0]
+    for s in spans:
+        cu.append(cu[-1] + s)
+    T_total = cu[-1]
+    logits = torch.randn(T_total, num_classes, generator=gen, dtype=torch.float32) * sigma
+    log_probs = torch.log_softmax(logits, dim=-1).to(dtype)
+    flat = torch.cat(seqs) if seqs else torch.zeros(0, dtype=torch.int64)
+    mtl = max([int(t) for t in target_lengths] + [0]) if max_target_len is None else max_target_len
+    return Batch(
+        name=name,
+        log_probs=log_probs,
+        cu_seqlens=torch.tensor(cu, dtype=torch.int32),
+        lengths=torch.tensor(list(lengths), dtype=torch.int32),
+        targets=flat.to(torch.int32),
+        target_lengths=torch.tensor(list(target_lengths), dtype=torch.int32),
+        blank=blank,
+        zero_infinity=zero_infinity,
+        reduction=reduction,
+        max_target_len=mtl,
+    )
+
+
+def _tiny():
+    return make_batch([50, 37, 64, 20], [10, 8, 12, 4], 32, dtype=torch.float32, seed=0, sigma=2.0,
+                      label_low=1, label_high=31, reduction="none", zero_infinity=False, name="tiny")
+
+
+def _lengths(gen, B, t_lo, t_hi, u_num_lo, u_den_lo, u_num_hi, u_den_hi):
+    Ts, Us = [], []
+    for _ in range(B):
+        T = _uniform_int(gen, t_lo, t_hi)
+        lo = math.ceil(T * u_num_lo / u_den_lo)
+        hi = (T * u_num_hi) // u_den_hi
+        Ts.append(T)
+        Us.append(_uniform_int(gen, lo, hi))
+    return Ts, Us
+
+
+def _conformer():
+    gen = torch.Generator().manual_seed(0)
+    Ts, Us = _lengths(gen, 32, 200, 400, 1, 6, 1, 4)
+    return make_batch(Ts, Us, 1025, dtype=torch.bfloat16, seed=1, sigma=3.0, label_low=1, label_high=1024,
+                      repeat_prob=0.10, redraw_infeasible=True, reduction="mean", name="conformer")
+
+
+def _longform():
+    gen = torch.Generator().manual_seed(0)
+    Ts, Us = _lengths(gen, 8, 1500, 2000, 1, 4, 1, 3)
+    T_bad = _uniform_int(gen, 1500, 2000)
+    U_bad = T_bad // 2 + 1
+    bad_label = _uniform_int(gen, 1, 1024)
+    lab_gen = torch.Generator().manual_seed(2)
+    seqs = [torch.randint(1, 1025, (u,), generator=lab_gen).tolist() for u in Us]
+    seqs.append([bad_label] * U_bad)
+    return make_batch(Ts + [T_bad], Us + [U_bad], 1025, dtype=torch.float32, seed=1, sigma=2.0, targets=seqs,
+                      zero_infinity=True, reduction="sum", name="longform")
+
+
+def _char():
+    gen = torch.Generator().manual_seed(0)
+    Ts, Us = _lengths(gen, 256, 100, 1000, 1, 8, 1, 3)
+    return make_batch(Ts, Us, 29, dtype=torch.float16, seed=1, sigma=2.0, label_low=1, label_high=28,
+                      repeat_prob=0.20, redraw_infeasible=True, reduction="mean", name="char")
+
+
+def _largevocab():
+    gen = torch.Generator().manual_seed(0)
+    Ts, Us = _lengths(gen, 64, 400, 800, 1, 8, 1, 4)
+    return make_batch(Ts, Us, 8193, dtype=torch.bfloat16, seed=1, sigma=3.0, label_low=1, label_high=8192,
+                      reduction="none", name="largevocab")
+
+
+WORKLOADS = {
+    "tiny": _tiny,
+    "conformer": _conformer,
+    "longform": _longform,
+    "char": _char,
+    "largevocab": _largevocab,
+}
+
+
+def workload(name: str) -> Batch:
+    """One of the five named benchmark workloads, generated from seed 0."""
+    return WORKLOADS[name]()
+
+
+def padded_targets(batch: Batch, width: Optional[int] = None, fill: int = 0) -> torch.Tensor:
+    """The concatenated targets as a padded ``(B, width)`` int64 tensor."""
+    width = batch.max_target_len if width is None else width
+    out = torch.full((batch.B, max(width, 0)), fill, dtype=torch.int64)
+    off = 0
+    for b in range(batch.B):
+        u = int(batch.target_lengths[b])
+        out[b, :u] = batch.targets[off: off + u].to(torch.int64)
+        off += u
+    return out
+
+
+def select_utterances(batch: Batch, index: Sequence[int]) -> Batch:
+    """A new tight batch made of the chosen utterances (rows copied out)."""
+    toff = [0]
+    for u in batch.target_lengths.tolist():
+        toff.append(toff[-1] + int(u))
+    rows, seqs, Ts, Us, cu = [], [], [], [], [0]
+    for b in index:
+        s = int(batch.cu_seqlens[b])
+        T = int(batch.lengths[b])
+        rows.append(batch.log_probs[s: s + T])
+        seqs.append(batch.targets[toff[b]: toff[b + 1]])
+        Ts.append(T)
+        Us.append(int(batch.target_lengths[b]))
+        cu.append(cu[-1] + T)
+    return Batch(
+        name=f"{batch.name}[{len(index)}]",
+        log_probs=torch.cat(rows) if rows else batch.log_probs[:0],
+        cu_seqlens=torch.tensor(cu, dtype=torch.int32),
+        lengths=torch.tensor(Ts, dtype=torch.int32),
+        targets=torch.cat(seqs) if seqs else batch.targets[:0],
+        target_lengths=torch.tensor(Us, dtype=torch.int32),
+        blank=batch.blank,
+        zero_infinity=batch.zero_infinity,
+        reduction=batch.reduction,
+        max_target_len=max(Us + [0]),
+    )
