@@ -1,0 +1,425 @@
+"""Benchmark of the packed CTC loss forward + backward on GB300.
+
+One step is one ``ctc_packed_forward`` + one ``ctc_packed_backward`` (upstream
+gradient 1) over the large-vocabulary workload: 64 utterances, T ~ U[400,800]
+frames, D = 8193 classes, U ~ U[T/8, T/4] targets, bfloat16 log-softmax of
+N(0, 3^2) logits, reduction none.  Its 638 MB of log probabilities exceed the
+129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0): frames/s over the whole job, the roofline of
+the dominant kernel (the gradient kernel, timed live with CUDA events on its
+stream), the whole-path roofline, an end-to-end figure through the C-ABI with
+host buffers, the SM clocks sampled during the timed region, and the fp64
+CPU oracle timed on a bounded sample on this host.
+
+``--impl reference`` times the reference arm instead: the fp64 oracle, as it
+stands, on the host cores, on a bounded sample of the same workload per step.
+Under torchrun every rank runs its own replica of the workload (weak scaling,
+no data-path collective).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "packed CTC fwd+bwd frames/s and achieved HBM GB/s (% of GB300 peak)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="largevocab")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _workload_description(batch):
+    lengths = batch.lengths.tolist()
+    tls = batch.target_lengths.tolist()
+    dt = {"torch.float32": "fp32", "torch.bfloat16": "bf16", "torch.float16": "fp16"}[str(batch.log_probs.dtype)]
+    return {
+        "workload": f"{batch.name}: B={batch.B}, T_total={batch.T_total}, D={batch.D}, {dt} log probs, "
+                    f"reduction={batch.reduction}",
+        "B": batch.B,
+        "T_total": batch.T_total,
+        "frames": int(sum(lengths)),
+        "D": batch.D,
+        "io_dtype": dt,
+        "max_target_len": batch.max_target_len,
+        "target_len_range": [min(tls), max(tls)] if tls else [0, 0],
+        "reduction": batch.reduction,
+        "zero_infinity": batch.zero_infinity,
+        "l2": f"inputs larger than L2 ({batch.T_total * batch.D * batch.log_probs.element_size() / 1e6:.0f} MB "
+              "of log probabilities per step)",
+    }
+
+
+def algorithmic_bytes(batch):
+    """Bytes the path must move: the forward's
+    label-column gathers, the alpha store and reload (fp32), the full dense
+    read of the log probabilities and write of the gradient."""
+    e = batch.log_probs.element_size()
+    D = batch.D
+    gather = alpha = 0
+    for T, U in zip(batch.lengths.tolist(), batch.target_lengths.tolist()):
+        S = 2 * U + 1
+        gather += T * min(U + 1, D) * e
+        alpha += 2 * T * S * 4
+    dense = 2 * batch.T_total * D * e
+    grad_kernel = dense + alpha // 2  # the gradient kernel reads lp, writes grad, reloads alpha
+    return {"gather": gather, "alpha": alpha, "dense": dense, "total": gather + alpha + dense,
+            "grad_kernel": grad_kernel}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_query_id):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.gpu = gpu_query_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu is not None:
+            cmd += ["-i", str(self.gpu)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def snapshot(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits"]
+        if self.gpu is not None:
+            cmd += ["-i", str(self.gpu)]
+        try:
+            out = subprocess.run(cmd, capture_output=True, text=True, timeout=20).stdout.strip().splitlines()
+            if out:
+                self.samples.append((time.time(), out[0]))
+        except Exception:
+            pass
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.3]
+        use = inside or rows[-1:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for _, p in use if num(p[1]) is not None]
+        smax = [num(p[2]) for _, p in use if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in use for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use), "in_window": len(inside),
+                "power_w_max": max([num(p[3]) for _, p in use if num(p[3]) is not None] or [0])}
+
+
+def _gpu_query_id(torch, dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+def cpu_baseline(batch, seconds, steps=1, warmup=0):
+    """Time the fp64 oracle (as it stands) on a bounded sample of utterances."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    threads = oracle.max_threads()
+    lengths = batch.lengths.tolist()
+    # calibrate on two utterances, then take as many as fit the time budget
+    probe = workloads.select_utterances(batch, [0, 1] if batch.B > 1 else [0])
+    t = time.perf_counter()
+    oracle.oracle_batch(probe, threads=1)
+    per_frame = (time.perf_counter() - t) / max(1, probe.frames)
+    budget_frames = seconds * threads / max(per_frame, 1e-9)
+    take, frames = [], 0
+    for b in range(batch.B):
+        if take and frames + lengths[b] > budget_frames:
+            break
+        take.append(b)
+        frames += lengths[b]
+    sample = workloads.select_utterances(batch, take)
+    for _ in range(warmup):
+        oracle.oracle_batch(sample, threads=threads)
+    times = []
+    for _ in range(steps):
+        t = time.perf_counter()
+        oracle.oracle_batch(sample, threads=threads)
+        times.append(time.perf_counter() - t)
+    dt = float(np.mean(times))
+    return {"value": sample.frames / dt, "unit": "frames/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(take)} of {batch.B} utterances ({sample.frames} frames) of the same workload, "
+                      f"fp64 loss + gradient, OpenMP over utterances",
+            "seconds_per_sample": dt}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    import workloads
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    batch = workloads.workload(args.workload, device=dev)
+    batch.log_probs = batch.log_probs.cpu()
+    # each step is a sample sized so that warmup + steps end within a few minutes
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    base = cpu_baseline(batch, per_step, steps=args.steps, warmup=args.warmup)
+    cfg = _workload_description(batch)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "frames/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": base["seconds_per_sample"] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": cfg,
+        "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": base["value"], "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import packed_sequence_ctc_gb300 as pk
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    batch = workloads.workload(args.workload, device=dev)
+    lp = batch.log_probs.contiguous()
+    cu, ln, tg, tl = (x.to(dev) for x in (batch.cu_seqlens, batch.lengths, batch.targets, batch.target_lengths))
+    B, T_total, D = batch.B, batch.T_total, batch.D
+    mtl = batch.max_target_len
+    red = batch.reduction
+    ws = pk.Workspace(T_total, B, mtl, D, lp.dtype, dev).tensor
+    nloss = B if red == "none" else 1
+    loss = torch.empty(nloss, dtype=torch.float32, device=dev)
+    g_up = torch.ones(nloss, dtype=torch.float32, device=dev)
+    grad = torch.empty_like(lp)
+
+    def step():
+        pk.ctc_packed_forward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, loss, ws, mtl,
+                              stream=stream)
+        pk.ctc_packed_backward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, g_up, ws, grad, mtl,
+                               stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    status = pk.ctc_packed_read_status(ws)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(_gpu_query_id(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        pk.ctc_packed_forward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, loss, ws, mtl,
+                              stream=stream)
+        ev[k][1].record(stream)
+        pk.ctc_packed_backward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, g_up, ws, grad, mtl,
+                               stream=stream)
+        ev[k][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    sampler.snapshot()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / K
+    frames_all = batch.frames * world
+    value = frames_all / (ms_per_step / 1e3)
+
+    hbm_peak, peak_kind = _peaks()
+    ab = algorithmic_bytes(batch)
+    grad_avg_ms = sum(bwd_ms) / K
+    fwd_avg_ms = sum(fwd_ms) / K
+    achieved = ab["grad_kernel"] / (grad_avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "grad_kernel", "achieved": round(achieved, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                "algorithmic_bytes_per_launch": ab["grad_kernel"], "avg_launch_ms": round(grad_avg_ms, 5)}
+    path_gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
+    path_roofline = {"achieved": round(path_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(path_gbs / hbm_peak, 4), "algorithmic_bytes_per_step": ab["total"],
+                     "bytes": {k: ab[k] for k in ("gather", "alpha", "dense")},
+                     "forward_ms": round(fwd_avg_ms, 5), "backward_ms": round(grad_avg_ms, 5)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        batch.log_probs = lp.cpu()
+        base = cpu_baseline(batch, args.cpu_seconds)
+        cpu = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        dt = {"fp32": "f32", "bf16": "f32", "fp16": "f32"}
+        cfg = _workload_description(batch)
+        cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "frames/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dt[cfg["io_dtype"]], "data": "synthetic",
+            "config": cfg, "hbm_gbs": round(path_gbs, 1), "roofline": roofline, "path_roofline": path_roofline,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world):
+    """Same metric through the C-ABI from pinned host buffers: every step
+    copies its inputs host->device, runs forward + backward and reads the
+    loss back."""
+    host = {
+        "lp": lp.cpu().pin_memory(),
+        "cu": batch.cu_seqlens.pin_memory(),
+        "ln": batch.lengths.pin_memory(),
+        "tg": batch.targets.pin_memory(),
+        "tl": batch.target_lengths.pin_memory(),
+    }
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    loss = torch.empty(nloss, dtype=torch.float32, device=dev)
+    loss_host = torch.empty(nloss, dtype=torch.float32).pin_memory()
+    g_up = torch.ones(nloss, dtype=torch.float32, device=dev)
+    grad = torch.empty_like(lp)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = loss_host.numel() * 4
+
+    def step():
+        with torch.cuda.stream(stream):
+            for k in host:
+                dev_in[k].copy_(host[k], non_blocking=True)
+        d = dev_in
+        pk.ctc_packed_forward(d["lp"], d["cu"], d["ln"], d["tg"], d["tl"], batch.blank, batch.zero_infinity, red,
+                              loss, ws, mtl, stream=stream)
+        pk.ctc_packed_backward(d["lp"], d["cu"], d["ln"], d["tg"], d["tl"], batch.blank, batch.zero_infinity, red,
+                               g_up, ws, grad, mtl, stream=stream)
+        with torch.cuda.stream(stream):
+            loss_host.copy_(loss, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    K = max(3, min(args.steps, 100))
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(K):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / K
+    return {"value": round(batch.frames * world / (ms / 1e3), 1), "unit": "frames/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": K}
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+/*
+ * ctc_packed.h -- CTC loss and gradient over sequence-packed log probabilities
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  Page "feat(asr): native CTC loss kernel over
+ * sequence-packed log probabilities" (NVIDIA-NeMo/Speech PR #16437), file
+ * nemo/collections/asr/parts/triton/ctc_loss.py, module docstring and
+ * packed_ctc_loss:
+ *
+ *   - The log probabilities of a batch are ONE token-flat (T_total, D) buffer:
+ *     utterance b owns rows [cu_seqlens[b], cu_seqlens[b] + lengths[b]).  The
+ *     padded (B, T, D) tensor and its padded gradient are never formed.
+ *   - Per utterance the loss is the CTC negative log-likelihood over the
+ *     extended label sequence (blank, l_1, blank, ..., l_U, blank), S = 2U+1
+ *     states; the skip over a blank is allowed between two different target
+ *     ids (a target id equal to the blank is a label like any other).
+ *     An utterance that cannot be aligned has loss +inf, or 0 with
+ *     zero_infinity, which also zeroes its gradient.  An utterance with no
+ *     frames has loss 0 without targets and +inf with targets.
+ *   - The gradient has the layout and dtype of log_probs: row t of utterance
+ *     b is  scale_b * ( exp(lp[t, c]) - sum over states s with l'_s = c of
+ *     posterior_t(s) ),  the gradient with respect to the logits when
+ *     log_probs is a log_softmax output.  Rows outside every utterance are 0.
+ *   - Reductions (file nemo/collections/asr/losses/ctc.py, forward_packed):
+ *     NONE keeps the B losses, SUM adds them, MEAN divides each by
+ *     max(target_length, 1) and averages over the B utterances.
+ *   - Inputs may be float32, bfloat16 or float16; all arithmetic is float32
+ *     (offsets that keep the recursion accurate are integers, the
+ *     per-utterance log-likelihood is assembled in float64).
+ *
+ * Conventions shared by every call:
+ *   - All array arguments are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing and keeps no state between calls except what
+ *     the caller's workspace holds.
+ *   - Calls are asynchronous on `stream` and never synchronise with the
+ *     host, so a forward + backward pair can be captured in a CUDA graph and
+ *     replayed with new contents in the same buffers.  ctc_packed_read_status
+ *     is the one call that waits.
+ *   - Integer metadata is int32.  Row and element offsets are computed in
+ *     64-bit inside the kernels.
+ *   - Targets are CONCATENATED: utterance b's ids are
+ *     targets[sum_{j<b} target_lengths[j] + i], i < target_lengths[b].  The
+ *     buffer must hold sum(target_lengths) ints.
+ *   - max_target_len is the caller's bound on every target_lengths[b] (the
+ *     page sizes its states by the longest target, or by the targets width
+ *     under graph capture).  Results do not depend on it; it only sizes the
+ *     workspace and the kernels' state lanes.
+ *
+ * Errors.  Arguments that the host can check (null pointers, D < 1, blank
+ * outside [0, D), unknown dtype or reduction, workspace too small, sizes the
+ * kernels do not support) make the call return an error code before anything
+ * is enqueued.  Errors that only the device can see set bits of a status
+ * word in the workspace and give that utterance a NaN loss; they never trap:
+ *   negative target length, target length above max_target_len, lengths[b]
+ *   negative or longer than its cu_seqlens span, cu_seqlens decreasing or
+ *   past T_total, a target id outside [0, D).
+ */
+#ifndef CTC_PACKED_H
+#define CTC_PACKED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CTC_PACKED_F32 = 0,  /* float32 log probabilities and gradient */
+    CTC_PACKED_BF16 = 1, /* bfloat16 */
+    CTC_PACKED_F16 = 2   /* float16 */
+} ctc_packed_dtype;
+
+typedef enum {
+    CTC_PACKED_NONE = 0, /* loss has B entries */
+    CTC_PACKED_SUM = 1,  /* loss has 1 entry: sum of the B losses */
+    CTC_PACKED_MEAN = 2  /* loss has 1 entry: mean over b of loss_b / max(U_b, 1) */
+} ctc_packed_reduction;
+
+typedef enum {
+    CTC_PACKED_OK = 0,
+    CTC_PACKED_ERR_INVALID_ARGUMENT = 1, /* a host-checkable argument is wrong */
+    CTC_PACKED_ERR_WORKSPACE = 2,        /* workspace NULL or smaller than ctc_packed_workspace_size */
+    CTC_PACKED_ERR_CUDA = 3,             /* a CUDA runtime call failed (see cudaGetLastError) */
+    CTC_PACKED_ERR_UNSUPPORTED = 4       /* sizes beyond what the kernels support (D > 16384 or max_target_len > 8191) */
+} ctc_packed_status;
+
+/* Bits of the device status word (ctc_packed_read_status). */
+#define CTC_PACKED_DEV_NEGATIVE_TARGET_LENGTH 0x1u
+#define CTC_PACKED_DEV_TARGET_LENGTH_EXCEEDS_MAX 0x2u
+#define CTC_PACKED_DEV_BAD_LENGTH 0x4u
+#define CTC_PACKED_DEV_BAD_CU_SEQLENS 0x8u
+#define CTC_PACKED_DEV_LABEL_OUT_OF_RANGE 0x10u
+#define CTC_PACKED_DEV_WAIT_TIMEOUT 0x20u /* a bounded wait inside a kernel gave up */
+#define CTC_PACKED_DEV_NO_GRAD_STATE 0x40u /* backward after a CTC_PACKED_FLAG_LOSS_ONLY forward: rows left zero */
+
+/* Flags of ctc_packed_forward. */
+#define CTC_PACKED_FLAG_LOSS_ONLY 0x1u /* skip the work only the backward needs; ctc_packed_backward then fails */
+
+/*
+ * Bytes of device workspace a forward/backward pair with these sizes needs.
+ * The workspace carries the per-utterance metadata, the work queue, the
+ * stored forward (alpha) and backward (beta) state rows, their per-frame
+ * offsets and the per-utterance log-likelihoods.  Returns 0 when the sizes
+ * are invalid (negative) or unsupported.
+ */
+size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
+                                 ctc_packed_dtype dtype);
+
+/*
+ * Forward: per-utterance CTC loss, reduced as asked.
+ *
+ *   log_probs      (T_total, D) row-major, dtype `dtype`, device.
+ *   cu_seqlens     (B + 1) int32: utterance b's rows start at cu_seqlens[b];
+ *                  cu_seqlens[B] <= T_total.
+ *   lengths        (B) int32: frames of utterance b, at most its span
+ *                  cu_seqlens[b+1] - cu_seqlens[b] (rows past it are a gap).
+ *   targets        concatenated int32 target ids (see the header comment).
+ *   target_lengths (B) int32, each in [0, max_target_len].
+ *   blank          class index of the blank, in [0, D).
+ *   loss           float32 device output: B entries for NONE, 1 otherwise.
+ *   workspace      device buffer of at least ctc_packed_workspace_size bytes;
+ *                  pass the same one, unchanged, to ctc_packed_backward.
+ *   flags          0, or CTC_PACKED_FLAG_LOSS_ONLY.
+ */
+ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                     const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                     const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                     int32_t blank, int zero_infinity, ctc_packed_reduction reduction, float* loss,
+                                     void* workspace, size_t workspace_bytes, unsigned flags, cudaStream_t stream);
+
+/*
+ * Backward: gradient of the reduced loss with respect to log_probs.
+ *
+ * Same inputs as the forward that filled `workspace` (same values, same
+ * buffers or copies of them).  grad_loss is the float32 upstream gradient of
+ * the loss (B entries for NONE, 1 otherwise).  grad_log_probs receives
+ * (T_total, D) values in `dtype` (rounded to nearest even from float32); it
+ * may not overlap log_probs.  Every row is written: rows outside every
+ * utterance get 0.  The backward only reads the workspace, except for the
+ * status word.
+ */
+ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                      const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                      const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                      int32_t blank, int zero_infinity, ctc_packed_reduction reduction,
+                                      const float* grad_loss, void* workspace, size_t workspace_bytes,
+                                      void* grad_log_probs, cudaStream_t stream);
+
+/*
+ * Copies the device status word of `workspace` (an OR of CTC_PACKED_DEV_*
+ * bits, 0 when every utterance was well formed) into *device_status after
+ * the work queued on `stream` so far has finished.  This call synchronises
+ * the stream; do not call it during graph capture.
+ */
+ctc_packed_status ctc_packed_read_status(const void* workspace, uint32_t* device_status, cudaStream_t stream);
+
+/* Human-readable name of a ctc_packed_status value (static storage). */
+const char* ctc_packed_status_string(ctc_packed_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CTC_PACKED_H */

@@ -1,0 +1,165 @@
+// C-ABI entry points of the packed CTC library: host-side argument checks,
+// workspace layout and kernel launches.  No host synchronisation except in
+// ctc_packed_read_status.
+#include <cstdint>
+#include <cstring>
+
+#include "ctc_common.cuh"
+#include "ctc_kernels.h"
+
+using namespace ctcp;
+
+namespace {
+
+int elem_bytes(ctc_packed_dtype d) { return d == CTC_PACKED_F32 ? 4 : 2; }
+
+bool valid_dtype(int d) { return d == CTC_PACKED_F32 || d == CTC_PACKED_BF16 || d == CTC_PACKED_F16; }
+bool valid_reduction(int r) { return r == CTC_PACKED_NONE || r == CTC_PACKED_SUM || r == CTC_PACKED_MEAN; }
+
+// Checks shared by forward and backward.  Returns CTC_PACKED_OK or the error.
+ctc_packed_status check_common(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                               const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* target_lengths,
+                               int32_t B, int32_t max_target_len, int32_t blank, int reduction,
+                               const void* workspace, size_t workspace_bytes) {
+    if (!valid_dtype(dtype) || !valid_reduction(reduction)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (blank < 0 || blank >= D) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return CTC_PACKED_ERR_UNSUPPORTED;
+    if (cu_seqlens == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && (lengths == nullptr || target_lengths == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (T_total > 0 && log_probs == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(log_probs) % elem_bytes(dtype) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (workspace == nullptr) return CTC_PACKED_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return CTC_PACKED_ERR_WORKSPACE;
+    const Layout L = make_layout(T_total, B, max_target_len, D);
+    if (workspace_bytes < L.total) return CTC_PACKED_ERR_WORKSPACE;
+    return CTC_PACKED_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
+                                 ctc_packed_dtype dtype) {
+    if (!valid_dtype(dtype) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return 0;
+    if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return 0;
+    return make_layout(T_total, B, max_target_len, D).total;
+}
+
+ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                     const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                     const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                     int32_t blank, int zero_infinity, ctc_packed_reduction reduction, float* loss,
+                                     void* workspace, size_t workspace_bytes, unsigned flags, cudaStream_t stream) {
+    ctc_packed_status st = check_common(log_probs, dtype, T_total, D, cu_seqlens, lengths, target_lengths, B,
+                                        max_target_len, blank, reduction, workspace, workspace_bytes);
+    if (st != CTC_PACKED_OK) return st;
+    if (loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if ((flags & ~CTC_PACKED_FLAG_LOSS_ONLY) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const Layout L = make_layout(T_total, B, max_target_len, D);
+    const int P = chain_pairs_per_thread(max_target_len);
+    const int nw = chain_warps(max_target_len, P);
+    const bool need_grad = (flags & CTC_PACKED_FLAG_LOSS_ONLY) == 0;
+
+    PrepArgs pa{};
+    pa.L = L;
+    pa.ws = workspace;
+    pa.cu = cu_seqlens;
+    pa.lengths = lengths;
+    pa.target_lengths = target_lengths;
+    pa.loss = loss;
+    pa.reduction = reduction;
+    pa.zero_infinity = zero_infinity ? 1 : 0;
+    pa.need_grad = need_grad ? 1 : 0;
+    pa.pairs_per_thread = P;
+    if (launch_prep(pa, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+
+    ChainArgs ca{};
+    ca.L = L;
+    ca.ws = workspace;
+    ca.lp = log_probs;
+    ca.lp_bytes = T_total * (int64_t)D * elem_bytes(dtype);
+    ca.targets = targets;
+    ca.target_lengths = target_lengths;
+    ca.loss = loss;
+    ca.D = D;
+    ca.blank = blank;
+    ca.reduction = reduction;
+    ca.zero_infinity = zero_infinity ? 1 : 0;
+    if (launch_chain(ca, P, nw, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    return CTC_PACKED_OK;
+}
+
+ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                      const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                      const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                      int32_t blank, int zero_infinity, ctc_packed_reduction reduction,
+                                      const float* grad_loss, void* workspace, size_t workspace_bytes,
+                                      void* grad_log_probs, cudaStream_t stream) {
+    ctc_packed_status st = check_common(log_probs, dtype, T_total, D, cu_seqlens, lengths, target_lengths, B,
+                                        max_target_len, blank, reduction, workspace, workspace_bytes);
+    if (st != CTC_PACKED_OK) return st;
+    if (T_total == 0) return CTC_PACKED_OK;
+    if (grad_log_probs == nullptr || (B > 0 && grad_loss == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const int eb = elem_bytes(dtype);
+    if (reinterpret_cast<uintptr_t>(grad_log_probs) % eb != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(grad_log_probs), l0 = reinterpret_cast<uintptr_t>(log_probs);
+    const uintptr_t nbytes = (uintptr_t)(T_total * (int64_t)D * eb);
+    if (g0 < l0 + nbytes && l0 < g0 + nbytes) return CTC_PACKED_ERR_INVALID_ARGUMENT;  // overlap
+
+    GradArgs ga{};
+    ga.L = make_layout(T_total, B, max_target_len, D);
+    ga.ws = workspace;
+    ga.lp = log_probs;
+    ga.grad = grad_log_probs;
+    ga.cu = cu_seqlens;
+    ga.targets = targets;
+    ga.grad_loss = grad_loss;
+    ga.D = D;
+    ga.blank = blank;
+    ga.reduction = reduction;
+    ga.zero_infinity = zero_infinity ? 1 : 0;
+    int k = kTileElems / D;
+    if (k < 1) k = 1;
+    if (k > 1024) k = 1024;
+    ga.rows_per_tile = k;
+    ga.n_tiles = (T_total + k - 1) / k;
+    ga.congruent = ((g0 ^ l0) & 15u) == 0 ? 1 : 0;
+    if (launch_grad(ga, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    return CTC_PACKED_OK;
+}
+
+ctc_packed_status ctc_packed_read_status(const void* workspace, uint32_t* device_status, cudaStream_t stream) {
+    if (workspace == nullptr || device_status == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return CTC_PACKED_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    *device_status = v;
+    return CTC_PACKED_OK;
+}
+
+const char* ctc_packed_status_string(ctc_packed_status status) {
+    switch (status) {
+        case CTC_PACKED_OK: return "ok";
+        case CTC_PACKED_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case CTC_PACKED_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case CTC_PACKED_ERR_CUDA: return "CUDA runtime error";
+        case CTC_PACKED_ERR_UNSUPPORTED: return "unsupported size (D > 16384 or max_target_len > 8191)";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"
+
+namespace ctcp {
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
+    prep_kernel<<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ctcp

@@ -1,0 +1,255 @@
+// Shared definitions of the packed CTC kernels: workspace layout, log-space
+// arithmetic in base 2, element conversions and the async-copy primitives.
+//
+// All log-space state lives in base-2 units (x * log2(e)) so that the
+// hardware ex2/lg2 approximations serve directly.  "log 0" is the finite
+// stand-in kNeg = -1e30: adding any realistic value to it leaves it unchanged
+// (its ulp is ~7e22), so unreachable states stay unreachable without special
+// cases, and a difference of two such values is 0 rather than NaN.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ctc_packed.h"
+
+namespace ctcp {
+
+constexpr int kRing = 16;             // frames of label columns kept in flight per chain
+constexpr float kNeg = -1.0e30f;      // log2 of zero probability
+constexpr float kNegHalf = -5.0e29f;  // anything below is "zero probability"
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr double kLog2eD = 1.4426950408889634074;
+constexpr double kLn2D = 0.69314718055994530942;
+constexpr int kMaxD = 16384;          // one gradient row must fit a shared-memory tile
+constexpr int kMaxTargetLen = 8191;   // 8 state pairs per thread x 1024 threads
+constexpr int kTileElems = 8192;      // elements per backward tile (whole rows, at least one)
+constexpr int kGradThreads = 256;
+constexpr long long kSpinLimit = 1ll << 26;  // bounded waits give up after this many polls
+
+// Control block at the start of the workspace.
+struct Control {
+    uint32_t status;      // OR of CTC_PACKED_DEV_* bits
+    uint32_t big_head;    // next multi-warp chain item
+    uint32_t small_head;  // next single-warp chain item
+    uint32_t lab_head;    // next label-analysis item
+    uint32_t done_ctas;   // CTAs of the chain kernel that have finished
+    uint32_t grad_ready;  // 1 once a forward has stored what the backward needs
+    int32_t n_big, n_small, n_lab;
+    uint32_t pad[7];
+};
+static_assert(sizeof(Control) == 64, "control block is 64 bytes");
+
+// Per-utterance metadata written by the prep kernel.
+struct UttInfo {
+    int32_t start;      // first row
+    int32_t T;          // frames
+    int32_t U;          // target length (0 when invalid)
+    int32_t toff;       // first target id in the concatenated targets
+    int32_t moff;       // first slot of this utterance in the label-metadata arrays
+    int32_t valid;      // metadata well formed
+    int32_t labels_ok;  // every target id in [0, D) (set by the label analysis)
+    int32_t n_owners;   // distinct non-blank target classes + 1 (the blank group)
+};
+
+// Byte offsets of every array inside the caller's workspace.
+struct Layout {
+    int64_t T_total;
+    int32_t B, max_U, D, pitch;  // pitch: floats per stored state row (>= 2 * (max_U + 1))
+    int64_t lab_cap;             // label-metadata slots: B * max_U + B
+    size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
+    size_t off_nxt, off_rank, off_owner, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// State pairs (blank, label) each thread of a chain holds, from the target bound.
+__host__ __device__ inline int pairs_for_max_u(int max_u) {
+    const int pairs = max_u + 1;
+    return pairs <= 1024 ? 1 : pairs <= 2048 ? 2 : pairs <= 4096 ? 4 : 8;
+}
+
+__host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_t max_U, int32_t D) {
+    Layout L{};
+    L.T_total = T_total;
+    L.B = B;
+    L.max_U = max_U;
+    L.D = D;
+    // a row holds 2 floats per state pair; a thread stores its P pairs as one
+    // aligned vector, so the pitch is a multiple of 2P floats (and of 4)
+    const int P = pairs_for_max_u(max_U);
+    L.pitch = (int32_t)align_up((size_t)(2 * (max_U + 1)), (size_t)(2 * P > 4 ? 2 * P : 4));
+    L.lab_cap = (int64_t)B * max_U + B;
+    size_t o = 0;
+    L.off_ctrl = o;   o = align_up(o + sizeof(Control), 256);
+    L.off_utt = o;    o = align_up(o + sizeof(UttInfo) * (size_t)B, 256);
+    L.off_queue = o;  o = align_up(o + sizeof(int32_t) * (3 * (size_t)B + 1), 256);
+    L.off_nll = o;    o = align_up(o + sizeof(double) * (size_t)B, 256);
+    L.off_aoff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total, 256);
+    L.off_boff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total, 256);
+    L.off_alpha = o;  o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)L.pitch, 256);
+    L.off_beta = o;   o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)L.pitch, 256);
+    L.off_nxt = o;    o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
+    L.off_rank = o;   o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
+    L.off_owner = o;  o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+__host__ __device__ inline T* ws_at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<unsigned char*>(ws) + off);
+}
+template <typename T>
+__host__ __device__ inline const T* ws_at(const void* ws, size_t off) {
+    return reinterpret_cast<const T*>(static_cast<const unsigned char*>(ws) + off);
+}
+
+// Element types: 0 float32, 1 bfloat16, 2 float16.
+template <int DT>
+struct Elem {
+    static constexpr int bytes = DT == 0 ? 4 : 2;
+};
+
+// ---------------------------------------------------------------- arithmetic
+
+__device__ __forceinline__ float fast_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Maximum that propagates NaN (so a NaN input poisons the recursion).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float y;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+    return y;
+}
+// log2(2^a + 2^b)
+__device__ __forceinline__ float lse2(float a, float b) {
+    float m = max_nan(a, b);
+    float n = fminf(a, b);
+    return m + fast_lg2(1.0f + fast_ex2(n - m));
+}
+// log2(2^a + 2^b + 2^c)
+__device__ __forceinline__ float lse3(float a, float b, float c) {
+    float hi = max_nan(a, b), lo = fminf(a, b);
+    float m = max_nan(hi, c), mid = fminf(hi, c);
+    return m + fast_lg2(1.0f + fast_ex2(lo - m) + fast_ex2(mid - m));
+}
+
+// A float as an int whose signed order is the float order (non-NaN inputs).
+__device__ __forceinline__ int float_order_key(float x) {
+    int i = __float_as_int(x);
+    return i ^ ((i >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float warp_max(float x) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// ------------------------------------------------------------- conversions
+
+// The value of element `half` (0 low, 1 high) of a 32-bit word in dtype DT.
+template <int DT>
+__device__ __forceinline__ float word_to_float(uint32_t w, int half) {
+    if constexpr (DT == 0) {
+        return __uint_as_float(w);
+    } else if constexpr (DT == 1) {
+        return __uint_as_float(half ? (w & 0xffff0000u) : (w << 16));
+    } else {
+        unsigned short h = half ? (unsigned short)(w >> 16) : (unsigned short)(w & 0xffffu);
+        return __half2float(__ushort_as_half(h));
+    }
+}
+template <int DT>
+__device__ __forceinline__ float bits_to_float(uint32_t bits) {  // bits of one element in the low part
+    if constexpr (DT == 0) {
+        return __uint_as_float(bits);
+    } else if constexpr (DT == 1) {
+        return __uint_as_float(bits << 16);
+    } else {
+        return __half2float(__ushort_as_half((unsigned short)bits));
+    }
+}
+// Round-to-nearest-even conversion of two floats into one packed word.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (DT == 1) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+template <int DT>
+__device__ __forceinline__ uint32_t pack1(float x) {  // one element in the low bits
+    if constexpr (DT == 0) {
+        return __float_as_uint(x);
+    } else if constexpr (DT == 1) {
+        __nv_bfloat16 v = __float2bfloat16_rn(x);
+        return (uint32_t)(*reinterpret_cast<unsigned short*>(&v));
+    } else {
+        __half v = __float2half_rn(x);
+        return (uint32_t)(*reinterpret_cast<unsigned short*>(&v));
+    }
+}
+
+// ------------------------------------------------------- async-copy helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+// Returns true once the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Bulk copy global -> shared (both 16-byte aligned, size a multiple of 16),
+// completion reported on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void set_status(Control* ctrl, uint32_t bits) { atomicOr(&ctrl->status, bits); }
+
+}  // namespace ctcp

@@ -1,0 +1,65 @@
+// Argument blocks and entry points of the packed CTC kernels (internal).
+#pragma once
+
+#include "ctc_common.cuh"
+
+namespace ctcp {
+
+struct PrepArgs {
+    Layout L;
+    void* ws;
+    const int32_t* cu;
+    const int32_t* lengths;
+    const int32_t* target_lengths;
+    float* loss;
+    int reduction;
+    int zero_infinity;
+    int need_grad;
+    int pairs_per_thread;
+};
+
+struct ChainArgs {
+    Layout L;
+    void* ws;
+    const void* lp;      // (T_total, D) log probabilities
+    int64_t lp_bytes;    // T_total * D * element bytes
+    const int32_t* targets;
+    const int32_t* target_lengths;
+    float* loss;
+    int D;
+    int blank;
+    int reduction;
+    int zero_infinity;
+};
+
+struct GradArgs {
+    Layout L;
+    void* ws;
+    const void* lp;
+    void* grad;
+    const int32_t* cu;
+    const int32_t* targets;
+    const float* grad_loss;
+    int D;
+    int blank;
+    int reduction;
+    int zero_infinity;
+    int rows_per_tile;
+    int64_t n_tiles;
+    int congruent;  // lp and grad share their address modulo 16
+};
+
+__global__ void prep_kernel(PrepArgs a);
+template <int P, int DT>
+__global__ void chain_kernel(ChainArgs a);
+template <int DT>
+__global__ void grad_kernel(GradArgs a);
+
+// Host launchers (defined next to their kernels).
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_chain(const ChainArgs& a, int pairs_per_thread, int warps, int dtype, cudaStream_t s);
+cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s);
+int chain_pairs_per_thread(int max_target_len);
+int chain_warps(int max_target_len, int pairs_per_thread);
+
+}  // namespace ctcp

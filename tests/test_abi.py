@@ -1,0 +1,111 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+that include/ctc_packed.h declares, sizes workspaces, and rejects the
+arguments the host can check before any CUDA call is made."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ctc_packed.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from packed_sequence_ctc_gb300 import build as b
+
+    path = b.build()
+    import packed_sequence_ctc_gb300 as p
+
+    return p.load_library(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ctc_packed_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["ctc_packed_workspace_size", "ctc_packed_forward", "ctc_packed_backward", "ctc_packed_read_status",
+              "ctc_packed_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, f"{name} is declared but not exported"
+        assert hasattr(lib, name)
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "ctc_packed.h"\nint main(void) { return (int)sizeof(ctc_packed_status); }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", str(src), "-o", str(tmp_path / "t.o"),
+                    "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include"], check=True)
+
+
+def test_workspace_size(lib):
+    f = lib.ctc_packed_workspace_size
+    n = f(38400, 64, 200, 8193, 1)
+    # two state-row buffers of T_total x pitch floats dominate
+    assert 2 * 38400 * 402 * 4 <= n < 2 * 38400 * 402 * 4 + 10 * 2**20
+    assert f(0, 0, 0, 1, 0) > 0
+    assert f(-1, 1, 1, 4, 0) == 0
+    assert f(10, 1, 1, 0, 0) == 0
+    assert f(10, 1, 1, 16385, 0) == 0  # unsupported D
+    assert f(10, 1, 8192, 8, 0) == 0  # unsupported target bound
+    assert f(10, 1, 1, 8, 7) == 0  # unknown dtype
+
+
+def _fwd(lib, **kw):
+    args = dict(lp=8, dtype=0, T=10, D=5, cu=16, ln=24, tg=32, tl=40, B=2, mtl=3, blank=0, zi=0, red=0, loss=48,
+                ws=256, wsb=1 << 30, flags=0, stream=None)
+    args.update(kw)
+    return lib.ctc_packed_forward(args["lp"], args["dtype"], args["T"], args["D"], args["cu"], args["ln"], args["tg"],
+                                  args["tl"], args["B"], args["mtl"], args["blank"], args["zi"], args["red"],
+                                  args["loss"], args["ws"], args["wsb"], args["flags"], args["stream"])
+
+
+def test_host_argument_checks_return_before_any_cuda_call(lib):
+    INVALID, WORKSPACE, UNSUPPORTED = 1, 2, 4
+    assert _fwd(lib, D=0) == INVALID
+    assert _fwd(lib, blank=5) == INVALID
+    assert _fwd(lib, blank=-1) == INVALID
+    assert _fwd(lib, dtype=3) == INVALID
+    assert _fwd(lib, red=3) == INVALID
+    assert _fwd(lib, B=-1) == INVALID
+    assert _fwd(lib, cu=None) == INVALID
+    assert _fwd(lib, loss=None) == INVALID
+    assert _fwd(lib, lp=None) == INVALID
+    assert _fwd(lib, lp=9) == INVALID  # misaligned float32 pointer
+    assert _fwd(lib, flags=4) == INVALID
+    assert _fwd(lib, ws=None) == WORKSPACE
+    assert _fwd(lib, ws=128) == WORKSPACE  # not 256-byte aligned
+    assert _fwd(lib, wsb=16) == WORKSPACE
+    assert _fwd(lib, D=16385) == UNSUPPORTED
+    assert _fwd(lib, mtl=8192) == UNSUPPORTED
+    b = lib.ctc_packed_backward
+    # grad overlapping log_probs
+    assert b(4096, 0, 10, 5, 16, 24, 32, 40, 2, 3, 0, 0, 0, 48, 256, 1 << 30, 4096 + 20, None) == INVALID
+    assert b(4096, 0, 10, 5, 16, 24, 32, 40, 2, 3, 0, 0, 0, None, 256, 1 << 30, 1 << 20, None) == INVALID
+    assert lib.ctc_packed_read_status(None, None, None) == INVALID
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.ctc_packed_status_string(code)
+    assert lib.ctc_packed_status_string(99) == b"unknown status"
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    import packed_sequence_ctc_gb300 as p
+
+    with pytest.raises(RuntimeError, match="no fallback"):
+        p.load_library(str(tmp_path / "missing.so"))

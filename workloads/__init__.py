@@ -39,7 +39,8 @@ __all__ = ["Batch", "WORKLOADS", "make_batch", "workload", "padded_targets", "se
 
 @dataclasses.dataclass
 class Batch:
-    """One packed batch, all tensors on the CPU.
+    """One packed batch: metadata on the CPU, log probabilities on the device
+    they were drawn on.
 
     ``log_probs`` is ``(T_total, D)``; utterance ``b`` owns rows
     ``[cu_seqlens[b], cu_seqlens[b] + lengths[b])``.  ``targets`` holds the
@@ -114,12 +115,18 @@ def make_batch(
     gaps: Optional[Sequence[int]] = None,
     redraw_infeasible: bool = False,
     name: str = "custom",
+    device="cpu",
 ) -> Batch:
     """Build a packed batch with the given per-utterance frame and target counts.
 
     ``gaps[b]`` extra rows may follow utterance ``b`` inside its cu_seqlens
     span (a gapped layout); those rows hold log probabilities too but belong
     to no utterance.
+
+    The logits are drawn on ``device`` (a CUDA device draws the 300M-element
+    large-vocabulary batch in milliseconds; the CPU takes about a minute);
+    ``log_probs`` stays there.  The same seed gives the same batch on the same
+    kind of device.
     """
     gen = torch.Generator().manual_seed(seed)
     B = len(lengths)
@@ -140,8 +147,12 @@ def make_batch(
     for s in spans:
         cu.append(cu[-1] + s)
     T_total = cu[-1]
-    logits = torch.randn(T_total, num_classes, generator=gen, dtype=torch.float32) * sigma
+    dev = torch.device(device)
+    dgen = torch.Generator(device=dev).manual_seed(seed + 7919)
+    logits = torch.randn(T_total, num_classes, generator=dgen, dtype=torch.float32, device=dev)
+    logits.mul_(sigma)
     log_probs = torch.log_softmax(logits, dim=-1).to(dtype)
+    del logits
     flat = torch.cat(seqs) if seqs else torch.zeros(0, dtype=torch.int64)
     mtl = max([int(t) for t in target_lengths] + [0]) if max_target_len is None else max_target_len
     return Batch(
@@ -158,9 +169,9 @@ def make_batch(
     )
 
 
-def _tiny():
+def _tiny(device="cpu"):
     return make_batch([50, 37, 64, 20], [10, 8, 12, 4], 32, dtype=torch.float32, seed=0, sigma=2.0,
-                      label_low=1, label_high=31, reduction="none", zero_infinity=False, name="tiny")
+                      label_low=1, label_high=31, reduction="none", zero_infinity=False, name="tiny", device=device)
 
 
 def _lengths(gen, B, t_lo, t_hi, u_num_lo, u_den_lo, u_num_hi, u_den_hi):
@@ -174,14 +185,15 @@ def _lengths(gen, B, t_lo, t_hi, u_num_lo, u_den_lo, u_num_hi, u_den_hi):
     return Ts, Us
 
 
-def _conformer():
+def _conformer(device="cpu"):
     gen = torch.Generator().manual_seed(0)
     Ts, Us = _lengths(gen, 32, 200, 400, 1, 6, 1, 4)
     return make_batch(Ts, Us, 1025, dtype=torch.bfloat16, seed=1, sigma=3.0, label_low=1, label_high=1024,
-                      repeat_prob=0.10, redraw_infeasible=True, reduction="mean", name="conformer")
+                      repeat_prob=0.10, redraw_infeasible=True, reduction="mean", name="conformer",
+                      device=device)
 
 
-def _longform():
+def _longform(device="cpu"):
     gen = torch.Generator().manual_seed(0)
     Ts, Us = _lengths(gen, 8, 1500, 2000, 1, 4, 1, 3)
     T_bad = _uniform_int(gen, 1500, 2000)
@@ -191,21 +203,21 @@ def _longform():
     seqs = [torch.randint(1, 1025, (u,), generator=lab_gen).tolist() for u in Us]
     seqs.append([bad_label] * U_bad)
     return make_batch(Ts + [T_bad], Us + [U_bad], 1025, dtype=torch.float32, seed=1, sigma=2.0, targets=seqs,
-                      zero_infinity=True, reduction="sum", name="longform")
+                      zero_infinity=True, reduction="sum", name="longform", device=device)
 
 
-def _char():
+def _char(device="cpu"):
     gen = torch.Generator().manual_seed(0)
     Ts, Us = _lengths(gen, 256, 100, 1000, 1, 8, 1, 3)
     return make_batch(Ts, Us, 29, dtype=torch.float16, seed=1, sigma=2.0, label_low=1, label_high=28,
-                      repeat_prob=0.20, redraw_infeasible=True, reduction="mean", name="char")
+                      repeat_prob=0.20, redraw_infeasible=True, reduction="mean", name="char", device=device)
 
 
-def _largevocab():
+def _largevocab(device="cpu"):
     gen = torch.Generator().manual_seed(0)
     Ts, Us = _lengths(gen, 64, 400, 800, 1, 8, 1, 4)
     return make_batch(Ts, Us, 8193, dtype=torch.bfloat16, seed=1, sigma=3.0, label_low=1, label_high=8192,
-                      reduction="none", name="largevocab")
+                      reduction="none", name="largevocab", device=device)
 
 
 WORKLOADS = {
@@ -217,9 +229,9 @@ WORKLOADS = {
 }
 
 
-def workload(name: str) -> Batch:
+def workload(name: str, device="cpu") -> Batch:
     """One of the five named benchmark workloads, generated from seed 0."""
-    return WORKLOADS[name]()
+    return WORKLOADS[name](device=device)
 
 
 def padded_targets(batch: Batch, width: Optional[int] = None, fill: int = 0) -> torch.Tensor:
@@ -243,14 +255,14 @@ def select_utterances(batch: Batch, index: Sequence[int]) -> Batch:
     for b in index:
         s = int(batch.cu_seqlens[b])
         T = int(batch.lengths[b])
-        rows.append(batch.log_probs[s: s + T])
+        rows.append(batch.log_probs[s: s + T].cpu())
         seqs.append(batch.targets[toff[b]: toff[b + 1]])
         Ts.append(T)
         Us.append(int(batch.target_lengths[b]))
         cu.append(cu[-1] + T)
     return Batch(
         name=f"{batch.name}[{len(index)}]",
-        log_probs=torch.cat(rows) if rows else batch.log_probs[:0],
+        log_probs=torch.cat(rows) if rows else batch.log_probs[:0].cpu(),
         cu_seqlens=torch.tensor(cu, dtype=torch.int32),
         lengths=torch.tensor(Ts, dtype=torch.int32),
         targets=torch.cat(seqs) if seqs else batch.targets[:0],
