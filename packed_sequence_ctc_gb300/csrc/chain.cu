@@ -28,18 +28,18 @@
 // 2-byte element is fetched whole and the right half picked on use), so no
 // global-memory latency sits on the recursion.
 //
-// Accuracy: the recursion runs in base-2 log space in float32, and each frame
-// subtracts an integer offset delta_t from every state, so the states near
-// the maximum stay near 0 where float32 is dense (the page's absolute float32
-// alphas reach |1e4| and lose ~1e-3).  delta_t is chosen two frames late from
-// the exact maximum of frame t-2 (delta_t = round(max_{t-2}) - delta_{t-1},
-// a dead-beat correction), so the reduction never sits on the critical path.
-// The running offsets are exact int32 sums, stored per frame (aoff / boff)
-// and added back in float64 where the log-likelihood is assembled.
+// Arithmetic: the recursion runs on probabilities in extended range (a float
+// mantissa and an int32 binary exponent per state, see ctc_common.cuh):
+// alpha_t(s) = (alpha_{t-1}(s) + alpha_{t-1}(s-1) + [skip] alpha_{t-1}(s-2)) * p_t(s),
+// i.e. only multiply-adds and integer exponent arithmetic on the critical
+// path, no exp or log, no cross-warp normalisation.
 //
-// What is stored for the backward: alpha rows hold the *pre-emission* value
-// alpha_t(s) - lp[t, l'_s] - A_t (so the backward needs no lp gather), beta
-// rows hold beta_t(s) - B_t, both in (T_total, pitch) float32 rows.
+// What is stored for the backward, as int32 fixed-point log2 values with 19
+// fraction bits relative to a per-(frame, warp) integer offset (the warp's
+// largest exponent, stored per frame in aoff / boff): alpha rows hold the
+// value *before* the frame's emission, alpha_t(s) / p_t(s), so the backward
+// needs no log-probability gather; beta rows hold beta_t(s).  The posterior
+// is then an exact integer sum plus one ex2.
 #include <cstdio>
 
 #include "ctc_common.cuh"
@@ -55,9 +55,8 @@ struct Group {
     int warp;        // warp index within the CTA (CTA mode)
     int nw;          // warps in the CTA (CTA mode)
     uint32_t* ring;  // kRing slots of (n * P + 1) words
-    float* halo;     // [2][nw]   (CTA mode)
-    float* maxima;   // [4][nw]   (CTA mode)
-    float* fin;      // 2 floats private to the group
+    float* halo;     // [2][nw] extended values (m, e)   (CTA mode)
+    float* fin;      // 2 extended values private to the group
 };
 
 template <bool CTA>
@@ -69,39 +68,33 @@ __device__ __forceinline__ void group_sync() {
     }
 }
 
-// Issue the gather of element `elem` of the log probabilities into `dst`.
+// Per-thread gather stream of one class column: the byte address of the
+// element for the next frame to prefetch, and which half of its 4-byte word
+// holds a 2-byte element on frame 0.
+struct Column {
+    uintptr_t next;   // byte address of the element of the next frame to issue
+    int half0;        // half of the word on step 0 (2-byte types)
+};
+
 template <int DT>
-__device__ __forceinline__ void gather_word(uint32_t* dst, const unsigned char* lp, int64_t lp_bytes, int64_t elem) {
-    const unsigned char* p = lp + elem * Elem<DT>::bytes;
+__device__ __forceinline__ uintptr_t word_of(uintptr_t addr) {
     if constexpr (DT == 0) {
-        cp_async4(smem_addr(dst), p);
+        return addr;
     } else {
-        const uintptr_t addr = reinterpret_cast<uintptr_t>(p);
-        const uintptr_t word = addr & ~uintptr_t(3);
-        const uintptr_t lo = reinterpret_cast<uintptr_t>(lp);
-        if (word >= lo && word + 4 <= lo + (uintptr_t)lp_bytes) {
-            cp_async4(smem_addr(dst), reinterpret_cast<const void*>(word));
-        } else {
-            // the aligned word would leave the buffer: read the element alone
-            reinterpret_cast<unsigned short*>(dst)[(addr >> 1) & 1] = *reinterpret_cast<const unsigned short*>(p);
-        }
+        return addr & ~uintptr_t(3);
     }
 }
 
-// The gathered value of element `elem` in base-2 log units, -inf clamped to kNeg.
+// Copy the word holding element `addr` into the ring slot `dst`.  `safe`
+// says the whole column stays inside the buffer; otherwise a word that would
+// leave it is replaced by a plain 2-byte read of the element.
 template <int DT>
-__device__ __forceinline__ float gathered_log2(uint32_t w, const unsigned char* lp, int64_t elem) {
-    int half = 0;
-    if constexpr (DT != 0) half = (int)((reinterpret_cast<uintptr_t>(lp + elem * 2) >> 1) & 1);
-    return max_nan(word_to_float<DT>(w, half) * kLog2e, kNeg);
-}
-
-// Maximum of one value per thread over the group, for the offset controller.
-template <bool CTA>
-__device__ __forceinline__ void publish_max(const Group& g, int slot, float m) {
-    const float wm = warp_max(m);
-    if constexpr (CTA) {
-        if ((g.tid & 31) == 0) g.maxima[slot * g.nw + g.warp] = wm;
+__device__ __forceinline__ void gather(uint32_t* dst, uintptr_t addr, bool safe, uintptr_t lo, uintptr_t hi) {
+    const uintptr_t w = word_of<DT>(addr);
+    if (safe || (w >= lo && w + 4 <= hi)) {
+        cp_async4(smem_addr(dst), reinterpret_cast<const void*>(w));
+    } else {
+        reinterpret_cast<unsigned short*>(dst)[(addr >> 1) & 1] = *reinterpret_cast<const unsigned short*>(addr);
     }
 }
 
@@ -113,11 +106,9 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
     const int b = item >> 1;
     const int dir = item & 1;  // 0 alpha, 1 beta
     const int T = info.T, U = info.U;
-    const int64_t start = info.start;
-    const int64_t D = a.D;
     const int lane = g.tid & 31;
-    const unsigned char* lp = static_cast<const unsigned char*>(a.lp);
     const int32_t* tg = a.targets + info.toff;
+    constexpr int E = Elem<DT>::bytes;
 
     // labels of my pairs and their skip transitions
     int cls[P];
@@ -135,7 +126,7 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
             cls[p] = has_label[p] ? tg[j - 1] : 0;
             skip[p] = j >= 1 && j < U && cls[p] != tg[j];
         }
-        if (has_label[p] && (cls[p] < 0 || (int64_t)cls[p] >= D)) bad = true;
+        if (has_label[p] && (cls[p] < 0 || cls[p] >= a.D)) bad = true;
     }
     if constexpr (CTA) {
         bad = __syncthreads_or(bad);
@@ -154,90 +145,124 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
         return;
     }
 
+    // gather streams: frame 0 is row start (alpha) or row start + T - 1 (beta)
+    const uintptr_t buf_lo = reinterpret_cast<uintptr_t>(a.lp);
+    const uintptr_t buf_hi = buf_lo + (uintptr_t)a.lp_bytes;
+    const int64_t row0 = dir == 0 ? (int64_t)info.start : (int64_t)info.start + T - 1;
+    const int64_t row_last = dir == 0 ? (int64_t)info.start + T - 1 : (int64_t)info.start;
+    const intptr_t step_bytes = (dir == 0 ? 1 : -1) * (intptr_t)a.D * E;
+    const int d_odd = (E == 2) ? (a.D & 1) : 0;
+    Column col[P];
+    Column colb;
+    bool safe = true;
+    {
+        auto inside = [&](int64_t row, int c) {
+            const uintptr_t w = word_of<DT>(buf_lo + (uintptr_t)((row * a.D + c) * E));
+            return w >= buf_lo && w + 4 <= buf_hi;
+        };
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            col[p].next = buf_lo + (uintptr_t)((row0 * a.D + cls[p]) * E);
+            col[p].half0 = (int)((col[p].next >> 1) & 1);
+            if (has_label[p]) safe = safe && inside(row0, cls[p]) && inside(row_last, cls[p]);
+        }
+        colb.next = buf_lo + (uintptr_t)((row0 * a.D + a.blank) * E);
+        colb.half0 = (int)((colb.next >> 1) & 1);
+        if (g.tid == 0) safe = safe && inside(row0, a.blank) && inside(row_last, a.blank);
+    }
+
     const int SS = g.n * P + 1;  // words per ring slot: P label words per thread, then the blank
-    auto row_of = [&](int k) -> int64_t { return dir == 0 ? start + k : start + (T - 1 - k); };
     auto issue = [&](int k) {
         if (k < T) {
-            const int64_t rowD = row_of(k) * D;
-            uint32_t* slot = g.ring + (k % kRing) * SS;
+            uint32_t* slot = g.ring + (k & (kRing - 1)) * SS;
 #pragma unroll
-            for (int p = 0; p < P; ++p)
-                if (has_label[p]) gather_word<DT>(slot + p * g.n + g.tid, lp, a.lp_bytes, rowD + cls[p]);
-            if (g.tid == 0) gather_word<DT>(slot + g.n * P, lp, a.lp_bytes, rowD + a.blank);
+            for (int p = 0; p < P; ++p) {
+                if (has_label[p]) gather<DT>(slot + p * g.n + g.tid, col[p].next, safe, buf_lo, buf_hi);
+                col[p].next += step_bytes;
+            }
+            if (g.tid == 0) gather<DT>(slot + g.n * P, colb.next, safe, buf_lo, buf_hi);
+            colb.next += step_bytes;
         }
         cp_async_commit();
     };
-    float lpl[P];
-    float lpb;
+    // emissions of step k as extended probabilities
+    XP eml[P];
+    XP emb;
     auto consume = [&](int k) {
-        const int64_t rowD = row_of(k) * D;
-        const uint32_t* slot = g.ring + (k % kRing) * SS;
-        lpb = gathered_log2<DT>(slot[g.n * P], lp, rowD + a.blank);
+        const uint32_t* slot = g.ring + (k & (kRing - 1)) * SS;
+        const int flip = d_odd & k;  // with D odd a 2-byte element changes halves every frame
+        emb = xp_from_log(word_to_float<DT>(slot[g.n * P], colb.half0 ^ flip));
 #pragma unroll
         for (int p = 0; p < P; ++p)
-            lpl[p] = has_label[p] ? gathered_log2<DT>(slot[p * g.n + g.tid], lp, rowD + cls[p]) : kNeg;
+            eml[p] = has_label[p] ? xp_from_log(word_to_float<DT>(slot[p * g.n + g.tid], col[p].half0 ^ flip))
+                                  : XP{0.0f, kEZero};
     };
 
-    float* store_base = ws_at<float>(a.ws, dir == 0 ? a.L.off_alpha : a.L.off_beta);
-    int32_t* off_base = ws_at<int32_t>(a.ws, dir == 0 ? a.L.off_aoff : a.L.off_boff);
     const int j0 = g.tid * P;
     const bool store_me = j0 <= U;
-    auto store_row = [&](int64_t row, const float (&x)[P], const float (&y)[P]) {
-        if (!store_me) return;
-        float* dst = store_base + row * a.L.pitch + 2 * j0;
-        if constexpr (P == 1) {
-            *reinterpret_cast<float2*>(dst) = make_float2(x[0], y[0]);
-        } else {
+    int* st = ws_at<int>(a.ws, dir == 0 ? a.L.off_alpha : a.L.off_beta) + row0 * a.L.pitch + 2 * j0;
+    const intptr_t st_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.pitch;
+    int32_t* offp = ws_at<int32_t>(a.ws, dir == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo +
+                    (CTA ? g.warp : 0);
+    const intptr_t off_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.nwo;
+    auto store_row = [&](const int (&x)[P], const int (&y)[P], int A) {
+        if (store_me) {
+            if constexpr (P == 1) {
+                *reinterpret_cast<int2*>(st) = make_int2(x[0], y[0]);
+            } else {
 #pragma unroll
-            for (int p = 0; p < P; p += 2)
-                *reinterpret_cast<float4*>(dst + 2 * p) = make_float4(x[p], y[p], x[p + 1], y[p + 1]);
+                for (int p = 0; p < P; p += 2)
+                    *reinterpret_cast<int4*>(st + 2 * p) = make_int4(x[p], y[p], x[p + 1], y[p + 1]);
+            }
         }
+        if (lane == 0) *offp = A;
+        st += st_step;
+        offp += off_step;
     };
 
     // prologue: kRing-1 frames in flight
 #pragma unroll 1
     for (int k = 0; k < kRing - 1; ++k) issue(k);
 
-    float vb[P], vl[P];  // post-emission values, base 2, minus the running offset
-    int acc_off = 0, delta_prev = 0;
-    float m_last = kNeg, m_before = kNeg;  // group maxima of the two previous frames (warp mode)
+    XP vb[P], vl[P];  // alpha (blank 2j, label 2j+1) / beta (label 2j-1, blank 2j), extended probabilities
 
-    // frame of step 0
+    // step 0
     cp_async_wait<kRing - 2>();
     group_sync<CTA>();
     consume(0);
     {
-        float x[P], y[P];
+        int x[P], y[P];
+        int emax = kEZero;
 #pragma unroll
         for (int p = 0; p < P; ++p) {
             const int j = j0 + p;
             if (dir == 0) {
-                vb[p] = j == 0 ? lpb : kNeg;
-                vl[p] = (j == 0 && U >= 1) ? lpl[p] : kNeg;
-                x[p] = j == 0 ? 0.0f : kNeg;  // pre-emission: log2(1) for the two start states
-                y[p] = (j == 0 && U >= 1) ? 0.0f : kNeg;
+                vb[p] = j == 0 ? emb : XP{0.0f, kEZero};
+                vl[p] = (j == 0 && U >= 1) ? eml[p] : XP{0.0f, kEZero};
             } else {
-                vb[p] = j == U ? lpb : kNeg;
-                vl[p] = (j == U && U >= 1) ? lpl[p] : kNeg;
-                x[p] = vl[p];
-                y[p] = vb[p];
+                vb[p] = j == U ? emb : XP{0.0f, kEZero};
+                vl[p] = (j == U && U >= 1) ? eml[p] : XP{0.0f, kEZero};
+            }
+            vb[p] = xp_norm(vb[p].m, vb[p].e);
+            vl[p] = xp_norm(vl[p].m, vl[p].e);
+            emax = max(emax, max(vb[p].e, vl[p].e));
+        }
+        const int A = dir == 0 ? 0 : __reduce_max_sync(0xffffffffu, emax);
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int j = j0 + p;
+            if (dir == 0) {  // before the emission the two start states have probability 1
+                x[p] = j == 0 ? 0 : kFixZero;
+                y[p] = (j == 0 && U >= 1) ? 0 : kFixZero;
+            } else {
+                x[p] = fix_log2(vl[p].m, vl[p].e, A);
+                y[p] = fix_log2(vb[p].m, vb[p].e, A);
             }
         }
-        const int64_t row = row_of(0);
-        if (dir == 0) {
-            store_row(row, x, y);
-        } else {
-            store_row(row, vl, vb);
-        }
-        if (g.tid == 0) off_base[row] = 0;
-        float m = kNeg;
-#pragma unroll
-        for (int p = 0; p < P; ++p) m = fmaxf(m, fmaxf(vb[p], vl[p]));
-        publish_max<CTA>(g, 0, m);
-        if constexpr (!CTA) m_last = warp_max(m);
+        store_row(x, y, A);
         if constexpr (CTA) {
-            if (dir == 0 && lane == 31) g.halo[0 * g.nw + g.warp] = vl[P - 1];
-            if (dir == 1 && lane == 0) g.halo[0 * g.nw + g.warp] = vl[0];
+            if (dir == 0 && lane == 31) reinterpret_cast<XP*>(g.halo)[0 * g.nw + g.warp] = vl[P - 1];
+            if (dir == 1 && lane == 0) reinterpret_cast<XP*>(g.halo)[0 * g.nw + g.warp] = vl[0];
         }
     }
     issue(kRing - 1);
@@ -247,104 +272,100 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
         cp_async_wait<kRing - 2>();
         group_sync<CTA>();
         consume(i);
-        // the state just below (alpha) or above (beta) my pairs, from the previous frame
-        float nb;
+        // the label state just below (alpha) or above (beta) my pairs, previous frame
+        XP nb;
         if (dir == 0) {
-            nb = __shfl_up_sync(0xffffffffu, vl[P - 1], 1);
+            nb.m = __shfl_up_sync(0xffffffffu, vl[P - 1].m, 1);
+            nb.e = __shfl_up_sync(0xffffffffu, vl[P - 1].e, 1);
             if (lane == 0) {
-                nb = kNeg;
+                nb = XP{0.0f, kEZero};
                 if constexpr (CTA) {
-                    if (g.warp > 0) nb = g.halo[((i - 1) & 1) * g.nw + g.warp - 1];
+                    if (g.warp > 0) nb = reinterpret_cast<const XP*>(g.halo)[((i - 1) & 1) * g.nw + g.warp - 1];
                 }
             }
         } else {
-            nb = __shfl_down_sync(0xffffffffu, vl[0], 1);
+            nb.m = __shfl_down_sync(0xffffffffu, vl[0].m, 1);
+            nb.e = __shfl_down_sync(0xffffffffu, vl[0].e, 1);
             if (lane == 31) {
-                nb = kNeg;
+                nb = XP{0.0f, kEZero};
                 if constexpr (CTA) {
-                    if (g.warp < g.nw - 1) nb = g.halo[((i - 1) & 1) * g.nw + g.warp + 1];
+                    if (g.warp < g.nw - 1) nb = reinterpret_cast<const XP*>(g.halo)[((i - 1) & 1) * g.nw + g.warp + 1];
                 }
             }
         }
-        // offset of this frame from the exact maximum two frames back
-        float m2 = kNeg;
-        if (i >= 2) {
-            if constexpr (CTA) {
-                const float v = lane < g.nw ? g.maxima[((i - 2) & 3) * g.nw + lane] : kNeg;
-                m2 = warp_max(v);
-            } else {
-                m2 = m_before;
-            }
-        }
-        int delta = 0;
-        if (m2 > kNegHalf) delta = min(max(__float2int_rn(m2) - delta_prev, -(1 << 20)), 1 << 20);
-        const float fd = (float)delta;
-
-        float nbv[P], nlv[P];
+        float Sb[P], Sl[P];
+        int Eb[P], El[P];
+        int emax = kEZero;
         if (dir == 0) {
-            float pb[P], pl[P];
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                const float prev = p ? vl[p - 1] : nb;
-                pb[p] = lse2(vb[p], prev) - fd;
-                pl[p] = lse3(vl[p], vb[p], skip[p] ? prev : kNeg) - fd;
-                nbv[p] = pb[p] + lpb;
-                nlv[p] = pl[p] + lpl[p];
+                const XP prev = p ? vl[p - 1] : nb;
+                xp_sum2(vb[p], prev, Sb[p], Eb[p]);
+                xp_sum3(vl[p], vb[p], skip[p] ? prev : XP{0.0f, kEZero}, Sl[p], El[p]);
+                emax = max(emax, max(Eb[p], El[p]));
             }
-            store_row(row_of(i), pb, pl);
         } else {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                const float next = (p < P - 1) ? vl[p + 1] : nb;
-                nbv[p] = lse2(vb[p], next) - fd + lpb;
-                nlv[p] = lse3(vl[p], vb[p], skip[p] ? next : kNeg) - fd + lpl[p];
+                const XP next = (p < P - 1) ? vl[p + 1] : nb;
+                xp_sum2(vb[p], next, Sb[p], Eb[p]);
+                xp_sum3(vl[p], vb[p], skip[p] ? next : XP{0.0f, kEZero}, Sl[p], El[p]);
             }
-            store_row(row_of(i), nlv, nbv);
         }
-        float m = kNeg;
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            vb[p] = nbv[p];
-            vl[p] = nlv[p];
-            m = fmaxf(m, fmaxf(vb[p], vl[p]));
+            vb[p] = xp_norm(Sb[p] * emb.m, Eb[p] + emb.e);
+            vl[p] = xp_norm(Sl[p] * eml[p].m, El[p] + eml[p].e);
+            if (dir == 1) emax = max(emax, max(vb[p].e, vl[p].e));
         }
-        acc_off += delta;
-        delta_prev = delta;
-        if (g.tid == 0) off_base[row_of(i)] = acc_off;
         if constexpr (CTA) {
-            if (dir == 0 && lane == 31) g.halo[(i & 1) * g.nw + g.warp] = vl[P - 1];
-            if (dir == 1 && lane == 0) g.halo[(i & 1) * g.nw + g.warp] = vl[0];
-            publish_max<CTA>(g, i & 3, m);
-        } else {
-            m_before = m_last;
-            m_last = warp_max(m);
+            if (dir == 0 && lane == 31) reinterpret_cast<XP*>(g.halo)[(i & 1) * g.nw + g.warp] = vl[P - 1];
+            if (dir == 1 && lane == 0) reinterpret_cast<XP*>(g.halo)[(i & 1) * g.nw + g.warp] = vl[0];
         }
+        // stored rows: alpha before the emission, beta after it, relative to the warp's largest exponent
+        const int A = __reduce_max_sync(0xffffffffu, emax);
+        int x[P], y[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            if (dir == 0) {
+                x[p] = fix_log2(Sb[p], Eb[p], A);
+                y[p] = fix_log2(Sl[p], El[p], A);
+            } else {
+                x[p] = fix_log2(vl[p].m, vl[p].e, A);
+                y[p] = fix_log2(vb[p].m, vb[p].e, A);
+            }
+        }
+        store_row(x, y, A);
         issue(i + kRing - 1);
     }
 
     if (dir == 0) {
         // the paths end in the last blank (pair U) or the last label (pair U-1)
+        XP* fin = reinterpret_cast<XP*>(g.fin);
         if (g.tid == 0) {
-            g.fin[0] = kNeg;
-            g.fin[1] = kNeg;
+            fin[0] = XP{0.0f, kEZero};
+            fin[1] = XP{0.0f, kEZero};
         }
         group_sync<CTA>();
 #pragma unroll
         for (int p = 0; p < P; ++p) {
             const int j = j0 + p;
-            if (j == U) g.fin[0] = vb[p];
-            if (U >= 1 && j == U - 1) g.fin[1] = vl[p];
+            if (j == U) fin[0] = vb[p];
+            if (U >= 1 && j == U - 1) fin[1] = vl[p];
         }
         group_sync<CTA>();
         if (g.tid == 0) {
-            const float x = lse2(g.fin[0], g.fin[1]);
+            const XP f0 = fin[0], f1 = fin[1];
             double v;
-            if (isnan(x)) {
-                v = (double)x;
-            } else if (x <= kNegHalf) {
+            if (isnan(f0.m) || isnan(f1.m)) {
+                v = __longlong_as_double(0x7ff8000000000000ll);
+            } else if (f0.m == 0.0f && f1.m == 0.0f) {
                 v = __longlong_as_double(0x7ff0000000000000ll);  // no path: +inf
             } else {
-                v = -((double)acc_off + (double)x) * kLn2D;
+                const int Em = max(f0.e, f1.e);
+                const double s = (double)f0.m * exp2((double)(max(f0.e - Em, -1100))) +
+                                 (double)f1.m * exp2((double)(max(f1.e - Em, -1100)));
+                v = -((double)Em + log2(s)) * kLn2D;
             }
             nll_out[b] = v;
             if (a.reduction == CTC_PACKED_NONE) {
@@ -428,12 +449,11 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
     uint32_t* ring = reinterpret_cast<uint32_t*>(smem_raw);
     const int ring_words = kRing * (NT * P + NW);
     float* halo = reinterpret_cast<float*>(ring + ring_words);
-    float* maxima = halo + 2 * NW;
-    float* fin = maxima + 4 * NW;  // 2 per warp
+    float* fin = halo + 4 * NW;  // 2 extended values per warp
     const int n_big = ctrl->n_big, n_small = ctrl->n_small, n_lab = ctrl->n_lab;
 
     // 1. multi-warp chains, longest first, one at a time per CTA
-    Group cg{tid, NT, warp, NW, ring, halo, maxima, fin};
+    Group cg{tid, NT, warp, NW, ring, halo, fin};
     for (;;) {
         if (tid == 0) s_item = (int)atomicAdd(&ctrl->big_head, 1u);
         __syncthreads();
@@ -443,7 +463,7 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
         run_chain_item<P, DT, true>(a, queue[k], cg);
     }
     // 2. single-warp chains, each warp on its own
-    Group wg{lane, 32, warp, NW, ring + warp * kRing * (32 * P + 1), halo, maxima, fin + 2 * warp};
+    Group wg{lane, 32, warp, NW, ring + warp * kRing * (32 * P + 1), halo, fin + 4 * warp};
     for (;;) {
         int k = 0;
         if (lane == 0) k = (int)atomicAdd(&ctrl->small_head, 1u);
@@ -500,9 +520,6 @@ CTCP_INSTANTIATE_CHAIN(2, 2)
 CTCP_INSTANTIATE_CHAIN(4, 0)
 CTCP_INSTANTIATE_CHAIN(4, 1)
 CTCP_INSTANTIATE_CHAIN(4, 2)
-CTCP_INSTANTIATE_CHAIN(8, 0)
-CTCP_INSTANTIATE_CHAIN(8, 1)
-CTCP_INSTANTIATE_CHAIN(8, 2)
 
 int chain_pairs_per_thread(int max_target_len) { return pairs_for_max_u(max_target_len); }
 
@@ -514,7 +531,7 @@ int chain_warps(int max_target_len, int P) {
 
 static size_t chain_smem_bytes(int P, int nw) {
     const int nt = 32 * nw;
-    return sizeof(uint32_t) * (size_t)kRing * (nt * P + nw) + sizeof(float) * (size_t)(2 * nw + 4 * nw + 2 * nw);
+    return sizeof(uint32_t) * (size_t)kRing * (nt * P + nw) + sizeof(float) * (size_t)(4 * nw + 4 * nw);
 }
 
 template <int P, int DT>
@@ -549,7 +566,6 @@ cudaError_t launch_chain(const ChainArgs& a, int P, int nw, int dtype, cudaStrea
     CTCP_CASE(1, 0) CTCP_CASE(1, 1) CTCP_CASE(1, 2)
     CTCP_CASE(2, 0) CTCP_CASE(2, 1) CTCP_CASE(2, 2)
     CTCP_CASE(4, 0) CTCP_CASE(4, 1) CTCP_CASE(4, 2)
-    CTCP_CASE(8, 0) CTCP_CASE(8, 1) CTCP_CASE(8, 2)
 #undef CTCP_CASE
     return cudaErrorInvalidValue;
 }

@@ -1,11 +1,12 @@
 // Shared definitions of the packed CTC kernels: workspace layout, log-space
 // arithmetic in base 2, element conversions and the async-copy primitives.
 //
-// All log-space state lives in base-2 units (x * log2(e)) so that the
-// hardware ex2/lg2 approximations serve directly.  "log 0" is the finite
-// stand-in kNeg = -1e30: adding any realistic value to it leaves it unchanged
-// (its ulp is ~7e22), so unreachable states stay unreachable without special
-// cases, and a difference of two such values is 0 rather than NaN.
+// Log-space state is in natural-log units, so a log probability is added
+// exactly as the caller gave it; the hardware base-2 ex2/lg2 approximations
+// only ever see small scaled differences.  "log 0" is the finite stand-in
+// kNeg = -1e30: adding any realistic value to it leaves it unchanged (its ulp
+// is ~7e22), so unreachable states stay unreachable without special cases,
+// and a difference of two such values is 0 rather than NaN.
 #pragma once
 
 #include <cstddef>
@@ -20,13 +21,14 @@
 namespace ctcp {
 
 constexpr int kRing = 16;             // frames of label columns kept in flight per chain
-constexpr float kNeg = -1.0e30f;      // log2 of zero probability
+constexpr float kNeg = -1.0e30f;      // log of zero probability
 constexpr float kNegHalf = -5.0e29f;  // anything below is "zero probability"
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr double kLog2eD = 1.4426950408889634074;
 constexpr double kLn2D = 0.69314718055994530942;
 constexpr int kMaxD = 16384;          // one gradient row must fit a shared-memory tile
-constexpr int kMaxTargetLen = 8191;   // 8 state pairs per thread x 1024 threads
+constexpr int kMaxTargetLen = 4095;   // 4 state pairs per thread x 1024 threads
 constexpr int kTileElems = 8192;      // elements per backward tile (whole rows, at least one)
 constexpr int kGradThreads = 256;
 constexpr long long kSpinLimit = 1ll << 26;  // bounded waits give up after this many polls
@@ -56,13 +58,34 @@ struct UttInfo {
     int32_t n_owners;   // distinct non-blank target classes + 1 (the blank group)
 };
 
+// Per-row record the posterior kernel leaves for the dense gradient kernel.
+struct RowInfo4 {
+    int covered;  // the row is a frame of a well-formed utterance
+    float scale;  // upstream gradient of its utterance (0 when zeroed)
+    int n;        // (class, scale * posterior sum) corrections that follow in the entry row
+    int pad;
+};
+
+// Rows of log probabilities per dense-kernel tile: about kTileElems
+// elements, and few enough that two tiles of corrections fit 32 KB.
+__host__ __device__ inline int dense_rows_per_tile(int D, int ecap) {
+    int k = kTileElems / D;
+    const int k2 = 2048 / (ecap > 0 ? ecap : 1);
+    if (k2 < k) k = k2;
+    if (k < 1) k = 1;
+    if (k > 1024) k = 1024;
+    return k;
+}
+
 // Byte offsets of every array inside the caller's workspace.
 struct Layout {
     int64_t T_total;
     int32_t B, max_U, D, pitch;  // pitch: floats per stored state row (>= 2 * (max_U + 1))
+    int32_t ecap;                // per-row (class, value) gradient corrections: min(max_U + 1, D), even
+    int32_t nwo;                 // per-frame offsets stored per chain row (one per warp of a chain CTA)
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
-    size_t off_nxt, off_rank, off_owner, total;
+    size_t off_nxt, off_rank, off_owner, off_rinfo, off_ent, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -70,7 +93,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // State pairs (blank, label) each thread of a chain holds, from the target bound.
 __host__ __device__ inline int pairs_for_max_u(int max_u) {
     const int pairs = max_u + 1;
-    return pairs <= 1024 ? 1 : pairs <= 2048 ? 2 : pairs <= 4096 ? 4 : 8;
+    return pairs <= 1024 ? 1 : pairs <= 2048 ? 2 : 4;
 }
 
 __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_t max_U, int32_t D) {
@@ -83,19 +106,27 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     // aligned vector, so the pitch is a multiple of 2P floats (and of 4)
     const int P = pairs_for_max_u(max_U);
     L.pitch = (int32_t)align_up((size_t)(2 * (max_U + 1)), (size_t)(2 * P > 4 ? 2 * P : 4));
+    L.ecap = (int32_t)align_up((size_t)((max_U + 1) < D ? (max_U + 1) : D), 2);
+    {
+        const int pairs = max_U + 1;
+        const int nw = (pairs + 32 * P - 1) / (32 * P);
+        L.nwo = nw < 1 ? 1 : (nw > 32 ? 32 : nw);
+    }
     L.lab_cap = (int64_t)B * max_U + B;
     size_t o = 0;
     L.off_ctrl = o;   o = align_up(o + sizeof(Control), 256);
     L.off_utt = o;    o = align_up(o + sizeof(UttInfo) * (size_t)B, 256);
     L.off_queue = o;  o = align_up(o + sizeof(int32_t) * (3 * (size_t)B + 1), 256);
     L.off_nll = o;    o = align_up(o + sizeof(double) * (size_t)B, 256);
-    L.off_aoff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total, 256);
-    L.off_boff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total, 256);
-    L.off_alpha = o;  o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)L.pitch, 256);
-    L.off_beta = o;   o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)L.pitch, 256);
+    L.off_aoff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.nwo, 256);
+    L.off_boff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.nwo, 256);
+    L.off_alpha = o;  o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.pitch, 256);
+    L.off_beta = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.pitch, 256);
     L.off_nxt = o;    o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_rank = o;   o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_owner = o;  o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
+    L.off_rinfo = o;  o = align_up(o + sizeof(RowInfo4) * (size_t)T_total, 256);
+    L.off_ent = o;    o = align_up(o + sizeof(int2) * (size_t)T_total * (size_t)L.ecap, 256);
     L.total = o;
     return L;
 }
@@ -146,15 +177,86 @@ __device__ __forceinline__ float lse3(float a, float b, float c) {
     return m + fast_lg2(1.0f + fast_ex2(lo - m) + fast_ex2(mid - m));
 }
 
-// A float as an int whose signed order is the float order (non-NaN inputs).
-__device__ __forceinline__ int float_order_key(float x) {
-    int i = __float_as_int(x);
-    return i ^ ((i >> 31) & 0x7fffffff);
-}
-__device__ __forceinline__ float warp_max(float x) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+// ------------------------------------------- extended-range probabilities
+//
+// The recursions run on probabilities, not logs: a state is m * 2^e with a
+// float mantissa m in [1, 2) (0 for an unreachable state) and its own int32
+// binary exponent e, so no state ever under- or overflows and the chain needs
+// no exp/log at all -- only multiply-adds and integer exponent arithmetic,
+// rounded to nearest (unbiased).  An emission p = exp(lp) enters as
+// (mp, ep) with lp * log2(e) split exactly into an integer and a fraction;
+// the ex2 approximation of the fraction acts as a ~1e-7 relative perturbation
+// of that one input probability, shared bit for bit by the forward and the
+// backward chain.  (A log-space float32 recursion instead accumulates the
+// bias of the fast log2 near 1 on every step: ~2e-5 on the posteriors of a
+// 2000-frame utterance.)
+
+constexpr int kEZero = -(1 << 29);  // exponent of an unreachable state (m = 0)
+constexpr float kL2eHi = 1.4426950216293335f;     // float(log2 e)
+constexpr float kL2eLo = 1.9259629911783890e-8f;  // log2 e - kL2eHi
+
+struct XP {
+    float m;  // mantissa, 0 for probability 0
+    int e;    // binary exponent
+};
+
+// exp(lp) in extended form.  lp * log2 e = yh + yl exactly (FMA), then
+// exp(lp) = 2^floor(yh) * 2^((yh - floor(yh)) + yl), the mantissa in (1-2^-23, 2].
+__device__ __forceinline__ XP xp_from_log(float lp) {
+    const float yh = lp * kL2eHi;
+    const float yl = fmaf(lp, kL2eLo, fmaf(lp, kL2eHi, -yh));
+    const float fl = floorf(yh);
+    XP r;
+    r.m = fast_ex2((yh - fl) + yl);
+    r.e = (int)fl;
+    if (!(yh > -3.0e7f)) {  // exp(lp) == 0 (lp = -inf or below any representable probability)
+        r.m = (yh != yh) ? yh : 0.0f;  // keep a NaN
+        r.e = kEZero;
+    }
     return r;
+}
+
+// 2^k for k <= 0, flushed to 0 below 2^-126 (an exact power of two).
+__device__ __forceinline__ float pow2_nonpos(int k) { return __int_as_float(max(127 + k, 0) << 23); }
+
+// (m, e) with m rescaled into [1, 2); 0 stays (0, kEZero); inf and NaN stay.
+__device__ __forceinline__ XP xp_norm(float m, int e) {
+    const int bits = __float_as_int(m);
+    const int ex = (bits >> 23) & 0xff;
+    XP r;
+    if (ex == 0) {
+        r.m = 0.0f;
+        r.e = kEZero;
+    } else if (ex == 255) {
+        r.m = m;
+        r.e = e;
+    } else {
+        r.m = __int_as_float((bits & 0x807fffff) | 0x3f800000);
+        r.e = e + (ex - 127);
+    }
+    return r;
+}
+
+// Sum of two / three extended values, as an unnormalised (S, E): S in [0, 6).
+__device__ __forceinline__ void xp_sum2(XP a, XP b, float& S, int& E) {
+    E = max(a.e, b.e);
+    S = fmaf(a.m, pow2_nonpos(a.e - E), b.m * pow2_nonpos(b.e - E));
+}
+__device__ __forceinline__ void xp_sum3(XP a, XP b, XP c, float& S, int& E) {
+    E = max(a.e, max(b.e, c.e));
+    S = fmaf(a.m, pow2_nonpos(a.e - E), fmaf(b.m, pow2_nonpos(b.e - E), c.m * pow2_nonpos(c.e - E)));
+}
+
+// Stored form of a state for the backward: log2 of the value relative to an
+// int offset A, as a signed fixed-point int with kFixFrac fraction bits.
+// The range (-4095, +4096) and the uniform 2^-20 resolution hold wherever the
+// state sits relative to A (a float log would lose bits with distance).
+constexpr int kFixFrac = 19;
+constexpr int kFixZero = (int)0x80000000;  // probability 0
+__device__ __forceinline__ int fix_log2(float S, int E, int A) {
+    const int k = max(E - A, -4095);
+    const int v = (k << kFixFrac) + __float2int_rn(fast_lg2(S) * (float)(1 << kFixFrac));
+    return S > 0.0f ? v : kFixZero;
 }
 
 // ------------------------------------------------------------- conversions
