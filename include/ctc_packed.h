@@ -112,7 +112,7 @@ size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_
 /*
  * Forward: per-utterance CTC loss, reduced as asked.
  *
- *   log_probs      (T_total, D) row-major, dtype `dtype`, device.
+ *   log_probs      (T_total, D) row-major, dtype `dtype`, device; 4-byte aligned.
  *   cu_seqlens     (B + 1) int32: utterance b's rows start at cu_seqlens[b];
  *                  cu_seqlens[B] <= T_total.
  *   lengths        (B) int32: frames of utterance b, at most its span

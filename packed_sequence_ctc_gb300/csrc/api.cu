@@ -28,7 +28,8 @@ ctc_packed_status check_common(const void* log_probs, ctc_packed_dtype dtype, in
     if (cu_seqlens == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (B > 0 && (lengths == nullptr || target_lengths == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (T_total > 0 && log_probs == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if (reinterpret_cast<uintptr_t>(log_probs) % elem_bytes(dtype) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    // 4-byte alignment even for 2-byte types: the label-column gathers fetch aligned 4-byte words
+    if (reinterpret_cast<uintptr_t>(log_probs) % 4 != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (workspace == nullptr) return CTC_PACKED_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return CTC_PACKED_ERR_WORKSPACE;
     const Layout L = make_layout(T_total, B, max_target_len, D);
@@ -122,10 +123,12 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
     ga.blank = blank;
     ga.reduction = reduction;
     ga.zero_infinity = zero_infinity ? 1 : 0;
-    int k = kTileElems / D;
-    if (k < 1) k = 1;
-    if (k > 1024) k = 1024;
+    int k = 1, cap = 1;
+    size_t wsm = 0;
+    grad_geometry(ga.L, D, k, cap, wsm);
     ga.rows_per_tile = k;
+    ga.entry_cap = cap;
+    ga.warp_smem = wsm;
     ga.n_tiles = (T_total + k - 1) / k;
     ga.congruent = ((g0 ^ l0) & 15u) == 0 ? 1 : 0;
     if (launch_grad(ga, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;

@@ -68,14 +68,6 @@ __device__ __forceinline__ void group_sync() {
     }
 }
 
-// Per-thread gather stream of one class column: the byte address of the
-// element for the next frame to prefetch, and which half of its 4-byte word
-// holds a 2-byte element on frame 0.
-struct Column {
-    uintptr_t next;   // byte address of the element of the next frame to issue
-    int half0;        // half of the word on step 0 (2-byte types)
-};
-
 template <int DT>
 __device__ __forceinline__ uintptr_t word_of(uintptr_t addr) {
     if constexpr (DT == 0) {
@@ -85,17 +77,18 @@ __device__ __forceinline__ uintptr_t word_of(uintptr_t addr) {
     }
 }
 
-// Copy the word holding element `addr` into the ring slot `dst`.  `safe`
-// says the whole column stays inside the buffer; otherwise a word that would
-// leave it is replaced by a plain 2-byte read of the element.
+// Copy the 4-byte word holding element `addr` into the ring slot `dst`.  The
+// buffer starts 4-byte aligned, so the word never starts before it; a word
+// that would run past its end copies only the element's 2 bytes (cp.async
+// zero-fills the rest).  `live` false copies nothing (the address is then a
+// valid one that is not read).
 template <int DT>
-__device__ __forceinline__ void gather(uint32_t* dst, uintptr_t addr, bool safe, uintptr_t lo, uintptr_t hi) {
+__device__ __forceinline__ void gather(uint32_t dst, uintptr_t addr, uintptr_t hi, bool live) {
     const uintptr_t w = word_of<DT>(addr);
-    if (safe || (w >= lo && w + 4 <= hi)) {
-        cp_async4(smem_addr(dst), reinterpret_cast<const void*>(w));
-    } else {
-        reinterpret_cast<unsigned short*>(dst)[(addr >> 1) & 1] = *reinterpret_cast<const unsigned short*>(addr);
-    }
+    int n = 4;
+    if constexpr (DT != 0) n = (w + 4 <= hi) ? 4 : 2;
+    n = live ? n : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(w), "r"(n) : "memory");
 }
 
 template <int P, int DT, bool CTA>
@@ -149,53 +142,48 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
     const uintptr_t buf_lo = reinterpret_cast<uintptr_t>(a.lp);
     const uintptr_t buf_hi = buf_lo + (uintptr_t)a.lp_bytes;
     const int64_t row0 = dir == 0 ? (int64_t)info.start : (int64_t)info.start + T - 1;
-    const int64_t row_last = dir == 0 ? (int64_t)info.start + T - 1 : (int64_t)info.start;
     const intptr_t step_bytes = (dir == 0 ? 1 : -1) * (intptr_t)a.D * E;
     const int d_odd = (E == 2) ? (a.D & 1) : 0;
-    Column col[P];
-    Column colb;
-    bool safe = true;
-    {
-        auto inside = [&](int64_t row, int c) {
-            const uintptr_t w = word_of<DT>(buf_lo + (uintptr_t)((row * a.D + c) * E));
-            return w >= buf_lo && w + 4 <= buf_hi;
-        };
+    uintptr_t gnext[P], gfirst[P];
+    int half0[P];
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-            col[p].next = buf_lo + (uintptr_t)((row0 * a.D + cls[p]) * E);
-            col[p].half0 = (int)((col[p].next >> 1) & 1);
-            if (has_label[p]) safe = safe && inside(row0, cls[p]) && inside(row_last, cls[p]);
-        }
-        colb.next = buf_lo + (uintptr_t)((row0 * a.D + a.blank) * E);
-        colb.half0 = (int)((colb.next >> 1) & 1);
-        if (g.tid == 0) safe = safe && inside(row0, a.blank) && inside(row_last, a.blank);
+    for (int p = 0; p < P; ++p) {
+        gfirst[p] = gnext[p] = buf_lo + (uintptr_t)((row0 * a.D + cls[p]) * E);
+        half0[p] = (int)((gfirst[p] >> 1) & 1);
     }
+    const uintptr_t bfirst = buf_lo + (uintptr_t)((row0 * a.D + a.blank) * E);
+    uintptr_t bnext = bfirst;
+    const int bhalf0 = (int)((bfirst >> 1) & 1);
 
     const int SS = g.n * P + 1;  // words per ring slot: P label words per thread, then the blank
+    const uint32_t ring_s = smem_addr(g.ring);
     auto issue = [&](int k) {
-        if (k < T) {
-            uint32_t* slot = g.ring + (k & (kRing - 1)) * SS;
+        const bool live = k < T;
+        const uint32_t slot = ring_s + (uint32_t)((k & (kRing - 1)) * SS) * 4u;
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                if (has_label[p]) gather<DT>(slot + p * g.n + g.tid, col[p].next, safe, buf_lo, buf_hi);
-                col[p].next += step_bytes;
-            }
-            if (g.tid == 0) gather<DT>(slot + g.n * P, colb.next, safe, buf_lo, buf_hi);
-            colb.next += step_bytes;
+        for (int p = 0; p < P; ++p) {
+            gather<DT>(slot + (uint32_t)(p * g.n + g.tid) * 4u, live ? gnext[p] : gfirst[p], buf_hi,
+                       live && has_label[p]);
+            gnext[p] += live ? step_bytes : 0;
         }
+        if (g.tid == 0) gather<DT>(slot + (uint32_t)(g.n * P) * 4u, live ? bnext : bfirst, buf_hi, live);
+        bnext += live ? step_bytes : 0;
         cp_async_commit();
     };
-    // emissions of step k as extended probabilities
-    XP eml[P];
-    XP emb;
-    auto consume = [&](int k) {
+    // emissions of step k as extended probabilities; a NaN log probability is remembered
+    bool saw_nan = false;
+    auto consume = [&](int k, XP& eb, XP (&el)[P]) {
         const uint32_t* slot = g.ring + (k & (kRing - 1)) * SS;
         const int flip = d_odd & k;  // with D odd a 2-byte element changes halves every frame
-        emb = xp_from_log(word_to_float<DT>(slot[g.n * P], colb.half0 ^ flip));
+        const float lb = word_to_float<DT>(slot[g.n * P], bhalf0 ^ flip);
+        saw_nan |= lb != lb;
+        eb = xp_from_log(lb);
 #pragma unroll
-        for (int p = 0; p < P; ++p)
-            eml[p] = has_label[p] ? xp_from_log(word_to_float<DT>(slot[p * g.n + g.tid], col[p].half0 ^ flip))
-                                  : XP{0.0f, kEZero};
+        for (int p = 0; p < P; ++p) {
+            const float ll = word_to_float<DT>(slot[p * g.n + g.tid], half0[p] ^ flip);
+            saw_nan |= has_label[p] && ll != ll;
+            el[p] = has_label[p] ? xp_from_log(ll) : XP{0.0f, kEZero};
+        }
     };
 
     const int j0 = g.tid * P;
@@ -219,17 +207,21 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
         st += st_step;
         offp += off_step;
     };
+    XP* halo = reinterpret_cast<XP*>(g.halo);
+    const XP zero{0.0f, kEZero};
 
     // prologue: kRing-1 frames in flight
 #pragma unroll 1
     for (int k = 0; k < kRing - 1; ++k) issue(k);
 
     XP vb[P], vl[P];  // alpha (blank 2j, label 2j+1) / beta (label 2j-1, blank 2j), extended probabilities
+    XP eb_cur, el_cur[P], eb_nxt, el_nxt[P];
 
-    // step 0
-    cp_async_wait<kRing - 2>();
+    // step 0 (frames 0 and 1 have landed)
+    cp_async_wait<kRing - 3>();
     group_sync<CTA>();
-    consume(0);
+    consume(0, eb_cur, el_cur);
+    consume(1, eb_nxt, el_nxt);
     {
         int x[P], y[P];
         int emax = kEZero;
@@ -237,15 +229,19 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
         for (int p = 0; p < P; ++p) {
             const int j = j0 + p;
             if (dir == 0) {
-                vb[p] = j == 0 ? emb : XP{0.0f, kEZero};
-                vl[p] = (j == 0 && U >= 1) ? eml[p] : XP{0.0f, kEZero};
+                vb[p] = j == 0 ? eb_cur : zero;
+                vl[p] = (j == 0 && U >= 1) ? el_cur[p] : zero;
             } else {
-                vb[p] = j == U ? emb : XP{0.0f, kEZero};
-                vl[p] = (j == U && U >= 1) ? eml[p] : XP{0.0f, kEZero};
+                vb[p] = j == U ? eb_cur : zero;
+                vl[p] = (j == U && U >= 1) ? el_cur[p] : zero;
             }
             vb[p] = xp_norm(vb[p].m, vb[p].e);
             vl[p] = xp_norm(vl[p].m, vl[p].e);
             emax = max(emax, max(vb[p].e, vl[p].e));
+        }
+        if constexpr (CTA) {
+            if (dir == 0 && lane == 31) halo[g.warp] = vl[P - 1];
+            if (dir == 1 && lane == 0) halo[g.warp] = vl[0];
         }
         const int A = dir == 0 ? 0 : __reduce_max_sync(0xffffffffu, emax);
 #pragma unroll
@@ -260,74 +256,64 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
             }
         }
         store_row(x, y, A);
-        if constexpr (CTA) {
-            if (dir == 0 && lane == 31) reinterpret_cast<XP*>(g.halo)[0 * g.nw + g.warp] = vl[P - 1];
-            if (dir == 1 && lane == 0) reinterpret_cast<XP*>(g.halo)[0 * g.nw + g.warp] = vl[0];
-        }
     }
     issue(kRing - 1);
 
 #pragma unroll 1
     for (int i = 1; i < T; ++i) {
-        cp_async_wait<kRing - 2>();
+        cp_async_wait<kRing - 3>();  // frames i and i+1 have landed
         group_sync<CTA>();
-        consume(i);
+        eb_cur = eb_nxt;
+#pragma unroll
+        for (int p = 0; p < P; ++p) el_cur[p] = el_nxt[p];
         // the label state just below (alpha) or above (beta) my pairs, previous frame
         XP nb;
-        if (dir == 0) {
-            nb.m = __shfl_up_sync(0xffffffffu, vl[P - 1].m, 1);
-            nb.e = __shfl_up_sync(0xffffffffu, vl[P - 1].e, 1);
-            if (lane == 0) {
-                nb = XP{0.0f, kEZero};
-                if constexpr (CTA) {
-                    if (g.warp > 0) nb = reinterpret_cast<const XP*>(g.halo)[((i - 1) & 1) * g.nw + g.warp - 1];
-                }
-            }
-        } else {
-            nb.m = __shfl_down_sync(0xffffffffu, vl[0].m, 1);
-            nb.e = __shfl_down_sync(0xffffffffu, vl[0].e, 1);
-            if (lane == 31) {
-                nb = XP{0.0f, kEZero};
-                if constexpr (CTA) {
-                    if (g.warp < g.nw - 1) nb = reinterpret_cast<const XP*>(g.halo)[((i - 1) & 1) * g.nw + g.warp + 1];
-                }
-            }
+        {
+            const int src = dir == 0 ? max(g.warp - 1, 0) : min(g.warp + 1, g.nw - 1);
+            const XP h = CTA ? halo[((i - 1) & 1) * g.nw + src] : zero;
+            const bool edge = dir == 0 ? (lane == 0) : (lane == 31);
+            const bool has_nb = CTA && (dir == 0 ? g.warp > 0 : g.warp < g.nw - 1);
+            const XP mine = dir == 0 ? vl[P - 1] : vl[0];
+            nb.m = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.m, 1) : __shfl_down_sync(0xffffffffu, mine.m, 1);
+            nb.e = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.e, 1) : __shfl_down_sync(0xffffffffu, mine.e, 1);
+            if (edge) nb = has_nb ? h : zero;
         }
         float Sb[P], Sl[P];
         int Eb[P], El[P];
-        int emax = kEZero;
         if (dir == 0) {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 const XP prev = p ? vl[p - 1] : nb;
+                xp_sum3(vl[p], vb[p], skip[p] ? prev : zero, Sl[p], El[p]);
                 xp_sum2(vb[p], prev, Sb[p], Eb[p]);
-                xp_sum3(vl[p], vb[p], skip[p] ? prev : XP{0.0f, kEZero}, Sl[p], El[p]);
-                emax = max(emax, max(Eb[p], El[p]));
             }
         } else {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 const XP next = (p < P - 1) ? vl[p + 1] : nb;
+                xp_sum3(vl[p], vb[p], skip[p] ? next : zero, Sl[p], El[p]);
                 xp_sum2(vb[p], next, Sb[p], Eb[p]);
-                xp_sum3(vl[p], vb[p], skip[p] ? next : XP{0.0f, kEZero}, Sl[p], El[p]);
             }
         }
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            vb[p] = xp_norm(Sb[p] * emb.m, Eb[p] + emb.e);
-            vl[p] = xp_norm(Sl[p] * eml[p].m, El[p] + eml[p].e);
-            if (dir == 1) emax = max(emax, max(vb[p].e, vl[p].e));
+            vl[p] = xp_norm(Sl[p] * el_cur[p].m, El[p] + el_cur[p].e);
+            vb[p] = xp_norm(Sb[p] * eb_cur.m, Eb[p] + eb_cur.e);
         }
-        if constexpr (CTA) {
-            if (dir == 0 && lane == 31) reinterpret_cast<XP*>(g.halo)[(i & 1) * g.nw + g.warp] = vl[P - 1];
-            if (dir == 1 && lane == 0) reinterpret_cast<XP*>(g.halo)[(i & 1) * g.nw + g.warp] = vl[0];
+        if constexpr (CTA) {  // the critical value first: the neighbour warp waits for it
+            if (dir == 0 && lane == 31) halo[(i & 1) * g.nw + g.warp] = vl[P - 1];
+            if (dir == 1 && lane == 0) halo[(i & 1) * g.nw + g.warp] = vl[0];
         }
-        // stored rows: alpha before the emission, beta after it, relative to the warp's largest exponent
+        // off the critical path: the next frame's emissions, the stored rows, the next gather
+        consume(i + 1, eb_nxt, el_nxt);
+        int emax = kEZero;
+#pragma unroll
+        for (int p = 0; p < P; ++p) emax = dir == 0 ? max(emax, max(Eb[p], El[p])) : max(emax, max(vb[p].e, vl[p].e));
         const int A = __reduce_max_sync(0xffffffffu, emax);
         int x[P], y[P];
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            if (dir == 0) {
+            if (dir == 0) {  // alpha rows: before the emission
                 x[p] = fix_log2(Sb[p], Eb[p], A);
                 y[p] = fix_log2(Sl[p], El[p], A);
             } else {
@@ -353,11 +339,17 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
             if (j == U) fin[0] = vb[p];
             if (U >= 1 && j == U - 1) fin[1] = vl[p];
         }
-        group_sync<CTA>();
+        bool any_nan;
+        if constexpr (CTA) {
+            any_nan = __syncthreads_or(saw_nan);
+        } else {
+            any_nan = __any_sync(0xffffffffu, saw_nan);
+            __syncwarp();
+        }
         if (g.tid == 0) {
             const XP f0 = fin[0], f1 = fin[1];
             double v;
-            if (isnan(f0.m) || isnan(f1.m)) {
+            if (any_nan) {
                 v = __longlong_as_double(0x7ff8000000000000ll);
             } else if (f0.m == 0.0f && f1.m == 0.0f) {
                 v = __longlong_as_double(0x7ff0000000000000ll);  // no path: +inf

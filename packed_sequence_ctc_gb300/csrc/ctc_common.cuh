@@ -29,8 +29,6 @@ constexpr double kLog2eD = 1.4426950408889634074;
 constexpr double kLn2D = 0.69314718055994530942;
 constexpr int kMaxD = 16384;          // one gradient row must fit a shared-memory tile
 constexpr int kMaxTargetLen = 4095;   // 4 state pairs per thread x 1024 threads
-constexpr int kTileElems = 8192;      // elements per backward tile (whole rows, at least one)
-constexpr int kGradThreads = 256;
 constexpr long long kSpinLimit = 1ll << 26;  // bounded waits give up after this many polls
 
 // Control block at the start of the workspace.
@@ -58,34 +56,15 @@ struct UttInfo {
     int32_t n_owners;   // distinct non-blank target classes + 1 (the blank group)
 };
 
-// Per-row record the posterior kernel leaves for the dense gradient kernel.
-struct RowInfo4 {
-    int covered;  // the row is a frame of a well-formed utterance
-    float scale;  // upstream gradient of its utterance (0 when zeroed)
-    int n;        // (class, scale * posterior sum) corrections that follow in the entry row
-    int pad;
-};
-
-// Rows of log probabilities per dense-kernel tile: about kTileElems
-// elements, and few enough that two tiles of corrections fit 32 KB.
-__host__ __device__ inline int dense_rows_per_tile(int D, int ecap) {
-    int k = kTileElems / D;
-    const int k2 = 2048 / (ecap > 0 ? ecap : 1);
-    if (k2 < k) k = k2;
-    if (k < 1) k = 1;
-    if (k > 1024) k = 1024;
-    return k;
-}
-
 // Byte offsets of every array inside the caller's workspace.
 struct Layout {
     int64_t T_total;
     int32_t B, max_U, D, pitch;  // pitch: floats per stored state row (>= 2 * (max_U + 1))
-    int32_t ecap;                // per-row (class, value) gradient corrections: min(max_U + 1, D), even
+    int32_t ecap;                // distinct classes a target can have: min(max_U + 1, D)
     int32_t nwo;                 // per-frame offsets stored per chain row (one per warp of a chain CTA)
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
-    size_t off_nxt, off_rank, off_owner, off_rinfo, off_ent, total;
+    size_t off_nxt, off_rank, off_owner, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -106,7 +85,7 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     // aligned vector, so the pitch is a multiple of 2P floats (and of 4)
     const int P = pairs_for_max_u(max_U);
     L.pitch = (int32_t)align_up((size_t)(2 * (max_U + 1)), (size_t)(2 * P > 4 ? 2 * P : 4));
-    L.ecap = (int32_t)align_up((size_t)((max_U + 1) < D ? (max_U + 1) : D), 2);
+    L.ecap = (max_U + 1) < D ? (max_U + 1) : D;
     {
         const int pairs = max_U + 1;
         const int nw = (pairs + 32 * P - 1) / (32 * P);
@@ -125,8 +104,6 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_nxt = o;    o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_rank = o;   o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_owner = o;  o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
-    L.off_rinfo = o;  o = align_up(o + sizeof(RowInfo4) * (size_t)T_total, 256);
-    L.off_ent = o;    o = align_up(o + sizeof(int2) * (size_t)T_total * (size_t)L.ecap, 256);
     L.total = o;
     return L;
 }
@@ -209,8 +186,8 @@ __device__ __forceinline__ XP xp_from_log(float lp) {
     XP r;
     r.m = fast_ex2((yh - fl) + yl);
     r.e = (int)fl;
-    if (!(yh > -3.0e7f)) {  // exp(lp) == 0 (lp = -inf or below any representable probability)
-        r.m = (yh != yh) ? yh : 0.0f;  // keep a NaN
+    if (!(yh > -3.0e7f)) {  // exp(lp) == 0: lp = -inf, below any representable probability, or NaN
+        r.m = 0.0f;         // (callers flag a NaN separately)
         r.e = kEZero;
     }
     return r;
@@ -219,21 +196,14 @@ __device__ __forceinline__ XP xp_from_log(float lp) {
 // 2^k for k <= 0, flushed to 0 below 2^-126 (an exact power of two).
 __device__ __forceinline__ float pow2_nonpos(int k) { return __int_as_float(max(127 + k, 0) << 23); }
 
-// (m, e) with m rescaled into [1, 2); 0 stays (0, kEZero); inf and NaN stay.
+// (m, e) with m rescaled into [1, 2); 0 becomes (0, kEZero).  m is a finite
+// non-negative normal number or 0 (a sum of normalised mantissas times an
+// emission mantissa never leaves [1, 12)).
 __device__ __forceinline__ XP xp_norm(float m, int e) {
     const int bits = __float_as_int(m);
-    const int ex = (bits >> 23) & 0xff;
     XP r;
-    if (ex == 0) {
-        r.m = 0.0f;
-        r.e = kEZero;
-    } else if (ex == 255) {
-        r.m = m;
-        r.e = e;
-    } else {
-        r.m = __int_as_float((bits & 0x807fffff) | 0x3f800000);
-        r.e = e + (ex - 127);
-    }
+    r.m = bits == 0 ? 0.0f : __int_as_float((bits & 0x007fffff) | 0x3f800000);
+    r.e = bits == 0 ? kEZero : e + ((bits >> 23) - 127);
     return r;
 }
 

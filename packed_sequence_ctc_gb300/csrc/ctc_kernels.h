@@ -44,9 +44,11 @@ struct GradArgs {
     int blank;
     int reduction;
     int zero_infinity;
-    int rows_per_tile;
-    int64_t n_tiles;
-    int congruent;  // lp and grad share their address modulo 16
+    int rows_per_tile;   // rows per warp group
+    int64_t n_tiles;     // warp groups
+    int entry_cap;       // corrections a group can hold
+    size_t warp_smem;    // shared memory bytes per warp
+    int congruent;       // lp and grad share their address modulo 16
 };
 
 __global__ void prep_kernel(PrepArgs a);
@@ -54,6 +56,7 @@ template <int P, int DT>
 __global__ void chain_kernel(ChainArgs a);
 template <int DT>
 __global__ void grad_kernel(GradArgs a);
+void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& warp_smem);
 
 // Host launchers (defined next to their kernels).
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
