@@ -18,12 +18,12 @@
 //      occurrence walking the chain of its later occurrences.  No atomics and
 //      a fixed order, so the gradient is bitwise reproducible.  The sums wait
 //      in the warp's slice of shared memory as (row, class, scale * sum).
-//   2. the dense part: the group's rows are one contiguous span, streamed in
+//   2. the group's rows are one contiguous span, streamed in batches of
 //      16-byte chunks (vector loads and stores, several in flight per lane):
-//      grad = scale * exp(lp), or 0 outside every utterance.
-//   3. the corrections: for each (row, class) of step 1 the warp rewrites
-//      that element as scale * exp(lp) - scale * sum.  The row was written a
-//      moment ago, so these few scattered accesses hit L2.
+//      grad = scale * exp(lp) - P, or 0 outside every utterance.  Before a
+//      batch the warp drops the batch's few class sums into a small shared
+//      tile P and marks their chunks, so a chunk reads P only when marked and
+//      every gradient element is written exactly once, in one rounding.
 //
 // The stored rows are fixed-point log2 values of alpha_t(s) / p_t(s) (before
 // the emission) and of beta_t(s), each relative to an integer offset of its
@@ -37,7 +37,8 @@ namespace ctcp {
 namespace {
 
 constexpr int kMaxWarpsPerBlock = 8;
-constexpr int kUnroll = 4;  // 16-byte chunks in flight per lane
+constexpr int kUnroll = 4;                   // 16-byte chunks in flight per lane
+constexpr int kBatchChunks = 32 * kUnroll;   // chunks a warp streams per batch
 
 __device__ __forceinline__ int find_utterance(const int32_t* cu, int B, int64_t row) {
     int lo = 0, hi = B - 1, ans = -1;
@@ -90,7 +91,7 @@ __device__ __forceinline__ void store_elem(uintptr_t addr, uint32_t bits) {
 }  // namespace
 
 template <int DT>
-__global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArgs a) {
+__global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArgs a) {
     constexpr int E = Elem<DT>::bytes;
     constexpr int V = 16 / E;  // elements per 16-byte chunk
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -105,6 +106,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
     int* e_key = reinterpret_cast<int*>(ws + 2 * align_up(4 * (size_t)K, 16));
     float* e_val = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_key) + align_up(4 * (size_t)cap, 16));
     float* gam = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_val) + align_up(4 * (size_t)cap, 16));
+    float* ptile = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(gam) + align_up(4 * (size_t)ulen, 16));
+    uint32_t* pmark = reinterpret_cast<uint32_t*>(ptile + kBatchChunks * V);  // kBatchChunks / 32 words
 
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
@@ -127,10 +130,24 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
     const int wpb = blockDim.x >> 5;
     const int64_t warps = (int64_t)gridDim.x * wpb;
 
+    for (int i = lane; i < kBatchChunks * V; i += 32) ptile[i] = 0.0f;
+    if (lane < kBatchChunks / 32) pmark[lane] = 0u;
+    __syncwarp();
+
     for (int64_t grp = (int64_t)blockIdx.x * wpb + warp; grp < n_groups; grp += warps) {
         const int64_t r0 = grp * K;
         const int nrows = (int)min((int64_t)K, a.L.T_total - r0);
 
+        // the next group's stored rows start their way into L2
+        {
+            const int64_t nr0 = (grp + warps) * K;
+            const int64_t nrows_next = nr0 < a.L.T_total ? min((int64_t)K, a.L.T_total - nr0) : 0;
+            const int64_t bytes = nrows_next * (int64_t)a.L.pitch * 4;
+            for (int64_t off = (int64_t)lane * 128; off < bytes; off += 32 * 128) {
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(alpha + nr0 * a.L.pitch + off / 4));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + nr0 * a.L.pitch + off / 4));
+            }
+        }
         // 1. posteriors of every row of the group
         int count = 0;  // corrections so far (warp-uniform)
         int b = find_utterance(a.cu, B, r0);
@@ -195,12 +212,12 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
                 if (kind >= 0) {
                     float s = gam[j];
                     for (int jj = nx[j]; jj >= 0; jj = nx[jj]) s += gam[jj];
-                    e_key[count + kind] = (rr << 16) | tg[j];
+                    e_key[count + kind] = rr * D + tg[j];
                     e_val[count + kind] = scale * s;
                 }
             }
             if (lane == 0) {
-                e_key[count + u.n_owners - 1] = (rr << 16) | a.blank;
+                e_key[count + u.n_owners - 1] = rr * D + a.blank;
                 e_val[count + u.n_owners - 1] = scale * blank_sum;
             }
             count += u.n_owners;
@@ -213,6 +230,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
         const uintptr_t g0 = gr0 + (uintptr_t)(r0 * D * E);
         const uintptr_t g1 = g0 + (uintptr_t)nrows * D * E;
         const uintptr_t qb = g0 & ~uintptr_t(15);
+        const int pshift = (int)((g0 - qb) / E);  // element f of the group lies in chunk (f + pshift) / V
         const int nq = (int)((((g1 + 15) & ~uintptr_t(15)) - qb) / 16);
         const float invD = 1.0f / (float)D;
         // element index (within the group) of the first element of chunk q, and its row
@@ -225,7 +243,100 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
             }
             return r;
         };
-        for (int q0 = 0; q0 < nq; q0 += 32 * kUnroll) {
+        if (nrows == 1 && a.congruent) {
+            // one row, lp and grad congruent modulo 16: chunks [qf0, qf1) are whole and aligned
+            const int qf0 = pshift > 0 ? 1 : 0;
+            const int qf1 = (int)((g1 - qb) / 16);
+            const uintptr_t lpq = qb + (a0 - g0);  // lp address of chunk 0
+            const bool cov = row_cov[0] != 0;
+            const float s = row_scale[0];
+            for (int q0 = 0; q0 < nq; q0 += kBatchChunks) {
+                uint4 in[kUnroll];
+#pragma unroll
+                for (int k = 0; k < kUnroll; ++k) {
+                    const int q = q0 + k * 32 + lane;
+                    if (cov && q >= qf0 && q < qf1) in[k] = ld_stream(reinterpret_cast<const void*>(lpq + (uintptr_t)q * 16));
+                }
+                const int f_begin = q0 * V - pshift, f_end = f_begin + kBatchChunks * V;
+                for (int e = lane; e < count; e += 32) {
+                    const int f = e_key[e];
+                    if (f >= f_begin && f < f_end) {
+                        const int idx = f - f_begin;
+                        ptile[idx] = e_val[e];
+                        atomicOr(&pmark[idx / (32 * V)], 1u << ((idx / V) & 31));
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < kUnroll; ++k) {
+                    const int q = q0 + k * 32 + lane;
+                    if (q >= nq) continue;
+                    const int ql = k * 32 + lane;
+                    const bool marked = (pmark[k] >> lane) & 1u;
+                    const uintptr_t c0 = qb + (uintptr_t)q * 16;
+                    if (q >= qf0 && q < qf1) {
+                        float pv[V];
+#pragma unroll
+                        for (int i = 0; i < V; ++i) pv[i] = 0.0f;
+                        if (marked) {
+#pragma unroll
+                            for (int i = 0; i < V; i += 4) {
+                                const float4 v = reinterpret_cast<const float4*>(ptile + ql * V)[i / 4];
+                                pv[i] = v.x;
+                                pv[i + 1] = v.y;
+                                pv[i + 2] = v.z;
+                                pv[i + 3] = v.w;
+                                reinterpret_cast<float4*>(ptile + ql * V)[i / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+                        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                        if (cov) {
+                            const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
+                            float out[V];
+#pragma unroll
+                            for (int i = 0; i < V; ++i) {
+                                float x;
+                                if constexpr (E == 4) {
+                                    x = __uint_as_float(w[i]);
+                                } else if constexpr (DT == 1) {  // bfloat16: the high half is already a float
+                                    x = __uint_as_float((i & 1) ? (w[i >> 1] & 0xffff0000u) : (w[i >> 1] << 16));
+                                } else {
+                                    x = bits_to_float<DT>((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu));
+                                }
+                                out[i] = fmaf(s, fast_ex2(x * kLog2e), -pv[i]);
+                            }
+                            if constexpr (E == 4) {
+                                o = make_uint4(__float_as_uint(out[0]), __float_as_uint(out[1]), __float_as_uint(out[2]),
+                                               __float_as_uint(out[3]));
+                            } else {
+                                o = make_uint4(pack2<DT>(out[0], out[1]), pack2<DT>(out[2], out[3]),
+                                               pack2<DT>(out[4], out[5]), pack2<DT>(out[6], out[7]));
+                            }
+                        }
+                        *reinterpret_cast<uint4*>(c0) = o;
+                    } else {
+                        // the ragged first / last chunk of the row
+                        const uintptr_t lo = c0 > g0 ? c0 : g0;
+                        const uintptr_t hi = c0 + 16 < g1 ? c0 + 16 : g1;
+                        for (uintptr_t ad = lo; ad < hi; ad += E) {
+                            const size_t f = (ad - g0) / E;
+                            const float x = bits_to_float<DT>(load_elem<DT>(a0 + f * E));
+                            const float pk = marked ? ptile[ql * V + (int)(f + pshift) - q * V] : 0.0f;
+                            const float gv = cov ? fmaf(s, fast_ex2(x * kLog2e), -pk) : 0.0f;
+                            store_elem<DT>(ad, pack1<DT>(gv));
+                        }
+                        if (marked) {
+                            for (int i = 0; i < V; ++i) ptile[ql * V + i] = 0.0f;
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane < kBatchChunks / 32) pmark[lane] = 0u;
+                __syncwarp();
+            }
+            continue;
+        }
+        for (int q0 = 0; q0 < nq; q0 += kBatchChunks) {
             uint4 in[kUnroll];
             bool fast[kUnroll];
 #pragma unroll
@@ -235,6 +346,17 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
                 fast[k] = q < nq && c0 >= g0 && c0 + 16 <= g1 && a.congruent;
                 if (fast[k]) in[k] = ld_stream(reinterpret_cast<const void*>(a0 + (c0 - g0)));
             }
+            // this batch's class sums into the tile: element f sits at ptile[f + pshift - q0 * V]
+            const int f_begin = q0 * V - pshift, f_end = (q0 + kBatchChunks) * V - pshift;
+            for (int e = lane; e < count; e += 32) {
+                const int f = e_key[e];
+                if (f >= f_begin && f < f_end) {
+                    const int idx = f - f_begin;
+                    ptile[idx] = e_val[e];
+                    atomicOr(&pmark[idx / V / 32], 1u << ((idx / V) & 31));
+                }
+            }
+            __syncwarp();
 #pragma unroll
             for (int k = 0; k < kUnroll; ++k) {
                 const int q = q0 + k * 32 + lane;
@@ -245,7 +367,24 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
                 const int f_lo = (int)((lo - g0) / E);
                 int r = chunk_row(f_lo);
                 int c = f_lo - r * D;
+                // the chunk's class sums (zero unless marked), cleared once read
+                const int ql = q - q0;
+                const bool marked = (pmark[ql >> 5] >> (ql & 31)) & 1u;
                 if (fast[k] && c + V <= D) {
+                    float pv[V];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) pv[i] = 0.0f;
+                    if (marked) {
+#pragma unroll
+                        for (int i = 0; i < V; i += 4) {
+                            const float4 v = reinterpret_cast<const float4*>(ptile + ql * V)[i / 4];
+                            pv[i] = v.x;
+                            pv[i + 1] = v.y;
+                            pv[i + 2] = v.z;
+                            pv[i + 3] = v.w;
+                            reinterpret_cast<float4*>(ptile + ql * V)[i / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
                     // a whole chunk inside one row
                     uint4 o = make_uint4(0u, 0u, 0u, 0u);
                     if (row_cov[r]) {
@@ -260,7 +399,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
                             } else {
                                 bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
                             }
-                            out[i] = s * fast_ex2(bits_to_float<DT>(bits) * kLog2e);
+                            out[i] = fmaf(s, fast_ex2(bits_to_float<DT>(bits) * kLog2e), -pv[i]);
                         }
                         if constexpr (E == 4) {
                             o = make_uint4(__float_as_uint(out[0]), __float_as_uint(out[1]), __float_as_uint(out[2]),
@@ -280,22 +419,19 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 4) grad_kernel(GradArg
                             ++r;
                         }
                         const float x = bits_to_float<DT>(load_elem<DT>(a0 + (size_t)f * E));
-                        const float gv = row_cov[r] ? row_scale[r] * fast_ex2(x * kLog2e) : 0.0f;
+                        const float pk = marked ? ptile[ql * V + f + pshift - q * V] : 0.0f;
+                        const float gv = row_cov[r] ? fmaf(row_scale[r], fast_ex2(x * kLog2e), -pk) : 0.0f;
                         store_elem<DT>(g0 + (size_t)f * E, pack1<DT>(gv));
                         ++c;
                     }
+                    if (marked) {
+                        for (int i = 0; i < V; ++i) ptile[ql * V + i] = 0.0f;
+                    }
                 }
             }
-        }
-        __syncwarp();  // the dense stores of the warp come before its corrections
-
-        // 3. the corrections, one element each
-        for (int e = lane; e < count; e += 32) {
-            const int key = e_key[e];
-            const int rr = key >> 16, cls = key & 0xffff;
-            const size_t f = (size_t)rr * D + cls;
-            const float x = bits_to_float<DT>(load_elem<DT>(a0 + f * E));
-            store_elem<DT>(g0 + f * E, pack1<DT>(fmaf(row_scale[rr], fast_ex2(x * kLog2e), -e_val[e])));
+            __syncwarp();
+            if (lane < kBatchChunks / 32) pmark[lane] = 0u;
+            __syncwarp();
         }
         __syncwarp();
     }
@@ -339,7 +475,8 @@ void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& wa
     rows = k;
     entry_cap = k * ecap;
     warp_smem = 2 * align_up(4 * (size_t)k, 16) + 2 * align_up(4 * (size_t)entry_cap, 16) +
-                align_up(4 * (size_t)(L.max_U + 1), 16);
+                align_up(4 * (size_t)(L.max_U + 1), 16) + 4 * (size_t)kBatchChunks * 8 + 4 * (kBatchChunks / 32);
+    warp_smem = align_up(warp_smem, 16);
 }
 
 cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s) {
