@@ -371,6 +371,306 @@ __device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
     group_sync<CTA>();
 }
 
+// A multi-warp chain item, split by role.  Consumer warps (the first nwc)
+// hold the state pairs and run the recursion; producer warps gather each
+// frame's label and blank words kRawFrames-1 frames ahead with cp.async
+// (a raw ring), turn them into extended-range emissions one frame ahead of
+// use (a converted ring) and leave the consumers nothing but the
+// recursion, the halo exchange and the stores.  One CTA barrier per frame
+// orders both rings.
+constexpr int kRawFrames = 16;
+constexpr int kConvFrames = 2;
+
+template <int P, int DT>
+__device__ void run_chain_item_split(const ChainArgs& a, int item, int nwc, unsigned char* smem) {
+    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    const UttInfo info = ws_at<UttInfo>(a.ws, a.L.off_utt)[item >> 1];
+    double* nll_out = ws_at<double>(a.ws, a.L.off_nll);
+    const int b = item >> 1;
+    const int dir = item & 1;  // 0 alpha, 1 beta
+    const int T = info.T, U = info.U;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NC = 32 * nwc;                 // consumer threads
+    const int NP = (int)blockDim.x - NC;     // producer threads
+    const bool consumer = tid < NC;
+    const int ptid = tid - NC;
+    const int32_t* tg = a.targets + info.toff;
+    constexpr int E = Elem<DT>::bytes;
+    const int W = a.L.max_U + 1;  // words per frame in the rings: labels 0..U-1, the blank at U
+    uint32_t* raw = reinterpret_cast<uint32_t*>(smem);
+    XP* conv = reinterpret_cast<XP*>(smem + sizeof(uint32_t) * kRawFrames * W);
+    XP* halo = conv + kConvFrames * W;  // [2][nwc]
+    XP* fin = halo + 2 * 32;
+
+    // consumers: labels of the pairs and their skip transitions
+    bool has_label[P], skip[P];
+    bool bad = false;
+    const int j0 = consumer ? tid * P : 0;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const int j = j0 + p;
+        has_label[p] = false;
+        skip[p] = false;
+        if (consumer) {
+            if (dir == 0) {  // (blank 2j, label 2j+1 = l_j)
+                has_label[p] = j < U;
+                skip[p] = j >= 1 && j < U && tg[j] != tg[j - 1];
+            } else {  // (label 2j-1 = l_{j-1}, blank 2j)
+                has_label[p] = j >= 1 && j <= U;
+                skip[p] = j >= 1 && j < U && tg[j - 1] != tg[j];
+            }
+        }
+    }
+    // producers: the words they gather, and a range check of every label
+    for (int w = consumer ? U + 1 : ptid; w < U; w += NP) {
+        const int c = tg[w];
+        if (c < 0 || c >= a.D) bad = true;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (tid == 0) {
+            set_status(ctrl, CTC_PACKED_DEV_LABEL_OUT_OF_RANGE);
+            if (dir == 0) {
+                nll_out[b] = __longlong_as_double(0x7ff8000000000000ll);
+                if (a.reduction == CTC_PACKED_NONE) a.loss[b] = __int_as_float(0x7fc00000);
+            }
+        }
+        __syncthreads();
+        return;
+    }
+
+    // producer streams: frame k is row start + k (alpha) or start + T - 1 - k (beta).  A
+    // producer thread owns the words w = ptid and ptid + NP (at most two; the blank is word U)
+    const uintptr_t buf_lo = reinterpret_cast<uintptr_t>(a.lp);
+    const uintptr_t buf_hi = buf_lo + (uintptr_t)a.lp_bytes;
+    const int64_t row0 = dir == 0 ? (int64_t)info.start : (int64_t)info.start + T - 1;
+    const intptr_t step_bytes = (dir == 0 ? 1 : -1) * (intptr_t)a.D * E;
+    const int d_odd = (E == 2) ? (a.D & 1) : 0;
+    const uint32_t raw_s = smem_addr(raw);
+    bool saw_nan = false;
+    bool own[2];
+    uintptr_t gfirst[2], gnext[2];
+    int half0[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int w = ptid + q * NP;
+        own[q] = !consumer && w <= U;
+        const int c = own[q] ? (w < U ? tg[w] : a.blank) : a.blank;
+        gfirst[q] = gnext[q] = buf_lo + (uintptr_t)((row0 * a.D + c) * E);
+        half0[q] = (int)((gfirst[q] >> 1) & 1);
+    }
+    auto issue_raw = [&](int k) {
+        if (!consumer) {
+            const bool live = k < T;
+            const uint32_t slot = raw_s + (uint32_t)((k & (kRawFrames - 1)) * W) * 4u;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                if (own[q]) gather<DT>(slot + (uint32_t)(ptid + q * NP) * 4u, live ? gnext[q] : gfirst[q], buf_hi, live);
+                gnext[q] += live ? step_bytes : 0;
+            }
+            cp_async_commit();
+        }
+    };
+    auto convert = [&](int k) {  // raw frame k -> converted ring
+        if (!consumer && k < T) {
+            const uint32_t* rs = raw + (k & (kRawFrames - 1)) * W;
+            XP* cs = conv + (k % kConvFrames) * W;
+            const int flip = d_odd & k;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                if (own[q]) {
+                    const int w = ptid + q * NP;
+                    const float x = word_to_float<DT>(rs[w], half0[q] ^ flip);
+                    saw_nan |= x != x;
+                    cs[w] = xp_from_log(x);
+                }
+            }
+        }
+    };
+
+    const bool store_me = consumer && j0 <= U;
+    int* st = ws_at<int>(a.ws, dir == 0 ? a.L.off_alpha : a.L.off_beta) + row0 * a.L.pitch + 2 * j0;
+    const intptr_t st_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.pitch;
+    int32_t* offp = ws_at<int32_t>(a.ws, dir == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo + warp;
+    const intptr_t off_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.nwo;
+    auto store_row = [&](const int (&x)[P], const int (&y)[P], int A) {
+        if (store_me) {
+            if constexpr (P == 1) {
+                *reinterpret_cast<int2*>(st) = make_int2(x[0], y[0]);
+            } else {
+#pragma unroll
+                for (int p = 0; p < P; p += 2)
+                    *reinterpret_cast<int4*>(st + 2 * p) = make_int4(x[p], y[p], x[p + 1], y[p + 1]);
+            }
+        }
+        if (lane == 0) *offp = A;
+        st += st_step;
+        offp += off_step;
+    };
+    const XP zero{0.0f, kEZero};
+    // emissions of frame k for my pairs, from the converted ring
+    auto emissions = [&](int k, XP& eb, XP (&el)[P]) {
+        const XP* cs = conv + (k % kConvFrames) * W;
+        eb = cs[U];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int j = j0 + p;
+            const int w = dir == 0 ? j : j - 1;
+            el[p] = has_label[p] ? cs[w] : zero;
+        }
+    };
+
+    // prologue: raw frames 0 .. kRawFrames-2 in flight, frames 0 .. kConvFrames-2 converted
+#pragma unroll 1
+    for (int k = 0; k < kRawFrames - 1; ++k) issue_raw(k);
+    if (!consumer) {
+        cp_async_wait<kRawFrames - kConvFrames>();
+        for (int k = 0; k < kConvFrames - 1; ++k) convert(k);
+    }
+
+    XP vb[P], vl[P];
+#pragma unroll 1
+    for (int i = 0; i < T; ++i) {
+        __syncthreads();
+        if (!consumer) {
+            // producers: frame i + kConvFrames - 1 into the converted ring, frame i + kRawFrames - 1 requested
+            cp_async_wait<kRawFrames - kConvFrames - 1>();
+            convert(i + kConvFrames - 1);
+            issue_raw(i + kRawFrames - 1);
+            continue;
+        }
+        XP eb, el[P];
+        emissions(i, eb, el);
+        if (i == 0) {
+            int x[P], y[P];
+            int emax = kEZero;
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const int j = j0 + p;
+                if (dir == 0) {
+                    vb[p] = j == 0 ? eb : zero;
+                    vl[p] = (j == 0 && U >= 1) ? el[p] : zero;
+                } else {
+                    vb[p] = j == U ? eb : zero;
+                    vl[p] = (j == U && U >= 1) ? el[p] : zero;
+                }
+                vb[p] = xp_norm(vb[p].m, vb[p].e);
+                vl[p] = xp_norm(vl[p].m, vl[p].e);
+                emax = max(emax, max(vb[p].e, vl[p].e));
+            }
+            if (dir == 0 && lane == 31) halo[warp] = vl[P - 1];
+            if (dir == 1 && lane == 0) halo[warp] = vl[0];
+            const int A = dir == 0 ? 0 : __reduce_max_sync(0xffffffffu, emax);
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const int j = j0 + p;
+                if (dir == 0) {
+                    x[p] = j == 0 ? 0 : kFixZero;
+                    y[p] = (j == 0 && U >= 1) ? 0 : kFixZero;
+                } else {
+                    x[p] = fix_log2(vl[p].m, vl[p].e, A);
+                    y[p] = fix_log2(vb[p].m, vb[p].e, A);
+                }
+            }
+            store_row(x, y, A);
+            continue;
+        }
+        // the label state just below (alpha) or above (beta) my pairs, previous frame
+        XP nb;
+        {
+            const int src = dir == 0 ? max(warp - 1, 0) : min(warp + 1, nwc - 1);
+            const XP h = halo[((i - 1) & 1) * nwc + src];
+            const bool edge = dir == 0 ? (lane == 0) : (lane == 31);
+            const bool has_nb = dir == 0 ? warp > 0 : warp < nwc - 1;
+            const XP mine = dir == 0 ? vl[P - 1] : vl[0];
+            nb.m = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.m, 1) : __shfl_down_sync(0xffffffffu, mine.m, 1);
+            nb.e = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.e, 1) : __shfl_down_sync(0xffffffffu, mine.e, 1);
+            if (edge) nb = has_nb ? h : zero;
+        }
+        float Sb[P], Sl[P];
+        int Eb[P], El[P];
+        if (dir == 0) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const XP prev = p ? vl[p - 1] : nb;
+                xp_sum3(vl[p], vb[p], skip[p] ? prev : zero, Sl[p], El[p]);
+                xp_sum2(vb[p], prev, Sb[p], Eb[p]);
+            }
+        } else {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const XP next = (p < P - 1) ? vl[p + 1] : nb;
+                xp_sum3(vl[p], vb[p], skip[p] ? next : zero, Sl[p], El[p]);
+                xp_sum2(vb[p], next, Sb[p], Eb[p]);
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            vl[p] = xp_norm(Sl[p] * el[p].m, El[p] + el[p].e);
+            vb[p] = xp_norm(Sb[p] * eb.m, Eb[p] + eb.e);
+        }
+        if (dir == 0 && lane == 31) halo[(i & 1) * nwc + warp] = vl[P - 1];
+        if (dir == 1 && lane == 0) halo[(i & 1) * nwc + warp] = vl[0];
+        int emax = kEZero;
+#pragma unroll
+        for (int p = 0; p < P; ++p) emax = dir == 0 ? max(emax, max(Eb[p], El[p])) : max(emax, max(vb[p].e, vl[p].e));
+        const int A = __reduce_max_sync(0xffffffffu, emax);
+        int x[P], y[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            if (dir == 0) {  // alpha rows: before the emission
+                x[p] = fix_log2(Sb[p], Eb[p], A);
+                y[p] = fix_log2(Sl[p], El[p], A);
+            } else {
+                x[p] = fix_log2(vl[p].m, vl[p].e, A);
+                y[p] = fix_log2(vb[p].m, vb[p].e, A);
+            }
+        }
+        store_row(x, y, A);
+    }
+
+    const bool any_nan = __syncthreads_or(saw_nan);
+    if (dir == 0) {
+        // the paths end in the last blank (pair U) or the last label (pair U-1)
+        if (tid == 0) {
+            fin[0] = zero;
+            fin[1] = zero;
+        }
+        __syncthreads();
+        if (consumer) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const int j = j0 + p;
+                if (j == U) fin[0] = vb[p];
+                if (U >= 1 && j == U - 1) fin[1] = vl[p];
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const XP f0 = fin[0], f1 = fin[1];
+            double v;
+            if (any_nan) {
+                v = __longlong_as_double(0x7ff8000000000000ll);
+            } else if (f0.m == 0.0f && f1.m == 0.0f) {
+                v = __longlong_as_double(0x7ff0000000000000ll);  // no path: +inf
+            } else {
+                const int Em = max(f0.e, f1.e);
+                const double sum = (double)f0.m * exp2((double)(max(f0.e - Em, -1100))) +
+                                   (double)f1.m * exp2((double)(max(f1.e - Em, -1100)));
+                v = -((double)Em + log2(sum)) * kLn2D;
+            }
+            nll_out[b] = v;
+            if (a.reduction == CTC_PACKED_NONE) {
+                float out = (float)v;
+                if (a.zero_infinity && isinf(v)) out = 0.0f;
+                a.loss[b] = out;
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+}
+
 // Label metadata the backward needs, one warp per utterance: for each target
 // position whether it is the first occurrence of its class (then it owns the
 // class's posterior sum), the next position with the same class, and whether
@@ -445,14 +745,18 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
     const int n_big = ctrl->n_big, n_small = ctrl->n_small, n_lab = ctrl->n_lab;
 
     // 1. multi-warp chains, longest first, one at a time per CTA
-    Group cg{tid, NT, warp, NW, ring, halo, fin};
     for (;;) {
         if (tid == 0) s_item = (int)atomicAdd(&ctrl->big_head, 1u);
         __syncthreads();
         const int k = s_item;
         __syncthreads();
         if (k >= n_big) break;
-        run_chain_item<P, DT, true>(a, queue[k], cg);
+        if (P == 1 && a.consumer_warps < NW) {
+            run_chain_item_split<P, DT>(a, queue[k], a.consumer_warps, smem_raw);
+        } else {  // every warp holds pairs and gathers its own columns
+            Group cg{tid, NT, warp, NW, ring, halo, fin};
+            run_chain_item<P, DT, true>(a, queue[k], cg);
+        }
     }
     // 2. single-warp chains, each warp on its own
     Group wg{lane, 32, warp, NW, ring + warp * kRing * (32 * P + 1), halo, fin + 4 * warp};
@@ -518,18 +822,32 @@ int chain_pairs_per_thread(int max_target_len) { return pairs_for_max_u(max_targ
 int chain_warps(int max_target_len, int P) {
     const int pairs = max_target_len + 1;
     int nw = (pairs + 32 * P - 1) / (32 * P);
-    return nw < 1 ? 1 : (nw > 32 ? 32 : nw);
+    return nw < 1 ? 1 : (nw > 30 ? 30 : nw);
 }
 
-static size_t chain_smem_bytes(int P, int nw) {
+static size_t chain_smem_bytes(int P, int nw, int max_u) {
     const int nt = 32 * nw;
-    return sizeof(uint32_t) * (size_t)kRing * (nt * P + nw) + sizeof(float) * (size_t)(4 * nw + 4 * nw);
+    const size_t warp_mode = sizeof(uint32_t) * (size_t)kRing * (nt * P + nw) + sizeof(float) * (size_t)(4 * nw + 4 * nw);
+    const size_t W = (size_t)max_u + 1;
+    const size_t split = P == 1 ? sizeof(uint32_t) * kRawFrames * W + sizeof(XP) * (kConvFrames * W + 2 * 32 + 2) : 0;
+    return warp_mode > split ? warp_mode : split;
+}
+
+// Producer warps a chain CTA gets: enough that each producer thread owns at
+// most two of the max_U + 1 columns, when consumers and producers fit 32 warps.
+static int producer_warps(int P, int nwc, int max_u) {
+    if (P != 1) return 0;
+    const int nwp = (max_u + 1 + 63) / 64;
+    return nwc + nwp <= 32 ? nwp : 0;
 }
 
 template <int P, int DT>
-static cudaError_t launch_chain_t(const ChainArgs& a, int nw, cudaStream_t s) {
+static cudaError_t launch_chain_t(const ChainArgs& a0, int nwc, cudaStream_t s) {
+    ChainArgs a = a0;
+    a.consumer_warps = nwc;
+    const int nw = nwc + producer_warps(P, nwc, a.L.max_U);
     static int configured_smem = -1;
-    const size_t smem = chain_smem_bytes(P, nw);
+    const size_t smem = chain_smem_bytes(P, nw, a.L.max_U);
     cudaError_t e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;

@@ -28,7 +28,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr double kLog2eD = 1.4426950408889634074;
 constexpr double kLn2D = 0.69314718055994530942;
 constexpr int kMaxD = 16384;          // one gradient row must fit a shared-memory tile
-constexpr int kMaxTargetLen = 4095;   // 4 state pairs per thread x 1024 threads
+constexpr int kMaxTargetLen = 3839;   // 4 state pairs per thread x 30 warps of a chain CTA
 constexpr long long kSpinLimit = 1ll << 26;  // bounded waits give up after this many polls
 
 // Control block at the start of the workspace.
@@ -72,7 +72,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // State pairs (blank, label) each thread of a chain holds, from the target bound.
 __host__ __device__ inline int pairs_for_max_u(int max_u) {
     const int pairs = max_u + 1;
-    return pairs <= 1024 ? 1 : pairs <= 2048 ? 2 : 4;
+    return pairs <= 960 ? 1 : pairs <= 1920 ? 2 : 4;  // at most 30 warps hold the pairs
 }
 
 __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_t max_U, int32_t D) {
@@ -89,7 +89,7 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     {
         const int pairs = max_U + 1;
         const int nw = (pairs + 32 * P - 1) / (32 * P);
-        L.nwo = nw < 1 ? 1 : (nw > 32 ? 32 : nw);
+        L.nwo = nw < 1 ? 1 : (nw > 30 ? 30 : nw);
     }
     L.lab_cap = (int64_t)B * max_U + B;
     size_t o = 0;

@@ -30,6 +30,7 @@ struct ChainArgs {
     int blank;
     int reduction;
     int zero_infinity;
+    int consumer_warps;  // warps of a chain CTA that hold state pairs (the rest gather)
 };
 
 struct GradArgs {
