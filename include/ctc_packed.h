@@ -157,6 +157,59 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
  */
 ctc_packed_status ctc_packed_read_status(const void* workspace, uint32_t* device_status, cudaStream_t stream);
 
+/*
+ * Bytes of the fixed scratch array behind ctc_packed_forward_noalloc (32 MiB).
+ * A batch fits when ctc_packed_workspace_size(...) <= this value.
+ */
+#define CTC_PACKED_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * Loss-only forward for callers that cannot allocate device memory and so
+ * cannot hand the library a workspace.  Examples: a plain C host with no
+ * device allocator; a process whose device memory is reserved by another
+ * framework's pool, where a new allocation could fail; a scoring loop
+ * (validation, n-best rescoring) that must not stall on the device-wide
+ * synchronisation that freeing memory brings.  The page "feat(asr): native
+ * CTC loss kernel over sequence-packed log probabilities" has no counterpart:
+ * its forward always allocates its own buffers.
+ *
+ * Arguments and the loss are those of ctc_packed_forward with
+ * CTC_PACKED_FLAG_LOSS_ONLY; there is no workspace argument and no backward.
+ * The scratch is an array of CTC_PACKED_NOALLOC_SCRATCH_BYTES in the memory of
+ * each device, built into the library.  The function calls no allocator
+ * (no cudaMalloc or cudaFree, nothing of a framework's).
+ *
+ *   - Size limit: a batch whose ctc_packed_workspace_size exceeds
+ *     CTC_PACKED_NOALLOC_SCRATCH_BYTES is rejected with
+ *     CTC_PACKED_ERR_WORKSPACE before any CUDA call.  Sizes that are invalid
+ *     or unsupported return the codes ctc_packed_forward would return.
+ *   - Device: the call uses the scratch of the CURRENT device, and `stream`
+ *     must belong to it.
+ *   - First call on a device: it looks up the scratch's device address once
+ *     (cudaGetSymbolAddress), which may load the library's device code on
+ *     that device; later calls reuse the address.  Make that first call
+ *     before any stream capture starts.  If the look-up fails, the call
+ *     returns CTC_PACKED_ERR_CUDA and clears the CUDA error it left.
+ *   - Memory: the array holds 32 MiB of device memory on every device where
+ *     the library's device code is loaded, at the latest from the first call
+ *     on that device.
+ *   - Zeroing: nothing needs clearing by the caller.  The first kernel of
+ *     every call resets, on `stream`, the counters and queue heads that must
+ *     start at zero; the rest is written before it is read.
+ *   - Overlap: all calls on one device share the one scratch.  Two calls whose
+ *     GPU work can overlap (different streams without an ordering event,
+ *     different host threads) race and give wrong losses.  Issue them on
+ *     one stream, or order them with events.
+ *   - Malformed inputs that only the device can see give that utterance a
+ *     NaN loss, as in ctc_packed_forward.  The status word lives in the
+ *     scratch and cannot be read by the caller.
+ */
+ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total,
+                                             int32_t D, const int32_t* cu_seqlens, const int32_t* lengths,
+                                             const int32_t* targets, const int32_t* target_lengths, int32_t B,
+                                             int32_t max_target_len, int32_t blank, int zero_infinity,
+                                             ctc_packed_reduction reduction, float* loss, cudaStream_t stream);
+
 /* Human-readable name of a ctc_packed_status value (static storage). */
 const char* ctc_packed_status_string(ctc_packed_status status);
 

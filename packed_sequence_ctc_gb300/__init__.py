@@ -25,6 +25,7 @@ __all__ = [
     "load_library", "ctc_packed_workspace_size", "ctc_packed_forward", "ctc_packed_backward",
     "ctc_packed_read_status", "ctc_packed_status_string", "packed_ctc_loss", "PackedCTCLoss", "Workspace",
     "DTYPE_CODES", "REDUCTION_CODES", "DEVICE_STATUS_BITS", "CTCPackedError",
+    "ctc_packed_forward_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +34,7 @@ LIB_PATH = os.path.join(_HERE, "libctc_packed.so")
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 REDUCTION_CODES = {"none": 0, "sum": 1, "mean": 2}
 FLAG_LOSS_ONLY = 0x1
+NOALLOC_SCRATCH_BYTES = 32 << 20  # CTC_PACKED_NOALLOC_SCRATCH_BYTES
 DEVICE_STATUS_BITS = {
     0x1: "target_lengths must not be negative",
     0x2: "target_lengths must not exceed the targets width (max_target_len)",
@@ -73,6 +75,9 @@ def load_library(path: Optional[str] = None):
     lib.ctc_packed_read_status.restype = ctypes.c_int
     lib.ctc_packed_status_string.argtypes = [ctypes.c_int]
     lib.ctc_packed_status_string.restype = ctypes.c_char_p
+    lib.ctc_packed_forward_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32,
+                                               ctypes.c_int, ctypes.c_int, vp, vp]
+    lib.ctc_packed_forward_noalloc.restype = ctypes.c_int
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -124,6 +129,19 @@ def ctc_packed_backward(log_probs, cu_seqlens, lengths, targets, target_lengths,
         _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
         int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(grad_loss), _ptr(workspace), workspace.numel(),
         _ptr(grad_log_probs), _stream(stream)))
+
+
+def ctc_packed_forward_noalloc(log_probs, cu_seqlens, lengths, targets, target_lengths, blank: int,
+                               zero_infinity: bool, reduction: str, loss, max_target_len: int, stream=None):
+    """Enqueue the loss-only forward that uses the library's own fixed scratch
+    (for callers that cannot allocate a workspace; calls overlapping on the
+    GPU race, see the C declaration)."""
+    T_total, D = log_probs.shape
+    B = lengths.numel()
+    _check(load_library().ctc_packed_forward_noalloc(
+        _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
+        _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
+        int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(loss), _stream(stream)))
 
 
 def ctc_packed_read_status(workspace, stream=None) -> int:
