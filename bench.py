@@ -35,6 +35,8 @@ if ROOT not in sys.path:
 
 METRIC = "packed CTC fwd+bwd frames/s and achieved HBM GB/s (% of GB300 peak)"
 FALLBACK_HBM_GBS = 6800.0
+# kernels of one step: prep, emission gather, chains (forward); gradient (backward)
+KERNELS_PER_STEP = 4
 L2_BYTES = 129 * 2**20
 
 
@@ -387,7 +389,7 @@ def run_ours(args):
             "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dt[cfg["io_dtype"]], "data": "synthetic",
             "config": cfg, "hbm_gbs": round(path_gbs, 1), "roofline": roofline, "path_roofline": path_roofline,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * K, "clocks": clocks,
             "device_status": status,
         }
         print(json.dumps(line), flush=True)

@@ -60,8 +60,6 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if ((flags & ~CTC_PACKED_FLAG_LOSS_ONLY) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     const Layout L = make_layout(T_total, B, max_target_len, D);
-    const int P = chain_pairs_per_thread(max_target_len);
-    const int nw = chain_warps(max_target_len, P);
     const bool need_grad = (flags & CTC_PACKED_FLAG_LOSS_ONLY) == 0;
 
     PrepArgs pa{};
@@ -74,7 +72,7 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     pa.reduction = reduction;
     pa.zero_infinity = zero_infinity ? 1 : 0;
     pa.need_grad = need_grad ? 1 : 0;
-    pa.pairs_per_thread = P;
+    pa.group_pairs = L.gpairs;
     if (launch_prep(pa, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
 
     ChainArgs ca{};
@@ -82,6 +80,7 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     ca.ws = workspace;
     ca.lp = log_probs;
     ca.lp_bytes = T_total * (int64_t)D * elem_bytes(dtype);
+    ca.cu = cu_seqlens;
     ca.targets = targets;
     ca.target_lengths = target_lengths;
     ca.loss = loss;
@@ -89,7 +88,8 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     ca.blank = blank;
     ca.reduction = reduction;
     ca.zero_infinity = zero_infinity ? 1 : 0;
-    if (launch_chain(ca, P, nw, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    if (launch_emit(ca, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    if (launch_chain(ca, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     return CTC_PACKED_OK;
 }
 

@@ -14,19 +14,27 @@
 // How it maps to the GPU.  Each utterance is two independent work items, its
 // alpha chain and its beta chain, so both serial recursions of an utterance
 // run at the same time on different SMs (the page runs beta inside its
-// backward program, after the forward).  A chain item is run by a group of
-// threads: the whole CTA when the target is long, one warp when 2U+1 states
-// fit in a warp.  Thread j of a group holds P consecutive *state pairs*:
+// backward program, after the forward).  Lane l of a chain warp holds P
+// consecutive *state pairs*:
 //   alpha pair j = (blank 2j, label 2j+1),   beta pair j = (label 2j-1, blank 2j),
-// so a frame step needs the state just below (alpha) or above (beta) the
-// thread's pairs only: one warp shuffle, plus a shared-memory halo across
-// warps and one CTA barrier per frame.
+// so a frame step needs only the state just below (alpha) or above (beta) the
+// lane's pairs: one warp shuffle.
 //
-// Label columns: every frame a chain reads lp[t, blank] and lp[t, l_j] for its
-// labels.  Each thread gathers its own labels' words with 4-byte cp.async
-// kRing-1 frames ahead into a shared-memory ring (the word that holds a
-// 2-byte element is fetched whole and the right half picked on use), so no
-// global-memory latency sits on the recursion.
+// Ghost lanes.  A long target spreads over several warps of a CTA.  Each
+// warp owns (32 - G) * P pairs; its G extra lanes at the edge facing its
+// neighbour (below for alpha, above for beta) shadow the neighbour's G * P
+// edge pairs.  The shadow copies are exact right after a halo exchange and
+// go wrong one pair per frame from the outer edge inward, so the owned pairs
+// stay exact for G * P frames: the warps exchange their edges through shared
+// memory, under one named barrier, only every G * P frames, and run the
+// frames in between on shuffles alone.  Outside the target range (the lower
+// shadow of the first warp, the upper one of the last) the states are zero
+// and stay exactly zero.
+//
+// Emissions come from the emission matrix (emit.cu): every frame a lane
+// needs its P label emissions and the blank's, contiguous in that row.  Each
+// warp keeps 16 / P frames of them in flight with 8-byte cp.async copies
+// into its own shared-memory ring.
 //
 // Arithmetic: the recursion runs on probabilities in extended range (a float
 // mantissa and an int32 binary exponent per state, see ctc_common.cuh):
@@ -34,14 +42,14 @@
 // i.e. only multiply-adds and integer exponent arithmetic on the critical
 // path, no exp or log, no cross-warp normalisation.
 //
-// What is stored for the backward, as int32 fixed-point log2 values with 19
-// fraction bits relative to a per-(frame, warp) integer offset (the warp's
-// largest exponent, stored per frame in aoff / boff): alpha rows hold the
+// What is stored for the backward, one int32 per state holding m * 2^k
+// exactly up to a 19-bit mantissa (enc_state in ctc_common.cuh), k relative
+// to a per-(frame, warp) integer offset (the largest exponent among the
+// warp's owned states, stored per frame in aoff / boff): alpha rows hold the
 // value *before* the frame's emission, alpha_t(s) / p_t(s), so the backward
-// needs no log-probability gather; beta rows hold beta_t(s).  The posterior
-// is then an exact integer sum plus one ex2.
-#include <cstdio>
-
+// needs no log-probability gather; beta rows hold beta_t(s).  A row is
+// encoded and stored one frame late, so that work overlaps the next frame's
+// dependent chain.
 #include "ctc_common.cuh"
 #include "ctc_kernels.h"
 
@@ -49,451 +57,151 @@ namespace ctcp {
 
 namespace {
 
-struct Group {
-    int tid;         // thread index within the group
-    int n;           // threads in the group
-    int warp;        // warp index within the CTA (CTA mode)
-    int nw;          // warps in the CTA (CTA mode)
-    uint32_t* ring;  // kRing slots of (n * P + 1) words
-    float* halo;     // [2][nw] extended values (m, e)   (CTA mode)
-    float* fin;      // 2 extended values private to the group
+template <int P>
+struct ChainShape {
+    static constexpr int G = ghost_lanes(P);  // shadow lanes per warp
+    static constexpr int GP = group_pairs(P); // pairs a warp owns
+    static constexpr int F = G * P;           // frames between halo exchanges (4 for every P)
+    static constexpr int R = P == 4 ? 4 : 8;  // emission frames in flight per warp
+    static constexpr int LW = P + 1;          // extended emissions per lane and frame: P labels, the blank
+    static constexpr int XW = G * P * 2;      // extended values one warp sends per exchange
+    static_assert(F == 4, "frames are run in blocks of one exchange period");
+    static_assert(R % F == 0, "a block of frames maps onto consecutive ring slots");
 };
 
-template <bool CTA>
-__device__ __forceinline__ void group_sync() {
-    if constexpr (CTA) {
-        __syncthreads();
-    } else {
-        __syncwarp();
-    }
+__device__ __forceinline__ void bar_named(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool bar_named_or(int id, int n, bool v) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((int)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+// 8-byte async copy global -> shared.
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
 
-template <int DT>
-__device__ __forceinline__ uintptr_t word_of(uintptr_t addr) {
-    if constexpr (DT == 0) {
-        return addr;
-    } else {
-        return addr & ~uintptr_t(3);
-    }
-}
+struct ItemCtx {
+    int w;     // this warp's index among the item's warps
+    int nw;    // warps running the item (1: a single-warp item, no exchanges)
+    XP* ring;  // this warp's emission ring
+    XP* xch;   // halo exchange buffers, [2][nw][XW]
+    XP* fin;   // 2 extended values shared by the item's warps
+};
 
-// Copy the 4-byte word holding element `addr` into the ring slot `dst`.  The
-// buffer starts 4-byte aligned, so the word never starts before it; a word
-// that would run past its end copies only the element's 2 bytes (cp.async
-// zero-fills the rest).  `live` false copies nothing (the address is then a
-// valid one that is not read).
-template <int DT>
-__device__ __forceinline__ void gather(uint32_t dst, uintptr_t addr, uintptr_t hi, bool live) {
-    const uintptr_t w = word_of<DT>(addr);
-    int n = 4;
-    if constexpr (DT != 0) n = (w + 4 <= hi) ? 4 : 2;
-    n = live ? n : 0;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(w), "r"(n) : "memory");
-}
-
-template <int P, int DT, bool CTA>
-__device__ void run_chain_item(const ChainArgs& a, int item, const Group& g) {
+// One chain (DIR 0 alpha, 1 beta) of utterance b, run by warp c.w of c.nw.
+//
+// Frame 0 is the initialisation; frames 1.. run in blocks of F = 4: each
+// frame is one recursion step on shuffles alone, the row of the frame
+// before is encoded and stored on the side, and the emissions of the frame
+// R - 1 ahead are requested.  After a block the states are renormalised
+// (between renormalisations a mantissa grows at most 12x a frame) and the
+// warps of a multi-warp item exchange their edges.
+template <int P, int DIR>
+__device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
+    using S = ChainShape<P>;
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
-    const UttInfo info = ws_at<UttInfo>(a.ws, a.L.off_utt)[item >> 1];
+    const UttInfo info = ws_at<UttInfo>(a.ws, a.L.off_utt)[b];
     double* nll_out = ws_at<double>(a.ws, a.L.off_nll);
-    const int b = item >> 1;
-    const int dir = item & 1;  // 0 alpha, 1 beta
     const int T = info.T, U = info.U;
-    const int lane = g.tid & 31;
+    const int lane = threadIdx.x & 31;
+    const bool multi = c.nw > 1;
+    const int nthreads = 32 * c.nw;
     const int32_t* tg = a.targets + info.toff;
-    constexpr int E = Elem<DT>::bytes;
-
-    // labels of my pairs and their skip transitions
-    int cls[P];
-    bool has_label[P], skip[P];
-    bool bad = false;
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-        const int j = g.tid * P + p;
-        if (dir == 0) {  // (blank 2j, label 2j+1 = l_j)
-            has_label[p] = j < U;
-            cls[p] = has_label[p] ? tg[j] : 0;
-            skip[p] = j >= 1 && j < U && cls[p] != tg[j - 1];
-        } else {  // (label 2j-1 = l_{j-1}, blank 2j)
-            has_label[p] = j >= 1 && j <= U;
-            cls[p] = has_label[p] ? tg[j - 1] : 0;
-            skip[p] = j >= 1 && j < U && cls[p] != tg[j];
-        }
-        if (has_label[p] && (cls[p] < 0 || cls[p] >= a.D)) bad = true;
-    }
-    if constexpr (CTA) {
-        bad = __syncthreads_or(bad);
-    } else {
-        bad = __any_sync(0xffffffffu, bad);
-    }
-    if (bad) {
-        if (g.tid == 0) {
-            set_status(ctrl, CTC_PACKED_DEV_LABEL_OUT_OF_RANGE);
-            if (dir == 0) {
-                nll_out[b] = __longlong_as_double(0x7ff8000000000000ll);
-                if (a.reduction == CTC_PACKED_NONE) a.loss[b] = __int_as_float(0x7fc00000);
-            }
-        }
-        group_sync<CTA>();
-        return;
-    }
-
-    // gather streams: frame 0 is row start (alpha) or row start + T - 1 (beta)
-    const uintptr_t buf_lo = reinterpret_cast<uintptr_t>(a.lp);
-    const uintptr_t buf_hi = buf_lo + (uintptr_t)a.lp_bytes;
-    const int64_t row0 = dir == 0 ? (int64_t)info.start : (int64_t)info.start + T - 1;
-    const intptr_t step_bytes = (dir == 0 ? 1 : -1) * (intptr_t)a.D * E;
-    const int d_odd = (E == 2) ? (a.D & 1) : 0;
-    uintptr_t gnext[P], gfirst[P];
-    int half0[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-        gfirst[p] = gnext[p] = buf_lo + (uintptr_t)((row0 * a.D + cls[p]) * E);
-        half0[p] = (int)((gfirst[p] >> 1) & 1);
-    }
-    const uintptr_t bfirst = buf_lo + (uintptr_t)((row0 * a.D + a.blank) * E);
-    uintptr_t bnext = bfirst;
-    const int bhalf0 = (int)((bfirst >> 1) & 1);
-
-    const int SS = g.n * P + 1;  // words per ring slot: P label words per thread, then the blank
-    const uint32_t ring_s = smem_addr(g.ring);
-    auto issue = [&](int k) {
-        const bool live = k < T;
-        const uint32_t slot = ring_s + (uint32_t)((k & (kRing - 1)) * SS) * 4u;
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            gather<DT>(slot + (uint32_t)(p * g.n + g.tid) * 4u, live ? gnext[p] : gfirst[p], buf_hi,
-                       live && has_label[p]);
-            gnext[p] += live ? step_bytes : 0;
-        }
-        if (g.tid == 0) gather<DT>(slot + (uint32_t)(g.n * P) * 4u, live ? bnext : bfirst, buf_hi, live);
-        bnext += live ? step_bytes : 0;
-        cp_async_commit();
-    };
-    // emissions of step k as extended probabilities; a NaN log probability is remembered
-    bool saw_nan = false;
-    auto consume = [&](int k, XP& eb, XP (&el)[P]) {
-        const uint32_t* slot = g.ring + (k & (kRing - 1)) * SS;
-        const int flip = d_odd & k;  // with D odd a 2-byte element changes halves every frame
-        const float lb = word_to_float<DT>(slot[g.n * P], bhalf0 ^ flip);
-        saw_nan |= lb != lb;
-        eb = xp_from_log(lb);
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const float ll = word_to_float<DT>(slot[p * g.n + g.tid], half0[p] ^ flip);
-            saw_nan |= has_label[p] && ll != ll;
-            el[p] = has_label[p] ? xp_from_log(ll) : XP{0.0f, kEZero};
-        }
-    };
-
-    const int j0 = g.tid * P;
-    const bool store_me = j0 <= U;
-    int* st = ws_at<int>(a.ws, dir == 0 ? a.L.off_alpha : a.L.off_beta) + row0 * a.L.pitch + 2 * j0;
-    const intptr_t st_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.pitch;
-    int32_t* offp = ws_at<int32_t>(a.ws, dir == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo +
-                    (CTA ? g.warp : 0);
-    const intptr_t off_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.nwo;
-    auto store_row = [&](const int (&x)[P], const int (&y)[P], int A) {
-        if (store_me) {
-            if constexpr (P == 1) {
-                *reinterpret_cast<int2*>(st) = make_int2(x[0], y[0]);
-            } else {
-#pragma unroll
-                for (int p = 0; p < P; p += 2)
-                    *reinterpret_cast<int4*>(st + 2 * p) = make_int4(x[p], y[p], x[p + 1], y[p + 1]);
-            }
-        }
-        if (lane == 0) *offp = A;
-        st += st_step;
-        offp += off_step;
-    };
-    XP* halo = reinterpret_cast<XP*>(g.halo);
     const XP zero{0.0f, kEZero};
 
-    // prologue: kRing-1 frames in flight
-#pragma unroll 1
-    for (int k = 0; k < kRing - 1; ++k) issue(k);
-
-    XP vb[P], vl[P];  // alpha (blank 2j, label 2j+1) / beta (label 2j-1, blank 2j), extended probabilities
-    XP eb_cur, el_cur[P], eb_nxt, el_nxt[P];
-
-    // step 0 (frames 0 and 1 have landed)
-    cp_async_wait<kRing - 3>();
-    group_sync<CTA>();
-    consume(0, eb_cur, el_cur);
-    consume(1, eb_nxt, el_nxt);
-    {
-        int x[P], y[P];
-        int emax = kEZero;
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const int j = j0 + p;
-            if (dir == 0) {
-                vb[p] = j == 0 ? eb_cur : zero;
-                vl[p] = (j == 0 && U >= 1) ? el_cur[p] : zero;
-            } else {
-                vb[p] = j == U ? eb_cur : zero;
-                vl[p] = (j == U && U >= 1) ? el_cur[p] : zero;
-            }
-            vb[p] = xp_norm(vb[p].m, vb[p].e);
-            vl[p] = xp_norm(vl[p].m, vl[p].e);
-            emax = max(emax, max(vb[p].e, vl[p].e));
-        }
-        if constexpr (CTA) {
-            if (dir == 0 && lane == 31) halo[g.warp] = vl[P - 1];
-            if (dir == 1 && lane == 0) halo[g.warp] = vl[0];
-        }
-        const int A = dir == 0 ? 0 : __reduce_max_sync(0xffffffffu, emax);
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const int j = j0 + p;
-            if (dir == 0) {  // before the emission the two start states have probability 1
-                x[p] = j == 0 ? 0 : kFixZero;
-                y[p] = (j == 0 && U >= 1) ? 0 : kFixZero;
-            } else {
-                x[p] = fix_log2(vl[p].m, vl[p].e, A);
-                y[p] = fix_log2(vb[p].m, vb[p].e, A);
-            }
-        }
-        store_row(x, y, A);
-    }
-    issue(kRing - 1);
-
-#pragma unroll 1
-    for (int i = 1; i < T; ++i) {
-        cp_async_wait<kRing - 3>();  // frames i and i+1 have landed
-        group_sync<CTA>();
-        eb_cur = eb_nxt;
-#pragma unroll
-        for (int p = 0; p < P; ++p) el_cur[p] = el_nxt[p];
-        // the label state just below (alpha) or above (beta) my pairs, previous frame
-        XP nb;
-        {
-            const int src = dir == 0 ? max(g.warp - 1, 0) : min(g.warp + 1, g.nw - 1);
-            const XP h = CTA ? halo[((i - 1) & 1) * g.nw + src] : zero;
-            const bool edge = dir == 0 ? (lane == 0) : (lane == 31);
-            const bool has_nb = CTA && (dir == 0 ? g.warp > 0 : g.warp < g.nw - 1);
-            const XP mine = dir == 0 ? vl[P - 1] : vl[0];
-            nb.m = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.m, 1) : __shfl_down_sync(0xffffffffu, mine.m, 1);
-            nb.e = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.e, 1) : __shfl_down_sync(0xffffffffu, mine.e, 1);
-            if (edge) nb = has_nb ? h : zero;
-        }
-        float Sb[P], Sl[P];
-        int Eb[P], El[P];
-        if (dir == 0) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const XP prev = p ? vl[p - 1] : nb;
-                xp_sum3(vl[p], vb[p], skip[p] ? prev : zero, Sl[p], El[p]);
-                xp_sum2(vb[p], prev, Sb[p], Eb[p]);
-            }
-        } else {
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const XP next = (p < P - 1) ? vl[p + 1] : nb;
-                xp_sum3(vl[p], vb[p], skip[p] ? next : zero, Sl[p], El[p]);
-                xp_sum2(vb[p], next, Sb[p], Eb[p]);
-            }
-        }
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            vl[p] = xp_norm(Sl[p] * el_cur[p].m, El[p] + el_cur[p].e);
-            vb[p] = xp_norm(Sb[p] * eb_cur.m, Eb[p] + eb_cur.e);
-        }
-        if constexpr (CTA) {  // the critical value first: the neighbour warp waits for it
-            if (dir == 0 && lane == 31) halo[(i & 1) * g.nw + g.warp] = vl[P - 1];
-            if (dir == 1 && lane == 0) halo[(i & 1) * g.nw + g.warp] = vl[0];
-        }
-        // off the critical path: the next frame's emissions, the stored rows, the next gather
-        consume(i + 1, eb_nxt, el_nxt);
-        int emax = kEZero;
-#pragma unroll
-        for (int p = 0; p < P; ++p) emax = dir == 0 ? max(emax, max(Eb[p], El[p])) : max(emax, max(vb[p].e, vl[p].e));
-        const int A = __reduce_max_sync(0xffffffffu, emax);
-        int x[P], y[P];
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            if (dir == 0) {  // alpha rows: before the emission
-                x[p] = fix_log2(Sb[p], Eb[p], A);
-                y[p] = fix_log2(Sl[p], El[p], A);
-            } else {
-                x[p] = fix_log2(vl[p].m, vl[p].e, A);
-                y[p] = fix_log2(vb[p].m, vb[p].e, A);
-            }
-        }
-        store_row(x, y, A);
-        issue(i + kRing - 1);
-    }
-
-    if (dir == 0) {
-        // the paths end in the last blank (pair U) or the last label (pair U-1)
-        XP* fin = reinterpret_cast<XP*>(g.fin);
-        if (g.tid == 0) {
-            fin[0] = XP{0.0f, kEZero};
-            fin[1] = XP{0.0f, kEZero};
-        }
-        group_sync<CTA>();
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const int j = j0 + p;
-            if (j == U) fin[0] = vb[p];
-            if (U >= 1 && j == U - 1) fin[1] = vl[p];
-        }
-        bool any_nan;
-        if constexpr (CTA) {
-            any_nan = __syncthreads_or(saw_nan);
-        } else {
-            any_nan = __any_sync(0xffffffffu, saw_nan);
-            __syncwarp();
-        }
-        if (g.tid == 0) {
-            const XP f0 = fin[0], f1 = fin[1];
-            double v;
-            if (any_nan) {
-                v = __longlong_as_double(0x7ff8000000000000ll);
-            } else if (f0.m == 0.0f && f1.m == 0.0f) {
-                v = __longlong_as_double(0x7ff0000000000000ll);  // no path: +inf
-            } else {
-                const int Em = max(f0.e, f1.e);
-                const double s = (double)f0.m * exp2((double)(max(f0.e - Em, -1100))) +
-                                 (double)f1.m * exp2((double)(max(f1.e - Em, -1100)));
-                v = -((double)Em + log2(s)) * kLn2D;
-            }
-            nll_out[b] = v;
-            if (a.reduction == CTC_PACKED_NONE) {
-                float out = (float)v;
-                if (a.zero_infinity && isinf(v)) out = 0.0f;
-                a.loss[b] = out;
-            }
-        }
-    }
-    cp_async_wait<0>();
-    group_sync<CTA>();
-}
-
-// A multi-warp chain item, split by role.  Consumer warps (the first nwc)
-// hold the state pairs and run the recursion; producer warps gather each
-// frame's label and blank words kRawFrames-1 frames ahead with cp.async
-// (a raw ring), turn them into extended-range emissions one frame ahead of
-// use (a converted ring) and leave the consumers nothing but the
-// recursion, the halo exchange and the stores.  One CTA barrier per frame
-// orders both rings.
-constexpr int kRawFrames = 16;
-constexpr int kConvFrames = 2;
-
-template <int P, int DT>
-__device__ void run_chain_item_split(const ChainArgs& a, int item, int nwc, unsigned char* smem) {
-    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
-    const UttInfo info = ws_at<UttInfo>(a.ws, a.L.off_utt)[item >> 1];
-    double* nll_out = ws_at<double>(a.ws, a.L.off_nll);
-    const int b = item >> 1;
-    const int dir = item & 1;  // 0 alpha, 1 beta
-    const int T = info.T, U = info.U;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int NC = 32 * nwc;                 // consumer threads
-    const int NP = (int)blockDim.x - NC;     // producer threads
-    const bool consumer = tid < NC;
-    const int ptid = tid - NC;
-    const int32_t* tg = a.targets + info.toff;
-    constexpr int E = Elem<DT>::bytes;
-    const int W = a.L.max_U + 1;  // words per frame in the rings: labels 0..U-1, the blank at U
-    uint32_t* raw = reinterpret_cast<uint32_t*>(smem);
-    XP* conv = reinterpret_cast<XP*>(smem + sizeof(uint32_t) * kRawFrames * W);
-    XP* halo = conv + kConvFrames * W;  // [2][nwc]
-    XP* fin = halo + 2 * 32;
-
-    // consumers: labels of the pairs and their skip transitions
+    // my pairs: owned lanes in pair order, shadow lanes at the edge
+    const bool own = DIR == 0 ? lane >= S::G : lane < 32 - S::G;
+    const int j0 = DIR == 0 ? c.w * S::GP + (lane - S::G) * P : c.w * S::GP + lane * P;
     bool has_label[P], skip[P];
+    int wl[P];  // emission-row word of my label state (U + 1: the zero emission)
     bool bad = false;
-    const int j0 = consumer ? tid * P : 0;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
         const int j = j0 + p;
-        has_label[p] = false;
-        skip[p] = false;
-        if (consumer) {
-            if (dir == 0) {  // (blank 2j, label 2j+1 = l_j)
-                has_label[p] = j < U;
-                skip[p] = j >= 1 && j < U && tg[j] != tg[j - 1];
-            } else {  // (label 2j-1 = l_{j-1}, blank 2j)
-                has_label[p] = j >= 1 && j <= U;
-                skip[p] = j >= 1 && j < U && tg[j - 1] != tg[j];
-            }
+        if (DIR == 0) {  // (blank 2j, label 2j+1 = l_j)
+            has_label[p] = j >= 0 && j < U;
+            wl[p] = has_label[p] ? j : U + 1;
+            skip[p] = j >= 1 && j < U && tg[j] != tg[j - 1];
+        } else {  // (label 2j-1 = l_{j-1}, blank 2j)
+            has_label[p] = j >= 1 && j <= U;
+            wl[p] = has_label[p] ? j - 1 : U + 1;
+            skip[p] = j >= 1 && j < U && tg[j - 1] != tg[j];
+        }
+        if (own && has_label[p]) {
+            const int cl = tg[wl[p]];
+            if (cl < 0 || cl >= a.D) bad = true;
         }
     }
-    // producers: the words they gather, and a range check of every label
-    for (int w = consumer ? U + 1 : ptid; w < U; w += NP) {
-        const int c = tg[w];
-        if (c < 0 || c >= a.D) bad = true;
+    if (c.w == 0 && lane == 0) {
+        c.fin[0] = zero;
+        c.fin[1] = zero;
     }
-    bad = __syncthreads_or(bad);
+    bad = multi ? bar_named_or(1, nthreads, bad) : __any_sync(0xffffffffu, bad);
     if (bad) {
-        if (tid == 0) {
+        if (DIR == 0 && c.w == 0 && lane == 0) {
             set_status(ctrl, CTC_PACKED_DEV_LABEL_OUT_OF_RANGE);
-            if (dir == 0) {
-                nll_out[b] = __longlong_as_double(0x7ff8000000000000ll);
-                if (a.reduction == CTC_PACKED_NONE) a.loss[b] = __int_as_float(0x7fc00000);
-            }
+            nll_out[b] = __longlong_as_double(0x7ff8000000000000ll);
+            if (a.reduction == CTC_PACKED_NONE) a.loss[b] = __int_as_float(0x7fc00000);
         }
-        __syncthreads();
         return;
     }
 
-    // producer streams: frame k is row start + k (alpha) or start + T - 1 - k (beta).  A
-    // producer thread owns the words w = ptid and ptid + NP (at most two; the blank is word U)
-    const uintptr_t buf_lo = reinterpret_cast<uintptr_t>(a.lp);
-    const uintptr_t buf_hi = buf_lo + (uintptr_t)a.lp_bytes;
-    const int64_t row0 = dir == 0 ? (int64_t)info.start : (int64_t)info.start + T - 1;
-    const intptr_t step_bytes = (dir == 0 ? 1 : -1) * (intptr_t)a.D * E;
-    const int d_odd = (E == 2) ? (a.D & 1) : 0;
-    const uint32_t raw_s = smem_addr(raw);
-    bool saw_nan = false;
-    bool own[2];
-    uintptr_t gfirst[2], gnext[2];
-    int half0[2];
+    // emission stream: frame k is row start + k (alpha) or start + T - 1 - k
+    // (beta); the matrix has kEmPad >= R rows of padding at both ends, so
+    // frames up to R - 1 past the utterance are read without a check
+    const XP* em = ws_at<XP>(a.ws, em_base(a.L));
+    const int64_t row0 = DIR == 0 ? (int64_t)info.start : (int64_t)info.start + T - 1;
+    const int64_t estep = DIR == 0 ? (int64_t)a.L.epitch : -(int64_t)a.L.epitch;
+    const XP* gsrc[P + 1];  // next frame's sources: my labels, then the blank
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const int w = ptid + q * NP;
-        own[q] = !consumer && w <= U;
-        const int c = own[q] ? (w < U ? tg[w] : a.blank) : a.blank;
-        gfirst[q] = gnext[q] = buf_lo + (uintptr_t)((row0 * a.D + c) * E);
-        half0[q] = (int)((gfirst[q] >> 1) & 1);
-    }
-    auto issue_raw = [&](int k) {
-        if (!consumer) {
-            const bool live = k < T;
-            const uint32_t slot = raw_s + (uint32_t)((k & (kRawFrames - 1)) * W) * 4u;
+    for (int p = 0; p < P; ++p) gsrc[p] = em + row0 * a.L.epitch + wl[p];
+    gsrc[P] = em + row0 * a.L.epitch + U;
+    // ring slot of frame k: (k - 1) mod R; lane l's entries are LW consecutive values
+    const uint32_t ring_lane = smem_addr(c.ring) + (uint32_t)(lane * S::LW) * 8u;
+    constexpr uint32_t kSlotBytes = 32u * S::LW * 8u;
+    auto request = [&](uint32_t slot) {  // the next frame into ring slot `slot`
+        const uint32_t dst = ring_lane + slot * kSlotBytes;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                if (own[q]) gather<DT>(slot + (uint32_t)(ptid + q * NP) * 4u, live ? gnext[q] : gfirst[q], buf_hi, live);
-                gnext[q] += live ? step_bytes : 0;
-            }
-            cp_async_commit();
+        for (int p = 0; p <= P; ++p) {
+            cp_async8(dst + 8u * p, gsrc[p]);
+            gsrc[p] += estep;
         }
+        cp_async_commit();
     };
-    auto convert = [&](int k) {  // raw frame k -> converted ring
-        if (!consumer && k < T) {
-            const uint32_t* rs = raw + (k & (kRawFrames - 1)) * W;
-            XP* cs = conv + (k % kConvFrames) * W;
-            const int flip = d_odd & k;
+    auto emissions = [&](uint32_t slot, XP (&el)[P], XP& eb) {
+        const XP* e = reinterpret_cast<const XP*>(c.ring) + slot * 32 * S::LW + lane * S::LW;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                if (own[q]) {
-                    const int w = ptid + q * NP;
-                    const float x = word_to_float<DT>(rs[w], half0[q] ^ flip);
-                    saw_nan |= x != x;
-                    cs[w] = xp_from_log(x);
-                }
-            }
-        }
+        for (int p = 0; p < P; ++p) el[p] = e[p];
+        eb = e[P];
     };
 
-    const bool store_me = consumer && j0 <= U;
-    int* st = ws_at<int>(a.ws, dir == 0 ? a.L.off_alpha : a.L.off_beta) + row0 * a.L.pitch + 2 * j0;
-    const intptr_t st_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.pitch;
-    int32_t* offp = ws_at<int32_t>(a.ws, dir == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo + warp;
-    const intptr_t off_step = (dir == 0 ? 1 : -1) * (intptr_t)a.L.nwo;
-    auto store_row = [&](const int (&x)[P], const int (&y)[P], int A) {
+    // stored rows, written one frame late
+    const bool store_me = own && j0 <= U;
+    int* st = ws_at<int>(a.ws, DIR == 0 ? a.L.off_alpha : a.L.off_beta) + row0 * a.L.pitch + 2 * max(j0, 0);
+    const intptr_t st_step = (DIR == 0 ? 1 : -1) * (intptr_t)a.L.pitch;
+    int32_t* offp = ws_at<int32_t>(a.ws, DIR == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo + c.w;
+    const intptr_t off_step = (DIR == 0 ? 1 : -1) * (intptr_t)a.L.nwo;
+    // alpha rows: (blank, label) sums before the emission; beta: (label, blank) after it
+    float rx[P], ry[P];
+    int ex[P], ey[P];
+    auto flush_row = [&]() {
+        int emax = kEZero;
+#pragma unroll
+        for (int p = 0; p < P; ++p) emax = max(emax, max(ex[p], ey[p]));
+        const int A = __reduce_max_sync(0xffffffffu, own ? emax : kEZero);
+        int x[P], y[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            x[p] = enc_state(rx[p], ex[p], A);
+            y[p] = enc_state(ry[p], ey[p], A);
+        }
         if (store_me) {
             if constexpr (P == 1) {
                 *reinterpret_cast<int2*>(st) = make_int2(x[0], y[0]);
@@ -507,149 +215,158 @@ __device__ void run_chain_item_split(const ChainArgs& a, int item, int nwc, unsi
         st += st_step;
         offp += off_step;
     };
-    const XP zero{0.0f, kEZero};
-    // emissions of frame k for my pairs, from the converted ring
-    auto emissions = [&](int k, XP& eb, XP (&el)[P]) {
-        const XP* cs = conv + (k % kConvFrames) * W;
-        eb = cs[U];
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const int j = j0 + p;
-            const int w = dir == 0 ? j : j - 1;
-            el[p] = has_label[p] ? cs[w] : zero;
-        }
-    };
 
-    // prologue: raw frames 0 .. kRawFrames-2 in flight, frames 0 .. kConvFrames-2 converted
-#pragma unroll 1
-    for (int k = 0; k < kRawFrames - 1; ++k) issue_raw(k);
-    if (!consumer) {
-        cp_async_wait<kRawFrames - kConvFrames>();
-        for (int k = 0; k < kConvFrames - 1; ++k) convert(k);
-    }
-
-    XP vb[P], vl[P];
-#pragma unroll 1
-    for (int i = 0; i < T; ++i) {
-        __syncthreads();
-        if (!consumer) {
-            // producers: frame i + kConvFrames - 1 into the converted ring, frame i + kRawFrames - 1 requested
-            cp_async_wait<kRawFrames - kConvFrames - 1>();
-            convert(i + kConvFrames - 1);
-            issue_raw(i + kRawFrames - 1);
-            continue;
-        }
-        XP eb, el[P];
-        emissions(i, eb, el);
-        if (i == 0) {
-            int x[P], y[P];
-            int emax = kEZero;
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const int j = j0 + p;
-                if (dir == 0) {
-                    vb[p] = j == 0 ? eb : zero;
-                    vl[p] = (j == 0 && U >= 1) ? el[p] : zero;
-                } else {
-                    vb[p] = j == U ? eb : zero;
-                    vl[p] = (j == U && U >= 1) ? el[p] : zero;
-                }
-                vb[p] = xp_norm(vb[p].m, vb[p].e);
-                vl[p] = xp_norm(vl[p].m, vl[p].e);
-                emax = max(emax, max(vb[p].e, vl[p].e));
-            }
-            if (dir == 0 && lane == 31) halo[warp] = vl[P - 1];
-            if (dir == 1 && lane == 0) halo[warp] = vl[0];
-            const int A = dir == 0 ? 0 : __reduce_max_sync(0xffffffffu, emax);
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const int j = j0 + p;
-                if (dir == 0) {
-                    x[p] = j == 0 ? 0 : kFixZero;
-                    y[p] = (j == 0 && U >= 1) ? 0 : kFixZero;
-                } else {
-                    x[p] = fix_log2(vl[p].m, vl[p].e, A);
-                    y[p] = fix_log2(vb[p].m, vb[p].e, A);
-                }
-            }
-            store_row(x, y, A);
-            continue;
-        }
-        // the label state just below (alpha) or above (beta) my pairs, previous frame
+    XP vb[P], vl[P];  // alpha (blank 2j, label 2j+1) / beta (label 2j-1, blank 2j)
+    // one recursion step with this frame's emissions.  The shuffle hands lane 0
+    // (alpha) / lane 31 (beta) its own state: those lanes shadow pairs that
+    // are either outside the target (zero, and zero feeds zero) or
+    // overwritten at the next exchange.
+    auto step = [&](const XP (&el)[P], const XP& eb) {
         XP nb;
         {
-            const int src = dir == 0 ? max(warp - 1, 0) : min(warp + 1, nwc - 1);
-            const XP h = halo[((i - 1) & 1) * nwc + src];
-            const bool edge = dir == 0 ? (lane == 0) : (lane == 31);
-            const bool has_nb = dir == 0 ? warp > 0 : warp < nwc - 1;
-            const XP mine = dir == 0 ? vl[P - 1] : vl[0];
-            nb.m = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.m, 1) : __shfl_down_sync(0xffffffffu, mine.m, 1);
-            nb.e = dir == 0 ? __shfl_up_sync(0xffffffffu, mine.e, 1) : __shfl_down_sync(0xffffffffu, mine.e, 1);
-            if (edge) nb = has_nb ? h : zero;
+            const XP mine = DIR == 0 ? vl[P - 1] : vl[0];
+            nb.m = DIR == 0 ? __shfl_up_sync(0xffffffffu, mine.m, 1) : __shfl_down_sync(0xffffffffu, mine.m, 1);
+            nb.e = DIR == 0 ? __shfl_up_sync(0xffffffffu, mine.e, 1) : __shfl_down_sync(0xffffffffu, mine.e, 1);
         }
         float Sb[P], Sl[P];
         int Eb[P], El[P];
-        if (dir == 0) {
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const XP prev = p ? vl[p - 1] : nb;
-                xp_sum3(vl[p], vb[p], skip[p] ? prev : zero, Sl[p], El[p]);
-                xp_sum2(vb[p], prev, Sb[p], Eb[p]);
-            }
-        } else {
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const XP next = (p < P - 1) ? vl[p + 1] : nb;
-                xp_sum3(vl[p], vb[p], skip[p] ? next : zero, Sl[p], El[p]);
-                xp_sum2(vb[p], next, Sb[p], Eb[p]);
-            }
+        for (int p = 0; p < P; ++p) {
+            const XP o = DIR == 0 ? (p ? vl[p - 1] : nb) : (p < P - 1 ? vl[p + 1] : nb);
+            xp_sum3(vl[p], vb[p], skip[p] ? o : zero, Sl[p], El[p]);
+            xp_sum2(vb[p], o, Sb[p], Eb[p]);
         }
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            vl[p] = xp_norm(Sl[p] * el[p].m, El[p] + el[p].e);
-            vb[p] = xp_norm(Sb[p] * eb.m, Eb[p] + eb.e);
-        }
-        if (dir == 0 && lane == 31) halo[(i & 1) * nwc + warp] = vl[P - 1];
-        if (dir == 1 && lane == 0) halo[(i & 1) * nwc + warp] = vl[0];
-        int emax = kEZero;
-#pragma unroll
-        for (int p = 0; p < P; ++p) emax = dir == 0 ? max(emax, max(Eb[p], El[p])) : max(emax, max(vb[p].e, vl[p].e));
-        const int A = __reduce_max_sync(0xffffffffu, emax);
-        int x[P], y[P];
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            if (dir == 0) {  // alpha rows: before the emission
-                x[p] = fix_log2(Sb[p], Eb[p], A);
-                y[p] = fix_log2(Sl[p], El[p], A);
+            vl[p] = XP{Sl[p] * el[p].m, El[p] + el[p].e};
+            vb[p] = XP{Sb[p] * eb.m, Eb[p] + eb.e};
+            if (DIR == 0) {
+                rx[p] = Sb[p];
+                ex[p] = Eb[p];
+                ry[p] = Sl[p];
+                ey[p] = El[p];
             } else {
-                x[p] = fix_log2(vl[p].m, vl[p].e, A);
-                y[p] = fix_log2(vb[p].m, vb[p].e, A);
+                rx[p] = vl[p].m;
+                ex[p] = vl[p].e;
+                ry[p] = vb[p].m;
+                ey[p] = vb[p].e;
             }
         }
-        store_row(x, y, A);
+    };
+    auto renormalise = [&]() {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            vb[p] = xp_norm(vb[p].m, vb[p].e);
+            vl[p] = xp_norm(vl[p].m, vl[p].e);
+        }
+    };
+    // halo exchange e: alpha sends its top shadowed lanes up, beta its bottom ones down
+    auto exchange = [&](int e) {
+        XP* buf = c.xch + (e & 1) * (c.nw * S::XW);
+        const int qs = DIR == 0 ? lane - (32 - S::G) : lane;
+        if (qs >= 0 && qs < S::G) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                buf[c.w * S::XW + (qs * P + p) * 2] = vb[p];
+                buf[c.w * S::XW + (qs * P + p) * 2 + 1] = vl[p];
+            }
+        }
+        bar_named(1, nthreads);
+        const int src = DIR == 0 ? c.w - 1 : c.w + 1;
+        const int qr = DIR == 0 ? lane : lane - (32 - S::G);
+        if (src >= 0 && src < c.nw && qr >= 0 && qr < S::G) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                vb[p] = buf[src * S::XW + (qr * P + p) * 2];
+                vl[p] = buf[src * S::XW + (qr * P + p) * 2 + 1];
+            }
+        }
+    };
+
+    // prologue: frames 0 .. R-2 requested (frame k into slot (k - 1) mod R)
+#pragma unroll
+    for (int k = 0; k < S::R - 1; ++k) request((uint32_t)((k + S::R - 1) & (S::R - 1)));
+
+    // frame 0
+    {
+        cp_async_wait<S::R - 2>();
+        XP el[P], eb;
+        emissions(S::R - 1, el, eb);
+        request(S::R - 2);  // frame R - 1
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int j = j0 + p;
+            if (DIR == 0) {
+                vb[p] = j == 0 ? xp_norm(eb.m, eb.e) : zero;
+                vl[p] = (j == 0 && U >= 1) ? xp_norm(el[p].m, el[p].e) : zero;
+                // before the first emission the start states hold 1
+                rx[p] = j == 0 ? 1.0f : 0.0f;
+                ex[p] = j == 0 ? 0 : kEZero;
+                ry[p] = (j == 0 && U >= 1) ? 1.0f : 0.0f;
+                ey[p] = (j == 0 && U >= 1) ? 0 : kEZero;
+            } else {
+                vb[p] = j == U ? xp_norm(eb.m, eb.e) : zero;
+                vl[p] = (j == U && U >= 1) ? xp_norm(el[p].m, el[p].e) : zero;
+                rx[p] = vl[p].m;
+                ex[p] = vl[p].e;
+                ry[p] = vb[p].m;
+                ey[p] = vb[p].e;
+            }
+        }
     }
 
-    const bool any_nan = __syncthreads_or(saw_nan);
-    if (dir == 0) {
-        // the paths end in the last blank (pair U) or the last label (pair U-1)
-        if (tid == 0) {
-            fin[0] = zero;
-            fin[1] = zero;
+    // full blocks: frames i0 .. i0+3, i0 = 1 mod 4, in slots base .. base+3;
+    // the request made at frame i goes to frame i-1's slot
+    int i0 = 1;
+#pragma unroll 1
+    for (; i0 + S::F - 1 < T; i0 += S::F) {
+        const uint32_t base = (uint32_t)((i0 - 1) & (S::R - 1));
+#pragma unroll
+        for (int q = 0; q < S::F; ++q) {
+            cp_async_wait<S::R - 2>();
+            XP el[P], eb;
+            emissions(base + q, el, eb);
+            request((base + q + S::R - 1) & (S::R - 1));
+            flush_row();  // frame i0 + q - 1
+            step(el, eb);
         }
-        __syncthreads();
-        if (consumer) {
+        renormalise();
+        if (multi) exchange((i0 - 1) / S::F);
+    }
+    // the last frames (fewer than 4: no exchange needed)
+#pragma unroll 1
+    for (int i = i0; i < T; ++i) {
+        cp_async_wait<S::R - 2>();
+        XP el[P], eb;
+        const uint32_t slot = (uint32_t)((i - 1) & (S::R - 1));
+        emissions(slot, el, eb);
+        request((slot + S::R - 1) & (S::R - 1));
+        flush_row();
+        step(el, eb);
+    }
+    flush_row();  // frame T - 1 (T >= 1 for every queued item)
+    cp_async_wait<0>();
+    renormalise();
+
+    if (DIR == 0) {
+        // the paths end in the last blank (pair U) or the last label (pair U-1)
+        if (own) {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 const int j = j0 + p;
-                if (j == U) fin[0] = vb[p];
-                if (U >= 1 && j == U - 1) fin[1] = vl[p];
+                if (j == U) c.fin[0] = vb[p];
+                if (U >= 1 && j == U - 1) c.fin[1] = vl[p];
             }
         }
-        __syncthreads();
-        if (tid == 0) {
-            const XP f0 = fin[0], f1 = fin[1];
+        if (multi) {
+            bar_named(1, nthreads);
+        } else {
+            __syncwarp();
+        }
+        if (c.w == 0 && lane == 0) {
+            const XP f0 = c.fin[0], f1 = c.fin[1];
             double v;
-            if (any_nan) {
+            if (info.has_nan) {
                 v = __longlong_as_double(0x7ff8000000000000ll);
             } else if (f0.m == 0.0f && f1.m == 0.0f) {
                 v = __longlong_as_double(0x7ff0000000000000ll);  // no path: +inf
@@ -667,8 +384,15 @@ __device__ void run_chain_item_split(const ChainArgs& a, int item, int nwc, unsi
             }
         }
     }
-    cp_async_wait<0>();
-    __syncthreads();
+}
+
+template <int P>
+__device__ __forceinline__ void run_item(const ChainArgs& a, int item, const ItemCtx& c) {
+    if (item & 1) {
+        run_chain<P, 1>(a, item >> 1, c);
+    } else {
+        run_chain<P, 0>(a, item >> 1, c);
+    }
 }
 
 // Label metadata the backward needs, one warp per utterance: for each target
@@ -726,22 +450,25 @@ __device__ void run_label_item(const ChainArgs& a, int b, int lane) {
     }
 }
 
+
 }  // namespace
 
-template <int P, int DT>
+template <int P>
 __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
+    using S = ChainShape<P>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_item;
     __shared__ int s_last;
     __shared__ double s_red[32];
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const int32_t* queue = ws_at<int32_t>(a.ws, a.L.off_queue);
+    const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
     const int NT = blockDim.x, NW = NT >> 5;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint32_t* ring = reinterpret_cast<uint32_t*>(smem_raw);
-    const int ring_words = kRing * (NT * P + NW);
-    float* halo = reinterpret_cast<float*>(ring + ring_words);
-    float* fin = halo + 4 * NW;  // 2 extended values per warp
+    XP* rings = reinterpret_cast<XP*>(smem_raw);
+    XP* xch = rings + NW * S::R * 32 * S::LW;
+    XP* fins = xch + 2 * NW * S::XW;
+    XP* my_ring = rings + warp * S::R * 32 * S::LW;
     const int n_big = ctrl->n_big, n_small = ctrl->n_small, n_lab = ctrl->n_lab;
 
     // 1. multi-warp chains, longest first, one at a time per CTA
@@ -751,21 +478,18 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
         const int k = s_item;
         __syncthreads();
         if (k >= n_big) break;
-        if (P == 1 && a.consumer_warps < NW) {
-            run_chain_item_split<P, DT>(a, queue[k], a.consumer_warps, smem_raw);
-        } else {  // every warp holds pairs and gathers its own columns
-            Group cg{tid, NT, warp, NW, ring, halo, fin};
-            run_chain_item<P, DT, true>(a, queue[k], cg);
-        }
+        const int item = queue[k];
+        const int U = utt[item >> 1].U;
+        const int nw = min(NW, (U + 1 + S::GP - 1) / S::GP);
+        if (warp < nw) run_item<P>(a, item, ItemCtx{warp, nw, my_ring, xch, fins});
     }
     // 2. single-warp chains, each warp on its own
-    Group wg{lane, 32, warp, NW, ring + warp * kRing * (32 * P + 1), halo, fin + 4 * warp};
     for (;;) {
         int k = 0;
         if (lane == 0) k = (int)atomicAdd(&ctrl->small_head, 1u);
         k = __shfl_sync(0xffffffffu, k, 0);
         if (k >= n_small) break;
-        run_chain_item<P, DT, false>(a, queue[n_big + k], wg);
+        run_item<P>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp});
     }
     // 3. label metadata for the backward
     for (;;) {
@@ -806,78 +530,43 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
     }
 }
 
-#define CTCP_INSTANTIATE_CHAIN(P, DT) template __global__ void chain_kernel<P, DT>(ChainArgs);
-CTCP_INSTANTIATE_CHAIN(1, 0)
-CTCP_INSTANTIATE_CHAIN(1, 1)
-CTCP_INSTANTIATE_CHAIN(1, 2)
-CTCP_INSTANTIATE_CHAIN(2, 0)
-CTCP_INSTANTIATE_CHAIN(2, 1)
-CTCP_INSTANTIATE_CHAIN(2, 2)
-CTCP_INSTANTIATE_CHAIN(4, 0)
-CTCP_INSTANTIATE_CHAIN(4, 1)
-CTCP_INSTANTIATE_CHAIN(4, 2)
+template __global__ void chain_kernel<1>(ChainArgs);
+template __global__ void chain_kernel<2>(ChainArgs);
+template __global__ void chain_kernel<4>(ChainArgs);
 
-int chain_pairs_per_thread(int max_target_len) { return pairs_for_max_u(max_target_len); }
-
-int chain_warps(int max_target_len, int P) {
-    const int pairs = max_target_len + 1;
-    int nw = (pairs + 32 * P - 1) / (32 * P);
-    return nw < 1 ? 1 : (nw > 30 ? 30 : nw);
-}
-
-static size_t chain_smem_bytes(int P, int nw, int max_u) {
-    const int nt = 32 * nw;
-    const size_t warp_mode = sizeof(uint32_t) * (size_t)kRing * (nt * P + nw) + sizeof(float) * (size_t)(4 * nw + 4 * nw);
-    const size_t W = (size_t)max_u + 1;
-    const size_t split = P == 1 ? sizeof(uint32_t) * kRawFrames * W + sizeof(XP) * (kConvFrames * W + 2 * 32 + 2) : 0;
-    return warp_mode > split ? warp_mode : split;
-}
-
-// Producer warps a chain CTA gets: enough that each producer thread owns at
-// most two of the max_U + 1 columns, when consumers and producers fit 32 warps.
-static int producer_warps(int P, int nwc, int max_u) {
-    if (P != 1) return 0;
-    const int nwp = (max_u + 1 + 63) / 64;
-    return nwc + nwp <= 32 ? nwp : 0;
-}
-
-template <int P, int DT>
-static cudaError_t launch_chain_t(const ChainArgs& a0, int nwc, cudaStream_t s) {
-    ChainArgs a = a0;
-    a.consumer_warps = nwc;
-    const int nw = nwc + producer_warps(P, nwc, a.L.max_U);
+template <int P>
+static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
+    using S = ChainShape<P>;
+    const int nw = a.L.nwo;  // warps for the longest possible target
+    const size_t smem = sizeof(XP) * ((size_t)nw * S::R * 32 * S::LW + 2 * (size_t)nw * S::XW + 2 * (size_t)nw);
     static int configured_smem = -1;
-    const size_t smem = chain_smem_bytes(P, nw, a.L.max_U);
     cudaError_t e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((int)smem > configured_smem) {
-        e = cudaFuncSetAttribute(chain_kernel<P, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(chain_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured_smem = (int)smem;
     }
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P, DT>, 32 * nw, smem)) !=
-        cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P>, 32 * nw, smem)) != cudaSuccess)
         return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     // persistent grid: enough CTAs for every item, never more than fit at once
     long long want = 2ll * a.L.B;
     long long grid = (long long)sms * per_sm;
     if (want < grid) grid = want > 0 ? want : 1;
-    chain_kernel<P, DT><<<(unsigned)grid, 32 * nw, smem, s>>>(a);
+    chain_kernel<P><<<(unsigned)grid, 32 * nw, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_chain(const ChainArgs& a, int P, int nw, int dtype, cudaStream_t s) {
-#define CTCP_CASE(PP, DD) \
-    if (P == PP && dtype == DD) return launch_chain_t<PP, DD>(a, nw, s);
-    CTCP_CASE(1, 0) CTCP_CASE(1, 1) CTCP_CASE(1, 2)
-    CTCP_CASE(2, 0) CTCP_CASE(2, 1) CTCP_CASE(2, 2)
-    CTCP_CASE(4, 0) CTCP_CASE(4, 1) CTCP_CASE(4, 2)
-#undef CTCP_CASE
-    return cudaErrorInvalidValue;
+cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s) {
+    switch (pairs_for_max_u(a.L.max_U)) {
+        case 1: return launch_chain_t<1>(a, s);
+        case 2: return launch_chain_t<2>(a, s);
+        default: return launch_chain_t<4>(a, s);
+    }
 }
 
 }  // namespace ctcp

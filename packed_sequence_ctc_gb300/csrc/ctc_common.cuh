@@ -1,12 +1,6 @@
-// Shared definitions of the packed CTC kernels: workspace layout, log-space
-// arithmetic in base 2, element conversions and the async-copy primitives.
-//
-// Log-space state is in natural-log units, so a log probability is added
-// exactly as the caller gave it; the hardware base-2 ex2/lg2 approximations
-// only ever see small scaled differences.  "log 0" is the finite stand-in
-// kNeg = -1e30: adding any realistic value to it leaves it unchanged (its ulp
-// is ~7e22), so unreachable states stay unreachable without special cases,
-// and a difference of two such values is 0 rather than NaN.
+// Shared definitions of the packed CTC kernels: workspace layout, the
+// extended-range probability arithmetic of the recursions, the stored state
+// encoding, element conversions and the async-copy primitives.
 #pragma once
 
 #include <cstddef>
@@ -20,15 +14,12 @@
 
 namespace ctcp {
 
-constexpr int kRing = 16;             // frames of label columns kept in flight per chain
-constexpr float kNeg = -1.0e30f;      // log of zero probability
-constexpr float kNegHalf = -5.0e29f;  // anything below is "zero probability"
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr double kLog2eD = 1.4426950408889634074;
 constexpr double kLn2D = 0.69314718055994530942;
 constexpr int kMaxD = 16384;          // one gradient row must fit a shared-memory tile
-constexpr int kMaxTargetLen = 3839;   // 4 state pairs per thread x 30 warps of a chain CTA
+constexpr int kMaxTargetLen = 3839;   // 4 state pairs per lane, 31 own lanes in each of 32 warps
 constexpr long long kSpinLimit = 1ll << 26;  // bounded waits give up after this many polls
 
 // Control block at the start of the workspace.
@@ -54,26 +45,39 @@ struct UttInfo {
     int32_t valid;      // metadata well formed
     int32_t labels_ok;  // every target id in [0, D) (set by the label analysis)
     int32_t n_owners;   // distinct non-blank target classes + 1 (the blank group)
+    int32_t has_nan;    // a label or blank log probability of the utterance is NaN (set by the emission gather)
 };
 
 // Byte offsets of every array inside the caller's workspace.
 struct Layout {
     int64_t T_total;
-    int32_t B, max_U, D, pitch;  // pitch: floats per stored state row (>= 2 * (max_U + 1))
+    int32_t B, max_U, D, pitch;  // pitch: ints per stored state row (>= 2 * (max_U + 1))
     int32_t ecap;                // distinct classes a target can have: min(max_U + 1, D)
-    int32_t nwo;                 // per-frame offsets stored per chain row (one per warp of a chain CTA)
+    int32_t gpairs;              // state pairs a chain warp owns (its offset group)
+    int32_t nwo;                 // per-frame offsets stored per chain row (one per offset group)
+    int32_t epitch;              // extended emissions per row of the emission matrix (>= max_U + 2, even)
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
-    size_t off_nxt, off_rank, off_owner, total;
+    size_t off_nxt, off_rank, off_owner, off_em, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// State pairs (blank, label) each thread of a chain holds, from the target bound.
+// Rows of padding before and after the emission matrix: a chain prefetches
+// up to this many frames past either end of its utterance without a bounds
+// check (those rows are never consumed).
+constexpr int kEmPad = 8;
+
+// State pairs (blank, label) each lane of a chain warp holds, from the target
+// bound; a warp owns (32 - ghost lanes) * P pairs and at most 32 warps run a chain.
 __host__ __device__ inline int pairs_for_max_u(int max_u) {
     const int pairs = max_u + 1;
-    return pairs <= 960 ? 1 : pairs <= 1920 ? 2 : 4;  // at most 30 warps hold the pairs
+    return pairs <= 28 * 32 ? 1 : pairs <= 30 * 2 * 32 ? 2 : 4;
 }
+// Lanes of a chain warp that shadow the neighbouring warp's edge pairs, so
+// the warp runs ghost_lanes(P) * P frames between two halo exchanges.
+__host__ __device__ constexpr int ghost_lanes(int P) { return P == 1 ? 4 : P == 2 ? 2 : 1; }
+__host__ __device__ constexpr int group_pairs(int P) { return (32 - ghost_lanes(P)) * P; }
 
 __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_t max_U, int32_t D) {
     Layout L{};
@@ -81,16 +85,18 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.B = B;
     L.max_U = max_U;
     L.D = D;
-    // a row holds 2 floats per state pair; a thread stores its P pairs as one
-    // aligned vector, so the pitch is a multiple of 2P floats (and of 4)
+    // a row holds 2 ints per state pair; a lane stores its P pairs as one
+    // aligned vector, so the pitch is a multiple of 2P ints (and of 4)
     const int P = pairs_for_max_u(max_U);
     L.pitch = (int32_t)align_up((size_t)(2 * (max_U + 1)), (size_t)(2 * P > 4 ? 2 * P : 4));
     L.ecap = (max_U + 1) < D ? (max_U + 1) : D;
+    L.gpairs = group_pairs(P);
     {
         const int pairs = max_U + 1;
-        const int nw = (pairs + 32 * P - 1) / (32 * P);
-        L.nwo = nw < 1 ? 1 : (nw > 30 ? 30 : nw);
+        const int nw = (pairs + L.gpairs - 1) / L.gpairs;
+        L.nwo = nw < 1 ? 1 : nw;
     }
+    L.epitch = (int32_t)align_up((size_t)(max_U + 2), 2);  // labels, the blank, a zero emission
     L.lab_cap = (int64_t)B * max_U + B;
     size_t o = 0;
     L.off_ctrl = o;   o = align_up(o + sizeof(Control), 256);
@@ -104,6 +110,7 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_nxt = o;    o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_rank = o;   o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_owner = o;  o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
+    L.off_em = o;     o = align_up(o + 8 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
     L.total = o;
     return L;
 }
@@ -116,6 +123,8 @@ template <typename T>
 __host__ __device__ inline const T* ws_at(const void* ws, size_t off) {
     return reinterpret_cast<const T*>(static_cast<const unsigned char*>(ws) + off);
 }
+// Row 0 of the emission matrix (after its leading padding).
+__host__ __device__ inline size_t em_base(const Layout& L) { return L.off_em + 8 * (size_t)kEmPad * (size_t)L.epitch; }
 
 // Element types: 0 float32, 1 bfloat16, 2 float16.
 template <int DT>
@@ -130,30 +139,6 @@ __device__ __forceinline__ float fast_ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float fast_lg2(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-// Maximum that propagates NaN (so a NaN input poisons the recursion).
-__device__ __forceinline__ float max_nan(float a, float b) {
-    float y;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
-    return y;
-}
-// log2(2^a + 2^b)
-__device__ __forceinline__ float lse2(float a, float b) {
-    float m = max_nan(a, b);
-    float n = fminf(a, b);
-    return m + fast_lg2(1.0f + fast_ex2(n - m));
-}
-// log2(2^a + 2^b + 2^c)
-__device__ __forceinline__ float lse3(float a, float b, float c) {
-    float hi = max_nan(a, b), lo = fminf(a, b);
-    float m = max_nan(hi, c), mid = fminf(hi, c);
-    return m + fast_lg2(1.0f + fast_ex2(lo - m) + fast_ex2(mid - m));
-}
-
 // ------------------------------------------- extended-range probabilities
 //
 // The recursions run on probabilities, not logs: a state is m * 2^e with a
@@ -168,7 +153,9 @@ __device__ __forceinline__ float lse3(float a, float b, float c) {
 // bias of the fast log2 near 1 on every step: ~2e-5 on the posteriors of a
 // 2000-frame utterance.)
 
-constexpr int kEZero = -(1 << 29);  // exponent of an unreachable state (m = 0)
+constexpr int kEZero = -(1 << 29);    // exponent of an unreachable state (m = 0)
+constexpr int kEZeroEm = -(1 << 24);  // exponent of a zero emission: a recursion adds emission
+                                      // exponents over a few frames between renormalisations
 constexpr float kL2eHi = 1.4426950216293335f;     // float(log2 e)
 constexpr float kL2eLo = 1.9259629911783890e-8f;  // log2 e - kL2eHi
 
@@ -185,10 +172,10 @@ __device__ __forceinline__ XP xp_from_log(float lp) {
     const float fl = floorf(yh);
     XP r;
     r.m = fast_ex2((yh - fl) + yl);
-    r.e = (int)fl;
+    r.e = (int)fminf(fl, 16777216.0f);  // log probabilities above 2^24 saturate (no overflow downstream)
     if (!(yh > -3.0e7f)) {  // exp(lp) == 0: lp = -inf, below any representable probability, or NaN
         r.m = 0.0f;         // (callers flag a NaN separately)
-        r.e = kEZero;
+        r.e = kEZeroEm;
     }
     return r;
 }
@@ -217,16 +204,22 @@ __device__ __forceinline__ void xp_sum3(XP a, XP b, XP c, float& S, int& E) {
     S = fmaf(a.m, pow2_nonpos(a.e - E), fmaf(b.m, pow2_nonpos(b.e - E), c.m * pow2_nonpos(c.e - E)));
 }
 
-// Stored form of a state for the backward: log2 of the value relative to an
-// int offset A, as a signed fixed-point int with kFixFrac fraction bits.
-// The range (-4095, +4096) and the uniform 2^-20 resolution hold wherever the
-// state sits relative to A (a float log would lose bits with distance).
+// Stored form of a state for the backward: the value S * 2^(E - A), relative
+// to a per-(frame, warp) integer offset A, as one int32 that holds it
+// exactly up to rounding: the top 13 bits are the signed binary exponent k,
+// the low kFixFrac = 19 bits the mantissa fraction (rounded to nearest), so
+// v = k * 2^19 + frac19 and the value is (1 + frac19 / 2^19) * 2^k.  The int
+// order follows the value order.  Built from the float's own bits (no log):
+// (bits + 8) >> 4 is the float's biased exponent and top 19 mantissa bits,
+// rounded, with a carry moving into the exponent.  S may be any finite
+// non-negative float, normalised or not.  A state more than 2^3800 below the
+// offset is stored as zero (a posterior can only be understated by it).
 constexpr int kFixFrac = 19;
 constexpr int kFixZero = (int)0x80000000;  // probability 0
-__device__ __forceinline__ int fix_log2(float S, int E, int A) {
-    const int k = max(E - A, -4095);
-    const int v = (k << kFixFrac) + __float2int_rn(fast_lg2(S) * (float)(1 << kFixFrac));
-    return S > 0.0f ? v : kFixZero;
+__device__ __forceinline__ int enc_state(float S, int E, int A) {
+    const int d = E - A;
+    const int v = ((__float_as_int(S) + 8) >> 4) + ((d - 127) << kFixFrac);
+    return (S > 0.0f && d >= -3800) ? v : kFixZero;
 }
 
 // ------------------------------------------------------------- conversions

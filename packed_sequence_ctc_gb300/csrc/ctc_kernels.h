@@ -15,7 +15,7 @@ struct PrepArgs {
     int reduction;
     int zero_infinity;
     int need_grad;
-    int pairs_per_thread;
+    int group_pairs;  // pairs one chain warp owns: longer targets run on a whole CTA
 };
 
 struct ChainArgs {
@@ -23,6 +23,7 @@ struct ChainArgs {
     void* ws;
     const void* lp;      // (T_total, D) log probabilities
     int64_t lp_bytes;    // T_total * D * element bytes
+    const int32_t* cu;   // cu_seqlens
     const int32_t* targets;
     const int32_t* target_lengths;
     float* loss;
@@ -30,7 +31,6 @@ struct ChainArgs {
     int blank;
     int reduction;
     int zero_infinity;
-    int consumer_warps;  // warps of a chain CTA that hold state pairs (the rest gather)
 };
 
 struct GradArgs {
@@ -53,7 +53,9 @@ struct GradArgs {
 };
 
 __global__ void prep_kernel(PrepArgs a);
-template <int P, int DT>
+template <int DT>
+__global__ void emit_kernel(ChainArgs a);
+template <int P>
 __global__ void chain_kernel(ChainArgs a);
 template <int DT>
 __global__ void grad_kernel(GradArgs a);
@@ -61,9 +63,8 @@ void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& wa
 
 // Host launchers (defined next to their kernels).
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
-cudaError_t launch_chain(const ChainArgs& a, int pairs_per_thread, int warps, int dtype, cudaStream_t s);
+cudaError_t launch_emit(const ChainArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s);
-int chain_pairs_per_thread(int max_target_len);
-int chain_warps(int max_target_len, int pairs_per_thread);
 
 }  // namespace ctcp

@@ -1,0 +1,130 @@
+// Emission gather of the forward: for every frame of every utterance, the
+// log probabilities of the utterance's target labels and of the blank,
+// lp[t, l_1..l_U] and lp[t, blank], converted once into extended-range
+// probabilities (ctc_common.cuh, XP) and written as one contiguous row of the
+// workspace's emission matrix: em[row][w] for w < U is label l_{w+1}, em[row][U]
+// the blank, em[row][U + 1] a zero emission (read by lanes without a label).
+//
+// Page "feat(asr): native CTC loss kernel over sequence-packed log
+// probabilities", ctc_loss.py ``_alpha_kernel`` and ``_beta_grad_kernel``:
+// both recursions read exactly these columns, lp[t, l'_s], each frame.
+//
+// Why a kernel of its own: the label columns are scattered through rows of
+// D elements, so each read costs a whole DRAM sector.  Gathered inside the
+// serial recursions (one chain per SM, both the alpha and the beta chain of
+// an utterance reading the same columns), they run into the number of reads
+// an SM can keep in flight.  Here every SM gathers with many independent
+// loads per thread, each column once, and the recursions then read short
+// contiguous rows, mostly from L2.
+#include "ctc_common.cuh"
+#include "ctc_kernels.h"
+
+namespace ctcp {
+
+namespace {
+
+constexpr int kEmitRows = 8;       // frame rows per CTA: independent loads in flight per thread
+constexpr int kEmitThreads = 256;
+
+__device__ __forceinline__ int utterance_of_row(const int32_t* cu, int B, int64_t row) {
+    int lo = 0, hi = B - 1, ans = -1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] <= row) {
+            ans = mid;
+            lo = mid + 1;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return ans;
+}
+
+template <int DT>
+__device__ __forceinline__ float load_lp(const void* lp, int64_t idx) {
+    if constexpr (DT == 0) {
+        return __ldg(reinterpret_cast<const float*>(lp) + idx);
+    } else {
+        const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(lp) + idx);
+        return bits_to_float<DT>((uint32_t)h);
+    }
+}
+
+}  // namespace
+
+template <int DT>
+__global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
+    __shared__ int s_b[kEmitRows], s_u[kEmitRows], s_toff[kEmitRows];
+    __shared__ int s_maxw;
+    const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
+    UttInfo* uttw = ws_at<UttInfo>(a.ws, a.L.off_utt);
+    XP* em = ws_at<XP>(a.ws, em_base(a.L));
+    const int64_t r0 = (int64_t)blockIdx.x * kEmitRows;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_maxw = 0;
+    __syncthreads();
+    if (tid < kEmitRows) {
+        const int64_t row = r0 + tid;
+        int b = -1, U = -1, toff = 0;
+        if (row < a.L.T_total) {
+            b = utterance_of_row(a.cu, a.L.B, row);
+            if (b >= 0) {
+                const UttInfo u = utt[b];
+                const int64_t t = row - u.start;
+                if (u.valid && t >= 0 && t < u.T) {
+                    U = u.U;
+                    toff = u.toff;
+                } else {
+                    b = -1;
+                }
+            }
+        }
+        s_b[tid] = b;
+        s_u[tid] = U;
+        s_toff[tid] = toff;
+        if (b >= 0) atomicMax(&s_maxw, U + 2);
+    }
+    __syncthreads();
+    const int maxw = s_maxw;
+    for (int w = tid; w < maxw; w += kEmitThreads) {
+        int cls[kEmitRows];
+#pragma unroll
+        for (int rr = 0; rr < kEmitRows; ++rr) {
+            cls[rr] = -1;
+            if (s_b[rr] >= 0 && w <= s_u[rr]) cls[rr] = w < s_u[rr] ? a.targets[s_toff[rr] + w] : a.blank;
+            if (s_b[rr] >= 0 && w == s_u[rr] + 1) cls[rr] = -2;  // the zero emission
+        }
+        float x[kEmitRows];
+#pragma unroll
+        for (int rr = 0; rr < kEmitRows; ++rr) {
+            // an id outside [0, D) is not read (the chain reports it); its emission is 0
+            const bool live = cls[rr] >= 0 && cls[rr] < a.D;
+            x[rr] = live ? load_lp<DT>(a.lp, (r0 + rr) * (int64_t)a.D + cls[rr]) : -INFINITY;
+        }
+#pragma unroll
+        for (int rr = 0; rr < kEmitRows; ++rr) {
+            if (cls[rr] >= 0) {
+                em[(r0 + rr) * (int64_t)a.L.epitch + w] = xp_from_log(x[rr]);
+                if (x[rr] != x[rr]) atomicOr(&uttw[s_b[rr]].has_nan, 1);
+            } else if (cls[rr] == -2) {
+                em[(r0 + rr) * (int64_t)a.L.epitch + w] = XP{0.0f, kEZeroEm};
+            }
+        }
+    }
+}
+
+template __global__ void emit_kernel<0>(ChainArgs);
+template __global__ void emit_kernel<1>(ChainArgs);
+template __global__ void emit_kernel<2>(ChainArgs);
+
+cudaError_t launch_emit(const ChainArgs& a, int dtype, cudaStream_t s) {
+    if (a.L.T_total == 0 || a.L.B == 0) return cudaSuccess;
+    const int64_t grid = (a.L.T_total + kEmitRows - 1) / kEmitRows;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    if (dtype == 0) emit_kernel<0><<<(unsigned)grid, kEmitThreads, 0, s>>>(a);
+    else if (dtype == 1) emit_kernel<1><<<(unsigned)grid, kEmitThreads, 0, s>>>(a);
+    else emit_kernel<2><<<(unsigned)grid, kEmitThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ctcp

@@ -25,10 +25,11 @@
 //      tile P and marks their chunks, so a chunk reads P only when marked and
 //      every gradient element is written exactly once, in one rounding.
 //
-// The stored rows are fixed-point log2 values of alpha_t(s) / p_t(s) (before
-// the emission) and of beta_t(s), each relative to an integer offset of its
-// (frame, warp); a posterior's exponent alpha~ + beta~ + offsets + nll is
-// summed exactly in 64-bit integers and meets one ex2 at the end.
+// The stored rows hold alpha_t(s) / p_t(s) (before the emission) and
+// beta_t(s) as exact mantissa-exponent words, each relative to an integer
+// offset of its (frame, warp).  A posterior is the product of two mantissas
+// and the per-utterance constant 2^frac(nll log2 e), scaled by 2 to the
+// integer sum of the exponents, the offsets and floor(nll log2 e).
 #include "ctc_common.cuh"
 #include "ctc_kernels.h"
 
@@ -54,13 +55,15 @@ __device__ __forceinline__ int find_utterance(const int32_t* cu, int B, int64_t 
     return ans;
 }
 
-// Posterior of one state from its stored alpha / beta fixed-point values and
-// the integer part `base` = ((A + B) << frac) + round(nll * log2 e << frac).
-__device__ __forceinline__ float posterior(int va, int vb, long long base) {
+// Posterior of one state from its stored alpha / beta words (see enc_state):
+// (ma * mb * c) * 2^(ka + kb + base), where base = A + B + floor(nll log2 e)
+// and c = 2^frac(nll log2 e).  Results below 2^-126 flush to 0.
+__device__ __forceinline__ float posterior(int va, int vb, int base, float c) {
     if (va == kFixZero || vb == kFixZero) return 0.0f;
-    long long t = (long long)va + (long long)vb + base;
-    t = t < -(200ll << kFixFrac) ? -(200ll << kFixFrac) : (t > (200ll << kFixFrac) ? (200ll << kFixFrac) : t);
-    return fast_ex2((float)(int)t * (1.0f / (float)(1 << kFixFrac)));
+    const float ma = __int_as_float(((va & 0x7ffff) << 4) | 0x3f800000);
+    const float mb = __int_as_float(((vb & 0x7ffff) << 4) | 0x3f800000);
+    const int n = min(max((va >> kFixFrac) + (vb >> kFixFrac) + base, -200), 64);
+    return __int_as_float(max(__float_as_int(ma * mb * c) + (n << 23), 0));
 }
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -118,7 +121,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
     const int* __restrict__ beta = ws_at<int>(a.ws, a.L.off_beta);
     const int32_t* __restrict__ nxt = ws_at<int32_t>(a.ws, a.L.off_nxt);
     const int32_t* __restrict__ rank = ws_at<int32_t>(a.ws, a.L.off_rank);
-    const int P = pairs_for_max_u(a.L.max_U);
+    const int GP = a.L.gpairs;  // pairs per offset group of a stored row
     const bool ready = ctrl->grad_ready != 0;
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.L.T_total > 0 && !ready)
         set_status(ctrl, CTC_PACKED_DEV_NO_GRAD_STATE);
@@ -179,7 +182,12 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
             }
             if (!covered || scale == 0.0f) continue;
 
-            const long long kfix = __double2ll_rn(nll[b] * kLog2eD * (double)(1 << kFixFrac));
+            // an infinite nll (no alignment, zero_infinity off) leaves these rows unspecified: NaN scale factor
+            const double nl2 = nll[b] * kLog2eD;
+            const bool nfin = isfinite(nl2);
+            const double kfl = nfin ? floor(nl2) : 0.0;
+            const int kint = (int)fmin(fmax(kfl, -1.0e9), 1.0e9);
+            const float cfrac = nfin ? (float)exp2(nl2 - kfl) : __int_as_float(0x7fc00000);
             const int32_t* ao = aoff + row * a.L.nwo;
             const int32_t* bo = boff + row * a.L.nwo;
             const int* ar = alpha + row * a.L.pitch;
@@ -187,18 +195,16 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
             const int32_t* rk = rank + u.moff;
             const int32_t* nx = nxt + u.moff;
             const int32_t* tg = a.targets + u.toff;
-            // alpha pair j holds states (2j, 2j+1) at positions 2j, 2j+1 (warp (j/P)/32 of its chain);
+            // alpha pair j holds states (2j, 2j+1) at positions 2j, 2j+1 (offset group j / GP of its chain);
             // beta pair j holds states (2j-1, 2j) at positions 2j, 2j+1, so state s sits at s+1
-            auto base_of = [&](int ja, int jb) -> long long {
-                return ((long long)ao[(ja / P) >> 5] + (long long)bo[(jb / P) >> 5]) * (1ll << kFixFrac) + kfix;
-            };
+            auto base_of = [&](int ja, int jb) -> int { return ao[ja / GP] + bo[jb / GP] + kint; };
             float blank_sum = 0.0f;
             for (int j = lane; j <= u.U; j += 32) {
                 const int2 av = *reinterpret_cast<const int2*>(ar + 2 * j);
                 const int2 bv = *reinterpret_cast<const int2*>(br + 2 * j);
-                blank_sum += posterior(av.x, bv.y, base_of(j, j));
+                blank_sum += posterior(av.x, bv.y, base_of(j, j), cfrac);
                 if (j < u.U) {
-                    const float gl = posterior(av.y, br[2 * j + 2], base_of(j, j + 1));
+                    const float gl = posterior(av.y, br[2 * j + 2], base_of(j, j + 1), cfrac);
                     gam[j] = gl;
                     if (rk[j] == -2) blank_sum += gl;
                 }

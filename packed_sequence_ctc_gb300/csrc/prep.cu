@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
             info.valid = valid;
             info.labels_ok = 1;
             info.n_owners = 1;
+            info.has_nan = 0;
             utt[b] = info;
             // utterances that need no recursion get their loss here
             if (!valid || T == 0) {
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
             }
         }
     }
-    const int warp_pairs = 32 * a.pairs_per_thread;
+    const int warp_pairs = a.group_pairs;  // pairs one chain warp owns
     int big_base = 0, small_base = 0, lab_base = 0;
     // first pass counts the big items, so the small ones can follow them
     int n_big = 0;

@@ -174,7 +174,9 @@ def test_odd_class_counts(cuda_device, D, dtype):
     assert_grad_close(grad, ref_grad, dtype, rows=_defined_rows(batch, nll))
 
 
-@pytest.mark.parametrize("U", [30, 31, 32, 33, 63, 64, 65, 200, 511, 1000])
+# a chain warp owns 28 state pairs (4 of its 32 lanes shadow the neighbour):
+# targets of 27/28 labels switch from one warp to several, 55/56 from 2 to 3
+@pytest.mark.parametrize("U", [26, 27, 28, 29, 30, 31, 32, 33, 55, 56, 57, 63, 64, 65, 84, 200, 511, 1000])
 def test_state_counts_across_warp_boundaries(cuda_device, U):
     T = 2 * U + 37
     batch = workloads.make_batch([T, T // 2 + 3, 11], [U, min(U, T // 4), 3], 40, seed=U, repeat_prob=0.2,
@@ -187,13 +189,25 @@ def test_state_counts_across_warp_boundaries(cuda_device, U):
 
 
 def test_two_pairs_per_thread(cuda_device):
-    # a target bound above 1023 puts two state pairs in each thread
+    # a target bound above 895 puts two state pairs in each lane
     batch = workloads.make_batch([2600, 300, 50], [1200, 60, 10], 48, seed=5, reduction="sum")
     loss, grad, status = run_gpu(batch, max_target_len=1500)
     assert status == 0
     ref_loss, ref_grad, _ = _ref(batch)
     assert_loss_close(loss, ref_loss)
     assert_grad_close(grad, ref_grad, torch.float32)
+
+
+def test_four_pairs_per_thread(cuda_device):
+    # a target bound above 1919 puts four state pairs in each lane; the
+    # targets span several warps (124 pairs each) and some stay in one
+    batch = workloads.make_batch([700, 420, 90, 5], [300, 130, 40, 2], 37, seed=9, repeat_prob=0.2,
+                                 reduction="none")
+    loss, grad, status = run_gpu(batch, max_target_len=2100)
+    assert status == 0
+    ref_loss, ref_grad, nll = _ref(batch)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, torch.float32, rows=_defined_rows(batch, nll))
 
 
 @pytest.mark.parametrize("offset", [2, 4, 8])
