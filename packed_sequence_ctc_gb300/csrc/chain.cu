@@ -31,10 +31,11 @@
 // shadow of the first warp, the upper one of the last) the states are zero
 // and stay exactly zero.
 //
-// Emissions come from the emission matrix (emit.cu): every frame a lane
-// needs its P label emissions and the blank's, contiguous in that row.  Each
-// warp keeps 16 / P frames of them in flight with 8-byte cp.async copies
-// into its own shared-memory ring.
+// Emissions come from the emission matrix (emit.cu), whose entries pair a
+// label's emission with the frame's blank: every frame a lane copies its
+// first pair's entry (16 bytes, label and blank) and the label halves of
+// its other pairs into its slice of the warp's shared-memory ring, R frames
+// ahead.  No lane reads another lane's slice, so no warp sync is needed.
 //
 // Arithmetic: the recursion runs on probabilities in extended range (a float
 // mantissa and an int32 binary exponent per state, see ctc_common.cuh):
@@ -62,8 +63,10 @@ struct ChainShape {
     static constexpr int G = ghost_lanes(P);  // shadow lanes per warp
     static constexpr int GP = group_pairs(P); // pairs a warp owns
     static constexpr int F = G * P;           // frames between halo exchanges (4 for every P)
-    static constexpr int R = P == 4 ? 4 : 8;  // emission frames in flight per warp
-    static constexpr int LW = P + 1;          // extended emissions per lane and frame: P labels, the blank
+    static constexpr int R = P == 1 ? 8 : 4;  // emission frames in flight per warp
+    // extended values per lane and frame in the ring: (label 0, blank), the
+    // other labels, padded to 16 bytes
+    static constexpr int LW = 2 * ((P + 2) / 2);
     static constexpr int XW = G * P * 2;      // extended values one warp sends per exchange
     static_assert(F == 4, "frames are run in blocks of one exchange period");
     static_assert(R % F == 0, "a block of frames maps onto consecutive ring slots");
@@ -82,9 +85,12 @@ __device__ __forceinline__ bool bar_named_or(int id, int n, bool v) {
         : "memory");
     return r != 0;
 }
-// 8-byte async copy global -> shared.
+// 8- and 16-byte async copies global -> shared.
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 struct ItemCtx {
@@ -120,18 +126,18 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     const bool own = DIR == 0 ? lane >= S::G : lane < 32 - S::G;
     const int j0 = DIR == 0 ? c.w * S::GP + (lane - S::G) * P : c.w * S::GP + lane * P;
     bool has_label[P], skip[P];
-    int wl[P];  // emission-row word of my label state (U + 1: the zero emission)
+    int wl[P];  // emission-row entry of my label state (U: the zero emission)
     bool bad = false;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
         const int j = j0 + p;
         if (DIR == 0) {  // (blank 2j, label 2j+1 = l_j)
             has_label[p] = j >= 0 && j < U;
-            wl[p] = has_label[p] ? j : U + 1;
+            wl[p] = has_label[p] ? j : U;
             skip[p] = j >= 1 && j < U && tg[j] != tg[j - 1];
         } else {  // (label 2j-1 = l_{j-1}, blank 2j)
             has_label[p] = j >= 1 && j <= U;
-            wl[p] = has_label[p] ? j - 1 : U + 1;
+            wl[p] = has_label[p] ? j - 1 : U;
             skip[p] = j >= 1 && j < U && tg[j - 1] != tg[j];
         }
         if (own && has_label[p]) {
@@ -156,30 +162,31 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     // emission stream: frame k is row start + k (alpha) or start + T - 1 - k
     // (beta); the matrix has kEmPad >= R rows of padding at both ends, so
     // frames up to R - 1 past the utterance are read without a check
-    const XP* em = ws_at<XP>(a.ws, em_base(a.L));
+    const XP2* em = ws_at<XP2>(a.ws, em_base(a.L));
     const int64_t row0 = DIR == 0 ? (int64_t)info.start : (int64_t)info.start + T - 1;
     const int64_t estep = DIR == 0 ? (int64_t)a.L.epitch : -(int64_t)a.L.epitch;
-    const XP* gsrc[P + 1];  // next frame's sources: my labels, then the blank
+    const XP2* src0[P];  // my entries in frame 0's row
 #pragma unroll
-    for (int p = 0; p < P; ++p) gsrc[p] = em + row0 * a.L.epitch + wl[p];
-    gsrc[P] = em + row0 * a.L.epitch + U;
-    // ring slot of frame k: (k - 1) mod R; lane l's entries are LW consecutive values
+    for (int p = 0; p < P; ++p) src0[p] = em + row0 * a.L.epitch + wl[p];
+    // ring slot of frame k: (k - 1) mod R; lane l's values are LW consecutive XP
     const uint32_t ring_lane = smem_addr(c.ring) + (uint32_t)(lane * S::LW) * 8u;
     constexpr uint32_t kSlotBytes = 32u * S::LW * 8u;
-    auto request = [&](uint32_t slot) {  // the next frame into ring slot `slot`
+    // frame k into ring slot `slot`; each address is formed from frame 0's, so
+    // no register that a copy in flight still reads is written over
+    auto request = [&](uint32_t slot, int k) {
         const uint32_t dst = ring_lane + slot * kSlotBytes;
+        const int64_t off = (int64_t)k * estep;
+        cp_async16(dst, src0[0] + off);
 #pragma unroll
-        for (int p = 0; p <= P; ++p) {
-            cp_async8(dst + 8u * p, gsrc[p]);
-            gsrc[p] += estep;
-        }
+        for (int p = 1; p < P; ++p) cp_async8(dst + 8u * (p + 1), &src0[p][off].l);
         cp_async_commit();
     };
     auto emissions = [&](uint32_t slot, XP (&el)[P], XP& eb) {
         const XP* e = reinterpret_cast<const XP*>(c.ring) + slot * 32 * S::LW + lane * S::LW;
+        el[0] = e[0];
+        eb = e[1];
 #pragma unroll
-        for (int p = 0; p < P; ++p) el[p] = e[p];
-        eb = e[P];
+        for (int p = 1; p < P; ++p) el[p] = e[p + 1];
     };
 
     // stored rows, written one frame late
@@ -285,14 +292,14 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
 
     // prologue: frames 0 .. R-2 requested (frame k into slot (k - 1) mod R)
 #pragma unroll
-    for (int k = 0; k < S::R - 1; ++k) request((uint32_t)((k + S::R - 1) & (S::R - 1)));
+    for (int k = 0; k < S::R - 1; ++k) request((uint32_t)((k + S::R - 1) & (S::R - 1)), k);
 
     // frame 0
     {
         cp_async_wait<S::R - 2>();
         XP el[P], eb;
         emissions(S::R - 1, el, eb);
-        request(S::R - 2);  // frame R - 1
+        request(S::R - 2, S::R - 1);
 #pragma unroll
         for (int p = 0; p < P; ++p) {
             const int j = j0 + p;
@@ -326,7 +333,7 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             cp_async_wait<S::R - 2>();
             XP el[P], eb;
             emissions(base + q, el, eb);
-            request((base + q + S::R - 1) & (S::R - 1));
+            request((base + q + S::R - 1) & (S::R - 1), i0 + q + S::R - 1);
             flush_row();  // frame i0 + q - 1
             step(el, eb);
         }
@@ -340,7 +347,7 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         XP el[P], eb;
         const uint32_t slot = (uint32_t)((i - 1) & (S::R - 1));
         emissions(slot, el, eb);
-        request((slot + S::R - 1) & (S::R - 1));
+        request((slot + S::R - 1) & (S::R - 1), i + S::R - 1);
         flush_row();
         step(el, eb);
     }

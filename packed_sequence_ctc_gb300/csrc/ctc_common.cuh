@@ -55,7 +55,7 @@ struct Layout {
     int32_t ecap;                // distinct classes a target can have: min(max_U + 1, D)
     int32_t gpairs;              // state pairs a chain warp owns (its offset group)
     int32_t nwo;                 // per-frame offsets stored per chain row (one per offset group)
-    int32_t epitch;              // extended emissions per row of the emission matrix (>= max_U + 2, even)
+    int32_t epitch;              // entries per row of the emission matrix (max_U + 1)
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
     size_t off_nxt, off_rank, off_owner, off_em, total;
@@ -96,7 +96,7 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
         const int nw = (pairs + L.gpairs - 1) / L.gpairs;
         L.nwo = nw < 1 ? 1 : nw;
     }
-    L.epitch = (int32_t)align_up((size_t)(max_U + 2), 2);  // labels, the blank, a zero emission
+    L.epitch = max_U + 1;  // (label, blank) entries, then (zero, blank)
     L.lab_cap = (int64_t)B * max_U + B;
     size_t o = 0;
     L.off_ctrl = o;   o = align_up(o + sizeof(Control), 256);
@@ -110,7 +110,7 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_nxt = o;    o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_rank = o;   o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_owner = o;  o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
-    L.off_em = o;     o = align_up(o + 8 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
+    L.off_em = o;     o = align_up(o + 16 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
     L.total = o;
     return L;
 }
@@ -124,7 +124,7 @@ __host__ __device__ inline const T* ws_at(const void* ws, size_t off) {
     return reinterpret_cast<const T*>(static_cast<const unsigned char*>(ws) + off);
 }
 // Row 0 of the emission matrix (after its leading padding).
-__host__ __device__ inline size_t em_base(const Layout& L) { return L.off_em + 8 * (size_t)kEmPad * (size_t)L.epitch; }
+__host__ __device__ inline size_t em_base(const Layout& L) { return L.off_em + 16 * (size_t)kEmPad * (size_t)L.epitch; }
 
 // Element types: 0 float32, 1 bfloat16, 2 float16.
 template <int DT>
@@ -162,6 +162,11 @@ constexpr float kL2eLo = 1.9259629911783890e-8f;  // log2 e - kL2eHi
 struct XP {
     float m;  // mantissa, 0 for probability 0
     int e;    // binary exponent
+};
+// One entry of the emission matrix: a label's emission and the frame's blank
+// emission side by side, so one 16-byte copy brings a lane both.
+struct __align__(16) XP2 {
+    XP l, b;
 };
 
 // exp(lp) in extended form.  lp * log2 e = yh + yl exactly (FMA), then

@@ -2,8 +2,9 @@
 // log probabilities of the utterance's target labels and of the blank,
 // lp[t, l_1..l_U] and lp[t, blank], converted once into extended-range
 // probabilities (ctc_common.cuh, XP) and written as one contiguous row of the
-// workspace's emission matrix: em[row][w] for w < U is label l_{w+1}, em[row][U]
-// the blank, em[row][U + 1] a zero emission (read by lanes without a label).
+// workspace's emission matrix.  Entry em[row][w] pairs label l_{w+1} (w < U)
+// with the frame's blank; em[row][U] pairs a zero emission with the blank,
+// for the recursion lanes that hold no label.
 //
 // Page "feat(asr): native CTC loss kernel over sequence-packed log
 // probabilities", ctc_loss.py ``_alpha_kernel`` and ``_beta_grad_kernel``:
@@ -55,10 +56,11 @@ __device__ __forceinline__ float load_lp(const void* lp, int64_t idx) {
 template <int DT>
 __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
     __shared__ int s_b[kEmitRows], s_u[kEmitRows], s_toff[kEmitRows];
+    __shared__ XP s_blank[kEmitRows];
     __shared__ int s_maxw;
     const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
     UttInfo* uttw = ws_at<UttInfo>(a.ws, a.L.off_utt);
-    XP* em = ws_at<XP>(a.ws, em_base(a.L));
+    XP2* em = ws_at<XP2>(a.ws, em_base(a.L));
     const int64_t r0 = (int64_t)blockIdx.x * kEmitRows;
     const int tid = threadIdx.x;
     if (tid == 0) s_maxw = 0;
@@ -82,7 +84,12 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
         s_b[tid] = b;
         s_u[tid] = U;
         s_toff[tid] = toff;
-        if (b >= 0) atomicMax(&s_maxw, U + 2);
+        if (b >= 0) {
+            const float x = load_lp<DT>(a.lp, row * (int64_t)a.D + a.blank);
+            s_blank[tid] = xp_from_log(x);
+            if (x != x) atomicOr(&uttw[b].has_nan, 1);
+            atomicMax(&s_maxw, U + 1);
+        }
     }
     __syncthreads();
     const int maxw = s_maxw;
@@ -90,9 +97,9 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
         int cls[kEmitRows];
 #pragma unroll
         for (int rr = 0; rr < kEmitRows; ++rr) {
-            cls[rr] = -1;
-            if (s_b[rr] >= 0 && w <= s_u[rr]) cls[rr] = w < s_u[rr] ? a.targets[s_toff[rr] + w] : a.blank;
-            if (s_b[rr] >= 0 && w == s_u[rr] + 1) cls[rr] = -2;  // the zero emission
+            cls[rr] = -1;  // no entry
+            if (s_b[rr] >= 0 && w < s_u[rr]) cls[rr] = a.targets[s_toff[rr] + w];
+            if (s_b[rr] >= 0 && w == s_u[rr]) cls[rr] = -2;  // (zero, blank): read by lanes without a label
         }
         float x[kEmitRows];
 #pragma unroll
@@ -103,11 +110,12 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
         }
 #pragma unroll
         for (int rr = 0; rr < kEmitRows; ++rr) {
-            if (cls[rr] >= 0) {
-                em[(r0 + rr) * (int64_t)a.L.epitch + w] = xp_from_log(x[rr]);
+            if (cls[rr] != -1) {
+                XP2 v;
+                v.l = cls[rr] == -2 ? XP{0.0f, kEZeroEm} : xp_from_log(x[rr]);
+                v.b = s_blank[rr];
+                em[(r0 + rr) * (int64_t)a.L.epitch + w] = v;
                 if (x[rr] != x[rr]) atomicOr(&uttw[s_b[rr]].has_nan, 1);
-            } else if (cls[rr] == -2) {
-                em[(r0 + rr) * (int64_t)a.L.epitch + w] = XP{0.0f, kEZeroEm};
             }
         }
     }
