@@ -131,6 +131,9 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
     ga.warp_smem = wsm;
     ga.n_tiles = (T_total + k - 1) / k;
     ga.congruent = ((g0 ^ l0) & 15u) == 0 ? 1 : 0;
+    ga.gp_mul = grad_group_multiplier(ga.L);
+    if (ga.gp_mul == 0) return CTC_PACKED_ERR_UNSUPPORTED;
+    if (launch_post(ga, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     if (launch_grad(ga, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     return CTC_PACKED_OK;
 }

@@ -224,6 +224,8 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     };
 
     XP vb[P], vl[P];  // alpha (blank 2j, label 2j+1) / beta (label 2j-1, blank 2j)
+#pragma unroll
+    for (int p = 0; p < P; ++p) vb[p] = vl[p] = zero;
     // one recursion step with this frame's emissions.  The shuffle hands lane 0
     // (alpha) / lane 31 (beta) its own state: those lanes shadow pairs that
     // are either outside the target (zero, and zero feeds zero) or
@@ -373,16 +375,27 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         if (c.w == 0 && lane == 0) {
             const XP f0 = c.fin[0], f1 = c.fin[1];
             double v;
+            UttInfo* uw = ws_at<UttInfo>(a.ws, a.L.off_utt) + b;
+            int kint = 0, ninf = 0;
+            float cfrac = __int_as_float(0x7fc00000);  // the backward's posterior factor, NaN unless nll is finite
             if (info.has_nan) {
                 v = __longlong_as_double(0x7ff8000000000000ll);
             } else if (f0.m == 0.0f && f1.m == 0.0f) {
                 v = __longlong_as_double(0x7ff0000000000000ll);  // no path: +inf
+                ninf = 1;
             } else {
                 const int Em = max(f0.e, f1.e);
                 const double sum = (double)f0.m * exp2((double)(max(f0.e - Em, -1100))) +
                                    (double)f1.m * exp2((double)(max(f1.e - Em, -1100)));
-                v = -((double)Em + log2(sum)) * kLn2D;
+                const double nl2 = -((double)Em + log2(sum));  // nll in bits
+                v = nl2 * kLn2D;
+                const double kf = floor(nl2);
+                kint = (int)fmin(fmax(kf, -1.0e9), 1.0e9);
+                cfrac = (float)exp2(nl2 - kf);
             }
+            uw->kint = kint;
+            uw->cfrac = cfrac;
+            uw->nll_inf = ninf;
             nll_out[b] = v;
             if (a.reduction == CTC_PACKED_NONE) {
                 float out = (float)v;

@@ -46,6 +46,19 @@ struct UttInfo {
     int32_t labels_ok;  // every target id in [0, D) (set by the label analysis)
     int32_t n_owners;   // distinct non-blank target classes + 1 (the blank group)
     int32_t has_nan;    // a label or blank log probability of the utterance is NaN (set by the emission gather)
+    // nll * log2(e) = kint + log2(cfrac), cfrac in [1, 2), and whether nll is +inf (set by the alpha chain)
+    int32_t kint;
+    float cfrac;
+    int32_t nll_inf;
+    int32_t pad;
+};
+
+// Per-row header of the backward's class sums (written by the posterior pass).
+struct RowHead {
+    int32_t count;    // class-sum entries of the row
+    float scale;      // upstream gradient factor of the row's utterance (0 when not covered)
+    int32_t covered;  // the row belongs to a well-formed utterance's frames
+    int32_t pad;
 };
 
 // Byte offsets of every array inside the caller's workspace.
@@ -58,7 +71,7 @@ struct Layout {
     int32_t epitch;              // entries per row of the emission matrix (max_U + 1)
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
-    size_t off_nxt, off_rank, off_owner, off_em, total;
+    size_t off_nxt, off_rank, off_owner, off_em, off_head, off_ent, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -111,6 +124,8 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_rank = o;   o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_owner = o;  o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
     L.off_em = o;     o = align_up(o + 16 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
+    L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
+    L.off_ent = o;    o = align_up(o + 8 * (size_t)T_total * (size_t)L.ecap, 256);
     L.total = o;
     return L;
 }

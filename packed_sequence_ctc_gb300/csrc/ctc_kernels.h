@@ -50,6 +50,7 @@ struct GradArgs {
     int entry_cap;       // corrections a group can hold
     size_t warp_smem;    // shared memory bytes per warp
     int congruent;       // lp and grad share their address modulo 16
+    uint32_t gp_mul;     // offset group of pair j: (j * gp_mul) >> 21 == j / L.gpairs
 };
 
 __global__ void prep_kernel(PrepArgs a);
@@ -57,14 +58,17 @@ template <int DT>
 __global__ void emit_kernel(ChainArgs a);
 template <int P>
 __global__ void chain_kernel(ChainArgs a);
+__global__ void post_kernel(GradArgs a);
 template <int DT>
 __global__ void grad_kernel(GradArgs a);
 void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& warp_smem);
+uint32_t grad_group_multiplier(const Layout& L);  // 0 if no exact multiplier exists
 
 // Host launchers (defined next to their kernels).
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_emit(const ChainArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
+cudaError_t launch_post(const GradArgs& a, cudaStream_t s);
 cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s);
 
 }  // namespace ctcp

@@ -38,8 +38,12 @@ namespace ctcp {
 namespace {
 
 constexpr int kMaxWarpsPerBlock = 8;
+constexpr int kPostThreads = 256;
+constexpr int kPostRows = 4;  // rows a warp of the class-sum pass walks together
 constexpr int kUnroll = 4;                   // 16-byte chunks in flight per lane
 constexpr int kBatchChunks = 32 * kUnroll;   // chunks a warp streams per batch
+constexpr int kMaxBatches = 40;
+constexpr int kGroupShift = 21;             // offset group of pair j: (j * gp_mul) >> kGroupShift              // batches of one row (D <= 16384, 4-byte elements: 33)
 
 __device__ __forceinline__ int find_utterance(const int32_t* cu, int B, int64_t row) {
     int lo = 0, hi = B - 1, ans = -1;
@@ -91,42 +95,207 @@ __device__ __forceinline__ void store_elem(uintptr_t addr, uint32_t bits) {
     }
 }
 
+// Gradient of one whole 16-byte chunk: s * exp(lp) + pn element by element,
+// pn the chunk's negated class sums (zero where none), in pairs on the
+// paired fp32 pipes, rounded once into the chunk's dtype.
+template <int DT>
+__device__ __forceinline__ uint4 chunk_grad(uint4 in, float s, const float (&pn)[16 / Elem<DT>::bytes]) {
+    const float2 l2e = make_float2(kLog2e, kLog2e), s2 = make_float2(s, s);
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    if constexpr (DT == 0) {
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            const float2 t = __fmul2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e);
+            const float2 r = __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[i], pn[i + 1]));
+            o[i] = r.x;
+            o[i + 1] = r.y;
+        }
+        return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+    } else {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 x;
+            if constexpr (DT == 1) {  // bfloat16: the high half is already a float
+                x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+            } else {
+                x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            }
+            const float2 t = __fmul2_rn(x, l2e);
+            const float2 r =
+                __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[2 * i], pn[2 * i + 1]));
+            o[i] = pack2<DT>(r.x, r.y);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 }  // namespace
 
-template <int DT>
-__global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArgs a) {
-    constexpr int E = Elem<DT>::bytes;
-    constexpr int V = 16 / E;  // elements per 16-byte chunk
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+// Class sums of every row.  A warp takes kPostRows consecutive rows at a
+// time and walks their states together, so each round trip to memory serves
+// all of them.  For a covered row with a nonzero scale, each distinct class
+// of its utterance (the blank last) gets one entry (class, -scale * sum of
+// its states' posteriors); the header holds the entry count, the scale and
+// whether the row is covered.
+__global__ void __launch_bounds__(kPostThreads) post_kernel(GradArgs a) {
+    extern __shared__ __align__(16) float post_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int K = a.rows_per_tile;   // rows per group
-    const int cap = a.entry_cap;     // corrections a group can hold
-    const int ulen = a.L.max_U + 1;  // label posteriors a row can hold
-    // this warp's slice: row scales, corrections (packed row/class, value), label posteriors
-    unsigned char* ws = smem_raw + (size_t)warp * a.warp_smem;
-    float* row_scale = reinterpret_cast<float*>(ws);  // K entries, NaN-free: 0 when not covered
-    int* row_cov = reinterpret_cast<int*>(ws + align_up(4 * (size_t)K, 16));
-    int* e_key = reinterpret_cast<int*>(ws + 2 * align_up(4 * (size_t)K, 16));
-    float* e_val = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_key) + align_up(4 * (size_t)cap, 16));
-    float* gam = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_val) + align_up(4 * (size_t)cap, 16));
-    float* ptile = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(gam) + align_up(4 * (size_t)ulen, 16));
-    uint32_t* pmark = reinterpret_cast<uint32_t*>(ptile + kBatchChunks * V);  // kBatchChunks / 32 words
-
+    const int ulen = (int)align_up((size_t)a.L.max_U + 1, 4);
+    float* gam = post_smem + (size_t)warp * kPostRows * ulen;  // label posteriors of the rows, [row][j]
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
-    const double* nll = ws_at<double>(a.ws, a.L.off_nll);
     const int32_t* __restrict__ aoff = ws_at<int32_t>(a.ws, a.L.off_aoff);
     const int32_t* __restrict__ boff = ws_at<int32_t>(a.ws, a.L.off_boff);
     const int* __restrict__ alpha = ws_at<int>(a.ws, a.L.off_alpha);
     const int* __restrict__ beta = ws_at<int>(a.ws, a.L.off_beta);
     const int32_t* __restrict__ nxt = ws_at<int32_t>(a.ws, a.L.off_nxt);
     const int32_t* __restrict__ rank = ws_at<int32_t>(a.ws, a.L.off_rank);
-    const int GP = a.L.gpairs;  // pairs per offset group of a stored row
+    RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
+    int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
+    const uint32_t gp_mul = a.gp_mul;  // j / gpairs == (j * gp_mul) >> kGroupShift for every pair j
     const bool ready = ctrl->grad_ready != 0;
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.L.T_total > 0 && !ready)
         set_status(ctrl, CTC_PACKED_DEV_NO_GRAD_STATE);
-    const int D = a.D;
     const int B = a.L.B;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t n_blocks = (a.L.T_total + kPostRows - 1) / kPostRows;
+
+    for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; blk < n_blocks; blk += warps) {
+        const int64_t r0 = blk * kPostRows;
+        // per row: its utterance, scale and the constants of its posteriors
+        int U[kPostRows], moff[kPostRows], toff[kPostRows], kint[kPostRows], nown[kPostRows];
+        float scale[kPostRows], cfrac[kPostRows];
+        bool live[kPostRows], covered[kPostRows];
+        int jmax = -1;
+        {
+            int b = find_utterance(a.cu, B, r0);
+#pragma unroll
+            for (int r = 0; r < kPostRows; ++r) {
+                const int64_t row = r0 + r;
+                covered[r] = false;
+                scale[r] = 0.0f;
+                U[r] = 0;
+                moff[r] = toff[r] = kint[r] = nown[r] = 0;
+                cfrac[r] = 0.0f;
+                if (row < a.L.T_total) {
+                    while (b + 1 < B && (int64_t)a.cu[b + 1] <= row) ++b;  // rows ascend: walk forward
+                    if (b >= 0) {
+                        const UttInfo u = utt[b];
+                        const int64_t t = row - u.start;
+                        covered[r] = ready && u.valid && u.labels_ok && t >= 0 && t < u.T;
+                        if (covered[r]) {
+                            if (a.reduction == CTC_PACKED_NONE) {
+                                scale[r] = a.grad_loss[b];
+                            } else if (a.reduction == CTC_PACKED_SUM) {
+                                scale[r] = a.grad_loss[0];
+                            } else {
+                                scale[r] = __fdiv_rn(a.grad_loss[0], (float)B * (float)max(u.U, 1));
+                            }
+                            if (a.zero_infinity && u.nll_inf) scale[r] = 0.0f;
+                            // an infinite nll (no alignment, zero_infinity off) leaves the row unspecified
+                            kint[r] = u.kint;
+                            cfrac[r] = u.cfrac;
+                            U[r] = u.U;
+                            moff[r] = u.moff;
+                            toff[r] = u.toff;
+                            nown[r] = u.n_owners;
+                        }
+                    }
+                }
+                live[r] = covered[r] && scale[r] != 0.0f;
+                if (live[r]) jmax = max(jmax, U[r]);
+            }
+        }
+        // 1. posteriors of every state pair of the rows
+        float blank_sum[kPostRows];
+#pragma unroll
+        for (int r = 0; r < kPostRows; ++r) blank_sum[r] = 0.0f;
+        for (int j = lane; j <= jmax; j += 32) {
+            const uint32_t ga = ((uint32_t)j * gp_mul) >> kGroupShift;
+            const uint32_t gb = ((uint32_t)(j + 1) * gp_mul) >> kGroupShift;
+            int2 av[kPostRows], bv[kPostRows];
+            int bl[kPostRows], oa[kPostRows], ob0[kPostRows], ob1[kPostRows], rk[kPostRows];
+#pragma unroll
+            for (int r = 0; r < kPostRows; ++r) {
+                const bool on = live[r] && j <= U[r];
+                const bool lab = live[r] && j < U[r];
+                const int64_t row = r0 + r;
+                av[r] = on ? *reinterpret_cast<const int2*>(alpha + row * a.L.pitch + 2 * j) : make_int2(kFixZero, kFixZero);
+                bv[r] = on ? *reinterpret_cast<const int2*>(beta + row * a.L.pitch + 2 * j) : make_int2(kFixZero, kFixZero);
+                bl[r] = lab ? beta[row * a.L.pitch + 2 * j + 2] : kFixZero;
+                oa[r] = on ? aoff[row * a.L.nwo + ga] : 0;
+                ob0[r] = on ? boff[row * a.L.nwo + ga] : 0;
+                ob1[r] = lab ? boff[row * a.L.nwo + gb] : 0;
+                rk[r] = lab ? rank[moff[r] + j] : -1;
+            }
+#pragma unroll
+            for (int r = 0; r < kPostRows; ++r) {
+                blank_sum[r] += posterior(av[r].x, bv[r].y, oa[r] + ob0[r] + kint[r], cfrac[r]);
+                const float gl = posterior(av[r].y, bl[r], oa[r] + ob1[r] + kint[r], cfrac[r]);
+                if (live[r] && j < U[r]) gam[r * ulen + j] = gl;
+                if (rk[r] == -2) blank_sum[r] += gl;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kPostRows; ++r) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) blank_sum[r] += __shfl_xor_sync(0xffffffffu, blank_sum[r], o);
+        }
+        __syncwarp();
+        // 2. each distinct class, summed by its first occurrence in target order
+        for (int j = lane; j < jmax; j += 32) {
+#pragma unroll
+            for (int r = 0; r < kPostRows; ++r) {
+                if (!(live[r] && j < U[r])) continue;
+                const int kind = rank[moff[r] + j];
+                if (kind >= 0) {
+                    const int32_t* nx = nxt + moff[r];
+                    float sum = gam[r * ulen + j];
+                    for (int jj = nx[j]; jj >= 0; jj = nx[jj]) sum += gam[r * ulen + jj];
+                    ent[(r0 + r) * a.L.ecap + kind] = make_int2(a.targets[toff[r] + j], __float_as_int(-scale[r] * sum));
+                }
+            }
+        }
+        if (lane < kPostRows) {
+#pragma unroll
+            for (int r = 0; r < kPostRows; ++r) {
+                if (r != lane || r0 + r >= a.L.T_total) continue;
+                if (live[r])
+                    ent[(r0 + r) * a.L.ecap + nown[r] - 1] = make_int2(a.blank, __float_as_int(-scale[r] * blank_sum[r]));
+                head[r0 + r] = RowHead{live[r] ? nown[r] : 0, covered[r] ? scale[r] : 0.0f, covered[r] ? 1 : 0, 0};
+            }
+        }
+        __syncwarp();
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArgs a) {
+    constexpr int E = Elem<DT>::bytes;
+    constexpr int V = 16 / E;  // elements per 16-byte chunk
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int K = a.rows_per_tile;   // rows per group
+    const int cap = a.entry_cap;     // corrections a group can hold
+    // this warp's slice: row scales, corrections (packed row/class, value), the batch tile
+    unsigned char* ws = smem_raw + (size_t)warp * a.warp_smem;
+    float* row_scale = reinterpret_cast<float*>(ws);  // K entries, NaN-free: 0 when not covered
+    int* row_cov = reinterpret_cast<int*>(ws + align_up(4 * (size_t)K, 16));
+    int* e_key = reinterpret_cast<int*>(ws + 2 * align_up(4 * (size_t)K, 16));
+    float* e_val = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_key) + align_up(4 * (size_t)cap, 16));
+    float* ptile = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_val) + align_up(4 * (size_t)cap, 16));
+    uint32_t* pmark = reinterpret_cast<uint32_t*>(ptile + kBatchChunks * 8);  // kBatchChunks / 32 words
+    // a row's class sums bucketed by batch: bstart[b] .. bstart[b + 1] in skey / sval
+    int* bstart = reinterpret_cast<int*>(pmark + 4);
+    int* bfill = bstart + (kMaxBatches + 4);
+    int* skey = bfill + (kMaxBatches + 4);
+    float* sval = reinterpret_cast<float*>(skey + align_up((size_t)cap, 4));
+
+    const RowHead* __restrict__ head = ws_at<RowHead>(a.ws, a.L.off_head);
+    const int2* __restrict__ ent = ws_at<int2>(a.ws, a.L.off_ent);
+    const int D = a.D;
     const uintptr_t lp0 = reinterpret_cast<uintptr_t>(a.lp);
     const uintptr_t gr0 = reinterpret_cast<uintptr_t>(a.grad);
     const int64_t n_groups = a.n_tiles;
@@ -141,93 +310,29 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
         const int64_t r0 = grp * K;
         const int nrows = (int)min((int64_t)K, a.L.T_total - r0);
 
-        // the next group's stored rows start their way into L2
+        // the next group's class sums start their way into L2
         {
             const int64_t nr0 = (grp + warps) * K;
             const int64_t nrows_next = nr0 < a.L.T_total ? min((int64_t)K, a.L.T_total - nr0) : 0;
-            const int64_t bytes = nrows_next * (int64_t)a.L.pitch * 4;
-            for (int64_t off = (int64_t)lane * 128; off < bytes; off += 32 * 128) {
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(alpha + nr0 * a.L.pitch + off / 4));
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + nr0 * a.L.pitch + off / 4));
-            }
+            const int64_t bytes = nrows_next * (int64_t)a.L.ecap * 8;
+            for (int64_t off = (int64_t)lane * 128; off < bytes; off += 32 * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(ent + nr0 * a.L.ecap) + off));
         }
-        // 1. posteriors of every row of the group
+        // 1. the group's rows: scale, coverage and class sums (key = row in group * D + class)
         int count = 0;  // corrections so far (warp-uniform)
-        int b = find_utterance(a.cu, B, r0);
         for (int rr = 0; rr < nrows; ++rr) {
-            const int64_t row = r0 + rr;
-            while (b + 1 < B && (int64_t)a.cu[b + 1] <= row) ++b;  // rows ascend: walk forward
-            int covered = 0;
-            float scale = 0.0f;
-            UttInfo u{};
-            if (b >= 0) {
-                u = utt[b];
-                const int64_t t = row - u.start;
-                covered = ready && u.valid && u.labels_ok && t >= 0 && t < u.T;
-                if (covered) {
-                    if (a.reduction == CTC_PACKED_NONE) {
-                        scale = a.grad_loss[b];
-                    } else if (a.reduction == CTC_PACKED_SUM) {
-                        scale = a.grad_loss[0];
-                    } else {
-                        scale = (float)((double)a.grad_loss[0] / ((double)B * (double)max(u.U, 1)));
-                    }
-                    const double v = nll[b];
-                    if (a.zero_infinity && isinf(v) && v > 0) scale = 0.0f;
-                }
-            }
+            const RowHead h = head[r0 + rr];
             if (lane == 0) {
-                row_scale[rr] = covered ? scale : 0.0f;
-                row_cov[rr] = covered;
+                row_scale[rr] = h.scale;
+                row_cov[rr] = h.covered;
             }
-            if (!covered || scale == 0.0f) continue;
-
-            // an infinite nll (no alignment, zero_infinity off) leaves these rows unspecified: NaN scale factor
-            const double nl2 = nll[b] * kLog2eD;
-            const bool nfin = isfinite(nl2);
-            const double kfl = nfin ? floor(nl2) : 0.0;
-            const int kint = (int)fmin(fmax(kfl, -1.0e9), 1.0e9);
-            const float cfrac = nfin ? (float)exp2(nl2 - kfl) : __int_as_float(0x7fc00000);
-            const int32_t* ao = aoff + row * a.L.nwo;
-            const int32_t* bo = boff + row * a.L.nwo;
-            const int* ar = alpha + row * a.L.pitch;
-            const int* br = beta + row * a.L.pitch;
-            const int32_t* rk = rank + u.moff;
-            const int32_t* nx = nxt + u.moff;
-            const int32_t* tg = a.targets + u.toff;
-            // alpha pair j holds states (2j, 2j+1) at positions 2j, 2j+1 (offset group j / GP of its chain);
-            // beta pair j holds states (2j-1, 2j) at positions 2j, 2j+1, so state s sits at s+1
-            auto base_of = [&](int ja, int jb) -> int { return ao[ja / GP] + bo[jb / GP] + kint; };
-            float blank_sum = 0.0f;
-            for (int j = lane; j <= u.U; j += 32) {
-                const int2 av = *reinterpret_cast<const int2*>(ar + 2 * j);
-                const int2 bv = *reinterpret_cast<const int2*>(br + 2 * j);
-                blank_sum += posterior(av.x, bv.y, base_of(j, j), cfrac);
-                if (j < u.U) {
-                    const float gl = posterior(av.y, br[2 * j + 2], base_of(j, j + 1), cfrac);
-                    gam[j] = gl;
-                    if (rk[j] == -2) blank_sum += gl;
-                }
+            const int2* er = ent + (r0 + rr) * a.L.ecap;
+            for (int e = lane; e < h.count; e += 32) {
+                const int2 v = er[e];
+                e_key[count + e] = rr * D + v.x;
+                e_val[count + e] = __int_as_float(v.y);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) blank_sum += __shfl_xor_sync(0xffffffffu, blank_sum, o);
-            __syncwarp();
-            // each distinct class, summed by its first occurrence in target order
-            for (int j = lane; j < u.U; j += 32) {
-                const int kind = rk[j];
-                if (kind >= 0) {
-                    float s = gam[j];
-                    for (int jj = nx[j]; jj >= 0; jj = nx[jj]) s += gam[jj];
-                    e_key[count + kind] = rr * D + tg[j];
-                    e_val[count + kind] = scale * s;
-                }
-            }
-            if (lane == 0) {
-                e_key[count + u.n_owners - 1] = rr * D + a.blank;
-                e_val[count + u.n_owners - 1] = scale * blank_sum;
-            }
-            count += u.n_owners;
-            __syncwarp();
+            count += h.count;
         }
         __syncwarp();
 
@@ -256,21 +361,54 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
             const uintptr_t lpq = qb + (a0 - g0);  // lp address of chunk 0
             const bool cov = row_cov[0] != 0;
             const float s = row_scale[0];
-            for (int q0 = 0; q0 < nq; q0 += kBatchChunks) {
-                uint4 in[kUnroll];
+            const int nb = (nq + kBatchChunks - 1) / kBatchChunks;
+            // bucket the class sums by batch, once per row
+            for (int i = lane; i <= nb; i += 32) bfill[i] = 0;
+            __syncwarp();
+            for (int e = lane; e < count; e += 32) atomicAdd(&bfill[(e_key[e] + pshift) / (kBatchChunks * V)], 1);
+            __syncwarp();
+            {
+                int run = 0;
+                for (int base = 0; base <= nb; base += 32) {
+                    const int i = base + lane;
+                    const int c = i < nb ? bfill[i] : 0;
+                    int x = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    if (i <= nb) bstart[i] = run + x - c;
+                    run += __shfl_sync(0xffffffffu, x, 31);
+                }
+            }
+            __syncwarp();
+            for (int i = lane; i < nb; i += 32) bfill[i] = bstart[i];
+            __syncwarp();
+            for (int e = lane; e < count; e += 32) {
+                const int f = e_key[e];
+                const int pos = atomicAdd(&bfill[(f + pshift) / (kBatchChunks * V)], 1);
+                skey[pos] = f;
+                sval[pos] = e_val[e];
+            }
+            __syncwarp();
+
+            auto load_batch = [&](int q0, uint4 (&dst)[kUnroll]) {
 #pragma unroll
                 for (int k = 0; k < kUnroll; ++k) {
                     const int q = q0 + k * 32 + lane;
-                    if (cov && q >= qf0 && q < qf1) in[k] = ld_stream(reinterpret_cast<const void*>(lpq + (uintptr_t)q * 16));
+                    if (cov && q >= qf0 && q < qf1) dst[k] = ld_stream(reinterpret_cast<const void*>(lpq + (uintptr_t)q * 16));
                 }
-                const int f_begin = q0 * V - pshift, f_end = f_begin + kBatchChunks * V;
-                for (int e = lane; e < count; e += 32) {
-                    const int f = e_key[e];
-                    if (f >= f_begin && f < f_end) {
-                        const int idx = f - f_begin;
-                        ptile[idx] = e_val[e];
-                        atomicOr(&pmark[idx / (32 * V)], 1u << ((idx / V) & 31));
-                    }
+            };
+            uint4 cur[kUnroll], nxt[kUnroll];
+            load_batch(0, cur);
+            for (int bi = 0; bi < nb; ++bi) {
+                const int q0 = bi * kBatchChunks;
+                if (bi + 1 < nb) load_batch(q0 + kBatchChunks, nxt);  // in flight while this batch computes
+                for (int e = bstart[bi] + lane; e < bstart[bi + 1]; e += 32) {
+                    const int idx = skey[e] + pshift - q0 * V;
+                    ptile[idx] = sval[e];
+                    atomicOr(&pmark[idx / (32 * V)], 1u << ((idx / V) & 31));
                 }
                 __syncwarp();
 #pragma unroll
@@ -281,45 +419,21 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
                     const bool marked = (pmark[k] >> lane) & 1u;
                     const uintptr_t c0 = qb + (uintptr_t)q * 16;
                     if (q >= qf0 && q < qf1) {
-                        float pv[V];
+                        float pn[V];
 #pragma unroll
-                        for (int i = 0; i < V; ++i) pv[i] = 0.0f;
+                        for (int i = 0; i < V; ++i) pn[i] = 0.0f;
                         if (marked) {
 #pragma unroll
                             for (int i = 0; i < V; i += 4) {
                                 const float4 v = reinterpret_cast<const float4*>(ptile + ql * V)[i / 4];
-                                pv[i] = v.x;
-                                pv[i + 1] = v.y;
-                                pv[i + 2] = v.z;
-                                pv[i + 3] = v.w;
+                                pn[i] = v.x;
+                                pn[i + 1] = v.y;
+                                pn[i + 2] = v.z;
+                                pn[i + 3] = v.w;
                                 reinterpret_cast<float4*>(ptile + ql * V)[i / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
                             }
                         }
-                        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-                        if (cov) {
-                            const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
-                            float out[V];
-#pragma unroll
-                            for (int i = 0; i < V; ++i) {
-                                float x;
-                                if constexpr (E == 4) {
-                                    x = __uint_as_float(w[i]);
-                                } else if constexpr (DT == 1) {  // bfloat16: the high half is already a float
-                                    x = __uint_as_float((i & 1) ? (w[i >> 1] & 0xffff0000u) : (w[i >> 1] << 16));
-                                } else {
-                                    x = bits_to_float<DT>((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu));
-                                }
-                                out[i] = fmaf(s, fast_ex2(x * kLog2e), -pv[i]);
-                            }
-                            if constexpr (E == 4) {
-                                o = make_uint4(__float_as_uint(out[0]), __float_as_uint(out[1]), __float_as_uint(out[2]),
-                                               __float_as_uint(out[3]));
-                            } else {
-                                o = make_uint4(pack2<DT>(out[0], out[1]), pack2<DT>(out[2], out[3]),
-                                               pack2<DT>(out[4], out[5]), pack2<DT>(out[6], out[7]));
-                            }
-                        }
-                        *reinterpret_cast<uint4*>(c0) = o;
+                        *reinterpret_cast<uint4*>(c0) = cov ? chunk_grad<DT>(cur[k], s, pn) : make_uint4(0u, 0u, 0u, 0u);
                     } else {
                         // the ragged first / last chunk of the row
                         const uintptr_t lo = c0 > g0 ? c0 : g0;
@@ -328,7 +442,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
                             const size_t f = (ad - g0) / E;
                             const float x = bits_to_float<DT>(load_elem<DT>(a0 + f * E));
                             const float pk = marked ? ptile[ql * V + (int)(f + pshift) - q * V] : 0.0f;
-                            const float gv = cov ? fmaf(s, fast_ex2(x * kLog2e), -pk) : 0.0f;
+                            const float gv = cov ? fmaf(s, fast_ex2(x * kLog2e), pk) : 0.0f;
                             store_elem<DT>(ad, pack1<DT>(gv));
                         }
                         if (marked) {
@@ -339,6 +453,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
                 __syncwarp();
                 if (lane < kBatchChunks / 32) pmark[lane] = 0u;
                 __syncwarp();
+#pragma unroll
+                for (int k = 0; k < kUnroll; ++k) cur[k] = nxt[k];
             }
             continue;
         }
@@ -405,7 +521,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
                             } else {
                                 bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
                             }
-                            out[i] = fmaf(s, fast_ex2(bits_to_float<DT>(bits) * kLog2e), -pv[i]);
+                            out[i] = fmaf(s, fast_ex2(bits_to_float<DT>(bits) * kLog2e), pv[i]);
                         }
                         if constexpr (E == 4) {
                             o = make_uint4(__float_as_uint(out[0]), __float_as_uint(out[1]), __float_as_uint(out[2]),
@@ -426,7 +542,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 3) grad_kernel(GradArg
                         }
                         const float x = bits_to_float<DT>(load_elem<DT>(a0 + (size_t)f * E));
                         const float pk = marked ? ptile[ql * V + f + pshift - q * V] : 0.0f;
-                        const float gv = row_cov[r] ? fmaf(row_scale[r], fast_ex2(x * kLog2e), -pk) : 0.0f;
+                        const float gv = row_cov[r] ? fmaf(row_scale[r], fast_ex2(x * kLog2e), pk) : 0.0f;
                         store_elem<DT>(g0 + (size_t)f * E, pack1<DT>(gv));
                         ++c;
                     }
@@ -481,8 +597,40 @@ void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& wa
     rows = k;
     entry_cap = k * ecap;
     warp_smem = 2 * align_up(4 * (size_t)k, 16) + 2 * align_up(4 * (size_t)entry_cap, 16) +
-                align_up(4 * (size_t)(L.max_U + 1), 16) + 4 * (size_t)kBatchChunks * 8 + 4 * (kBatchChunks / 32);
+                4 * (size_t)kBatchChunks * 8 + 4 * (kBatchChunks / 32) +
+                4 * 2 * (size_t)(kMaxBatches + 4) + 2 * 4 * align_up((size_t)entry_cap, 4);
     warp_smem = align_up(warp_smem, 16);
+}
+
+uint32_t grad_group_multiplier(const Layout& L) {
+    const uint32_t m = ((1u << kGroupShift) + (uint32_t)L.gpairs - 1) / (uint32_t)L.gpairs;
+    for (uint32_t j = 0; j <= (uint32_t)L.max_U + 1; ++j)
+        if (((j * m) >> kGroupShift) != j / (uint32_t)L.gpairs) return 0;
+    return m;
+}
+
+cudaError_t launch_post(const GradArgs& a, cudaStream_t s) {
+    if (a.L.T_total == 0) return cudaSuccess;
+    // as many warps per block (up to 8) as 200 KB of shared memory hold
+    const size_t warp_smem = sizeof(float) * kPostRows * align_up((size_t)a.L.max_U + 1, 4);
+    int wpb = (int)(200 * 1024 / warp_smem);
+    wpb = wpb < 1 ? 1 : (wpb > kPostThreads / 32 ? kPostThreads / 32 : wpb);
+    const size_t smem = (size_t)wpb * warp_smem;
+    cudaError_t e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, post_kernel, 32 * wpb, smem)) != cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    long long grid = (long long)sms * per_sm;
+    const long long blocks = (a.L.T_total + kPostRows - 1) / kPostRows;
+    const long long want = (blocks + wpb - 1) / wpb;
+    if (want < grid) grid = want;
+    post_kernel<<<(unsigned)grid, 32 * wpb, smem, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s) {

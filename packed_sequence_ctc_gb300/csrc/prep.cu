@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
             info.labels_ok = 1;
             info.n_owners = 1;
             info.has_nan = 0;
+            info.kint = 0;
+            info.cfrac = 0.0f;
+            info.nll_inf = (valid && T == 0 && U > 0) ? 1 : 0;
+            info.pad = 0;
             utt[b] = info;
             // utterances that need no recursion get their loss here
             if (!valid || T == 0) {
