@@ -39,7 +39,7 @@ namespace {
 
 constexpr int kMaxWarpsPerBlock = 8;
 constexpr int kPostThreads = 256;
-constexpr int kPostRows = 4;  // rows a warp of the class-sum pass walks together
+constexpr int kPostRows = 2;  // rows a warp of the class-sum pass walks together
 constexpr int kUnroll = 4;                   // 16-byte chunks in flight per lane
 constexpr int kBatchChunks = 32 * kUnroll;   // chunks a warp streams per batch
 constexpr int kMaxBatches = 40;
@@ -306,6 +306,162 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
     if (lane < kBatchChunks / 32) pmark[lane] = 0u;
     __syncwarp();
 
+    if (K == 1 && a.congruent) {
+        // One row per warp task, lp and grad congruent modulo 16.  The batches
+        // of a warp's rows form one continuous stream: the next batch, the
+        // next row's first one included, is always in flight while the current
+        // one computes, so a row's setup (header, class sums) waits on no
+        // empty pipe.  Chunk q of a row covers grad bytes [qb + 16q, +16); the
+        // ragged end chunks are read whole and stored element by element.
+        const int64_t T = a.L.T_total;
+        const uintptr_t lp_end = lp0 + (uintptr_t)T * D * E;
+        struct RowGeo {
+            uintptr_t g0, g1, qb, lpq;
+            int pshift, nq, nb;
+        };
+        auto geo = [&](int64_t row) {
+            RowGeo r;
+            r.g0 = gr0 + (uintptr_t)(row * D * E);
+            r.g1 = r.g0 + (uintptr_t)D * E;
+            r.qb = r.g0 & ~uintptr_t(15);
+            r.pshift = (int)((r.g0 - r.qb) / E);
+            r.nq = (int)((((r.g1 + 15) & ~uintptr_t(15)) - r.qb) / 16);
+            r.nb = (r.nq + kBatchChunks - 1) / kBatchChunks;
+            r.lpq = r.qb + (lp0 + (uintptr_t)(row * D * E) - r.g0);
+            return r;
+        };
+        auto load_batch = [&](const RowGeo& g, int bi, uint4 (&dst)[kUnroll]) {
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int q = bi * kBatchChunks + k * 32 + lane;
+                const uintptr_t c = g.lpq + (uintptr_t)q * 16;
+                if (q < g.nq && c >= lp0 && c + 16 <= lp_end) dst[k] = ld_stream(reinterpret_cast<const void*>(c));
+            }
+        };
+        int64_t row = (int64_t)blockIdx.x * wpb + warp;
+        if (row >= T) return;
+        RowGeo g = geo(row);
+        uint4 cur[kUnroll], nxt[kUnroll];
+        load_batch(g, 0, cur);
+        for (;;) {
+            // the row's header and class sums, bucketed by batch
+            const RowHead h = head[row];
+            const int2* er = ent + row * a.L.ecap;
+            const int count = h.count;
+            const bool cov = h.covered != 0;
+            const float s = h.scale;
+            for (int i = lane; i <= g.nb; i += 32) bfill[i] = 0;
+            __syncwarp();
+            for (int e = lane; e < count; e += 32) atomicAdd(&bfill[(er[e].x + g.pshift) / (kBatchChunks * V)], 1);
+            __syncwarp();
+            {
+                int run = 0;
+                for (int base = 0; base <= g.nb; base += 32) {
+                    const int i = base + lane;
+                    const int c = i < g.nb ? bfill[i] : 0;
+                    int x = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    if (i <= g.nb) bstart[i] = run + x - c;
+                    run += __shfl_sync(0xffffffffu, x, 31);
+                }
+            }
+            __syncwarp();
+            for (int i = lane; i < g.nb; i += 32) bfill[i] = bstart[i];
+            __syncwarp();
+            for (int e = lane; e < count; e += 32) {
+                const int2 v = er[e];
+                const int pos = atomicAdd(&bfill[(v.x + g.pshift) / (kBatchChunks * V)], 1);
+                skey[pos] = v.x;
+                sval[pos] = __int_as_float(v.y);
+            }
+            __syncwarp();
+
+            const int64_t nrow = row + warps;
+            RowGeo gn = g;
+            if (nrow < T) gn = geo(nrow);
+            for (int bi = 0; bi < g.nb; ++bi) {
+                if (bi + 1 < g.nb) {
+                    load_batch(g, bi + 1, nxt);
+                } else if (nrow < T) {
+                    load_batch(gn, 0, nxt);
+                }
+                const int q0 = bi * kBatchChunks;
+                for (int e = bstart[bi] + lane; e < bstart[bi + 1]; e += 32) {
+                    const int idx = skey[e] + g.pshift - q0 * V;
+                    ptile[idx] = sval[e];
+                    atomicOr(&pmark[idx / (32 * V)], 1u << ((idx / V) & 31));
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < kUnroll; ++k) {
+                    const int q = q0 + k * 32 + lane;
+                    if (q >= g.nq) continue;
+                    const int ql = k * 32 + lane;
+                    const bool marked = (pmark[k] >> lane) & 1u;
+                    const uintptr_t c0 = g.qb + (uintptr_t)q * 16;
+                    const uintptr_t cl = g.lpq + (uintptr_t)q * 16;
+                    float pn[V];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) pn[i] = 0.0f;
+                    if (marked) {
+#pragma unroll
+                        for (int i = 0; i < V; i += 4) {
+                            const float4 v = reinterpret_cast<const float4*>(ptile + ql * V)[i / 4];
+                            pn[i] = v.x;
+                            pn[i + 1] = v.y;
+                            pn[i + 2] = v.z;
+                            pn[i + 3] = v.w;
+                            reinterpret_cast<float4*>(ptile + ql * V)[i / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                    if (c0 >= g.g0 && c0 + 16 <= g.g1) {
+                        *reinterpret_cast<uint4*>(c0) = cov ? chunk_grad<DT>(cur[k], s, pn) : make_uint4(0u, 0u, 0u, 0u);
+                    } else if (cl >= lp0 && cl + 16 <= lp_end) {
+                        // a ragged end chunk, read whole: store only the row's elements
+                        const uint4 o = cov ? chunk_grad<DT>(cur[k], s, pn) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                        for (int i = 0; i < V; ++i) {
+                            const uintptr_t ad = c0 + (uintptr_t)i * E;
+                            if (ad >= g.g0 && ad < g.g1) {
+                                if constexpr (E == 4) {
+                                    store_elem<DT>(ad, w[i]);
+                                } else {
+                                    store_elem<DT>(ad, (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu));
+                                }
+                            }
+                        }
+                    } else {
+                        // a ragged chunk at an end of the lp buffer: element by element
+                        const uintptr_t lo = c0 > g.g0 ? c0 : g.g0;
+                        const uintptr_t hi = c0 + 16 < g.g1 ? c0 + 16 : g.g1;
+                        for (uintptr_t ad = lo; ad < hi; ad += E) {
+                            const float x = bits_to_float<DT>(load_elem<DT>(cl + (ad - c0)));
+                            const int i = (int)((ad - c0) / E);
+                            float pk = 0.0f;  // pn[i], selected without dynamic indexing
+#pragma unroll
+                            for (int ii = 0; ii < V; ++ii) pk = ii == i ? pn[ii] : pk;
+                            const float gv = cov ? fmaf(s, fast_ex2(x * kLog2e), pk) : 0.0f;
+                            store_elem<DT>(ad, pack1<DT>(gv));
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane < kBatchChunks / 32) pmark[lane] = 0u;
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < kUnroll; ++k) cur[k] = nxt[k];
+            }
+            if (nrow >= T) break;
+            row = nrow;
+            g = gn;
+        }
+        return;
+    }
     for (int64_t grp = (int64_t)blockIdx.x * wpb + warp; grp < n_groups; grp += warps) {
         const int64_t r0 = grp * K;
         const int nrows = (int)min((int64_t)K, a.L.T_total - r0);
