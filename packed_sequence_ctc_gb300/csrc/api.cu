@@ -164,8 +164,7 @@ const char* ctc_packed_status_string(ctc_packed_status status) {
 namespace ctcp {
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
-    prep_kernel<<<1, 1024, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prep_kernel, dim3(1), dim3(1024), 0, s, a);
 }
 
 }  // namespace ctcp

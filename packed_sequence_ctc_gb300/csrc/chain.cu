@@ -483,6 +483,8 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const int32_t* queue = ws_at<int32_t>(a.ws, a.L.off_queue);
     const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
+    pdl_wait();     // queue, metadata and emission matrix from the earlier kernels
+    pdl_trigger();  // persistent grid: every CTA is already resident
     const int NT = blockDim.x, NW = NT >> 5;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     XP* rings = reinterpret_cast<XP*>(smem_raw);
@@ -577,8 +579,7 @@ static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
     long long want = 2ll * a.L.B;
     long long grid = (long long)sms * per_sm;
     if (want < grid) grid = want > 0 ? want : 1;
-    chain_kernel<P><<<(unsigned)grid, 32 * nw, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(chain_kernel<P>, dim3((unsigned)grid), dim3(32 * nw), smem, s, a);
 }
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s) {

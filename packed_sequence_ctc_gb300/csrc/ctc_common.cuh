@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -336,5 +337,33 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 __device__ __forceinline__ void set_status(Control* ctrl, uint32_t bits) { atomicOr(&ctrl->status, bits); }
+
+// ------------------------------------------------ programmatic dependent launch
+//
+// Every kernel is launched with programmatic stream serialization, so it can
+// be scheduled while the kernel before it on the stream drains.  pdl_wait()
+// blocks until that kernel has completed and its writes are visible (a no-op
+// when launched without the attribute); it comes before anything that reads
+// what the stream's earlier work wrote.  pdl_trigger() lets the next kernel's
+// blocks be scheduled from now on; only kernels whose blocks are all resident
+// from the start (persistent grids, one-CTA kernels) call it early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace ctcp

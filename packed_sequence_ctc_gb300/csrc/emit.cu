@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
     XP2* em = ws_at<XP2>(a.ws, em_base(a.L));
     const int64_t r0 = (int64_t)blockIdx.x * kEmitRows;
     const int tid = threadIdx.x;
+    pdl_wait();  // utterance metadata from the prep kernel
     if (tid == 0) s_maxw = 0;
     __syncthreads();
     if (tid < kEmitRows) {
@@ -129,10 +130,9 @@ cudaError_t launch_emit(const ChainArgs& a, int dtype, cudaStream_t s) {
     if (a.L.T_total == 0 || a.L.B == 0) return cudaSuccess;
     const int64_t grid = (a.L.T_total + kEmitRows - 1) / kEmitRows;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    if (dtype == 0) emit_kernel<0><<<(unsigned)grid, kEmitThreads, 0, s>>>(a);
-    else if (dtype == 1) emit_kernel<1><<<(unsigned)grid, kEmitThreads, 0, s>>>(a);
-    else emit_kernel<2><<<(unsigned)grid, kEmitThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    if (dtype == 0) return launch_pdl(emit_kernel<0>, dim3((unsigned)grid), dim3(kEmitThreads), 0, s, a);
+    if (dtype == 1) return launch_pdl(emit_kernel<1>, dim3((unsigned)grid), dim3(kEmitThreads), 0, s, a);
+    return launch_pdl(emit_kernel<2>, dim3((unsigned)grid), dim3(kEmitThreads), 0, s, a);
 }
 
 }  // namespace ctcp

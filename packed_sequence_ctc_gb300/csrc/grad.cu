@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(kPostThreads) post_kernel(GradArgs a) {
     RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
     int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
     const uint32_t gp_mul = a.gp_mul;  // j / gpairs == (j * gp_mul) >> kGroupShift for every pair j
+    pdl_wait();     // the forward's stored rows and metadata
+    pdl_trigger();  // persistent grid: every block is already resident
     const bool ready = ctrl->grad_ready != 0;
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.L.T_total > 0 && !ready)
         set_status(ctrl, CTC_PACKED_DEV_NO_GRAD_STATE);
@@ -305,6 +307,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
     for (int i = lane; i < kBatchChunks * V; i += 32) ptile[i] = 0.0f;
     if (lane < kBatchChunks / 32) pmark[lane] = 0u;
     __syncwarp();
+    pdl_wait();     // the class sums of the pass before
+    pdl_trigger();  // persistent grid: every block is already resident
 
     if (K == 1 && a.congruent) {
         // One row per warp task, lp and grad congruent modulo 16.  The batches
@@ -739,8 +743,7 @@ static cudaError_t launch_grad_t(const GradArgs& a, cudaStream_t s) {
     const long long want = (a.n_tiles + wpb - 1) / wpb;
     if (want < grid) grid = want;
     if (grid < 1) return cudaSuccess;
-    grad_kernel<DT><<<(unsigned)grid, wpb * 32, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(grad_kernel<DT>, dim3((unsigned)grid), dim3(wpb * 32), smem, s, a);
 }
 
 // Rows per warp group and the shared memory each warp needs.
@@ -785,8 +788,7 @@ cudaError_t launch_post(const GradArgs& a, cudaStream_t s) {
     const long long blocks = (a.L.T_total + kPostRows - 1) / kPostRows;
     const long long want = (blocks + wpb - 1) / wpb;
     if (want < grid) grid = want;
-    post_kernel<<<(unsigned)grid, 32 * wpb, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(post_kernel, dim3((unsigned)grid), dim3(32 * wpb), smem, s, a);
 }
 
 cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s) {

@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
     double* nll = ws_at<double>(a.ws, a.L.off_nll);
     const int B = a.L.B;
     const int tid = threadIdx.x;
+    pdl_wait();     // the stream's earlier work may still use this workspace
+    pdl_trigger();  // one CTA: the emission gather's blocks may queue up behind it
 
     if (tid == 0) {
         ctrl->status = 0;
