@@ -41,12 +41,20 @@ __device__ __forceinline__ int utterance_of_row(const int32_t* cu, int B, int64_
     return ans;
 }
 
+// One log probability.  The loads are scattered, so each asks L2 to fetch
+// only the 64-byte segment around it from DRAM (the default fetch is larger
+// and mostly wasted here).
 template <int DT>
 __device__ __forceinline__ float load_lp(const void* lp, int64_t idx) {
     if constexpr (DT == 0) {
-        return __ldg(reinterpret_cast<const float*>(lp) + idx);
+        const float* p = reinterpret_cast<const float*>(lp) + idx;
+        float v;
+        asm volatile("ld.global.nc.L2::64B.f32 %0, [%1];" : "=f"(v) : "l"(p));
+        return v;
     } else {
-        const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(lp) + idx);
+        const unsigned short* p = reinterpret_cast<const unsigned short*>(lp) + idx;
+        unsigned short h;
+        asm volatile("ld.global.nc.L2::64B.u16 %0, [%1];" : "=h"(h) : "l"(p));
         return bits_to_float<DT>((uint32_t)h);
     }
 }
