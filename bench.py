@@ -7,8 +7,9 @@ N(0, 3^2) logits, reduction none.  Its 638 MB of log probabilities exceed the
 129 MB L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0): frames/s over the whole job, the roofline of
-the dominant kernel (the gradient kernel, timed live with CUDA events on its
-stream), the whole-path roofline, an end-to-end figure through the C-ABI with
+the dominant work (the backward call: its class-sum and gradient kernels,
+timed live with CUDA events on their stream), the whole-path roofline, an
+end-to-end figure through the C-ABI with
 host buffers, the SM clocks sampled during the timed region, and the fp64
 CPU oracle timed on a bounded sample on this host.
 
@@ -41,15 +42,16 @@ L2_BYTES = 129 * 2**20
 
 
 def _profiled_traffic(workload):
-    """DRAM bytes per launch of the gradient kernel from the committed ncu
-    summary, while the kernel source still matches the one profiled."""
+    """DRAM bytes of one backward call (class-sum and gradient kernels) from
+    the committed ncu summary, while their source still matches the one
+    profiled."""
     import hashlib
     import re
 
     if workload != "largevocab":
         return None
     try:
-        text = open(os.path.join(ROOT, "profiles", "grad_kernel_largevocab.md")).read()
+        text = open(os.path.join(ROOT, "profiles", "backward_largevocab.md")).read()
         src = open(os.path.join(ROOT, "packed_sequence_ctc_gb300", "csrc", "grad.cu"), "rb").read()
     except OSError:
         return None
