@@ -271,6 +271,21 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def job_throughput(total_ms, steps, frames_per_rank, world, device="cpu"):
+    """Whole-job throughput of a timed region: the slowest rank's time (a max
+    over ranks when world > 1, so every rank must call this) and the frames
+    of all ranks.  Returns (ms per step, frames per second)."""
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        tt = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, frames_per_rank * world / (ms_per_step / 1e3)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -349,13 +364,7 @@ def run_ours(args):
     sampler.stop()
     clocks = sampler.summary(t0, t1)
 
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    ms_per_step = total_ms / K
-    frames_all = batch.frames * world
-    value = frames_all / (ms_per_step / 1e3)
+    ms_per_step, value = job_throughput(total_ms, K, batch.frames, world, dev)
 
     hbm_peak, peak_kind = _peaks()
     ab = algorithmic_bytes(batch)
