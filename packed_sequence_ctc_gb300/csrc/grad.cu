@@ -42,8 +42,8 @@ constexpr int kPostThreads = 256;
 constexpr int kPostRows = 2;  // rows a warp of the class-sum pass walks together
 constexpr int kUnroll = 4;                   // 16-byte chunks in flight per lane
 constexpr int kBatchChunks = 32 * kUnroll;   // chunks a warp streams per batch
-constexpr int kMaxBatches = 40;
-constexpr int kGroupShift = 21;             // offset group of pair j: (j * gp_mul) >> kGroupShift              // batches of one row (D <= 16384, 4-byte elements: 33)
+constexpr int kMaxBatches = 40;              // batches of one row (D <= 16384, 4-byte elements: 33)
+constexpr int kGroupShift = 21;             // offset group of pair j: (j * gp_mul) >> kGroupShift
 
 __device__ __forceinline__ int find_utterance(const int32_t* cu, int B, int64_t row) {
     int lo = 0, hi = B - 1, ans = -1;
@@ -68,6 +68,15 @@ __device__ __forceinline__ float posterior(int va, int vb, int base, float c) {
     const float mb = __int_as_float(((vb & 0x7ffff) << 4) | 0x3f800000);
     const int n = min(max((va >> kFixFrac) + (vb >> kFixFrac) + base, -200), 64);
     return __int_as_float(max(__float_as_int(ma * mb * c) + (n << 23), 0));
+}
+
+// Asks L2 to fetch bytes [lo, hi) ahead of use, rounded inward to 16 bytes
+// (a bulk prefetch is a hint: it holds no register and completes nothing).
+__device__ __forceinline__ void prefetch_l2(uintptr_t lo, uintptr_t hi) {
+    lo = (lo + 15) & ~uintptr_t(15);
+    hi &= ~uintptr_t(15);
+    if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
 }
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -387,6 +396,13 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
             const int64_t nrow = row + warps;
             RowGeo gn = g;
             if (nrow < T) gn = geo(nrow);
+            // the whole row is requested from DRAM at once, while its first
+            // batch is already in flight (measured: fetching further ahead, a
+            // row or a few batches, is slower)
+            if (lane == 0) {
+                const uintptr_t lo = lp0 + (uintptr_t)(row * D * E);
+                prefetch_l2(lo, lo + (uintptr_t)D * E);
+            }
             for (int bi = 0; bi < g.nb; ++bi) {
                 if (bi + 1 < g.nb) {
                     load_batch(g, bi + 1, nxt);
