@@ -62,13 +62,13 @@ template <int P>
 struct ChainShape {
     static constexpr int G = ghost_lanes(P);  // shadow lanes per warp
     static constexpr int GP = group_pairs(P); // pairs a warp owns
-    static constexpr int F = G * P;           // frames between halo exchanges (4 for every P)
+    static constexpr int F = G * P;           // frames between halo exchanges (8, 4, 4)
     static constexpr int R = P == 1 ? 8 : 4;  // emission frames in flight per warp
     // extended values per lane and frame in the ring: (label 0, blank), the
     // other labels, padded to 16 bytes
     static constexpr int LW = 2 * ((P + 2) / 2);
     static constexpr int XW = G * P * 2;      // extended values one warp sends per exchange
-    static_assert(F == 4, "frames are run in blocks of one exchange period");
+    static_assert(F <= 8, "between renormalisations a mantissa grows at most 12x a frame");
     static_assert(R % F == 0, "a block of frames maps onto consecutive ring slots");
 };
 
@@ -103,7 +103,7 @@ struct ItemCtx {
 
 // One chain (DIR 0 alpha, 1 beta) of utterance b, run by warp c.w of c.nw.
 //
-// Frame 0 is the initialisation; frames 1.. run in blocks of F = 4: each
+// Frame 0 is the initialisation; frames 1.. run in blocks of F: each
 // frame is one recursion step on shuffles alone, the row of the frame
 // before is encoded and stored on the side, and the emissions of the frame
 // R - 1 ahead are requested.  After a block the states are renormalised
@@ -324,7 +324,7 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         }
     }
 
-    // full blocks: frames i0 .. i0+3, i0 = 1 mod 4, in slots base .. base+3;
+    // full blocks: frames i0 .. i0+F-1, i0 = 1 mod F, in slots base .. base+F-1;
     // the request made at frame i goes to frame i-1's slot
     int i0 = 1;
 #pragma unroll 1
@@ -342,7 +342,7 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         renormalise();
         if (multi) exchange((i0 - 1) / S::F);
     }
-    // the last frames (fewer than 4: no exchange needed)
+    // the last frames (fewer than F: no exchange needed)
 #pragma unroll 1
     for (int i = i0; i < T; ++i) {
         cp_async_wait<S::R - 2>();

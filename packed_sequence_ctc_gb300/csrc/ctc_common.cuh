@@ -82,16 +82,19 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // check (those rows are never consumed).
 constexpr int kEmPad = 8;
 
+// Lanes of a chain warp that shadow the neighbouring warp's edge pairs, so
+// the warp runs ghost_lanes(P) * P frames between two halo exchanges: 8, 4
+// and 4 frames.  (Measured with one pair per lane on the 8193-class
+// workload: 8 shadow lanes beat 4, 2 and 16; fewer frames per exchange pay
+// for more barriers, more shadow lanes for more warps.)
+__host__ __device__ constexpr int ghost_lanes(int P) { return P == 1 ? 8 : P == 2 ? 2 : 1; }
+__host__ __device__ constexpr int group_pairs(int P) { return (32 - ghost_lanes(P)) * P; }
 // State pairs (blank, label) each lane of a chain warp holds, from the target
-// bound; a warp owns (32 - ghost lanes) * P pairs and at most 32 warps run a chain.
+// bound; a warp owns group_pairs(P) pairs and at most 32 warps run a chain.
 __host__ __device__ inline int pairs_for_max_u(int max_u) {
     const int pairs = max_u + 1;
-    return pairs <= 28 * 32 ? 1 : pairs <= 30 * 2 * 32 ? 2 : 4;
+    return pairs <= group_pairs(1) * 32 ? 1 : pairs <= group_pairs(2) * 32 ? 2 : 4;
 }
-// Lanes of a chain warp that shadow the neighbouring warp's edge pairs, so
-// the warp runs ghost_lanes(P) * P frames between two halo exchanges.
-__host__ __device__ constexpr int ghost_lanes(int P) { return P == 1 ? 4 : P == 2 ? 2 : 1; }
-__host__ __device__ constexpr int group_pairs(int P) { return (32 - ghost_lanes(P)) * P; }
 
 __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_t max_U, int32_t D) {
     Layout L{};

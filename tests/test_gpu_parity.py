@@ -174,9 +174,11 @@ def test_odd_class_counts(cuda_device, D, dtype):
     assert_grad_close(grad, ref_grad, dtype, rows=_defined_rows(batch, nll))
 
 
-# a chain warp owns 28 state pairs (4 of its 32 lanes shadow the neighbour):
-# targets of 27/28 labels switch from one warp to several, 55/56 from 2 to 3
-@pytest.mark.parametrize("U", [26, 27, 28, 29, 30, 31, 32, 33, 55, 56, 57, 63, 64, 65, 84, 200, 511, 1000])
+# a chain warp owns 24 state pairs (8 of its 32 lanes shadow the neighbour):
+# targets of 23/24 labels switch from one warp to several, 47/48 from 2 to 3,
+# 71/72 from 3 to 4
+@pytest.mark.parametrize("U", [22, 23, 24, 25, 26, 27, 28, 29, 30, 31, 32, 33, 46, 47, 48, 49, 55, 56, 57, 63, 64, 65,
+                               71, 72, 84, 200, 511, 767, 768, 1000])
 def test_state_counts_across_warp_boundaries(cuda_device, U):
     T = 2 * U + 37
     batch = workloads.make_batch([T, T // 2 + 3, 11], [U, min(U, T // 4), 3], 40, seed=U, repeat_prob=0.2,
@@ -189,7 +191,7 @@ def test_state_counts_across_warp_boundaries(cuda_device, U):
 
 
 def test_two_pairs_per_thread(cuda_device):
-    # a target bound above 895 puts two state pairs in each lane
+    # a target bound above 767 puts two state pairs in each lane
     batch = workloads.make_batch([2600, 300, 50], [1200, 60, 10], 48, seed=5, reduction="sum")
     loss, grad, status = run_gpu(batch, max_target_len=1500)
     assert status == 0
