@@ -68,6 +68,11 @@ struct ChainShape {
     // other labels, padded to 16 bytes
     static constexpr int LW = 2 * ((P + 2) / 2);
     static constexpr int XW = G * P * 2;      // extended values one warp sends per exchange
+    // One-pair chains stage a block's encoded rows in shared memory and write
+    // them out together after the block; the others store each row as it is
+    // made (their rings leave no room for a stage at 31 warps).
+    static constexpr bool kStaged = P == 1;
+    static constexpr int kStageInts = kStaged ? F * 32 * 2 * P : 0;  // per warp
     static_assert(F <= 8, "between renormalisations a mantissa grows at most 12x a frame");
     static_assert(R % F == 0, "a block of frames maps onto consecutive ring slots");
 };
@@ -99,6 +104,7 @@ struct ItemCtx {
     XP* ring;  // this warp's emission ring
     XP* xch;   // halo exchange buffers, [2][nw][XW]
     XP* fin;   // 2 extended values shared by the item's warps
+    int* stage;  // this warp's encoded rows of one block of frames (one-pair chains)
 };
 
 // One chain (DIR 0 alpha, 1 beta) of utterance b, run by warp c.w of c.nw.
@@ -189,16 +195,27 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         for (int p = 1; p < P; ++p) el[p] = e[p + 1];
     };
 
-    // stored rows, written one frame late
+    // stored rows, written one frame late: row k of the chain (frame k) is
+    // packed row row0 + k (alpha) or row0 - k (beta)
     const bool store_me = own && j0 <= U;
-    int* st = ws_at<int>(a.ws, DIR == 0 ? a.L.off_alpha : a.L.off_beta) + row0 * a.L.pitch + 2 * max(j0, 0);
+    int* const st_base = ws_at<int>(a.ws, DIR == 0 ? a.L.off_alpha : a.L.off_beta);
+    int* st = st_base + row0 * a.L.pitch + 2 * max(j0, 0);
     const intptr_t st_step = (DIR == 0 ? 1 : -1) * (intptr_t)a.L.pitch;
-    int32_t* offp = ws_at<int32_t>(a.ws, DIR == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo + c.w;
+    int32_t* const off_base = ws_at<int32_t>(a.ws, DIR == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo + c.w;
+    int32_t* offp = off_base;
     const intptr_t off_step = (DIR == 0 ? 1 : -1) * (intptr_t)a.L.nwo;
+    // the warp's own pairs [p0, p0 + np) are contiguous in the row and, in the
+    // stage, from lane `lane0` on; written in 16-byte chunks of two pairs
+    // (an odd count also writes pair U + 1, which the row's pitch holds and
+    // no reader uses)
+    const int p0 = c.w * S::GP, np = min(S::GP, U + 1 - p0), nch = (np + 1) >> 1;
+    const int lane0 = DIR == 0 ? S::G : 0;
+    const uint32_t ch_mul = (65536u + (uint32_t)nch - 1) / (uint32_t)max(nch, 1);  // c / nch for c < 256
+    int a_hold = 0;  // lane q: the offset of the block's row q
     // alpha rows: (blank, label) sums before the emission; beta: (label, blank) after it
     float rx[P], ry[P];
     int ex[P], ey[P];
-    auto flush_row = [&]() {
+    auto flush_row = [&](int slot) {
         int emax = kEZero;
 #pragma unroll
         for (int p = 0; p < P; ++p) emax = max(emax, max(ex[p], ey[p]));
@@ -209,18 +226,35 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             x[p] = enc_state(rx[p], ex[p], A);
             y[p] = enc_state(ry[p], ey[p], A);
         }
-        if (store_me) {
-            if constexpr (P == 1) {
-                *reinterpret_cast<int2*>(st) = make_int2(x[0], y[0]);
-            } else {
+        if constexpr (S::kStaged) {
+            reinterpret_cast<int2*>(c.stage)[slot * 32 + lane] = make_int2(x[0], y[0]);
+            if (lane == slot) a_hold = A;
+        } else {
+            if (store_me) {
 #pragma unroll
                 for (int p = 0; p < P; p += 2)
                     *reinterpret_cast<int4*>(st + 2 * p) = make_int4(x[p], y[p], x[p + 1], y[p + 1]);
             }
+            if (lane == 0) *offp = A;
+            st += st_step;
+            offp += off_step;
         }
-        if (lane == 0) *offp = A;
-        st += st_step;
-        offp += off_step;
+    };
+    // rows k0 .. k0 + n - 1 of the chain, staged in slots 0 .. n - 1: the
+    // warp's segments as 16-byte chunks spread over all lanes, and the offsets
+    auto write_rows = [&](int k0, int n) {
+        if constexpr (S::kStaged) {
+            __syncwarp();
+            const int total = n * nch;
+            for (int cq = lane; cq < total; cq += 32) {
+                const int r = (int)(((uint32_t)cq * ch_mul) >> 16), k = cq - r * nch;
+                const int4 v = reinterpret_cast<const int4*>(c.stage + r * 64 + 2 * lane0)[k];
+                const int64_t row = row0 + (DIR == 0 ? (int64_t)(k0 + r) : -(int64_t)(k0 + r));
+                reinterpret_cast<int4*>(st_base + row * a.L.pitch + 2 * p0)[k] = v;
+            }
+            if (lane < n) off_base[(intptr_t)(k0 + lane) * off_step] = a_hold;
+            __syncwarp();
+        }
     };
 
     XP vb[P], vl[P];  // alpha (blank 2j, label 2j+1) / beta (label 2j-1, blank 2j)
@@ -336,11 +370,12 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             XP el[P], eb;
             emissions(base + q, el, eb);
             request((base + q + S::R - 1) & (S::R - 1), i0 + q + S::R - 1);
-            flush_row();  // frame i0 + q - 1
+            flush_row(q);  // frame i0 + q - 1
             step(el, eb);
         }
         renormalise();
         if (multi) exchange((i0 - 1) / S::F);
+        write_rows(i0 - 1, S::F);
     }
     // the last frames (fewer than F: no exchange needed)
 #pragma unroll 1
@@ -350,10 +385,11 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         const uint32_t slot = (uint32_t)((i - 1) & (S::R - 1));
         emissions(slot, el, eb);
         request((slot + S::R - 1) & (S::R - 1), i + S::R - 1);
-        flush_row();
+        flush_row(i - i0);  // frame i - 1
         step(el, eb);
     }
-    flush_row();  // frame T - 1 (T >= 1 for every queued item)
+    flush_row(T - i0);  // frame T - 1 (T >= 1 for every queued item)
+    write_rows(i0 - 1, T - i0 + 1);
     cp_async_wait<0>();
     renormalise();
 
@@ -473,8 +509,12 @@ __device__ void run_label_item(const ChainArgs& a, int b, int lane) {
 
 }  // namespace
 
-template <int P>
-__global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
+// MAXT: the most threads a CTA launches with.  An item of up to 8 warps runs
+// under a 256-thread bound, which leaves the compiler room for ~120
+// registers a thread instead of 64 (measured: 13 us faster on the 8193-class
+// workload's 8-warp chains).
+template <int P, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
     using S = ChainShape<P>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_item;
@@ -491,6 +531,8 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
     XP* xch = rings + NW * S::R * 32 * S::LW;
     XP* fins = xch + 2 * NW * S::XW;
     XP* my_ring = rings + warp * S::R * 32 * S::LW;
+    // stages after the 2 * NW fin values, on a 16-byte boundary
+    int* my_stage = reinterpret_cast<int*>(fins + 2 * NW) + warp * S::kStageInts;
     const int n_big = ctrl->n_big, n_small = ctrl->n_small, n_lab = ctrl->n_lab;
 
     // 1. multi-warp chains, longest first, one at a time per CTA
@@ -503,7 +545,7 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
         const int item = queue[k];
         const int U = utt[item >> 1].U;
         const int nw = min(NW, (U + 1 + S::GP - 1) / S::GP);
-        if (warp < nw) run_item<P>(a, item, ItemCtx{warp, nw, my_ring, xch, fins});
+        if (warp < nw) run_item<P>(a, item, ItemCtx{warp, nw, my_ring, xch, fins, my_stage});
     }
     // 2. single-warp chains, each warp on its own
     for (;;) {
@@ -511,7 +553,7 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
         if (lane == 0) k = (int)atomicAdd(&ctrl->small_head, 1u);
         k = __shfl_sync(0xffffffffu, k, 0);
         if (k >= n_small) break;
-        run_item<P>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp});
+        run_item<P>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp, my_stage});
     }
     // 3. label metadata for the backward
     for (;;) {
@@ -552,41 +594,46 @@ __global__ void __launch_bounds__(1024, 1) chain_kernel(ChainArgs a) {
     }
 }
 
-template __global__ void chain_kernel<1>(ChainArgs);
-template __global__ void chain_kernel<2>(ChainArgs);
-template __global__ void chain_kernel<4>(ChainArgs);
+template __global__ void chain_kernel<1, 256>(ChainArgs);
+template __global__ void chain_kernel<1, 1024>(ChainArgs);
+template __global__ void chain_kernel<2, 1024>(ChainArgs);
+template __global__ void chain_kernel<4, 1024>(ChainArgs);
 
-template <int P>
+template <int P, int MAXT>
 static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
     using S = ChainShape<P>;
     const int nw = a.L.nwo;  // warps for the longest possible target
-    const size_t smem = sizeof(XP) * ((size_t)nw * S::R * 32 * S::LW + 2 * (size_t)nw * S::XW + 2 * (size_t)nw);
-    static int configured_smem = -1;
+    const size_t smem = sizeof(XP) * ((size_t)nw * S::R * 32 * S::LW + 2 * (size_t)nw * S::XW + 2 * (size_t)nw) +
+                        sizeof(int) * (size_t)nw * S::kStageInts;
     cudaError_t e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((int)smem > configured_smem) {
-        e = cudaFuncSetAttribute(chain_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the dynamic shared memory bound is set per device, and only raised
+    constexpr int kMaxDevices = 64;
+    static int configured_smem[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices || (int)smem > configured_smem[dev]) {
+        e = cudaFuncSetAttribute(chain_kernel<P, MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured_smem = (int)smem;
+        if (dev >= 0 && dev < kMaxDevices) configured_smem[dev] = (int)smem;
     }
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P>, 32 * nw, smem)) != cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P, MAXT>, 32 * nw, smem)) !=
+        cudaSuccess)
         return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     // persistent grid: enough CTAs for every item, never more than fit at once
     long long want = 2ll * a.L.B;
     long long grid = (long long)sms * per_sm;
     if (want < grid) grid = want > 0 ? want : 1;
-    return launch_pdl(chain_kernel<P>, dim3((unsigned)grid), dim3(32 * nw), smem, s, a);
+    return launch_pdl(chain_kernel<P, MAXT>, dim3((unsigned)grid), dim3(32 * nw), smem, s, a);
 }
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s) {
     switch (pairs_for_max_u(a.L.max_U)) {
-        case 1: return launch_chain_t<1>(a, s);
-        case 2: return launch_chain_t<2>(a, s);
-        default: return launch_chain_t<4>(a, s);
+        case 1: return a.L.nwo <= 8 ? launch_chain_t<1, 256>(a, s) : launch_chain_t<1, 1024>(a, s);
+        case 2: return launch_chain_t<2, 1024>(a, s);
+        default: return launch_chain_t<4, 1024>(a, s);
     }
 }
 

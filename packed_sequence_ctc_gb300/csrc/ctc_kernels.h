@@ -56,7 +56,7 @@ struct GradArgs {
 __global__ void prep_kernel(PrepArgs a);
 template <int DT>
 __global__ void emit_kernel(ChainArgs a);
-template <int P>
+template <int P, int MAXT>
 __global__ void chain_kernel(ChainArgs a);
 __global__ void post_kernel(GradArgs a);
 template <int DT>
