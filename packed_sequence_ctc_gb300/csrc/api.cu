@@ -164,7 +164,11 @@ const char* ctc_packed_status_string(ctc_packed_status status) {
 namespace ctcp {
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
-    return launch_pdl(prep_kernel, dim3(1), dim3(1024), 0, s, a);
+    // one thread per utterance, in whole warps (64 to 1024): the kernel is a
+    // chain of CTA barriers, which cost more the more warps take part
+    int nt = (a.L.B + 31) / 32 * 32;
+    nt = nt < 64 ? 64 : (nt > 1024 ? 1024 : nt);
+    return launch_pdl(prep_kernel, dim3(1), dim3(nt), 0, s, a);
 }
 
 }  // namespace ctcp

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
     int32_t* queue = ws_at<int32_t>(a.ws, a.L.off_queue);
     double* nll = ws_at<double>(a.ws, a.L.off_nll);
     const int B = a.L.B;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, nt = blockDim.x;
     pdl_wait();     // the stream's earlier work may still use this workspace
     pdl_trigger();  // one CTA: the emission gather's blocks may queue up behind it
 
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
     //    label-metadata offsets (valid lengths plus one blank slot each)
     uint32_t bad_bits = 0;
     int toff_base = 0, moff_base = 0;
-    for (int base = 0; base < B; base += kPrepThreads) {
+    for (int base = 0; base < B; base += nt) {
         const int b = base + tid;
         int T = 0, U = 0, start = 0, valid = 0, uraw = 0;
         if (b < B) {
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
     if (sorted) {
         int n = 1;
         while (n < B) n <<= 1;
-        for (int i = tid; i < n; i += kPrepThreads) {
+        for (int i = tid; i < n; i += nt) {
             if (i < B) {
                 const UttInfo& u = utt[i];
                 const int key = (u.valid && u.T > 0) ? u.T : -1;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
         __syncthreads();
         for (int k = 2; k <= n; k <<= 1) {
             for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int i = tid; i < n; i += kPrepThreads) {
+                for (int i = tid; i < n; i += nt) {
                     const int ixj = i ^ j;
                     if (ixj > i) {
                         const long long x = s_keys[i], y = s_keys[ixj];
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
     int big_base = 0, small_base = 0, lab_base = 0;
     // first pass counts the big items, so the small ones can follow them
     int n_big = 0;
-    for (int base = 0; base < B; base += kPrepThreads) {
+    for (int base = 0; base < B; base += nt) {
         const int i = base + tid;
         int is_big = 0;
         if (i < B) {
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
         n_big += t;
     }
     const int per = a.need_grad ? 2 : 1;
-    for (int base = 0; base < B; base += kPrepThreads) {
+    for (int base = 0; base < B; base += nt) {
         const int i = base + tid;
         int b = -1, is_big = 0, is_small = 0, is_lab = 0;
         if (i < B) {
