@@ -5,5 +5,5 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU baseline leg of
 library and never imports it.
 """
 
-from .ctc_oracle import (build, ctc_loss_packed, max_threads, oracle_batch, raw_nll_and_grad,  # noqa: F401
-                         reduce_losses, utterance_scales)
+from .ctc_oracle import (build, ctc_loss_packed, ctc_loss_packed_logits, log_softmax_rows,  # noqa: F401
+                         max_threads, oracle_batch, raw_nll_and_grad, reduce_losses, utterance_scales)

@@ -177,6 +177,37 @@ def ctc_loss_packed(log_probs, cu_seqlens, lengths, targets, target_lengths, bla
     return loss, grad, nll
 
 
+def log_softmax_rows(logits) -> np.ndarray:
+    """Row-wise log_softmax in float64: ``z - max - log(sum(exp(z - max)))``
+    over the class axis (a row of -inf stays NaN, as log_softmax gives)."""
+    z = _as_f64(logits)
+    if z.ndim != 2:
+        raise ValueError("logits must be (T_total, D)")
+    with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+        m = z.max(axis=1, keepdims=True) if z.shape[1] else np.zeros((z.shape[0], 1))
+        return z - m - np.log(np.exp(z - m).sum(axis=1, keepdims=True))
+
+
+def ctc_loss_packed_logits(logits, cu_seqlens, lengths, targets, target_lengths, blank: int,
+                           zero_infinity: bool = False, reduction: str = "none", grad_loss=None,
+                           need_grad: bool = True, threads: int = 0):
+    """The packed CTC loss of ``log_softmax(logits)`` and its gradient with
+    respect to the logits, in float64.
+
+    Page "feat(asr): native CTC loss kernel over sequence-packed log
+    probabilities", ``ctc_loss.py``: the path's inputs are the log_softmax
+    of a model's logits, and the gradient it returns, ``scale * exp(lp) - P``,
+    is the gradient with respect to those logits (each row of
+    ``exp(lp) - P`` sums to zero, so log_softmax's backward leaves it
+    unchanged).  With ``lp = log_softmax(logits)`` that is
+    ``scale * softmax(logits) - P``: the loss and gradient of
+    ``ctc_loss_packed`` on the normalised rows.  Returns ``(loss, grad, nll)``
+    as ``ctc_loss_packed`` does, ``grad`` with respect to the logits.
+    """
+    return ctc_loss_packed(log_softmax_rows(logits), cu_seqlens, lengths, targets, target_lengths, blank,
+                           zero_infinity, reduction, grad_loss=grad_loss, need_grad=need_grad, threads=threads)
+
+
 def oracle_batch(batch, grad_loss=None, need_grad: bool = True, threads: int = 0):
     """``ctc_loss_packed`` on a ``workloads.Batch``-like object."""
     return ctc_loss_packed(batch.log_probs, batch.cu_seqlens, batch.lengths, batch.targets, batch.target_lengths,
