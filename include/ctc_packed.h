@@ -98,6 +98,21 @@ typedef enum {
 
 /* Flags of ctc_packed_forward. */
 #define CTC_PACKED_FLAG_LOSS_ONLY 0x1u /* skip the work only the backward needs; ctc_packed_backward then fails */
+/*
+ * The (T_total, D) input holds a model's unnormalised logits z, not log
+ * probabilities.  The forward takes log_softmax over each row itself: one
+ * extra dense read of z computes each row's log-sum-exp lse[t] (kept in the
+ * workspace), and the path then uses lp[t, c] = z[t, c] - lse[t] in float32,
+ * so no normalised copy of the rows is ever written.  The following
+ * ctc_packed_backward returns the gradient with respect to the logits,
+ * scale * softmax(z)[t, c] - P[t, c] (the log_softmax backward is fused; it
+ * is the identity on rows that sum to zero).  A row holding NaN or +inf gets
+ * a NaN log_softmax, a row of -inf a NaN one too, as log_softmax gives.
+ * Page "feat(asr): native CTC loss kernel over sequence-packed log
+ * probabilities", ctc_loss.py: the path's input is log_softmax(logits) and
+ * its gradient scale * exp(lp) - P is the gradient with respect to them.
+ */
+#define CTC_PACKED_FLAG_LOGITS 0x2u
 
 /*
  * Bytes of device workspace a forward/backward pair with these sizes needs.
@@ -123,7 +138,8 @@ size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_
  *   loss           float32 device output: B entries for NONE, 1 otherwise.
  *   workspace      device buffer of at least ctc_packed_workspace_size bytes;
  *                  pass the same one, unchanged, to ctc_packed_backward.
- *   flags          0, or CTC_PACKED_FLAG_LOSS_ONLY.
+ *   flags          0, or an OR of CTC_PACKED_FLAG_LOSS_ONLY and
+ *                  CTC_PACKED_FLAG_LOGITS; other bits are invalid.
  */
 ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
                                      const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
@@ -132,7 +148,8 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
                                      void* workspace, size_t workspace_bytes, unsigned flags, cudaStream_t stream);
 
 /*
- * Backward: gradient of the reduced loss with respect to log_probs.
+ * Backward: gradient of the reduced loss with respect to log_probs (with
+ * respect to the logits after a forward with CTC_PACKED_FLAG_LOGITS).
  *
  * Same inputs as the forward that filled `workspace` (same values, same
  * buffers or copies of them).  grad_loss is the float32 upstream gradient of

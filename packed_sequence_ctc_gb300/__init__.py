@@ -25,7 +25,7 @@ __all__ = [
     "load_library", "ctc_packed_workspace_size", "ctc_packed_forward", "ctc_packed_backward",
     "ctc_packed_read_status", "ctc_packed_status_string", "packed_ctc_loss", "PackedCTCLoss", "Workspace",
     "DTYPE_CODES", "REDUCTION_CODES", "DEVICE_STATUS_BITS", "CTCPackedError",
-    "ctc_packed_forward_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "ctc_packed_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "FLAG_LOSS_ONLY", "FLAG_LOGITS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +34,7 @@ LIB_PATH = os.path.join(_HERE, "libctc_packed.so")
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 REDUCTION_CODES = {"none": 0, "sum": 1, "mean": 2}
 FLAG_LOSS_ONLY = 0x1
+FLAG_LOGITS = 0x2  # the input rows are logits: log_softmax is taken inside, the gradient is w.r.t. the logits
 NOALLOC_SCRATCH_BYTES = 32 << 20  # CTC_PACKED_NOALLOC_SCRATCH_BYTES
 DEVICE_STATUS_BITS = {
     0x1: "target_lengths must not be negative",
@@ -177,7 +178,7 @@ class PackedCTCLoss(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, log_probs, cu_seqlens, lengths, targets, target_lengths, blank, zero_infinity, reduction,
-                max_target_len, check):
+                max_target_len, check, logits=False):
         if log_probs.dtype not in DTYPE_CODES:
             raise TypeError(f"log_probs must be float32, bfloat16 or float16, got {log_probs.dtype}.")
         if log_probs.ndim != 2 or not log_probs.is_cuda:
@@ -189,7 +190,8 @@ class PackedCTCLoss(torch.autograd.Function):
         T_total, D = log_probs.shape
         ws = Workspace(T_total, B, max_target_len, D, log_probs.dtype, dev).tensor
         loss = torch.empty(B if reduction == "none" else 1, dtype=torch.float32, device=dev)
-        ctc_packed_forward(log_probs, cu, ln, tg, tl, blank, zero_infinity, reduction, loss, ws, max_target_len)
+        ctc_packed_forward(log_probs, cu, ln, tg, tl, blank, zero_infinity, reduction, loss, ws, max_target_len,
+                           flags=FLAG_LOGITS if logits else 0)
         if check:
             _raise_on_status(ctc_packed_read_status(ws))
         ctx.save_for_backward(log_probs, cu, ln, tg, tl, ws)
@@ -203,13 +205,18 @@ class PackedCTCLoss(torch.autograd.Function):
         g = grad_out.to(torch.float32).reshape(-1).contiguous()
         grad = torch.empty_like(log_probs)
         ctc_packed_backward(log_probs, cu, ln, tg, tl, blank, zero_infinity, reduction, g, ws, grad, max_target_len)
-        return grad, None, None, None, None, None, None, None, None, None
+        return grad, None, None, None, None, None, None, None, None, None, None
 
 
 def packed_ctc_loss(log_probs: torch.Tensor, cu_seqlens: torch.Tensor, lengths: torch.Tensor, targets: torch.Tensor,
                     target_lengths: torch.Tensor, *, blank: int, zero_infinity: bool = False, reduction: str = "none",
-                    max_target_len: Optional[int] = None, check: Optional[bool] = None) -> torch.Tensor:
+                    max_target_len: Optional[int] = None, check: Optional[bool] = None,
+                    logits: bool = False) -> torch.Tensor:
     """CTC loss over token-flat log probabilities (targets concatenated).
+
+    ``logits=True``: the rows are a model's unnormalised logits; the library
+    takes log_softmax of each row itself (no normalised copy is written) and
+    the gradient is with respect to the logits.
 
     ``max_target_len`` bounds every target length (the width of a padded
     targets buffer); when omitted it is read from ``target_lengths``, which
@@ -231,4 +238,4 @@ def packed_ctc_loss(log_probs: torch.Tensor, cu_seqlens: torch.Tensor, lengths: 
     if check is None:
         check = not capturing
     return PackedCTCLoss.apply(log_probs, cu_seqlens, lengths, targets, target_lengths, blank, zero_infinity,
-                               reduction, max_target_len, check)
+                               reduction, max_target_len, check, logits)

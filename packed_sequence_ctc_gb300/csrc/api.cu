@@ -58,7 +58,8 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     if (st != CTC_PACKED_OK) return st;
     if (loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if ((flags & ~CTC_PACKED_FLAG_LOSS_ONLY) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if ((flags & ~(CTC_PACKED_FLAG_LOSS_ONLY | CTC_PACKED_FLAG_LOGITS)) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const bool logits = (flags & CTC_PACKED_FLAG_LOGITS) != 0;
     const Layout L = make_layout(T_total, B, max_target_len, D);
     const bool need_grad = (flags & CTC_PACKED_FLAG_LOSS_ONLY) == 0;
 
@@ -73,6 +74,7 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     pa.zero_infinity = zero_infinity ? 1 : 0;
     pa.need_grad = need_grad ? 1 : 0;
     pa.group_pairs = L.gpairs;
+    pa.logits = logits ? 1 : 0;
     if (launch_prep(pa, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
 
     ChainArgs ca{};
@@ -88,6 +90,12 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     ca.blank = blank;
     ca.reduction = reduction;
     ca.zero_infinity = zero_infinity ? 1 : 0;
+    ca.lse = nullptr;
+    if (logits) {
+        // one dense pass over the logits: each row's log-sum-exp
+        if (launch_lse(ca, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+        ca.lse = ws_at<float>(workspace, L.off_lse);
+    }
     if (launch_emit(ca, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     if (launch_chain(ca, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     return CTC_PACKED_OK;

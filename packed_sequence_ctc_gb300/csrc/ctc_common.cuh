@@ -32,7 +32,8 @@ struct Control {
     uint32_t done_ctas;   // CTAs of the chain kernel that have finished
     uint32_t grad_ready;  // 1 once a forward has stored what the backward needs
     int32_t n_big, n_small, n_lab;
-    uint32_t pad[7];
+    uint32_t logits;      // 1: the forward took logits, normalised each row, and kept its log-sum-exp
+    uint32_t pad[6];
 };
 static_assert(sizeof(Control) == 64, "control block is 64 bytes");
 
@@ -72,7 +73,7 @@ struct Layout {
     int32_t epitch;              // entries per row of the emission matrix (max_U + 1)
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
-    size_t off_nxt, off_rank, off_owner, off_em, off_head, off_ent, total;
+    size_t off_nxt, off_rank, off_owner, off_em, off_head, off_ent, off_lse, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -130,6 +131,7 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_em = o;     o = align_up(o + 16 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
     L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
     L.off_ent = o;    o = align_up(o + 8 * (size_t)T_total * (size_t)L.ecap, 256);
+    L.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)T_total, 256);
     L.total = o;
     return L;
 }

@@ -16,6 +16,7 @@ struct PrepArgs {
     int zero_infinity;
     int need_grad;
     int group_pairs;  // pairs one chain warp owns: longer targets run on a whole CTA
+    int logits;       // the input rows are logits (log_softmax is taken by the path)
 };
 
 struct ChainArgs {
@@ -31,6 +32,7 @@ struct ChainArgs {
     int blank;
     int reduction;
     int zero_infinity;
+    const float* lse;    // per-row log-sum-exp of logits input, subtracted from each value; null for log probabilities
 };
 
 struct GradArgs {
@@ -55,6 +57,8 @@ struct GradArgs {
 
 __global__ void prep_kernel(PrepArgs a);
 template <int DT>
+__global__ void lse_kernel(ChainArgs a);
+template <int DT>
 __global__ void emit_kernel(ChainArgs a);
 template <int P, int MAXT>
 __global__ void chain_kernel(ChainArgs a);
@@ -66,6 +70,7 @@ uint32_t grad_group_multiplier(const Layout& L);  // 0 if no exact multiplier ex
 
 // Host launchers (defined next to their kernels).
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_lse(const ChainArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_emit(const ChainArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_post(const GradArgs& a, cudaStream_t s);

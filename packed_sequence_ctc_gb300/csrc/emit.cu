@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
         s_u[tid] = U;
         s_toff[tid] = toff;
         if (b >= 0) {
-            const float x = load_lp<DT>(a.lp, row * (int64_t)a.D + a.blank);
+            float x = load_lp<DT>(a.lp, row * (int64_t)a.D + a.blank);
+            if (a.lse != nullptr) x -= a.lse[row];  // logits: log_softmax of the row
             s_blank[tid] = xp_from_log(x);
             if (x != x) atomicOr(&uttw[b].has_nan, 1);
             atomicMax(&s_maxw, U + 1);
@@ -105,6 +106,10 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
     }
     __syncthreads();
     const int maxw = s_maxw;
+    float lse_r[kEmitRows];
+#pragma unroll
+    for (int rr = 0; rr < kEmitRows; ++rr)
+        lse_r[rr] = (a.lse != nullptr && s_b[rr] >= 0) ? a.lse[r0 + rr] : 0.0f;
     for (int w = tid; w < maxw; w += kEmitThreads) {
         int cls[kEmitRows];
 #pragma unroll
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
         for (int rr = 0; rr < kEmitRows; ++rr) {
             // an id outside [0, D) is not read (the chain reports it); its emission is 0
             const bool live = cls[rr] >= 0 && cls[rr] < a.D;
-            x[rr] = live ? load_lp<DT>(a.lp, (r0 + rr) * (int64_t)a.D + cls[rr]) : -INFINITY;
+            x[rr] = live ? load_lp<DT>(a.lp, (r0 + rr) * (int64_t)a.D + cls[rr]) - lse_r[rr] : -INFINITY;
         }
 #pragma unroll
         for (int rr = 0; rr < kEmitRows; ++rr) {

@@ -106,16 +106,19 @@ __device__ __forceinline__ void store_elem(uintptr_t addr, uint32_t bits) {
 
 // Gradient of one whole 16-byte chunk: s * exp(lp) + pn element by element,
 // pn the chunk's negated class sums (zero where none), in pairs on the
-// paired fp32 pipes, rounded once into the chunk's dtype.
+// paired fp32 pipes, rounded once into the chunk's dtype.  exp(lp) is
+// 2^(x log2 e + bias): bias = 0 for log probabilities, -lse log2 e for a row
+// of logits (then exp(lp) is the row's softmax); x log2 e + 0 rounds as the
+// product alone, so log-probability rows are unchanged by the bias.
 template <int DT>
-__device__ __forceinline__ uint4 chunk_grad(uint4 in, float s, const float (&pn)[16 / Elem<DT>::bytes]) {
-    const float2 l2e = make_float2(kLog2e, kLog2e), s2 = make_float2(s, s);
+__device__ __forceinline__ uint4 chunk_grad(uint4 in, float s, const float (&pn)[16 / Elem<DT>::bytes], float bias) {
+    const float2 l2e = make_float2(kLog2e, kLog2e), s2 = make_float2(s, s), b2 = make_float2(bias, bias);
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     if constexpr (DT == 0) {
         float o[4];
 #pragma unroll
         for (int i = 0; i < 4; i += 2) {
-            const float2 t = __fmul2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e);
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e, b2);
             const float2 r = __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[i], pn[i + 1]));
             o[i] = r.x;
             o[i + 1] = r.y;
@@ -131,7 +134,7 @@ __device__ __forceinline__ uint4 chunk_grad(uint4 in, float s, const float (&pn)
             } else {
                 x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
             }
-            const float2 t = __fmul2_rn(x, l2e);
+            const float2 t = __ffma2_rn(x, l2e, b2);
             const float2 r =
                 __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[2 * i], pn[2 * i + 1]));
             o[i] = pack2<DT>(r.x, r.y);
@@ -294,7 +297,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
     unsigned char* ws = smem_raw + (size_t)warp * a.warp_smem;
     float* row_scale = reinterpret_cast<float*>(ws);  // K entries, NaN-free: 0 when not covered
     int* row_cov = reinterpret_cast<int*>(ws + align_up(4 * (size_t)K, 16));
-    int* e_key = reinterpret_cast<int*>(ws + 2 * align_up(4 * (size_t)K, 16));
+    float* row_bias = reinterpret_cast<float*>(ws + 2 * align_up(4 * (size_t)K, 16));  // exponent bias of each row
+    int* e_key = reinterpret_cast<int*>(ws + 3 * align_up(4 * (size_t)K, 16));
     float* e_val = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_key) + align_up(4 * (size_t)cap, 16));
     float* ptile = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(e_val) + align_up(4 * (size_t)cap, 16));
     uint32_t* pmark = reinterpret_cast<uint32_t*>(ptile + kBatchChunks * 8);  // kBatchChunks / 32 words
@@ -318,6 +322,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
     __syncwarp();
     pdl_wait();     // the class sums of the pass before
     pdl_trigger();  // persistent grid: every block is already resident
+    // logits input: exp(lp) = exp(z - lse) = 2^(z log2 e - lse log2 e)
+    const bool logits = ws_at<Control>(a.ws, a.L.off_ctrl)->logits != 0;
+    const float* __restrict__ lse = ws_at<float>(a.ws, a.L.off_lse);
 
     if (K == 1 && a.congruent) {
         // One row per warp task, lp and grad congruent modulo 16.  The batches
@@ -363,6 +370,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
             const int count = h.count;
             const bool cov = h.covered != 0;
             const float s = h.scale;
+            const float bias = logits ? -lse[row] * kLog2e : 0.0f;
             for (int i = lane; i <= g.nb; i += 32) bfill[i] = 0;
             __syncwarp();
             for (int e = lane; e < count; e += 32) atomicAdd(&bfill[(er[e].x + g.pshift) / (kBatchChunks * V)], 1);
@@ -439,10 +447,10 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
                         }
                     }
                     if (c0 >= g.g0 && c0 + 16 <= g.g1) {
-                        *reinterpret_cast<uint4*>(c0) = cov ? chunk_grad<DT>(cur[k], s, pn) : make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(c0) = cov ? chunk_grad<DT>(cur[k], s, pn, bias) : make_uint4(0u, 0u, 0u, 0u);
                     } else if (cl >= lp0 && cl + 16 <= lp_end) {
                         // a ragged end chunk, read whole: store only the row's elements
-                        const uint4 o = cov ? chunk_grad<DT>(cur[k], s, pn) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 o = cov ? chunk_grad<DT>(cur[k], s, pn, bias) : make_uint4(0u, 0u, 0u, 0u);
                         const uint32_t w[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                         for (int i = 0; i < V; ++i) {
@@ -465,7 +473,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
                             float pk = 0.0f;  // pn[i], selected without dynamic indexing
 #pragma unroll
                             for (int ii = 0; ii < V; ++ii) pk = ii == i ? pn[ii] : pk;
-                            const float gv = cov ? fmaf(s, fast_ex2(x * kLog2e), pk) : 0.0f;
+                            const float gv = cov ? fmaf(s, fast_ex2(fmaf(x, kLog2e, bias)), pk) : 0.0f;
                             store_elem<DT>(ad, pack1<DT>(gv));
                         }
                     }
@@ -501,6 +509,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
             if (lane == 0) {
                 row_scale[rr] = h.scale;
                 row_cov[rr] = h.covered;
+                row_bias[rr] = logits ? -lse[r0 + rr] * kLog2e : 0.0f;
             }
             const int2* er = ent + (r0 + rr) * a.L.ecap;
             for (int e = lane; e < h.count; e += 32) {
@@ -537,6 +546,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
             const uintptr_t lpq = qb + (a0 - g0);  // lp address of chunk 0
             const bool cov = row_cov[0] != 0;
             const float s = row_scale[0];
+            const float bias = row_bias[0];
             const int nb = (nq + kBatchChunks - 1) / kBatchChunks;
             // bucket the class sums by batch, once per row
             for (int i = lane; i <= nb; i += 32) bfill[i] = 0;
@@ -609,7 +619,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
                                 reinterpret_cast<float4*>(ptile + ql * V)[i / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
                             }
                         }
-                        *reinterpret_cast<uint4*>(c0) = cov ? chunk_grad<DT>(cur[k], s, pn) : make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(c0) = cov ? chunk_grad<DT>(cur[k], s, pn, bias) : make_uint4(0u, 0u, 0u, 0u);
                     } else {
                         // the ragged first / last chunk of the row
                         const uintptr_t lo = c0 > g0 ? c0 : g0;
@@ -618,7 +628,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
                             const size_t f = (ad - g0) / E;
                             const float x = bits_to_float<DT>(load_elem<DT>(a0 + f * E));
                             const float pk = marked ? ptile[ql * V + (int)(f + pshift) - q * V] : 0.0f;
-                            const float gv = cov ? fmaf(s, fast_ex2(x * kLog2e), pk) : 0.0f;
+                            const float gv = cov ? fmaf(s, fast_ex2(fmaf(x, kLog2e, bias)), pk) : 0.0f;
                             store_elem<DT>(ad, pack1<DT>(gv));
                         }
                         if (marked) {
@@ -686,7 +696,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
                     // a whole chunk inside one row
                     uint4 o = make_uint4(0u, 0u, 0u, 0u);
                     if (row_cov[r]) {
-                        const float s = row_scale[r];
+                        const float s = row_scale[r], bias = row_bias[r];
                         const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
                         float out[V];
 #pragma unroll
@@ -697,7 +707,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
                             } else {
                                 bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
                             }
-                            out[i] = fmaf(s, fast_ex2(bits_to_float<DT>(bits) * kLog2e), pv[i]);
+                            out[i] = fmaf(s, fast_ex2(fmaf(bits_to_float<DT>(bits), kLog2e, bias)), pv[i]);
                         }
                         if constexpr (E == 4) {
                             o = make_uint4(__float_as_uint(out[0]), __float_as_uint(out[1]), __float_as_uint(out[2]),
@@ -718,7 +728,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
                         }
                         const float x = bits_to_float<DT>(load_elem<DT>(a0 + (size_t)f * E));
                         const float pk = marked ? ptile[ql * V + f + pshift - q * V] : 0.0f;
-                        const float gv = row_cov[r] ? fmaf(row_scale[r], fast_ex2(x * kLog2e), pk) : 0.0f;
+                        const float gv =
+                            row_cov[r] ? fmaf(row_scale[r], fast_ex2(fmaf(x, kLog2e, row_bias[r])), pk) : 0.0f;
                         store_elem<DT>(g0 + (size_t)f * E, pack1<DT>(gv));
                         ++c;
                     }
@@ -771,7 +782,7 @@ void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& wa
     if (k < 1) k = 1;
     rows = k;
     entry_cap = k * ecap;
-    warp_smem = 2 * align_up(4 * (size_t)k, 16) + 2 * align_up(4 * (size_t)entry_cap, 16) +
+    warp_smem = 3 * align_up(4 * (size_t)k, 16) + 2 * align_up(4 * (size_t)entry_cap, 16) +
                 4 * (size_t)kBatchChunks * 8 + 4 * (kBatchChunks / 32) +
                 4 * 2 * (size_t)(kMaxBatches + 4) + 2 * 4 * align_up((size_t)entry_cap, 4);
     warp_smem = align_up(warp_smem, 16);

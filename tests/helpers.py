@@ -70,11 +70,12 @@ def to_device(batch, device="cuda"):
 
 
 def run_gpu(batch, grad_loss=None, max_target_len=None, need_grad=True, grad_offset_bytes=0, guard_bytes=64,
-            device="cuda", log_probs=None):
+            device="cuda", log_probs=None, logits=False):
     """Forward + backward of `batch` through the C-ABI on the current stream.
 
     The gradient lands inside a larger buffer whose margins hold a sentinel,
-    so writes outside [0, T_total*D) are caught.  Returns (loss, grad, status).
+    so writes outside [0, T_total*D) are caught.  ``logits=True`` passes the
+    rows as logits (CTC_PACKED_FLAG_LOGITS).  Returns (loss, grad, status).
     """
     d = to_device(batch, device)
     lp = d["log_probs"] if log_probs is None else log_probs
@@ -85,7 +86,8 @@ def run_gpu(batch, grad_loss=None, max_target_len=None, need_grad=True, grad_off
     red = batch.reduction
     loss = torch.full((B if red == "none" else 1,), float("nan"), dtype=torch.float32, device=device)
     pk.ctc_packed_forward(lp, d["cu"], d["lengths"], d["targets"], d["target_lengths"], batch.blank,
-                          batch.zero_infinity, red, loss, ws, mtl, flags=0 if need_grad else pk.FLAG_LOSS_ONLY)
+                          batch.zero_infinity, red, loss, ws, mtl,
+                          flags=(0 if need_grad else pk.FLAG_LOSS_ONLY) | (pk.FLAG_LOGITS if logits else 0))
     grad = None
     if need_grad:
         if grad_loss is None:

@@ -234,6 +234,19 @@ def workload(name: str, device="cpu") -> Batch:
     return WORKLOADS[name](device=device)
 
 
+def unnormalised_logits(batch: Batch, seed: int = 0, offset: float = 8.0) -> torch.Tensor:
+    """Logits for the logits input form: the batch's log probabilities plus a
+    seeded per-row offset drawn uniformly from [-offset, offset] (in float32,
+    then cast to the batch's dtype), so that each row's log_softmax is the
+    batch's row up to that cast."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    T_total = batch.log_probs.shape[0]
+    shift = (torch.rand(T_total, 1, generator=gen, dtype=torch.float32) * 2.0 - 1.0) * offset
+    z = batch.log_probs.detach().cpu().float() + shift
+    return z.to(batch.log_probs.dtype)
+
+
 def padded_targets(batch: Batch, width: Optional[int] = None, fill: int = 0) -> torch.Tensor:
     """The concatenated targets as a padded ``(B, width)`` int64 tensor."""
     width = batch.max_target_len if width is None else width
