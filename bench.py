@@ -71,6 +71,8 @@ def _args():
     p.add_argument("--workload", default="largevocab")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--input", default="log_probs", choices=["log_probs", "logits"],
+                   help="logits: the rows are unnormalised logits and the path takes log_softmax itself")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return p.parse_args()
 
@@ -108,10 +110,12 @@ def _workload_description(batch, flush=False):
     }
 
 
-def algorithmic_bytes(batch):
+def algorithmic_bytes(batch, logits=False):
     """Bytes the path must move: the forward's
     label-column gathers, the alpha store and reload (fp32), the full dense
-    read of the log probabilities and write of the gradient."""
+    read of the log probabilities and write of the gradient; with logits
+    input also the forward's dense read of the logits (the row
+    log-sum-exp)."""
     e = batch.log_probs.element_size()
     D = batch.D
     gather = alpha = 0
@@ -121,7 +125,8 @@ def algorithmic_bytes(batch):
         alpha += 2 * T * S * 4
     dense = 2 * batch.T_total * D * e
     grad_kernel = dense + alpha // 2  # the backward reads lp, writes grad, reloads the stored rows
-    return {"gather": gather, "alpha": alpha, "dense": dense, "total": gather + alpha + dense,
+    lse = batch.T_total * D * e if logits else 0
+    return {"gather": gather, "alpha": alpha, "dense": dense, "lse": lse, "total": gather + alpha + dense + lse,
             "grad_kernel": grad_kernel}
 
 
@@ -208,19 +213,26 @@ def _gpu_query_id(torch, dev):
         return None
 
 
-def cpu_baseline(batch, seconds, steps=1, warmup=0):
-    """Time the fp64 oracle (as it stands) on a bounded sample of utterances."""
+def cpu_baseline(batch, seconds, steps=1, warmup=0, logits=False):
+    """Time the fp64 oracle (as it stands) on a bounded sample of utterances
+    (its logits form when the rows are logits)."""
     import numpy as np
 
     import oracle
     import workloads
+
+    def run(b, threads):
+        if logits:
+            return oracle.ctc_loss_packed_logits(b.log_probs, b.cu_seqlens, b.lengths, b.targets, b.target_lengths,
+                                                 b.blank, b.zero_infinity, b.reduction, threads=threads)
+        return oracle.oracle_batch(b, threads=threads)
 
     threads = oracle.max_threads()
     lengths = batch.lengths.tolist()
     # calibrate on two utterances, then take as many as fit the time budget
     probe = workloads.select_utterances(batch, [0, 1] if batch.B > 1 else [0])
     t = time.perf_counter()
-    oracle.oracle_batch(probe, threads=1)
+    run(probe, 1)
     per_frame = (time.perf_counter() - t) / max(1, probe.frames)
     budget_frames = seconds * threads / max(per_frame, 1e-9)
     take, frames = [], 0
@@ -231,16 +243,16 @@ def cpu_baseline(batch, seconds, steps=1, warmup=0):
         frames += lengths[b]
     sample = workloads.select_utterances(batch, take)
     for _ in range(warmup):
-        oracle.oracle_batch(sample, threads=threads)
+        run(sample, threads)
     times = []
     for _ in range(steps):
         t = time.perf_counter()
-        oracle.oracle_batch(sample, threads=threads)
+        run(sample, threads)
         times.append(time.perf_counter() - t)
     dt = float(np.mean(times))
     return {"value": sample.frames / dt, "unit": "frames/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(take)} of {batch.B} utterances ({sample.frames} frames) of the same workload, "
-                      f"fp64 loss + gradient, OpenMP over utterances",
+                      f"fp64 {'log_softmax + ' if logits else ''}loss + gradient, OpenMP over utterances",
             "seconds_per_sample": dt}
 
 
@@ -256,10 +268,14 @@ def run_reference(args):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     batch = workloads.workload(args.workload, device=dev)
     batch.log_probs = batch.log_probs.cpu()
+    logits = args.input == "logits"
+    if logits:
+        batch.log_probs = workloads.unnormalised_logits(batch, seed=17)
     # each step is a sample sized so that warmup + steps end within a few minutes
     per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
-    base = cpu_baseline(batch, per_step, steps=args.steps, warmup=args.warmup)
+    base = cpu_baseline(batch, per_step, steps=args.steps, warmup=args.warmup, logits=logits)
     cfg = _workload_description(batch)
+    cfg["input"] = args.input
     line = {
         "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "frames/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": base["seconds_per_sample"] * 1e3,
@@ -303,7 +319,12 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     batch = workloads.workload(args.workload, device=dev)
+    logits = args.input == "logits"
     lp = batch.log_probs.contiguous()
+    fflags = 0
+    if logits:  # unnormalised rows: the forward takes their log_softmax itself
+        lp = workloads.unnormalised_logits(batch, seed=17).to(dev).contiguous()
+        fflags = pk.FLAG_LOGITS
     cu, ln, tg, tl = (x.to(dev) for x in (batch.cu_seqlens, batch.lengths, batch.targets, batch.target_lengths))
     B, T_total, D = batch.B, batch.T_total, batch.D
     mtl = batch.max_target_len
@@ -316,7 +337,7 @@ def run_ours(args):
 
     def step():
         pk.ctc_packed_forward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, loss, ws, mtl,
-                              stream=stream)
+                              flags=fflags, stream=stream)
         pk.ctc_packed_backward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, g_up, ws, grad, mtl,
                                stream=stream)
 
@@ -345,7 +366,7 @@ def run_ours(args):
                 scrub.fill_(float(k))
         ev[k][0].record(stream)
         pk.ctc_packed_forward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, loss, ws, mtl,
-                              stream=stream)
+                              flags=fflags, stream=stream)
         ev[k][1].record(stream)
         pk.ctc_packed_backward(lp, cu, ln, tg, tl, batch.blank, batch.zero_infinity, red, g_up, ws, grad, mtl,
                                stream=stream)
@@ -367,7 +388,7 @@ def run_ours(args):
     ms_per_step, value = job_throughput(total_ms, K, batch.frames, world, dev)
 
     hbm_peak, peak_kind = _peaks()
-    ab = algorithmic_bytes(batch)
+    ab = algorithmic_bytes(batch, logits)
     grad_avg_ms = sum(bwd_ms) / K
     fwd_avg_ms = sum(fwd_ms) / K
     achieved = ab["grad_kernel"] / (grad_avg_ms / 1e3) / 1e9
@@ -378,29 +399,30 @@ def run_ours(args):
     path_gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
     path_roofline = {"achieved": round(path_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(path_gbs / hbm_peak, 4), "algorithmic_bytes_per_step": ab["total"],
-                     "bytes": {k: ab[k] for k in ("gather", "alpha", "dense")},
+                     "bytes": {k: ab[k] for k in ("gather", "alpha", "dense", "lse")},
                      "forward_ms": round(fwd_avg_ms, 5), "backward_ms": round(grad_avg_ms, 5)}
 
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world)
+        e2e = _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world, fflags)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         batch.log_probs = lp.cpu()
-        base = cpu_baseline(batch, args.cpu_seconds)
+        base = cpu_baseline(batch, args.cpu_seconds, logits=logits)
         cpu = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if rank == 0:
         dt = {"fp32": "f32", "bf16": "f32", "fp16": "f32"}
         cfg = _workload_description(batch, flush)
         cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+        cfg["input"] = args.input
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "frames/s", "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dt[cfg["io_dtype"]], "data": "synthetic",
             "config": cfg, "hbm_gbs": round(path_gbs, 1), "roofline": roofline, "path_roofline": path_roofline,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * K, "clocks": clocks,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (KERNELS_PER_STEP + (1 if logits else 0)) * K, "clocks": clocks,
             "device_status": status,
         }
         print(json.dumps(line), flush=True)
@@ -408,7 +430,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world):
+def _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world, fflags=0):
     """Same metric through the C-ABI from pinned host buffers: every step
     copies its inputs host->device, runs forward + backward and reads the
     loss back.  The copies run on a copy stream into two alternating input
@@ -445,7 +467,7 @@ def _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world):
             copied[j].record(copy_stream)
         stream.wait_event(copied[j])
         pk.ctc_packed_forward(d["lp"], d["cu"], d["ln"], d["tg"], d["tl"], batch.blank, batch.zero_infinity, red,
-                              loss, ws, mtl, stream=stream)
+                              loss, ws, mtl, flags=fflags, stream=stream)
         pk.ctc_packed_backward(d["lp"], d["cu"], d["ln"], d["tg"], d["tl"], batch.blank, batch.zero_infinity, red,
                                g_up, ws, grad, mtl, stream=stream)
         released[j].record(stream)

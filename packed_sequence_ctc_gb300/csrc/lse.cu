@@ -64,6 +64,29 @@ __device__ __forceinline__ void fold(const float (&x)[N], const bool (&ok)[N], f
         if (ok[i]) s += fast_ex2(fmaf(x[i], kLog2e, mb));  // exp(x - m); exactly 0 for x = -inf
 }
 
+// The same for a chunk whose values all belong to the row (every chunk but
+// the row's two ends): no per-value checks.  A NaN, or +inf against a finite
+// maximum, turns s into NaN, which marks the row bad at the end.
+template <int N>
+__device__ __forceinline__ void fold_inner(const float (&x)[N], float& m, float& s) {
+    float cm = x[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) cm = fmaxf(cm, x[i]);
+    if (cm > m) {
+        s *= fast_ex2((m - cm) * kLog2e);  // 0 * 0 while m is still -inf
+        m = cm;
+    }
+    if (m == -INFINITY) return;  // nothing but -inf so far
+    const float2 l2e = make_float2(kLog2e, kLog2e), mb = make_float2(-m * kLog2e, -m * kLog2e);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), l2e, mb);
+        acc = __fadd2_rn(acc, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
+    }
+    s += acc.x + acc.y;
+}
+
 }  // namespace
 
 template <int DT>
@@ -112,6 +135,13 @@ __global__ void __launch_bounds__(kLseWarps * 32) lse_kernel(ChainArgs a) {
                             bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
                         }
                         x[i] = bits_to_float<DT>(bits);
+                    }
+                    if (c >= r0 && c + 16 <= r1) {
+                        fold_inner(x, m, s);
+                        continue;
+                    }
+#pragma unroll
+                    for (int i = 0; i < V; ++i) {
                         const uintptr_t ad = c + (uintptr_t)i * E;
                         ok[i] = ad >= r0 && ad < r1;
                     }
@@ -135,7 +165,7 @@ __global__ void __launch_bounds__(kLseWarps * 32) lse_kernel(ChainArgs a) {
             }
         }
         // combine the lanes' (m, s): M = max m, S = sum s * exp(m - M)
-        const bool row_bad = __any_sync(0xffffffffu, bad);
+        const bool row_bad = __any_sync(0xffffffffu, bad || s != s || m == INFINITY);
         float M = m;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
