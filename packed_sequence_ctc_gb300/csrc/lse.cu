@@ -10,9 +10,8 @@
 // gradient with respect to the logits.
 //
 // One warp per row, rows strided over a persistent grid.  A row is read as
-// the 16-byte chunks that cover its bytes, 4 per lane in flight, after one
-// bulk L2 prefetch of the whole row; the ragged chunks at the two ends of the
-// buffer are read element by element.  Each lane keeps a running maximum m
+// the 16-byte chunks that cover its bytes, 2 per lane in flight; the ragged
+// chunks at the two ends of the buffer are read element by element.  Each lane keeps a running maximum m
 // and a sum s of exp(z - m) (rescaled when m grows), the warp combines the
 // lanes' pairs, and lane 0 writes m + log(s).  A row of -inf gives -inf; a
 // NaN or +inf logit gives NaN, as log_softmax does.
@@ -24,7 +23,9 @@ namespace ctcp {
 namespace {
 
 constexpr int kLseWarps = 8;    // warps per CTA
-constexpr int kLseUnroll = 4;   // 16-byte chunks in flight per lane
+// 16-byte chunks in flight per lane.  Measured on the 8193-class workload:
+// 2 beat 1, 4 and 8, and an L2 prefetch of the whole row cost 2 to 6 us.
+constexpr int kLseUnroll = 2;
 
 __device__ __forceinline__ uint4 ld_row_chunk(uintptr_t p) {
     uint4 v;
@@ -32,13 +33,6 @@ __device__ __forceinline__ uint4 ld_row_chunk(uintptr_t p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
-}
-
-__device__ __forceinline__ void prefetch_row_l2(uintptr_t lo, uintptr_t hi) {
-    lo = (lo + 15) & ~uintptr_t(15);
-    hi &= ~uintptr_t(15);
-    if (hi > lo)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
 }
 
 // Folds the valid values of one chunk into the running (m, s); a NaN or a
@@ -103,7 +97,6 @@ __global__ void __launch_bounds__(kLseWarps * 32) lse_kernel(ChainArgs a) {
     pdl_wait();  // the workspace may still be read by the stream's earlier work
     for (int64_t row = (int64_t)blockIdx.x * kLseWarps + (threadIdx.x >> 5); row < T; row += warps) {
         const uintptr_t r0 = z0 + (uintptr_t)(row * D * E), r1 = r0 + (uintptr_t)D * E;
-        if (lane == 0) prefetch_row_l2(r0, r1);
         const uintptr_t qb = r0 & ~uintptr_t(15);
         const int nq = (int)((((r1 + 15) & ~uintptr_t(15)) - qb) / 16);
         float m = -INFINITY, s = 0.0f;
