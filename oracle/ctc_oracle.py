@@ -19,6 +19,10 @@ probabilities" (NVIDIA-NeMo/Speech PR #16437):
 * ``nemo/collections/asr/losses/ctc.py``, ``forward_packed``: reduction
   ``sum`` adds the losses; ``mean`` divides each loss by its target length
   clamped to at least 1 and averages over the batch; ``none`` keeps them.
+  The module's own ``reduce`` then offers ``mean_batch`` and ``mean_volume``
+  (the page's tests parametrize both; the page does not print their
+  bodies).  Read here as the batch mean of the losses and as the sum of the
+  losses over the sum of the target lengths.
 
 Half-precision inputs are upcast exactly to float64 before anything else,
 so the oracle sees the very values the kernels read.
@@ -129,6 +133,13 @@ def utterance_scales(nll: np.ndarray, target_lengths, reduction: str, zero_infin
     elif reduction == "mean":
         g = 1.0 if grad_loss is None else float(_as_f64(grad_loss).reshape(-1)[0])
         scale = g / (B * np.maximum(tl, 1).astype(np.float64))
+    elif reduction == "mean_batch":
+        g = 1.0 if grad_loss is None else float(_as_f64(grad_loss).reshape(-1)[0])
+        scale = np.full(B, g / B) if B else np.zeros(0)
+    elif reduction == "mean_volume":
+        g = 1.0 if grad_loss is None else float(_as_f64(grad_loss).reshape(-1)[0])
+        with np.errstate(divide="ignore", invalid="ignore"):
+            scale = np.full(B, np.float64(g) / np.float64(tl.sum()))
     else:
         raise ValueError(f"unknown reduction {reduction!r}")
     if zero_infinity:
@@ -148,6 +159,13 @@ def reduce_losses(nll: np.ndarray, target_lengths, reduction: str, zero_infinity
         if losses.shape[0] == 0:
             return np.float64(np.nan)
         return np.float64((losses / np.maximum(tl, 1)).mean())
+    if reduction == "mean_batch":
+        if losses.shape[0] == 0:
+            return np.float64(np.nan)
+        return np.float64(losses.mean())
+    if reduction == "mean_volume":
+        with np.errstate(divide="ignore", invalid="ignore"):
+            return np.float64(losses.sum()) / np.float64(tl.sum())
     raise ValueError(f"unknown reduction {reduction!r}")
 
 
