@@ -74,9 +74,15 @@ typedef enum {
 } ctc_packed_dtype;
 
 typedef enum {
-    CTC_PACKED_NONE = 0, /* loss has B entries */
-    CTC_PACKED_SUM = 1,  /* loss has 1 entry: sum of the B losses */
-    CTC_PACKED_MEAN = 2  /* loss has 1 entry: mean over b of loss_b / max(U_b, 1) */
+    CTC_PACKED_NONE = 0,       /* loss has B entries */
+    CTC_PACKED_SUM = 1,        /* loss has 1 entry: sum of the B losses */
+    CTC_PACKED_MEAN = 2,       /* loss has 1 entry: mean over b of loss_b / max(U_b, 1) */
+    /* NeMo's further reductions of the per-utterance losses (page
+     * "feat(asr): native CTC loss kernel over sequence-packed log
+     * probabilities", test_ctc_loss.py parametrizes both; the page does not
+     * print their bodies, read as): */
+    CTC_PACKED_MEAN_BATCH = 3, /* loss has 1 entry: (1/B) sum_b loss_b */
+    CTC_PACKED_MEAN_VOLUME = 4 /* loss has 1 entry: sum_b loss_b / sum_b max(U_b, 0) */
 } ctc_packed_reduction;
 
 typedef enum {

@@ -32,7 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libctc_packed.so")
 
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
-REDUCTION_CODES = {"none": 0, "sum": 1, "mean": 2}
+REDUCTION_CODES = {"none": 0, "sum": 1, "mean": 2, "mean_batch": 3, "mean_volume": 4}
 FLAG_LOSS_ONLY = 0x1
 FLAG_LOGITS = 0x2  # the input rows are logits: log_softmax is taken inside, the gradient is w.r.t. the logits
 NOALLOC_SCRATCH_BYTES = 32 << 20  # CTC_PACKED_NOALLOC_SCRATCH_BYTES

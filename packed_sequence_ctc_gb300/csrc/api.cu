@@ -14,7 +14,10 @@ namespace {
 int elem_bytes(ctc_packed_dtype d) { return d == CTC_PACKED_F32 ? 4 : 2; }
 
 bool valid_dtype(int d) { return d == CTC_PACKED_F32 || d == CTC_PACKED_BF16 || d == CTC_PACKED_F16; }
-bool valid_reduction(int r) { return r == CTC_PACKED_NONE || r == CTC_PACKED_SUM || r == CTC_PACKED_MEAN; }
+bool valid_reduction(int r) {
+    return r == CTC_PACKED_NONE || r == CTC_PACKED_SUM || r == CTC_PACKED_MEAN || r == CTC_PACKED_MEAN_BATCH ||
+           r == CTC_PACKED_MEAN_VOLUME;
+}
 
 // Checks shared by forward and backward.  Returns CTC_PACKED_OK or the error.
 ctc_packed_status check_common(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,

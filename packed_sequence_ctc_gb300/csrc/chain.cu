@@ -589,7 +589,9 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
     if (tid == 0) {
         double total = 0.0;
         for (int w = 0; w < NW; ++w) total += s_red[w];
-        if (a.reduction == CTC_PACKED_MEAN) total = B > 0 ? total / (double)B : __longlong_as_double(0x7ff8000000000000ll);
+        if (a.reduction == CTC_PACKED_MEAN || a.reduction == CTC_PACKED_MEAN_BATCH)
+            total = B > 0 ? total / (double)B : __longlong_as_double(0x7ff8000000000000ll);
+        if (a.reduction == CTC_PACKED_MEAN_VOLUME) total = total / (double)ctrl->tl_total;  // x / 0: inf or NaN
         a.loss[0] = (float)total;
     }
 }

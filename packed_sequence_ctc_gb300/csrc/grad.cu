@@ -204,8 +204,12 @@ __global__ void __launch_bounds__(kPostThreads) post_kernel(GradArgs a) {
                                 scale[r] = a.grad_loss[b];
                             } else if (a.reduction == CTC_PACKED_SUM) {
                                 scale[r] = a.grad_loss[0];
-                            } else {
+                            } else if (a.reduction == CTC_PACKED_MEAN) {
                                 scale[r] = __fdiv_rn(a.grad_loss[0], (float)B * (float)max(u.U, 1));
+                            } else if (a.reduction == CTC_PACKED_MEAN_BATCH) {
+                                scale[r] = __fdiv_rn(a.grad_loss[0], (float)B);
+                            } else {  // mean_volume
+                                scale[r] = __fdiv_rn(a.grad_loss[0], (float)ctrl->tl_total);
                             }
                             if (a.zero_infinity && u.nll_inf) scale[r] = 0.0f;
                             // an infinite nll (no alignment, zero_infinity off) leaves the row unspecified

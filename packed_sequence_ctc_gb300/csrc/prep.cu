@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
         moff_base += total_m;
     }
     if (bad_bits) atomicOr(&ctrl->status, bad_bits);
+    if (tid == 0) ctrl->tl_total = toff_base;
     __syncthreads();
 
     // 2. order the utterances longest first (the serial chain of the longest

@@ -82,7 +82,7 @@ def test_host_argument_checks_return_before_any_cuda_call(lib):
     assert _fwd(lib, blank=5) == INVALID
     assert _fwd(lib, blank=-1) == INVALID
     assert _fwd(lib, dtype=3) == INVALID
-    assert _fwd(lib, red=3) == INVALID
+    assert _fwd(lib, red=5) == INVALID  # 0..4 are none, sum, mean, mean_batch, mean_volume
     assert _fwd(lib, B=-1) == INVALID
     assert _fwd(lib, cu=None) == INVALID
     assert _fwd(lib, loss=None) == INVALID
