@@ -101,6 +101,7 @@ typedef enum {
 #define CTC_PACKED_DEV_LABEL_OUT_OF_RANGE 0x10u
 #define CTC_PACKED_DEV_WAIT_TIMEOUT 0x20u /* a bounded wait inside a kernel gave up */
 #define CTC_PACKED_DEV_NO_GRAD_STATE 0x40u /* backward after a CTC_PACKED_FLAG_LOSS_ONLY forward: rows left zero */
+#define CTC_PACKED_DEV_BAD_FSA 0x80u       /* FSA path: a sequence's states, edges or offsets out of range */
 
 /* Flags of ctc_packed_forward. */
 #define CTC_PACKED_FLAG_LOSS_ONLY 0x1u /* skip the work only the backward needs; ctc_packed_backward then fails */
@@ -232,6 +233,55 @@ ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_d
                                              const int32_t* targets, const int32_t* target_lengths, int32_t B,
                                              int32_t max_target_len, int32_t blank, int zero_infinity,
                                              ctc_packed_reduction reduction, float* loss, cudaStream_t stream);
+
+/*
+ * Full-sum loss over a generic FSA on the same packed layout.
+ *
+ * Page "feat(asr): native CTC loss kernel over sequence-packed log
+ * probabilities", ctc_loss.py, module docstring: the packed CTC loss follows
+ * RETURNN's packed full-sum loss over a generic FSA edge list and differs by
+ * building the CTC topology into its recursion.  These calls take the
+ * topology as data instead.
+ *
+ * Sequence b (frames as in ctc_packed_forward: rows cu_seqlens[b] ..
+ * cu_seqlens[b] + lengths[b]) owns:
+ *   - states [state_offsets[b], state_offsets[b+1]) of start_weight and
+ *     final_weight (num_states floats each, log weights, -inf: none);
+ *     1 <= states of a sequence <= max_states <= 4096;
+ *   - edges [edge_offsets[b], edge_offsets[b+1]) of `edges` (num_edges rows
+ *     of int32 (from, to, label), states local to the sequence, label in
+ *     [0, D)) with a log weight each in edge_weight.
+ * Every edge consumes one frame.  The loss is -log of the sum over all paths
+ * of lengths[b] edges of exp(start + edge weights + lp of the edges' labels
+ * + final); +inf with no path (0 with zero_infinity).  The backward writes
+ * scale_b * (exp(lp[t, c]) - sum of the occupancies of frame t's edges with
+ * label c), scale_b = grad_loss[b] (0 for an infinite loss), and 0 on rows
+ * outside every sequence; the page's gradient convention (the gradient with
+ * respect to the logits of a log_softmax).  The recursions run in float32 log
+ * space with shared-memory atomics: the last bits depend on the run.
+ *
+ * All pointers are device memory.  Errors the host can see return before
+ * anything is enqueued; malformed FSA data or lengths set the status word
+ * (ctc_packed_read_status works on this workspace) and a NaN loss.  The
+ * workspace holds the status word, each sequence's log-sum and every frame's
+ * forward values; pass it unchanged to the backward.
+ */
+size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states);
+ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                         const int32_t* cu_seqlens, const int32_t* lengths, int32_t B,
+                                         const int32_t* state_offsets, const float* start_weight,
+                                         const float* final_weight, int32_t num_states, const int32_t* edge_offsets,
+                                         const int32_t* edges, const float* edge_weight, int32_t num_edges,
+                                         int32_t max_states, int zero_infinity, float* loss, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream);
+ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                          const int32_t* cu_seqlens, const int32_t* lengths, int32_t B,
+                                          const int32_t* state_offsets, const float* start_weight,
+                                          const float* final_weight, int32_t num_states,
+                                          const int32_t* edge_offsets, const int32_t* edges,
+                                          const float* edge_weight, int32_t num_edges, int32_t max_states,
+                                          int zero_infinity, const float* grad_loss, void* workspace,
+                                          size_t workspace_bytes, void* grad_log_probs, cudaStream_t stream);
 
 /* Human-readable name of a ctc_packed_status value (static storage). */
 const char* ctc_packed_status_string(ctc_packed_status status);

@@ -26,6 +26,7 @@ __all__ = [
     "ctc_packed_read_status", "ctc_packed_status_string", "packed_ctc_loss", "PackedCTCLoss", "Workspace",
     "DTYPE_CODES", "REDUCTION_CODES", "DEVICE_STATUS_BITS", "CTCPackedError",
     "ctc_packed_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "FLAG_LOSS_ONLY", "FLAG_LOGITS",
+    "ctc_packed_fsa_workspace_size", "ctc_packed_fsa_forward", "ctc_packed_fsa_backward",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +45,7 @@ DEVICE_STATUS_BITS = {
     0x10: "target ids must lie in [0, D)",
     0x20: "a bounded wait inside a kernel gave up",
     0x40: "backward after a loss-only forward",
+    0x80: "FSA states, edges or offsets out of range",
 }
 
 _lib = None
@@ -79,6 +81,14 @@ def load_library(path: Optional[str] = None):
     lib.ctc_packed_forward_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32,
                                                ctypes.c_int, ctypes.c_int, vp, vp]
     lib.ctc_packed_forward_noalloc.restype = ctypes.c_int
+    lib.ctc_packed_fsa_workspace_size.argtypes = [i64, i32, i32]
+    lib.ctc_packed_fsa_workspace_size.restype = sz
+    lib.ctc_packed_fsa_forward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, i32,
+                                           i32, ctypes.c_int, vp, vp, sz, vp]
+    lib.ctc_packed_fsa_forward.restype = ctypes.c_int
+    lib.ctc_packed_fsa_backward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp,
+                                            i32, i32, ctypes.c_int, vp, vp, sz, vp, vp]
+    lib.ctc_packed_fsa_backward.restype = ctypes.c_int
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -143,6 +153,36 @@ def ctc_packed_forward_noalloc(log_probs, cu_seqlens, lengths, targets, target_l
         _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
         _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
         int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(loss), _stream(stream)))
+
+
+def ctc_packed_fsa_workspace_size(T_total: int, B: int, max_states: int) -> int:
+    return int(load_library().ctc_packed_fsa_workspace_size(T_total, B, max_states))
+
+
+def _fsa_args(log_probs, cu_seqlens, lengths, fsa):
+    """Marshal the FSA tensors: fsa = (state_offsets, start_weight,
+    final_weight, edge_offsets, edges (E, 3) int32, edge_weight)."""
+    so, sw, fw, eo, ed, ew = fsa
+    T_total, D = log_probs.shape
+    return (_ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
+            lengths.numel(), _ptr(so), _ptr(sw), _ptr(fw), sw.numel(), _ptr(eo),
+            _ptr(ed) if ed.numel() else None, _ptr(ew) if ew.numel() else None, ed.shape[0])
+
+
+def ctc_packed_fsa_forward(log_probs, cu_seqlens, lengths, fsa, max_states: int, zero_infinity: bool, loss,
+                           workspace, stream=None):
+    """Enqueue the FSA full-sum forward (per-sequence losses into `loss`)."""
+    _check(load_library().ctc_packed_fsa_forward(
+        *_fsa_args(log_probs, cu_seqlens, lengths, fsa), max_states, int(bool(zero_infinity)), _ptr(loss),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ctc_packed_fsa_backward(log_probs, cu_seqlens, lengths, fsa, max_states: int, zero_infinity: bool, grad_loss,
+                            workspace, grad_log_probs, stream=None):
+    """Enqueue the FSA full-sum backward (gradient rows into `grad_log_probs`)."""
+    _check(load_library().ctc_packed_fsa_backward(
+        *_fsa_args(log_probs, cu_seqlens, lengths, fsa), max_states, int(bool(zero_infinity)), _ptr(grad_loss),
+        _ptr(workspace), workspace.numel(), _ptr(grad_log_probs), _stream(stream)))
 
 
 def ctc_packed_read_status(workspace, stream=None) -> int:

@@ -1,0 +1,489 @@
+// Full-sum loss over a generic FSA on the packed layout: the topology the
+// CTC kernels build into their recursion, given instead as an edge list.
+//
+// Page "feat(asr): native CTC loss kernel over sequence-packed log
+// probabilities", ctc_loss.py, module docstring: the packed CTC loss follows
+// RETURNN's packed full-sum loss over a generic FSA edge list (scores
+// addressed in the token-flat buffer through per-sequence start offsets,
+// posteriors scattered back into a buffer of the same layout, the gradient
+// exp(log_probs) - posterior masked per frame); it differs by building the
+// CTC topology into the recursion.  This file is that generic form.
+//
+// Sequence b owns states [state_offsets[b], state_offsets[b+1]) of the start
+// and final weight arrays (log weights, -inf: none) and edges
+// [edge_offsets[b], edge_offsets[b+1]) of (from, to, label) with a log
+// weight each, state ids local to the sequence; every edge consumes one
+// frame.  With lp the sequence's rows:
+//   alpha_0(s) = start(s),  alpha_{t+1}(s') = logsumexp_{e=(s,s',c,w)} alpha_t(s) + w + lp[t, c]
+//   Z = logsumexp_s alpha_T(s) + final(s),  loss = -Z
+//   beta_T(s) = final(s),   beta_t(s) = logsumexp_{e=(s,s',c,w)} w + lp[t, c] + beta_{t+1}(s')
+//   grad[t, c] = scale * (exp(lp[t, c]) - sum_{e with label c} exp(alpha_t(s) + w + lp[t, c] + beta_{t+1}(s') - Z))
+//
+// One CTA per sequence walks its frames; the states' values sit in shared
+// memory in float32 log space and each frame's log-sum-exp over the edges
+// into a state is two passes over the edges: an atomic maximum (on an
+// order-preserving integer key), then an atomic sum of exp(v - max).  The
+// shared-memory atomics make the summation order, and so the last bits,
+// run-dependent (as the page's own label scatter is).  The forward stores
+// alpha_t of every frame in the workspace; the backward runs beta, forms the
+// edge occupancies, sums them per class in a shared row of D values and
+// writes each gradient row densely, in the log probabilities' dtype.
+#include <cstdint>
+
+#include "ctc_common.cuh"
+#include "ctc_kernels.h"
+
+namespace ctcp {
+
+namespace {
+
+constexpr int kFsaThreads = 256;
+
+// Workspace of the FSA path: status header, log Z per sequence (double),
+// each frame's forward values relative to the frame's own offset (float)
+// and that offset (double).
+struct FsaLayout {
+    size_t off_z, off_coff, off_alpha, total;
+};
+__host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int32_t max_states) {
+    FsaLayout L{};
+    size_t o = 256;  // the status word sits at offset 0, as in the CTC workspace
+    L.off_z = o;
+    o = align_up(o + sizeof(double) * (size_t)(B > 0 ? B : 1), 256);
+    L.off_coff = o;
+    o = align_up(o + sizeof(double) * (size_t)T_total, 256);
+    L.off_alpha = o;
+    o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)max_states, 256);
+    L.total = o;
+    return L;
+}
+
+struct FsaArgs {
+    const void* lp;
+    int64_t T_total;
+    int D;
+    const int32_t* cu;
+    const int32_t* lengths;
+    int B;
+    const int32_t* state_offsets;
+    const float* start_weight;
+    const float* final_weight;
+    const int32_t* edge_offsets;
+    const int32_t* edges;  // (from, to, label) per edge
+    const float* edge_weight;
+    int max_states;
+    int S_total;  // entries of the start / final weight arrays
+    int E_total;  // edges
+    int zero_infinity;
+    float* loss;
+    const float* grad_loss;
+    void* grad;
+    void* ws;
+    FsaLayout L;
+};
+
+// Order-preserving map of a float onto a signed int (and back), so that an
+// integer atomic maximum is a float maximum.
+__device__ __forceinline__ int fkey(float f) {
+    const int b = __float_as_int(f);
+    return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float fdekey(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
+template <int DT>
+__device__ __forceinline__ float lp_at(const void* lp, int64_t idx) {
+    if constexpr (DT == 0) {
+        return reinterpret_cast<const float*>(lp)[idx];
+    } else {
+        return bits_to_float<DT>(reinterpret_cast<const unsigned short*>(lp)[idx]);
+    }
+}
+
+// Checks sequence b's sizes and edges; returns false (and flags the status)
+// when the sequence cannot be run.
+__device__ bool fsa_check(const FsaArgs& a, int b, int S, int e0, int E, int64_t start, int T, bool& bad_label) {
+    Control* ctrl = ws_at<Control>(a.ws, 0);
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    const int64_t span = (int64_t)a.cu[b + 1] - start;
+    const int s0 = a.state_offsets[b];
+    if (threadIdx.x == 0) {
+        if (S < 1 || S > a.max_states || E < 0 || s0 < 0 || (int64_t)s0 + S > a.S_total || e0 < 0 ||
+            (int64_t)e0 + E > a.E_total)
+            atomicOr(&s_bad, 1);
+        if (start < 0 || span < 0 || (int64_t)a.cu[b + 1] > a.T_total || T < 0 || T > span) atomicOr(&s_bad, 4);
+    }
+    __syncthreads();
+    if (s_bad == 0) {  // the edge range is known to lie inside the edge array
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int* ed = a.edges + 3 * (size_t)(e0 + e);
+            if (ed[0] < 0 || ed[0] >= S || ed[1] < 0 || ed[1] >= S) atomicOr(&s_bad, 1);
+            if (ed[2] < 0 || ed[2] >= a.D) atomicOr(&s_bad, 2);
+        }
+    }
+    __syncthreads();
+    const int bad = s_bad;
+    if (threadIdx.x == 0 && bad) {
+        set_status(ctrl, (bad & 1 ? CTC_PACKED_DEV_BAD_FSA : 0u) | (bad & 2 ? CTC_PACKED_DEV_LABEL_OUT_OF_RANGE : 0u) |
+                             (bad & 4 ? CTC_PACKED_DEV_BAD_LENGTH : 0u));
+    }
+    bad_label = bad != 0;
+    return bad == 0;
+}
+
+// Block-wide maximum of v[0 .. n).
+__device__ float block_max(const float* v, int n, float* red) {
+    float m = -INFINITY;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, v[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = -INFINITY;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+    __syncthreads();
+    return m;
+}
+
+// Shifts v[0 .. n) down by its maximum (when finite) and returns the shift:
+// the recursions keep every frame's values near 0, so their float32 rounding
+// stays relative to the frame, and carry the shifts in double.
+__device__ float renormalise(float* v, int n, float* red) {
+    const float m = block_max(v, n, red);
+    if (m > -INFINITY && m < INFINITY) {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) v[i] -= m;
+        __syncthreads();
+        return m;
+    }
+    return 0.0f;
+}
+
+// Block-wide logsumexp of v[0 .. n) (one value per thread slot, strided).
+__device__ float block_lse(const float* v, const float* w, int n, float* red) {
+    float m = -INFINITY;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, v[i] + w[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = -INFINITY;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+    __syncthreads();
+    float s = 0.0f;
+    if (m > -INFINITY)
+        for (int i = threadIdx.x; i < n; i += blockDim.x) s += expf(v[i] + w[i] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    s = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
+    __syncthreads();
+    return m > -INFINITY ? m + logf(s) : -INFINITY;
+}
+
+}  // namespace
+
+template <int DT>
+__global__ void __launch_bounds__(kFsaThreads) fsa_forward_kernel(FsaArgs a) {
+    extern __shared__ __align__(16) float fsa_smem[];
+    __shared__ float red[kFsaThreads / 32];
+    const int b = blockIdx.x;
+    const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
+    const int e0 = a.edge_offsets[b], E = a.edge_offsets[b + 1] - e0;
+    const int64_t start = a.cu[b];
+    const int T = a.lengths[b];
+    double* z_out = ws_at<double>(a.ws, a.L.off_z);
+    double* coff = ws_at<double>(a.ws, a.L.off_coff);
+    bool bad = false;
+    if (!fsa_check(a, b, S, e0, E, start, T, bad)) {
+        if (threadIdx.x == 0) {
+            z_out[b] = __longlong_as_double(0x7ff8000000000000ll);
+            a.loss[b] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
+    float* al = fsa_smem;                                   // alpha_t
+    int* mk = reinterpret_cast<int*>(fsa_smem + a.max_states);  // max key per state
+    float* sm = fsa_smem + 2 * a.max_states;                // sum per state
+    float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
+    for (int s = threadIdx.x; s < S; s += blockDim.x) al[s] = a.start_weight[s0 + s];
+    __syncthreads();
+    double C = renormalise(al, S, red);  // alpha_t = al + C
+    for (int t = 0; t < T; ++t) {
+        float* row = alpha_rows + (start + t) * (int64_t)a.max_states;
+        if (threadIdx.x == 0) coff[start + t] = C;
+        for (int s = threadIdx.x; s < S; s += blockDim.x) {
+            row[s] = al[s];
+            mk[s] = fkey(-INFINITY);
+            sm[s] = 0.0f;
+        }
+        __syncthreads();
+        const int64_t lrow = (start + t) * (int64_t)a.D;
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int* ed = a.edges + 3 * (size_t)(e0 + e);
+            const float v = al[ed[0]] + a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]);
+            if (v > -INFINITY) atomicMax(&mk[ed[1]], fkey(v));
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int* ed = a.edges + 3 * (size_t)(e0 + e);
+            const float v = al[ed[0]] + a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]);
+            if (v > -INFINITY) atomicAdd(&sm[ed[1]], expf(v - fdekey(mk[ed[1]])));
+        }
+        __syncthreads();
+        for (int s = threadIdx.x; s < S; s += blockDim.x)
+            al[s] = sm[s] > 0.0f ? fdekey(mk[s]) + logf(sm[s]) : (sm[s] != sm[s] ? sm[s] : -INFINITY);
+        __syncthreads();
+        C += renormalise(al, S, red);
+    }
+    const float zr = block_lse(al, a.final_weight + s0, S, red);
+    if (threadIdx.x == 0) {
+        const double Z = zr > -INFINITY ? C + (double)zr : (double)zr;
+        z_out[b] = Z;
+        float l = (float)-Z;
+        if (a.zero_infinity && Z == -INFINITY) l = 0.0f;
+        a.loss[b] = l;
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
+    using El = Elem<DT>;
+    extern __shared__ __align__(16) float fsa_smem[];
+    const int b = blockIdx.x;
+    const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
+    const int e0 = a.edge_offsets[b], E = a.edge_offsets[b + 1] - e0;
+    const int64_t start = a.cu[b];
+    const int T = a.lengths[b];
+    __shared__ float red[kFsaThreads / 32];
+    const double Z = ws_at<double>(a.ws, a.L.off_z)[b];
+    const double* coff = ws_at<double>(a.ws, a.L.off_coff);
+    bool bad = false;
+    if (!fsa_check(a, b, S, e0, E, start, T, bad)) return;  // rows left as they are: the loss is NaN
+    float scale = a.grad_loss[b];
+    if (!(Z > -INFINITY)) scale = 0.0f;  // no path: zero rows (defined only with zero_infinity)
+    float* be = fsa_smem;                                   // beta_{t+1}
+    int* mk = reinterpret_cast<int*>(fsa_smem + a.max_states);
+    float* sm = fsa_smem + 2 * a.max_states;
+    float* P = fsa_smem + 3 * a.max_states;                 // class occupancies of the frame, D values
+    const float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
+    for (int s = threadIdx.x; s < S; s += blockDim.x) be[s] = a.final_weight[s0 + s];
+    __syncthreads();
+    double Dn = renormalise(be, S, red);  // beta_{t+1} = be + Dn
+    for (int t = T - 1; t >= 0; --t) {
+        // occupancy exponent: alpha row + edge + beta, plus this constant
+        const float K = scale != 0.0f ? (float)(coff[start + t] + Dn - Z) : 0.0f;
+        for (int s = threadIdx.x; s < S; s += blockDim.x) {
+            mk[s] = fkey(-INFINITY);
+            sm[s] = 0.0f;
+        }
+        for (int c = threadIdx.x; c < a.D; c += blockDim.x) P[c] = 0.0f;
+        __syncthreads();
+        const int64_t lrow = (start + t) * (int64_t)a.D;
+        const float* arow = alpha_rows + (start + t) * (int64_t)a.max_states;
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int* ed = a.edges + 3 * (size_t)(e0 + e);
+            const float v = a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]) + be[ed[1]];
+            if (v > -INFINITY) atomicMax(&mk[ed[0]], fkey(v));
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int* ed = a.edges + 3 * (size_t)(e0 + e);
+            const float v = a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]) + be[ed[1]];
+            if (v > -INFINITY) {
+                atomicAdd(&sm[ed[0]], expf(v - fdekey(mk[ed[0]])));
+                if (scale != 0.0f) {
+                    const float occ = expf(arow[ed[0]] + v + K);
+                    if (occ > 0.0f) atomicAdd(&P[ed[2]], occ);
+                }
+            }
+        }
+        __syncthreads();
+        // the dense gradient row, in the input dtype
+        for (int c = threadIdx.x; c < a.D; c += blockDim.x) {
+            const float x = lp_at<DT>(a.lp, lrow + c);
+            const float g = scale != 0.0f ? scale * (expf(x) - P[c]) : 0.0f;
+            if constexpr (El::bytes == 4) {
+                reinterpret_cast<float*>(a.grad)[lrow + c] = g;
+            } else {
+                reinterpret_cast<unsigned short*>(a.grad)[lrow + c] = (unsigned short)pack1<DT>(g);
+            }
+        }
+        for (int s = threadIdx.x; s < S; s += blockDim.x)
+            be[s] = sm[s] > 0.0f ? fdekey(mk[s]) + logf(sm[s]) : (sm[s] != sm[s] ? sm[s] : -INFINITY);
+        __syncthreads();
+        Dn += renormalise(be, S, red);
+    }
+}
+
+// Rows outside every sequence get a zero gradient.
+template <int DT>
+__global__ void fsa_zero_uncovered_kernel(FsaArgs a) {
+    using El = Elem<DT>;
+    for (int64_t row = blockIdx.x; row < a.T_total; row += gridDim.x) {
+        int lo = 0, hi = a.B - 1, b = -1;
+        while (lo <= hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)a.cu[mid] <= row) {
+                b = mid;
+                lo = mid + 1;
+            } else {
+                hi = mid - 1;
+            }
+        }
+        // rows of a sequence that fails its checks stay as they are
+        const bool covered = b >= 0 && row - a.cu[b] < a.lengths[b] && a.lengths[b] >= 0;
+        if (covered) continue;
+        for (int c = threadIdx.x; c < a.D; c += blockDim.x) {
+            if constexpr (El::bytes == 4) {
+                reinterpret_cast<float*>(a.grad)[row * a.D + c] = 0.0f;
+            } else {
+                reinterpret_cast<unsigned short*>(a.grad)[row * a.D + c] = 0;
+            }
+        }
+    }
+}
+
+}  // namespace ctcp
+
+using namespace ctcp;
+
+namespace {
+
+bool fsa_valid_dtype(int d) { return d == CTC_PACKED_F32 || d == CTC_PACKED_BF16 || d == CTC_PACKED_F16; }
+
+ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_total, int32_t D, const int32_t* cu,
+                                 const int32_t* lengths, int32_t B, const int32_t* so, const float* sw,
+                                 const float* fw, int32_t S_total, const int32_t* eo, const int32_t* edges,
+                                 const float* ew, int32_t E_total, int32_t max_states, const void* ws,
+                                 size_t ws_bytes) {
+    if (!fsa_valid_dtype(dtype) || T_total < 0 || B < 0 || D < 1 || S_total < 0 || E_total < 0)
+        return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (D > kMaxD || T_total > INT32_MAX || max_states < 1 || max_states > kFsaMaxStates)
+        return CTC_PACKED_ERR_UNSUPPORTED;
+    if (cu == nullptr || so == nullptr || eo == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && (lengths == nullptr || sw == nullptr || fw == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (E_total > 0 && (edges == nullptr || ew == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (T_total > 0 && log_probs == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(log_probs) % (dtype == CTC_PACKED_F32 ? 4 : 2) != 0)
+        return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return CTC_PACKED_ERR_WORKSPACE;
+    if (ws_bytes < fsa_layout(T_total, B, max_states).total) return CTC_PACKED_ERR_WORKSPACE;
+    return CTC_PACKED_OK;
+}
+
+// A plain launch (no early start): these kernels read what the kernel before
+// them on the stream wrote without a programmatic wait.
+template <typename K>
+cudaError_t launch_fsa(K kernel, unsigned grid, size_t smem, cudaStream_t s, const FsaArgs& a) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kFsaThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const int32_t* cu, const int32_t* lengths,
+                      int32_t B, const int32_t* so, const float* sw, const float* fw, int32_t S_total,
+                      const int32_t* eo, const int32_t* edges, const float* ew, int32_t E_total, int32_t max_states,
+                      int zero_infinity, void* ws) {
+    FsaArgs a{};
+    a.lp = log_probs;
+    a.T_total = T_total;
+    a.D = D;
+    a.cu = cu;
+    a.lengths = lengths;
+    a.B = B;
+    a.state_offsets = so;
+    a.start_weight = sw;
+    a.final_weight = fw;
+    a.edge_offsets = eo;
+    a.edges = edges;
+    a.edge_weight = ew;
+    a.max_states = max_states;
+    a.S_total = S_total;
+    a.E_total = E_total;
+    a.zero_infinity = zero_infinity ? 1 : 0;
+    a.ws = ws;
+    a.L = fsa_layout(T_total, B, max_states);
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states) {
+    if (T_total < 0 || B < 0 || max_states < 1 || max_states > kFsaMaxStates || T_total > INT32_MAX) return 0;
+    return fsa_layout(T_total, B, max_states).total;
+}
+
+ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                         const int32_t* cu_seqlens, const int32_t* lengths, int32_t B,
+                                         const int32_t* state_offsets, const float* start_weight,
+                                         const float* final_weight, int32_t num_states, const int32_t* edge_offsets,
+                                         const int32_t* edges, const float* edge_weight, int32_t num_edges,
+                                         int32_t max_states, int zero_infinity, float* loss, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream) {
+    const ctc_packed_status st =
+        fsa_check_args(log_probs, dtype, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
+                       final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states, workspace,
+                       workspace_bytes);
+    if (st != CTC_PACKED_OK) return st;
+    if (B > 0 && loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    // the status word is cleared on the stream, before the kernels can set it
+    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    if (B == 0) return CTC_PACKED_OK;
+    FsaArgs a = make_fsa_args(log_probs, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
+                              final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states,
+                              zero_infinity, workspace);
+    a.loss = loss;
+    const size_t smem = sizeof(float) * 3 * (size_t)max_states;
+    cudaError_t e = dtype == CTC_PACKED_F32    ? launch_fsa(fsa_forward_kernel<0>, (unsigned)B, smem, stream, a)
+                    : dtype == CTC_PACKED_BF16 ? launch_fsa(fsa_forward_kernel<1>, (unsigned)B, smem, stream, a)
+                                               : launch_fsa(fsa_forward_kernel<2>, (unsigned)B, smem, stream, a);
+    return e == cudaSuccess ? CTC_PACKED_OK : CTC_PACKED_ERR_CUDA;
+}
+
+ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                          const int32_t* cu_seqlens, const int32_t* lengths, int32_t B,
+                                          const int32_t* state_offsets, const float* start_weight,
+                                          const float* final_weight, int32_t num_states,
+                                          const int32_t* edge_offsets, const int32_t* edges,
+                                          const float* edge_weight, int32_t num_edges, int32_t max_states,
+                                          int zero_infinity, const float* grad_loss, void* workspace,
+                                          size_t workspace_bytes, void* grad_log_probs, cudaStream_t stream) {
+    const ctc_packed_status st =
+        fsa_check_args(log_probs, dtype, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
+                       final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states, workspace,
+                       workspace_bytes);
+    if (st != CTC_PACKED_OK) return st;
+    if (T_total == 0) return CTC_PACKED_OK;
+    if (grad_log_probs == nullptr || (B > 0 && grad_loss == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const int eb = dtype == CTC_PACKED_F32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(grad_log_probs) % eb != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(grad_log_probs), l0 = reinterpret_cast<uintptr_t>(log_probs);
+    const uintptr_t nbytes = (uintptr_t)(T_total * (int64_t)D * eb);
+    if (g0 < l0 + nbytes && l0 < g0 + nbytes) return CTC_PACKED_ERR_INVALID_ARGUMENT;  // overlap
+    FsaArgs a = make_fsa_args(log_probs, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
+                              final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states,
+                              zero_infinity, workspace);
+    a.grad_loss = grad_loss;
+    a.grad = grad_log_probs;
+    const size_t smem = sizeof(float) * (3 * (size_t)max_states + (size_t)D);
+    cudaError_t e = cudaSuccess;
+    if (B > 0) {
+        e = dtype == CTC_PACKED_F32    ? launch_fsa(fsa_backward_kernel<0>, (unsigned)B, smem, stream, a)
+            : dtype == CTC_PACKED_BF16 ? launch_fsa(fsa_backward_kernel<1>, (unsigned)B, smem, stream, a)
+                                       : launch_fsa(fsa_backward_kernel<2>, (unsigned)B, smem, stream, a);
+        if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    }
+    const unsigned zgrid = (unsigned)(T_total < 4096 ? T_total : 4096);
+    e = dtype == CTC_PACKED_F32    ? launch_fsa(fsa_zero_uncovered_kernel<0>, zgrid, 0, stream, a)
+        : dtype == CTC_PACKED_BF16 ? launch_fsa(fsa_zero_uncovered_kernel<1>, zgrid, 0, stream, a)
+                                   : launch_fsa(fsa_zero_uncovered_kernel<2>, zgrid, 0, stream, a);
+    return e == cudaSuccess ? CTC_PACKED_OK : CTC_PACKED_ERR_CUDA;
+}
+
+}  // extern "C"

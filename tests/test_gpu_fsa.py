@@ -1,0 +1,143 @@
+"""GPU parity of the generic FSA full-sum path (ctc_packed_fsa_forward /
+ctc_packed_fsa_backward) against the float64 FSA oracle.
+
+Cases: the CTC lattice written as an FSA (also checked against the CTC
+path), seeded random FSAs with weights, several start and final states and
+loops, in the three dtypes; a sequence without a path (with and without
+zero_infinity), frameless sequences and gap rows; a large vocabulary; and
+out-of-range FSA data, which must set the status word and a NaN loss.  The
+recursions run in float32 log space: losses within 1e-4 relative, float32
+gradients within 2e-5 (on these lengths), half types within one unit in the
+last place plus 1e-3.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import packed_sequence_ctc_gb300 as pk
+import workloads
+from oracle import fsa_oracle
+from tests.helpers import assert_grad_close, assert_loss_close, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lp, cu, lengths, fsa, max_states, zero_infinity=False, grad_loss=None, guard=64):
+    dev = "cuda"
+    T_total, D = lp.shape
+    B = lengths.numel()
+    fsa_d = tuple(x.to(dev).contiguous() for x in fsa)
+    cu_d, ln_d = cu.to(dev).to(torch.int32), lengths.to(dev).to(torch.int32)
+    lp_d = lp.to(dev).contiguous()
+    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, B, max_states), dtype=torch.uint8, device=dev)
+    loss = torch.full((B,), float("nan"), device=dev)
+    pk.ctc_packed_fsa_forward(lp_d, cu_d, ln_d, fsa_d, max_states, zero_infinity, loss, ws)
+    g = torch.ones(B) if grad_loss is None else torch.as_tensor(grad_loss, dtype=torch.float32)
+    n = T_total * D * lp.element_size()
+    raw = torch.full((n + 2 * guard,), 0xA5, dtype=torch.uint8, device=dev)
+    grad = raw[guard:guard + n].view(lp.dtype).view(T_total, D)
+    pk.ctc_packed_fsa_backward(lp_d, cu_d, ln_d, fsa_d, max_states, zero_infinity, g.to(dev), ws, grad)
+    torch.cuda.synchronize()
+    assert bool((raw[:guard] == 0xA5).all()) and bool((raw[guard + n:] == 0xA5).all()), "write outside the gradient"
+    status = pk.ctc_packed_read_status(ws)
+    return loss.double().cpu().numpy(), grad.clone(), status, g.numpy()
+
+
+def _oracle(lp, cu, lengths, fsa, grad_loss, zero_infinity=False):
+    so, sw, fw, eo, ed, ew = fsa
+    return fsa_oracle.fsa_loss_packed(lp, cu, lengths, so, sw, fw, eo, ed, ew, grad_loss=grad_loss,
+                                      zero_infinity=zero_infinity)
+
+
+def _max_states(fsa):
+    so = fsa[0]
+    return int((so[1:] - so[:-1]).max())
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ctc_lattice_as_fsa(cuda_device, dtype):
+    batch = workloads.make_batch([120, 90, 64, 30], [25, 20, 12, 5], 37, dtype=dtype, seed=17, repeat_prob=0.25,
+                                 redraw_infeasible=True, reduction="none")
+    offs = np.concatenate([[0], np.cumsum(batch.target_lengths.numpy())])
+    tg = batch.targets.numpy()
+    fsa = workloads.pack_fsas([workloads.ctc_lattice_fsa(tg[offs[b]:offs[b + 1]], batch.blank)
+                               for b in range(batch.B)])
+    loss, grad, status, g = _run(batch.log_probs, batch.cu_seqlens, batch.lengths, fsa, _max_states(fsa))
+    assert status == 0
+    ref_loss, ref_grad = _oracle(batch.log_probs, batch.cu_seqlens, batch.lengths, fsa, g)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)
+    # and the CTC path on the same batch
+    ctc_loss, ctc_grad, _ = run_gpu(batch)
+    assert_loss_close(loss, ctc_loss)
+    assert_grad_close(grad, ctc_grad.double().cpu().numpy(), dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_random_fsas(cuda_device, dtype):
+    lengths = [150, 77, 0, 33, 200]
+    gaps = [0, 3, 0, 2, 0]
+    D = 23
+    cu = [0]
+    for T, gp in zip(lengths, gaps):
+        cu.append(cu[-1] + T + gp)
+    gen = torch.Generator().manual_seed(5)
+    lp = torch.log_softmax(torch.randn(cu[-1], D, generator=gen) * 2.0, -1).to(dtype)
+    fsas = [workloads.random_fsa(S, E, D, seed=100 + i) for i, (S, E) in enumerate([(9, 30), (5, 12), (3, 5),
+                                                                                  (40, 150), (17, 60)])]
+    fsa = workloads.pack_fsas(fsas)
+    cu_t = torch.tensor(cu, dtype=torch.int32)
+    ln_t = torch.tensor(lengths, dtype=torch.int32)
+    gl = [1.0, -0.5, 2.0, 0.7, 1.3]
+    loss, grad, status, g = _run(lp, cu_t, ln_t, fsa, _max_states(fsa), grad_loss=gl)
+    assert status == 0
+    ref_loss, ref_grad = _oracle(lp, cu_t, ln_t, fsa, g)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)  # gap rows: 0 on both sides
+
+
+@pytest.mark.parametrize("zero_infinity", [True, False])
+def test_sequence_without_a_path(cuda_device, zero_infinity):
+    D = 7
+    lp = torch.log_softmax(torch.randn(30, D, generator=torch.Generator().manual_seed(2)), -1)
+    inf = float("-inf")
+    dead = ([0.0, inf], [inf, 0.0], [(0, 0, 1)], [0.0])  # the final state is never reached
+    live = workloads.random_fsa(6, 20, D, seed=9)
+    fsa = workloads.pack_fsas([live, dead])
+    cu = torch.tensor([0, 18, 30], dtype=torch.int32)
+    ln = torch.tensor([18, 12], dtype=torch.int32)
+    loss, grad, status, g = _run(lp, cu, ln, fsa, 6, zero_infinity=zero_infinity)
+    assert status == 0
+    ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g, zero_infinity=zero_infinity)
+    assert_loss_close(loss, ref_loss)
+    rows = slice(0, 30) if zero_infinity else slice(0, 18)
+    assert_grad_close(grad[rows], ref_grad[rows], torch.float32)
+
+
+def test_large_vocabulary_ctc_lattices(cuda_device):
+    batch = workloads.make_batch([97, 64, 40], [20, 12, 9], 8193, dtype=torch.bfloat16, seed=23, sigma=3.0,
+                                 label_high=8192, reduction="none")
+    offs = np.concatenate([[0], np.cumsum(batch.target_lengths.numpy())])
+    tg = batch.targets.numpy()
+    fsa = workloads.pack_fsas([workloads.ctc_lattice_fsa(tg[offs[b]:offs[b + 1]], batch.blank)
+                               for b in range(batch.B)])
+    loss, grad, status, g = _run(batch.log_probs, batch.cu_seqlens, batch.lengths, fsa, _max_states(fsa))
+    assert status == 0
+    ref_loss, ref_grad = _oracle(batch.log_probs, batch.cu_seqlens, batch.lengths, fsa, g)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, torch.bfloat16)
+
+
+def test_out_of_range_fsa_data_sets_the_status(cuda_device):
+    D = 5
+    lp = torch.log_softmax(torch.randn(20, D, generator=torch.Generator().manual_seed(4)), -1)
+    good = workloads.random_fsa(4, 10, D, seed=1)
+    bad_state = ([0.0, float("-inf")], [float("-inf"), 0.0], [(0, 7, 1)], [0.0])  # state 7 of 2
+    bad_label = ([0.0, float("-inf")], [float("-inf"), 0.0], [(0, 1, 9)], [0.0])  # class 9 of 5
+    fsa = workloads.pack_fsas([good, bad_state, bad_label])
+    cu = torch.tensor([0, 8, 14, 20], dtype=torch.int32)
+    ln = torch.tensor([8, 6, 6], dtype=torch.int32)
+    loss, _, status, _ = _run(lp, cu, ln, fsa, 4)
+    assert status & 0x80 and status & 0x10
+    assert np.isfinite(loss[0]) and np.isnan(loss[1]) and np.isnan(loss[2])

@@ -247,6 +247,77 @@ def unnormalised_logits(batch: Batch, seed: int = 0, offset: float = 8.0) -> tor
     return z.to(batch.log_probs.dtype)
 
 
+def pack_fsas(fsas):
+    """Concatenate per-sequence FSAs ``(start, final, edges (E, 3), weights)``
+    into the packed arrays of the FSA entry points: ``(state_offsets,
+    start_weight, final_weight, edge_offsets, edges, edge_weight)`` as
+    int32 / float32 CPU tensors."""
+    so, eo = [0], [0]
+    sw, fw, ed, ew = [], [], [], []
+    for start, final, edges, weights in fsas:
+        sw += list(start)
+        fw += list(final)
+        ed += [list(e) for e in edges]
+        ew += list(weights)
+        so.append(so[-1] + len(start))
+        eo.append(eo[-1] + len(edges))
+    return (torch.tensor(so, dtype=torch.int32), torch.tensor(sw, dtype=torch.float32),
+            torch.tensor(fw, dtype=torch.float32), torch.tensor(eo, dtype=torch.int32),
+            torch.tensor(ed, dtype=torch.int32).reshape(-1, 3), torch.tensor(ew, dtype=torch.float32))
+
+
+def ctc_lattice_fsa(targets: Sequence[int], blank: int):
+    """The CTC lattice of one target sequence as FSA data: states 0 .. 2U of
+    ``blank, l_1, blank, ..., l_U, blank`` plus an entry state 2U + 1; each
+    state's edges into itself, into the next state and (from a label over a
+    blank to a different label) two states on, each labelled with the class
+    of the state it enters; the entry state starts, the last two states end
+    (and the entry state too for an empty target)."""
+    U = len(targets)
+    S = 2 * U + 1
+    ext = [blank if s % 2 == 0 else int(targets[(s - 1) // 2]) for s in range(S)]
+    edges = []
+    for s in range(S):
+        edges.append((s, s, ext[s]))
+        if s + 1 < S:
+            edges.append((s, s + 1, ext[s + 1]))
+        if s + 2 < S and s % 2 == 1 and ext[s + 2] != ext[s]:
+            edges.append((s, s + 2, ext[s + 2]))
+    edges.append((S, 0, ext[0]))
+    if S > 1:
+        edges.append((S, 1, ext[1]))
+    inf = float("-inf")
+    start = [inf] * (S + 1)
+    start[S] = 0.0
+    final = [inf] * (S + 1)
+    final[S - 1] = 0.0
+    if S > 1:
+        final[S - 2] = 0.0
+    if U == 0:
+        final[S] = 0.0
+    return start, final, edges, [0.0] * len(edges)
+
+
+def random_fsa(num_states: int, num_edges: int, num_classes: int, seed: int):
+    """A seeded random FSA: a left-to-right chain (so that paths exist) plus
+    random extra edges, N(0, 0.5^2) edge weights, state 0 starting and the
+    last state ending with weight 0, a few more start and final states."""
+    gen = torch.Generator().manual_seed(seed)
+    S = num_states
+    edges = [(s, s + 1, int(torch.randint(0, num_classes, (1,), generator=gen))) for s in range(S - 1)]
+    edges += [(s, s, int(torch.randint(0, num_classes, (1,), generator=gen))) for s in range(S)]
+    while len(edges) < num_edges:
+        a, b, c = (int(torch.randint(0, n, (1,), generator=gen)) for n in (S, S, num_classes))
+        edges.append((a, b, c))
+    weights = (torch.randn(len(edges), generator=gen) * 0.5).tolist()
+    inf = float("-inf")
+    start = [0.0] + [(float(torch.randn(1, generator=gen)) * 0.3 if float(torch.rand(1, generator=gen)) < 0.2
+                      else inf) for _ in range(S - 1)]
+    final = [(float(torch.randn(1, generator=gen)) * 0.3 if float(torch.rand(1, generator=gen)) < 0.2 else inf)
+             for _ in range(S - 1)] + [0.0]
+    return start, final, edges, weights
+
+
 def padded_targets(batch: Batch, width: Optional[int] = None, fill: int = 0) -> torch.Tensor:
     """The concatenated targets as a padded ``(B, width)`` int64 tensor."""
     width = batch.max_target_len if width is None else width
