@@ -73,6 +73,8 @@ def _args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--input", default="log_probs", choices=["log_probs", "logits"],
                    help="logits: the rows are unnormalised logits and the path takes log_softmax itself")
+    p.add_argument("--topology", default="ctc", choices=["ctc", "fsa"],
+                   help="fsa: the same utterances' CTC lattices through the generic FSA path")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return p.parse_args()
 
@@ -493,10 +495,96 @@ def _e2e(args, pk, torch, batch, dev, stream, lp, ws, mtl, red, nloss, world, ff
                        "overlapping the previous step's compute"}
 
 
+def run_fsa(args):
+    """The workload's CTC lattices as FSA edge lists through the generic FSA
+    path (ctc_packed_fsa_forward + ctc_packed_fsa_backward), timed like the
+    CTC path; one JSON line."""
+    import numpy as np
+    import torch
+
+    import packed_sequence_ctc_gb300 as pk
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    batch = workloads.workload(args.workload, device=dev)
+    lp = batch.log_probs.contiguous()
+    offs = np.concatenate([[0], np.cumsum(batch.target_lengths.cpu().numpy())])
+    tg = batch.targets.cpu().numpy()
+    fsa_h = workloads.pack_fsas([workloads.ctc_lattice_fsa(tg[offs[b]:offs[b + 1]], batch.blank)
+                                 for b in range(batch.B)])
+    fsa = tuple(x.to(dev).contiguous() for x in fsa_h)
+    so = fsa_h[0]
+    max_states = int((so[1:] - so[:-1]).max())
+    cu, ln = batch.cu_seqlens.to(dev).to(torch.int32), batch.lengths.to(dev).to(torch.int32)
+    T_total, D = lp.shape
+    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, batch.B, max_states), dtype=torch.uint8, device=dev)
+    loss = torch.empty(batch.B, device=dev)
+    g_up = torch.ones(batch.B, device=dev)
+    grad = torch.empty_like(lp)
+    zi = batch.zero_infinity
+
+    def fwd():
+        pk.ctc_packed_fsa_forward(lp, cu, ln, fsa, max_states, zi, loss, ws, stream=stream)
+
+    def bwd():
+        pk.ctc_packed_fsa_backward(lp, cu, ln, fsa, max_states, zi, g_up, ws, grad, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    status = pk.ctc_packed_read_status(ws)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(_gpu_query_id(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for k in range(K):
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    sampler.snapshot()
+    time.sleep(0.25)
+    sampler.stop()
+    fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    ms = fwd_ms + bwd_ms
+    hbm_peak, peak_kind = _peaks()
+    e = lp.element_size()
+    dense = 2 * T_total * D * e  # the backward reads the rows and writes the gradient
+    achieved = dense / (bwd_ms / 1e3) / 1e9
+    cfg = _workload_description(batch, False)
+    cfg["topology"] = f"fsa: CTC lattices as edge lists ({int(fsa_h[4].shape[0])} edges, up to {max_states} states)"
+    cfg["parallelism"] = "single GPU"
+    line = {
+        "metric": METRIC, "value": round(batch.frames / (ms / 1e3), 1), "unit": "frames/s", "n_gpus": 1,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "kernel": "fsa_backward_kernel (the FSA backward call)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "peak_kind": f"{peak_kind} copy bandwidth (burst)", "algorithmic_bytes_per_launch": dense,
+                     "avg_launch_ms": round(bwd_ms, 5)},
+        "forward_ms": round(fwd_ms, 5), "backward_ms": round(bwd_ms, 5), "cpu_baseline": None, "e2e": None,
+        "gpu_launches": 3 * K, "clocks": sampler.summary(t0, t1), "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.topology == "fsa":
+        run_fsa(args)
     else:
         run_ours(args)
 
