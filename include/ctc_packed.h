@@ -23,7 +23,12 @@
  *     log_probs is a log_softmax output.  Rows outside every utterance are 0.
  *   - Reductions (file nemo/collections/asr/losses/ctc.py, forward_packed):
  *     NONE keeps the B losses, SUM adds them, MEAN divides each by
- *     max(target_length, 1) and averages over the B utterances.
+ *     max(target_length, 1) and averages over the B utterances; MEAN_BATCH
+ *     and MEAN_VOLUME are the module's further reductions (see the enum).
+ *   - The input may also be a model's unnormalised logits
+ *     (CTC_PACKED_FLAG_LOGITS): log_softmax is then taken inside the path.
+ *   - The same full-sum loss over a generic FSA edge list instead of the
+ *     CTC lattice: ctc_packed_fsa_forward / ctc_packed_fsa_backward.
  *   - Inputs may be float32, bfloat16 or float16; all arithmetic is float32
  *     (offsets that keep the recursion accurate are integers, the
  *     per-utterance log-likelihood is assembled in float64).
