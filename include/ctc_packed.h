@@ -255,7 +255,8 @@ ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_d
  *     1 <= states of a sequence <= max_states <= 4096;
  *   - edges [edge_offsets[b], edge_offsets[b+1]) of `edges` (num_edges rows
  *     of int32 (from, to, label), states local to the sequence, label in
- *     [0, D)) with a log weight each in edge_weight.
+ *     [0, D)) with a log weight each in edge_weight; max_labels bounds the
+ *     distinct labels of one sequence's edges (more: status bit, zero rows).
  * Every edge consumes one frame.  The loss is -log of the sum over all paths
  * of lengths[b] edges of exp(start + edge weights + lp of the edges' labels
  * + final); +inf with no path (0 with zero_infinity).  The backward writes
@@ -268,25 +269,28 @@ ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_d
  * All pointers are device memory.  Errors the host can see return before
  * anything is enqueued; malformed FSA data or lengths set the status word
  * (ctc_packed_read_status works on this workspace) and a NaN loss.  The
- * workspace holds the status word, each sequence's log-sum and every frame's
- * forward values; pass it unchanged to the backward.
+ * workspace holds the status word, each sequence's log-sum, every frame's
+ * forward values and, after the backward, each row's class sums; pass it
+ * unchanged from the forward to the backward.  The backward writes the dense
+ * gradient rows with the CTC path's all-SM gradient stream.
  */
-size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states);
+size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states, int32_t max_labels, int32_t D);
 ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
                                          const int32_t* cu_seqlens, const int32_t* lengths, int32_t B,
                                          const int32_t* state_offsets, const float* start_weight,
                                          const float* final_weight, int32_t num_states, const int32_t* edge_offsets,
                                          const int32_t* edges, const float* edge_weight, int32_t num_edges,
-                                         int32_t max_states, int zero_infinity, float* loss, void* workspace,
-                                         size_t workspace_bytes, cudaStream_t stream);
+                                         int32_t max_states, int32_t max_labels, int zero_infinity, float* loss,
+                                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
                                           const int32_t* cu_seqlens, const int32_t* lengths, int32_t B,
                                           const int32_t* state_offsets, const float* start_weight,
                                           const float* final_weight, int32_t num_states,
                                           const int32_t* edge_offsets, const int32_t* edges,
                                           const float* edge_weight, int32_t num_edges, int32_t max_states,
-                                          int zero_infinity, const float* grad_loss, void* workspace,
-                                          size_t workspace_bytes, void* grad_log_probs, cudaStream_t stream);
+                                          int32_t max_labels, int zero_infinity, const float* grad_loss,
+                                          void* workspace, size_t workspace_bytes, void* grad_log_probs,
+                                          cudaStream_t stream);
 
 /* Human-readable name of a ctc_packed_status value (static storage). */
 const char* ctc_packed_status_string(ctc_packed_status status);

@@ -81,13 +81,13 @@ def load_library(path: Optional[str] = None):
     lib.ctc_packed_forward_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32,
                                                ctypes.c_int, ctypes.c_int, vp, vp]
     lib.ctc_packed_forward_noalloc.restype = ctypes.c_int
-    lib.ctc_packed_fsa_workspace_size.argtypes = [i64, i32, i32]
+    lib.ctc_packed_fsa_workspace_size.argtypes = [i64, i32, i32, i32, i32]
     lib.ctc_packed_fsa_workspace_size.restype = sz
     lib.ctc_packed_fsa_forward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, i32,
-                                           i32, ctypes.c_int, vp, vp, sz, vp]
+                                           i32, i32, ctypes.c_int, vp, vp, sz, vp]
     lib.ctc_packed_fsa_forward.restype = ctypes.c_int
     lib.ctc_packed_fsa_backward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp,
-                                            i32, i32, ctypes.c_int, vp, vp, sz, vp, vp]
+                                            i32, i32, i32, ctypes.c_int, vp, vp, sz, vp, vp]
     lib.ctc_packed_fsa_backward.restype = ctypes.c_int
     if path == LIB_PATH:
         _lib = lib
@@ -155,8 +155,8 @@ def ctc_packed_forward_noalloc(log_probs, cu_seqlens, lengths, targets, target_l
         int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(loss), _stream(stream)))
 
 
-def ctc_packed_fsa_workspace_size(T_total: int, B: int, max_states: int) -> int:
-    return int(load_library().ctc_packed_fsa_workspace_size(T_total, B, max_states))
+def ctc_packed_fsa_workspace_size(T_total: int, B: int, max_states: int, max_labels: int, D: int) -> int:
+    return int(load_library().ctc_packed_fsa_workspace_size(T_total, B, max_states, max_labels, D))
 
 
 def _fsa_args(log_probs, cu_seqlens, lengths, fsa):
@@ -169,20 +169,20 @@ def _fsa_args(log_probs, cu_seqlens, lengths, fsa):
             _ptr(ed) if ed.numel() else None, _ptr(ew) if ew.numel() else None, ed.shape[0])
 
 
-def ctc_packed_fsa_forward(log_probs, cu_seqlens, lengths, fsa, max_states: int, zero_infinity: bool, loss,
-                           workspace, stream=None):
+def ctc_packed_fsa_forward(log_probs, cu_seqlens, lengths, fsa, max_states: int, max_labels: int,
+                           zero_infinity: bool, loss, workspace, stream=None):
     """Enqueue the FSA full-sum forward (per-sequence losses into `loss`)."""
     _check(load_library().ctc_packed_fsa_forward(
-        *_fsa_args(log_probs, cu_seqlens, lengths, fsa), max_states, int(bool(zero_infinity)), _ptr(loss),
-        _ptr(workspace), workspace.numel(), _stream(stream)))
+        *_fsa_args(log_probs, cu_seqlens, lengths, fsa), max_states, max_labels, int(bool(zero_infinity)),
+        _ptr(loss), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
-def ctc_packed_fsa_backward(log_probs, cu_seqlens, lengths, fsa, max_states: int, zero_infinity: bool, grad_loss,
-                            workspace, grad_log_probs, stream=None):
+def ctc_packed_fsa_backward(log_probs, cu_seqlens, lengths, fsa, max_states: int, max_labels: int,
+                            zero_infinity: bool, grad_loss, workspace, grad_log_probs, stream=None):
     """Enqueue the FSA full-sum backward (gradient rows into `grad_log_probs`)."""
     _check(load_library().ctc_packed_fsa_backward(
-        *_fsa_args(log_probs, cu_seqlens, lengths, fsa), max_states, int(bool(zero_infinity)), _ptr(grad_loss),
-        _ptr(workspace), workspace.numel(), _ptr(grad_log_probs), _stream(stream)))
+        *_fsa_args(log_probs, cu_seqlens, lengths, fsa), max_states, max_labels, int(bool(zero_infinity)),
+        _ptr(grad_loss), _ptr(workspace), workspace.numel(), _ptr(grad_log_probs), _stream(stream)))
 
 
 def ctc_packed_read_status(workspace, stream=None) -> int:

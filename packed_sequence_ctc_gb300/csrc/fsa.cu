@@ -43,10 +43,13 @@ constexpr int kFsaThreads = 256;
 // each frame's forward values relative to the frame's own offset (float)
 // and that offset (double).
 struct FsaLayout {
-    size_t off_z, off_coff, off_alpha, total;
+    size_t off_z, off_coff, off_alpha, off_head, off_ent, total;
+    int cap;  // class sums a row can hold: min(max_labels, D)
 };
-__host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int32_t max_states) {
+__host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int32_t max_states, int32_t max_labels,
+                                                int32_t D) {
     FsaLayout L{};
+    L.cap = max_labels < D ? max_labels : D;
     size_t o = 256;  // the status word sits at offset 0, as in the CTC workspace
     L.off_z = o;
     o = align_up(o + sizeof(double) * (size_t)(B > 0 ? B : 1), 256);
@@ -54,6 +57,12 @@ __host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int3
     o = align_up(o + sizeof(double) * (size_t)T_total, 256);
     L.off_alpha = o;
     o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)max_states, 256);
+    // per row: a header and the row's class sums, in the format the dense
+    // gradient stream of the CTC path reads
+    L.off_head = o;
+    o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
+    L.off_ent = o;
+    o = align_up(o + 8 * (size_t)T_total * (size_t)(L.cap > 0 ? L.cap : 1), 256);
     L.total = o;
     return L;
 }
@@ -72,6 +81,7 @@ struct FsaArgs {
     const int32_t* edges;  // (from, to, label) per edge
     const float* edge_weight;
     int max_states;
+    int max_labels;
     int S_total;  // entries of the start / final weight arrays
     int E_total;  // edges
     int zero_infinity;
@@ -250,25 +260,47 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_forward_kernel(FsaArgs a) {
 
 template <int DT>
 __global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
-    using El = Elem<DT>;
     extern __shared__ __align__(16) float fsa_smem[];
+    __shared__ float red[kFsaThreads / 32];
+    __shared__ int s_nlab;
     const int b = blockIdx.x;
     const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
     const int e0 = a.edge_offsets[b], E = a.edge_offsets[b + 1] - e0;
     const int64_t start = a.cu[b];
     const int T = a.lengths[b];
-    __shared__ float red[kFsaThreads / 32];
     const double Z = ws_at<double>(a.ws, a.L.off_z)[b];
     const double* coff = ws_at<double>(a.ws, a.L.off_coff);
     bool bad = false;
-    if (!fsa_check(a, b, S, e0, E, start, T, bad)) return;  // rows left as they are: the loss is NaN
+    if (!fsa_check(a, b, S, e0, E, start, T, bad)) return;  // the rows keep zero headers: zero gradient
     float scale = a.grad_loss[b];
     if (!(Z > -INFINITY)) scale = 0.0f;  // no path: zero rows (defined only with zero_infinity)
     float* be = fsa_smem;                                   // beta_{t+1}
     int* mk = reinterpret_cast<int*>(fsa_smem + a.max_states);
     float* sm = fsa_smem + 2 * a.max_states;
     float* P = fsa_smem + 3 * a.max_states;                 // class occupancies of the frame, D values
+    int* labs = reinterpret_cast<int*>(P + a.D);            // the sequence's distinct labels, cap entries
+    const int cap = a.L.cap;
     const float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
+    RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
+    int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
+    // the distinct labels of the edges, found once: P serves as the marker row
+    int* mark = reinterpret_cast<int*>(P);
+    for (int c = threadIdx.x; c < a.D; c += blockDim.x) mark[c] = 0;
+    if (threadIdx.x == 0) s_nlab = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int c = a.edges[3 * (size_t)(e0 + e) + 2];
+        if (atomicExch(&mark[c], 1) == 0) {
+            const int i = atomicAdd(&s_nlab, 1);
+            if (i < cap) labs[i] = c;
+        }
+    }
+    __syncthreads();
+    const int nlab = s_nlab;
+    if (nlab > cap) {  // more distinct labels than max_labels: the rows keep zero headers
+        if (threadIdx.x == 0) set_status(ws_at<Control>(a.ws, 0), CTC_PACKED_DEV_BAD_FSA);
+        return;
+    }
     for (int s = threadIdx.x; s < S; s += blockDim.x) be[s] = a.final_weight[s0 + s];
     __syncthreads();
     double Dn = renormalise(be, S, red);  // beta_{t+1} = be + Dn
@@ -279,7 +311,7 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
             mk[s] = fkey(-INFINITY);
             sm[s] = 0.0f;
         }
-        for (int c = threadIdx.x; c < a.D; c += blockDim.x) P[c] = 0.0f;
+        for (int i = threadIdx.x; i < nlab; i += blockDim.x) P[labs[i]] = 0.0f;
         __syncthreads();
         const int64_t lrow = (start + t) * (int64_t)a.D;
         const float* arow = alpha_rows + (start + t) * (int64_t)a.max_states;
@@ -301,16 +333,13 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
             }
         }
         __syncthreads();
-        // the dense gradient row, in the input dtype
-        for (int c = threadIdx.x; c < a.D; c += blockDim.x) {
-            const float x = lp_at<DT>(a.lp, lrow + c);
-            const float g = scale != 0.0f ? scale * (expf(x) - P[c]) : 0.0f;
-            if constexpr (El::bytes == 4) {
-                reinterpret_cast<float*>(a.grad)[lrow + c] = g;
-            } else {
-                reinterpret_cast<unsigned short*>(a.grad)[lrow + c] = (unsigned short)pack1<DT>(g);
-            }
-        }
+        // the row's class sums (class, -scale * occupancy) and header; the
+        // dense rows are written afterwards by the all-SM gradient stream
+        const int64_t row = start + t;
+        const int n = scale != 0.0f ? nlab : 0;
+        for (int i = threadIdx.x; i < n; i += blockDim.x)
+            ent[row * cap + i] = make_int2(labs[i], __float_as_int(-scale * P[labs[i]]));
+        if (threadIdx.x == 0) head[row] = RowHead{n, scale, 1, 0};
         for (int s = threadIdx.x; s < S; s += blockDim.x)
             be[s] = sm[s] > 0.0f ? fdekey(mk[s]) + logf(sm[s]) : (sm[s] != sm[s] ? sm[s] : -INFINITY);
         __syncthreads();
@@ -318,32 +347,13 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
     }
 }
 
-// Rows outside every sequence get a zero gradient.
-template <int DT>
-__global__ void fsa_zero_uncovered_kernel(FsaArgs a) {
-    using El = Elem<DT>;
-    for (int64_t row = blockIdx.x; row < a.T_total; row += gridDim.x) {
-        int lo = 0, hi = a.B - 1, b = -1;
-        while (lo <= hi) {
-            const int mid = (lo + hi) >> 1;
-            if ((int64_t)a.cu[mid] <= row) {
-                b = mid;
-                lo = mid + 1;
-            } else {
-                hi = mid - 1;
-            }
-        }
-        // rows of a sequence that fails its checks stay as they are
-        const bool covered = b >= 0 && row - a.cu[b] < a.lengths[b] && a.lengths[b] >= 0;
-        if (covered) continue;
-        for (int c = threadIdx.x; c < a.D; c += blockDim.x) {
-            if constexpr (El::bytes == 4) {
-                reinterpret_cast<float*>(a.grad)[row * a.D + c] = 0.0f;
-            } else {
-                reinterpret_cast<unsigned short*>(a.grad)[row * a.D + c] = 0;
-            }
-        }
-    }
+// Every row's header starts as "not covered, no class sums"; the backward
+// then fills the rows of the sequences it runs.
+__global__ void fsa_head_init_kernel(FsaArgs a) {
+    RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
+    for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < a.T_total;
+         row += (int64_t)gridDim.x * blockDim.x)
+        head[row] = RowHead{0, 0.0f, 0, 0};
 }
 
 }  // namespace ctcp
@@ -357,10 +367,11 @@ bool fsa_valid_dtype(int d) { return d == CTC_PACKED_F32 || d == CTC_PACKED_BF16
 ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_total, int32_t D, const int32_t* cu,
                                  const int32_t* lengths, int32_t B, const int32_t* so, const float* sw,
                                  const float* fw, int32_t S_total, const int32_t* eo, const int32_t* edges,
-                                 const float* ew, int32_t E_total, int32_t max_states, const void* ws,
-                                 size_t ws_bytes) {
+                                 const float* ew, int32_t E_total, int32_t max_states, int32_t max_labels,
+                                 const void* ws, size_t ws_bytes) {
     if (!fsa_valid_dtype(dtype) || T_total < 0 || B < 0 || D < 1 || S_total < 0 || E_total < 0)
         return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (max_labels < 1) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (D > kMaxD || T_total > INT32_MAX || max_states < 1 || max_states > kFsaMaxStates)
         return CTC_PACKED_ERR_UNSUPPORTED;
     if (cu == nullptr || so == nullptr || eo == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
@@ -370,7 +381,7 @@ ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_tot
     if (reinterpret_cast<uintptr_t>(log_probs) % (dtype == CTC_PACKED_F32 ? 4 : 2) != 0)
         return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return CTC_PACKED_ERR_WORKSPACE;
-    if (ws_bytes < fsa_layout(T_total, B, max_states).total) return CTC_PACKED_ERR_WORKSPACE;
+    if (ws_bytes < fsa_layout(T_total, B, max_states, max_labels, D).total) return CTC_PACKED_ERR_WORKSPACE;
     return CTC_PACKED_OK;
 }
 
@@ -387,7 +398,7 @@ cudaError_t launch_fsa(K kernel, unsigned grid, size_t smem, cudaStream_t s, con
 FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const int32_t* cu, const int32_t* lengths,
                       int32_t B, const int32_t* so, const float* sw, const float* fw, int32_t S_total,
                       const int32_t* eo, const int32_t* edges, const float* ew, int32_t E_total, int32_t max_states,
-                      int zero_infinity, void* ws) {
+                      int32_t max_labels, int zero_infinity, void* ws) {
     FsaArgs a{};
     a.lp = log_probs;
     a.T_total = T_total;
@@ -402,11 +413,12 @@ FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const i
     a.edges = edges;
     a.edge_weight = ew;
     a.max_states = max_states;
+    a.max_labels = max_labels;
     a.S_total = S_total;
     a.E_total = E_total;
     a.zero_infinity = zero_infinity ? 1 : 0;
     a.ws = ws;
-    a.L = fsa_layout(T_total, B, max_states);
+    a.L = fsa_layout(T_total, B, max_states, max_labels, D);
     return a;
 }
 
@@ -414,9 +426,11 @@ FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const i
 
 extern "C" {
 
-size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states) {
-    if (T_total < 0 || B < 0 || max_states < 1 || max_states > kFsaMaxStates || T_total > INT32_MAX) return 0;
-    return fsa_layout(T_total, B, max_states).total;
+size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states, int32_t max_labels, int32_t D) {
+    if (T_total < 0 || B < 0 || max_states < 1 || max_states > kFsaMaxStates || T_total > INT32_MAX ||
+        max_labels < 1 || D < 1 || D > kMaxD)
+        return 0;
+    return fsa_layout(T_total, B, max_states, max_labels, D).total;
 }
 
 ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
@@ -424,20 +438,21 @@ ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype
                                          const int32_t* state_offsets, const float* start_weight,
                                          const float* final_weight, int32_t num_states, const int32_t* edge_offsets,
                                          const int32_t* edges, const float* edge_weight, int32_t num_edges,
-                                         int32_t max_states, int zero_infinity, float* loss, void* workspace,
-                                         size_t workspace_bytes, cudaStream_t stream) {
+                                         int32_t max_states, int32_t max_labels, int zero_infinity, float* loss,
+                                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     const ctc_packed_status st =
         fsa_check_args(log_probs, dtype, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
-                       final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states, workspace,
-                       workspace_bytes);
+                       final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states, max_labels,
+                       workspace, workspace_bytes);
     if (st != CTC_PACKED_OK) return st;
     if (B > 0 && loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    // the status word is cleared on the stream, before the kernels can set it
-    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    // the control block (status word, and the input mode the gradient stream
+    // reads: log probabilities) is cleared on the stream before any kernel
+    if (cudaMemsetAsync(workspace, 0, sizeof(Control), stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     if (B == 0) return CTC_PACKED_OK;
     FsaArgs a = make_fsa_args(log_probs, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
                               final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states,
-                              zero_infinity, workspace);
+                              max_labels, zero_infinity, workspace);
     a.loss = loss;
     const size_t smem = sizeof(float) * 3 * (size_t)max_states;
     cudaError_t e = dtype == CTC_PACKED_F32    ? launch_fsa(fsa_forward_kernel<0>, (unsigned)B, smem, stream, a)
@@ -452,12 +467,13 @@ ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtyp
                                           const float* final_weight, int32_t num_states,
                                           const int32_t* edge_offsets, const int32_t* edges,
                                           const float* edge_weight, int32_t num_edges, int32_t max_states,
-                                          int zero_infinity, const float* grad_loss, void* workspace,
-                                          size_t workspace_bytes, void* grad_log_probs, cudaStream_t stream) {
+                                          int32_t max_labels, int zero_infinity, const float* grad_loss,
+                                          void* workspace, size_t workspace_bytes, void* grad_log_probs,
+                                          cudaStream_t stream) {
     const ctc_packed_status st =
         fsa_check_args(log_probs, dtype, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
-                       final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states, workspace,
-                       workspace_bytes);
+                       final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states, max_labels,
+                       workspace, workspace_bytes);
     if (st != CTC_PACKED_OK) return st;
     if (T_total == 0) return CTC_PACKED_OK;
     if (grad_log_probs == nullptr || (B > 0 && grad_loss == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
@@ -468,22 +484,46 @@ ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtyp
     if (g0 < l0 + nbytes && l0 < g0 + nbytes) return CTC_PACKED_ERR_INVALID_ARGUMENT;  // overlap
     FsaArgs a = make_fsa_args(log_probs, T_total, D, cu_seqlens, lengths, B, state_offsets, start_weight,
                               final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states,
-                              zero_infinity, workspace);
+                              max_labels, zero_infinity, workspace);
     a.grad_loss = grad_loss;
     a.grad = grad_log_probs;
-    const size_t smem = sizeof(float) * (3 * (size_t)max_states + (size_t)D);
-    cudaError_t e = cudaSuccess;
+    // 1. every row header "not covered"
+    const long long hgrid = (T_total + kFsaThreads - 1) / kFsaThreads;
+    if (launch_fsa(fsa_head_init_kernel, (unsigned)(hgrid < 4096 ? hgrid : 4096), 0, stream, a) != cudaSuccess)
+        return CTC_PACKED_ERR_CUDA;
+    // 2. per sequence: beta, edge occupancies, each row's class sums and header
     if (B > 0) {
-        e = dtype == CTC_PACKED_F32    ? launch_fsa(fsa_backward_kernel<0>, (unsigned)B, smem, stream, a)
+        const size_t smem = sizeof(float) * (3 * (size_t)max_states + (size_t)D) + sizeof(int) * (size_t)a.L.cap;
+        const cudaError_t e =
+            dtype == CTC_PACKED_F32    ? launch_fsa(fsa_backward_kernel<0>, (unsigned)B, smem, stream, a)
             : dtype == CTC_PACKED_BF16 ? launch_fsa(fsa_backward_kernel<1>, (unsigned)B, smem, stream, a)
                                        : launch_fsa(fsa_backward_kernel<2>, (unsigned)B, smem, stream, a);
         if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     }
-    const unsigned zgrid = (unsigned)(T_total < 4096 ? T_total : 4096);
-    e = dtype == CTC_PACKED_F32    ? launch_fsa(fsa_zero_uncovered_kernel<0>, zgrid, 0, stream, a)
-        : dtype == CTC_PACKED_BF16 ? launch_fsa(fsa_zero_uncovered_kernel<1>, zgrid, 0, stream, a)
-                                   : launch_fsa(fsa_zero_uncovered_kernel<2>, zgrid, 0, stream, a);
-    return e == cudaSuccess ? CTC_PACKED_OK : CTC_PACKED_ERR_CUDA;
+    // 3. the dense rows, scale * exp(lp) + class sums, by the CTC path's
+    //    all-SM gradient stream over this workspace's headers and sums
+    GradArgs ga{};
+    ga.L.T_total = T_total;
+    ga.L.B = B;
+    ga.L.D = D;
+    ga.L.ecap = a.L.cap;
+    ga.L.off_ctrl = 0;
+    ga.L.off_head = a.L.off_head;
+    ga.L.off_ent = a.L.off_ent;
+    ga.L.off_lse = 0;  // not read: the control block says log probabilities
+    ga.ws = workspace;
+    ga.lp = log_probs;
+    ga.grad = grad_log_probs;
+    ga.D = D;
+    int k = 1, cap = 1;
+    size_t wsm = 0;
+    grad_geometry(ga.L, D, k, cap, wsm);
+    ga.rows_per_tile = k;
+    ga.entry_cap = cap;
+    ga.warp_smem = wsm;
+    ga.n_tiles = (T_total + k - 1) / k;
+    ga.congruent = ((g0 ^ l0) & 15u) == 0 ? 1 : 0;
+    return launch_grad(ga, (int)dtype, stream) == cudaSuccess ? CTC_PACKED_OK : CTC_PACKED_ERR_CUDA;
 }
 
 }  // extern "C"

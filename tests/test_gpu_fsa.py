@@ -30,14 +30,16 @@ def _run(lp, cu, lengths, fsa, max_states, zero_infinity=False, grad_loss=None, 
     fsa_d = tuple(x.to(dev).contiguous() for x in fsa)
     cu_d, ln_d = cu.to(dev).to(torch.int32), lengths.to(dev).to(torch.int32)
     lp_d = lp.to(dev).contiguous()
-    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, B, max_states), dtype=torch.uint8, device=dev)
+    max_labels = _max_labels(fsa)
+    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, B, max_states, max_labels, D), dtype=torch.uint8,
+                     device=dev)
     loss = torch.full((B,), float("nan"), device=dev)
-    pk.ctc_packed_fsa_forward(lp_d, cu_d, ln_d, fsa_d, max_states, zero_infinity, loss, ws)
+    pk.ctc_packed_fsa_forward(lp_d, cu_d, ln_d, fsa_d, max_states, max_labels, zero_infinity, loss, ws)
     g = torch.ones(B) if grad_loss is None else torch.as_tensor(grad_loss, dtype=torch.float32)
     n = T_total * D * lp.element_size()
     raw = torch.full((n + 2 * guard,), 0xA5, dtype=torch.uint8, device=dev)
     grad = raw[guard:guard + n].view(lp.dtype).view(T_total, D)
-    pk.ctc_packed_fsa_backward(lp_d, cu_d, ln_d, fsa_d, max_states, zero_infinity, g.to(dev), ws, grad)
+    pk.ctc_packed_fsa_backward(lp_d, cu_d, ln_d, fsa_d, max_states, max_labels, zero_infinity, g.to(dev), ws, grad)
     torch.cuda.synchronize()
     assert bool((raw[:guard] == 0xA5).all()) and bool((raw[guard + n:] == 0xA5).all()), "write outside the gradient"
     status = pk.ctc_packed_read_status(ws)
@@ -48,6 +50,11 @@ def _oracle(lp, cu, lengths, fsa, grad_loss, zero_infinity=False):
     so, sw, fw, eo, ed, ew = fsa
     return fsa_oracle.fsa_loss_packed(lp, cu, lengths, so, sw, fw, eo, ed, ew, grad_loss=grad_loss,
                                       zero_infinity=zero_infinity)
+
+
+def _max_labels(fsa):
+    eo, ed = fsa[3], fsa[4]
+    return max(1, max(len(set(ed[eo[i]:eo[i + 1], 2].tolist())) for i in range(len(eo) - 1)))
 
 
 def _max_states(fsa):
