@@ -112,3 +112,46 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
 
     with pytest.raises(RuntimeError, match="no fallback"):
         p.load_library(str(tmp_path / "missing.so"))
+
+
+def _fsa_fwd(lib, **kw):
+    args = dict(lp=8, dtype=0, T=10, D=5, cu=16, ln=24, B=2, so=32, sw=40, fw=48, S=6, eo=56, ed=64, ew=72, E=4,
+                ms=3, ml=2, zi=0, loss=80, ws=256, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return lib.ctc_packed_fsa_forward(args["lp"], args["dtype"], args["T"], args["D"], args["cu"], args["ln"],
+                                      args["B"], args["so"], args["sw"], args["fw"], args["S"], args["eo"],
+                                      args["ed"], args["ew"], args["E"], args["ms"], args["ml"], args["zi"],
+                                      args["loss"], args["ws"], args["wsb"], args["stream"])
+
+
+def test_fsa_host_checks_return_before_any_cuda_call(lib):
+    INVALID, WORKSPACE, UNSUPPORTED = 1, 2, 4
+    assert _fsa_fwd(lib, D=0) == INVALID
+    assert _fsa_fwd(lib, dtype=3) == INVALID
+    assert _fsa_fwd(lib, B=-1) == INVALID
+    assert _fsa_fwd(lib, ml=0) == INVALID  # max_labels below 1
+    assert _fsa_fwd(lib, S=-1) == INVALID
+    assert _fsa_fwd(lib, cu=None) == INVALID
+    assert _fsa_fwd(lib, so=None) == INVALID
+    assert _fsa_fwd(lib, ed=None) == INVALID  # edges announced but missing
+    assert _fsa_fwd(lib, loss=None) == INVALID
+    assert _fsa_fwd(lib, ms=0) == UNSUPPORTED
+    assert _fsa_fwd(lib, ms=4097) == UNSUPPORTED  # more states than a shared-memory row holds
+    assert _fsa_fwd(lib, D=16385) == UNSUPPORTED
+    assert _fsa_fwd(lib, ws=None) == WORKSPACE
+    assert _fsa_fwd(lib, ws=128) == WORKSPACE  # not 256-byte aligned
+    assert _fsa_fwd(lib, wsb=64) == WORKSPACE
+
+
+def test_fsa_workspace_size():
+    import packed_sequence_ctc_gb300 as pk
+    from packed_sequence_ctc_gb300 import build as b
+
+    lib = pk.load_library(b.build())
+    assert lib.ctc_packed_fsa_workspace_size(100, 4, 0, 5, 10) == 0
+    assert lib.ctc_packed_fsa_workspace_size(100, 4, 10, 0, 10) == 0
+    n = lib.ctc_packed_fsa_workspace_size(1000, 4, 50, 20, 30)
+    # alpha rows (4 B x states) and class sums (8 B x min(labels, D)) per frame at least
+    assert n >= 1000 * 50 * 4 + 1000 * 20 * 8 + 1000 * 8
+    assert lib.ctc_packed_fsa_workspace_size(1000, 4, 50, 200, 30) < lib.ctc_packed_fsa_workspace_size(
+        1000, 4, 50, 200, 300)  # the class sums a row holds are capped at D
