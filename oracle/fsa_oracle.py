@@ -79,6 +79,8 @@ def fsa_sequence(lp: np.ndarray, start: np.ndarray, final: np.ndarray, edges: np
         alpha[t + 1] = nxt
     Z = _logsumexp(alpha[T] + final)
     grad = np.zeros((T, D))
+    if np.isnan(Z):  # a NaN score anywhere on the lattice (as a NaN log probability gives torch's CTC loss)
+        return np.nan, np.full((T, D), np.nan)
     if not np.isfinite(Z):
         if zero_infinity:
             return 0.0, grad
