@@ -38,6 +38,11 @@ namespace ctcp {
 namespace {
 
 constexpr int kFsaThreads = 256;
+// Edges a thread keeps in registers (its edges tid, tid + 256, ...): their
+// ids, weight and the label values of this frame and the next, which load
+// while the frame's barriers run.  A sequence's further edges are read from
+// memory each frame.
+constexpr int kFsaRegEdges = 4;
 
 // Workspace of the FSA path: status header, log Z per sequence (double),
 // each frame's forward values relative to the frame's own offset (float)
@@ -218,9 +223,25 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_forward_kernel(FsaArgs a) {
     int* mk = reinterpret_cast<int*>(fsa_smem + a.max_states);  // max key per state
     float* sm = fsa_smem + 2 * a.max_states;                // sum per state
     float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
+    int efr[kFsaRegEdges], eto[kFsaRegEdges], elab[kFsaRegEdges];
+    float ew[kFsaRegEdges], lpc[kFsaRegEdges], lpn[kFsaRegEdges], ev[kFsaRegEdges];
+#pragma unroll
+    for (int k = 0; k < kFsaRegEdges; ++k) {
+        const int e = threadIdx.x + k * kFsaThreads;
+        const bool on = e < E;
+        const int* ed = a.edges + 3 * (size_t)(e0 + (on ? e : 0));
+        efr[k] = on ? ed[0] : 0;
+        eto[k] = on ? ed[1] : 0;
+        elab[k] = on ? ed[2] : 0;
+        ew[k] = on ? a.edge_weight[e0 + e] : -INFINITY;  // an absent edge never contributes
+        lpc[k] = (on && T > 0) ? lp_at<DT>(a.lp, start * (int64_t)a.D + elab[k]) : 0.0f;
+        lpn[k] = 0.0f;
+    }
+    const int e_reg = kFsaRegEdges * kFsaThreads;  // edges from here on are read each frame
     for (int s = threadIdx.x; s < S; s += blockDim.x) al[s] = a.start_weight[s0 + s];
     __syncthreads();
     double C = renormalise(al, S, red);  // alpha_t = al + C
+    bool nan_seen = false;               // a NaN edge value: the loss is NaN
     for (int t = 0; t < T; ++t) {
         float* row = alpha_rows + (start + t) * (int64_t)a.max_states;
         if (threadIdx.x == 0) coff[start + t] = C;
@@ -231,13 +252,28 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_forward_kernel(FsaArgs a) {
         }
         __syncthreads();
         const int64_t lrow = (start + t) * (int64_t)a.D;
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+#pragma unroll
+        for (int k = 0; k < kFsaRegEdges; ++k) {
+            ev[k] = al[efr[k]] + ew[k] + lpc[k];
+            nan_seen |= ev[k] != ev[k];
+            if (ev[k] > -INFINITY) atomicMax(&mk[eto[k]], fkey(ev[k]));
+        }
+        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
             const int* ed = a.edges + 3 * (size_t)(e0 + e);
             const float v = al[ed[0]] + a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]);
+            nan_seen |= v != v;
             if (v > -INFINITY) atomicMax(&mk[ed[1]], fkey(v));
         }
+        if (t + 1 < T) {  // the next frame's label values, in flight across the barriers
+#pragma unroll
+            for (int k = 0; k < kFsaRegEdges; ++k)
+                if (threadIdx.x + k * kFsaThreads < E) lpn[k] = lp_at<DT>(a.lp, lrow + a.D + elab[k]);
+        }
         __syncthreads();
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+#pragma unroll
+        for (int k = 0; k < kFsaRegEdges; ++k)
+            if (ev[k] > -INFINITY) atomicAdd(&sm[eto[k]], expf(ev[k] - fdekey(mk[eto[k]])));
+        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
             const int* ed = a.edges + 3 * (size_t)(e0 + e);
             const float v = al[ed[0]] + a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]);
             if (v > -INFINITY) atomicAdd(&sm[ed[1]], expf(v - fdekey(mk[ed[1]])));
@@ -247,10 +283,14 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_forward_kernel(FsaArgs a) {
             al[s] = sm[s] > 0.0f ? fdekey(mk[s]) + logf(sm[s]) : (sm[s] != sm[s] ? sm[s] : -INFINITY);
         __syncthreads();
         C += renormalise(al, S, red);
+#pragma unroll
+        for (int k = 0; k < kFsaRegEdges; ++k) lpc[k] = lpn[k];
     }
     const float zr = block_lse(al, a.final_weight + s0, S, red);
+    const bool any_nan = __syncthreads_or(nan_seen) != 0;
     if (threadIdx.x == 0) {
-        const double Z = zr > -INFINITY ? C + (double)zr : (double)zr;
+        const double Z = any_nan ? __longlong_as_double(0x7ff8000000000000ll)
+                                 : (zr > -INFINITY ? C + (double)zr : (double)zr);
         z_out[b] = Z;
         float l = (float)-Z;
         if (a.zero_infinity && Z == -INFINITY) l = 0.0f;
@@ -301,6 +341,24 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
         if (threadIdx.x == 0) set_status(ws_at<Control>(a.ws, 0), CTC_PACKED_DEV_BAD_FSA);
         return;
     }
+    int efr[kFsaRegEdges], eto[kFsaRegEdges], elab[kFsaRegEdges];
+    float ew[kFsaRegEdges], lpc[kFsaRegEdges], lpn[kFsaRegEdges], ac[kFsaRegEdges], an[kFsaRegEdges];
+    float ev[kFsaRegEdges];
+#pragma unroll
+    for (int k = 0; k < kFsaRegEdges; ++k) {
+        const int e = threadIdx.x + k * kFsaThreads;
+        const bool on = e < E;
+        const int* ed = a.edges + 3 * (size_t)(e0 + (on ? e : 0));
+        efr[k] = on ? ed[0] : 0;
+        eto[k] = on ? ed[1] : 0;
+        elab[k] = on ? ed[2] : 0;
+        ew[k] = on ? a.edge_weight[e0 + e] : -INFINITY;  // an absent edge never contributes
+        // this frame's label value and forward value at the edge's origin
+        lpc[k] = (on && T > 0) ? lp_at<DT>(a.lp, (start + T - 1) * (int64_t)a.D + elab[k]) : 0.0f;
+        ac[k] = (on && T > 0) ? alpha_rows[(start + T - 1) * (int64_t)a.max_states + efr[k]] : 0.0f;
+        lpn[k] = an[k] = 0.0f;
+    }
+    const int e_reg = kFsaRegEdges * kFsaThreads;  // edges from here on are read each frame
     for (int s = threadIdx.x; s < S; s += blockDim.x) be[s] = a.final_weight[s0 + s];
     __syncthreads();
     double Dn = renormalise(be, S, red);  // beta_{t+1} = be + Dn
@@ -315,13 +373,37 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
         __syncthreads();
         const int64_t lrow = (start + t) * (int64_t)a.D;
         const float* arow = alpha_rows + (start + t) * (int64_t)a.max_states;
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+#pragma unroll
+        for (int k = 0; k < kFsaRegEdges; ++k) {
+            ev[k] = ew[k] + lpc[k] + be[eto[k]];
+            if (ev[k] > -INFINITY) atomicMax(&mk[efr[k]], fkey(ev[k]));
+        }
+        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
             const int* ed = a.edges + 3 * (size_t)(e0 + e);
             const float v = a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]) + be[ed[1]];
             if (v > -INFINITY) atomicMax(&mk[ed[0]], fkey(v));
         }
+        if (t > 0) {  // the previous frame's label and forward values, in flight across the barriers
+#pragma unroll
+            for (int k = 0; k < kFsaRegEdges; ++k) {
+                if (threadIdx.x + k * kFsaThreads < E) {
+                    lpn[k] = lp_at<DT>(a.lp, lrow - a.D + elab[k]);
+                    an[k] = arow[efr[k] - a.max_states];
+                }
+            }
+        }
         __syncthreads();
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+#pragma unroll
+        for (int k = 0; k < kFsaRegEdges; ++k) {
+            if (ev[k] > -INFINITY) {
+                atomicAdd(&sm[efr[k]], expf(ev[k] - fdekey(mk[efr[k]])));
+                if (scale != 0.0f) {
+                    const float occ = expf(ac[k] + ev[k] + K);
+                    if (occ > 0.0f) atomicAdd(&P[elab[k]], occ);
+                }
+            }
+        }
+        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
             const int* ed = a.edges + 3 * (size_t)(e0 + e);
             const float v = a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]) + be[ed[1]];
             if (v > -INFINITY) {
@@ -333,6 +415,11 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
             }
         }
         __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kFsaRegEdges; ++k) {
+            lpc[k] = lpn[k];
+            ac[k] = an[k];
+        }
         // the row's class sums (class, -scale * occupancy) and header; the
         // dense rows are written afterwards by the all-SM gradient stream
         const int64_t row = start + t;

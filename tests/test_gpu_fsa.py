@@ -148,3 +148,21 @@ def test_out_of_range_fsa_data_sets_the_status(cuda_device):
     loss, _, status, _ = _run(lp, cu, ln, fsa, 4)
     assert status & 0x80 and status & 0x10
     assert np.isfinite(loss[0]) and np.isnan(loss[1]) and np.isnan(loss[2])
+
+
+def test_many_edges_per_sequence_and_a_nan(cuda_device):
+    # more edges than the threads keep in registers (4 x 256), and a NaN
+    # label value in one sequence, which must make only its loss NaN
+    D = 19
+    lp = torch.log_softmax(torch.randn(130, D, generator=torch.Generator().manual_seed(8)), -1)
+    big = workloads.random_fsa(60, 1500, D, seed=77)
+    small = workloads.random_fsa(5, 14, D, seed=78)
+    fsa = workloads.pack_fsas([big, small, small])
+    cu = torch.tensor([0, 70, 100, 130], dtype=torch.int32)
+    ln = torch.tensor([70, 30, 30], dtype=torch.int32)
+    lp[110, :] = float("nan")  # a row of the third sequence
+    loss, grad, status, g = _run(lp, cu, ln, fsa, 60)
+    ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
+    assert np.isnan(loss[2]) and np.isnan(ref_loss[2])
+    assert_loss_close(loss[:2], ref_loss[:2])
+    assert_grad_close(grad[:100], ref_grad[:100], torch.float32)
