@@ -610,14 +610,10 @@ static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
     cudaError_t e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    // the dynamic shared memory bound is set per device, and only raised
-    constexpr int kMaxDevices = 64;
-    static int configured_smem[kMaxDevices] = {};
-    if (dev < 0 || dev >= kMaxDevices || (int)smem > configured_smem[dev]) {
-        e = cudaFuncSetAttribute(chain_kernel<P, MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) configured_smem[dev] = (int)smem;
-    }
+    // set on every call (on the current device): a cached value could go
+    // stale between host threads launching with different sizes
+    e = cudaFuncSetAttribute(chain_kernel<P, MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P, MAXT>, 32 * nw, smem)) !=
