@@ -269,7 +269,7 @@ def packed_ctc_loss(log_probs: torch.Tensor, cu_seqlens: torch.Tensor, lengths: 
         raise ValueError(f"unexpected reduction {reduction!r}")
     if not 0 <= blank < log_probs.shape[-1]:
         raise ValueError(f"blank must be a class index below {log_probs.shape[-1]}, got {blank}.")
-    capturing = torch.cuda.is_current_stream_capturing()
+    capturing = torch.cuda.is_available() and torch.cuda.is_current_stream_capturing()
     if max_target_len is None:
         if capturing:
             raise ValueError("max_target_len is required under graph capture")

@@ -1,0 +1,53 @@
+"""Host-side behaviour of the Python binding that needs no GPU: argument
+checks of the autograd wrapper before any launch, the status-bit messages,
+and that the library's entry points are bound with the arity the header
+declares (a call with a wrong argument count would fail in ctypes)."""
+
+import re
+import os
+
+import pytest
+import torch
+
+import packed_sequence_ctc_gb300 as pk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_wrapper_rejects_bad_arguments_before_any_launch():
+    lp = torch.zeros(10, 5)
+    cu = torch.tensor([0, 6, 10])
+    ln = torch.tensor([6, 4])
+    tg = torch.tensor([1, 2, 3])
+    tl = torch.tensor([2, 1])
+    with pytest.raises(ValueError, match="unexpected reduction"):
+        pk.packed_ctc_loss(lp, cu, ln, tg, tl, blank=0, reduction="average")
+    with pytest.raises(ValueError, match="blank"):
+        pk.packed_ctc_loss(lp, cu, ln, tg, tl, blank=5, max_target_len=2)
+    with pytest.raises((ValueError, TypeError)):
+        pk.packed_ctc_loss(lp.double(), cu, ln, tg, tl, blank=0, max_target_len=2)  # float64 is not read
+    with pytest.raises(ValueError, match="CUDA"):
+        pk.packed_ctc_loss(lp, cu, ln, tg, tl, blank=0, max_target_len=2)  # a CPU tensor: no CPU path
+
+
+def test_reduction_and_flag_codes_match_the_header():
+    text = open(os.path.join(ROOT, "include", "ctc_packed.h")).read()
+    enum = dict((name.lower(), int(v)) for name, v in re.findall(r"CTC_PACKED_(NONE|SUM|MEAN|MEAN_BATCH|MEAN_VOLUME)"
+                                                                  r"\s*=\s*(\d+)", text))
+    assert enum == pk.REDUCTION_CODES
+    assert int(re.search(r"#define CTC_PACKED_FLAG_LOSS_ONLY (0x\w+)u", text).group(1), 16) == pk.FLAG_LOSS_ONLY
+    assert int(re.search(r"#define CTC_PACKED_FLAG_LOGITS (0x\w+)u", text).group(1), 16) == pk.FLAG_LOGITS
+    bits = {int(v, 16) for v in re.findall(r"#define CTC_PACKED_DEV_\w+ (0x\w+)u", text)}
+    assert bits == set(pk.DEVICE_STATUS_BITS)
+
+
+def test_entry_points_are_bound_with_the_declared_arity():
+    from packed_sequence_ctc_gb300 import build as b
+
+    lib = pk.load_library(b.build())
+    text = open(os.path.join(ROOT, "include", "ctc_packed.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    for name, params in re.findall(r"\b(ctc_packed_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None and len(fn.argtypes) == n, name
