@@ -197,7 +197,7 @@ def _longform(device="cpu"):
     gen = torch.Generator().manual_seed(0)
     Ts, Us = _lengths(gen, 8, 1500, 2000, 1, 4, 1, 3)
     T_bad = _uniform_int(gen, 1500, 2000)
-    U_bad = T_bad // 2 + 1
+    U_bad = (T_bad + 1) // 2 + 1  # all one id: aligning needs 2U - 1 > T frames
     bad_label = _uniform_int(gen, 1, 1024)
     lab_gen = torch.Generator().manual_seed(2)
     seqs = [torch.randint(1, 1025, (u,), generator=lab_gen).tolist() for u in Us]
