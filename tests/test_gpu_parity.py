@@ -292,3 +292,29 @@ def test_functional_raises_on_negative_target_length(cuda_device):
     with pytest.raises(TypeError, match="float32"):
         pk.packed_ctc_loss(batch.log_probs.double().cuda(), batch.cu_seqlens.cuda(), batch.lengths.cuda(),
                            batch.targets.cuda(), batch.target_lengths.cuda(), blank=0)
+
+
+def test_maximum_target_length(cuda_device):
+    # the longest target the library takes (3839 labels: four state pairs per
+    # lane, 31 warps), with a short one beside it
+    U = 3839
+    batch = workloads.make_batch([U + 240, 30], [U, 6], 64, dtype=torch.float32, seed=31, label_low=1,
+                                 label_high=63, redraw_infeasible=True, reduction="none")
+    assert batch.max_target_len == U
+    loss, grad, status = run_gpu(batch)
+    assert status == 0
+    ref_loss, ref_grad, nll = _ref(batch)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, torch.float32, rows=_defined_rows(batch, nll))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_maximum_vocabulary(cuda_device, dtype):
+    # D = 16384, the widest row the gradient stream takes
+    batch = workloads.make_batch([45, 30, 12], [9, 6, 3], 16384, dtype=dtype, seed=32, label_high=16383,
+                                 reduction="mean", gaps=[0, 2, 1])
+    loss, grad, status = run_gpu(batch)
+    assert status == 0
+    ref_loss, ref_grad, _ = _ref(batch)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)
