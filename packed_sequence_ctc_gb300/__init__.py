@@ -161,8 +161,22 @@ def ctc_packed_fsa_workspace_size(T_total: int, B: int, max_states: int, max_lab
 
 def _fsa_args(log_probs, cu_seqlens, lengths, fsa):
     """Marshal the FSA tensors: fsa = (state_offsets, start_weight,
-    final_weight, edge_offsets, edges (E, 3) int32, edge_weight)."""
+    final_weight, edge_offsets, edges (E, 3) int32, edge_weight); each must
+    be a contiguous tensor of that dtype on the log probabilities' device."""
     so, sw, fw, eo, ed, ew = fsa
+    want = ((cu_seqlens, torch.int32, "cu_seqlens"), (lengths, torch.int32, "lengths"),
+            (so, torch.int32, "state_offsets"), (sw, torch.float32, "start_weight"),
+            (fw, torch.float32, "final_weight"), (eo, torch.int32, "edge_offsets"), (ed, torch.int32, "edges"),
+            (ew, torch.float32, "edge_weight"))
+    for t, dt, name in want:
+        if t.dtype != dt or not t.is_contiguous() or t.device != log_probs.device:
+            raise TypeError(f"{name} must be a contiguous {dt} tensor on {log_probs.device}")
+    if ed.ndim != 2 or ed.shape[1] != 3:
+        raise ValueError("edges must have shape (E, 3): from, to, label")
+    if ew.numel() != ed.shape[0] or fw.numel() != sw.numel():
+        raise ValueError("edge_weight needs one value per edge, final_weight one per start_weight entry")
+    if so.numel() != lengths.numel() + 1 or eo.numel() != lengths.numel() + 1:
+        raise ValueError("state_offsets and edge_offsets need B + 1 entries")
     T_total, D = log_probs.shape
     return (_ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
             lengths.numel(), _ptr(so), _ptr(sw), _ptr(fw), sw.numel(), _ptr(eo),

@@ -51,3 +51,26 @@ def test_entry_points_are_bound_with_the_declared_arity():
         n = 0 if params.strip() in ("", "void") else params.count(",") + 1
         fn = getattr(lib, name)
         assert fn.argtypes is not None and len(fn.argtypes) == n, name
+
+
+def test_fsa_wrappers_check_their_tensors_before_any_call():
+    import workloads
+
+    lp = torch.zeros(8, 4)
+    cu = torch.tensor([0, 8], dtype=torch.int32)
+    ln = torch.tensor([8], dtype=torch.int32)
+    fsa = workloads.pack_fsas([workloads.random_fsa(3, 6, 4, seed=0)])
+    ws = torch.empty(1 << 20, dtype=torch.uint8)
+    loss = torch.empty(1)
+    pk.ctc_packed_fsa_forward  # bound
+    bad_edges = (fsa[0], fsa[1], fsa[2], fsa[3], fsa[4].long(), fsa[5])
+    with pytest.raises(TypeError, match="edges"):
+        pk.ctc_packed_fsa_forward(lp, cu, ln, bad_edges, 3, 4, False, loss, ws)
+    flat = (fsa[0], fsa[1], fsa[2], fsa[3], fsa[4].reshape(-1), fsa[5])
+    with pytest.raises(ValueError, match="shape"):
+        pk.ctc_packed_fsa_forward(lp, cu, ln, flat, 3, 4, False, loss, ws)
+    short = (fsa[0], fsa[1], fsa[2], fsa[3], fsa[4], fsa[5][:-1])
+    with pytest.raises(ValueError, match="edge_weight"):
+        pk.ctc_packed_fsa_forward(lp, cu, ln, short, 3, 4, False, loss, ws)
+    with pytest.raises(TypeError, match="cu_seqlens"):
+        pk.ctc_packed_fsa_forward(lp, cu.long(), ln, fsa, 3, 4, False, loss, ws)
