@@ -2,6 +2,7 @@
 // workspace layout and kernel launches.  No host synchronisation except in
 // ctc_packed_read_status.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "ctc_common.cuh"
@@ -38,6 +39,46 @@ ctc_packed_status check_common(const void* log_probs, ctc_packed_dtype dtype, in
     const Layout L = make_layout(T_total, B, max_target_len, D);
     if (workspace_bytes < L.total) return CTC_PACKED_ERR_WORKSPACE;
     return CTC_PACKED_OK;
+}
+
+// Rows of at least this many bytes take the bulk-copy gradient stream
+// (stream.cu); narrower rows the class-sum pass plus the row-group stream
+// (grad.cu), which packs several rows per warp.
+constexpr long long kStreamMinRowBytes = 2048;
+
+// CTC_PACKED_STREAM=0 keeps every backward on the class-sum pass and the
+// row-group stream, =1 sends every supported one through the bulk-copy
+// stream; unset, the row width decides.
+int stream_override() {
+    const char* e = std::getenv("CTC_PACKED_STREAM");
+    if (e == nullptr || e[0] == '\0') return -1;
+    return e[0] == '0' ? 0 : 1;
+}
+
+// Fills `sa` for the bulk-copy stream; false when it cannot run this call
+// (unaligned buffers, or one team's slots do not fit shared memory).
+bool plan_stream(StreamArgs& sa, const Layout& L, const void* lp, void* grad, ctc_packed_dtype dtype, int32_t D,
+                 const int32_t* cu, const int32_t* targets, const float* grad_loss, int32_t blank, int reduction, int zero_infinity,
+                 void* workspace, bool fused) {
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(lp), g0 = reinterpret_cast<uintptr_t>(grad);
+    if ((l0 & 15u) != 0 || (g0 & 15u) != 0) return false;
+    sa = StreamArgs{};
+    sa.L = L;
+    sa.ws = workspace;
+    sa.lp = lp;
+    sa.grad = grad;
+    sa.cu = cu;
+    sa.targets = targets;
+    sa.grad_loss = grad_loss;
+    sa.D = D;
+    sa.blank = blank;
+    sa.reduction = reduction;
+    sa.zero_infinity = zero_infinity ? 1 : 0;
+    sa.elem_bytes = elem_bytes(dtype);
+    sa.fused = fused ? 1 : 0;
+    sa.gp_mul = grad_group_multiplier(L);
+    if (sa.gp_mul == 0) return false;
+    return stream_plan(sa);
 }
 
 }  // namespace
@@ -144,6 +185,15 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
     ga.congruent = ((g0 ^ l0) & 15u) == 0 ? 1 : 0;
     ga.gp_mul = grad_group_multiplier(ga.L);
     if (ga.gp_mul == 0) return CTC_PACKED_ERR_UNSUPPORTED;
+    const int ov = stream_override();
+    if (ov != 0 && (ov == 1 || (long long)D * eb >= kStreamMinRowBytes)) {
+        StreamArgs sa;
+        if (plan_stream(sa, ga.L, log_probs, grad_log_probs, dtype, D, cu_seqlens, targets, grad_loss, blank, reduction,
+                        zero_infinity, workspace, false)) {
+            if (launch_stream(sa, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+            return CTC_PACKED_OK;
+        }
+    }
     if (launch_post(ga, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     if (launch_grad(ga, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     return CTC_PACKED_OK;

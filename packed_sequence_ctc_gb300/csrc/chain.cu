@@ -199,11 +199,12 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     // packed row row0 + k (alpha) or row0 - k (beta)
     const bool store_me = own && j0 <= U;
     int* const st_base = ws_at<int>(a.ws, DIR == 0 ? a.L.off_alpha : a.L.off_beta);
-    int* st = st_base + row0 * a.L.pitch + 2 * max(j0, 0);
-    const intptr_t st_step = (DIR == 0 ? 1 : -1) * (intptr_t)a.L.pitch;
-    int32_t* const off_base = ws_at<int32_t>(a.ws, DIR == 0 ? a.L.off_aoff : a.L.off_boff) + row0 * a.L.nwo + c.w;
+    // a stored row is [the per-warp offsets, owo ints][the state pairs, pitch ints]
+    int* st = st_base + row0 * a.L.spitch + a.L.owo + 2 * max(j0, 0);
+    const intptr_t st_step = (DIR == 0 ? 1 : -1) * (intptr_t)a.L.spitch;
+    int32_t* const off_base = st_base + row0 * a.L.spitch + c.w;
     int32_t* offp = off_base;
-    const intptr_t off_step = (DIR == 0 ? 1 : -1) * (intptr_t)a.L.nwo;
+    const intptr_t off_step = st_step;
     // the warp's own pairs [p0, p0 + np) are contiguous in the row and, in the
     // stage, from lane `lane0` on; written in 16-byte chunks of two pairs
     // (an odd count also writes pair U + 1, which the row's pitch holds and
@@ -250,7 +251,7 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
                 const int r = (int)(((uint32_t)cq * ch_mul) >> 16), k = cq - r * nch;
                 const int4 v = reinterpret_cast<const int4*>(c.stage + r * 64 + 2 * lane0)[k];
                 const int64_t row = row0 + (DIR == 0 ? (int64_t)(k0 + r) : -(int64_t)(k0 + r));
-                reinterpret_cast<int4*>(st_base + row * a.L.pitch + 2 * p0)[k] = v;
+                reinterpret_cast<int4*>(st_base + row * a.L.spitch + a.L.owo + 2 * p0)[k] = v;
             }
             if (lane < n) off_base[(intptr_t)(k0 + lane) * off_step] = a_hold;
             __syncwarp();
@@ -461,9 +462,7 @@ __device__ void run_label_item(const ChainArgs& a, int b, int lane) {
     const UttInfo info = utt[b];
     const int U = info.U;
     const int32_t* tg = a.targets + info.toff;
-    int32_t* nxt = ws_at<int32_t>(a.ws, a.L.off_nxt) + info.moff;
-    int32_t* rank = ws_at<int32_t>(a.ws, a.L.off_rank) + info.moff;
-    int32_t* owner = ws_at<int32_t>(a.ws, a.L.off_owner) + info.moff;
+    LabelRec* lbl = ws_at<LabelRec>(a.ws, a.L.off_lbl) + info.moff;
     bool bad = false;
     int running = 0;
     for (int j0 = 0; j0 < U; j0 += 32) {
@@ -491,15 +490,12 @@ __device__ void run_label_item(const ChainArgs& a, int b, int lane) {
         const unsigned m = __ballot_sync(0xffffffffu, first);
         const int r = running + __popc(m & ((1u << lane) - 1u));
         if (j < U) {
-            nxt[j] = nx;
-            rank[j] = first ? r : (is_blank ? -2 : -1);
-            if (first) owner[r] = c;
+            lbl[j] = LabelRec{first ? r : (is_blank ? -2 : -1), nx, c, 0};
         }
         running += __popc(m);
     }
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-        owner[running] = a.blank;
         utt[b].n_owners = running + 1;
         utt[b].labels_ok = bad ? 0 : 1;
         if (bad) set_status(ctrl, CTC_PACKED_DEV_LABEL_OUT_OF_RANGE);

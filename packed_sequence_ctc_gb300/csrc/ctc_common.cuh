@@ -35,7 +35,10 @@ struct Control {
     int32_t n_big, n_small, n_lab;
     uint32_t logits;      // 1: the forward took logits, normalised each row, and kept its log-sum-exp
     int32_t tl_total;     // sum of the target lengths (negative ones as 0): mean_volume's divisor
-    uint32_t pad[5];
+    uint32_t gap_head;    // gradient stream: next uncovered row (index into the gap list) to zero
+    uint32_t stream_done; // gradient stream: CTAs that have finished
+    uint32_t chain_live;  // forward-backward call: the chain kernel has started (its inputs are visible)
+    uint32_t pad[2];
 };
 static_assert(sizeof(Control) == 64, "control block is 64 bytes");
 
@@ -57,6 +60,15 @@ struct UttInfo {
     int32_t pad;
 };
 
+// Label record of target position j of an utterance (written by the label
+// analysis): rank >= 0 for the first occurrence of a class (its index among
+// the utterance's distinct classes), -1 for a later occurrence, -2 for a
+// target id equal to the blank; next: the next position with the same class
+// (-1: none); cls: the class.
+struct LabelRec {
+    int32_t rank, next, cls, pad;
+};
+
 // Per-row header of the backward's class sums (written by the posterior pass).
 struct RowHead {
     int32_t count;    // class-sum entries of the row
@@ -73,9 +85,15 @@ struct Layout {
     int32_t gpairs;              // state pairs a chain warp owns (its offset group)
     int32_t nwo;                 // per-frame offsets stored per chain row (one per offset group)
     int32_t epitch;              // entries per row of the emission matrix (max_U + 1)
+    int32_t owo;                 // per-frame offsets at the head of a stored row: nwo rounded up to 4
+    int32_t spitch;              // ints per stored row: owo offsets, then pitch state ints
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
-    size_t off_ctrl, off_utt, off_queue, off_nll, off_aoff, off_boff, off_alpha, off_beta;
-    size_t off_nxt, off_rank, off_owner, off_em, off_head, off_ent, off_lse, total;
+    size_t off_ctrl, off_utt, off_queue, off_nll, off_alpha, off_beta;
+    size_t off_lbl, off_em, off_head, off_ent, off_lse;
+    size_t off_claim;            // gradient stream: rows of each utterance handed out so far (B ints)
+    size_t off_prog;             // rows each chain has stored: [2b] alpha from the first frame, [2b+1] beta from the last
+    size_t off_gap;              // uncovered row ranges: first row of gap g (B + 2 ints), then the prefix of their lengths (B + 3 ints)
+    size_t total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -116,6 +134,8 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
         const int nw = (pairs + L.gpairs - 1) / L.gpairs;
         L.nwo = nw < 1 ? 1 : nw;
     }
+    L.owo = (L.nwo + 3) / 4 * 4;
+    L.spitch = L.owo + L.pitch;
     L.epitch = max_U + 1;  // (label, blank) entries, then (zero, blank)
     L.lab_cap = (int64_t)B * max_U + B;
     size_t o = 0;
@@ -123,17 +143,16 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_utt = o;    o = align_up(o + sizeof(UttInfo) * (size_t)B, 256);
     L.off_queue = o;  o = align_up(o + sizeof(int32_t) * (3 * (size_t)B + 1), 256);
     L.off_nll = o;    o = align_up(o + sizeof(double) * (size_t)B, 256);
-    L.off_aoff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.nwo, 256);
-    L.off_boff = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.nwo, 256);
-    L.off_alpha = o;  o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.pitch, 256);
-    L.off_beta = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.pitch, 256);
-    L.off_nxt = o;    o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
-    L.off_rank = o;   o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
-    L.off_owner = o;  o = align_up(o + sizeof(int32_t) * (size_t)L.lab_cap, 256);
+    L.off_alpha = o;  o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.spitch, 256);
+    L.off_beta = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.spitch, 256);
+    L.off_lbl = o;    o = align_up(o + sizeof(int4) * (size_t)L.lab_cap, 256);
     L.off_em = o;     o = align_up(o + 16 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
     L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
     L.off_ent = o;    o = align_up(o + 8 * (size_t)T_total * (size_t)L.ecap, 256);
     L.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)T_total, 256);
+    L.off_claim = o;  o = align_up(o + sizeof(int32_t) * (size_t)B, 256);
+    L.off_prog = o;   o = align_up(o + sizeof(int32_t) * 2 * (size_t)B, 256);
+    L.off_gap = o;    o = align_up(o + sizeof(int32_t) * (2 * (size_t)B + 5), 256);
     L.total = o;
     return L;
 }
@@ -306,6 +325,11 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -321,6 +345,9 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 // Returns true once the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -341,6 +368,117 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// ------------------------------------------------- dense gradient chunks
+
+// Asks L2 to fetch bytes [lo, hi) ahead of use, rounded inward to 16 bytes
+// (a bulk prefetch is a hint: it holds no register and completes nothing).
+__device__ __forceinline__ void prefetch_l2(uintptr_t lo, uintptr_t hi) {
+    lo = (lo + 15) & ~uintptr_t(15);
+    hi &= ~uintptr_t(15);
+    if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t load_elem(uintptr_t addr) {
+    if constexpr (Elem<DT>::bytes == 4) {
+        return *reinterpret_cast<const uint32_t*>(addr);
+    } else {
+        return *reinterpret_cast<const unsigned short*>(addr);
+    }
+}
+template <int DT>
+__device__ __forceinline__ void store_elem(uintptr_t addr, uint32_t bits) {
+    if constexpr (Elem<DT>::bytes == 4) {
+        *reinterpret_cast<uint32_t*>(addr) = bits;
+    } else {
+        *reinterpret_cast<unsigned short*>(addr) = (unsigned short)bits;
+    }
+}
+
+// Gradient of one whole 16-byte chunk: s * exp(lp) + pn element by element,
+// pn the chunk's negated class sums (zero where none), in pairs on the
+// paired fp32 pipes, rounded once into the chunk's dtype.  exp(lp) is
+// 2^(x log2 e + bias): bias = 0 for log probabilities, -lse log2 e for a row
+// of logits (then exp(lp) is the row's softmax); x log2 e + 0 rounds as the
+// product alone, so log-probability rows are unchanged by the bias.
+template <int DT>
+__device__ __forceinline__ uint4 chunk_grad(uint4 in, float s, const float (&pn)[16 / Elem<DT>::bytes], float bias) {
+    const float2 l2e = make_float2(kLog2e, kLog2e), s2 = make_float2(s, s), b2 = make_float2(bias, bias);
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    if constexpr (DT == 0) {
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e, b2);
+            const float2 r = __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[i], pn[i + 1]));
+            o[i] = r.x;
+            o[i + 1] = r.y;
+        }
+        return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+    } else {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 x;
+            if constexpr (DT == 1) {  // bfloat16: the high half is already a float
+                x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+            } else {
+                x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            }
+            const float2 t = __ffma2_rn(x, l2e, b2);
+            const float2 r =
+                __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[2 * i], pn[2 * i + 1]));
+            o[i] = pack2<DT>(r.x, r.y);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+
+// s * exp(lp) of a whole 16-byte chunk, element by element in pairs,
+// rounded once into the chunk's dtype: the gradient of a chunk that holds no
+// class sum.
+template <int DT>
+__device__ __forceinline__ uint4 chunk_scaled(uint4 in, float s, float bias) {
+    const float2 l2e = make_float2(kLog2e, kLog2e), s2 = make_float2(s, s), b2 = make_float2(bias, bias);
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    if constexpr (DT == 0) {
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e, b2);
+            const float2 r = __fmul2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
+            o[i] = r.x;
+            o[i + 1] = r.y;
+        }
+        return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+    } else {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 x;
+            if constexpr (DT == 1) {
+                x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+            } else {
+                x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            }
+            const float2 t = __ffma2_rn(x, l2e, b2);
+            const float2 r = __fmul2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
+            o[i] = pack2<DT>(r.x, r.y);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
 __device__ __forceinline__ void set_status(Control* ctrl, uint32_t bits) { atomicOr(&ctrl->status, bits); }

@@ -55,6 +55,29 @@ struct GradArgs {
     uint32_t gp_mul;     // offset group of pair j: (j * gp_mul) >> 21 == j / L.gpairs
 };
 
+// The gradient stream for wide rows (stream.cu): class sums and dense rows in
+// one pass, fed by bulk copies into per-team shared-memory slots.
+struct StreamArgs {
+    Layout L;
+    void* ws;
+    const void* lp;
+    void* grad;
+    const int32_t* cu;  // cu_seqlens
+    const int32_t* targets;
+    const float* grad_loss;
+    int D;
+    int blank;
+    int reduction;
+    int zero_infinity;
+    int elem_bytes;
+    int fused;          // forward-backward call: rows are claimed as the chains publish them
+    uint32_t gp_mul;    // offset group of pair j: (j * gp_mul) >> 21 == j / L.gpairs
+    int nteams, nslots; // teams of four warps per CTA, shared-memory slots per team
+    int team_bytes;     // shared memory of one team
+    int lp_cap, sr_cap, slot_bytes;  // a slot: lp span, stored alpha row, stored beta row, label records
+    int desc_off, mbar_off, slots_off, ecls_off, eval_off, labm_off, labe_off, blkm_off, blke_off, red_off;
+};
+
 __global__ void prep_kernel(PrepArgs a);
 template <int DT>
 __global__ void lse_kernel(ChainArgs a);
@@ -65,6 +88,9 @@ __global__ void chain_kernel(ChainArgs a);
 __global__ void post_kernel(GradArgs a);
 template <int DT>
 __global__ void grad_kernel(GradArgs a);
+template <int DT>
+__global__ void stream_kernel(StreamArgs a);
+bool stream_plan(StreamArgs& a);  // team count and slot layout; false when one team does not fit
 void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& warp_smem);
 uint32_t grad_group_multiplier(const Layout& L);  // 0 if no exact multiplier exists
 
@@ -75,5 +101,6 @@ cudaError_t launch_emit(const ChainArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_post(const GradArgs& a, cudaStream_t s);
 cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_stream(const StreamArgs& a, int dtype, cudaStream_t s);
 
 }  // namespace ctcp

@@ -70,79 +70,6 @@ __device__ __forceinline__ float posterior(int va, int vb, int base, float c) {
     return __int_as_float(max(__float_as_int(ma * mb * c) + (n << 23), 0));
 }
 
-// Asks L2 to fetch bytes [lo, hi) ahead of use, rounded inward to 16 bytes
-// (a bulk prefetch is a hint: it holds no register and completes nothing).
-__device__ __forceinline__ void prefetch_l2(uintptr_t lo, uintptr_t hi) {
-    lo = (lo + 15) & ~uintptr_t(15);
-    hi &= ~uintptr_t(15);
-    if (hi > lo)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-template <int DT>
-__device__ __forceinline__ uint32_t load_elem(uintptr_t addr) {
-    if constexpr (Elem<DT>::bytes == 4) {
-        return *reinterpret_cast<const uint32_t*>(addr);
-    } else {
-        return *reinterpret_cast<const unsigned short*>(addr);
-    }
-}
-template <int DT>
-__device__ __forceinline__ void store_elem(uintptr_t addr, uint32_t bits) {
-    if constexpr (Elem<DT>::bytes == 4) {
-        *reinterpret_cast<uint32_t*>(addr) = bits;
-    } else {
-        *reinterpret_cast<unsigned short*>(addr) = (unsigned short)bits;
-    }
-}
-
-// Gradient of one whole 16-byte chunk: s * exp(lp) + pn element by element,
-// pn the chunk's negated class sums (zero where none), in pairs on the
-// paired fp32 pipes, rounded once into the chunk's dtype.  exp(lp) is
-// 2^(x log2 e + bias): bias = 0 for log probabilities, -lse log2 e for a row
-// of logits (then exp(lp) is the row's softmax); x log2 e + 0 rounds as the
-// product alone, so log-probability rows are unchanged by the bias.
-template <int DT>
-__device__ __forceinline__ uint4 chunk_grad(uint4 in, float s, const float (&pn)[16 / Elem<DT>::bytes], float bias) {
-    const float2 l2e = make_float2(kLog2e, kLog2e), s2 = make_float2(s, s), b2 = make_float2(bias, bias);
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    if constexpr (DT == 0) {
-        float o[4];
-#pragma unroll
-        for (int i = 0; i < 4; i += 2) {
-            const float2 t = __ffma2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e, b2);
-            const float2 r = __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[i], pn[i + 1]));
-            o[i] = r.x;
-            o[i + 1] = r.y;
-        }
-        return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
-    } else {
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 x;
-            if constexpr (DT == 1) {  // bfloat16: the high half is already a float
-                x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-            } else {
-                x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            }
-            const float2 t = __ffma2_rn(x, l2e, b2);
-            const float2 r =
-                __ffma2_rn(s2, make_float2(fast_ex2(t.x), fast_ex2(t.y)), make_float2(pn[2 * i], pn[2 * i + 1]));
-            o[i] = pack2<DT>(r.x, r.y);
-        }
-        return make_uint4(o[0], o[1], o[2], o[3]);
-    }
-}
-
 }  // namespace
 
 // Class sums of every row.  A warp takes kPostRows consecutive rows at a
@@ -158,12 +85,10 @@ __global__ void __launch_bounds__(kPostThreads) post_kernel(GradArgs a) {
     float* gam = post_smem + (size_t)warp * kPostRows * ulen;  // label posteriors of the rows, [row][j]
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
-    const int32_t* __restrict__ aoff = ws_at<int32_t>(a.ws, a.L.off_aoff);
-    const int32_t* __restrict__ boff = ws_at<int32_t>(a.ws, a.L.off_boff);
+    // a stored row is [the per-warp offsets, owo ints][the state pairs, pitch ints]
     const int* __restrict__ alpha = ws_at<int>(a.ws, a.L.off_alpha);
     const int* __restrict__ beta = ws_at<int>(a.ws, a.L.off_beta);
-    const int32_t* __restrict__ nxt = ws_at<int32_t>(a.ws, a.L.off_nxt);
-    const int32_t* __restrict__ rank = ws_at<int32_t>(a.ws, a.L.off_rank);
+    const LabelRec* __restrict__ lbl = ws_at<LabelRec>(a.ws, a.L.off_lbl);
     RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
     int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
     const uint32_t gp_mul = a.gp_mul;  // j / gpairs == (j * gp_mul) >> kGroupShift for every pair j
@@ -240,13 +165,15 @@ __global__ void __launch_bounds__(kPostThreads) post_kernel(GradArgs a) {
                 const bool on = live[r] && j <= U[r];
                 const bool lab = live[r] && j < U[r];
                 const int64_t row = r0 + r;
-                av[r] = on ? *reinterpret_cast<const int2*>(alpha + row * a.L.pitch + 2 * j) : make_int2(kFixZero, kFixZero);
-                bv[r] = on ? *reinterpret_cast<const int2*>(beta + row * a.L.pitch + 2 * j) : make_int2(kFixZero, kFixZero);
-                bl[r] = lab ? beta[row * a.L.pitch + 2 * j + 2] : kFixZero;
-                oa[r] = on ? aoff[row * a.L.nwo + ga] : 0;
-                ob0[r] = on ? boff[row * a.L.nwo + ga] : 0;
-                ob1[r] = lab ? boff[row * a.L.nwo + gb] : 0;
-                rk[r] = lab ? rank[moff[r] + j] : -1;
+                const int* ar = alpha + row * a.L.spitch;
+                const int* br = beta + row * a.L.spitch;
+                av[r] = on ? *reinterpret_cast<const int2*>(ar + a.L.owo + 2 * j) : make_int2(kFixZero, kFixZero);
+                bv[r] = on ? *reinterpret_cast<const int2*>(br + a.L.owo + 2 * j) : make_int2(kFixZero, kFixZero);
+                bl[r] = lab ? br[a.L.owo + 2 * j + 2] : kFixZero;
+                oa[r] = on ? ar[ga] : 0;
+                ob0[r] = on ? br[ga] : 0;
+                ob1[r] = lab ? br[gb] : 0;
+                rk[r] = lab ? lbl[moff[r] + j].rank : -1;
             }
 #pragma unroll
             for (int r = 0; r < kPostRows; ++r) {
@@ -267,11 +194,12 @@ __global__ void __launch_bounds__(kPostThreads) post_kernel(GradArgs a) {
 #pragma unroll
             for (int r = 0; r < kPostRows; ++r) {
                 if (!(live[r] && j < U[r])) continue;
-                const int kind = rank[moff[r] + j];
+                const LabelRec lr = lbl[moff[r] + j];
+                const int kind = lr.rank;
                 if (kind >= 0) {
-                    const int32_t* nx = nxt + moff[r];
+                    const LabelRec* lb = lbl + moff[r];
                     float sum = gam[r * ulen + j];
-                    for (int jj = nx[j]; jj >= 0; jj = nx[jj]) sum += gam[r * ulen + jj];
+                    for (int jj = lr.next; jj >= 0; jj = lb[jj].next) sum += gam[r * ulen + jj];
                     ent[(r0 + r) * a.L.ecap + kind] = make_int2(a.targets[toff[r] + j], __float_as_int(-scale[r] * sum));
                 }
             }

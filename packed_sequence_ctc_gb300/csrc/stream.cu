@@ -1,0 +1,703 @@
+// Gradient of the packed CTC loss for wide rows: one pass that forms each
+// row's class sums and writes its dense gradient, fed by bulk (TMA) copies.
+//
+// Page "feat(asr): native CTC loss kernel over sequence-packed log
+// probabilities", ctc_loss.py ``_beta_grad_kernel``:
+//
+//   posterior_t(s) = alpha_t(s) beta_t(s) / p_t(l'_s) / Z,
+//   grad[t, c]     = scale * (exp(lp[t, c]) - sum over s with l'_s = c of posterior_t(s)),
+//   rows outside every utterance are 0, and so are the rows of an utterance
+//   whose loss is infinite under zero_infinity.
+//
+// Z is the utterance's total path probability.  Every frame's states carry
+// all of it: Z = sum_s alpha_t(s) beta_t(s) / p_t(l'_s) for each t.  So each
+// row is normalised by its own sum, which needs nothing from the end of the
+// alpha chain (the forward-backward call streams rows while the chains still
+// run) and makes each frame's posteriors sum to one to float32 rounding.  A
+// row whose sum is zero has no path through it: the utterance cannot be
+// aligned (its loss is +inf).
+//
+// Structure.  One CTA per SM, made of teams of four warps.  A team owns a few
+// shared-memory slots.  For each row it takes, one thread issues bulk
+// copies of everything the row needs into a free slot: the log-probability
+// row (its 16-byte aligned span), the stored alpha and beta rows and their
+// per-warp offsets, all completing on the slot's mbarrier.  The team works on
+// the oldest slot while the copies of the next ones are in flight:
+//   1. class sums: the state posteriors of the row from the slot, summed per
+//      distinct class in a fixed order (no atomics on values; bitwise
+//      reproducible), each class sum linked to the 16-byte chunk of the row
+//      that holds its class;
+//   2. the dense row: every chunk is read from the slot, gets
+//      scale * exp(lp) plus the chunk's class sums (if any), is rounded once
+//      into the row's dtype and stored as one 16-byte vector (the ragged
+//      chunks at the ends element by element).
+//
+// Work is handed out per utterance: a team scans the utterances for one with
+// rows left and claims its next row with an atomic counter.  In the
+// forward-backward call the rows of an utterance are handed out from its
+// middle outwards, the order in which both chains reach them, and a row is
+// only claimed once the chains have published that they stored it.  Rows
+// outside every utterance come last, from a list the prep kernel made.
+#include "ctc_common.cuh"
+#include "ctc_kernels.h"
+
+namespace ctcp {
+
+namespace {
+
+constexpr int kTeamWarps = 4;
+constexpr int kTeamThreads = 32 * kTeamWarps;
+constexpr int kMaxTeams = 4;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // a bounded wait gives up after 2 s
+
+enum : int { kEnd = 0, kGrad = 1, kZero = 2 };
+
+// What a team knows about the row in a slot (written by the team's leader).
+struct SlotDesc {
+    int32_t kind;   // kEnd, kGrad or kZero
+    int32_t row;    // row of the (T_total, D) buffers
+    int32_t b;      // utterance (kGrad)
+    int32_t U;
+    int32_t toff, moff, nown, has_nan;
+    float scale;
+    float bias;     // exponent bias of exp(lp): -lse log2 e for logits input, else 0
+    int32_t pad[2];
+};
+static_assert(sizeof(SlotDesc) == 48, "slot descriptor is 48 bytes");
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void team_bar(int team) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(kTeamThreads) : "memory");
+}
+// Team barrier that also ORs a predicate over the team's threads.
+__device__ __forceinline__ bool team_bar_or(int team, bool v) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((int)v), "r"(1 + team), "r"(kTeamThreads)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
+
+// Waits (bounded) until the slot's copies have landed.  False: gave up.
+__device__ __forceinline__ bool wait_slot(uint64_t* bar, uint32_t parity) {
+    for (int i = 0; i < 4; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        for (int i = 0; i < 8; ++i) {
+            if (mbar_try_wait(bar, parity)) return true;
+            __nanosleep(64);  // leave the issue slots to the warps that have work
+        }
+        if (globaltimer() - t0 > kWaitNs) return false;
+    }
+}
+
+// Row of utterance frame order k when rows are handed out from the middle
+// outwards: m, m - 1, m + 1, m - 2, ... (m = T / 2).
+__device__ __forceinline__ int middle_out(int k, int T) {
+    const int m = T >> 1;
+    const int i = k >> 1;
+    if ((k & 1) == 0) return m + i;
+    if (i < m) return m - 1 - i;
+    return m + i;  // unreachable for k < T
+}
+
+// Exponent of a zero product (below every real one).
+constexpr int kXSumNone = -(1 << 30);
+
+// Product of a stored alpha word and a stored beta word (enc_state): the
+// mantissa product in [1, 4) and its binary exponent (offsets added).
+__device__ __forceinline__ void state_product(int va, int vb, int off, float& m, int& e) {
+    if (va == kFixZero || vb == kFixZero) {
+        m = 0.0f;
+        e = kXSumNone;
+        return;
+    }
+    const float ma = __int_as_float(((va & 0x7ffff) << 4) | 0x3f800000);
+    const float mb = __int_as_float(((vb & 0x7ffff) << 4) | 0x3f800000);
+    m = ma * mb;
+    e = (va >> kFixFrac) + (vb >> kFixFrac) + off;
+}
+
+}  // namespace
+
+// Everything row `row` needs from the utterance b that covers it (kGrad), or a
+// zero row.  `u` is b's metadata.
+__device__ __forceinline__ SlotDesc describe_row(const StreamArgs& a, int row, int b, const UttInfo& u, bool logits,
+                                                 float inv_count, const float* lse) {
+    SlotDesc d{};
+    d.row = row;
+    d.b = b;
+    if (b < 0 || !u.valid || !u.labels_ok || row - u.start >= u.T) {
+        d.kind = kZero;
+        return d;
+    }
+    d.kind = kGrad;
+    d.U = u.U;
+    d.toff = u.toff;
+    d.moff = u.moff;
+    d.nown = u.n_owners;
+    d.has_nan = u.has_nan;
+    float sc;
+    if (a.reduction == CTC_PACKED_NONE) {
+        sc = a.grad_loss[b];
+    } else if (a.reduction == CTC_PACKED_SUM) {
+        sc = a.grad_loss[0];
+    } else if (a.reduction == CTC_PACKED_MEAN) {
+        sc = __fdiv_rn(a.grad_loss[0], (float)a.L.B * (float)max(u.U, 1));
+    } else {  // mean_batch: g / B, mean_volume: g / sum(U)
+        sc = __fdiv_rn(a.grad_loss[0], inv_count);
+    }
+    d.scale = sc;
+    d.bias = logits ? -lse[row] * kLog2e : 0.0f;
+    return d;
+}
+
+// Rows [lo, hi] that frames k0 .. k1 - 1 of the middle-out order cover.
+__device__ __forceinline__ void middle_out_span(int k0, int k1, int T, int& lo, int& hi) {
+    const int a = middle_out(k1 - 1, T);
+    const int b = k1 - 2 >= k0 ? middle_out(k1 - 2, T) : a;
+    lo = min(a, b);
+    hi = max(a, b);
+    const int f = middle_out(k0, T);  // k0 alone: the middle row
+    lo = min(lo, f);
+    hi = max(hi, f);
+}
+
+template <int DT>
+__global__ void __launch_bounds__((32 + kTeamThreads) * kMaxTeams, 1) stream_kernel(StreamArgs a) {
+    constexpr int E = Elem<DT>::bytes;
+    constexpr int V = 16 / E;
+    constexpr int kBatch = 4;  // rows the forward-backward call claims at once
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // a team: one producer warp and kTeamWarps worker warps
+    const int team = threadIdx.x / (kTeamThreads + 32);
+    const int tw = threadIdx.x % (kTeamThreads + 32);
+    const bool producer = tw < 32;
+    const int tt = producer ? tw : tw - 32;
+    const int lane = threadIdx.x & 31, wt = tt >> 5;
+    const int NS = a.nslots, NT = a.nteams;
+    unsigned char* tb = smem_raw + (size_t)team * a.team_bytes;
+    SlotDesc* desc = reinterpret_cast<SlotDesc*>(tb + a.desc_off);
+    uint64_t* full = reinterpret_cast<uint64_t*>(tb + a.mbar_off);
+    uint64_t* empty = full + NS;
+    unsigned char* slots = tb + a.slots_off;
+    int* ent_cls = reinterpret_cast<int*>(tb + a.ecls_off);
+    float* ent_val = reinterpret_cast<float*>(tb + a.eval_off);
+    float* lab_m = reinterpret_cast<float*>(tb + a.labm_off);
+    int* lab_e = reinterpret_cast<int*>(tb + a.labe_off);
+    float* blk_m = reinterpret_cast<float*>(tb + a.blkm_off);  // blank state of pair j
+    int* blk_e = reinterpret_cast<int*>(tb + a.blke_off);
+    int* red = reinterpret_cast<int*>(tb + a.red_off);  // [warp][4]: Z (M, S), blank (M, S)
+
+    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
+    const int32_t* queue = ws_at<int32_t>(a.ws, a.L.off_queue);
+    int32_t* claim = ws_at<int32_t>(a.ws, a.L.off_claim);
+    const int32_t* prog = ws_at<int32_t>(a.ws, a.L.off_prog);
+    const int32_t* gap_lo = ws_at<int32_t>(a.ws, a.L.off_gap);
+    const int32_t* gap_pre = gap_lo + (a.L.B + 2);
+    const float* lse = ws_at<float>(a.ws, a.L.off_lse);
+    const int D = a.D;
+    const int64_t T_total = a.L.T_total;
+    const uintptr_t lp0 = reinterpret_cast<uintptr_t>(a.lp);
+    const uintptr_t gr0 = reinterpret_cast<uintptr_t>(a.grad);
+    const uintptr_t lp_end = lp0 + (uintptr_t)T_total * D * E;
+    const uintptr_t lp_end16 = lp_end & ~uintptr_t(15);
+
+    if (!producer) {
+        if (tt == 0) {
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 1);
+            }
+            fence_mbar_init();
+        }
+    }
+    __syncthreads();
+    if (!a.fused) {
+        pdl_wait();  // the forward's stored rows and metadata
+        pdl_trigger();
+    }
+
+    if (producer) {
+        // ------------------------------------------------------------ producer
+        // The forward-backward call starts while the chain kernel runs; what
+        // the prep and emission kernels wrote is visible once the chain kernel
+        // has started (it waited for them) and said so.
+        bool failed = false;
+        if (a.fused) {
+            const unsigned long long t0 = globaltimer();
+            int live = 0;
+            if (lane == 0) {
+                while ((live = ld_acquire(reinterpret_cast<const int32_t*>(&ctrl->chain_live))) == 0) {
+                    __nanosleep(256);
+                    if (globaltimer() - t0 > kWaitNs) break;
+                }
+            }
+            live = __shfl_sync(0xffffffffu, live, 0);
+            if (!live) {
+                if (lane == 0) set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
+                failed = true;
+            }
+        }
+        const uint32_t status0 = ld_volatile(reinterpret_cast<const int32_t*>(&ctrl->status));
+        const bool ready = ctrl->grad_ready != 0;
+        if (!a.fused && blockIdx.x == 0 && lane == 0 && T_total > 0 && !ready)
+            set_status(ctrl, CTC_PACKED_DEV_NO_GRAD_STATE);
+        // malformed spans or no stored state: every row is written as zero
+        const bool all_zero = !ready || (status0 & CTC_PACKED_DEV_BAD_CU_SEQLENS) != 0;
+        const bool logits = ctrl->logits != 0;
+        const float inv_count = a.reduction == CTC_PACKED_MEAN_VOLUME ? (float)ctrl->tl_total : (float)a.L.B;
+
+        int k = 0;  // slots of this team handed out so far: slot k % NS, its use k / NS
+        // hands descriptor d to the team's next slot (lane 0), issuing the row's bulk copies
+        auto emit = [&](const SlotDesc& d) -> bool {
+            const int s = k % NS, use = k / NS;
+            ++k;
+            unsigned char* tbp = tb;
+            SlotDesc* dsc = desc;
+            uint64_t* fl = full;
+            uint64_t* em = empty;
+            if (use >= 1 && !wait_slot(&em[s], (uint32_t)(use - 1) & 1u)) {
+                set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
+                return false;
+            }
+            dsc[s] = d;
+            if (d.kind != kGrad) {
+                mbar_arrive(&fl[s]);
+                return true;
+            }
+            unsigned char* sl = tbp + a.slots_off + (size_t)s * a.slot_bytes;
+            const uintptr_t rs = lp0 + (uintptr_t)d.row * D * E;
+            const uintptr_t base = rs & ~uintptr_t(15);
+            uintptr_t cend = (rs + (uintptr_t)D * E + 15) & ~uintptr_t(15);
+            if (cend > lp_end16) cend = lp_end16;
+            const uint32_t lp_bytes = cend > base ? (uint32_t)(cend - base) : 0u;
+            // a stored row: the per-warp offsets, then the state pairs up to pair U
+            const uint32_t sr_bytes = (uint32_t)align_up(4 * (size_t)a.L.owo + 8 * (size_t)(d.U + 1), 16);
+            const uint32_t lb_bytes = 16u * (uint32_t)d.U;
+            mbar_expect_tx(&fl[s], lp_bytes + 2 * sr_bytes + lb_bytes);
+            if (lp_bytes) bulk_g2s(sl, reinterpret_cast<const void*>(base), lp_bytes, &fl[s]);
+            const unsigned char* wsb = static_cast<const unsigned char*>(a.ws);
+            bulk_g2s(sl + a.lp_cap, wsb + a.L.off_alpha + (size_t)d.row * a.L.spitch * 4, sr_bytes, &fl[s]);
+            bulk_g2s(sl + a.lp_cap + a.sr_cap, wsb + a.L.off_beta + (size_t)d.row * a.L.spitch * 4, sr_bytes, &fl[s]);
+            if (lb_bytes) bulk_g2s(sl + a.lp_cap + 2 * a.sr_cap, wsb + a.L.off_lbl + 16 * (size_t)d.moff, lb_bytes, &fl[s]);
+            return true;
+        };
+
+        if (!a.fused) {
+            // the backward call: team g of G takes rows g, g + G, ... ; each row's
+            // utterance by walking cu_seqlens forward (rows only grow)
+            if (lane == 0 && !failed) {
+                int b = -1;
+                UttInfo u{};
+                const int B = a.L.B;
+                const int32_t* cu = a.cu;
+                const int64_t G = (int64_t)gridDim.x * NT;
+                for (int64_t r = (int64_t)blockIdx.x * NT + team; r < T_total; r += G) {
+                    SlotDesc d;
+                    if (all_zero) {
+                        d = SlotDesc{};
+                        d.kind = kZero;
+                        d.row = (int)r;
+                    } else {
+                        int nb = b;
+                        while (nb + 1 < B && (int64_t)cu[nb + 1] <= r) ++nb;
+                        if (nb != b) {
+                            b = nb;
+                            u = utt[b];
+                        }
+                        d = describe_row(a, (int)r, b, u, logits, inv_count, lse);
+                    }
+                    if (!emit(d)) {
+                        failed = true;
+                        break;
+                    }
+                }
+            }
+        } else if (!failed) {
+            // the forward-backward call: each utterance's rows from the middle
+            // outwards, kBatch at a time, once both chains have stored them
+            const int n_utt = all_zero ? 0 : ctrl->n_lab;
+            const int32_t* ulist = queue + 2 * a.L.B + 1;
+            int cursor = n_utt > 0 ? (int)(((int64_t)blockIdx.x * NT + team) % n_utt) : 0;
+            const unsigned long long t0 = globaltimer();
+            while (n_utt > 0) {
+                int found = -1;
+                bool pending = false;
+                for (int base = 0; base < n_utt && found < 0; base += 32) {
+                    const int i = base + lane;
+                    bool avail = false, rdy = false;
+                    if (i < n_utt) {
+                        int idx = cursor + i;
+                        if (idx >= n_utt) idx -= n_utt;
+                        const int b = ulist[idx];
+                        const int T = utt[b].T;
+                        const int kc = ld_volatile(claim + b);
+                        avail = kc < T;
+                        if (avail) {
+                            int lo, hi;
+                            middle_out_span(kc, min(kc + kBatch, T), T, lo, hi);
+                            rdy = ld_volatile(prog + 2 * b) >= hi + 1 && ld_volatile(prog + 2 * b + 1) >= T - lo;
+                        }
+                    }
+                    const unsigned rm = __ballot_sync(0xffffffffu, rdy);
+                    pending = pending || __any_sync(0xffffffffu, avail);
+                    if (rm) found = base + __ffs(rm) - 1;
+                }
+                if (found >= 0) {
+                    int idx = cursor + found;
+                    if (idx >= n_utt) idx -= n_utt;
+                    cursor = idx;
+                    const int b = ulist[idx];
+                    int ok = 1;
+                    if (lane == 0) {
+                        const UttInfo u = utt[b];
+                        const int T = u.T;
+                        const int kc = atomicAdd(claim + b, kBatch);
+                        if (kc < T) {
+                            const int k1 = min(kc + kBatch, T);
+                            int lo, hi;
+                            middle_out_span(kc, k1, T, lo, hi);
+                            // a race may hand out rows past the scan's: wait for the chains
+                            const unsigned long long w0 = globaltimer();
+                            while (!(ld_acquire(prog + 2 * b) >= hi + 1 && ld_acquire(prog + 2 * b + 1) >= T - lo)) {
+                                __nanosleep(128);
+                                if (globaltimer() - w0 > kWaitNs) {
+                                    ok = 0;
+                                    break;
+                                }
+                            }
+                            // the chains' rows are read by bulk copies (the async proxy)
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            for (int j = kc; j < k1 && ok; ++j) {
+                                const int row = u.start + middle_out(j, T);
+                                if (!emit(describe_row(a, row, b, u, logits, inv_count, lse))) ok = 0;
+                            }
+                            if (!ok) set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        failed = true;
+                        break;
+                    }
+                    continue;
+                }
+                if (!pending) break;  // every utterance is handed out
+                __nanosleep(512);     // rows remain but the chains have not reached them yet
+                int late = lane == 0 && globaltimer() - t0 > kWaitNs;
+                if (__shfl_sync(0xffffffffu, late, 0)) {
+                    if (lane == 0) set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
+                    failed = true;
+                    break;
+                }
+            }
+            // rows outside every utterance (every row, when nothing can be computed)
+            if (lane == 0 && !failed) {
+                const int gap_total = all_zero ? (int)T_total : gap_pre[a.L.B + 2];
+                for (;;) {
+                    const int g0 = (int)atomicAdd(&ctrl->gap_head, 8u);
+                    if (g0 >= gap_total) break;
+                    const int g1 = min(g0 + 8, gap_total);
+                    int gi = 0;
+                    if (!all_zero) {
+                        int lo = 0, hi = a.L.B + 1;  // gap_pre[lo] <= g0 < gap_pre[lo + 1]
+                        while (lo < hi) {
+                            const int mid = (lo + hi + 1) >> 1;
+                            if (gap_pre[mid] <= g0) {
+                                lo = mid;
+                            } else {
+                                hi = mid - 1;
+                            }
+                        }
+                        gi = lo;
+                    }
+                    for (int g = g0; g < g1 && !failed; ++g) {
+                        while (!all_zero && gap_pre[gi + 1] <= g) ++gi;
+                        SlotDesc d{};
+                        d.kind = kZero;
+                        d.row = all_zero ? g : gap_lo[gi] + (g - gap_pre[gi]);
+                        if (!emit(d)) failed = true;
+                    }
+                    if (failed) break;
+                }
+            }
+        }
+        // the end mark
+        if (lane == 0) {
+            SlotDesc d{};
+            d.kind = kEnd;
+            emit(d);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ teams
+    for (int i = 0;; ++i) {
+        const int cur = i % NS;
+        if (team_bar_or(team, !wait_slot(&full[cur], (uint32_t)(i / NS) & 1u))) {
+            if (tt == 0) set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
+            break;  // the producer stopped: nothing is in flight for this slot
+        }
+        const SlotDesc d = desc[cur];
+        if (d.kind == kEnd) break;
+        const unsigned char* sl = slots + (size_t)cur * a.slot_bytes;
+        const uintptr_t rs = lp0 + (uintptr_t)d.row * D * E;  // the row's lp bytes [rs, re)
+        const uintptr_t re = rs + (uintptr_t)D * E;
+        const uintptr_t base = rs & ~uintptr_t(15);
+        const int lead = (int)(rs - base);
+        const int nq = (int)((re - base + 15) >> 4);
+        // whole chunks [qa, qb): inside the row and inside the copied span
+        const int qa = lead == 0 ? 0 : 1;
+        uintptr_t wend = re & ~uintptr_t(15);
+        if (wend > lp_end16) wend = lp_end16;
+        const int qb = max(qa, (int)((wend - base) >> 4));
+        bool zero = d.kind != kGrad;
+        const float s = d.scale;
+        int n_ent = 0;  // class sums of the row (entries 0 .. n_ent - 1), applied after the dense pass
+        if (!zero) {
+            // 1. posteriors of the row.  Pass one: each state's product
+            // alpha * beta / p as (mantissa, exponent) into shared memory, and
+            // the row's largest exponent M.  Pass two: the row sum Z and the
+            // blank column's sum, both scaled by 2^-M.
+            const int* A = reinterpret_cast<const int*>(sl + a.lp_cap);  // offsets, then pairs
+            const int* Bt = reinterpret_cast<const int*>(sl + a.lp_cap + a.sr_cap);
+            const int4* LB = reinterpret_cast<const int4*>(sl + a.lp_cap + 2 * a.sr_cap);  // LabelRec
+            const int* Ap = A + a.L.owo;
+            const int* Bp = Bt + a.L.owo;
+            const int U = d.U;
+            int emax = kXSumNone;
+            for (int j = tt; j <= U; j += kTeamThreads) {
+                const int ga = (int)(((uint32_t)j * a.gp_mul) >> 21);
+                const int gb = (int)(((uint32_t)(j + 1) * a.gp_mul) >> 21);
+                const int2 av = reinterpret_cast<const int2*>(Ap)[j];
+                const int2 bv = reinterpret_cast<const int2*>(Bp)[j];
+                float m;
+                int e;
+                state_product(av.x, bv.y, A[ga] + Bt[ga], m, e);  // blank state 2j
+                blk_m[j] = m;
+                blk_e[j] = e;
+                emax = max(emax, e);
+                if (j < U) {
+                    state_product(av.y, Bp[2 * j + 2], A[ga] + Bt[gb], m, e);  // label state 2j+1
+                    lab_m[j] = m;
+                    lab_e[j] = e;
+                    emax = max(emax, e);
+                }
+            }
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            if (lane == 0) red[wt] = emax;
+            team_bar(team);
+            int M = red[0];
+#pragma unroll
+            for (int w = 1; w < kTeamWarps; ++w) M = max(M, red[w]);
+            float zs = 0.0f, bs = 0.0f;
+            for (int j = tt; j <= U; j += kTeamThreads) {
+                const float pb = blk_m[j] * pow2_nonpos(blk_e[j] - M);
+                zs += pb;
+                bs += pb;
+                if (j < U) {
+                    const float pl = lab_m[j] * pow2_nonpos(lab_e[j] - M);
+                    zs += pl;
+                    if (LB[j].x == -2) bs += pl;  // a target id equal to the blank
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {  // same order on every lane: same bits
+                zs += __shfl_xor_sync(0xffffffffu, zs, o);
+                bs += __shfl_xor_sync(0xffffffffu, bs, o);
+            }
+            if (lane == 0) {
+                red[kTeamWarps + wt] = __float_as_int(zs);
+                red[2 * kTeamWarps + wt] = __float_as_int(bs);
+            }
+            team_bar(team);
+            float Z = __int_as_float(red[kTeamWarps]), Bsum = __int_as_float(red[2 * kTeamWarps]);
+#pragma unroll
+            for (int w = 1; w < kTeamWarps; ++w) {
+                Z += __int_as_float(red[kTeamWarps + w]);
+                Bsum += __int_as_float(red[2 * kTeamWarps + w]);
+            }
+            auto link = [&](int r, int c, float v) {
+                ent_cls[r] = c;
+                ent_val[r] = v;
+            };
+            if (Z == 0.0f && a.zero_infinity) {
+                zero = true;  // no path: the loss is +inf, zeroed with its gradient
+            } else if (s != 0.0f) {
+                // 2. class sums, each distinct class summed by its first occurrence
+                const float ns = -s * __frcp_rn(Z);  // Z == 0 (no path): non-finite, as the loss
+                const bool nan_row = d.has_nan != 0;
+                for (int j = tt; j < U; j += kTeamThreads) {
+                    const int4 lr = LB[j];
+                    if (lr.x < 0) continue;
+                    float sum = lab_m[j] * pow2_nonpos(lab_e[j] - M);
+                    for (int jj = lr.y; jj >= 0; jj = LB[jj].y) sum = fmaf(lab_m[jj], pow2_nonpos(lab_e[jj] - M), sum);
+                    link(lr.x, lr.z, nan_row ? __int_as_float(0x7fc00000) : ns * sum);
+                }
+                if (tt == 0) link(d.nown - 1, a.blank, nan_row ? __int_as_float(0x7fc00000) : ns * Bsum);
+                n_ent = d.nown;
+            }
+        }
+        // 3. the dense row: scale * exp(lp) for every element, 16 bytes at a time
+        const float bias = d.kind == kGrad ? d.bias : 0.0f;
+        const uintptr_t gbase = gr0 + (base - lp0);
+        const int nint = qb - qa;
+        {
+            const uint32_t sq = smem_addr(sl) + 16u * (uint32_t)qa;
+            uint4* gq = reinterpret_cast<uint4*>(gbase) + qa;
+            if (zero) {
+                for (int i = tt; i < nint; i += kTeamThreads) gq[i] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+#pragma unroll 4
+                for (int i = tt; i < nint; i += kTeamThreads) gq[i] = chunk_scaled<DT>(lds128(sq + 16u * (uint32_t)i), s, bias);
+            }
+        }
+        // the ragged chunks at the row's ends (and past the buffer's last whole chunk)
+        const int nedge = qa + (nq - qb);
+        for (int k2 = tt; k2 < nedge; k2 += kTeamThreads) {
+            const int q = k2 < qa ? 0 : qb + (k2 - qa);
+            const uintptr_t cb = base + 16 * (uintptr_t)q;
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (!zero) {
+                uint4 in;
+                if (cb + 16 <= lp_end16) {
+                    in = *reinterpret_cast<const uint4*>(sl + 16 * q);
+                } else {  // past the last whole 16-byte chunk of the buffer: from global memory
+                    uint32_t w[4] = {0u, 0u, 0u, 0u};
+                    for (int i2 = 0; i2 < V; ++i2) {
+                        const uintptr_t ad = cb + (uintptr_t)i2 * E;
+                        if (ad >= rs && ad < re) {
+                            const uint32_t bits = load_elem<DT>(ad);
+                            if constexpr (E == 4) {
+                                w[i2] = bits;
+                            } else {
+                                w[i2 >> 1] |= bits << (16 * (i2 & 1));
+                            }
+                        }
+                    }
+                    in = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                out = chunk_scaled<DT>(in, s, bias);
+            }
+            const uintptr_t gq = gbase + 16 * (uintptr_t)q;
+            const uint32_t w[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+            for (int i2 = 0; i2 < V; ++i2) {
+                const uintptr_t ad = cb + (uintptr_t)i2 * E;
+                if (ad >= rs && ad < re) {
+                    if constexpr (E == 4) {
+                        store_elem<DT>(gq + (uintptr_t)i2 * E, w[i2]);
+                    } else {
+                        store_elem<DT>(gq + (uintptr_t)i2 * E, (i2 & 1) ? (w[i2 >> 1] >> 16) : (w[i2 >> 1] & 0xffffu));
+                    }
+                }
+            }
+        }
+        // 4. each class sum rewrites its element: scale * exp(lp) + (-scale * P),
+        // rounded once (after the barrier, so it lands after the dense store)
+        if (n_ent > 0) {
+            team_bar(team);
+            for (int r = tt; r < n_ent; r += kTeamThreads) {
+                const int c = ent_cls[r];
+                const float v = ent_val[r];
+                const uintptr_t ad = rs + (uintptr_t)c * E;
+                const uint32_t bits = ad + E <= lp_end16 ? (E == 4 ? *reinterpret_cast<const uint32_t*>(sl + (ad - base))
+                                                                   : (uint32_t)*reinterpret_cast<const unsigned short*>(sl + (ad - base)))
+                                                         : load_elem<DT>(ad);
+                const float g = fmaf(s, fast_ex2(fmaf(bits_to_float<DT>(bits), kLog2e, bias)), v);
+                store_elem<DT>(gbase + (ad - base), pack1<DT>(g));
+            }
+        }
+        team_bar(team);  // the slot is free again
+        if (tt == 0) mbar_arrive(&empty[cur]);
+    }
+}
+
+template __global__ void stream_kernel<0>(StreamArgs);
+template __global__ void stream_kernel<1>(StreamArgs);
+template __global__ void stream_kernel<2>(StreamArgs);
+
+// Shared-memory plan of one team with `nslots` slots; returns its bytes.
+static int plan_team(StreamArgs& a, int nslots) {
+    const int E = a.elem_bytes;
+    const size_t lp_cap = align_up((size_t)a.D * E + 32, 16);
+    const size_t sr_cap = align_up(4 * (size_t)a.L.owo + 8 * (size_t)(a.L.max_U + 1), 16);
+    const size_t lb_cap = 16 * (size_t)a.L.max_U;
+    const size_t slot = lp_cap + 2 * sr_cap + lb_cap;
+    const int ecap = a.L.ecap;
+    const int ulen = a.L.max_U + 1;
+    size_t o = 0;
+    a.desc_off = (int)o;  o = align_up(o + sizeof(SlotDesc) * nslots, 16);
+    a.mbar_off = (int)o;  o = align_up(o + 16 * (size_t)nslots, 16);
+    a.slots_off = (int)o; o = align_up(o + slot * nslots, 16);
+    a.ecls_off = (int)o;  o = align_up(o + 4 * (size_t)ecap, 16);
+    a.eval_off = (int)o;  o = align_up(o + 4 * (size_t)ecap, 16);
+    a.labm_off = (int)o;  o = align_up(o + 4 * (size_t)ulen, 16);
+    a.labe_off = (int)o;  o = align_up(o + 4 * (size_t)ulen, 16);
+    a.blkm_off = (int)o;  o = align_up(o + 4 * (size_t)ulen, 16);
+    a.blke_off = (int)o;  o = align_up(o + 4 * (size_t)ulen, 16);
+    a.red_off = (int)o;   o = align_up(o + 4 * (4 * kTeamWarps), 16);
+    a.lp_cap = (int)lp_cap;
+    a.sr_cap = (int)sr_cap;
+    a.slot_bytes = (int)slot;
+    a.nslots = nslots;
+    return (int)align_up(o, 128);
+}
+
+bool stream_plan(StreamArgs& a) {
+    constexpr int kBudget = 220 * 1024;
+    int best_t = 0, best_s = 0, best_rows = -1;
+    for (int nt = kMaxTeams; nt >= 1; --nt) {
+        for (int ns = 3; ns >= 2; --ns) {
+            const int tb = plan_team(a, ns);
+            if ((long long)tb * nt > kBudget) continue;
+            const int rows = nt * ns;  // slots per SM (all but the ones being worked on are in flight)
+            if (rows > best_rows) {
+                best_rows = rows;
+                best_t = nt;
+                best_s = ns;
+            }
+        }
+    }
+    if (best_rows < 0) return false;
+    a.team_bytes = plan_team(a, best_s);
+    a.nteams = best_t;
+    return true;
+}
+
+template <int DT>
+static cudaError_t launch_stream_t(const StreamArgs& a, cudaStream_t s) {
+    const size_t smem = (size_t)a.team_bytes * a.nteams;
+    cudaError_t e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    return launch_pdl(stream_kernel<DT>, dim3((unsigned)sms), dim3((32 + kTeamThreads) * a.nteams), smem, s, a);
+}
+
+cudaError_t launch_stream(const StreamArgs& a, int dtype, cudaStream_t s) {
+    if (a.L.T_total == 0) return cudaSuccess;
+    if (dtype == 0) return launch_stream_t<0>(a, s);
+    if (dtype == 1) return launch_stream_t<1>(a, s);
+    if (dtype == 2) return launch_stream_t<2>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ctcp

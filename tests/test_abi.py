@@ -54,10 +54,10 @@ def test_header_compiles_as_plain_c(tmp_path):
 def test_workspace_size(lib):
     f = lib.ctc_packed_workspace_size
     n = f(38400, 64, 200, 8193, 1)
-    # two state-row buffers of T_total x pitch ints, the emission matrix
-    # (T_total x 201 entries of 16 bytes) and the backward's class sums
-    # (T_total x 201 entries of 8 bytes) dominate
-    big = 2 * 38400 * 404 * 4 + 38400 * 201 * 16 + 38400 * 201 * 8
+    # two state-row buffers of T_total rows (12 offset ints + 404 state ints),
+    # the emission matrix (T_total x 201 entries of 16 bytes) and the
+    # backward's class sums (T_total x 201 entries of 8 bytes) dominate
+    big = 2 * 38400 * (12 + 404) * 4 + 38400 * 201 * 16 + 38400 * 201 * 8
     assert big <= n < big + 4 * 2**20
     assert f(0, 0, 0, 1, 0) > 0
     assert f(-1, 1, 1, 4, 0) == 0
