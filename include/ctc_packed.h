@@ -179,6 +179,29 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
                                       void* grad_log_probs, cudaStream_t stream);
 
 /*
+ * Forward and backward in one call, for callers that have the upstream
+ * gradient `grad_loss` at hand when they ask for the loss (a training step
+ * that reduces the loss and calls backward right away).  Page "feat(asr):
+ * native CTC loss kernel over sequence-packed log probabilities",
+ * ctc_loss.py ``_PackedCTCLoss``: its forward and backward run one after the
+ * other; here one call enqueues both.
+ *
+ * Arguments are those of ctc_packed_forward and ctc_packed_backward
+ * together; `flags` is 0 or CTC_PACKED_FLAG_LOGITS.  `loss` gets what
+ * ctc_packed_forward writes and `grad_log_probs` what ctc_packed_backward
+ * writes with the same inputs and grad_loss, bit for bit.  The workspace is
+ * left as after ctc_packed_forward, so ctc_packed_backward may follow with
+ * another grad_loss.
+ */
+ctc_packed_status ctc_packed_forward_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total,
+                                              int32_t D, const int32_t* cu_seqlens, const int32_t* lengths,
+                                              const int32_t* targets, const int32_t* target_lengths, int32_t B,
+                                              int32_t max_target_len, int32_t blank, int zero_infinity,
+                                              ctc_packed_reduction reduction, const float* grad_loss, float* loss,
+                                              void* grad_log_probs, void* workspace, size_t workspace_bytes,
+                                              unsigned flags, cudaStream_t stream);
+
+/*
  * Copies the device status word of `workspace` (an OR of CTC_PACKED_DEV_*
  * bits, 0 when every utterance was well formed) into *device_status after
  * the work queued on `stream` so far has finished.  This call synchronises

@@ -27,6 +27,7 @@ __all__ = [
     "DTYPE_CODES", "REDUCTION_CODES", "DEVICE_STATUS_BITS", "CTCPackedError",
     "ctc_packed_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "FLAG_LOSS_ONLY", "FLAG_LOGITS",
     "ctc_packed_fsa_workspace_size", "ctc_packed_fsa_forward", "ctc_packed_fsa_backward",
+    "ctc_packed_forward_backward",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +75,9 @@ def load_library(path: Optional[str] = None):
     lib.ctc_packed_backward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int,
                                         ctypes.c_int, vp, vp, sz, vp, vp]
     lib.ctc_packed_backward.restype = ctypes.c_int
+    lib.ctc_packed_forward_backward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32,
+                                                ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, sz, u32, vp]
+    lib.ctc_packed_forward_backward.restype = ctypes.c_int
     lib.ctc_packed_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.ctc_packed_read_status.restype = ctypes.c_int
     lib.ctc_packed_status_string.argtypes = [ctypes.c_int]
@@ -140,6 +144,20 @@ def ctc_packed_backward(log_probs, cu_seqlens, lengths, targets, target_lengths,
         _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
         int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(grad_loss), _ptr(workspace), workspace.numel(),
         _ptr(grad_log_probs), _stream(stream)))
+
+
+def ctc_packed_forward_backward(log_probs, cu_seqlens, lengths, targets, target_lengths, blank: int,
+                                zero_infinity: bool, reduction: str, grad_loss, loss, grad_log_probs, workspace,
+                                max_target_len: int, flags: int = 0, stream=None):
+    """Enqueue forward and backward in one call (bitwise equal to
+    ctc_packed_forward followed by ctc_packed_backward)."""
+    T_total, D = log_probs.shape
+    B = lengths.numel()
+    _check(load_library().ctc_packed_forward_backward(
+        _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
+        _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
+        int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(grad_loss), _ptr(loss), _ptr(grad_log_probs),
+        _ptr(workspace), workspace.numel(), flags, _stream(stream)))
 
 
 def ctc_packed_forward_noalloc(log_probs, cu_seqlens, lengths, targets, target_lengths, blank: int,

@@ -59,7 +59,7 @@ int stream_override() {
 // (unaligned buffers, or one team's slots do not fit shared memory).
 bool plan_stream(StreamArgs& sa, const Layout& L, const void* lp, void* grad, ctc_packed_dtype dtype, int32_t D,
                  const int32_t* cu, const int32_t* targets, const float* grad_loss, int32_t blank, int reduction, int zero_infinity,
-                 void* workspace, bool fused) {
+                 void* workspace) {
     const uintptr_t l0 = reinterpret_cast<uintptr_t>(lp), g0 = reinterpret_cast<uintptr_t>(grad);
     if ((l0 & 15u) != 0 || (g0 & 15u) != 0) return false;
     sa = StreamArgs{};
@@ -75,38 +75,19 @@ bool plan_stream(StreamArgs& sa, const Layout& L, const void* lp, void* grad, ct
     sa.reduction = reduction;
     sa.zero_infinity = zero_infinity ? 1 : 0;
     sa.elem_bytes = elem_bytes(dtype);
-    sa.fused = fused ? 1 : 0;
     sa.gp_mul = grad_group_multiplier(L);
     if (sa.gp_mul == 0) return false;
     return stream_plan(sa);
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
-                                 ctc_packed_dtype dtype) {
-    if (!valid_dtype(dtype) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return 0;
-    if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return 0;
-    return make_layout(T_total, B, max_target_len, D).total;
-}
-
-ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
-                                     const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
-                                     const int32_t* target_lengths, int32_t B, int32_t max_target_len,
-                                     int32_t blank, int zero_infinity, ctc_packed_reduction reduction, float* loss,
-                                     void* workspace, size_t workspace_bytes, unsigned flags, cudaStream_t stream) {
-    ctc_packed_status st = check_common(log_probs, dtype, T_total, D, cu_seqlens, lengths, target_lengths, B,
-                                        max_target_len, blank, reduction, workspace, workspace_bytes);
-    if (st != CTC_PACKED_OK) return st;
-    if (loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if ((flags & ~(CTC_PACKED_FLAG_LOSS_ONLY | CTC_PACKED_FLAG_LOGITS)) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    const bool logits = (flags & CTC_PACKED_FLAG_LOGITS) != 0;
+// The forward's kernels: prep, the logits' row log-sum-exp (logits input),
+// the emission gather with the label analysis, the chains.
+ctc_packed_status enqueue_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                  const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                  const int32_t* target_lengths, int32_t B, int32_t max_target_len, int32_t blank,
+                                  int zero_infinity, int reduction, float* loss, void* workspace, bool need_grad,
+                                  bool logits, cudaStream_t stream) {
     const Layout L = make_layout(T_total, B, max_target_len, D);
-    const bool need_grad = (flags & CTC_PACKED_FLAG_LOSS_ONLY) == 0;
-
     PrepArgs pa{};
     pa.L = L;
     pa.ws = workspace;
@@ -145,6 +126,48 @@ ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dty
     return CTC_PACKED_OK;
 }
 
+// Checks of the gradient arguments (backward and forward-backward calls).
+ctc_packed_status check_grad_args(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D, int32_t B,
+                                  int32_t max_target_len, const int32_t* targets, const float* grad_loss,
+                                  const void* grad_log_probs) {
+    if (grad_log_probs == nullptr || (B > 0 && grad_loss == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const int eb = elem_bytes(dtype);
+    if (reinterpret_cast<uintptr_t>(grad_log_probs) % eb != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(grad_log_probs), l0 = reinterpret_cast<uintptr_t>(log_probs);
+    const uintptr_t nbytes = (uintptr_t)(T_total * (int64_t)D * eb);
+    if (g0 < l0 + nbytes && l0 < g0 + nbytes) return CTC_PACKED_ERR_INVALID_ARGUMENT;  // overlap
+    return CTC_PACKED_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
+                                 ctc_packed_dtype dtype) {
+    if (!valid_dtype(dtype) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return 0;
+    if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return 0;
+    return make_layout(T_total, B, max_target_len, D).total;
+}
+
+ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
+                                     const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                     const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                     int32_t blank, int zero_infinity, ctc_packed_reduction reduction, float* loss,
+                                     void* workspace, size_t workspace_bytes, unsigned flags, cudaStream_t stream) {
+    ctc_packed_status st = check_common(log_probs, dtype, T_total, D, cu_seqlens, lengths, target_lengths, B,
+                                        max_target_len, blank, reduction, workspace, workspace_bytes);
+    if (st != CTC_PACKED_OK) return st;
+    if (loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if ((flags & ~(CTC_PACKED_FLAG_LOSS_ONLY | CTC_PACKED_FLAG_LOGITS)) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const bool logits = (flags & CTC_PACKED_FLAG_LOGITS) != 0;
+    const bool need_grad = (flags & CTC_PACKED_FLAG_LOSS_ONLY) == 0;
+    return enqueue_forward(log_probs, dtype, T_total, D, cu_seqlens, lengths, targets, target_lengths, B,
+                           max_target_len, blank, zero_infinity, reduction, loss, workspace, need_grad, logits, stream);
+}
+
 ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
                                       const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
                                       const int32_t* target_lengths, int32_t B, int32_t max_target_len,
@@ -155,13 +178,10 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
                                         max_target_len, blank, reduction, workspace, workspace_bytes);
     if (st != CTC_PACKED_OK) return st;
     if (T_total == 0) return CTC_PACKED_OK;
-    if (grad_log_probs == nullptr || (B > 0 && grad_loss == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    st = check_grad_args(log_probs, dtype, T_total, D, B, max_target_len, targets, grad_loss, grad_log_probs);
+    if (st != CTC_PACKED_OK) return st;
     const int eb = elem_bytes(dtype);
-    if (reinterpret_cast<uintptr_t>(grad_log_probs) % eb != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     const uintptr_t g0 = reinterpret_cast<uintptr_t>(grad_log_probs), l0 = reinterpret_cast<uintptr_t>(log_probs);
-    const uintptr_t nbytes = (uintptr_t)(T_total * (int64_t)D * eb);
-    if (g0 < l0 + nbytes && l0 < g0 + nbytes) return CTC_PACKED_ERR_INVALID_ARGUMENT;  // overlap
 
     GradArgs ga{};
     ga.L = make_layout(T_total, B, max_target_len, D);
@@ -189,7 +209,7 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
     if (ov != 0 && (ov == 1 || (long long)D * eb >= kStreamMinRowBytes)) {
         StreamArgs sa;
         if (plan_stream(sa, ga.L, log_probs, grad_log_probs, dtype, D, cu_seqlens, targets, grad_loss, blank, reduction,
-                        zero_infinity, workspace, false)) {
+                        zero_infinity, workspace)) {
             if (launch_stream(sa, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
             return CTC_PACKED_OK;
         }
@@ -197,6 +217,34 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
     if (launch_post(ga, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     if (launch_grad(ga, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     return CTC_PACKED_OK;
+}
+
+ctc_packed_status ctc_packed_forward_backward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total,
+                                              int32_t D, const int32_t* cu_seqlens, const int32_t* lengths,
+                                              const int32_t* targets, const int32_t* target_lengths, int32_t B,
+                                              int32_t max_target_len, int32_t blank, int zero_infinity,
+                                              ctc_packed_reduction reduction, const float* grad_loss, float* loss,
+                                              void* grad_log_probs, void* workspace, size_t workspace_bytes,
+                                              unsigned flags, cudaStream_t stream) {
+    ctc_packed_status st = check_common(log_probs, dtype, T_total, D, cu_seqlens, lengths, target_lengths, B,
+                                        max_target_len, blank, reduction, workspace, workspace_bytes);
+    if (st != CTC_PACKED_OK) return st;
+    if (loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if ((flags & ~CTC_PACKED_FLAG_LOGITS) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (T_total > 0) {
+        st = check_grad_args(log_probs, dtype, T_total, D, B, max_target_len, targets, grad_loss, grad_log_probs);
+        if (st != CTC_PACKED_OK) return st;
+    } else if (B > 0 && max_target_len > 0 && targets == nullptr) {
+        return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    }
+    // the forward's kernels, then the backward's, back to back on the stream
+    st = enqueue_forward(log_probs, dtype, T_total, D, cu_seqlens, lengths, targets, target_lengths, B, max_target_len,
+                         blank, zero_infinity, reduction, loss, workspace, true, (flags & CTC_PACKED_FLAG_LOGITS) != 0,
+                         stream);
+    if (st != CTC_PACKED_OK) return st;
+    return ctc_packed_backward(log_probs, dtype, T_total, D, cu_seqlens, lengths, targets, target_lengths, B,
+                               max_target_len, blank, zero_infinity, reduction, grad_loss, workspace, workspace_bytes,
+                               grad_log_probs, stream);
 }
 
 ctc_packed_status ctc_packed_read_status(const void* workspace, uint32_t* device_status, cudaStream_t stream) {

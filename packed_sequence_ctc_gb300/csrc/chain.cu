@@ -452,57 +452,6 @@ __device__ __forceinline__ void run_item(const ChainArgs& a, int item, const Ite
     }
 }
 
-// Label metadata the backward needs, one warp per utterance: for each target
-// position whether it is the first occurrence of its class (then it owns the
-// class's posterior sum), the next position with the same class, and whether
-// the id equals the blank (then its posterior joins the blank column).
-__device__ void run_label_item(const ChainArgs& a, int b, int lane) {
-    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
-    UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
-    const UttInfo info = utt[b];
-    const int U = info.U;
-    const int32_t* tg = a.targets + info.toff;
-    LabelRec* lbl = ws_at<LabelRec>(a.ws, a.L.off_lbl) + info.moff;
-    bool bad = false;
-    int running = 0;
-    for (int j0 = 0; j0 < U; j0 += 32) {
-        const int j = j0 + lane;
-        bool first = false, is_blank = false;
-        int nx = -1, c = 0;
-        if (j < U) {
-            c = tg[j];
-            if (c < 0 || c >= a.D) bad = true;
-            is_blank = c == a.blank;
-            if (!is_blank) {
-                first = true;
-                for (int k = j - 1; k >= 0; --k)
-                    if (tg[k] == c) {
-                        first = false;
-                        break;
-                    }
-                for (int k = j + 1; k < U; ++k)
-                    if (tg[k] == c) {
-                        nx = k;
-                        break;
-                    }
-            }
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, first);
-        const int r = running + __popc(m & ((1u << lane) - 1u));
-        if (j < U) {
-            lbl[j] = LabelRec{first ? r : (is_blank ? -2 : -1), nx, c, 0};
-        }
-        running += __popc(m);
-    }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-        utt[b].n_owners = running + 1;
-        utt[b].labels_ok = bad ? 0 : 1;
-        if (bad) set_status(ctrl, CTC_PACKED_DEV_LABEL_OUT_OF_RANGE);
-    }
-}
-
-
 }  // namespace
 
 // MAXT: the most threads a CTA launches with.  An item of up to 8 warps runs
@@ -529,7 +478,7 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
     XP* my_ring = rings + warp * S::R * 32 * S::LW;
     // stages after the 2 * NW fin values, on a 16-byte boundary
     int* my_stage = reinterpret_cast<int*>(fins + 2 * NW) + warp * S::kStageInts;
-    const int n_big = ctrl->n_big, n_small = ctrl->n_small, n_lab = ctrl->n_lab;
+    const int n_big = ctrl->n_big, n_small = ctrl->n_small;
 
     // 1. multi-warp chains, longest first, one at a time per CTA
     for (;;) {
@@ -551,15 +500,7 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
         if (k >= n_small) break;
         run_item<P>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp, my_stage});
     }
-    // 3. label metadata for the backward
-    for (;;) {
-        int k = 0;
-        if (lane == 0) k = (int)atomicAdd(&ctrl->lab_head, 1u);
-        k = __shfl_sync(0xffffffffu, k, 0);
-        if (k >= n_lab) break;
-        run_label_item(a, queue[2 * a.L.B + 1 + k], lane);
-    }
-
+    // 3. (the label analysis of the backward runs in the emission gather's kernel)
     // 4. the last CTA to finish reduces the losses (fixed order: deterministic)
     __syncthreads();
     if (tid == 0) {

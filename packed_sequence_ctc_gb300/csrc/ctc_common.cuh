@@ -29,16 +29,12 @@ struct Control {
     uint32_t status;      // OR of CTC_PACKED_DEV_* bits
     uint32_t big_head;    // next multi-warp chain item
     uint32_t small_head;  // next single-warp chain item
-    uint32_t lab_head;    // next label-analysis item
     uint32_t done_ctas;   // CTAs of the chain kernel that have finished
     uint32_t grad_ready;  // 1 once a forward has stored what the backward needs
     int32_t n_big, n_small, n_lab;
     uint32_t logits;      // 1: the forward took logits, normalised each row, and kept its log-sum-exp
     int32_t tl_total;     // sum of the target lengths (negative ones as 0): mean_volume's divisor
-    uint32_t gap_head;    // gradient stream: next uncovered row (index into the gap list) to zero
-    uint32_t stream_done; // gradient stream: CTAs that have finished
-    uint32_t chain_live;  // forward-backward call: the chain kernel has started (its inputs are visible)
-    uint32_t pad[2];
+    uint32_t pad[6];
 };
 static_assert(sizeof(Control) == 64, "control block is 64 bytes");
 
@@ -90,9 +86,6 @@ struct Layout {
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_alpha, off_beta;
     size_t off_lbl, off_em, off_head, off_ent, off_lse;
-    size_t off_claim;            // gradient stream: rows of each utterance handed out so far (B ints)
-    size_t off_prog;             // rows each chain has stored: [2b] alpha from the first frame, [2b+1] beta from the last
-    size_t off_gap;              // uncovered row ranges: first row of gap g (B + 2 ints), then the prefix of their lengths (B + 3 ints)
     size_t total;
 };
 
@@ -150,9 +143,6 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
     L.off_ent = o;    o = align_up(o + 8 * (size_t)T_total * (size_t)L.ecap, 256);
     L.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)T_total, 256);
-    L.off_claim = o;  o = align_up(o + sizeof(int32_t) * (size_t)B, 256);
-    L.off_prog = o;   o = align_up(o + sizeof(int32_t) * 2 * (size_t)B, 256);
-    L.off_gap = o;    o = align_up(o + sizeof(int32_t) * (2 * (size_t)B + 5), 256);
     L.total = o;
     return L;
 }

@@ -70,9 +70,8 @@ struct StreamArgs {
     int reduction;
     int zero_infinity;
     int elem_bytes;
-    int fused;          // forward-backward call: rows are claimed as the chains publish them
     uint32_t gp_mul;    // offset group of pair j: (j * gp_mul) >> 21 == j / L.gpairs
-    int nteams, nslots; // teams of four warps per CTA, shared-memory slots per team
+    int nteams, nslots; // teams (a producer warp and four worker warps) per CTA, shared-memory slots per team
     int team_bytes;     // shared memory of one team
     int lp_cap, sr_cap, slot_bytes;  // a slot: lp span, stored alpha row, stored beta row, label records
     int desc_off, mbar_off, slots_off, ecls_off, eval_off, labm_off, labe_off, blkm_off, blke_off, red_off;

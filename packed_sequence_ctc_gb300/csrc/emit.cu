@@ -62,6 +62,69 @@ __device__ __forceinline__ float load_lp(const void* lp, int64_t idx) {
     }
 }
 
+// Label records the backward needs, one CTA per utterance: for each target
+// position whether it is the first occurrence of its class (then it owns the
+// class's posterior sum and gets the next rank), the next position with the
+// same class, and whether the id equals the blank (then its posterior joins
+// the blank column).  Every position compares its class with all others,
+// which pass through shared memory one tile at a time.
+__device__ void run_label_block(const ChainArgs& a, int b) {
+    __shared__ int s_tile[kEmitThreads];
+    __shared__ int s_warp[kEmitThreads / 32];
+    __shared__ int s_bad;
+    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
+    const UttInfo info = utt[b];
+    const int U = info.U;
+    const int32_t* tg = a.targets + info.toff;
+    LabelRec* lbl = ws_at<LabelRec>(a.ws, a.L.off_lbl) + info.moff;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    int running = 0;  // distinct classes ranked so far
+    for (int j0 = 0; j0 < U; j0 += kEmitThreads) {
+        const int j = j0 + tid;
+        const int c = j < U ? tg[j] : -1;
+        const bool is_blank = c == a.blank;
+        bool first = j < U && !is_blank;
+        int nx = -1;
+        if (j < U && (c < 0 || c >= a.D)) s_bad = 1;
+        for (int k0 = 0; k0 < U; k0 += kEmitThreads) {
+            __syncthreads();
+            s_tile[tid] = k0 + tid < U ? tg[k0 + tid] : -1;
+            __syncthreads();
+            const int n = min(kEmitThreads, U - k0);
+            if (j < U && !is_blank) {
+                for (int kk = 0; kk < n; ++kk) {
+                    if (s_tile[kk] == c) {
+                        const int k = k0 + kk;
+                        if (k < j) first = false;
+                        if (k > j && nx < 0) nx = k;
+                    }
+                }
+            }
+        }
+        // ranks of the first occurrences, in target order
+        const unsigned m = __ballot_sync(0xffffffffu, first);
+        if (lane == 0) s_warp[warp] = __popc(m);
+        __syncthreads();
+        int before = running;
+        for (int w = 0; w < warp; ++w) before += s_warp[w];
+        int total = 0;
+        for (int w = 0; w < kEmitThreads / 32; ++w) total += s_warp[w];
+        const int r = before + __popc(m & ((1u << lane) - 1u));
+        if (j < U) lbl[j] = LabelRec{first ? r : (is_blank ? -2 : -1), nx, c, 0};
+        running += total;
+        __syncthreads();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        utt[b].n_owners = running + 1;
+        utt[b].labels_ok = s_bad ? 0 : 1;
+        if (s_bad) set_status(ctrl, CTC_PACKED_DEV_LABEL_OUT_OF_RANGE);
+    }
+}
+
 }  // namespace
 
 template <int DT>
@@ -75,6 +138,16 @@ __global__ void __launch_bounds__(kEmitThreads) emit_kernel(ChainArgs a) {
     const int64_t r0 = (int64_t)blockIdx.x * kEmitRows;
     const int tid = threadIdx.x;
     pdl_wait();  // utterance metadata from the prep kernel
+    // the blocks after the gather's are the label analysis of the backward,
+    // one per utterance with frames (before the chains, so that the gradient
+    // stream of the forward-backward call can use it while they run)
+    const int64_t n_gather = (a.L.T_total + kEmitRows - 1) / kEmitRows;
+    if ((int64_t)blockIdx.x >= n_gather) {
+        const Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+        const int k = (int)((int64_t)blockIdx.x - n_gather);
+        if (k < ctrl->n_lab) run_label_block(a, ws_at<int32_t>(a.ws, a.L.off_queue)[2 * a.L.B + 1 + k]);
+        return;
+    }
     if (tid == 0) s_maxw = 0;
     __syncthreads();
     if (tid < kEmitRows) {
@@ -144,7 +217,8 @@ template __global__ void emit_kernel<2>(ChainArgs);
 
 cudaError_t launch_emit(const ChainArgs& a, int dtype, cudaStream_t s) {
     if (a.L.T_total == 0 || a.L.B == 0) return cudaSuccess;
-    const int64_t grid = (a.L.T_total + kEmitRows - 1) / kEmitRows;
+    // gather blocks, then one label block per utterance
+    const int64_t grid = (a.L.T_total + kEmitRows - 1) / kEmitRows + a.L.B;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     if (dtype == 0) return launch_pdl(emit_kernel<0>, dim3((unsigned)grid), dim3(kEmitThreads), 0, s, a);
     if (dtype == 1) return launch_pdl(emit_kernel<1>, dim3((unsigned)grid), dim3(kEmitThreads), 0, s, a);

@@ -63,39 +63,18 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
         ctrl->status = 0;
         ctrl->big_head = 0;
         ctrl->small_head = 0;
-        ctrl->lab_head = 0;
         ctrl->done_ctas = 0;
         ctrl->grad_ready = a.need_grad ? 1u : 0u;
         ctrl->logits = a.logits ? 1u : 0u;
-        ctrl->gap_head = 0;
-        ctrl->stream_done = 0;
-        ctrl->chain_live = 0;
-    }
-    int32_t* claim = ws_at<int32_t>(a.ws, a.L.off_claim);
-    int32_t* prog = ws_at<int32_t>(a.ws, a.L.off_prog);
-    int32_t* gap_lo = ws_at<int32_t>(a.ws, a.L.off_gap);
-    int32_t* gap_pre = gap_lo + (B + 2);
-    for (int i = tid; i < B; i += nt) {
-        claim[i] = 0;
-        prog[2 * i] = 0;
-        prog[2 * i + 1] = 0;
     }
 
     // 1. validate, and scan the target offsets (raw lengths) and the
     //    label-metadata offsets (valid lengths plus one blank slot each)
     uint32_t bad_bits = 0;
-    int toff_base = 0, moff_base = 0, gap_base = 0;
-    // gap 0: rows before the first utterance's span
-    const int cu0 = B > 0 ? a.cu[0] : (int)a.L.T_total;
-    const int lead_gap = min(max(cu0, 0), (int)a.L.T_total);
-    if (tid == 0) {
-        gap_lo[0] = 0;
-        gap_pre[0] = 0;
-        gap_pre[1] = lead_gap;
-    }
+    int toff_base = 0, moff_base = 0;
     for (int base = 0; base < B; base += nt) {
         const int b = base + tid;
-        int T = 0, U = 0, start = 0, valid = 0, uraw = 0, glen = 0;
+        int T = 0, U = 0, start = 0, valid = 0, uraw = 0;
         if (b < B) {
             const int c0 = a.cu[b], c1 = a.cu[b + 1];
             T = a.lengths[b];
@@ -109,17 +88,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
             valid = bits == 0;
             start = c0;
             U = valid ? uraw : 0;
-            // gap b + 1: the rows of b's span past its frames (all of it when b is malformed);
-            // meaningful only when every span is well formed (no BAD_CU_SEQLENS bit)
-            const int covered_end = valid ? c0 + T : c0;
-            glen = max(c1 - covered_end, 0);
-            gap_lo[b + 1] = covered_end;
         }
-        int total_t, total_m, total_g;
+        int total_t, total_m;
         const int toff = toff_base + block_exclusive_scan(b < B ? max(uraw, 0) : 0, s_warp, &total_t);
         const int moff = moff_base + block_exclusive_scan(b < B ? U + 1 : 0, s_warp, &total_m);
-        const int gpre = gap_base + block_exclusive_scan(glen, s_warp, &total_g);
-        if (b < B) gap_pre[b + 2] = lead_gap + gpre + glen;
         if (b < B) {
             UttInfo info;
             info.start = start;
@@ -150,16 +122,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
         }
         toff_base += total_t;
         moff_base += total_m;
-        gap_base += total_g;
     }
     if (bad_bits) atomicOr(&ctrl->status, bad_bits);
-    if (tid == 0) {
-        ctrl->tl_total = toff_base;
-        // gap B + 1: rows after the last span
-        const int cuB = B > 0 ? min(max(a.cu[B], 0), (int)a.L.T_total) : lead_gap;
-        gap_lo[B + 1] = cuB;
-        gap_pre[B + 2] = lead_gap + gap_base + ((int)a.L.T_total - cuB);
-    }
+    if (tid == 0) ctrl->tl_total = toff_base;
     __syncthreads();
 
     // 2. order the utterances longest first (the serial chain of the longest

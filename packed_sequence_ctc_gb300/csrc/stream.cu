@@ -32,12 +32,9 @@
 //      into the row's dtype and stored as one 16-byte vector (the ragged
 //      chunks at the ends element by element).
 //
-// Work is handed out per utterance: a team scans the utterances for one with
-// rows left and claims its next row with an atomic counter.  In the
-// forward-backward call the rows of an utterance are handed out from its
-// middle outwards, the order in which both chains reach them, and a row is
-// only claimed once the chains have published that they stored it.  Rows
-// outside every utterance come last, from a list the prep kernel made.
+// Work: team g of the G teams of the grid takes rows g, g + G, ...; its
+// producer finds each row's utterance by walking cu_seqlens forward (rows
+// only grow) and writes rows outside every utterance as zero rows.
 #include "ctc_common.cuh"
 #include "ctc_kernels.h"
 
@@ -83,11 +80,6 @@ __device__ __forceinline__ bool team_bar_or(int team, bool v) {
         : "memory");
     return r != 0;
 }
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
 
 // Waits (bounded) until the slot's copies have landed.  False: gave up.
@@ -102,16 +94,6 @@ __device__ __forceinline__ bool wait_slot(uint64_t* bar, uint32_t parity) {
         }
         if (globaltimer() - t0 > kWaitNs) return false;
     }
-}
-
-// Row of utterance frame order k when rows are handed out from the middle
-// outwards: m, m - 1, m + 1, m - 2, ... (m = T / 2).
-__device__ __forceinline__ int middle_out(int k, int T) {
-    const int m = T >> 1;
-    const int i = k >> 1;
-    if ((k & 1) == 0) return m + i;
-    if (i < m) return m - 1 - i;
-    return m + i;  // unreachable for k < T
 }
 
 // Exponent of a zero product (below every real one).
@@ -165,22 +147,10 @@ __device__ __forceinline__ SlotDesc describe_row(const StreamArgs& a, int row, i
     return d;
 }
 
-// Rows [lo, hi] that frames k0 .. k1 - 1 of the middle-out order cover.
-__device__ __forceinline__ void middle_out_span(int k0, int k1, int T, int& lo, int& hi) {
-    const int a = middle_out(k1 - 1, T);
-    const int b = k1 - 2 >= k0 ? middle_out(k1 - 2, T) : a;
-    lo = min(a, b);
-    hi = max(a, b);
-    const int f = middle_out(k0, T);  // k0 alone: the middle row
-    lo = min(lo, f);
-    hi = max(hi, f);
-}
-
 template <int DT>
 __global__ void __launch_bounds__((32 + kTeamThreads) * kMaxTeams, 1) stream_kernel(StreamArgs a) {
     constexpr int E = Elem<DT>::bytes;
     constexpr int V = 16 / E;
-    constexpr int kBatch = 4;  // rows the forward-backward call claims at once
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // a team: one producer warp and kTeamWarps worker warps
     const int team = threadIdx.x / (kTeamThreads + 32);
@@ -204,11 +174,6 @@ __global__ void __launch_bounds__((32 + kTeamThreads) * kMaxTeams, 1) stream_ker
 
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const UttInfo* utt = ws_at<UttInfo>(a.ws, a.L.off_utt);
-    const int32_t* queue = ws_at<int32_t>(a.ws, a.L.off_queue);
-    int32_t* claim = ws_at<int32_t>(a.ws, a.L.off_claim);
-    const int32_t* prog = ws_at<int32_t>(a.ws, a.L.off_prog);
-    const int32_t* gap_lo = ws_at<int32_t>(a.ws, a.L.off_gap);
-    const int32_t* gap_pre = gap_lo + (a.L.B + 2);
     const float* lse = ws_at<float>(a.ws, a.L.off_lse);
     const int D = a.D;
     const int64_t T_total = a.L.T_total;
@@ -227,35 +192,15 @@ __global__ void __launch_bounds__((32 + kTeamThreads) * kMaxTeams, 1) stream_ker
         }
     }
     __syncthreads();
-    if (!a.fused) {
-        pdl_wait();  // the forward's stored rows and metadata
-        pdl_trigger();
-    }
+    pdl_wait();  // the forward's stored rows and metadata
+    pdl_trigger();
 
     if (producer) {
         // ------------------------------------------------------------ producer
-        // The forward-backward call starts while the chain kernel runs; what
-        // the prep and emission kernels wrote is visible once the chain kernel
-        // has started (it waited for them) and said so.
         bool failed = false;
-        if (a.fused) {
-            const unsigned long long t0 = globaltimer();
-            int live = 0;
-            if (lane == 0) {
-                while ((live = ld_acquire(reinterpret_cast<const int32_t*>(&ctrl->chain_live))) == 0) {
-                    __nanosleep(256);
-                    if (globaltimer() - t0 > kWaitNs) break;
-                }
-            }
-            live = __shfl_sync(0xffffffffu, live, 0);
-            if (!live) {
-                if (lane == 0) set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
-                failed = true;
-            }
-        }
         const uint32_t status0 = ld_volatile(reinterpret_cast<const int32_t*>(&ctrl->status));
         const bool ready = ctrl->grad_ready != 0;
-        if (!a.fused && blockIdx.x == 0 && lane == 0 && T_total > 0 && !ready)
+        if (blockIdx.x == 0 && team == 0 && lane == 0 && T_total > 0 && !ready)
             set_status(ctrl, CTC_PACKED_DEV_NO_GRAD_STATE);
         // malformed spans or no stored state: every row is written as zero
         const bool all_zero = !ready || (status0 & CTC_PACKED_DEV_BAD_CU_SEQLENS) != 0;
@@ -298,144 +243,36 @@ __global__ void __launch_bounds__((32 + kTeamThreads) * kMaxTeams, 1) stream_ker
             return true;
         };
 
-        if (!a.fused) {
-            // the backward call: team g of G takes rows g, g + G, ... ; each row's
-            // utterance by walking cu_seqlens forward (rows only grow)
-            if (lane == 0 && !failed) {
-                int b = -1;
-                UttInfo u{};
-                const int B = a.L.B;
-                const int32_t* cu = a.cu;
-                const int64_t G = (int64_t)gridDim.x * NT;
-                for (int64_t r = (int64_t)blockIdx.x * NT + team; r < T_total; r += G) {
-                    SlotDesc d;
-                    if (all_zero) {
-                        d = SlotDesc{};
-                        d.kind = kZero;
-                        d.row = (int)r;
-                    } else {
-                        int nb = b;
-                        while (nb + 1 < B && (int64_t)cu[nb + 1] <= r) ++nb;
-                        if (nb != b) {
-                            b = nb;
-                            u = utt[b];
-                        }
-                        d = describe_row(a, (int)r, b, u, logits, inv_count, lse);
+        // the backward call: team g of G takes rows g, g + G, ... ; each row's
+        // utterance by walking cu_seqlens forward (rows only grow)
+        if (lane == 0 && !failed) {
+            int b = -1;
+            UttInfo u{};
+            const int B = a.L.B;
+            const int32_t* cu = a.cu;
+            const int64_t G = (int64_t)gridDim.x * NT;
+            for (int64_t r = (int64_t)blockIdx.x * NT + team; r < T_total; r += G) {
+                SlotDesc d;
+                if (all_zero) {
+                    d = SlotDesc{};
+                    d.kind = kZero;
+                    d.row = (int)r;
+                } else {
+                    int nb = b;
+                    while (nb + 1 < B && (int64_t)cu[nb + 1] <= r) ++nb;
+                    if (nb != b) {
+                        b = nb;
+                        u = utt[b];
                     }
-                    if (!emit(d)) {
-                        failed = true;
-                        break;
-                    }
+                    d = describe_row(a, (int)r, b, u, logits, inv_count, lse);
                 }
-            }
-        } else if (!failed) {
-            // the forward-backward call: each utterance's rows from the middle
-            // outwards, kBatch at a time, once both chains have stored them
-            const int n_utt = all_zero ? 0 : ctrl->n_lab;
-            const int32_t* ulist = queue + 2 * a.L.B + 1;
-            int cursor = n_utt > 0 ? (int)(((int64_t)blockIdx.x * NT + team) % n_utt) : 0;
-            const unsigned long long t0 = globaltimer();
-            while (n_utt > 0) {
-                int found = -1;
-                bool pending = false;
-                for (int base = 0; base < n_utt && found < 0; base += 32) {
-                    const int i = base + lane;
-                    bool avail = false, rdy = false;
-                    if (i < n_utt) {
-                        int idx = cursor + i;
-                        if (idx >= n_utt) idx -= n_utt;
-                        const int b = ulist[idx];
-                        const int T = utt[b].T;
-                        const int kc = ld_volatile(claim + b);
-                        avail = kc < T;
-                        if (avail) {
-                            int lo, hi;
-                            middle_out_span(kc, min(kc + kBatch, T), T, lo, hi);
-                            rdy = ld_volatile(prog + 2 * b) >= hi + 1 && ld_volatile(prog + 2 * b + 1) >= T - lo;
-                        }
-                    }
-                    const unsigned rm = __ballot_sync(0xffffffffu, rdy);
-                    pending = pending || __any_sync(0xffffffffu, avail);
-                    if (rm) found = base + __ffs(rm) - 1;
-                }
-                if (found >= 0) {
-                    int idx = cursor + found;
-                    if (idx >= n_utt) idx -= n_utt;
-                    cursor = idx;
-                    const int b = ulist[idx];
-                    int ok = 1;
-                    if (lane == 0) {
-                        const UttInfo u = utt[b];
-                        const int T = u.T;
-                        const int kc = atomicAdd(claim + b, kBatch);
-                        if (kc < T) {
-                            const int k1 = min(kc + kBatch, T);
-                            int lo, hi;
-                            middle_out_span(kc, k1, T, lo, hi);
-                            // a race may hand out rows past the scan's: wait for the chains
-                            const unsigned long long w0 = globaltimer();
-                            while (!(ld_acquire(prog + 2 * b) >= hi + 1 && ld_acquire(prog + 2 * b + 1) >= T - lo)) {
-                                __nanosleep(128);
-                                if (globaltimer() - w0 > kWaitNs) {
-                                    ok = 0;
-                                    break;
-                                }
-                            }
-                            // the chains' rows are read by bulk copies (the async proxy)
-                            asm volatile("fence.proxy.async.global;" ::: "memory");
-                            for (int j = kc; j < k1 && ok; ++j) {
-                                const int row = u.start + middle_out(j, T);
-                                if (!emit(describe_row(a, row, b, u, logits, inv_count, lse))) ok = 0;
-                            }
-                            if (!ok) set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
-                        }
-                    }
-                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                        failed = true;
-                        break;
-                    }
-                    continue;
-                }
-                if (!pending) break;  // every utterance is handed out
-                __nanosleep(512);     // rows remain but the chains have not reached them yet
-                int late = lane == 0 && globaltimer() - t0 > kWaitNs;
-                if (__shfl_sync(0xffffffffu, late, 0)) {
-                    if (lane == 0) set_status(ctrl, CTC_PACKED_DEV_WAIT_TIMEOUT);
+                if (!emit(d)) {
                     failed = true;
                     break;
                 }
             }
-            // rows outside every utterance (every row, when nothing can be computed)
-            if (lane == 0 && !failed) {
-                const int gap_total = all_zero ? (int)T_total : gap_pre[a.L.B + 2];
-                for (;;) {
-                    const int g0 = (int)atomicAdd(&ctrl->gap_head, 8u);
-                    if (g0 >= gap_total) break;
-                    const int g1 = min(g0 + 8, gap_total);
-                    int gi = 0;
-                    if (!all_zero) {
-                        int lo = 0, hi = a.L.B + 1;  // gap_pre[lo] <= g0 < gap_pre[lo + 1]
-                        while (lo < hi) {
-                            const int mid = (lo + hi + 1) >> 1;
-                            if (gap_pre[mid] <= g0) {
-                                lo = mid;
-                            } else {
-                                hi = mid - 1;
-                            }
-                        }
-                        gi = lo;
-                    }
-                    for (int g = g0; g < g1 && !failed; ++g) {
-                        while (!all_zero && gap_pre[gi + 1] <= g) ++gi;
-                        SlotDesc d{};
-                        d.kind = kZero;
-                        d.row = all_zero ? g : gap_lo[gi] + (g - gap_pre[gi]);
-                        if (!emit(d)) failed = true;
-                    }
-                    if (failed) break;
-                }
-            }
         }
+
         // the end mark
         if (lane == 0) {
             SlotDesc d{};
@@ -659,7 +496,7 @@ static int plan_team(StreamArgs& a, int nslots) {
 }
 
 bool stream_plan(StreamArgs& a) {
-    constexpr int kBudget = 220 * 1024;
+    constexpr int kBudget = 220 * 1024;  // one CTA per SM
     int best_t = 0, best_s = 0, best_rows = -1;
     for (int nt = kMaxTeams; nt >= 1; --nt) {
         for (int ns = 3; ns >= 2; --ns) {

@@ -108,3 +108,34 @@ def run_gpu(batch, grad_loss=None, max_target_len=None, need_grad=True, grad_off
     status = pk.ctc_packed_read_status(ws)
     out = loss.double().cpu().numpy()
     return (out if red == "none" else out[0]), grad, status
+
+
+def run_gpu_fused(batch, grad_loss=None, max_target_len=None, guard_bytes=64, device="cuda", log_probs=None,
+                  logits=False, workspace=None):
+    """Forward and backward in one call (ctc_packed_forward_backward) on the
+    current stream, the gradient inside a sentinel-guarded buffer like
+    run_gpu.  Returns (loss, grad, status, workspace)."""
+    d = to_device(batch, device)
+    lp = d["log_probs"] if log_probs is None else log_probs
+    T_total, D = lp.shape
+    B = batch.B
+    mtl = batch.max_target_len if max_target_len is None else max_target_len
+    ws = pk.Workspace(T_total, B, mtl, D, lp.dtype, device).tensor if workspace is None else workspace
+    red = batch.reduction
+    loss = torch.full((B if red == "none" else 1,), float("nan"), dtype=torch.float32, device=device)
+    if grad_loss is None:
+        grad_loss = torch.ones(B if red == "none" else 1, dtype=torch.float32)
+    g_up = torch.as_tensor(grad_loss, dtype=torch.float32).reshape(-1).to(device)
+    n = T_total * D * lp.element_size()
+    raw = torch.full((n + 2 * guard_bytes + 16,), 0xA5, dtype=torch.uint8, device=device)
+    grad_view = raw[guard_bytes: guard_bytes + n].view(lp.dtype).view(T_total, D)
+    pk.ctc_packed_forward_backward(lp, d["cu"], d["lengths"], d["targets"], d["target_lengths"], batch.blank,
+                                   batch.zero_infinity, red, g_up, loss, grad_view, ws, mtl,
+                                   flags=pk.FLAG_LOGITS if logits else 0)
+    torch.cuda.synchronize()
+    head = raw[:guard_bytes].cpu()
+    tail = raw[guard_bytes + n:].cpu()
+    assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), "gradient write outside its buffer"
+    status = pk.ctc_packed_read_status(ws)
+    out = loss.double().cpu().numpy()
+    return (out if red == "none" else out[0]), grad_view.clone(), status, ws
