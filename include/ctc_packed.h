@@ -137,6 +137,15 @@ size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_
                                  ctc_packed_dtype dtype);
 
 /*
+ * Bytes of workspace a forward with CTC_PACKED_FLAG_LOSS_ONLY needs (the
+ * metadata, the work queue and the emission matrix: no state rows are
+ * stored).  At most ctc_packed_workspace_size.  0 for invalid or
+ * unsupported sizes.
+ */
+size_t ctc_packed_workspace_size_loss_only(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
+                                           ctc_packed_dtype dtype);
+
+/*
  * Forward: per-utterance CTC loss, reduced as asked.
  *
  *   log_probs      (T_total, D) row-major, dtype `dtype`, device; 4-byte aligned.
@@ -148,8 +157,10 @@ size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_
  *   target_lengths (B) int32, each in [0, max_target_len].
  *   blank          class index of the blank, in [0, D).
  *   loss           float32 device output: B entries for NONE, 1 otherwise.
- *   workspace      device buffer of at least ctc_packed_workspace_size bytes;
- *                  pass the same one, unchanged, to ctc_packed_backward.
+ *   workspace      device buffer of at least ctc_packed_workspace_size bytes
+ *                  (ctc_packed_workspace_size_loss_only with
+ *                  CTC_PACKED_FLAG_LOSS_ONLY); pass the same one, unchanged,
+ *                  to ctc_packed_backward.
  *   flags          0, or an OR of CTC_PACKED_FLAG_LOSS_ONLY and
  *                  CTC_PACKED_FLAG_LOGITS; other bits are invalid.
  */
@@ -211,7 +222,7 @@ ctc_packed_status ctc_packed_read_status(const void* workspace, uint32_t* device
 
 /*
  * Bytes of the fixed scratch array behind ctc_packed_forward_noalloc (32 MiB).
- * A batch fits when ctc_packed_workspace_size(...) <= this value.
+ * A batch fits when ctc_packed_workspace_size_loss_only(...) <= this value.
  */
 #define CTC_PACKED_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
@@ -231,17 +242,19 @@ ctc_packed_status ctc_packed_read_status(const void* workspace, uint32_t* device
  * each device, built into the library.  The function calls no allocator
  * (no cudaMalloc or cudaFree, nothing of a framework's).
  *
- *   - Size limit: a batch whose ctc_packed_workspace_size exceeds
+ *   - Size limit: a batch whose ctc_packed_workspace_size_loss_only exceeds
  *     CTC_PACKED_NOALLOC_SCRATCH_BYTES is rejected with
  *     CTC_PACKED_ERR_WORKSPACE before any CUDA call.  Sizes that are invalid
  *     or unsupported return the codes ctc_packed_forward would return.
  *   - Device: the call uses the scratch of the CURRENT device, and `stream`
  *     must belong to it.
- *   - First call on a device: it looks up the scratch's device address once
- *     (cudaGetSymbolAddress), which may load the library's device code on
- *     that device; later calls reuse the address.  Make that first call
- *     before any stream capture starts.  If the look-up fails, the call
- *     returns CTC_PACKED_ERR_CUDA and clears the CUDA error it left.
+ *   - Address look-up: every call asks the runtime for the scratch's device
+ *     address on the current device (cudaGetSymbolAddress; nothing is cached,
+ *     so a device reset leaves no stale address behind).  The first look-up
+ *     on a device may load the library's device code there: make the first
+ *     call on a device before any stream capture starts.  If the look-up
+ *     fails, the call returns CTC_PACKED_ERR_CUDA and clears the CUDA error
+ *     it left.
  *   - Memory: the array holds 32 MiB of device memory on every device where
  *     the library's device code is loaded, at the latest from the first call
  *     on that device.

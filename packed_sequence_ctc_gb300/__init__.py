@@ -27,7 +27,7 @@ __all__ = [
     "DTYPE_CODES", "REDUCTION_CODES", "DEVICE_STATUS_BITS", "CTCPackedError",
     "ctc_packed_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "FLAG_LOSS_ONLY", "FLAG_LOGITS",
     "ctc_packed_fsa_workspace_size", "ctc_packed_fsa_forward", "ctc_packed_fsa_backward",
-    "ctc_packed_forward_backward",
+    "ctc_packed_forward_backward", "ctc_packed_workspace_size_loss_only",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +69,8 @@ def load_library(path: Optional[str] = None):
     vp, i64, i32, sz, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_uint
     lib.ctc_packed_workspace_size.argtypes = [i64, i32, i32, i32, ctypes.c_int]
     lib.ctc_packed_workspace_size.restype = sz
+    lib.ctc_packed_workspace_size_loss_only.argtypes = [i64, i32, i32, i32, ctypes.c_int]
+    lib.ctc_packed_workspace_size_loss_only.restype = sz
     lib.ctc_packed_forward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int,
                                        ctypes.c_int, vp, vp, sz, u32, vp]
     lib.ctc_packed_forward.restype = ctypes.c_int
@@ -122,6 +124,10 @@ def ctc_packed_workspace_size(T_total: int, B: int, max_target_len: int, D: int,
     return int(load_library().ctc_packed_workspace_size(T_total, B, max_target_len, D, DTYPE_CODES[dtype]))
 
 
+def ctc_packed_workspace_size_loss_only(T_total: int, B: int, max_target_len: int, D: int, dtype: torch.dtype) -> int:
+    return int(load_library().ctc_packed_workspace_size_loss_only(T_total, B, max_target_len, D, DTYPE_CODES[dtype]))
+
+
 def ctc_packed_forward(log_probs, cu_seqlens, lengths, targets, target_lengths, blank: int, zero_infinity: bool,
                        reduction: str, loss, workspace, max_target_len: int, flags: int = 0, stream=None):
     """Enqueue the forward on `stream` (default: torch's current stream)."""
@@ -164,13 +170,27 @@ def ctc_packed_forward_noalloc(log_probs, cu_seqlens, lengths, targets, target_l
                                zero_infinity: bool, reduction: str, loss, max_target_len: int, stream=None):
     """Enqueue the loss-only forward that uses the library's own fixed scratch
     (for callers that cannot allocate a workspace; calls overlapping on the
-    GPU race, see the C declaration)."""
+    GPU race, see the C declaration).  The call runs on log_probs' device,
+    whose scratch it uses; every tensor (and `stream`) must be on that
+    device."""
+    if log_probs.dtype not in DTYPE_CODES or log_probs.ndim != 2 or not log_probs.is_contiguous():
+        raise TypeError("log_probs must be a contiguous (T_total, D) float32, bfloat16 or float16 tensor")
+    dev = log_probs.device
+    want = ((cu_seqlens, torch.int32, "cu_seqlens"), (lengths, torch.int32, "lengths"),
+            (targets, torch.int32, "targets"), (target_lengths, torch.int32, "target_lengths"),
+            (loss, torch.float32, "loss"))
+    for t, dt, name in want:
+        if t.dtype != dt or not t.is_contiguous() or t.device != dev:
+            raise TypeError(f"{name} must be a contiguous {dt} tensor on {dev}")
+    if stream is not None and getattr(stream, "device", dev) != dev:
+        raise ValueError(f"stream must belong to {dev}")
     T_total, D = log_probs.shape
     B = lengths.numel()
-    _check(load_library().ctc_packed_forward_noalloc(
-        _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
-        _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
-        int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(loss), _stream(stream)))
+    with torch.cuda.device(dev):
+        _check(load_library().ctc_packed_forward_noalloc(
+            _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
+            _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
+            int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(loss), _stream(stream)))
 
 
 def ctc_packed_fsa_workspace_size(T_total: int, B: int, max_states: int, max_labels: int, D: int) -> int:

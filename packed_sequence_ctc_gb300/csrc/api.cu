@@ -24,7 +24,7 @@ bool valid_reduction(int r) {
 ctc_packed_status check_common(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
                                const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* target_lengths,
                                int32_t B, int32_t max_target_len, int32_t blank, int reduction,
-                               const void* workspace, size_t workspace_bytes) {
+                               const void* workspace, size_t workspace_bytes, bool loss_only = false) {
     if (!valid_dtype(dtype) || !valid_reduction(reduction)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (blank < 0 || blank >= D) return CTC_PACKED_ERR_INVALID_ARGUMENT;
@@ -37,7 +37,7 @@ ctc_packed_status check_common(const void* log_probs, ctc_packed_dtype dtype, in
     if (workspace == nullptr) return CTC_PACKED_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return CTC_PACKED_ERR_WORKSPACE;
     const Layout L = make_layout(T_total, B, max_target_len, D);
-    if (workspace_bytes < L.total) return CTC_PACKED_ERR_WORKSPACE;
+    if (workspace_bytes < (loss_only ? L.loss_only_total : L.total)) return CTC_PACKED_ERR_WORKSPACE;
     return CTC_PACKED_OK;
 }
 
@@ -116,6 +116,7 @@ ctc_packed_status enqueue_forward(const void* log_probs, ctc_packed_dtype dtype,
     ca.reduction = reduction;
     ca.zero_infinity = zero_infinity ? 1 : 0;
     ca.lse = nullptr;
+    ca.store_rows = need_grad ? 1 : 0;
     if (logits) {
         // one dense pass over the logits: each row's log-sum-exp
         if (launch_lse(ca, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
@@ -151,13 +152,21 @@ size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_
     return make_layout(T_total, B, max_target_len, D).total;
 }
 
+size_t ctc_packed_workspace_size_loss_only(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
+                                           ctc_packed_dtype dtype) {
+    if (!valid_dtype(dtype) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return 0;
+    if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return 0;
+    return make_layout(T_total, B, max_target_len, D).loss_only_total;
+}
+
 ctc_packed_status ctc_packed_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
                                      const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
                                      const int32_t* target_lengths, int32_t B, int32_t max_target_len,
                                      int32_t blank, int zero_infinity, ctc_packed_reduction reduction, float* loss,
                                      void* workspace, size_t workspace_bytes, unsigned flags, cudaStream_t stream) {
     ctc_packed_status st = check_common(log_probs, dtype, T_total, D, cu_seqlens, lengths, target_lengths, B,
-                                        max_target_len, blank, reduction, workspace, workspace_bytes);
+                                        max_target_len, blank, reduction, workspace, workspace_bytes,
+                                        (flags & CTC_PACKED_FLAG_LOSS_ONLY) != 0);
     if (st != CTC_PACKED_OK) return st;
     if (loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;

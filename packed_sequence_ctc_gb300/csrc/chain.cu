@@ -371,12 +371,12 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             XP el[P], eb;
             emissions(base + q, el, eb);
             request((base + q + S::R - 1) & (S::R - 1), i0 + q + S::R - 1);
-            flush_row(q);  // frame i0 + q - 1
+            if (a.store_rows) flush_row(q);  // frame i0 + q - 1
             step(el, eb);
         }
         renormalise();
         if (multi) exchange((i0 - 1) / S::F);
-        write_rows(i0 - 1, S::F);
+        if (a.store_rows) write_rows(i0 - 1, S::F);
     }
     // the last frames (fewer than F: no exchange needed)
 #pragma unroll 1
@@ -386,11 +386,13 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         const uint32_t slot = (uint32_t)((i - 1) & (S::R - 1));
         emissions(slot, el, eb);
         request((slot + S::R - 1) & (S::R - 1), i + S::R - 1);
-        flush_row(i - i0);  // frame i - 1
+        if (a.store_rows) flush_row(i - i0);  // frame i - 1
         step(el, eb);
     }
-    flush_row(T - i0);  // frame T - 1 (T >= 1 for every queued item)
-    write_rows(i0 - 1, T - i0 + 1);
+    if (a.store_rows) {
+        flush_row(T - i0);  // frame T - 1 (T >= 1 for every queued item)
+        write_rows(i0 - 1, T - i0 + 1);
+    }
     cp_async_wait<0>();
     renormalise();
 

@@ -86,6 +86,7 @@ struct Layout {
     int64_t lab_cap;             // label-metadata slots: B * max_U + B
     size_t off_ctrl, off_utt, off_queue, off_nll, off_alpha, off_beta;
     size_t off_lbl, off_em, off_head, off_ent, off_lse;
+    size_t loss_only_total;      // a loss-only forward uses the arrays up to here only
     size_t total;
 };
 
@@ -136,13 +137,15 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.off_utt = o;    o = align_up(o + sizeof(UttInfo) * (size_t)B, 256);
     L.off_queue = o;  o = align_up(o + sizeof(int32_t) * (3 * (size_t)B + 1), 256);
     L.off_nll = o;    o = align_up(o + sizeof(double) * (size_t)B, 256);
+    L.off_em = o;     o = align_up(o + 16 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
+    L.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)T_total, 256);
+    L.loss_only_total = o;
+    // what only the backward reads: the stored rows, label records, class sums
     L.off_alpha = o;  o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.spitch, 256);
     L.off_beta = o;   o = align_up(o + sizeof(int32_t) * (size_t)T_total * (size_t)L.spitch, 256);
     L.off_lbl = o;    o = align_up(o + sizeof(int4) * (size_t)L.lab_cap, 256);
-    L.off_em = o;     o = align_up(o + 16 * (size_t)(T_total + 2 * kEmPad) * (size_t)L.epitch, 256);
     L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
     L.off_ent = o;    o = align_up(o + 8 * (size_t)T_total * (size_t)L.ecap, 256);
-    L.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)T_total, 256);
     L.total = o;
     return L;
 }

@@ -33,6 +33,7 @@ struct ChainArgs {
     int reduction;
     int zero_infinity;
     const float* lse;    // per-row log-sum-exp of logits input, subtracted from each value; null for log probabilities
+    int store_rows;      // store the state rows the backward needs (0 in a loss-only forward)
 };
 
 struct GradArgs {

@@ -13,7 +13,6 @@
 // CTC_PACKED_FLAG_LOSS_ONLY; the same prep and chain kernels run, with this
 // array as their workspace.
 #include <cstdint>
-#include <mutex>
 
 #include "ctc_common.cuh"
 
@@ -24,30 +23,16 @@ static __device__ __align__(256) unsigned char ctc_noalloc_scratch[CTC_PACKED_NO
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device.  The first call on a
-// device looks the address up (this may load the library's device code on
-// that device); later calls return the cached pointer.
+// Device address of the scratch on the current device.  Looked up on every
+// call (a cheap host-side query), so nothing cached can go stale; the first
+// look-up on a device may load the library's device code there.
 ctc_packed_status scratch_on_current_device(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, ctc_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();  // leave no error behind for the caller's next launch check
         return CTC_PACKED_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) return CTC_PACKED_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, ctc_noalloc_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();  // leave no error behind for the caller's next launch check
-            return CTC_PACKED_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return CTC_PACKED_OK;
 }
 
@@ -60,7 +45,7 @@ extern "C" ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, c
                                                         int zero_infinity, ctc_packed_reduction reduction,
                                                         float* loss, cudaStream_t stream) {
     // size check first, so an oversized call touches no device state
-    const size_t need = ctc_packed_workspace_size(T_total, B, max_target_len, D, dtype);
+    const size_t need = ctc_packed_workspace_size_loss_only(T_total, B, max_target_len, D, dtype);
     if (need == 0) {
         const bool in_range = (dtype == CTC_PACKED_F32 || dtype == CTC_PACKED_BF16 || dtype == CTC_PACKED_F16) &&
                               T_total >= 0 && B >= 0 && max_target_len >= 0 && D >= 1;
@@ -74,7 +59,8 @@ extern "C" ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, c
     // word, queue heads, CTA counter) on the stream before anything reads it;
     // every other scratch entry is written before it is read within the call.
     // So nothing needs clearing from the host, and one call leaves no state
-    // that the next depends on.
+    // that the next depends on.  A loss-only forward touches only the first
+    // ctc_packed_workspace_size_loss_only bytes of a workspace.
     return ctc_packed_forward(log_probs, dtype, T_total, D, cu_seqlens, lengths, targets, target_lengths, B,
                               max_target_len, blank, zero_infinity, reduction, loss, scratch,
                               (size_t)CTC_PACKED_NOALLOC_SCRATCH_BYTES, CTC_PACKED_FLAG_LOSS_ONLY, stream);

@@ -74,3 +74,22 @@ def test_fsa_wrappers_check_their_tensors_before_any_call():
         pk.ctc_packed_fsa_forward(lp, cu, ln, short, 3, 4, False, loss, ws)
     with pytest.raises(TypeError, match="cu_seqlens"):
         pk.ctc_packed_fsa_forward(lp, cu.long(), ln, fsa, 3, 4, False, loss, ws)
+
+
+def test_noalloc_wrapper_checks_its_tensors_before_any_launch():
+    lp = torch.zeros(10, 5)
+    cu = torch.tensor([0, 6, 10], dtype=torch.int32)
+    ln = torch.tensor([6, 4], dtype=torch.int32)
+    tg = torch.tensor([1, 2, 3], dtype=torch.int32)
+    tl = torch.tensor([2, 1], dtype=torch.int32)
+    loss = torch.zeros(2)
+    with pytest.raises(TypeError, match="log_probs"):
+        pk.ctc_packed_forward_noalloc(lp.double(), cu, ln, tg, tl, 0, False, "none", loss, 2)
+    with pytest.raises(TypeError, match="log_probs"):
+        pk.ctc_packed_forward_noalloc(lp.t(), cu, ln, tg, tl, 0, False, "none", loss, 2)  # not contiguous
+    with pytest.raises(TypeError, match="cu_seqlens"):
+        pk.ctc_packed_forward_noalloc(lp, cu.long(), ln, tg, tl, 0, False, "none", loss, 2)
+    with pytest.raises(TypeError, match="targets"):
+        pk.ctc_packed_forward_noalloc(lp, cu, ln, tg[::2], tl, 0, False, "none", loss, 2)
+    with pytest.raises(TypeError, match="loss"):
+        pk.ctc_packed_forward_noalloc(lp, cu, ln, tg, tl, 0, False, "none", loss.double(), 2)

@@ -8,8 +8,9 @@ things:
 * it gives the losses of the ordinary forward (with a caller-supplied
   workspace) within the loss tolerance, on two calls in a row on one stream
   with different batches, which shows that one call leaves nothing behind
-  that changes the next;
-* a batch that nearly fills the array still runs;
+  that changes the next, and the fp64 oracle's losses;
+* a batch that nearly fills the array (its loss-only workspace size) still
+  runs;
 * batches too large for the array are refused before any CUDA call.
 
 The file name puts these tests after all others. They must pass both there
@@ -24,6 +25,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import packed_sequence_ctc_gb300 as pk
 import workloads
 from tests.helpers import assert_loss_close, to_device
@@ -55,13 +57,15 @@ def test_scratch_size_matches_the_header():
 
 def test_oversized_batches_are_refused_before_any_cuda_call(lib):
     cap = pk.NOALLOC_SCRATCH_BYTES
-    # 4 state-row buffers' worth of frames: far beyond the scratch
-    assert lib.ctc_packed_workspace_size(100_000, 8, 200, 1025, 0) > cap
+    # far beyond the scratch
+    assert lib.ctc_packed_workspace_size_loss_only(100_000, 8, 200, 1025, 0) > cap
     assert _noalloc_raw(lib, 100_000, 8, 200, 1025) == ERR_WORKSPACE
     # the smallest frame count that no longer fits is refused too
     T = _largest_fitting_frames(lib, 8, 100, 1025)
-    assert lib.ctc_packed_workspace_size(T + 1, 8, 100, 1025, 0) > cap
+    assert lib.ctc_packed_workspace_size_loss_only(T + 1, 8, 100, 1025, 0) > cap
     assert _noalloc_raw(lib, T + 1, 8, 100, 1025) == ERR_WORKSPACE
+    # the limit is the loss-only workspace: the full one would be refused
+    assert lib.ctc_packed_workspace_size(T, 8, 100, 1025, 0) > cap
     assert pk.ctc_packed_status_string(ERR_WORKSPACE).startswith("workspace")
     # invalid and unsupported sizes keep the ordinary forward's codes
     assert _noalloc_raw(lib, -1, 1, 1, 5) == ERR_INVALID
@@ -74,7 +78,7 @@ def _largest_fitting_frames(lib, B, mtl, D):
     lo, hi = 0, 1 << 24
     while lo < hi:
         mid = (lo + hi + 1) // 2
-        if lib.ctc_packed_workspace_size(mid, B, mtl, D, 0) <= pk.NOALLOC_SCRATCH_BYTES:
+        if lib.ctc_packed_workspace_size_loss_only(mid, B, mtl, D, 0) <= pk.NOALLOC_SCRATCH_BYTES:
             lo = mid
         else:
             hi = mid - 1
@@ -107,8 +111,8 @@ def _second_batch():
 def test_two_calls_in_a_row_match_the_workspace_forward(cuda_device, lib):
     first = workloads.workload("tiny")
     second = _second_batch()
-    assert lib.ctc_packed_workspace_size(second.log_probs.shape[0], second.B, second.max_target_len, 1025,
-                                         1) <= pk.NOALLOC_SCRATCH_BYTES
+    assert lib.ctc_packed_workspace_size_loss_only(second.log_probs.shape[0], second.B, second.max_target_len, 1025,
+                                                   1) <= pk.NOALLOC_SCRATCH_BYTES
     # both calls go onto the same stream back to back, without a host wait
     a, keep_a = _losses(first, noalloc=True)
     b, keep_b = _losses(second, noalloc=True)
@@ -120,6 +124,11 @@ def test_two_calls_in_a_row_match_the_workspace_forward(cuda_device, lib):
     assert_loss_close(b.double().cpu().numpy(), rb.double().cpu().numpy())
     # the unalignable utterance keeps its +inf
     assert np.isinf(b[-1].item()) and np.isinf(rb[-1].item())
+    # and both calls give the fp64 oracle's losses
+    ref_a, _, _ = oracle.oracle_batch(first, need_grad=False)
+    ref_b, _, _ = oracle.oracle_batch(second, need_grad=False)
+    assert_loss_close(a.double().cpu().numpy(), ref_a)
+    assert_loss_close(b.double().cpu().numpy(), ref_b)
 
 
 @pytest.mark.gpu
@@ -142,7 +151,7 @@ def test_reductions_match_on_a_second_stream(cuda_device, lib, reduction):
 def test_batch_that_nearly_fills_the_scratch(cuda_device, lib):
     B, mtl, D = 8, 100, 65
     T = _largest_fitting_frames(lib, B, mtl, D)
-    assert lib.ctc_packed_workspace_size(T, B, mtl, D, 0) > pk.NOALLOC_SCRATCH_BYTES // 2
+    assert lib.ctc_packed_workspace_size_loss_only(T, B, mtl, D, 0) > pk.NOALLOC_SCRATCH_BYTES // 2
     per = T // B
     batch = workloads.make_batch([per] * B, [mtl] * (B - 1) + [7], D, seed=3, reduction="none",
                                  max_target_len=mtl, name="noalloc-full")
