@@ -536,7 +536,8 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
 }
 
 template __global__ void chain_kernel<1, 256>(ChainArgs);
-template __global__ void chain_kernel<1, 1024>(ChainArgs);
+template __global__ void chain_kernel<1, 512>(ChainArgs);
+template __global__ void chain_kernel<2, 512>(ChainArgs);
 template __global__ void chain_kernel<2, 1024>(ChainArgs);
 template __global__ void chain_kernel<4, 1024>(ChainArgs);
 
@@ -567,9 +568,11 @@ static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s) {
+    // the smallest thread bound that holds the chain's warps: fewer threads
+    // a CTA, more registers a thread
     switch (pairs_for_max_u(a.L.max_U)) {
-        case 1: return a.L.nwo <= 8 ? launch_chain_t<1, 256>(a, s) : launch_chain_t<1, 1024>(a, s);
-        case 2: return launch_chain_t<2, 1024>(a, s);
+        case 1: return a.L.nwo <= 8 ? launch_chain_t<1, 256>(a, s) : launch_chain_t<1, 512>(a, s);
+        case 2: return a.L.nwo <= 16 ? launch_chain_t<2, 512>(a, s) : launch_chain_t<2, 1024>(a, s);
         default: return launch_chain_t<4, 1024>(a, s);
     }
 }

@@ -106,9 +106,14 @@ __host__ __device__ constexpr int ghost_lanes(int P) { return P == 1 ? 8 : P == 
 __host__ __device__ constexpr int group_pairs(int P) { return (32 - ghost_lanes(P)) * P; }
 // State pairs (blank, label) each lane of a chain warp holds, from the target
 // bound; a warp owns group_pairs(P) pairs and at most 32 warps run a chain.
+// One pair per lane up to 16 warps (a chain CTA of at most 512 threads keeps
+// 128 registers a thread), then two pairs per lane (up to 16, then 32
+// warps), then four.
 __host__ __device__ inline int pairs_for_max_u(int max_u) {
     const int pairs = max_u + 1;
-    return pairs <= group_pairs(1) * 32 ? 1 : pairs <= group_pairs(2) * 32 ? 2 : 4;
+    if (pairs <= group_pairs(1) * 16) return 1;
+    if (pairs <= group_pairs(2) * 32) return 2;
+    return 4;
 }
 
 __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_t max_U, int32_t D) {
