@@ -55,6 +55,21 @@ int stream_override() {
     return e[0] == '0' ? 0 : 1;
 }
 
+// State-row policy: 1 keeps every frame's alpha and beta rows for the
+// backward; K > 1 (a power of two) keeps only the rows at multiples of K and
+// the backward recomputes the others (segpost.cu).  CTC_PACKED_CKPT=K
+// overrides (1 or a power of two the recompute supports).
+int checkpoint_interval(const Layout& L) {
+    const int kmax = segpost_max_ckpt(L);
+    const char* e = std::getenv("CTC_PACKED_CKPT");
+    if (e != nullptr && e[0] != '\0') {
+        const int k = std::atoi(e);
+        if (k >= 2 && (k & (k - 1)) == 0 && k <= kmax) return k;
+        return 1;
+    }
+    return 1;
+}
+
 // Fills `sa` for the bulk-copy stream; false when it cannot run this call
 // (unaligned buffers, or one team's slots do not fit shared memory).
 bool plan_stream(StreamArgs& sa, const Layout& L, const void* lp, void* grad, ctc_packed_dtype dtype, int32_t D,
@@ -100,6 +115,8 @@ ctc_packed_status enqueue_forward(const void* log_probs, ctc_packed_dtype dtype,
     pa.need_grad = need_grad ? 1 : 0;
     pa.group_pairs = L.gpairs;
     pa.logits = logits ? 1 : 0;
+    const int ckpt = checkpoint_interval(L);
+    pa.ckpt = ckpt;
     if (launch_prep(pa, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
 
     ChainArgs ca{};
@@ -116,7 +133,7 @@ ctc_packed_status enqueue_forward(const void* log_probs, ctc_packed_dtype dtype,
     ca.reduction = reduction;
     ca.zero_infinity = zero_infinity ? 1 : 0;
     ca.lse = nullptr;
-    ca.store_rows = need_grad ? 1 : 0;
+    ca.store_rows = need_grad ? ckpt : 0;
     if (logits) {
         // one dense pass over the logits: each row's log-sum-exp
         if (launch_lse(ca, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
@@ -214,6 +231,13 @@ ctc_packed_status ctc_packed_backward(const void* log_probs, ctc_packed_dtype dt
     ga.congruent = ((g0 ^ l0) & 15u) == 0 ? 1 : 0;
     ga.gp_mul = grad_group_multiplier(ga.L);
     if (ga.gp_mul == 0) return CTC_PACKED_ERR_UNSUPPORTED;
+    ga.ckpt = checkpoint_interval(ga.L);
+    if (ga.ckpt > 1) {
+        // checkpoint rows only: class sums by recomputation, then the row-group stream
+        if (launch_segpost(ga, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+        if (launch_grad(ga, (int)dtype, stream) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+        return CTC_PACKED_OK;
+    }
     const int ov = stream_override();
     if (ov != 0 && (ov == 1 || (long long)D * eb >= kStreamMinRowBytes)) {
         StreamArgs sa;

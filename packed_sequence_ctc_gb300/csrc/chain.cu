@@ -241,6 +241,25 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             offp += off_step;
         }
     };
+    // Checkpoint policy (store_rows = K > 1): only rows whose absolute index
+    // is a multiple of K are kept, written straight to their place (no stage);
+    // the backward recomputes the rows in between from them.
+    auto flush_ckpt = [&](int k) {  // the row of chain frame k, if it is a checkpoint
+        const int64_t row = row0 + (DIR == 0 ? (int64_t)k : -(int64_t)k);
+        if ((row & (int64_t)(a.store_rows - 1)) != 0) return;  // the same for every lane
+        int emax = kEZero;
+#pragma unroll
+        for (int p = 0; p < P; ++p) emax = max(emax, max(ex[p], ey[p]));
+        const int A = __reduce_max_sync(0xffffffffu, own ? emax : kEZero);
+        int* rp = st_base + row * a.L.spitch;
+        if (store_me) {
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                *reinterpret_cast<int2*>(rp + a.L.owo + 2 * (j0 + p)) =
+                    make_int2(enc_state(rx[p], ex[p], A), enc_state(ry[p], ey[p], A));
+        }
+        if (lane == 0) rp[c.w] = A;
+    };
     // rows k0 .. k0 + n - 1 of the chain, staged in slots 0 .. n - 1: the
     // warp's segments as 16-byte chunks spread over all lanes, and the offsets
     auto write_rows = [&](int k0, int n) {
@@ -371,12 +390,16 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             XP el[P], eb;
             emissions(base + q, el, eb);
             request((base + q + S::R - 1) & (S::R - 1), i0 + q + S::R - 1);
-            if (a.store_rows) flush_row(q);  // frame i0 + q - 1
+            if (a.store_rows == 1) {
+                flush_row(q);  // frame i0 + q - 1
+            } else if (a.store_rows > 1) {
+                flush_ckpt(i0 + q - 1);
+            }
             step(el, eb);
         }
         renormalise();
         if (multi) exchange((i0 - 1) / S::F);
-        if (a.store_rows) write_rows(i0 - 1, S::F);
+        if (a.store_rows == 1) write_rows(i0 - 1, S::F);
     }
     // the last frames (fewer than F: no exchange needed)
 #pragma unroll 1
@@ -386,12 +409,18 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         const uint32_t slot = (uint32_t)((i - 1) & (S::R - 1));
         emissions(slot, el, eb);
         request((slot + S::R - 1) & (S::R - 1), i + S::R - 1);
-        if (a.store_rows) flush_row(i - i0);  // frame i - 1
+        if (a.store_rows == 1) {
+            flush_row(i - i0);  // frame i - 1
+        } else if (a.store_rows > 1) {
+            flush_ckpt(i - 1);
+        }
         step(el, eb);
     }
-    if (a.store_rows) {
+    if (a.store_rows == 1) {
         flush_row(T - i0);  // frame T - 1 (T >= 1 for every queued item)
         write_rows(i0 - 1, T - i0 + 1);
+    } else if (a.store_rows > 1) {
+        flush_ckpt(T - 1);
     }
     cp_async_wait<0>();
     renormalise();

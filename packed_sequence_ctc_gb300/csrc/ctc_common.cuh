@@ -34,7 +34,8 @@ struct Control {
     int32_t n_big, n_small, n_lab;
     uint32_t logits;      // 1: the forward took logits, normalised each row, and kept its log-sum-exp
     int32_t tl_total;     // sum of the target lengths (negative ones as 0): mean_volume's divisor
-    uint32_t pad[6];
+    uint32_t ckpt;        // the forward kept every state row (1) or only those at multiples of ckpt
+    uint32_t pad[5];
 };
 static_assert(sizeof(Control) == 64, "control block is 64 bytes");
 

@@ -17,6 +17,7 @@ struct PrepArgs {
     int need_grad;
     int group_pairs;  // pairs one chain warp owns: longer targets run on a whole CTA
     int logits;       // the input rows are logits (log_softmax is taken by the path)
+    int ckpt;         // state rows kept: every one (1) or those at multiples of ckpt
 };
 
 struct ChainArgs {
@@ -33,7 +34,8 @@ struct ChainArgs {
     int reduction;
     int zero_infinity;
     const float* lse;    // per-row log-sum-exp of logits input, subtracted from each value; null for log probabilities
-    int store_rows;      // store the state rows the backward needs (0 in a loss-only forward)
+    int store_rows;      // state rows kept for the backward: 0 none (loss only), 1 every row,
+                         // K > 1 (a power of two) only rows whose index is a multiple of K
 };
 
 struct GradArgs {
@@ -54,6 +56,7 @@ struct GradArgs {
     size_t warp_smem;    // shared memory bytes per warp
     int congruent;       // lp and grad share their address modulo 16
     uint32_t gp_mul;     // offset group of pair j: (j * gp_mul) >> 21 == j / L.gpairs
+    int ckpt;            // the forward's checkpoint interval (1: every state row was stored)
 };
 
 // The gradient stream for wide rows (stream.cu): class sums and dense rows in
@@ -102,5 +105,8 @@ cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_post(const GradArgs& a, cudaStream_t s);
 cudaError_t launch_grad(const GradArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_stream(const StreamArgs& a, int dtype, cudaStream_t s);
+__global__ void segpost_kernel(GradArgs a);
+cudaError_t launch_segpost(const GradArgs& a, cudaStream_t s);
+int segpost_max_ckpt(const Layout& L);  // largest checkpoint interval the recompute supports (0: none)
 
 }  // namespace ctcp

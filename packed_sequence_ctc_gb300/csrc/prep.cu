@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
         ctrl->done_ctas = 0;
         ctrl->grad_ready = a.need_grad ? 1u : 0u;
         ctrl->logits = a.logits ? 1u : 0u;
+        ctrl->ckpt = (uint32_t)a.ckpt;
     }
 
     // 1. validate, and scan the target offsets (raw lengths) and the
