@@ -95,7 +95,7 @@ typedef enum {
     CTC_PACKED_ERR_INVALID_ARGUMENT = 1, /* a host-checkable argument is wrong */
     CTC_PACKED_ERR_WORKSPACE = 2,        /* workspace NULL or smaller than ctc_packed_workspace_size */
     CTC_PACKED_ERR_CUDA = 3,             /* a CUDA runtime call failed (see cudaGetLastError) */
-    CTC_PACKED_ERR_UNSUPPORTED = 4       /* sizes beyond what the kernels support (D > 16384 or max_target_len > 3839) */
+    CTC_PACKED_ERR_UNSUPPORTED = 4       /* sizes beyond what the kernels support (D > 1048576, max_target_len > 3839; FSA: D > 16384) */
 } ctc_packed_status;
 
 /* Bits of the device status word (ctc_packed_read_status). */

@@ -296,7 +296,7 @@ const char* ctc_packed_status_string(ctc_packed_status status) {
         case CTC_PACKED_ERR_INVALID_ARGUMENT: return "invalid argument";
         case CTC_PACKED_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case CTC_PACKED_ERR_CUDA: return "CUDA runtime error";
-        case CTC_PACKED_ERR_UNSUPPORTED: return "unsupported size (D > 16384 or max_target_len > 3839)";
+        case CTC_PACKED_ERR_UNSUPPORTED: return "unsupported size (D > 1048576, max_target_len > 3839, or FSA D > 16384)";
     }
     return "unknown status";
 }

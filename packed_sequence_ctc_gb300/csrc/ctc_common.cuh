@@ -19,7 +19,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr double kLog2eD = 1.4426950408889634074;
 constexpr double kLn2D = 0.69314718055994530942;
-constexpr int kMaxD = 16384;          // one gradient row must fit a shared-memory tile
+constexpr int kMaxD = 1 << 20;        // classes of the CTC path; rows are streamed in batches
+constexpr int kFsaMaxD = 16384;       // classes of the FSA path (its backward sums a frame in a shared row of D)
 constexpr int kFsaMaxStates = 4096;  // states of one FSA sequence (shared-memory rows)
 constexpr int kMaxTargetLen = 3839;   // 4 state pairs per lane, 31 own lanes in each of 32 warps
 constexpr long long kSpinLimit = 1ll << 26;  // bounded waits give up after this many polls

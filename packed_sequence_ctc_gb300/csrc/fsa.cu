@@ -459,7 +459,7 @@ ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_tot
     if (!fsa_valid_dtype(dtype) || T_total < 0 || B < 0 || D < 1 || S_total < 0 || E_total < 0)
         return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (max_labels < 1) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if (D > kMaxD || T_total > INT32_MAX || max_states < 1 || max_states > kFsaMaxStates)
+    if (D > kFsaMaxD || T_total > INT32_MAX || max_states < 1 || max_states > kFsaMaxStates)
         return CTC_PACKED_ERR_UNSUPPORTED;
     if (cu == nullptr || so == nullptr || eo == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (B > 0 && (lengths == nullptr || sw == nullptr || fw == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
@@ -515,7 +515,7 @@ extern "C" {
 
 size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states, int32_t max_labels, int32_t D) {
     if (T_total < 0 || B < 0 || max_states < 1 || max_states > kFsaMaxStates || T_total > INT32_MAX ||
-        max_labels < 1 || D < 1 || D > kMaxD)
+        max_labels < 1 || D < 1 || D > kFsaMaxD)
         return 0;
     return fsa_layout(T_total, B, max_states, max_labels, D).total;
 }

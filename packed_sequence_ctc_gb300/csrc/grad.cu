@@ -42,8 +42,13 @@ constexpr int kPostThreads = 256;
 constexpr int kPostRows = 2;  // rows a warp of the class-sum pass walks together
 constexpr int kUnroll = 4;                   // 16-byte chunks in flight per lane
 constexpr int kBatchChunks = 32 * kUnroll;   // chunks a warp streams per batch
-constexpr int kMaxBatches = 40;              // batches of one row (D <= 16384, 4-byte elements: 33)
 constexpr int kGroupShift = 21;             // offset group of pair j: (j * gp_mul) >> kGroupShift
+
+// Entries of a warp's per-batch tables: the batches of the widest row (4-byte
+// elements, shifted by up to 15 bytes), one more for the end mark, and slack.
+__host__ __device__ constexpr int batch_slots(int D) {
+    return (int)(((4ll * D + 32) / 16 + kBatchChunks - 1) / kBatchChunks) + 4;
+}
 
 __device__ __forceinline__ int find_utterance(const int32_t* cu, int B, int64_t row) {
     int lo = 0, hi = B - 1, ans = -1;
@@ -236,8 +241,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerBlock * 32, 2) grad_kernel(GradArg
     uint32_t* pmark = reinterpret_cast<uint32_t*>(ptile + kBatchChunks * 8);  // kBatchChunks / 32 words
     // a row's class sums bucketed by batch: bstart[b] .. bstart[b + 1] in skey / sval
     int* bstart = reinterpret_cast<int*>(pmark + 4);
-    int* bfill = bstart + (kMaxBatches + 4);
-    int* skey = bfill + (kMaxBatches + 4);
+    const int nslot = batch_slots(a.D);
+    int* bfill = bstart + nslot;
+    int* skey = bfill + nslot;
     float* sval = reinterpret_cast<float*>(skey + align_up((size_t)cap, 4));
 
     const RowHead* __restrict__ head = ws_at<RowHead>(a.ws, a.L.off_head);
@@ -716,7 +722,7 @@ void grad_geometry(const Layout& L, int D, int& rows, int& entry_cap, size_t& wa
     entry_cap = k * ecap;
     warp_smem = 3 * align_up(4 * (size_t)k, 16) + 2 * align_up(4 * (size_t)entry_cap, 16) +
                 4 * (size_t)kBatchChunks * 8 + 4 * (kBatchChunks / 32) +
-                4 * 2 * (size_t)(kMaxBatches + 4) + 2 * 4 * align_up((size_t)entry_cap, 4);
+                4 * 2 * (size_t)batch_slots(D) + 2 * 4 * align_up((size_t)entry_cap, 4);
     warp_smem = align_up(warp_smem, 16);
 }
 

@@ -62,7 +62,8 @@ def test_workspace_size(lib):
     assert f(0, 0, 0, 1, 0) > 0
     assert f(-1, 1, 1, 4, 0) == 0
     assert f(10, 1, 1, 0, 0) == 0
-    assert f(10, 1, 1, 16385, 0) == 0  # unsupported D
+    assert f(10, 1, 1, (1 << 20) + 1, 0) == 0  # unsupported D
+    assert f(10, 1, 1, 32769, 0) > 0  # rows wider than any shared-memory tile are streamed in batches
     assert f(10, 1, 3840, 8, 0) == 0  # unsupported target bound
     assert f(10, 1, 1, 8, 7) == 0  # unknown dtype
 
@@ -92,7 +93,7 @@ def test_host_argument_checks_return_before_any_cuda_call(lib):
     assert _fwd(lib, ws=None) == WORKSPACE
     assert _fwd(lib, ws=128) == WORKSPACE  # not 256-byte aligned
     assert _fwd(lib, wsb=16) == WORKSPACE
-    assert _fwd(lib, D=16385) == UNSUPPORTED
+    assert _fwd(lib, D=(1 << 20) + 1) == UNSUPPORTED
     assert _fwd(lib, mtl=3840) == UNSUPPORTED
     b = lib.ctc_packed_backward
     # grad overlapping log_probs

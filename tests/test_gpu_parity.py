@@ -309,11 +309,31 @@ def test_maximum_target_length(cuda_device):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_maximum_vocabulary(cuda_device, dtype):
-    # D = 16384, the widest row the gradient stream takes
+def test_sixteen_k_vocabulary(cuda_device, dtype):
+    # D = 16384: a row of 64 KB (fp32), 33 batches of the row stream
     batch = workloads.make_batch([45, 30, 12], [9, 6, 3], 16384, dtype=dtype, seed=32, label_high=16383,
                                  reduction="mean", gaps=[0, 2, 1])
     loss, grad, status = run_gpu(batch)
+    assert status == 0
+    ref_loss, ref_grad, _ = _ref(batch)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)
+
+
+@pytest.mark.parametrize("dtype,stream,offset", [(torch.float32, None, 0), (torch.bfloat16, None, 0),
+                                                 (torch.bfloat16, "0", 0), (torch.bfloat16, "0", 2),
+                                                 (torch.float32, None, 4)])
+def test_vocabulary_wider_than_shared_memory(cuda_device, monkeypatch, dtype, stream, offset):
+    # D = 32769, an odd width: an fp32 row (128 KB) is wider than two stream
+    # slots and is walked in batches by the row-group stream; a bf16 row fits
+    # one team of the bulk-copy stream (stream=None) or takes the row-group
+    # stream (stream="0"), with the gradient congruent to the input or not
+    if stream is not None:
+        monkeypatch.setenv("CTC_PACKED_STREAM", stream)
+    D = 32769
+    batch = workloads.make_batch([40, 23, 9], [8, 5, 0], D, dtype=dtype, seed=33, label_high=D - 1,
+                                 reduction="sum", gaps=[1, 0, 2])
+    loss, grad, status = run_gpu(batch, grad_offset_bytes=offset)
     assert status == 0
     ref_loss, ref_grad, _ = _ref(batch)
     assert_loss_close(loss, ref_loss)
