@@ -75,7 +75,11 @@ extern "C" {
 typedef enum {
     CTC_PACKED_F32 = 0,  /* float32 log probabilities and gradient */
     CTC_PACKED_BF16 = 1, /* bfloat16 */
-    CTC_PACKED_F16 = 2   /* float16 */
+    CTC_PACKED_F16 = 2,  /* float16 */
+    /* float64: sizes the workspace of ctc_packed_forward_f64 and
+     * ctc_packed_backward_f64, whose loss and upstream gradient are float64
+     * too; the entry points above reject it */
+    CTC_PACKED_F64 = 3
 } ctc_packed_dtype;
 
 typedef enum {
@@ -211,6 +215,37 @@ ctc_packed_status ctc_packed_forward_backward(const void* log_probs, ctc_packed_
                                               ctc_packed_reduction reduction, const float* grad_loss, float* loss,
                                               void* grad_log_probs, void* workspace, size_t workspace_bytes,
                                               unsigned flags, cudaStream_t stream);
+
+/*
+ * Float64 path: the forward and backward above for float64 log probabilities
+ * (or logits with CTC_PACKED_FLAG_LOGITS), with a float64 loss, upstream
+ * gradient and gradient; same layout, sizes, checks, device status bits,
+ * reductions and flags as ctc_packed_forward / ctc_packed_backward.  The
+ * workspace comes from ctc_packed_workspace_size(..., CTC_PACKED_F64) (or the
+ * loss-only size) and is not interchangeable with the other dtypes' one.
+ *   log_probs, grad_log_probs  8-byte aligned; not overlapping.
+ *   loss                       float64 device output: B entries for NONE, 1 otherwise.
+ *   grad_loss                  float64 device input: B entries for NONE, 1 otherwise.
+ * Precision: probabilities are carried as a float64 mantissa with an int
+ * exponent through both recursions, so no state underflows; the loss and
+ * gradient agree with an exact float64 evaluation to about 1e-12 relative.
+ * Page "feat(asr): native CTC loss kernel over sequence-packed log
+ * probabilities": ctc.py forward_packed serves float64 at float64 precision
+ * on a path of its own, and test_ctc_loss.py test_float64_takes_padded_path
+ * holds it to 1e-10; this path does the same without padding the batch.
+ */
+ctc_packed_status ctc_packed_forward_f64(const double* log_probs, int64_t T_total, int32_t D,
+                                         const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                         const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                         int32_t blank, int zero_infinity, ctc_packed_reduction reduction,
+                                         double* loss, void* workspace, size_t workspace_bytes, unsigned flags,
+                                         cudaStream_t stream);
+ctc_packed_status ctc_packed_backward_f64(const double* log_probs, int64_t T_total, int32_t D,
+                                          const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                          const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                          int32_t blank, int zero_infinity, ctc_packed_reduction reduction,
+                                          const double* grad_loss, void* workspace, size_t workspace_bytes,
+                                          double* grad_log_probs, cudaStream_t stream);
 
 /*
  * Copies the device status word of `workspace` (an OR of CTC_PACKED_DEV_*

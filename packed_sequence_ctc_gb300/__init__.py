@@ -27,13 +27,15 @@ __all__ = [
     "DTYPE_CODES", "REDUCTION_CODES", "DEVICE_STATUS_BITS", "CTCPackedError",
     "ctc_packed_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "FLAG_LOSS_ONLY", "FLAG_LOGITS",
     "ctc_packed_fsa_workspace_size", "ctc_packed_fsa_forward", "ctc_packed_fsa_backward",
-    "ctc_packed_forward_backward", "ctc_packed_workspace_size_loss_only",
+    "ctc_packed_forward_backward", "ctc_packed_workspace_size_loss_only", "WORKSPACE_DTYPE_CODES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libctc_packed.so")
 
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+# workspace sizes also exist for float64, whose calls are ctc_packed_forward_f64 / ctc_packed_backward_f64
+WORKSPACE_DTYPE_CODES = {**DTYPE_CODES, torch.float64: 3}
 REDUCTION_CODES = {"none": 0, "sum": 1, "mean": 2, "mean_batch": 3, "mean_volume": 4}
 FLAG_LOSS_ONLY = 0x1
 FLAG_LOGITS = 0x2  # the input rows are logits: log_softmax is taken inside, the gradient is w.r.t. the logits
@@ -80,6 +82,12 @@ def load_library(path: Optional[str] = None):
     lib.ctc_packed_forward_backward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32,
                                                 ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, sz, u32, vp]
     lib.ctc_packed_forward_backward.restype = ctypes.c_int
+    lib.ctc_packed_forward_f64.argtypes = [vp, i64, i32, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, ctypes.c_int,
+                                           vp, vp, sz, u32, vp]
+    lib.ctc_packed_forward_f64.restype = ctypes.c_int
+    lib.ctc_packed_backward_f64.argtypes = [vp, i64, i32, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, ctypes.c_int,
+                                            vp, vp, sz, vp, vp]
+    lib.ctc_packed_backward_f64.restype = ctypes.c_int
     lib.ctc_packed_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.ctc_packed_read_status.restype = ctypes.c_int
     lib.ctc_packed_status_string.argtypes = [ctypes.c_int]
@@ -121,18 +129,26 @@ def ctc_packed_status_string(status: int) -> str:
 
 
 def ctc_packed_workspace_size(T_total: int, B: int, max_target_len: int, D: int, dtype: torch.dtype) -> int:
-    return int(load_library().ctc_packed_workspace_size(T_total, B, max_target_len, D, DTYPE_CODES[dtype]))
+    return int(load_library().ctc_packed_workspace_size(T_total, B, max_target_len, D, WORKSPACE_DTYPE_CODES[dtype]))
 
 
 def ctc_packed_workspace_size_loss_only(T_total: int, B: int, max_target_len: int, D: int, dtype: torch.dtype) -> int:
-    return int(load_library().ctc_packed_workspace_size_loss_only(T_total, B, max_target_len, D, DTYPE_CODES[dtype]))
+    return int(load_library().ctc_packed_workspace_size_loss_only(T_total, B, max_target_len, D,
+                                                                  WORKSPACE_DTYPE_CODES[dtype]))
 
 
 def ctc_packed_forward(log_probs, cu_seqlens, lengths, targets, target_lengths, blank: int, zero_infinity: bool,
                        reduction: str, loss, workspace, max_target_len: int, flags: int = 0, stream=None):
-    """Enqueue the forward on `stream` (default: torch's current stream)."""
+    """Enqueue the forward on `stream` (default: torch's current stream).
+    float64 log probabilities take ctc_packed_forward_f64 (`loss` float64)."""
     T_total, D = log_probs.shape
     B = lengths.numel()
+    if log_probs.dtype == torch.float64:
+        _check(load_library().ctc_packed_forward_f64(
+            _ptr(log_probs), T_total, D, _ptr(cu_seqlens), _ptr(lengths), _ptr(targets) if targets.numel() else None,
+            _ptr(target_lengths), B, max_target_len, blank, int(bool(zero_infinity)), REDUCTION_CODES[reduction],
+            _ptr(loss), _ptr(workspace), workspace.numel(), flags, _stream(stream)))
+        return
     _check(load_library().ctc_packed_forward(
         _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
         _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
@@ -142,9 +158,16 @@ def ctc_packed_forward(log_probs, cu_seqlens, lengths, targets, target_lengths, 
 
 def ctc_packed_backward(log_probs, cu_seqlens, lengths, targets, target_lengths, blank: int, zero_infinity: bool,
                         reduction: str, grad_loss, workspace, grad_log_probs, max_target_len: int, stream=None):
-    """Enqueue the backward on `stream` (default: torch's current stream)."""
+    """Enqueue the backward on `stream` (default: torch's current stream).
+    float64 log probabilities take ctc_packed_backward_f64 (`grad_loss` float64)."""
     T_total, D = log_probs.shape
     B = lengths.numel()
+    if log_probs.dtype == torch.float64:
+        _check(load_library().ctc_packed_backward_f64(
+            _ptr(log_probs), T_total, D, _ptr(cu_seqlens), _ptr(lengths), _ptr(targets) if targets.numel() else None,
+            _ptr(target_lengths), B, max_target_len, blank, int(bool(zero_infinity)), REDUCTION_CODES[reduction],
+            _ptr(grad_loss), _ptr(workspace), workspace.numel(), _ptr(grad_log_probs), _stream(stream)))
+        return
     _check(load_library().ctc_packed_backward(
         _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
         _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
@@ -156,9 +179,17 @@ def ctc_packed_forward_backward(log_probs, cu_seqlens, lengths, targets, target_
                                 zero_infinity: bool, reduction: str, grad_loss, loss, grad_log_probs, workspace,
                                 max_target_len: int, flags: int = 0, stream=None):
     """Enqueue forward and backward in one call (bitwise equal to
-    ctc_packed_forward followed by ctc_packed_backward)."""
+    ctc_packed_forward followed by ctc_packed_backward).  float64 log
+    probabilities run exactly those two calls (the float64 path has no
+    single entry point)."""
     T_total, D = log_probs.shape
     B = lengths.numel()
+    if log_probs.dtype == torch.float64:
+        ctc_packed_forward(log_probs, cu_seqlens, lengths, targets, target_lengths, blank, zero_infinity, reduction,
+                           loss, workspace, max_target_len, flags=flags, stream=stream)
+        ctc_packed_backward(log_probs, cu_seqlens, lengths, targets, target_lengths, blank, zero_infinity, reduction,
+                            grad_loss, workspace, grad_log_probs, max_target_len, stream=stream)
+        return
     _check(load_library().ctc_packed_forward_backward(
         _ptr(log_probs), DTYPE_CODES[log_probs.dtype], T_total, D, _ptr(cu_seqlens), _ptr(lengths),
         _ptr(targets) if targets.numel() else None, _ptr(target_lengths), B, max_target_len, blank,
@@ -271,8 +302,8 @@ class PackedCTCLoss(torch.autograd.Function):
     @staticmethod
     def forward(ctx, log_probs, cu_seqlens, lengths, targets, target_lengths, blank, zero_infinity, reduction,
                 max_target_len, check, logits=False):
-        if log_probs.dtype not in DTYPE_CODES:
-            raise TypeError(f"log_probs must be float32, bfloat16 or float16, got {log_probs.dtype}.")
+        if log_probs.dtype not in WORKSPACE_DTYPE_CODES:
+            raise TypeError(f"log_probs must be float32, bfloat16, float16 or float64, got {log_probs.dtype}.")
         if log_probs.ndim != 2 or not log_probs.is_cuda:
             raise ValueError("log_probs must be a (T_total, D) CUDA tensor")
         dev = log_probs.device
@@ -281,7 +312,8 @@ class PackedCTCLoss(torch.autograd.Function):
         B = ln.numel()
         T_total, D = log_probs.shape
         ws = Workspace(T_total, B, max_target_len, D, log_probs.dtype, dev).tensor
-        loss = torch.empty(B if reduction == "none" else 1, dtype=torch.float32, device=dev)
+        loss_dtype = torch.float64 if log_probs.dtype == torch.float64 else torch.float32
+        loss = torch.empty(B if reduction == "none" else 1, dtype=loss_dtype, device=dev)
         ctc_packed_forward(log_probs, cu, ln, tg, tl, blank, zero_infinity, reduction, loss, ws, max_target_len,
                            flags=FLAG_LOGITS if logits else 0)
         if check:
@@ -294,7 +326,8 @@ class PackedCTCLoss(torch.autograd.Function):
     def backward(ctx, grad_out):
         log_probs, cu, ln, tg, tl, ws = ctx.saved_tensors
         blank, zero_infinity, reduction, max_target_len = ctx.args
-        g = grad_out.to(torch.float32).reshape(-1).contiguous()
+        g_dtype = torch.float64 if log_probs.dtype == torch.float64 else torch.float32
+        g = grad_out.to(g_dtype).reshape(-1).contiguous()
         grad = torch.empty_like(log_probs)
         ctc_packed_backward(log_probs, cu, ln, tg, tl, blank, zero_infinity, reduction, g, ws, grad, max_target_len)
         return grad, None, None, None, None, None, None, None, None, None, None

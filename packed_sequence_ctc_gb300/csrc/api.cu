@@ -164,15 +164,19 @@ extern "C" {
 
 size_t ctc_packed_workspace_size(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
                                  ctc_packed_dtype dtype) {
-    if (!valid_dtype(dtype) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return 0;
+    if ((!valid_dtype(dtype) && dtype != CTC_PACKED_F64) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1)
+        return 0;
     if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return 0;
+    if (dtype == CTC_PACKED_F64) return f64_workspace_bytes(T_total, B, max_target_len, D, false);
     return make_layout(T_total, B, max_target_len, D).total;
 }
 
 size_t ctc_packed_workspace_size_loss_only(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D,
                                            ctc_packed_dtype dtype) {
-    if (!valid_dtype(dtype) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return 0;
+    if ((!valid_dtype(dtype) && dtype != CTC_PACKED_F64) || T_total < 0 || B < 0 || max_target_len < 0 || D < 1)
+        return 0;
     if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return 0;
+    if (dtype == CTC_PACKED_F64) return f64_workspace_bytes(T_total, B, max_target_len, D, true);
     return make_layout(T_total, B, max_target_len, D).loss_only_total;
 }
 

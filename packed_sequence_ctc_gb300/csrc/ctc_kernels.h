@@ -108,5 +108,7 @@ cudaError_t launch_stream(const StreamArgs& a, int dtype, cudaStream_t s);
 __global__ void segpost_kernel(GradArgs a);
 cudaError_t launch_segpost(const GradArgs& a, cudaStream_t s);
 int segpost_max_ckpt(const Layout& L);  // largest checkpoint interval the recompute supports (0: none)
+// Workspace of the float64 path (f64.cu): the whole layout, or its loss-only prefix.
+size_t f64_workspace_bytes(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D, bool loss_only);
 
 }  // namespace ctcp

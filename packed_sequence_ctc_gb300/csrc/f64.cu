@@ -1,0 +1,931 @@
+// Float64 path of the packed CTC loss: float64 log probabilities (or logits)
+// in, a float64 loss and gradient out, on the same packed layout as the other
+// dtypes (token-flat rows, cu_seqlens, concatenated targets) and with no
+// padded tensor.
+//
+// Page "feat(asr): native CTC loss kernel over sequence-packed log
+// probabilities": ctc.py ``forward_packed`` keeps float64 inputs on a path of
+// their own at float64 precision (its Triton kernels take float32, bfloat16
+// and float16 only), and test_ctc_loss.py ``test_float64_takes_padded_path``
+// holds that path to 1e-10.  The recursion and gradient are the ones of
+// ctc_loss.py (``_alpha_kernel``, ``_beta_grad_kernel``): alpha over the
+// extended label sequence, beta recomputed in the backward from the last
+// frame, and grad[t, c] = scale * (exp(lp[t, c]) - sum_{s: l(s) = c} gamma_t(s))
+// with gamma_t(s) = alpha_t(s) beta_t(s) / Z.
+//
+// Arithmetic.  A probability is carried in extended range: a float64
+// mantissa m in [1, 2) and an int exponent e, value m * 2^e (zero: m = 0).
+// The recursions then take no exp or log per state and frame, which matters
+// on a part whose float64 rate is a small fraction of its float32 rate: a sum
+// aligns its terms to the largest exponent with exact power-of-two scales and
+// adds them, a product multiplies the mantissas and adds the exponents, and
+// each emission exp(lp[t, c]) is converted once, in a parallel gather.  Every
+// step rounds to float64 (a few ulps per frame), so the loss and gradient
+// keep about 13 significant digits over thousands of frames.
+//
+// Kernels, in stream order.  Forward:
+//   prep    one CTA: utterance checks, target offsets, the losses of
+//           utterances without frames
+//   lse     (logits) one warp per row: the row's log-sum-exp
+//   emit    one warp per row: exp(lp[t, c]) of the row's labels and blank
+//   alpha   one CTA per utterance, a thread per state (or per few): the
+//           forward recursion, one barrier per frame; every alpha row is
+//           stored for the backward, and Z and the nll per utterance
+//   reduce  one CTA: the reduced loss in a fixed summation order
+// Backward:
+//   beta    one CTA per utterance: the label analysis (distinct classes in
+//           target order), then the backward recursion from the last frame;
+//           per frame the posteriors and their sum per distinct class
+//   grad    one warp per row: scale * exp(lp) for every class, then each
+//           class sum rewrites its element, scale * exp(lp) - scale * P
+// Every sum runs in a fixed order, so results are bitwise reproducible.
+#include <cmath>
+#include <cstdint>
+
+#include "ctc_common.cuh"
+#include "ctc_kernels.h"
+
+namespace ctcp {
+
+namespace {
+
+constexpr int kZeroE = -(1 << 30);  // exponent of zero; values below 2^kZeroE flush to zero
+constexpr int kRowWarps = 8;        // warps (rows) per CTA of the row kernels
+constexpr int kMaxChainThreads = 1024;
+
+// Extended-range value m * 2^e, m in [1, 2), or zero (m = 0, e = kZeroE);
+// NaN and infinity are carried in m.
+struct X64 {
+    double m;
+    int e;
+};
+
+// Emission entry of the workspace (16 bytes).
+struct EmX {
+    double m;
+    int32_t e, pad;
+};
+
+// Per-utterance record of the float64 path (64 bytes).
+struct F64Utt {
+    int32_t start, T, U, toff;
+    int32_t valid;      // cu_seqlens, lengths and target length well formed
+    int32_t labels_ok;  // every target id in [0, D) (cleared by the alpha recursion)
+    int32_t has_nan;    // a label or blank log probability of the utterance is NaN
+    int32_t nll_inf;    // no alignment: Z = 0
+    int32_t ncls;       // distinct classes of the target, the blank included (backward)
+    int32_t ze, pad0, pad1;
+    double nll, zm;     // nll, and Z = zm * 2^ze
+};
+static_assert(sizeof(F64Utt) == 64, "utterance record is 64 bytes");
+
+struct F64Layout {
+    int64_t T_total;
+    int32_t B, max_U, D;
+    int32_t Ep;    // emission entries per row: max_U labels, then the blank
+    int32_t Sp;    // stored alpha states per row: 2 max_U + 1, padded to even
+    int32_t ecap;  // class sums a row can hold: min(max_U + 1, D)
+    size_t off_ctrl, off_utt, off_lse, off_em, loss_only_total, off_am, off_ae, off_cls, off_ent, total;
+};
+
+__host__ __device__ inline F64Layout f64_layout(int64_t T, int32_t B, int32_t max_U, int32_t D) {
+    F64Layout L{};
+    L.T_total = T;
+    L.B = B;
+    L.max_U = max_U;
+    L.D = D;
+    L.Ep = max_U + 1;
+    L.Sp = 2 * max_U + 2;
+    L.ecap = L.Ep < D ? L.Ep : D;
+    size_t o = 0;
+    L.off_ctrl = o; o = align_up(o + sizeof(Control), 256);
+    L.off_utt = o;  o = align_up(o + sizeof(F64Utt) * (size_t)B, 256);
+    L.off_lse = o;  o = align_up(o + sizeof(double) * (size_t)T, 256);
+    L.off_em = o;   o = align_up(o + sizeof(EmX) * (size_t)T * (size_t)L.Ep, 256);
+    L.loss_only_total = o;
+    // what only the backward reads
+    L.off_am = o;   o = align_up(o + sizeof(double) * (size_t)T * (size_t)L.Sp, 256);
+    L.off_ae = o;   o = align_up(o + sizeof(int32_t) * (size_t)T * (size_t)L.Sp, 256);
+    L.off_cls = o;  o = align_up(o + sizeof(int32_t) * (size_t)B * (size_t)L.Ep, 256);
+    L.off_ent = o;  o = align_up(o + sizeof(double) * (size_t)T * (size_t)L.ecap, 256);
+    L.total = o;
+    return L;
+}
+
+struct F64Args {
+    F64Layout L;
+    void* ws;
+    const double* lp;
+    double* grad;
+    const int32_t* cu;
+    const int32_t* lengths;
+    const int32_t* targets;
+    const int32_t* target_lengths;
+    double* loss;
+    const double* grad_loss;
+    int D, blank, reduction, zero_infinity, need_grad, logits;
+};
+
+// ------------------------------------------------------------ extended range
+
+__device__ __forceinline__ X64 x_zero() { return X64{0.0, kZeroE}; }
+
+// 2^d as a double for d in [-1022, 1023]; 0 below (a term that far below the
+// largest one of a sum is under its last bit).
+__device__ __forceinline__ double pow2_ll(long long d) {
+    if (d < -1022) return 0.0;
+    if (d > 1023) return __longlong_as_double(0x7ff0000000000000ll);
+    return __longlong_as_double((d + 1023) << 52);
+}
+
+// Brings m >= 0 to [1, 2), adjusting e; zero, subnormal results and
+// exponents below kZeroE give zero; NaN and infinity pass through.
+__device__ __forceinline__ X64 x_norm(double m, long long e) {
+    const long long bits = __double_as_longlong(m);
+    const int be = (int)((bits >> 52) & 0x7ff);
+    if (be == 0x7ff) return X64{m, 0};
+    if (be == 0) return x_zero();
+    const long long ne = e + (be - 1023);
+    if (ne <= kZeroE) return x_zero();
+    if (ne > (1ll << 30)) return X64{__longlong_as_double(0x7ff0000000000000ll), 0};
+    return X64{__longlong_as_double((bits & 0x800fffffffffffffll) | (1023ll << 52)), (int)ne};
+}
+
+__device__ __forceinline__ X64 x_add3(X64 a, X64 b, X64 c) {
+    const int E = max(a.e, max(b.e, c.e));
+    const double m = a.m * pow2_ll((long long)a.e - E) + b.m * pow2_ll((long long)b.e - E) +
+                     c.m * pow2_ll((long long)c.e - E);
+    return x_norm(m, E);
+}
+
+__device__ __forceinline__ X64 x_mul(X64 a, X64 b) { return x_norm(a.m * b.m, (long long)a.e + b.e); }
+
+// exp(x) in extended range: x = k ln2 + r with k = floor(x log2 e), then
+// exp(r) in [1, 2) up to rounding (renormalised).
+__device__ __forceinline__ X64 x_from_log(double x) {
+    if (x != x) return X64{x, 0};
+    if (x == -INFINITY) return x_zero();
+    if (x == INFINITY) return X64{x, 0};
+    const double k = floor(x * kLog2eD);
+    if (k < (double)kZeroE) return x_zero();
+    if (k > (double)(1 << 30)) return X64{__longlong_as_double(0x7ff0000000000000ll), 0};
+    const double r = fma(-k, kLn2D, x);
+    return x_norm(exp(r), (long long)k);
+}
+
+__device__ __forceinline__ X64 ld_em(const EmX* p) {
+    const double2 v = *reinterpret_cast<const double2*>(p);
+    return X64{v.x, (int)__double_as_longlong(v.y)};
+}
+
+// ------------------------------------------------------------ helpers
+
+__device__ __forceinline__ int f64_utterance_of_row(const int32_t* cu, int B, int64_t row) {
+    int lo = 0, hi = B - 1, ans = -1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] <= row) {
+            ans = mid;
+            lo = mid + 1;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return ans;
+}
+
+// Upstream gradient factor of utterance b under the call's reduction.
+__device__ __forceinline__ double f64_scale(const F64Args& a, const F64Utt& u, int b, int tl_total) {
+    double s;
+    if (a.reduction == CTC_PACKED_NONE) {
+        s = a.grad_loss[b];
+    } else if (a.reduction == CTC_PACKED_SUM) {
+        s = a.grad_loss[0];
+    } else if (a.reduction == CTC_PACKED_MEAN) {
+        s = a.grad_loss[0] / ((double)a.L.B * (double)max(u.U, 1));
+    } else if (a.reduction == CTC_PACKED_MEAN_BATCH) {
+        s = a.grad_loss[0] / (double)a.L.B;
+    } else {
+        s = a.grad_loss[0] / (double)tl_total;
+    }
+    if (a.zero_infinity && u.nll_inf) s = 0.0;
+    return s;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exclusive scan of one value per thread over the CTA (blockDim a multiple
+// of 32); the CTA total goes to *total.
+__device__ int f64_block_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int prefix = x - v + (warp > 0 ? s_warp[warp - 1] : 0);
+    *total = s_warp[nw - 1];
+    __syncthreads();
+    return prefix;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ forward kernels
+
+__global__ void __launch_bounds__(1024) f64_prep_kernel(F64Args a) {
+    __shared__ int s_warp[32];
+    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    const int B = a.L.B, tid = threadIdx.x, nt = blockDim.x;
+    if (tid == 0) {
+        *ctrl = Control{};
+        ctrl->grad_ready = a.need_grad ? 1u : 0u;
+        ctrl->logits = a.logits ? 1u : 0u;
+        ctrl->ckpt = 1;
+    }
+    __syncthreads();
+    uint32_t bad_bits = 0;
+    int toff_base = 0;
+    for (int base = 0; base < B; base += nt) {
+        const int b = base + tid;
+        int T = 0, uraw = 0, c0 = 0, valid = 0;
+        if (b < B) {
+            c0 = a.cu[b];
+            const int c1 = a.cu[b + 1];
+            T = a.lengths[b];
+            uraw = a.target_lengths[b];
+            uint32_t bits = 0;
+            if (uraw < 0) bits |= CTC_PACKED_DEV_NEGATIVE_TARGET_LENGTH;
+            if (uraw > a.L.max_U) bits |= CTC_PACKED_DEV_TARGET_LENGTH_EXCEEDS_MAX;
+            if (c0 < 0 || c1 < c0 || (int64_t)c1 > a.L.T_total) bits |= CTC_PACKED_DEV_BAD_CU_SEQLENS;
+            if (T < 0 || (int64_t)T > (int64_t)c1 - (int64_t)c0) bits |= CTC_PACKED_DEV_BAD_LENGTH;
+            bad_bits |= bits;
+            valid = bits == 0;
+        }
+        int total;
+        const int toff = toff_base + f64_block_scan(b < B ? max(uraw, 0) : 0, s_warp, &total);
+        if (b < B) {
+            F64Utt u{};
+            u.start = c0;
+            u.T = valid ? T : 0;
+            u.U = valid ? uraw : 0;
+            u.toff = toff;
+            u.valid = valid;
+            u.labels_ok = 1;
+            u.nll_inf = (valid && T == 0 && uraw > 0) ? 1 : 0;
+            u.ze = kZeroE;
+            // utterances without a recursion get their loss here
+            const double v = !valid ? __longlong_as_double(0x7ff8000000000000ll)
+                                    : (T == 0 ? (uraw == 0 ? 0.0 : __longlong_as_double(0x7ff0000000000000ll)) : 0.0);
+            u.nll = v;
+            utt[b] = u;
+            if ((!valid || T == 0) && a.reduction == CTC_PACKED_NONE)
+                a.loss[b] = (a.zero_infinity && isinf(v)) ? 0.0 : v;
+        }
+        toff_base += total;
+    }
+    if (bad_bits) atomicOr(&ctrl->status, bad_bits);
+    if (tid == 0) ctrl->tl_total = toff_base;
+}
+
+// Row log-sum-exp of logits: max, then the sum of exp(z - max).  A NaN or
+// +inf logit gives NaN, a row of -inf gives -inf.
+__global__ void __launch_bounds__(kRowWarps * 32) f64_lse_kernel(F64Args a) {
+    const int lane = threadIdx.x & 31;
+    double* lse = ws_at<double>(a.ws, a.L.off_lse);
+    const int D = a.D;
+    const int64_t warps = (int64_t)gridDim.x * kRowWarps;
+    for (int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); row < a.L.T_total; row += warps) {
+        const double* z = a.lp + row * D;
+        double m = -INFINITY;
+        bool bad = false;
+        for (int c = lane; c < D; c += 32) {
+            const double v = __ldg(z + c);
+            bad |= (v != v) || v == INFINITY;
+            m = fmax(m, v);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, o));
+        bad = __any_sync(0xffffffffu, bad);
+        double s = 0.0;
+        if (!bad && m > -INFINITY)
+            for (int c = lane; c < D; c += 32) s += exp(__ldg(z + c) - m);
+        s = warp_sum(s);
+        if (lane == 0)
+            lse[row] = bad ? __longlong_as_double(0x7ff8000000000000ll) : (m == -INFINITY ? m : m + log(s));
+    }
+}
+
+// exp(lp[t, c]) in extended range for the U labels of the row's utterance
+// and its blank (entry U).  A label outside [0, D) gets zero here; the
+// recursion rejects the utterance.
+__global__ void __launch_bounds__(kRowWarps * 32) f64_emit_kernel(F64Args a) {
+    const int lane = threadIdx.x & 31;
+    F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    EmX* em = ws_at<EmX>(a.ws, a.L.off_em);
+    const double* lse = ws_at<double>(a.ws, a.L.off_lse);
+    const int D = a.D, Ep = a.L.Ep;
+    const int64_t warps = (int64_t)gridDim.x * kRowWarps;
+    for (int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); row < a.L.T_total; row += warps) {
+        const int b = f64_utterance_of_row(a.cu, a.L.B, row);
+        if (b < 0) continue;
+        const F64Utt u = utt[b];
+        const int64_t t = row - u.start;
+        if (!u.valid || t < 0 || t >= u.T) continue;
+        const double sh = a.logits ? lse[row] : 0.0;
+        const double* x = a.lp + row * D;
+        EmX* out = em + row * Ep;
+        bool nan = false;
+        for (int k = lane; k <= u.U; k += 32) {
+            const int c = k < u.U ? a.targets[u.toff + k] : a.blank;
+            X64 v = x_zero();
+            if (c >= 0 && c < D) {
+                const double y = __ldg(x + c) - sh;
+                nan |= y != y;
+                v = x_from_log(y);
+            }
+            *reinterpret_cast<double2*>(out + k) = make_double2(v.m, __longlong_as_double((long long)v.e));
+        }
+        if (__any_sync(0xffffffffu, nan) && lane == 0) atomicOr(&utt[b].has_nan, 1);
+    }
+}
+
+// Forward recursion of one utterance: thread i holds states i, i + nt, ...
+// (PER of them); the previous frame's values sit in shared memory, double
+// buffered, so one barrier per frame separates a frame's writes from the
+// next frame's reads.  The next frame's emissions load during the current
+// frame.
+template <int PER>
+__global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_bad;
+    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    const F64Utt u = utt[b];
+    if (!u.valid || u.T == 0) return;
+    const int U = u.U, S = 2 * U + 1, T = u.T, Ep = a.L.Ep, Sp = a.L.Sp;
+    const int cap = PER * nt;
+    double* const mbuf = reinterpret_cast<double*>(smem);         // two buffers of cap mantissas
+    int* const ebuf = reinterpret_cast<int*>(mbuf + 2 * cap);      // two buffers of cap exponents
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    const int32_t* tg = a.targets + u.toff;
+    int ent[PER];
+    bool skip[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int s = tid + k * nt;
+        ent[k] = U;
+        skip[k] = false;
+        if (s < S && (s & 1)) {
+            const int j = s >> 1;
+            const int c = tg[j];
+            if (c < 0 || c >= a.D) s_bad = 1;
+            ent[k] = j;
+            skip[k] = j >= 1 && c != tg[j - 1];
+        }
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) {
+            set_status(ctrl, CTC_PACKED_DEV_LABEL_OUT_OF_RANGE);
+            const double nan = __longlong_as_double(0x7ff8000000000000ll);
+            utt[b].labels_ok = 0;
+            utt[b].nll = nan;
+            if (a.reduction == CTC_PACKED_NONE) a.loss[b] = nan;
+        }
+        return;
+    }
+    const EmX* em = ws_at<EmX>(a.ws, a.L.off_em) + (size_t)u.start * Ep;
+    double* am = ws_at<double>(a.ws, a.L.off_am) + (size_t)u.start * Sp;
+    int32_t* ae = ws_at<int32_t>(a.ws, a.L.off_ae) + (size_t)u.start * Sp;
+    const bool store = a.need_grad != 0;
+
+    X64 nx[PER];
+    // frame 0: the first blank and the first label
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int s = tid + k * nt;
+        X64 v = x_zero();
+        if (s < S && s <= 1) v = ld_em(em + ent[k]);
+        if (s < S) {
+            mbuf[s] = v.m;
+            ebuf[s] = v.e;
+            if (store) {
+                am[s] = v.m;
+                ae[s] = v.e;
+            }
+        }
+        nx[k] = (s < S && T > 1) ? ld_em(em + Ep + ent[k]) : x_zero();
+    }
+    __syncthreads();
+    int p = 0;
+    for (int t = 1; t < T; ++t) {
+        X64 e_t[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            e_t[k] = nx[k];
+            const int s = tid + k * nt;
+            if (s < S && t + 1 < T) nx[k] = ld_em(em + (size_t)(t + 1) * Ep + ent[k]);
+        }
+        const double* mp = mbuf + p * cap;
+        const int* ep = ebuf + p * cap;
+        double* mq = mbuf + (p ^ 1) * cap;
+        int* eq = ebuf + (p ^ 1) * cap;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            if (s < S) {
+                const X64 v0{mp[s], ep[s]};
+                const X64 v1 = s >= 1 ? X64{mp[s - 1], ep[s - 1]} : x_zero();
+                const X64 v2 = skip[k] ? X64{mp[s - 2], ep[s - 2]} : x_zero();
+                const X64 r = x_mul(x_add3(v0, v1, v2), e_t[k]);
+                mq[s] = r.m;
+                eq[s] = r.e;
+                if (store) {
+                    am[(size_t)t * Sp + s] = r.m;
+                    ae[(size_t)t * Sp + s] = r.e;
+                }
+            }
+        }
+        __syncthreads();
+        p ^= 1;
+    }
+    if (tid == 0) {
+        const double* mp = mbuf + p * cap;
+        const int* ep = ebuf + p * cap;
+        const X64 last{mp[S - 1], ep[S - 1]};
+        const X64 prev = S >= 2 ? X64{mp[S - 2], ep[S - 2]} : x_zero();
+        const X64 z = x_add3(last, prev, x_zero());
+        const bool has_nan = u.has_nan != 0;  // written by the emission gather
+        double v;
+        int inf = 0;
+        if (has_nan || z.m != z.m) {
+            v = __longlong_as_double(0x7ff8000000000000ll);
+        } else if (z.m == 0.0) {
+            v = __longlong_as_double(0x7ff0000000000000ll);
+            inf = 1;
+        } else {
+            v = -(log(z.m) + (double)z.e * kLn2D);
+        }
+        utt[b].nll = v;
+        utt[b].zm = z.m;
+        utt[b].ze = z.e;
+        utt[b].nll_inf = inf;
+        if (a.reduction == CTC_PACKED_NONE) a.loss[b] = (a.zero_infinity && inf) ? 0.0 : v;
+    }
+}
+
+// The reduced loss (sum, mean, mean_batch, mean_volume) in a fixed order.
+__global__ void __launch_bounds__(256) f64_reduce_kernel(F64Args a) {
+    __shared__ double s_red[8];
+    const F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    const Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    const int B = a.L.B, tid = threadIdx.x;
+    double acc = 0.0;
+    for (int b = tid; b < B; b += 256) {
+        double v = utt[b].nll;
+        if (a.zero_infinity && isinf(v) && v > 0) v = 0.0;
+        if (a.reduction == CTC_PACKED_MEAN) v /= (double)max(a.target_lengths[b], 1);
+        acc += v;
+    }
+    acc = warp_sum(acc);
+    if ((tid & 31) == 0) s_red[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        double total = 0.0;
+        for (int w = 0; w < 8; ++w) total += s_red[w];
+        if (a.reduction == CTC_PACKED_MEAN || a.reduction == CTC_PACKED_MEAN_BATCH)
+            total = B > 0 ? total / (double)B : __longlong_as_double(0x7ff8000000000000ll);
+        if (a.reduction == CTC_PACKED_MEAN_VOLUME) total = total / (double)ctrl->tl_total;
+        a.loss[0] = total;
+    }
+}
+
+// ------------------------------------------------------------ backward kernels
+
+// Backward recursion of one utterance from its last frame, with the
+// posteriors and their class sums.  beta_t(s) excludes frame t's emission,
+// g_t(s) = beta_t(s) * exp(lp[t, l(s)]) is what frame t - 1 reads:
+//   beta_{T-1}(s) = 1 for the last two states,
+//   beta_t(s) = g_{t+1}(s) + g_{t+1}(s + 1) + [l(s + 2) != l(s)] g_{t+1}(s + 2).
+// Two barriers per frame: after the reads of g (A), after the writes of g,
+// the label posteriors and the blank partial sums (B); the class sums of the
+// frame are read between B and the next A.
+template <int PER>
+__global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ double s_wsum[kMaxChainThreads / 32];
+    __shared__ int s_warp[32];
+    __shared__ int s_bfirst;
+    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = nt >> 5;
+    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    const F64Utt u = utt[b];
+    if (ctrl->grad_ready == 0 || !u.valid || !u.labels_ok || u.T == 0) return;
+    const double scale = f64_scale(a, u, b, ctrl->tl_total);
+    if (scale == 0.0) return;  // the row stream writes zeros without class sums
+    const int U = u.U, S = 2 * U + 1, T = u.T, Ep = a.L.Ep, Sp = a.L.Sp;
+    const int cap = PER * nt;
+    double* gm = reinterpret_cast<double*>(smem);             // g, mantissas
+    double* gam = gm + cap;                                   // label-state posteriors, U entries
+    int* ge = reinterpret_cast<int*>(gam + (U > 0 ? U : 1));  // g, exponents
+    int* lab = ge + cap;                                      // the target
+    int* nxt = lab + U;                                       // next position of the same class, -1: none
+    int* rnk = nxt + U;                                       // rank of a first occurrence, -1 otherwise
+
+    // 1. label analysis: first occurrences ranked in target order, links to
+    //    the next occurrence; labels equal to the blank join its class
+    if (tid == 0) s_bfirst = -1;
+    for (int j = tid; j < U; j += nt) lab[j] = a.targets[u.toff + j];
+    __syncthreads();
+    int running = 0;
+    for (int j0 = 0; j0 < U; j0 += nt) {
+        const int j = j0 + tid;
+        bool first = false;
+        if (j < U) {
+            const int c = lab[j];
+            first = true;
+            for (int k = 0; k < j; ++k)
+                if (lab[k] == c) {
+                    first = false;
+                    break;
+                }
+            int nx = -1;
+            for (int k = j + 1; k < U; ++k)
+                if (lab[k] == c) {
+                    nx = k;
+                    break;
+                }
+            nxt[j] = nx;
+            if (c == a.blank) {
+                if (first) s_bfirst = j;
+                first = false;
+            }
+        }
+        int total;
+        const int pre = f64_block_scan(first ? 1 : 0, s_warp, &total);
+        if (j < U) rnk[j] = first ? running + pre : -1;
+        running += total;
+    }
+    const int ncls = running + 1;
+    int32_t* cls = ws_at<int32_t>(a.ws, a.L.off_cls) + (size_t)b * Ep;
+    for (int j = tid; j < U; j += nt)
+        if (rnk[j] >= 0) cls[rnk[j]] = lab[j];
+    if (tid == 0) {
+        cls[ncls - 1] = a.blank;
+        utt[b].ncls = ncls;
+    }
+    __syncthreads();
+    const int bfirst = s_bfirst;
+
+    // 2. the recursion
+    const EmX* em = ws_at<EmX>(a.ws, a.L.off_em) + (size_t)u.start * Ep;
+    const double* am = ws_at<double>(a.ws, a.L.off_am) + (size_t)u.start * Sp;
+    const int32_t* ae = ws_at<int32_t>(a.ws, a.L.off_ae) + (size_t)u.start * Sp;
+    double* ent = ws_at<double>(a.ws, a.L.off_ent) + (size_t)u.start * a.L.ecap;
+    const double invz = 1.0 / u.zm;
+    const long long ze = u.ze;
+    const bool nan_utt = u.has_nan != 0;
+    const double qnan = __longlong_as_double(0x7ff8000000000000ll);
+    int eidx[PER];
+    bool skip2[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int s = tid + k * nt;
+        eidx[k] = (s & 1) ? (s >> 1) : U;
+        skip2[k] = (s & 1) && s + 2 < S && lab[(s + 2) >> 1] != lab[s >> 1];
+    }
+    X64 al[PER], et[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int s = tid + k * nt;
+        al[k] = s < S ? X64{am[(size_t)(T - 1) * Sp + s], ae[(size_t)(T - 1) * Sp + s]} : x_zero();
+        et[k] = s < S ? ld_em(em + (size_t)(T - 1) * Ep + eidx[k]) : x_zero();
+    }
+    for (int t = T - 1; t >= 0; --t) {
+        X64 gn[PER];
+        double gamma[PER];
+        X64 al_n[PER], et_n[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            al_n[k] = x_zero();
+            et_n[k] = x_zero();
+            if (s < S && t > 0) {
+                al_n[k] = X64{am[(size_t)(t - 1) * Sp + s], ae[(size_t)(t - 1) * Sp + s]};
+                et_n[k] = ld_em(em + (size_t)(t - 1) * Ep + eidx[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            gn[k] = x_zero();
+            gamma[k] = 0.0;
+            if (s < S) {
+                X64 be;
+                if (t == T - 1) {
+                    be = s >= S - 2 ? X64{1.0, 0} : x_zero();
+                } else {
+                    const X64 v0{gm[s], ge[s]};
+                    const X64 v1 = s + 1 < S ? X64{gm[s + 1], ge[s + 1]} : x_zero();
+                    const X64 v2 = skip2[k] ? X64{gm[s + 2], ge[s + 2]} : x_zero();
+                    be = x_add3(v0, v1, v2);
+                }
+                gn[k] = x_mul(be, et[k]);
+                const double g = al[k].m * be.m * invz * pow2_ll((long long)al[k].e + be.e - ze);
+                gamma[k] = nan_utt ? qnan : g;
+            }
+        }
+        __syncthreads();  // A
+        double bpart = 0.0;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            if (s < S) {
+                gm[s] = gn[k].m;
+                ge[s] = gn[k].e;
+                if (s & 1) {
+                    gam[s >> 1] = gamma[k];
+                } else {
+                    bpart += gamma[k];
+                }
+            }
+            al[k] = al_n[k];
+            et[k] = et_n[k];
+        }
+        bpart = warp_sum(bpart);
+        if (lane == 0) s_wsum[warp] = bpart;
+        __syncthreads();  // B
+        double* er = ent + (size_t)t * a.L.ecap;
+        for (int j = tid; j < U; j += nt) {
+            const int r = rnk[j];
+            if (r < 0) continue;
+            double P = gam[j];
+            for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gam[jj];
+            er[r] = -scale * P;
+        }
+        if (tid == 0) {
+            double P = 0.0;
+            for (int w = 0; w < nw; ++w) P += s_wsum[w];
+            for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gam[jj];
+            er[ncls - 1] = -scale * P;
+        }
+    }
+}
+
+// The dense gradient: one warp per row.  A row outside every utterance's
+// frames (or of a malformed utterance, or after a loss-only forward) is 0.
+__global__ void __launch_bounds__(kRowWarps * 32) f64_grad_kernel(F64Args a) {
+    const int lane = threadIdx.x & 31;
+    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    const F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    const double* lse = ws_at<double>(a.ws, a.L.off_lse);
+    const double* ent = ws_at<double>(a.ws, a.L.off_ent);
+    const int32_t* cls = ws_at<int32_t>(a.ws, a.L.off_cls);
+    const bool ready = ctrl->grad_ready != 0;
+    const bool logits = ctrl->logits != 0;
+    const int tl_total = ctrl->tl_total;
+    const int D = a.D;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.L.T_total > 0 && !ready)
+        set_status(ctrl, CTC_PACKED_DEV_NO_GRAD_STATE);
+    const int64_t warps = (int64_t)gridDim.x * kRowWarps;
+    for (int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); row < a.L.T_total; row += warps) {
+        const int b = f64_utterance_of_row(a.cu, a.L.B, row);
+        double* g = a.grad + row * D;
+        const double* x = a.lp + row * D;
+        bool covered = false;
+        F64Utt u{};
+        if (b >= 0) {
+            u = utt[b];
+            const int64_t t = row - u.start;
+            covered = ready && u.valid && u.labels_ok && t >= 0 && t < u.T;
+        }
+        if (!covered) {
+            for (int c = lane; c < D; c += 32) g[c] = 0.0;
+            continue;
+        }
+        const double scale = f64_scale(a, u, b, tl_total);
+        const double sh = logits ? lse[row] : 0.0;
+        int c = lane;
+        for (; c + 96 < D; c += 128) {
+            const double x0 = __ldg(x + c), x1 = __ldg(x + c + 32), x2 = __ldg(x + c + 64), x3 = __ldg(x + c + 96);
+            g[c] = scale * exp(x0 - sh);
+            g[c + 32] = scale * exp(x1 - sh);
+            g[c + 64] = scale * exp(x2 - sh);
+            g[c + 96] = scale * exp(x3 - sh);
+        }
+        for (; c < D; c += 32) g[c] = scale * exp(__ldg(x + c) - sh);
+        if (scale != 0.0) {
+            __syncwarp();  // the dense stores land before the class sums rewrite their elements
+            const double* er = ent + row * a.L.ecap;
+            const int32_t* cl = cls + (size_t)b * a.L.Ep;
+            for (int k = lane; k < u.ncls; k += 32) {
+                const int cc = cl[k];
+                g[cc] = fma(scale, exp(__ldg(x + cc) - sh), er[k]);
+            }
+        }
+    }
+}
+
+}  // namespace ctcp
+
+using namespace ctcp;
+
+namespace {
+
+bool f64_valid_reduction(int r) {
+    return r == CTC_PACKED_NONE || r == CTC_PACKED_SUM || r == CTC_PACKED_MEAN || r == CTC_PACKED_MEAN_BATCH ||
+           r == CTC_PACKED_MEAN_VOLUME;
+}
+
+ctc_packed_status f64_check(const double* log_probs, int64_t T_total, int32_t D, const int32_t* cu,
+                            const int32_t* lengths, const int32_t* targets, const int32_t* target_lengths, int32_t B,
+                            int32_t max_target_len, int32_t blank, int reduction, const void* ws, size_t ws_bytes,
+                            bool loss_only) {
+    if (!f64_valid_reduction(reduction)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (T_total < 0 || B < 0 || max_target_len < 0 || D < 1) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (blank < 0 || blank >= D) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (D > kMaxD || max_target_len > kMaxTargetLen || T_total > INT32_MAX) return CTC_PACKED_ERR_UNSUPPORTED;
+    if (cu == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && (lengths == nullptr || target_lengths == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (B > 0 && max_target_len > 0 && targets == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (T_total > 0 && log_probs == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(log_probs) % 8 != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return CTC_PACKED_ERR_WORKSPACE;
+    const F64Layout L = f64_layout(T_total, B, max_target_len, D);
+    if (ws_bytes < (loss_only ? L.loss_only_total : L.total)) return CTC_PACKED_ERR_WORKSPACE;
+    return CTC_PACKED_OK;
+}
+
+F64Args f64_args(const double* log_probs, int64_t T_total, int32_t D, const int32_t* cu, const int32_t* lengths,
+                 const int32_t* targets, const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                 int32_t blank, int zero_infinity, int reduction, void* ws) {
+    F64Args a{};
+    a.L = f64_layout(T_total, B, max_target_len, D);
+    a.ws = ws;
+    a.lp = log_probs;
+    a.cu = cu;
+    a.lengths = lengths;
+    a.targets = targets;
+    a.target_lengths = target_lengths;
+    a.D = D;
+    a.blank = blank;
+    a.reduction = reduction;
+    a.zero_infinity = zero_infinity ? 1 : 0;
+    return a;
+}
+
+// States per thread of the recursion CTAs and their thread count: at most
+// 1024 threads, each holding 1, 2, 4 or 8 states.
+void chain_shape(int max_U, int& per, int& nt) {
+    const int S = 2 * max_U + 1;
+    per = 1;
+    while (per * kMaxChainThreads < S) per <<= 1;
+    const int need = (S + per - 1) / per;
+    nt = (need + 31) / 32 * 32;
+}
+
+template <typename K>
+cudaError_t launch_chain_kernel(K kernel, unsigned grid, int nt, size_t smem, cudaStream_t s, const F64Args& a) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, nt, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// Persistent grid of one of the row kernels.
+template <typename K>
+cudaError_t launch_rows(K kernel, int64_t rows, cudaStream_t s, const F64Args& a) {
+    if (rows <= 0) return cudaSuccess;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kRowWarps * 32, 0)) != cudaSuccess)
+        return e;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = (long long)sms * per_sm;
+    const long long want = (rows + kRowWarps - 1) / kRowWarps;
+    if (want < grid) grid = want;
+    kernel<<<(unsigned)grid, kRowWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace ctcp {
+
+size_t f64_workspace_bytes(int64_t T_total, int32_t B, int32_t max_target_len, int32_t D, bool loss_only) {
+    const F64Layout L = f64_layout(T_total, B, max_target_len, D);
+    return loss_only ? L.loss_only_total : L.total;
+}
+
+}  // namespace ctcp
+
+extern "C" {
+
+ctc_packed_status ctc_packed_forward_f64(const double* log_probs, int64_t T_total, int32_t D,
+                                         const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                         const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                         int32_t blank, int zero_infinity, ctc_packed_reduction reduction,
+                                         double* loss, void* workspace, size_t workspace_bytes, unsigned flags,
+                                         cudaStream_t stream) {
+    if ((flags & ~(CTC_PACKED_FLAG_LOSS_ONLY | CTC_PACKED_FLAG_LOGITS)) != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const bool loss_only = (flags & CTC_PACKED_FLAG_LOSS_ONLY) != 0;
+    const ctc_packed_status st = f64_check(log_probs, T_total, D, cu_seqlens, lengths, targets, target_lengths, B,
+                                           max_target_len, blank, (int)reduction, workspace, workspace_bytes,
+                                           loss_only);
+    if (st != CTC_PACKED_OK) return st;
+    if (loss == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    F64Args a = f64_args(log_probs, T_total, D, cu_seqlens, lengths, targets, target_lengths, B, max_target_len,
+                         blank, zero_infinity, (int)reduction, workspace);
+    a.loss = loss;
+    a.need_grad = loss_only ? 0 : 1;
+    a.logits = (flags & CTC_PACKED_FLAG_LOGITS) != 0 ? 1 : 0;
+    f64_prep_kernel<<<1, 1024, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    if (a.logits && launch_rows(f64_lse_kernel, T_total, stream, a) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    if (launch_rows(f64_emit_kernel, T_total, stream, a) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    if (B > 0) {
+        int per = 1, nt = 32;
+        chain_shape(max_target_len, per, nt);
+        const size_t smem = 2 * (size_t)per * nt * (sizeof(double) + sizeof(int));
+        cudaError_t e;
+        switch (per) {
+            case 1: e = launch_chain_kernel(f64_alpha_kernel<1>, (unsigned)B, nt, smem, stream, a); break;
+            case 2: e = launch_chain_kernel(f64_alpha_kernel<2>, (unsigned)B, nt, smem, stream, a); break;
+            case 4: e = launch_chain_kernel(f64_alpha_kernel<4>, (unsigned)B, nt, smem, stream, a); break;
+            default: e = launch_chain_kernel(f64_alpha_kernel<8>, (unsigned)B, nt, smem, stream, a); break;
+        }
+        if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+        if (reduction != CTC_PACKED_NONE) {
+            f64_reduce_kernel<<<1, 256, 0, stream>>>(a);
+            if (cudaGetLastError() != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+        }
+    } else if (reduction != CTC_PACKED_NONE) {
+        f64_reduce_kernel<<<1, 256, 0, stream>>>(a);
+        if (cudaGetLastError() != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    }
+    return CTC_PACKED_OK;
+}
+
+ctc_packed_status ctc_packed_backward_f64(const double* log_probs, int64_t T_total, int32_t D,
+                                          const int32_t* cu_seqlens, const int32_t* lengths, const int32_t* targets,
+                                          const int32_t* target_lengths, int32_t B, int32_t max_target_len,
+                                          int32_t blank, int zero_infinity, ctc_packed_reduction reduction,
+                                          const double* grad_loss, void* workspace, size_t workspace_bytes,
+                                          double* grad_log_probs, cudaStream_t stream) {
+    const ctc_packed_status st = f64_check(log_probs, T_total, D, cu_seqlens, lengths, targets, target_lengths, B,
+                                           max_target_len, blank, (int)reduction, workspace, workspace_bytes, false);
+    if (st != CTC_PACKED_OK) return st;
+    if (grad_log_probs == nullptr || (B > 0 && grad_loss == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(grad_log_probs) % 8 != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(grad_log_probs), l0 = reinterpret_cast<uintptr_t>(log_probs);
+    const uintptr_t nbytes = (uintptr_t)(T_total * (int64_t)D * 8);
+    if (g0 < l0 + nbytes && l0 < g0 + nbytes) return CTC_PACKED_ERR_INVALID_ARGUMENT;  // overlap
+    if (T_total == 0) return CTC_PACKED_OK;
+    F64Args a = f64_args(log_probs, T_total, D, cu_seqlens, lengths, targets, target_lengths, B, max_target_len,
+                         blank, zero_infinity, (int)reduction, workspace);
+    a.grad = grad_log_probs;
+    a.grad_loss = grad_loss;
+    if (B > 0) {
+        int per = 1, nt = 32;
+        chain_shape(max_target_len, per, nt);
+        const int U = max_target_len > 0 ? max_target_len : 1;
+        const size_t smem = (size_t)per * nt * (sizeof(double) + sizeof(int)) + sizeof(double) * (size_t)U +
+                            3 * sizeof(int) * (size_t)U;
+        cudaError_t e;
+        switch (per) {
+            case 1: e = launch_chain_kernel(f64_beta_kernel<1>, (unsigned)B, nt, smem, stream, a); break;
+            case 2: e = launch_chain_kernel(f64_beta_kernel<2>, (unsigned)B, nt, smem, stream, a); break;
+            case 4: e = launch_chain_kernel(f64_beta_kernel<4>, (unsigned)B, nt, smem, stream, a); break;
+            default: e = launch_chain_kernel(f64_beta_kernel<8>, (unsigned)B, nt, smem, stream, a); break;
+        }
+        if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    }
+    if (launch_rows(f64_grad_kernel, T_total, stream, a) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+    return CTC_PACKED_OK;
+}
+
+}  // extern "C"

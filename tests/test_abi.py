@@ -102,6 +102,40 @@ def test_host_argument_checks_return_before_any_cuda_call(lib):
     assert lib.ctc_packed_read_status(None, None, None) == INVALID
 
 
+def _fwd64(lib, **kw):
+    args = dict(lp=8, T=10, D=5, cu=16, ln=24, tg=32, tl=40, B=2, mtl=3, blank=0, zi=0, red=0, loss=48,
+                ws=256, wsb=1 << 30, flags=0, stream=None)
+    args.update(kw)
+    return lib.ctc_packed_forward_f64(args["lp"], args["T"], args["D"], args["cu"], args["ln"], args["tg"],
+                                      args["tl"], args["B"], args["mtl"], args["blank"], args["zi"], args["red"],
+                                      args["loss"], args["ws"], args["wsb"], args["flags"], args["stream"])
+
+
+def test_float64_entry_points_check_before_any_cuda_call(lib):
+    INVALID, WORKSPACE, UNSUPPORTED = 1, 2, 4
+    F64 = 3
+    n = lib.ctc_packed_workspace_size(1000, 4, 50, 30, F64)
+    # alpha rows (12 bytes a state), emissions (16 bytes a label slot) and class sums (8 bytes) per frame
+    assert n >= 1000 * 101 * 12 + 1000 * 51 * 16 + 1000 * 30 * 8
+    assert 0 < lib.ctc_packed_workspace_size_loss_only(1000, 4, 50, 30, F64) < n
+    assert lib.ctc_packed_workspace_size(1000, 4, 3840, 30, F64) == 0
+    assert _fwd(lib, dtype=F64) == INVALID  # the generic entry points take no float64
+    assert _fwd64(lib, lp=12) == INVALID  # misaligned float64 pointer
+    assert _fwd64(lib, loss=None) == INVALID
+    assert _fwd64(lib, red=5) == INVALID
+    assert _fwd64(lib, blank=5) == INVALID
+    assert _fwd64(lib, flags=4) == INVALID
+    assert _fwd64(lib, D=(1 << 20) + 1) == UNSUPPORTED
+    assert _fwd64(lib, mtl=3840) == UNSUPPORTED
+    assert _fwd64(lib, ws=None) == WORKSPACE
+    assert _fwd64(lib, wsb=16) == WORKSPACE
+    b = lib.ctc_packed_backward_f64
+    # grad overlapping log_probs; grad misaligned; no upstream gradient
+    assert b(4096, 10, 5, 16, 24, 32, 40, 2, 3, 0, 0, 0, 48, 256, 1 << 30, 4096 + 40, None) == INVALID
+    assert b(4096, 10, 5, 16, 24, 32, 40, 2, 3, 0, 0, 0, 48, 256, 1 << 30, (1 << 20) + 4, None) == INVALID
+    assert b(4096, 10, 5, 16, 24, 32, 40, 2, 3, 0, 0, 0, None, 256, 1 << 30, 1 << 20, None) == INVALID
+
+
 def test_status_strings(lib):
     for code in range(5):
         assert lib.ctc_packed_status_string(code)
