@@ -579,7 +579,8 @@ def run_fsa(args):
     max_labels = max(1, max(len(set(ed_h[eo_h[i]:eo_h[i + 1], 2].tolist())) for i in range(batch.B)))
     cu, ln = batch.cu_seqlens.to(dev).to(torch.int32), batch.lengths.to(dev).to(torch.int32)
     T_total, D = lp.shape
-    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, batch.B, max_states, max_labels, D), dtype=torch.uint8,
+    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, batch.B, int(fsa_h[1].numel()), int(fsa_h[4].shape[0]),
+                                                      max_states, max_labels, D), dtype=torch.uint8,
                      device=dev)
     loss = torch.empty(batch.B, device=dev)
     g_up = torch.ones(batch.B, device=dev)

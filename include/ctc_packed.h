@@ -326,8 +326,9 @@ ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_d
  *     1 <= states of a sequence <= max_states <= 4096;
  *   - edges [edge_offsets[b], edge_offsets[b+1]) of `edges` (num_edges rows
  *     of int32 (from, to, label), states local to the sequence, label in
- *     [0, D)) with a log weight each in edge_weight; max_labels bounds the
- *     distinct labels of one sequence's edges (more: status bit, zero rows).
+ *     [0, D <= 16384)) with a log weight each in edge_weight; max_labels
+ *     bounds the distinct labels of one sequence's edges (more: the sequence
+ *     is rejected like malformed data: status bit, NaN loss, zero rows).
  * Every edge consumes one frame.  The loss is -log of the sum over all paths
  * of lengths[b] edges of exp(start + edge weights + lp of the edges' labels
  * + final); +inf with no path (0 with zero_infinity).  The backward writes
@@ -335,17 +336,23 @@ ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_d
  * label c), scale_b = grad_loss[b] (0 for an infinite loss), and 0 on rows
  * outside every sequence; the page's gradient convention (the gradient with
  * respect to the logits of a log_softmax).  The recursions run in float32 log
- * space with shared-memory atomics: the last bits depend on the run.
+ * space; every sum runs in a fixed order (each sequence's edges are sorted
+ * once per forward into per-state and per-label lists), so results are
+ * bitwise reproducible.
  *
- * All pointers are device memory.  Errors the host can see return before
+ * All pointers are device memory; log_probs is 4-byte aligned for every
+ * dtype.  Errors the host can see return before
  * anything is enqueued; malformed FSA data or lengths set the status word
  * (ctc_packed_read_status works on this workspace) and a NaN loss.  The
- * workspace holds the status word, each sequence's log-sum, every frame's
- * forward values and, after the backward, each row's class sums; pass it
- * unchanged from the forward to the backward.  The backward writes the dense
- * gradient rows with the CTC path's all-SM gradient stream.
+ * workspace holds the status word, each sequence's log-sum, its sorted edge
+ * lists, every frame's forward values and, after the backward, each row's
+ * class sums; it is sized by ctc_packed_fsa_workspace_size with the same
+ * num_states and num_edges as the calls.  Pass it unchanged from the forward
+ * to the backward.  The backward writes the dense gradient rows with the CTC
+ * path's all-SM gradient stream.
  */
-size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states, int32_t max_labels, int32_t D);
+size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t num_states, int32_t num_edges,
+                                     int32_t max_states, int32_t max_labels, int32_t D);
 ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
                                          const int32_t* cu_seqlens, const int32_t* lengths, int32_t B,
                                          const int32_t* state_offsets, const float* start_weight,

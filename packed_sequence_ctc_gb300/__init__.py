@@ -95,7 +95,7 @@ def load_library(path: Optional[str] = None):
     lib.ctc_packed_forward_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, vp, vp, i32, i32, i32,
                                                ctypes.c_int, ctypes.c_int, vp, vp]
     lib.ctc_packed_forward_noalloc.restype = ctypes.c_int
-    lib.ctc_packed_fsa_workspace_size.argtypes = [i64, i32, i32, i32, i32]
+    lib.ctc_packed_fsa_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32, i32]
     lib.ctc_packed_fsa_workspace_size.restype = sz
     lib.ctc_packed_fsa_forward.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, i32,
                                            i32, i32, ctypes.c_int, vp, vp, sz, vp]
@@ -224,8 +224,12 @@ def ctc_packed_forward_noalloc(log_probs, cu_seqlens, lengths, targets, target_l
             int(bool(zero_infinity)), REDUCTION_CODES[reduction], _ptr(loss), _stream(stream)))
 
 
-def ctc_packed_fsa_workspace_size(T_total: int, B: int, max_states: int, max_labels: int, D: int) -> int:
-    return int(load_library().ctc_packed_fsa_workspace_size(T_total, B, max_states, max_labels, D))
+def ctc_packed_fsa_workspace_size(T_total: int, B: int, num_states: int, num_edges: int, max_states: int,
+                                  max_labels: int, D: int) -> int:
+    """Workspace bytes of the FSA calls; num_states and num_edges are the
+    totals over the batch (start_weight entries and edge rows)."""
+    return int(load_library().ctc_packed_fsa_workspace_size(T_total, B, num_states, num_edges, max_states,
+                                                            max_labels, D))
 
 
 def _fsa_args(log_probs, cu_seqlens, lengths, fsa):

@@ -19,15 +19,26 @@
 //   beta_T(s) = final(s),   beta_t(s) = logsumexp_{e=(s,s',c,w)} w + lp[t, c] + beta_{t+1}(s')
 //   grad[t, c] = scale * (exp(lp[t, c]) - sum_{e with label c} exp(alpha_t(s) + w + lp[t, c] + beta_{t+1}(s') - Z))
 //
-// One CTA per sequence walks its frames; the states' values sit in shared
-// memory in float32 log space and each frame's log-sum-exp over the edges
-// into a state is two passes over the edges: an atomic maximum (on an
-// order-preserving integer key), then an atomic sum of exp(v - max).  The
-// shared-memory atomics make the summation order, and so the last bits,
-// run-dependent (as the page's own label scatter is).  The forward stores
-// alpha_t of every frame in the workspace; the backward runs beta, forms the
-// edge occupancies, sums them per class in a shared row of D values and
-// writes each gradient row densely, in the log probabilities' dtype.
+// Every sum runs in a fixed order, so results are bitwise reproducible:
+//   index    one CTA per sequence, once per forward: the edges sorted stably
+//            (counting sort; ties keep the edge order) by destination, by
+//            source and by label, as per-state and per-label lists; the
+//            sequence's distinct labels (at most max_labels) in increasing
+//            order, and each edge's slot among them.
+//   forward  one CTA per sequence, a thread per destination state (or a
+//            few): alpha_{t+1}(s') is a running log-sum-exp over the state's
+//            incoming edges in list order.  The label values of frame t + 1
+//            load during frame t; one barrier per frame.  Each frame's
+//            values are shifted by their maximum (the running shift is kept
+//            by one thread, stored as a float pair), so their float32
+//            rounding stays relative to the frame; alpha_t is stored for the
+//            backward with its shift.
+//   backward one CTA per sequence, a thread per source state: beta_t(s)
+//            over the state's outgoing edges in list order, each edge's
+//            occupancy into a double-buffered per-edge array, then after the
+//            frame's barrier the class sums, each label's edges in list
+//            order; the dense rows are written by the CTC path's all-SM
+//            gradient stream from the rows' class sums.
 #include <cstdint>
 
 #include "ctc_common.cuh"
@@ -37,37 +48,50 @@ namespace ctcp {
 
 namespace {
 
-constexpr int kFsaThreads = 256;
-// Edges a thread keeps in registers (its edges tid, tid + 256, ...): their
-// ids, weight and the label values of this frame and the next, which load
-// while the frame's barriers run.  A sequence's further edges are read from
-// memory each frame.
-constexpr int kFsaRegEdges = 4;
+constexpr int kIdxThreads = 256;      // threads of the index kernel
+constexpr int kFsaMaxThreads = 512;   // threads of a recursion CTA (states per thread <= 8)
+constexpr int kRing = 4;              // frames of label values (and alpha rows) in flight: kRing - 1 ahead
+constexpr int kFsaSmemBudget = 200 * 1024;  // shared memory of a recursion CTA
+constexpr int kShortList = 8;         // label lists up to this long are summed by one thread, longer by a warp
 
-// Workspace of the FSA path: status header, log Z per sequence (double),
-// each frame's forward values relative to the frame's own offset (float)
-// and that offset (double).
+// Workspace of the FSA path.  Per sequence: log Z (double) and the number of
+// distinct labels (-1: the sequence was rejected); per frame: the forward
+// values relative to the frame's shift (float) and that shift as an
+// unevaluated float pair hi + lo (about 48 bits: the recursions keep float64
+// arithmetic, slow on this part, out of their per-frame path); per
+// row: the class-sum header and sums read by the gradient stream; per state:
+// offsets of its incoming and outgoing edge lists; per edge: the records of
+// both lists, the label lists and the occupancies of two frames.
 struct FsaLayout {
-    size_t off_z, off_coff, off_alpha, off_head, off_ent, total;
-    int cap;  // class sums a row can hold: min(max_labels, D)
+    size_t off_z, off_nlab, off_coff, off_alpha, off_head, off_ent;
+    size_t off_inoff, off_outoff, off_rin, off_rout, off_elab, off_tmp, off_labs, off_laboff, off_occ, total;
+    int cap;       // class sums a row can hold: min(max_labels, D)
+    int E_total;   // edges of all sequences (the occupancy buffers' stride)
 };
-__host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int32_t max_states, int32_t max_labels,
-                                                int32_t D) {
+__host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int32_t S_total, int32_t E_total,
+                                                int32_t max_states, int32_t max_labels, int32_t D) {
     FsaLayout L{};
     L.cap = max_labels < D ? max_labels : D;
+    L.E_total = E_total;
+    const size_t Bn = (size_t)(B > 0 ? B : 1), cap = (size_t)(L.cap > 0 ? L.cap : 1);
     size_t o = 256;  // the status word sits at offset 0, as in the CTC workspace
-    L.off_z = o;
-    o = align_up(o + sizeof(double) * (size_t)(B > 0 ? B : 1), 256);
-    L.off_coff = o;
-    o = align_up(o + sizeof(double) * (size_t)T_total, 256);
-    L.off_alpha = o;
-    o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)max_states, 256);
+    L.off_z = o;      o = align_up(o + sizeof(double) * Bn, 256);
+    L.off_nlab = o;   o = align_up(o + sizeof(int32_t) * Bn, 256);
+    L.off_coff = o;   o = align_up(o + sizeof(double) * (size_t)T_total, 256);
+    L.off_alpha = o;  o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)max_states, 256);
     // per row: a header and the row's class sums, in the format the dense
     // gradient stream of the CTC path reads
-    L.off_head = o;
-    o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
-    L.off_ent = o;
-    o = align_up(o + 8 * (size_t)T_total * (size_t)(L.cap > 0 ? L.cap : 1), 256);
+    L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
+    L.off_ent = o;    o = align_up(o + 8 * (size_t)T_total * cap, 256);
+    L.off_inoff = o;  o = align_up(o + sizeof(int32_t) * ((size_t)S_total + Bn), 256);
+    L.off_outoff = o; o = align_up(o + sizeof(int32_t) * ((size_t)S_total + Bn), 256);
+    L.off_rin = o;    o = align_up(o + sizeof(int4) * (size_t)E_total, 256);
+    L.off_rout = o;   o = align_up(o + sizeof(int4) * (size_t)E_total, 256);
+    L.off_elab = o;   o = align_up(o + sizeof(int32_t) * (size_t)E_total, 256);
+    L.off_tmp = o;    o = align_up(o + sizeof(int32_t) * (size_t)E_total, 256);
+    L.off_labs = o;   o = align_up(o + sizeof(int32_t) * Bn * cap, 256);
+    L.off_laboff = o; o = align_up(o + sizeof(int32_t) * Bn * (cap + 1), 256);
+    L.off_occ = o;    o = align_up(o + sizeof(float) * 2 * (size_t)E_total, 256);
     L.total = o;
     return L;
 }
@@ -94,16 +118,9 @@ struct FsaArgs {
     const float* grad_loss;
     void* grad;
     void* ws;
+    int ecap_smem;  // a recursion CTA keeps a sequence's edge lists in shared memory up to this many edges
     FsaLayout L;
 };
-
-// Order-preserving map of a float onto a signed int (and back), so that an
-// integer atomic maximum is a float maximum.
-__device__ __forceinline__ int fkey(float f) {
-    const int b = __float_as_int(f);
-    return b >= 0 ? b : b ^ 0x7fffffff;
-}
-__device__ __forceinline__ float fdekey(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
 
 template <int DT>
 __device__ __forceinline__ float lp_at(const void* lp, int64_t idx) {
@@ -116,7 +133,7 @@ __device__ __forceinline__ float lp_at(const void* lp, int64_t idx) {
 
 // Checks sequence b's sizes and edges; returns false (and flags the status)
 // when the sequence cannot be run.
-__device__ bool fsa_check(const FsaArgs& a, int b, int S, int e0, int E, int64_t start, int T, bool& bad_label) {
+__device__ bool fsa_check(const FsaArgs& a, int b, int S, int e0, int E, int64_t start, int T) {
     Control* ctrl = ws_at<Control>(a.ws, 0);
     __shared__ int s_bad;
     if (threadIdx.x == 0) s_bad = 0;
@@ -143,38 +160,85 @@ __device__ bool fsa_check(const FsaArgs& a, int b, int S, int e0, int E, int64_t
         set_status(ctrl, (bad & 1 ? CTC_PACKED_DEV_BAD_FSA : 0u) | (bad & 2 ? CTC_PACKED_DEV_LABEL_OUT_OF_RANGE : 0u) |
                              (bad & 4 ? CTC_PACKED_DEV_BAD_LENGTH : 0u));
     }
-    bad_label = bad != 0;
     return bad == 0;
 }
 
-// Block-wide maximum of v[0 .. n).
-__device__ float block_max(const float* v, int n, float* red) {
-    float m = -INFINITY;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, v[i]);
+// Exclusive scan of one value per thread over the CTA; the CTA total goes to
+// *total.
+__device__ int fsa_block_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    m = -INFINITY;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
-    __syncthreads();
-    return m;
-}
-
-// Shifts v[0 .. n) down by its maximum (when finite) and returns the shift:
-// the recursions keep every frame's values near 0, so their float32 rounding
-// stays relative to the frame, and carry the shifts in double.
-__device__ float renormalise(float* v, int n, float* red) {
-    const float m = block_max(v, n, red);
-    if (m > -INFINITY && m < INFINITY) {
-        for (int i = threadIdx.x; i < n; i += blockDim.x) v[i] -= m;
-        __syncthreads();
-        return m;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    return 0.0f;
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int prefix = x - v + (warp > 0 ? s_warp[warp - 1] : 0);
+    *total = s_warp[nw - 1];
+    __syncthreads();
+    return prefix;
 }
 
-// Block-wide logsumexp of v[0 .. n) (one value per thread slot, strided).
+// cnt[0 .. K) becomes the exclusive prefix of itself (also written to
+// off_out[0 .. K] when given, off_out[K] = the total); returns the total.
+__device__ int scan_counts(int* cnt, int K, int* s_warp, int* off_out) {
+    int run = 0;
+    for (int k0 = 0; k0 < K; k0 += blockDim.x) {
+        const int k = k0 + threadIdx.x;
+        const int v = k < K ? cnt[k] : 0;
+        int total;
+        const int pre = fsa_block_scan(v, s_warp, &total);
+        if (k < K) {
+            cnt[k] = run + pre;
+            if (off_out != nullptr) off_out[k] = run + pre;
+        }
+        run += total;
+    }
+    if (off_out != nullptr && threadIdx.x == 0) off_out[K] = run;
+    __syncthreads();
+    return run;
+}
+
+// Places edge e at cursor[key(e)]++ in edge order (a stable counting sort's
+// last pass): the CTA walks the edges one warp at a time; inside a warp the
+// lanes with equal keys take consecutive slots in lane order.
+template <typename KeyF>
+__device__ void place_stable(int E, KeyF key, int* cursor, int* out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int c0 = 0; c0 < E; c0 += blockDim.x) {
+        for (int w = 0; w < nw; ++w) {
+            if (warp == w) {
+                const int e = c0 + threadIdx.x;
+                const bool on = e < E;
+                const int k = on ? key(e) : -1;
+                const unsigned peers = __match_any_sync(0xffffffffu, k);
+                const int leader = __ffs(peers) - 1;
+                int base = 0;
+                if (on && lane == leader) {
+                    base = cursor[k];
+                    cursor[k] = base + __popc(peers);
+                }
+                base = __shfl_sync(0xffffffffu, base, leader);
+                if (on) out[base + __popc(peers & ((1u << lane) - 1u))] = e;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Block-wide logsumexp of v[0 .. n) + w[0 .. n), fixed order.
 __device__ float block_lse(const float* v, const float* w, int n, float* red) {
     float m = -INFINITY;
     for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, v[i] + w[i]);
@@ -198,97 +262,386 @@ __device__ float block_lse(const float* v, const float* w, int n, float* red) {
     return m > -INFINITY ? m + logf(s) : -INFINITY;
 }
 
+// Running log-sum-exp (m, s): the sum is s * exp(m); -inf terms are skipped.
+__device__ __forceinline__ void lse_push(float& m, float& s, float v) {
+    if (!(v > -INFINITY)) return;
+    if (v > m) {
+        s = s * expf(m - v) + 1.0f;
+        m = v;
+    } else {
+        s += expf(v - m);
+    }
+}
+__device__ __forceinline__ float lse_value(float m, float s) { return s > 0.0f ? m + logf(s) : -INFINITY; }
+
+// Error-free sum (Knuth's TwoSum): a + b = s + err exactly, in float32.
+__device__ __forceinline__ float two_sum(float a, float b, float& err) {
+    const float s = a + b;
+    const float bb = s - a;
+    err = (a - (s - bb)) + (b - bb);
+    return s;
+}
+
+// Maximum over the warp maxima of the CTA (what the last barrier published),
+// every warp reducing the nw values by shuffles.
+__device__ __forceinline__ float max_of(const float* wmax, int nw) {
+    const int lane = threadIdx.x & 31;
+    float m = lane < nw ? wmax[lane] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return m;
+}
+
 }  // namespace
 
-template <int DT>
-__global__ void __launch_bounds__(kFsaThreads) fsa_forward_kernel(FsaArgs a) {
-    extern __shared__ __align__(16) float fsa_smem[];
-    __shared__ float red[kFsaThreads / 32];
+// Sorted edge lists of sequence b (see the file comment).  A sequence that
+// fails its checks, or has more distinct labels than max_labels, gets a NaN
+// loss and nlab = -1: the recursions skip it and its rows stay zero.
+__global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
+    extern __shared__ __align__(16) int idx_smem[];
+    __shared__ int s_warp[32];
     const int b = blockIdx.x;
     const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
     const int e0 = a.edge_offsets[b], E = a.edge_offsets[b + 1] - e0;
     const int64_t start = a.cu[b];
     const int T = a.lengths[b];
+    int* nlab_out = ws_at<int32_t>(a.ws, a.L.off_nlab);
     double* z_out = ws_at<double>(a.ws, a.L.off_z);
-    double* coff = ws_at<double>(a.ws, a.L.off_coff);
-    bool bad = false;
-    if (!fsa_check(a, b, S, e0, E, start, T, bad)) {
+    auto reject = [&]() {
         if (threadIdx.x == 0) {
+            nlab_out[b] = -1;
             z_out[b] = __longlong_as_double(0x7ff8000000000000ll);
             a.loss[b] = __int_as_float(0x7fc00000);
         }
+    };
+    if (!fsa_check(a, b, S, e0, E, start, T)) {
+        reject();
         return;
     }
-    float* al = fsa_smem;                                   // alpha_t
-    int* mk = reinterpret_cast<int*>(fsa_smem + a.max_states);  // max key per state
-    float* sm = fsa_smem + 2 * a.max_states;                // sum per state
-    float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
-    int efr[kFsaRegEdges], eto[kFsaRegEdges], elab[kFsaRegEdges];
-    float ew[kFsaRegEdges], lpc[kFsaRegEdges], lpn[kFsaRegEdges], ev[kFsaRegEdges];
-#pragma unroll
-    for (int k = 0; k < kFsaRegEdges; ++k) {
-        const int e = threadIdx.x + k * kFsaThreads;
-        const bool on = e < E;
-        const int* ed = a.edges + 3 * (size_t)(e0 + (on ? e : 0));
-        efr[k] = on ? ed[0] : 0;
-        eto[k] = on ? ed[1] : 0;
-        elab[k] = on ? ed[2] : 0;
-        ew[k] = on ? a.edge_weight[e0 + e] : -INFINITY;  // an absent edge never contributes
-        lpc[k] = (on && T > 0) ? lp_at<DT>(a.lp, start * (int64_t)a.D + elab[k]) : 0.0f;
-        lpn[k] = 0.0f;
-    }
-    const int e_reg = kFsaRegEdges * kFsaThreads;  // edges from here on are read each frame
-    for (int s = threadIdx.x; s < S; s += blockDim.x) al[s] = a.start_weight[s0 + s];
+    const int D = a.D, cap = a.L.cap;
+    int* cnt = idx_smem;         // max(S, D) counters
+    int* slot = idx_smem + (S > D ? S : D);  // label -> slot among the distinct labels, D entries
+    const int* ed = a.edges + 3 * (size_t)e0;
+    const float* ew = a.edge_weight + e0;
+    int* tmp = ws_at<int32_t>(a.ws, a.L.off_tmp) + e0;
+
+    // 1. labels: counts, the distinct ones in increasing order, their lists
+    for (int c = threadIdx.x; c < D; c += blockDim.x) cnt[c] = 0;
     __syncthreads();
-    double C = renormalise(al, S, red);  // alpha_t = al + C
-    bool nan_seen = false;               // a NaN edge value: the loss is NaN
-    for (int t = 0; t < T; ++t) {
-        float* row = alpha_rows + (start + t) * (int64_t)a.max_states;
-        if (threadIdx.x == 0) coff[start + t] = C;
-        for (int s = threadIdx.x; s < S; s += blockDim.x) {
-            row[s] = al[s];
-            mk[s] = fkey(-INFINITY);
-            sm[s] = 0.0f;
-        }
-        __syncthreads();
-        const int64_t lrow = (start + t) * (int64_t)a.D;
-#pragma unroll
-        for (int k = 0; k < kFsaRegEdges; ++k) {
-            ev[k] = al[efr[k]] + ew[k] + lpc[k];
-            nan_seen |= ev[k] != ev[k];
-            if (ev[k] > -INFINITY) atomicMax(&mk[eto[k]], fkey(ev[k]));
-        }
-        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
-            const int* ed = a.edges + 3 * (size_t)(e0 + e);
-            const float v = al[ed[0]] + a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]);
-            nan_seen |= v != v;
-            if (v > -INFINITY) atomicMax(&mk[ed[1]], fkey(v));
-        }
-        if (t + 1 < T) {  // the next frame's label values, in flight across the barriers
-#pragma unroll
-            for (int k = 0; k < kFsaRegEdges; ++k)
-                if (threadIdx.x + k * kFsaThreads < E) lpn[k] = lp_at<DT>(a.lp, lrow + a.D + elab[k]);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < kFsaRegEdges; ++k)
-            if (ev[k] > -INFINITY) atomicAdd(&sm[eto[k]], expf(ev[k] - fdekey(mk[eto[k]])));
-        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
-            const int* ed = a.edges + 3 * (size_t)(e0 + e);
-            const float v = al[ed[0]] + a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]);
-            if (v > -INFINITY) atomicAdd(&sm[ed[1]], expf(v - fdekey(mk[ed[1]])));
-        }
-        __syncthreads();
-        for (int s = threadIdx.x; s < S; s += blockDim.x)
-            al[s] = sm[s] > 0.0f ? fdekey(mk[s]) + logf(sm[s]) : (sm[s] != sm[s] ? sm[s] : -INFINITY);
-        __syncthreads();
-        C += renormalise(al, S, red);
-#pragma unroll
-        for (int k = 0; k < kFsaRegEdges; ++k) lpc[k] = lpn[k];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) atomicAdd(&cnt[ed[3 * e + 2]], 1);
+    __syncthreads();
+    int nlab = 0;
+    for (int c0 = 0; c0 < D; c0 += blockDim.x) {
+        const int c = c0 + threadIdx.x;
+        const int f = c < D && cnt[c] > 0 ? 1 : 0;
+        int total;
+        const int pre = fsa_block_scan(f, s_warp, &total);
+        if (c < D) slot[c] = nlab + pre;
+        nlab += total;
     }
-    const float zr = block_lse(al, a.final_weight + s0, S, red);
+    if (nlab > cap) {
+        if (threadIdx.x == 0) set_status(ws_at<Control>(a.ws, 0), CTC_PACKED_DEV_BAD_FSA);
+        reject();
+        return;
+    }
+    int* labs = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
+    int* laboff = ws_at<int32_t>(a.ws, a.L.off_laboff) + (size_t)b * (cap + 1);
+    for (int c = threadIdx.x; c < D; c += blockDim.x)
+        if (cnt[c] > 0) labs[slot[c]] = c;
+    scan_counts(cnt, D, s_warp, nullptr);  // cnt[c]: first list position of label c
+    // the distinct labels' list offsets: label c's list starts at cnt[c]
+    for (int i = threadIdx.x; i < nlab; i += blockDim.x) laboff[i] = cnt[labs[i]];
+    if (threadIdx.x == 0) laboff[nlab] = E;
+    __syncthreads();
+    place_stable(E, [&](int e) { return ed[3 * e + 2]; }, cnt, ws_at<int32_t>(a.ws, a.L.off_elab) + e0);
+
+    // 2. incoming lists (by destination): records (from, label slot, weight, edge)
+    int* inoff = ws_at<int32_t>(a.ws, a.L.off_inoff) + s0 + b;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) cnt[s] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) atomicAdd(&cnt[ed[3 * e + 1]], 1);
+    __syncthreads();
+    scan_counts(cnt, S, s_warp, inoff);
+    place_stable(E, [&](int e) { return ed[3 * e + 1]; }, cnt, tmp);
+    int4* rin = ws_at<int4>(a.ws, a.L.off_rin) + e0;
+    for (int k = threadIdx.x; k < E; k += blockDim.x) {
+        const int e = tmp[k];
+        rin[k] = make_int4(ed[3 * e], slot[ed[3 * e + 2]], __float_as_int(ew[e]), e);
+    }
+    __syncthreads();
+
+    // 3. outgoing lists (by source): records (to, label slot, weight, edge)
+    int* outoff = ws_at<int32_t>(a.ws, a.L.off_outoff) + s0 + b;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) cnt[s] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) atomicAdd(&cnt[ed[3 * e]], 1);
+    __syncthreads();
+    scan_counts(cnt, S, s_warp, outoff);
+    place_stable(E, [&](int e) { return ed[3 * e]; }, cnt, tmp);
+    int4* rout = ws_at<int4>(a.ws, a.L.off_rout) + e0;
+    for (int k = threadIdx.x; k < E; k += blockDim.x) {
+        const int e = tmp[k];
+        rout[k] = make_int4(ed[3 * e + 1], slot[ed[3 * e + 2]], __float_as_int(ew[e]), e);
+    }
+    if (threadIdx.x == 0) nlab_out[b] = nlab;
+}
+
+// Shared-memory plan of a recursion CTA (see FsaArgs::ecap_smem): the
+// sequence's edge lists when it has at most ecap_smem edges, then the
+// per-frame buffers.
+struct FsaSmem {
+    int4* rec;        // edge records of the list (incoming or outgoing), ecap_smem
+    int* off;         // list offsets per state, Smax + 1
+    int* elab;        // (backward) edge ids by label, ecap_smem
+    float* occ;       // (backward) occupancies of two frames, 2 * ecap_smem
+    float* val;       // alpha or beta of two frames, 2 * Smax
+    int* longl;       // (backward) the labels with long edge lists, cap
+    uint32_t* ring;   // words holding the label values of kRing frames, kRing * cap
+    float* aring;     // (backward) stored alpha rows of kRing frames, kRing * Smax
+    float2* cring;    // (backward) the stored rows' shifts of kRing frames (float pairs)
+    int* labs;        // the distinct labels, cap
+    int* laboff;      // (backward) label list offsets, cap + 1
+};
+__host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Smax, int cap, unsigned char* base,
+                                                FsaSmem* out) {
+    size_t o = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        o = align_up(o, align);
+        const size_t at = o;
+        o += bytes;
+        return at;
+    };
+    const size_t rec = take(16 * (size_t)ecap, 16);
+    const size_t off = take(4 * ((size_t)Smax + 1), 4);
+    const size_t elab = backward ? take(4 * (size_t)ecap, 4) : 0;
+    const size_t occ = backward ? take(8 * (size_t)ecap, 4) : 0;
+    const size_t val = take(8 * (size_t)Smax, 4);
+    const size_t longl = backward ? take(4 * (size_t)cap, 4) : 0;
+    const size_t ring = take(4 * (size_t)kRing * cap, 4);
+    const size_t aring = backward ? take(4 * (size_t)kRing * Smax, 4) : 0;
+    const size_t cring = backward ? take(8 * (size_t)kRing, 8) : 0;
+    const size_t labs = take(4 * (size_t)cap, 4);
+    const size_t laboff = backward ? take(4 * ((size_t)cap + 1), 4) : 0;
+    if (out != nullptr) {
+        out->rec = reinterpret_cast<int4*>(base + rec);
+        out->off = reinterpret_cast<int*>(base + off);
+        out->elab = reinterpret_cast<int*>(base + elab);
+        out->occ = reinterpret_cast<float*>(base + occ);
+        out->val = reinterpret_cast<float*>(base + val);
+        out->longl = reinterpret_cast<int*>(base + longl);
+        out->ring = reinterpret_cast<uint32_t*>(base + ring);
+        out->aring = reinterpret_cast<float*>(base + aring);
+        out->cring = reinterpret_cast<float2*>(base + cring);
+        out->labs = reinterpret_cast<int*>(base + labs);
+        out->laboff = reinterpret_cast<int*>(base + laboff);
+    }
+    return align_up(o, 16);
+}
+
+namespace {
+
+// Starts the copy of the aligned 32-bit word that holds element idx of the
+// log probabilities into *dst (row_flip and the label's parity say which
+// half is the element).
+// The buffer starts 4-byte aligned; only its last element of a 2-byte type
+// can end a word that would reach past the buffer, and that one is read
+// directly into the word's low half.
+template <int DT>
+__device__ __forceinline__ void fetch_word(uint32_t* dst, const void* lp, int64_t idx, uintptr_t lp_end) {
+    constexpr int E = DT == 0 ? 4 : 2;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(lp) + (uintptr_t)idx * E;
+    const uintptr_t w = addr & ~uintptr_t(3);
+    if (w + 4 <= lp_end) {
+        cp_async4(smem_addr(dst), reinterpret_cast<const void*>(w));
+    } else {
+        *dst = (uint32_t)*reinterpret_cast<const unsigned short*>(addr);
+    }
+}
+
+}  // namespace
+
+// Edges of a state held in registers across the frames (the first RE of
+// its list; a CTC lattice has at most three per state), and where the rest
+// of its list lies.
+template <int PER, int RE>
+struct EdgeRegs {
+    int peer[PER][RE];   // the other state of each edge (source forward, destination backward)
+    int slot[PER][RE];   // its label's slot among the sequence's distinct labels
+    float w[PER][RE];    // its log weight
+    int id[PER][RE];     // its edge id (backward: the occupancy's index)
+    int par[PER][RE];    // parity of its label's element in a row starting on a word (2-byte types)
+    int n[PER];          // edges held (at most RE)
+    int k0[PER], k1[PER];  // the rest of the list: entries [k0, k1)
+};
+
+template <int PER, int RE>
+__device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int* off, const int4* rec, int S,
+                                               const int* labs, int base_half) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int s = threadIdx.x + k * blockDim.x;
+        int b0 = 0, b1 = 0;
+        if (s < S) {
+            b0 = off[s];
+            b1 = off[s + 1];
+        }
+        const int n = min(b1 - b0, RE);
+        er.n[k] = n;
+        er.k0[k] = b0 + n;
+        er.k1[k] = b1;
+#pragma unroll
+        for (int j = 0; j < RE; ++j) {
+            const int4 r = j < n ? rec[b0 + j] : make_int4(0, 0, 0, 0);
+            er.peer[k][j] = r.x;
+            er.slot[k][j] = r.y;
+            er.w[k][j] = __int_as_float(r.z);
+            er.id[k][j] = r.w;
+            er.par[k][j] = (base_half ^ labs[r.y]) & 1;
+        }
+    }
+}
+
+// Which half of its 32-bit word holds a label's element of a 2-byte type in
+// row `row`: the parity of the element's position (row * D + label) plus
+// the buffer's own; `par` is the row-independent part (base ^ label).
+__device__ __forceinline__ int row_flip(int64_t row, int D) { return (int)(row & (int64_t)D) & 1; }
+
+// Starts the copies of the words holding labels labs[0 .. nlab) of row
+// `row` (thread i % nt copies label i).  Only the buffer's last row can hold
+// an element whose word would reach past the buffer.
+template <int DT>
+__device__ __forceinline__ void issue_row(uint32_t* dst, const void* lp, int64_t row, int D, int64_t T_total,
+                                          const int* labs, int nlab, uintptr_t lp_end) {
+    constexpr int E = DT == 0 ? 4 : 2;
+    if (DT == 0 || row + 1 < T_total) {
+        const uintptr_t rp = reinterpret_cast<uintptr_t>(lp) + (uintptr_t)(row * (int64_t)D) * E;
+        for (int i = threadIdx.x; i < nlab; i += blockDim.x)
+            cp_async4(smem_addr(dst + i), reinterpret_cast<const void*>((rp + (uintptr_t)labs[i] * E) & ~uintptr_t(3)));
+    } else {
+        for (int i = threadIdx.x; i < nlab; i += blockDim.x) fetch_word<DT>(dst + i, lp, row * (int64_t)D + labs[i], lp_end);
+    }
+}
+
+template <int DT, int PER>
+__global__ void __launch_bounds__(kFsaMaxThreads) fsa_forward_kernel(FsaArgs a) {
+    constexpr int RE = PER <= 2 ? 3 : (PER == 4 ? 2 : 1);
+    extern __shared__ __align__(16) unsigned char fsa_smem[];
+    __shared__ float wmax[2][kFsaMaxThreads / 32];
+    __shared__ float red[kFsaMaxThreads / 32];
+    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
+    const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
+    if (nlab < 0) return;  // rejected by the index pass (NaN loss written there)
+    const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
+    const int e0 = a.edge_offsets[b], E = a.edge_offsets[b + 1] - e0;
+    const int64_t start = a.cu[b];
+    const int T = a.lengths[b];
+    const int Smax = a.max_states, cap = a.L.cap, D = a.D;
+    FsaSmem sm;
+    fsa_smem_plan(false, a.ecap_smem, Smax, cap, fsa_smem, &sm);
+    const int* inoff_g = ws_at<int32_t>(a.ws, a.L.off_inoff) + s0 + b;
+    const int4* rin_g = ws_at<int4>(a.ws, a.L.off_rin) + e0;
+    const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
+    double* z_out = ws_at<double>(a.ws, a.L.off_z);
+    float2* coff = ws_at<float2>(a.ws, a.L.off_coff);
+    float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
+    const uintptr_t lp0 = reinterpret_cast<uintptr_t>(a.lp);
+    const uintptr_t lp_end = lp0 + (uintptr_t)(a.T_total * (int64_t)D * (DT == 0 ? 4 : 2));
+    const int base_half = (int)((lp0 >> 1) & 1);
+
+    // the sequence's incoming lists into shared memory when they fit
+    const bool local = E <= a.ecap_smem;
+    if (local) {
+        for (int k = tid; k < E; k += nt) sm.rec[k] = rin_g[k];
+        for (int s = tid; s <= S; s += nt) sm.off[s] = inoff_g[s];
+    }
+    const int4* rin = local ? sm.rec : rin_g;
+    const int* inoff = local ? sm.off : inoff_g;
+    for (int i = tid; i < nlab; i += nt) sm.labs[i] = labs_g[i];
+    // label values: the words of frames 0 .. kRing - 2 in flight (thread
+    // i % nt copies label i); a frame's words are read where they land
+    auto issue = [&](int f) {
+        if (f < T) issue_row<DT>(sm.ring + (f % kRing) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
+        cp_async_commit();
+    };
+    for (int f = 0; f < kRing - 1; ++f) issue(f);
+    float tm = -INFINITY;
+    for (int s = tid; s < S; s += nt) {
+        const float v = a.start_weight[s0 + s];
+        sm.val[s] = v;
+        tm = fmaxf(tm, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+    if ((tid & 31) == 0) wmax[0][tid >> 5] = tm;
+    cp_async_wait<kRing - 2>();
+    __syncthreads();
+    EdgeRegs<PER, RE> er;
+    load_edge_regs(er, inoff, rin, S, sm.labs, base_half);
+    float c_hi = 0.0f, c_lo = 0.0f;  // the running shift C, a float pair (thread 0 stores it)
+    bool nan_seen = false;  // a NaN edge value: the loss is NaN
+    int p = 0;
+    for (int t = 0; t < T; ++t) {
+        issue(t + kRing - 1);
+        const float* alp = sm.val + p * Smax;
+        float* alq = sm.val + (p ^ 1) * Smax;
+        const uint32_t* lw = sm.ring + (t % kRing) * cap;  // the frame's label words
+        const int flip = row_flip(start + t, D);
+        // the frame's shift: alpha_t is stored relative to C
+        const float m = max_of(wmax[p], nw);
+        const float sh = (m > -INFINITY && m < INFINITY) ? m : 0.0f;
+        {
+            float e;
+            c_hi = two_sum(c_hi, sh, e);
+            c_lo += e;
+        }
+        if (tid == 0) coff[start + t] = make_float2(c_hi, c_lo);
+        float* row = alpha_rows + (start + t) * (int64_t)Smax;
+        tm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            if (s < S) {
+                row[s] = alp[s] - sh;
+                // the held edges: maximum first, then the sum of exp(v - max)
+                float v[RE], lm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < RE; ++j) {
+                    v[j] = j < er.n[k] ? alp[er.peer[k][j]] + er.w[k][j] +
+                                             word_to_float<DT>(lw[er.slot[k][j]], er.par[k][j] ^ flip) - sh
+                                       : -INFINITY;
+                    nan_seen |= v[j] != v[j];
+                    lm = fmaxf(lm, v[j]);
+                }
+                float ls = 0.0f;
+                if (lm > -INFINITY) {
+#pragma unroll
+                    for (int j = 0; j < RE; ++j) ls += expf(v[j] - lm);
+                }
+                // the rest of the list, in order
+                for (int kk = er.k0[k]; kk < er.k1[k]; ++kk) {
+                    const int4 r = rin[kk];
+                    const float lv = word_to_float<DT>(lw[r.y], ((base_half ^ sm.labs[r.y]) & 1) ^ flip);
+                    const float vv = alp[r.x] - sh + __int_as_float(r.z) + lv;
+                    nan_seen |= vv != vv;
+                    lse_push(lm, ls, vv);
+                }
+                const float nv = lse_value(lm, ls);
+                alq[s] = nv;
+                tm = fmaxf(tm, nv);
+            }
+        }
+        cp_async_wait<kRing - 2>();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+        if ((tid & 31) == 0) wmax[p ^ 1][tid >> 5] = tm;
+        __syncthreads();
+        p ^= 1;
+    }
+    cp_async_wait<0>();
+    const float zr = block_lse(sm.val + p * Smax, a.final_weight + s0, S, red);
     const bool any_nan = __syncthreads_or(nan_seen) != 0;
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
+        const double C = (double)c_hi + (double)c_lo;
         const double Z = any_nan ? __longlong_as_double(0x7ff8000000000000ll)
                                  : (zr > -INFINITY ? C + (double)zr : (double)zr);
         z_out[b] = Z;
@@ -298,140 +651,212 @@ __global__ void __launch_bounds__(kFsaThreads) fsa_forward_kernel(FsaArgs a) {
     }
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kFsaThreads) fsa_backward_kernel(FsaArgs a) {
-    extern __shared__ __align__(16) float fsa_smem[];
-    __shared__ float red[kFsaThreads / 32];
-    __shared__ int s_nlab;
-    const int b = blockIdx.x;
+template <int DT, int PER>
+__global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a) {
+    constexpr int RE = PER <= 2 ? 3 : (PER == 4 ? 2 : 1);
+    extern __shared__ __align__(16) unsigned char fsa_smem[];
+    __shared__ float wmax[2][kFsaMaxThreads / 32];
+    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5, warp = tid >> 5, lane = tid & 31;
+    const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
+    if (nlab < 0) return;  // the rows keep zero headers: zero gradient
     const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
     const int e0 = a.edge_offsets[b], E = a.edge_offsets[b + 1] - e0;
     const int64_t start = a.cu[b];
     const int T = a.lengths[b];
+    const int Smax = a.max_states, cap = a.L.cap, D = a.D;
     const double Z = ws_at<double>(a.ws, a.L.off_z)[b];
-    const double* coff = ws_at<double>(a.ws, a.L.off_coff);
-    bool bad = false;
-    if (!fsa_check(a, b, S, e0, E, start, T, bad)) return;  // the rows keep zero headers: zero gradient
+    const float2* coff = ws_at<float2>(a.ws, a.L.off_coff);
     float scale = a.grad_loss[b];
     if (!(Z > -INFINITY)) scale = 0.0f;  // no path: zero rows (defined only with zero_infinity)
-    float* be = fsa_smem;                                   // beta_{t+1}
-    int* mk = reinterpret_cast<int*>(fsa_smem + a.max_states);
-    float* sm = fsa_smem + 2 * a.max_states;
-    float* P = fsa_smem + 3 * a.max_states;                 // class occupancies of the frame, D values
-    int* labs = reinterpret_cast<int*>(P + a.D);            // the sequence's distinct labels, cap entries
-    const int cap = a.L.cap;
+    // -Z as a float pair, once
+    const float nz_hi = (float)-Z, nz_lo = (float)(-Z - (double)nz_hi);
+    FsaSmem sm;
+    fsa_smem_plan(true, a.ecap_smem, Smax, cap, fsa_smem, &sm);
+    const int* outoff_g = ws_at<int32_t>(a.ws, a.L.off_outoff) + s0 + b;
+    const int4* rout_g = ws_at<int4>(a.ws, a.L.off_rout) + e0;
+    const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
+    const int* laboff_g = ws_at<int32_t>(a.ws, a.L.off_laboff) + (size_t)b * (cap + 1);
+    const int* elab_g = ws_at<int32_t>(a.ws, a.L.off_elab) + e0;
+    float* occ_g = ws_at<float>(a.ws, a.L.off_occ) + e0;
     const float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
     RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
     int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
-    // the distinct labels of the edges, found once: P serves as the marker row
-    int* mark = reinterpret_cast<int*>(P);
-    for (int c = threadIdx.x; c < a.D; c += blockDim.x) mark[c] = 0;
-    if (threadIdx.x == 0) s_nlab = 0;
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int c = a.edges[3 * (size_t)(e0 + e) + 2];
-        if (atomicExch(&mark[c], 1) == 0) {
-            const int i = atomicAdd(&s_nlab, 1);
-            if (i < cap) labs[i] = c;
+    const uintptr_t lp0 = reinterpret_cast<uintptr_t>(a.lp);
+    const uintptr_t lp_end = lp0 + (uintptr_t)(a.T_total * (int64_t)D * (DT == 0 ? 4 : 2));
+    const int base_half = (int)((lp0 >> 1) & 1);
+
+    // the sequence's outgoing lists, label lists and occupancies in shared
+    // memory when they fit
+    const bool local = E <= a.ecap_smem;
+    if (local) {
+        for (int k = tid; k < E; k += nt) {
+            sm.rec[k] = rout_g[k];
+            sm.elab[k] = elab_g[k];
         }
+        for (int s = tid; s <= S; s += nt) sm.off[s] = outoff_g[s];
     }
+    const int4* rout = local ? sm.rec : rout_g;
+    const int* outoff = local ? sm.off : outoff_g;
+    const int* elab = local ? sm.elab : elab_g;
+    float* occ_base = local ? sm.occ : occ_g;
+    const size_t occ_stride = local ? (size_t)a.ecap_smem : (size_t)a.L.E_total;
+    __shared__ int s_nlong;
+    if (tid == 0) s_nlong = 0;
+    for (int i = tid; i < nlab; i += nt) sm.labs[i] = labs_g[i];
+    for (int i = tid; i <= nlab; i += nt) sm.laboff[i] = laboff_g[i];
     __syncthreads();
-    const int nlab = s_nlab;
-    if (nlab > cap) {  // more distinct labels than max_labels: the rows keep zero headers
-        if (threadIdx.x == 0) set_status(ws_at<Control>(a.ws, 0), CTC_PACKED_DEV_BAD_FSA);
-        return;
+    // the labels whose lists a warp sums (any order: each sum is one warp's)
+    for (int i = tid; i < nlab; i += nt)
+        if (sm.laboff[i + 1] - sm.laboff[i] > kShortList) sm.longl[atomicAdd(&s_nlong, 1)] = i;
+    // frame f's label words, its stored alpha row (this thread's states) and
+    // the row's shift (thread 0) are copied kRing - 1 frames ahead
+    auto issue = [&](int f) {
+        if (f >= 0) {
+            issue_row<DT>(sm.ring + (f % kRing) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
+            for (int s = tid; s < S; s += nt)
+                cp_async4(smem_addr(sm.aring + (f % kRing) * Smax + s), alpha_rows + (start + f) * (int64_t)Smax + s);
+            if (tid == 0)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(sm.cring + f % kRing)),
+                             "l"(coff + start + f)
+                             : "memory");
+        }
+        cp_async_commit();
+    };
+    for (int j = 0; j < kRing - 1; ++j) issue(T - 1 - j);
+    float tm = -INFINITY;
+    for (int s = tid; s < S; s += nt) {
+        const float v = a.final_weight[s0 + s];
+        sm.val[s] = v;
+        tm = fmaxf(tm, v);
     }
-    int efr[kFsaRegEdges], eto[kFsaRegEdges], elab[kFsaRegEdges];
-    float ew[kFsaRegEdges], lpc[kFsaRegEdges], lpn[kFsaRegEdges], ac[kFsaRegEdges], an[kFsaRegEdges];
-    float ev[kFsaRegEdges];
 #pragma unroll
-    for (int k = 0; k < kFsaRegEdges; ++k) {
-        const int e = threadIdx.x + k * kFsaThreads;
-        const bool on = e < E;
-        const int* ed = a.edges + 3 * (size_t)(e0 + (on ? e : 0));
-        efr[k] = on ? ed[0] : 0;
-        eto[k] = on ? ed[1] : 0;
-        elab[k] = on ? ed[2] : 0;
-        ew[k] = on ? a.edge_weight[e0 + e] : -INFINITY;  // an absent edge never contributes
-        // this frame's label value and forward value at the edge's origin
-        lpc[k] = (on && T > 0) ? lp_at<DT>(a.lp, (start + T - 1) * (int64_t)a.D + elab[k]) : 0.0f;
-        ac[k] = (on && T > 0) ? alpha_rows[(start + T - 1) * (int64_t)a.max_states + efr[k]] : 0.0f;
-        lpn[k] = an[k] = 0.0f;
-    }
-    const int e_reg = kFsaRegEdges * kFsaThreads;  // edges from here on are read each frame
-    for (int s = threadIdx.x; s < S; s += blockDim.x) be[s] = a.final_weight[s0 + s];
+    for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+    if ((tid & 31) == 0) wmax[0][tid >> 5] = tm;
+    cp_async_wait<kRing - 2>();
     __syncthreads();
-    double Dn = renormalise(be, S, red);  // beta_{t+1} = be + Dn
+    const int nlong = s_nlong;
+    EdgeRegs<PER, RE> er;
+    load_edge_regs(er, outoff, rout, S, sm.labs, base_half);
+    float dn_hi = 0.0f, dn_lo = 0.0f;  // the running shift Dn, a float pair
+    int p = 0;
     for (int t = T - 1; t >= 0; --t) {
-        // occupancy exponent: alpha row + edge + beta, plus this constant
-        const float K = scale != 0.0f ? (float)(coff[start + t] + Dn - Z) : 0.0f;
-        for (int s = threadIdx.x; s < S; s += blockDim.x) {
-            mk[s] = fkey(-INFINITY);
-            sm[s] = 0.0f;
+        issue(t - (kRing - 1));
+        const float* bep = sm.val + p * Smax;
+        float* beq = sm.val + (p ^ 1) * Smax;
+        const uint32_t* lw = sm.ring + (t % kRing) * cap;  // the frame's label words
+        const int flip = row_flip(start + t, D);
+        const float* arow = sm.aring + (t % kRing) * Smax;
+        float* occ = occ_base + (size_t)(t & 1) * occ_stride;
+        const float m = max_of(wmax[p], nw);
+        const float sh = (m > -INFINITY && m < INFINITY) ? m : 0.0f;
+        {
+            float e;
+            dn_hi = two_sum(dn_hi, sh, e);  // beta_{t+1} = bep - sh + Dn
+            dn_lo += e;
         }
-        for (int i = threadIdx.x; i < nlab; i += blockDim.x) P[labs[i]] = 0.0f;
-        __syncthreads();
-        const int64_t lrow = (start + t) * (int64_t)a.D;
-        const float* arow = alpha_rows + (start + t) * (int64_t)a.max_states;
+        // occupancy exponent: alpha row + edge value (shifted beta) + this
+        // constant, K = coff_t + Dn - Z, summed as float pairs (the large
+        // parts cancel; K itself is of the order of the frame's spread)
+        float K = 0.0f;
+        if (scale != 0.0f) {
+            const float2 c = sm.cring[t % kRing];
+            float e1, e2;
+            const float s1 = two_sum(c.x, nz_hi, e1);
+            const float s2 = two_sum(s1, dn_hi, e2);
+            K = s2 + (e2 + (e1 + (c.y + nz_lo + dn_lo)));
+        }
+        tm = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < kFsaRegEdges; ++k) {
-            ev[k] = ew[k] + lpc[k] + be[eto[k]];
-            if (ev[k] > -INFINITY) atomicMax(&mk[efr[k]], fkey(ev[k]));
-        }
-        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
-            const int* ed = a.edges + 3 * (size_t)(e0 + e);
-            const float v = a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]) + be[ed[1]];
-            if (v > -INFINITY) atomicMax(&mk[ed[0]], fkey(v));
-        }
-        if (t > 0) {  // the previous frame's label and forward values, in flight across the barriers
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            if (s < S) {
+                const float as = arow[s];
+                float v[RE], e[RE], lm = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < kFsaRegEdges; ++k) {
-                if (threadIdx.x + k * kFsaThreads < E) {
-                    lpn[k] = lp_at<DT>(a.lp, lrow - a.D + elab[k]);
-                    an[k] = arow[efr[k] - a.max_states];
+                for (int j = 0; j < RE; ++j) {
+                    v[j] = j < er.n[k] ? er.w[k][j] + word_to_float<DT>(lw[er.slot[k][j]], er.par[k][j] ^ flip) +
+                                             bep[er.peer[k][j]] - sh
+                                       : -INFINITY;
+                    lm = fmaxf(lm, v[j]);
                 }
-            }
-        }
-        __syncthreads();
+                float ls = 0.0f;
 #pragma unroll
-        for (int k = 0; k < kFsaRegEdges; ++k) {
-            if (ev[k] > -INFINITY) {
-                atomicAdd(&sm[efr[k]], expf(ev[k] - fdekey(mk[efr[k]])));
+                for (int j = 0; j < RE; ++j) {
+                    e[j] = lm > -INFINITY ? expf(v[j] - lm) : 0.0f;
+                    ls += e[j];
+                }
                 if (scale != 0.0f) {
-                    const float occ = expf(ac[k] + ev[k] + K);
-                    if (occ > 0.0f) atomicAdd(&P[elab[k]], occ);
-                }
-            }
-        }
-        for (int e = e_reg + threadIdx.x; e < E; e += blockDim.x) {
-            const int* ed = a.edges + 3 * (size_t)(e0 + e);
-            const float v = a.edge_weight[e0 + e] + lp_at<DT>(a.lp, lrow + ed[2]) + be[ed[1]];
-            if (v > -INFINITY) {
-                atomicAdd(&sm[ed[0]], expf(v - fdekey(mk[ed[0]])));
-                if (scale != 0.0f) {
-                    const float occ = expf(arow[ed[0]] + v + K);
-                    if (occ > 0.0f) atomicAdd(&P[ed[2]], occ);
-                }
-            }
-        }
-        __syncthreads();
+                    // occupancy exp(as + v + K) = exp(v - max) * exp(as + max + K)
+                    const float g = lm > -INFINITY ? expf(as + lm + K) : 0.0f;
 #pragma unroll
-        for (int k = 0; k < kFsaRegEdges; ++k) {
-            lpc[k] = lpn[k];
-            ac[k] = an[k];
+                    for (int j = 0; j < RE; ++j) {
+                        if (j < er.n[k]) {
+                            const float o = e[j] * g;
+                            occ[er.id[k][j]] = o > 0.0f ? o : 0.0f;
+                        }
+                    }
+                }
+                // the rest of the list, in order
+                for (int kk = er.k0[k]; kk < er.k1[k]; ++kk) {
+                    const int4 r = rout[kk];
+                    const float lv = word_to_float<DT>(lw[r.y], ((base_half ^ sm.labs[r.y]) & 1) ^ flip);
+                    const float vv = __int_as_float(r.z) + lv + bep[r.x] - sh;
+                    lse_push(lm, ls, vv);
+                    if (scale != 0.0f) {
+                        const float o = vv > -INFINITY ? expf(as + vv + K) : 0.0f;
+                        occ[r.w] = o > 0.0f ? o : 0.0f;
+                    }
+                }
+                const float nv = lse_value(lm, ls);
+                beq[s] = nv;
+                tm = fmaxf(tm, nv);
+            }
         }
-        // the row's class sums (class, -scale * occupancy) and header; the
-        // dense rows are written afterwards by the all-SM gradient stream
+        cp_async_wait<kRing - 2>();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+        if ((tid & 31) == 0) wmax[p ^ 1][tid >> 5] = tm;
+        __syncthreads();
+        // the row's class sums (class, -scale * occupancy), each label's edges
+        // in list order; the dense rows are written afterwards by the all-SM
+        // gradient stream
         const int64_t row = start + t;
         const int n = scale != 0.0f ? nlab : 0;
-        for (int i = threadIdx.x; i < n; i += blockDim.x)
-            ent[row * cap + i] = make_int2(labs[i], __float_as_int(-scale * P[labs[i]]));
-        if (threadIdx.x == 0) head[row] = RowHead{n, scale, 1, 0};
-        for (int s = threadIdx.x; s < S; s += blockDim.x)
-            be[s] = sm[s] > 0.0f ? fdekey(mk[s]) + logf(sm[s]) : (sm[s] != sm[s] ? sm[s] : -INFINITY);
-        __syncthreads();
-        Dn += renormalise(be, S, red);
+        // short lists: a thread each, in list order
+        for (int i = tid; i < n; i += nt) {
+            const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
+            if (k1 - k0 > kShortList) continue;
+            float P = 0.0f;
+#pragma unroll 4
+            for (int k = k0; k < k1; ++k) P += occ[elab[k]];
+            ent[row * cap + i] = make_int2(sm.labs[i], __float_as_int(-scale * P));
+        }
+        // long lists (the blank of a CTC lattice has about two edges per
+        // label): a warp each, lane l summing entries l, l + 32, ... in order,
+        // then a fixed shuffle tree
+        for (int q = warp; q < (n > 0 ? nlong : 0); q += nw) {
+            const int i = sm.longl[q];
+            const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
+            // four independent partial sums per lane (entries l, l + 32, l + 64,
+            // l + 96 of each block of 128), combined in a fixed order
+            float P0 = 0.0f, P1 = 0.0f, P2 = 0.0f, P3 = 0.0f;
+            int k = k0 + lane;
+            for (; k + 96 < k1; k += 128) {
+                P0 += occ[elab[k]];
+                P1 += occ[elab[k + 32]];
+                P2 += occ[elab[k + 64]];
+                P3 += occ[elab[k + 96]];
+            }
+            for (; k < k1; k += 32) P0 += occ[elab[k]];
+            float P = (P0 + P1) + (P2 + P3);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) P += __shfl_xor_sync(0xffffffffu, P, o);
+            if (lane == 0) ent[row * cap + i] = make_int2(sm.labs[i], __float_as_int(-scale * P));
+        }
+        if (tid == 0) head[row] = RowHead{n, scale, 1, 0};
+        p ^= 1;
     }
+    cp_async_wait<0>();
 }
 
 // Every row's header starts as "not covered, no class sums"; the backward
@@ -465,21 +890,67 @@ ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_tot
     if (B > 0 && (lengths == nullptr || sw == nullptr || fw == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (E_total > 0 && (edges == nullptr || ew == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (T_total > 0 && log_probs == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if (reinterpret_cast<uintptr_t>(log_probs) % (dtype == CTC_PACKED_F32 ? 4 : 2) != 0)
-        return CTC_PACKED_ERR_INVALID_ARGUMENT;
+    // 4-byte alignment for every dtype: the recursions copy aligned 4-byte words
+    if (reinterpret_cast<uintptr_t>(log_probs) % 4 != 0) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return CTC_PACKED_ERR_WORKSPACE;
-    if (ws_bytes < fsa_layout(T_total, B, max_states, max_labels, D).total) return CTC_PACKED_ERR_WORKSPACE;
+    if (ws_bytes < fsa_layout(T_total, B, S_total, E_total, max_states, max_labels, D).total)
+        return CTC_PACKED_ERR_WORKSPACE;
     return CTC_PACKED_OK;
 }
 
 // A plain launch (no early start): these kernels read what the kernel before
 // them on the stream wrote without a programmatic wait.
 template <typename K>
-cudaError_t launch_fsa(K kernel, unsigned grid, size_t smem, cudaStream_t s, const FsaArgs& a) {
+cudaError_t launch_fsa(K kernel, unsigned grid, int threads, size_t smem, cudaStream_t s, const FsaArgs& a) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kFsaThreads, smem, s>>>(a);
+    kernel<<<grid, threads, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+// Threads of a recursion CTA: a thread per state of the largest sequence, in
+// whole warps, between 64 and 512 (at most 8 states a thread).
+int recursion_threads(int max_states) {
+    int nt = (max_states + 31) / 32 * 32;
+    if (nt < 64) nt = 64;
+    if (nt > kFsaMaxThreads) nt = kFsaMaxThreads;
+    return nt;
+}
+
+// Edges of one sequence a recursion CTA keeps in shared memory (16 bytes an
+// edge forward; 28 backward: the record, its label-list entry and two
+// occupancies): four times the batch's mean per sequence (at least 1024), at
+// most what the budget leaves after the per-frame buffers and at most the
+// batch's edges, so that CTAs of ordinary sequences share an SM.  A sequence
+// with more edges reads its lists from the workspace.
+int smem_edges(bool backward, int B, int E_total, int max_states, int cap) {
+    const size_t fixed = fsa_smem_plan(backward, 0, max_states, cap, nullptr, nullptr);
+    const size_t per = backward ? 28 : 16;
+    if (fixed + 64 >= (size_t)kFsaSmemBudget) return 0;
+    size_t e = ((size_t)kFsaSmemBudget - fixed - 64) / per;
+    size_t want = 4 * (((size_t)E_total + (size_t)B - 1) / (size_t)(B > 0 ? B : 1));
+    if (want < 1024) want = 1024;
+    if (e > want) e = want;
+    if (e > (size_t)E_total) e = (size_t)E_total;
+    return (int)e;
+}
+
+// The forward or backward recursion with PER states a thread: the smallest
+// of 1, 2, 4, 8 that covers max_states with nt threads.
+template <int DT, bool BACKWARD>
+cudaError_t launch_recursion(int max_states, int B, int nt, size_t smem, cudaStream_t s, const FsaArgs& a) {
+    const int per = (max_states + nt - 1) / nt;
+    if (per <= 1)
+        return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 1>, (unsigned)B, nt, smem, s, a)
+                        : launch_fsa(fsa_forward_kernel<DT, 1>, (unsigned)B, nt, smem, s, a);
+    if (per <= 2)
+        return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 2>, (unsigned)B, nt, smem, s, a)
+                        : launch_fsa(fsa_forward_kernel<DT, 2>, (unsigned)B, nt, smem, s, a);
+    if (per <= 4)
+        return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 4>, (unsigned)B, nt, smem, s, a)
+                        : launch_fsa(fsa_forward_kernel<DT, 4>, (unsigned)B, nt, smem, s, a);
+    return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 8>, (unsigned)B, nt, smem, s, a)
+                    : launch_fsa(fsa_forward_kernel<DT, 8>, (unsigned)B, nt, smem, s, a);
 }
 
 FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const int32_t* cu, const int32_t* lengths,
@@ -505,7 +976,7 @@ FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const i
     a.E_total = E_total;
     a.zero_infinity = zero_infinity ? 1 : 0;
     a.ws = ws;
-    a.L = fsa_layout(T_total, B, max_states, max_labels, D);
+    a.L = fsa_layout(T_total, B, S_total, E_total, max_states, max_labels, D);
     return a;
 }
 
@@ -513,11 +984,12 @@ FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const i
 
 extern "C" {
 
-size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t max_states, int32_t max_labels, int32_t D) {
-    if (T_total < 0 || B < 0 || max_states < 1 || max_states > kFsaMaxStates || T_total > INT32_MAX ||
-        max_labels < 1 || D < 1 || D > kFsaMaxD)
+size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t num_states, int32_t num_edges,
+                                     int32_t max_states, int32_t max_labels, int32_t D) {
+    if (T_total < 0 || B < 0 || num_states < 0 || num_edges < 0 || max_states < 1 || max_states > kFsaMaxStates ||
+        T_total > INT32_MAX || max_labels < 1 || D < 1 || D > kFsaMaxD)
         return 0;
-    return fsa_layout(T_total, B, max_states, max_labels, D).total;
+    return fsa_layout(T_total, B, num_states, num_edges, max_states, max_labels, D).total;
 }
 
 ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype dtype, int64_t T_total, int32_t D,
@@ -541,10 +1013,17 @@ ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype
                               final_weight, num_states, edge_offsets, edges, edge_weight, num_edges, max_states,
                               max_labels, zero_infinity, workspace);
     a.loss = loss;
-    const size_t smem = sizeof(float) * 3 * (size_t)max_states;
-    cudaError_t e = dtype == CTC_PACKED_F32    ? launch_fsa(fsa_forward_kernel<0>, (unsigned)B, smem, stream, a)
-                    : dtype == CTC_PACKED_BF16 ? launch_fsa(fsa_forward_kernel<1>, (unsigned)B, smem, stream, a)
-                                               : launch_fsa(fsa_forward_kernel<2>, (unsigned)B, smem, stream, a);
+    // 1. per sequence: the sorted edge lists
+    const size_t ismem = sizeof(int) * ((size_t)(max_states > D ? max_states : D) + (size_t)D);
+    if (launch_fsa(fsa_index_kernel, (unsigned)B, kIdxThreads, ismem, stream, a) != cudaSuccess)
+        return CTC_PACKED_ERR_CUDA;
+    // 2. per sequence: the forward recursion
+    const int nt = recursion_threads(max_states);
+    a.ecap_smem = smem_edges(false, B, num_edges, max_states, a.L.cap);
+    const size_t smem = fsa_smem_plan(false, a.ecap_smem, max_states, a.L.cap, nullptr, nullptr);
+    const cudaError_t e = dtype == CTC_PACKED_F32    ? launch_recursion<0, false>(max_states, B, nt, smem, stream, a)
+                          : dtype == CTC_PACKED_BF16 ? launch_recursion<1, false>(max_states, B, nt, smem, stream, a)
+                                                     : launch_recursion<2, false>(max_states, B, nt, smem, stream, a);
     return e == cudaSuccess ? CTC_PACKED_OK : CTC_PACKED_ERR_CUDA;
 }
 
@@ -575,16 +1054,18 @@ ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtyp
     a.grad_loss = grad_loss;
     a.grad = grad_log_probs;
     // 1. every row header "not covered"
-    const long long hgrid = (T_total + kFsaThreads - 1) / kFsaThreads;
-    if (launch_fsa(fsa_head_init_kernel, (unsigned)(hgrid < 4096 ? hgrid : 4096), 0, stream, a) != cudaSuccess)
+    const long long hgrid = (T_total + 255) / 256;
+    if (launch_fsa(fsa_head_init_kernel, (unsigned)(hgrid < 4096 ? hgrid : 4096), 256, 0, stream, a) != cudaSuccess)
         return CTC_PACKED_ERR_CUDA;
     // 2. per sequence: beta, edge occupancies, each row's class sums and header
     if (B > 0) {
-        const size_t smem = sizeof(float) * (3 * (size_t)max_states + (size_t)D) + sizeof(int) * (size_t)a.L.cap;
+        const int nt = recursion_threads(max_states);
+        a.ecap_smem = smem_edges(true, B, num_edges, max_states, a.L.cap);
+        const size_t smem = fsa_smem_plan(true, a.ecap_smem, max_states, a.L.cap, nullptr, nullptr);
         const cudaError_t e =
-            dtype == CTC_PACKED_F32    ? launch_fsa(fsa_backward_kernel<0>, (unsigned)B, smem, stream, a)
-            : dtype == CTC_PACKED_BF16 ? launch_fsa(fsa_backward_kernel<1>, (unsigned)B, smem, stream, a)
-                                       : launch_fsa(fsa_backward_kernel<2>, (unsigned)B, smem, stream, a);
+            dtype == CTC_PACKED_F32    ? launch_recursion<0, true>(max_states, B, nt, smem, stream, a)
+            : dtype == CTC_PACKED_BF16 ? launch_recursion<1, true>(max_states, B, nt, smem, stream, a)
+                                       : launch_recursion<2, true>(max_states, B, nt, smem, stream, a);
         if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     }
     // 3. the dense rows, scale * exp(lp) + class sums, by the CTC path's

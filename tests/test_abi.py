@@ -183,10 +183,15 @@ def test_fsa_workspace_size():
     from packed_sequence_ctc_gb300 import build as b
 
     lib = pk.load_library(b.build())
-    assert lib.ctc_packed_fsa_workspace_size(100, 4, 0, 5, 10) == 0
-    assert lib.ctc_packed_fsa_workspace_size(100, 4, 10, 0, 10) == 0
-    n = lib.ctc_packed_fsa_workspace_size(1000, 4, 50, 20, 30)
-    # alpha rows (4 B x states) and class sums (8 B x min(labels, D)) per frame at least
-    assert n >= 1000 * 50 * 4 + 1000 * 20 * 8 + 1000 * 8
-    assert lib.ctc_packed_fsa_workspace_size(1000, 4, 50, 200, 30) < lib.ctc_packed_fsa_workspace_size(
-        1000, 4, 50, 200, 300)  # the class sums a row holds are capped at D
+    f = lib.ctc_packed_fsa_workspace_size  # (T_total, B, num_states, num_edges, max_states, max_labels, D)
+    assert f(100, 4, 20, 60, 0, 5, 10) == 0
+    assert f(100, 4, 20, 60, 10, 0, 10) == 0
+    assert f(100, 4, -1, 60, 10, 5, 10) == 0
+    assert f(100, 4, 20, -1, 10, 5, 10) == 0
+    assert f(100, 4, 20, 60, 10, 5, 16385) == 0
+    n = f(1000, 4, 200, 600, 50, 20, 30)
+    # alpha rows (4 B x states) and class sums (8 B x min(labels, D)) per frame, and per edge two
+    # 16-byte list records and two occupancies at least
+    assert n >= 1000 * 50 * 4 + 1000 * 20 * 8 + 1000 * 8 + 600 * (32 + 8)
+    assert f(1000, 4, 200, 600, 50, 200, 30) < f(1000, 4, 200, 600, 50, 200, 300)  # class sums capped at D
+    assert f(1000, 4, 200, 600, 50, 20, 30) < f(1000, 4, 200, 6000, 50, 20, 30)  # edge lists grow with edges

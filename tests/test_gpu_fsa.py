@@ -5,7 +5,8 @@ Cases: the CTC lattice written as an FSA (also checked against the CTC
 path), seeded random FSAs with weights, several start and final states and
 loops, in the three dtypes; a sequence without a path (with and without
 zero_infinity), frameless sequences and gap rows; a large vocabulary; and
-out-of-range FSA data, which must set the status word and a NaN loss.  The
+out-of-range FSA data (and more distinct labels than max_labels), which must
+set the status word and a NaN loss; and bitwise reproducibility.  The
 recursions run in float32 log space: losses within 1e-4 relative, float32
 gradients within 2e-5 (on these lengths), half types within one unit in the
 last place plus 1e-3.
@@ -23,16 +24,17 @@ from tests.helpers import assert_grad_close, assert_loss_close, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-def _run(lp, cu, lengths, fsa, max_states, zero_infinity=False, grad_loss=None, guard=64):
+def _run(lp, cu, lengths, fsa, max_states, zero_infinity=False, grad_loss=None, guard=64, max_labels=None):
     dev = "cuda"
     T_total, D = lp.shape
     B = lengths.numel()
     fsa_d = tuple(x.to(dev).contiguous() for x in fsa)
     cu_d, ln_d = cu.to(dev).to(torch.int32), lengths.to(dev).to(torch.int32)
     lp_d = lp.to(dev).contiguous()
-    max_labels = _max_labels(fsa)
-    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, B, max_states, max_labels, D), dtype=torch.uint8,
-                     device=dev)
+    max_labels = _max_labels(fsa) if max_labels is None else max_labels
+    n_states, n_edges = int(fsa[1].numel()), int(fsa[4].shape[0])
+    ws = torch.empty(pk.ctc_packed_fsa_workspace_size(T_total, B, n_states, n_edges, max_states, max_labels, D),
+                     dtype=torch.uint8, device=dev)
     loss = torch.full((B,), float("nan"), device=dev)
     pk.ctc_packed_fsa_forward(lp_d, cu_d, ln_d, fsa_d, max_states, max_labels, zero_infinity, loss, ws)
     g = torch.ones(B) if grad_loss is None else torch.as_tensor(grad_loss, dtype=torch.float32)
@@ -166,3 +168,54 @@ def test_many_edges_per_sequence_and_a_nan(cuda_device):
     assert np.isnan(loss[2]) and np.isnan(ref_loss[2])
     assert_loss_close(loss[:2], ref_loss[:2])
     assert_grad_close(grad[:100], ref_grad[:100], torch.float32)
+
+
+def test_more_labels_than_max_labels_rejects_the_sequence(cuda_device):
+    D = 6
+    lp = torch.log_softmax(torch.randn(24, D, generator=torch.Generator().manual_seed(5)), -1)
+    two = ([0.0, float("-inf")], [float("-inf"), 0.0], [(0, 1, 1), (1, 1, 2), (0, 0, 2)], [0.0, 0.0, 0.0])
+    three = ([0.0, float("-inf")], [float("-inf"), 0.0], [(0, 1, 1), (1, 1, 2), (0, 0, 3)], [0.0, 0.0, 0.0])
+    fsa = workloads.pack_fsas([two, three])
+    cu = torch.tensor([0, 12, 24], dtype=torch.int32)
+    ln = torch.tensor([12, 12], dtype=torch.int32)
+    loss, grad, status, g = _run(lp, cu, ln, fsa, 2, max_labels=2)
+    assert status & 0x80
+    assert np.isfinite(loss[0]) and np.isnan(loss[1])
+    assert bool((grad[12:] == 0).all())
+    ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
+    assert_loss_close(loss[:1], ref_loss[:1])
+    assert_grad_close(grad[:12], ref_grad[:12], torch.float32)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_deterministic(cuda_device, dtype):
+    # every sum runs in a fixed order: two runs agree bit for bit
+    D = 23
+    lp = torch.log_softmax(torch.randn(420, D, generator=torch.Generator().manual_seed(11)), -1).to(dtype)
+    fsa = workloads.pack_fsas([workloads.random_fsa(40, 400, D, seed=31), workloads.random_fsa(25, 900, D, seed=32),
+                               workloads.random_fsa(7, 30, D, seed=33)])
+    cu = torch.tensor([0, 200, 350, 420], dtype=torch.int32)
+    ln = torch.tensor([190, 150, 70], dtype=torch.int32)
+    l1, g1, s1, _ = _run(lp, cu, ln, fsa, 40)
+    l2, g2, s2, _ = _run(lp, cu, ln, fsa, 40)
+    assert s1 == 0 and s2 == 0
+    assert np.array_equal(l1, l2)
+    assert torch.equal(g1.view(torch.int16) if dtype != torch.float32 else g1.view(torch.int32),
+                       g2.view(torch.int16) if dtype != torch.float32 else g2.view(torch.int32))
+
+
+def test_sequence_beyond_the_shared_memory_lists(cuda_device):
+    # one sequence with far more edges than four times the batch's mean keeps
+    # its lists in the workspace; the small ones keep theirs in shared memory
+    D = 17
+    lp = torch.log_softmax(torch.randn(60 + 12 * 20, D, generator=torch.Generator().manual_seed(12)), -1)
+    fsas = [workloads.random_fsa(50, 6000, D, seed=90)] + [workloads.random_fsa(4, 10, D, seed=91 + i)
+                                                           for i in range(12)]
+    fsa = workloads.pack_fsas(fsas)
+    cu = torch.tensor([0, 60] + [60 + 20 * (i + 1) for i in range(12)], dtype=torch.int32)
+    ln = torch.tensor([60] + [18] * 12, dtype=torch.int32)
+    loss, grad, status, g = _run(lp, cu, ln, fsa, 50)
+    assert status == 0
+    ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, torch.float32)

@@ -70,7 +70,7 @@ def test_oversized_batches_are_refused_before_any_cuda_call(lib):
     # invalid and unsupported sizes keep the ordinary forward's codes
     assert _noalloc_raw(lib, -1, 1, 1, 5) == ERR_INVALID
     assert _noalloc_raw(lib, 10, 1, 1, 0) == ERR_INVALID
-    assert _noalloc_raw(lib, 10, 1, 1, 20000) == ERR_UNSUPPORTED
+    assert _noalloc_raw(lib, 10, 1, 1, (1 << 20) + 1) == ERR_UNSUPPORTED
     assert _noalloc_raw(lib, 10, 1, 1, 5, dtype=7) == ERR_INVALID
 
 
