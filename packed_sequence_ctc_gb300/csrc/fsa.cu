@@ -35,10 +35,11 @@
 //            backward with its shift.
 //   backward one CTA per sequence, a thread per source state: beta_t(s)
 //            over the state's outgoing edges in list order, each edge's
-//            occupancy into a double-buffered per-edge array, then after the
-//            frame's barrier the class sums, each label's edges in list
-//            order; the dense rows are written by the CTC path's all-SM
-//            gradient stream from the rows' class sums.
+//            occupancy into a double-buffered per-edge array at the edge's
+//            position in label order, then after the frame's barrier the
+//            class sums, each label's contiguous range in order; the dense
+//            rows are written by the CTC path's all-SM gradient stream from
+//            the rows' class sums.
 #include <cstdint>
 
 #include "ctc_common.cuh"
@@ -64,7 +65,7 @@ constexpr int kShortList = 8;         // label lists up to this long are summed 
 // both lists, the label lists and the occupancies of two frames.
 struct FsaLayout {
     size_t off_z, off_nlab, off_coff, off_alpha, off_head, off_ent;
-    size_t off_inoff, off_outoff, off_rin, off_rout, off_elab, off_tmp, off_labs, off_laboff, off_occ, total;
+    size_t off_inoff, off_outoff, off_rin, off_rout, off_lpos, off_tmp, off_labs, off_laboff, off_occ, total;
     int cap;       // class sums a row can hold: min(max_labels, D)
     int E_total;   // edges of all sequences (the occupancy buffers' stride)
 };
@@ -87,7 +88,7 @@ __host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int3
     L.off_outoff = o; o = align_up(o + sizeof(int32_t) * ((size_t)S_total + Bn), 256);
     L.off_rin = o;    o = align_up(o + sizeof(int4) * (size_t)E_total, 256);
     L.off_rout = o;   o = align_up(o + sizeof(int4) * (size_t)E_total, 256);
-    L.off_elab = o;   o = align_up(o + sizeof(int32_t) * (size_t)E_total, 256);
+    L.off_lpos = o;   o = align_up(o + sizeof(int32_t) * (size_t)E_total, 256);  // position in label order
     L.off_tmp = o;    o = align_up(o + sizeof(int32_t) * (size_t)E_total, 256);
     L.off_labs = o;   o = align_up(o + sizeof(int32_t) * Bn * cap, 256);
     L.off_laboff = o; o = align_up(o + sizeof(int32_t) * Bn * (cap + 1), 256);
@@ -353,7 +354,13 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     for (int i = threadIdx.x; i < nlab; i += blockDim.x) laboff[i] = cnt[labs[i]];
     if (threadIdx.x == 0) laboff[nlab] = E;
     __syncthreads();
-    place_stable(E, [&](int e) { return ed[3 * e + 2]; }, cnt, ws_at<int32_t>(a.ws, a.L.off_elab) + e0);
+    // edge ids in label order into tmp, then each edge's position in that
+    // order (where the backward writes its occupancy, so that a label's
+    // occupancies are one contiguous range)
+    int* lpos = ws_at<int32_t>(a.ws, a.L.off_lpos) + e0;
+    place_stable(E, [&](int e) { return ed[3 * e + 2]; }, cnt, tmp);
+    for (int k = threadIdx.x; k < E; k += blockDim.x) lpos[tmp[k]] = k;
+    __syncthreads();
 
     // 2. incoming lists (by destination): records (from, label slot, weight, edge)
     int* inoff = ws_at<int32_t>(a.ws, a.L.off_inoff) + s0 + b;
@@ -370,7 +377,8 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     }
     __syncthreads();
 
-    // 3. outgoing lists (by source): records (to, label slot, weight, edge)
+    // 3. outgoing lists (by source): records (to, label slot, weight, the
+    //    edge's position in label order)
     int* outoff = ws_at<int32_t>(a.ws, a.L.off_outoff) + s0 + b;
     for (int s = threadIdx.x; s < S; s += blockDim.x) cnt[s] = 0;
     __syncthreads();
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     int4* rout = ws_at<int4>(a.ws, a.L.off_rout) + e0;
     for (int k = threadIdx.x; k < E; k += blockDim.x) {
         const int e = tmp[k];
-        rout[k] = make_int4(ed[3 * e + 1], slot[ed[3 * e + 2]], __float_as_int(ew[e]), e);
+        rout[k] = make_int4(ed[3 * e + 1], slot[ed[3 * e + 2]], __float_as_int(ew[e]), lpos[e]);
     }
     if (threadIdx.x == 0) nlab_out[b] = nlab;
 }
@@ -392,7 +400,6 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
 struct FsaSmem {
     int4* rec;        // edge records of the list (incoming or outgoing), ecap_smem
     int* off;         // list offsets per state, Smax + 1
-    int* elab;        // (backward) edge ids by label, ecap_smem
     float* occ;       // (backward) occupancies of two frames, 2 * ecap_smem
     float* val;       // alpha or beta of two frames, 2 * Smax
     int* longl;       // (backward) the labels with long edge lists, cap
@@ -413,7 +420,6 @@ __host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Sma
     };
     const size_t rec = take(16 * (size_t)ecap, 16);
     const size_t off = take(4 * ((size_t)Smax + 1), 4);
-    const size_t elab = backward ? take(4 * (size_t)ecap, 4) : 0;
     const size_t occ = backward ? take(8 * (size_t)ecap, 4) : 0;
     const size_t val = take(8 * (size_t)Smax, 4);
     const size_t longl = backward ? take(4 * (size_t)cap, 4) : 0;
@@ -425,7 +431,6 @@ __host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Sma
     if (out != nullptr) {
         out->rec = reinterpret_cast<int4*>(base + rec);
         out->off = reinterpret_cast<int*>(base + off);
-        out->elab = reinterpret_cast<int*>(base + elab);
         out->occ = reinterpret_cast<float*>(base + occ);
         out->val = reinterpret_cast<float*>(base + val);
         out->longl = reinterpret_cast<int*>(base + longl);
@@ -676,7 +681,6 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a)
     const int4* rout_g = ws_at<int4>(a.ws, a.L.off_rout) + e0;
     const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
     const int* laboff_g = ws_at<int32_t>(a.ws, a.L.off_laboff) + (size_t)b * (cap + 1);
-    const int* elab_g = ws_at<int32_t>(a.ws, a.L.off_elab) + e0;
     float* occ_g = ws_at<float>(a.ws, a.L.off_occ) + e0;
     const float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
     RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
@@ -691,13 +695,11 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a)
     if (local) {
         for (int k = tid; k < E; k += nt) {
             sm.rec[k] = rout_g[k];
-            sm.elab[k] = elab_g[k];
         }
         for (int s = tid; s <= S; s += nt) sm.off[s] = outoff_g[s];
     }
     const int4* rout = local ? sm.rec : rout_g;
     const int* outoff = local ? sm.off : outoff_g;
-    const int* elab = local ? sm.elab : elab_g;
     float* occ_base = local ? sm.occ : occ_g;
     const size_t occ_stride = local ? (size_t)a.ecap_smem : (size_t)a.L.E_total;
     __shared__ int s_nlong;
@@ -822,19 +824,22 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a)
         // gradient stream
         const int64_t row = start + t;
         const int n = scale != 0.0f ? nlab : 0;
-        // short lists: a thread each, in list order
+        // a label's occupancies are the contiguous range [laboff[i],
+        // laboff[i + 1]) in edge order.  Short lists: a thread each, in order
         for (int i = tid; i < n; i += nt) {
             const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
             if (k1 - k0 > kShortList) continue;
             float P = 0.0f;
-#pragma unroll 4
-            for (int k = k0; k < k1; ++k) P += occ[elab[k]];
+#pragma unroll
+            for (int j = 0; j < kShortList; ++j)
+                if (k0 + j < k1) P += occ[k0 + j];
             ent[row * cap + i] = make_int2(sm.labs[i], __float_as_int(-scale * P));
         }
         // long lists (the blank of a CTC lattice has about two edges per
-        // label): a warp each, lane l summing entries l, l + 32, ... in order,
+        // label): a warp each, from the last warp down (the last warps hold
+        // the fewest states), lane l summing entries l, l + 32, ... in order,
         // then a fixed shuffle tree
-        for (int q = warp; q < (n > 0 ? nlong : 0); q += nw) {
+        for (int q = nw - 1 - warp; q < (n > 0 ? nlong : 0); q += nw) {
             const int i = sm.longl[q];
             const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
             // four independent partial sums per lane (entries l, l + 32, l + 64,
@@ -842,12 +847,12 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a)
             float P0 = 0.0f, P1 = 0.0f, P2 = 0.0f, P3 = 0.0f;
             int k = k0 + lane;
             for (; k + 96 < k1; k += 128) {
-                P0 += occ[elab[k]];
-                P1 += occ[elab[k + 32]];
-                P2 += occ[elab[k + 64]];
-                P3 += occ[elab[k + 96]];
+                P0 += occ[k];
+                P1 += occ[k + 32];
+                P2 += occ[k + 64];
+                P3 += occ[k + 96];
             }
-            for (; k < k1; k += 32) P0 += occ[elab[k]];
+            for (; k < k1; k += 32) P0 += occ[k];
             float P = (P0 + P1) + (P2 + P3);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) P += __shfl_xor_sync(0xffffffffu, P, o);
@@ -918,14 +923,13 @@ int recursion_threads(int max_states) {
 }
 
 // Edges of one sequence a recursion CTA keeps in shared memory (16 bytes an
-// edge forward; 28 backward: the record, its label-list entry and two
-// occupancies): four times the batch's mean per sequence (at least 1024), at
+// edge forward; 24 backward: the record and two occupancies): four times the batch's mean per sequence (at least 1024), at
 // most what the budget leaves after the per-frame buffers and at most the
 // batch's edges, so that CTAs of ordinary sequences share an SM.  A sequence
 // with more edges reads its lists from the workspace.
 int smem_edges(bool backward, int B, int E_total, int max_states, int cap) {
     const size_t fixed = fsa_smem_plan(backward, 0, max_states, cap, nullptr, nullptr);
-    const size_t per = backward ? 28 : 16;
+    const size_t per = backward ? 24 : 16;
     if (fixed + 64 >= (size_t)kFsaSmemBudget) return 0;
     size_t e = ((size_t)kFsaSmemBudget - fixed - 64) / per;
     size_t want = 4 * (((size_t)E_total + (size_t)B - 1) / (size_t)(B > 0 ? B : 1));
