@@ -81,6 +81,9 @@ def _args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--input", default="log_probs", choices=["log_probs", "logits"],
                    help="logits: the rows are unnormalised logits and the path takes log_softmax itself")
+    p.add_argument("--dtype", default=None, choices=["f64"],
+                   help="f64: the workload's log probabilities in float64 through ctc_packed_forward_f64 / "
+                        "ctc_packed_backward_f64 (the float64 path)")
     p.add_argument("--topology", default="ctc", choices=["ctc", "fsa"],
                    help="fsa: the same utterances' CTC lattices through the generic FSA path")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -641,10 +644,95 @@ def run_fsa(args):
     print(json.dumps(line), flush=True)
 
 
+def run_f64(args):
+    """The workload's rows in float64 through the float64 path
+    (ctc_packed_forward_f64 + ctc_packed_backward_f64), timed like the CTC
+    path; one JSON line.  The dense rows are twice the bytes of the float32
+    path; the recursions run in float64 (extended range)."""
+    import torch
+
+    import packed_sequence_ctc_gb300 as pk
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    batch = workloads.workload(args.workload, device=dev)
+    cfg = _workload_description(batch, False)
+    lp = batch.log_probs.to(torch.float64).contiguous()
+    batch.log_probs = None
+    T_total, D = lp.shape
+    cu, ln = batch.cu_seqlens.to(dev).to(torch.int32), batch.lengths.to(dev).to(torch.int32)
+    tg, tl = batch.targets.to(dev).to(torch.int32), batch.target_lengths.to(dev).to(torch.int32)
+    mtl = batch.max_target_len
+    ws = pk.Workspace(T_total, batch.B, mtl, D, torch.float64, dev).tensor
+    red = batch.reduction
+    loss = torch.empty(batch.B if red == "none" else 1, dtype=torch.float64, device=dev)
+    g_up = torch.ones(batch.B if red == "none" else 1, dtype=torch.float64, device=dev)
+    grad = torch.empty_like(lp)
+    zi = batch.zero_infinity
+
+    def fwd():
+        pk.ctc_packed_forward(lp, cu, ln, tg, tl, batch.blank, zi, red, loss, ws, mtl, stream=stream)
+
+    def bwd():
+        pk.ctc_packed_backward(lp, cu, ln, tg, tl, batch.blank, zi, red, g_up, ws, grad, mtl, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    status = pk.ctc_packed_read_status(ws)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(_gpu_query_id(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for k in range(K):
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    sampler.snapshot()
+    time.sleep(0.25)
+    sampler.stop()
+    fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    ms = fwd_ms + bwd_ms
+    hbm_peak, peak_kind = _peaks()
+    dense = 2 * T_total * D * 8  # the backward reads the rows and writes the gradient
+    achieved = dense / (bwd_ms / 1e3) / 1e9
+    cfg["workload"] = cfg["workload"].replace(cfg["io_dtype"] + " log probs", "f64 log probs")
+    cfg["io_dtype"] = "f64"
+    cfg["l2"] = f"inputs larger than L2 ({T_total * D * 8 / 1e6:.0f} MB of log probabilities per step)"
+    cfg["parallelism"] = "single GPU"
+    line = {
+        "metric": METRIC, "value": round(batch.frames / (ms / 1e3), 1), "unit": "frames/s", "n_gpus": 1,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "kernel": "f64_beta_kernel+f64_grad_kernel (the float64 backward call)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "peak_kind": f"{peak_kind} copy bandwidth (burst)", "algorithmic_bytes_per_launch": dense,
+                     "avg_launch_ms": round(bwd_ms, 5)},
+        "forward_ms": round(fwd_ms, 5), "backward_ms": round(bwd_ms, 5), "cpu_baseline": None, "e2e": None,
+        "gpu_launches": (4 + (1 if red != "none" else 0)) * K, "clocks": sampler.summary(t0, t1),
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.dtype == "f64":
+        run_f64(args)
     elif args.topology == "fsa":
         run_fsa(args)
     else:

@@ -115,7 +115,9 @@ struct ItemCtx {
 // R - 1 ahead are requested.  After a block the states are renormalised
 // (between renormalisations a mantissa grows at most 12x a frame) and the
 // warps of a multi-warp item exchange their edges.
-template <int P, int DIR>
+// CKPT: the checkpoint policy (store_rows > 1) is compiled as a variant of
+// its own, so that the default (every row or none) keeps the plain loop.
+template <int P, int DIR, bool CKPT>
 __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     using S = ChainShape<P>;
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
@@ -390,16 +392,16 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             XP el[P], eb;
             emissions(base + q, el, eb);
             request((base + q + S::R - 1) & (S::R - 1), i0 + q + S::R - 1);
-            if (a.store_rows == 1) {
-                flush_row(q);  // frame i0 + q - 1
-            } else if (a.store_rows > 1) {
+            if (CKPT) {
                 flush_ckpt(i0 + q - 1);
+            } else if (a.store_rows) {
+                flush_row(q);  // frame i0 + q - 1
             }
             step(el, eb);
         }
         renormalise();
         if (multi) exchange((i0 - 1) / S::F);
-        if (a.store_rows == 1) write_rows(i0 - 1, S::F);
+        if (!CKPT && a.store_rows) write_rows(i0 - 1, S::F);
     }
     // the last frames (fewer than F: no exchange needed)
 #pragma unroll 1
@@ -409,18 +411,18 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         const uint32_t slot = (uint32_t)((i - 1) & (S::R - 1));
         emissions(slot, el, eb);
         request((slot + S::R - 1) & (S::R - 1), i + S::R - 1);
-        if (a.store_rows == 1) {
-            flush_row(i - i0);  // frame i - 1
-        } else if (a.store_rows > 1) {
+        if (CKPT) {
             flush_ckpt(i - 1);
+        } else if (a.store_rows) {
+            flush_row(i - i0);  // frame i - 1
         }
         step(el, eb);
     }
-    if (a.store_rows == 1) {
+    if (CKPT) {
+        flush_ckpt(T - 1);
+    } else if (a.store_rows) {
         flush_row(T - i0);  // frame T - 1 (T >= 1 for every queued item)
         write_rows(i0 - 1, T - i0 + 1);
-    } else if (a.store_rows > 1) {
-        flush_ckpt(T - 1);
     }
     cp_async_wait<0>();
     renormalise();
@@ -474,12 +476,12 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     }
 }
 
-template <int P>
+template <int P, bool CKPT>
 __device__ __forceinline__ void run_item(const ChainArgs& a, int item, const ItemCtx& c) {
     if (item & 1) {
-        run_chain<P, 1>(a, item >> 1, c);
+        run_chain<P, 1, CKPT>(a, item >> 1, c);
     } else {
-        run_chain<P, 0>(a, item >> 1, c);
+        run_chain<P, 0, CKPT>(a, item >> 1, c);
     }
 }
 
@@ -489,7 +491,9 @@ __device__ __forceinline__ void run_item(const ChainArgs& a, int item, const Ite
 // under a 256-thread bound, which leaves the compiler room for ~120
 // registers a thread instead of 64 (measured: 13 us faster on the 8193-class
 // workload's 8-warp chains).
-template <int P, int MAXT>
+// CKPT: the chains keep only checkpoint rows (store_rows > 1), a kernel of
+// its own so that the default one holds only the plain loop.
+template <int P, int MAXT, bool CKPT>
 __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
     using S = ChainShape<P>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -521,7 +525,7 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
         const int item = queue[k];
         const int U = utt[item >> 1].U;
         const int nw = min(NW, (U + 1 + S::GP - 1) / S::GP);
-        if (warp < nw) run_item<P>(a, item, ItemCtx{warp, nw, my_ring, xch, fins, my_stage});
+        if (warp < nw) run_item<P, CKPT>(a, item, ItemCtx{warp, nw, my_ring, xch, fins, my_stage});
     }
     // 2. single-warp chains, each warp on its own
     for (;;) {
@@ -529,7 +533,7 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
         if (lane == 0) k = (int)atomicAdd(&ctrl->small_head, 1u);
         k = __shfl_sync(0xffffffffu, k, 0);
         if (k >= n_small) break;
-        run_item<P>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp, my_stage});
+        run_item<P, CKPT>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp, my_stage});
     }
     // 3. (the label analysis of the backward runs in the emission gather's kernel)
     // 4. the last CTA to finish reduces the losses (fixed order: deterministic)
@@ -564,14 +568,19 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
     }
 }
 
-template __global__ void chain_kernel<1, 256>(ChainArgs);
-template __global__ void chain_kernel<1, 512>(ChainArgs);
-template __global__ void chain_kernel<2, 512>(ChainArgs);
-template __global__ void chain_kernel<2, 1024>(ChainArgs);
-template __global__ void chain_kernel<4, 1024>(ChainArgs);
+template __global__ void chain_kernel<1, 256, false>(ChainArgs);
+template __global__ void chain_kernel<1, 512, false>(ChainArgs);
+template __global__ void chain_kernel<2, 512, false>(ChainArgs);
+template __global__ void chain_kernel<2, 1024, false>(ChainArgs);
+template __global__ void chain_kernel<4, 1024, false>(ChainArgs);
+template __global__ void chain_kernel<1, 256, true>(ChainArgs);
+template __global__ void chain_kernel<1, 512, true>(ChainArgs);
+template __global__ void chain_kernel<2, 512, true>(ChainArgs);
+template __global__ void chain_kernel<2, 1024, true>(ChainArgs);
+template __global__ void chain_kernel<4, 1024, true>(ChainArgs);
 
-template <int P, int MAXT>
-static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
+template <int P, int MAXT, bool CKPT>
+static cudaError_t launch_chain_c(const ChainArgs& a, cudaStream_t s) {
     using S = ChainShape<P>;
     const int nw = a.L.nwo;  // warps for the longest possible target
     const size_t smem = sizeof(XP) * ((size_t)nw * S::R * 32 * S::LW + 2 * (size_t)nw * S::XW + 2 * (size_t)nw) +
@@ -581,11 +590,11 @@ static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     // set on every call (on the current device): a cached value could go
     // stale between host threads launching with different sizes
-    e = cudaFuncSetAttribute(chain_kernel<P, MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(chain_kernel<P, MAXT, CKPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P, MAXT>, 32 * nw, smem)) !=
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P, MAXT, CKPT>, 32 * nw, smem)) !=
         cudaSuccess)
         return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -593,7 +602,12 @@ static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
     long long want = 2ll * a.L.B;
     long long grid = (long long)sms * per_sm;
     if (want < grid) grid = want > 0 ? want : 1;
-    return launch_pdl(chain_kernel<P, MAXT>, dim3((unsigned)grid), dim3(32 * nw), smem, s, a);
+    return launch_pdl(chain_kernel<P, MAXT, CKPT>, dim3((unsigned)grid), dim3(32 * nw), smem, s, a);
+}
+
+template <int P, int MAXT>
+static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
+    return a.store_rows > 1 ? launch_chain_c<P, MAXT, true>(a, s) : launch_chain_c<P, MAXT, false>(a, s);
 }
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s) {
