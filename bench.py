@@ -70,6 +70,18 @@ def _profiled_traffic(workload, fused):
     return int(t.group(1))
 
 
+def _load_workload(args, dev):
+    """The named workload on `dev`; with --first N only its first N
+    utterances (a smaller case of the same shapes, e.g. for an ncu capture)."""
+    import workloads
+
+    batch = workloads.workload(args.workload, device=dev)
+    if args.first:
+        batch = workloads.select_utterances(batch, list(range(min(args.first, batch.B))))
+        batch.log_probs = batch.log_probs.to(dev)
+    return batch
+
+
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -77,6 +89,8 @@ def _args():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="largevocab")
+    p.add_argument("--first", type=int, default=0,
+                   help="only the workload's first N utterances (a smaller case of the same shapes)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--input", default="log_probs", choices=["log_probs", "logits"],
@@ -281,7 +295,7 @@ def run_reference(args):
     import workloads
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    batch = workloads.workload(args.workload, device=dev)
+    batch = _load_workload(args, dev)
     batch.log_probs = batch.log_probs.cpu()
     logits = args.input == "logits"
     if logits:
@@ -357,7 +371,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
 
-    batch = workloads.workload(args.workload, device=dev)
+    batch = _load_workload(args, dev)
     logits = args.input == "logits"
     lp = batch.log_probs.contiguous()
     fflags = 0
@@ -427,7 +441,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "kernel": "whole path: prep, emission gather, chains, gradient stream (" +
                 ("one forward-backward call" if head is fused else "a forward call then a backward call") + ")",
                 "achieved": round(path_gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(path_gbs / hbm_peak, 4),
-                "traffic": _profiled_traffic(args.workload, head is fused),
+                "traffic": None if args.first else _profiled_traffic(args.workload, head is fused),
                 "peak_kind": f"{peak_kind} copy bandwidth (burst)", "algorithmic_bytes_per_launch": ab["total"],
                 "avg_launch_ms": round(ms_per_step, 5),
                 "bytes": {k: ab[k] for k in ("gather", "alpha", "dense", "lse")}}
@@ -569,7 +583,7 @@ def run_fsa(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    batch = workloads.workload(args.workload, device=dev)
+    batch = _load_workload(args, dev)
     lp = batch.log_probs.contiguous()
     offs = np.concatenate([[0], np.cumsum(batch.target_lengths.cpu().numpy())])
     tg = batch.targets.cpu().numpy()
@@ -657,7 +671,7 @@ def run_f64(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    batch = workloads.workload(args.workload, device=dev)
+    batch = _load_workload(args, dev)
     cfg = _workload_description(batch, False)
     lp = batch.log_probs.to(torch.float64).contiguous()
     batch.log_probs = None
