@@ -17,24 +17,31 @@
 // row whose sum is zero has no path through it: the utterance cannot be
 // aligned (its loss is +inf).
 //
-// Structure.  One CTA per SM, made of teams of four warps.  A team owns a few
-// shared-memory slots.  For each row it takes, one thread issues bulk
-// copies of everything the row needs into a free slot: the log-probability
-// row (its 16-byte aligned span), the stored alpha and beta rows and their
-// per-warp offsets, all completing on the slot's mbarrier.  The team works on
-// the oldest slot while the copies of the next ones are in flight:
-//   1. class sums: the state posteriors of the row from the slot, summed per
-//      distinct class in a fixed order (no atomics on values; bitwise
-//      reproducible), each class sum linked to the 16-byte chunk of the row
-//      that holds its class;
-//   2. the dense row: every chunk is read from the slot, gets
-//      scale * exp(lp) plus the chunk's class sums (if any), is rounded once
-//      into the row's dtype and stored as one 16-byte vector (the ragged
-//      chunks at the ends element by element).
+// Structure.  One CTA per SM, made of teams: a producer warp and four worker
+// warps, with a few shared-memory slots per team (full / empty mbarriers).
+// For each row the team takes, the producer issues bulk copies of everything
+// the row needs into a free slot: the log-probability row (its 16-byte
+// aligned span), the stored alpha and beta rows with their per-warp offsets
+// at the head, and the utterance's label records, all completing on the
+// slot's full mbarrier.  The workers take the oldest slot while the copies
+// of the next ones are in flight:
+//   1. posteriors: the row's state values from the slot, normalised by the
+//      row's own sum (two passes: the largest exponent, then the sums), and
+//      summed per distinct class in a fixed order (each class by its first
+//      occurrence, walking the next-occurrence links; no atomics on values,
+//      bitwise reproducible);
+//   2. the dense row: scale * exp(lp) for every element, read from the slot
+//      and stored as 16-byte vectors (the ragged chunks at the ends element
+//      by element);
+//   3. after a team barrier (so that it lands after the dense store), each
+//      class sum rewrites its own element: scale * exp(lp) - scale * P,
+//      rounded once into the row's dtype.
+// The slot is then handed back to the producer.  Every wait is bounded (2 s):
+// a wait that gives up sets CTC_PACKED_DEV_WAIT_TIMEOUT and the team stops.
 //
 // Work: team g of the G teams of the grid takes rows g, g + G, ...; its
 // producer finds each row's utterance by walking cu_seqlens forward (rows
-// only grow) and writes rows outside every utterance as zero rows.
+// only grow) and hands rows outside every utterance over as zero rows.
 #include "ctc_common.cuh"
 #include "ctc_kernels.h"
 
