@@ -338,3 +338,17 @@ def test_vocabulary_wider_than_shared_memory(cuda_device, monkeypatch, dtype, st
     ref_loss, ref_grad, _ = _ref(batch)
     assert_loss_close(loss, ref_loss)
     assert_grad_close(grad, ref_grad, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_vocabulary_at_the_limit(cuda_device, dtype):
+    # D = 2^20, the widest row the library takes (4 MB in fp32): the row is
+    # streamed in 2 KB batches, the class sums bucketed by batch
+    D = 1 << 20
+    batch = workloads.make_batch([9, 6], [3, 2], D, dtype=dtype, seed=34, label_high=D - 1, reduction="mean",
+                                 gaps=[1, 0])
+    loss, grad, status = run_gpu(batch)
+    assert status == 0
+    ref_loss, ref_grad, _ = _ref(batch)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)
