@@ -36,8 +36,9 @@
 //   beta    one CTA per utterance: the label analysis (distinct classes in
 //           target order), then the backward recursion from the last frame;
 //           per frame the posteriors and their sum per distinct class
-//   grad    one warp per row: scale * exp(lp) for every class, then each
-//           class sum rewrites its element, scale * exp(lp) - scale * P
+//   grad    one warp per row: scale * exp(lp) for every class (a table-driven
+//           exp, see exp_table), then each class sum rewrites its element,
+//           scale * exp(lp) - scale * P
 // Every sum runs in a fixed order, so results are bitwise reproducible.
 #include <cmath>
 #include <cstdint>
@@ -171,6 +172,36 @@ __device__ __forceinline__ X64 x_from_log(double x) {
     if (k > (double)(1 << 30)) return X64{__longlong_as_double(0x7ff0000000000000ll), 0};
     const double r = fma(-k, kLn2D, x);
     return x_norm(exp(r), (long long)k);
+}
+
+// exp(x) by Tang's table-driven method (P. T. P. Tang, "Table-driven
+// implementation of the exponential function in IEEE floating-point
+// arithmetic", ACM TOMS 15(2), 1989), shaped for a part with a narrow float64
+// pipe.  x = (64 k + j) ln2/64 + r, with n = 64 k + j = round(x * 64/ln2)
+// taken in float32: a rounding off by one only leaves |r| < ln2/64.  Then r
+// is formed in float64 by one fused multiply-add, and exp(r) = 1 + r + q with
+// q = r^2/2 + r^3/6 + r^4/24 in float32: |q| < 6e-5, so float32 rounds it to
+// within 4e-12, and the dropped r^5/120 is below 1.3e-12.  Finally
+// exp(x) = 2^k * T[j] * (1 + r + q), with T[j] = 2^(j/64) from a table the
+// caller fills (shared memory), and 2^k added to the exponent field.  The
+// relative error is below about 1e-11; the gradient it feeds is held to
+// 1e-10.  Arguments outside [-700, 700], NaN and infinities take the
+// library exp.
+__device__ __forceinline__ double exp_table(double x, const double* T) {
+    const float xf = (float)x;
+    if (!(fabsf(xf) <= 700.0f)) return exp(x);
+    const int n = __float2int_rn(xf * 92.332482616893656f);  // 64 / ln 2
+    const double r = fma(-(double)n, 0.010830424696249145, x);  // ln 2 / 64 (exact in float64)
+    const float rf = (float)r;
+    const float q = rf * rf * fmaf(rf, fmaf(rf, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f);
+    const double t = T[n & 63];
+    const double y = fma(t, r + (double)q, t);  // in [1, 2.05): a normal number
+    return __longlong_as_double(__double_as_longlong(y) + ((long long)(n >> 6) << 52));
+}
+
+// Fills the 64-entry table of exp_table (2^(j/64)); the caller synchronises.
+__device__ __forceinline__ void fill_exp_table(double* T) {
+    if (threadIdx.x < 64) T[threadIdx.x] = exp2((double)threadIdx.x * (1.0 / 64.0));
 }
 
 __device__ __forceinline__ X64 ld_em(const EmX* p) {
@@ -309,6 +340,9 @@ __global__ void __launch_bounds__(1024) f64_prep_kernel(F64Args a) {
 // Row log-sum-exp of logits: max, then the sum of exp(z - max).  A NaN or
 // +inf logit gives NaN, a row of -inf gives -inf.
 __global__ void __launch_bounds__(kRowWarps * 32) f64_lse_kernel(F64Args a) {
+    __shared__ double s_exp[64];
+    fill_exp_table(s_exp);
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     double* lse = ws_at<double>(a.ws, a.L.off_lse);
     const int D = a.D;
@@ -327,7 +361,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_lse_kernel(F64Args a) {
         bad = __any_sync(0xffffffffu, bad);
         double s = 0.0;
         if (!bad && m > -INFINITY)
-            for (int c = lane; c < D; c += 32) s += exp(__ldg(z + c) - m);
+            for (int c = lane; c < D; c += 32) s += exp_table(__ldg(z + c) - m, s_exp);
         s = warp_sum(s);
         if (lane == 0)
             lse[row] = bad ? __longlong_as_double(0x7ff8000000000000ll) : (m == -INFINITY ? m : m + log(s));
@@ -697,6 +731,9 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
 // The dense gradient: one warp per row.  A row outside every utterance's
 // frames (or of a malformed utterance, or after a loss-only forward) is 0.
 __global__ void __launch_bounds__(kRowWarps * 32) f64_grad_kernel(F64Args a) {
+    __shared__ double s_exp[64];
+    fill_exp_table(s_exp);
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
@@ -730,19 +767,19 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_grad_kernel(F64Args a) {
         int c = lane;
         for (; c + 96 < D; c += 128) {
             const double x0 = __ldg(x + c), x1 = __ldg(x + c + 32), x2 = __ldg(x + c + 64), x3 = __ldg(x + c + 96);
-            g[c] = scale * exp(x0 - sh);
-            g[c + 32] = scale * exp(x1 - sh);
-            g[c + 64] = scale * exp(x2 - sh);
-            g[c + 96] = scale * exp(x3 - sh);
+            g[c] = scale * exp_table(x0 - sh, s_exp);
+            g[c + 32] = scale * exp_table(x1 - sh, s_exp);
+            g[c + 64] = scale * exp_table(x2 - sh, s_exp);
+            g[c + 96] = scale * exp_table(x3 - sh, s_exp);
         }
-        for (; c < D; c += 32) g[c] = scale * exp(__ldg(x + c) - sh);
+        for (; c < D; c += 32) g[c] = scale * exp_table(__ldg(x + c) - sh, s_exp);
         if (scale != 0.0) {
             __syncwarp();  // the dense stores land before the class sums rewrite their elements
             const double* er = ent + row * a.L.ecap;
             const int32_t* cl = cls + (size_t)b * a.L.Ep;
             for (int k = lane; k < u.ncls; k += 32) {
                 const int cc = cl[k];
-                g[cc] = fma(scale, exp(__ldg(x + cc) - sh), er[k]);
+                g[cc] = fma(scale, exp_table(__ldg(x + cc) - sh, s_exp), er[k]);
             }
         }
     }
