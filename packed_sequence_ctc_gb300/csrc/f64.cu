@@ -174,28 +174,60 @@ __device__ __forceinline__ X64 x_from_log(double x) {
     return x_norm(exp(r), (long long)k);
 }
 
+// Exact conversions by the numbers' bits, on the integer pipe (this part's
+// float64 pipe is narrow, and its conversions would use it):
+// a float64 in (2^-126, 2^127) to the float32 with its leading 24 bits
+// (truncated; smaller magnitudes give 0) ...
+__device__ __forceinline__ float f64_to_f32_bits(double x) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(x);
+    const int e = (int)((u >> 52) & 0x7ff) - 896;  // float32 exponent field
+    if (e <= 0) return 0.0f;
+    return __uint_as_float((unsigned)(u >> 32 & 0x80000000ull) | ((unsigned)e << 23) | (unsigned)(u >> 29 & 0x7fffff));
+}
+// ... a non-negative normal float32 (or 0) to float64, exactly ...
+__device__ __forceinline__ double f32_to_f64_bits(float f) {
+    const unsigned b = __float_as_uint(f);
+    if ((b & 0x7fffffffu) == 0) return 0.0;
+    return __longlong_as_double((long long)((unsigned long long)(b >> 31) << 63 |
+                                            (unsigned long long)((b >> 23 & 0xff) + 896) << 52 |
+                                            (unsigned long long)(b & 0x7fffff) << 29));
+}
+// ... and an int of magnitude below 2^30 to float64, exactly.
+__device__ __forceinline__ double int_to_f64_bits(int n) {
+    if (n == 0) return 0.0;
+    const unsigned a = (unsigned)(n < 0 ? -n : n);
+    const int lz = __clz(a);
+    // the bits below the leading one, moved to the top of the 52-bit field
+    const unsigned long long frac = ((unsigned long long)a << (lz + 21)) & 0xfffffffffffffull;
+    return __longlong_as_double((long long)((unsigned long long)(n < 0) << 63 |
+                                            (unsigned long long)(1023 + 31 - lz) << 52 | frac));
+}
+
 // exp(x) by Tang's table-driven method (P. T. P. Tang, "Table-driven
 // implementation of the exponential function in IEEE floating-point
 // arithmetic", ACM TOMS 15(2), 1989), shaped for a part with a narrow float64
-// pipe.  x = (64 k + j) ln2/64 + r, with n = 64 k + j = round(x * 64/ln2)
-// taken in float32: a rounding off by one only leaves |r| < ln2/64.  Then r
-// is formed in float64 by one fused multiply-add, and exp(r) = 1 + r + q with
-// q = r^2/2 + r^3/6 + r^4/24 in float32: |q| < 6e-5, so float32 rounds it to
-// within 4e-12, and the dropped r^5/120 is below 1.3e-12.  Finally
-// exp(x) = 2^k * T[j] * (1 + r + q), with T[j] = 2^(j/64) from a table the
-// caller fills (shared memory), and 2^k added to the exponent field.  The
-// relative error is below about 1e-11; the gradient it feeds is held to
-// 1e-10.  Arguments outside [-700, 700], NaN and infinities take the
-// library exp.
+// pipe: three float64 operations an element.  x = (64 k + j) ln2/64 + r,
+// with n = 64 k + j = round(x * 64/ln2) taken in float32: a rounding off by
+// one only leaves |r| < ln2/64.  Then r is formed in float64 by one fused
+// multiply-add, and exp(r) = 1 + r + q with q = r^2/2 + r^3/6 + r^4/24 in
+// float32: |q| < 6e-5, so float32 rounds it to within 4e-12, and the dropped
+// r^5/120 is below 1.3e-12.  Finally exp(x) = 2^k * T[j] * (1 + r + q), with
+// T[j] = 2^(j/64) from a table the caller fills (shared memory), and 2^k
+// added to the exponent field.  A table c * 2^(j/64) gives c * exp(x) (the
+// caller keeps c * exp(x) a normal number).  The relative error is below
+// about 1e-11; the gradient it feeds is held to 1e-10.  |x| >= 512, NaN and
+// infinities take the library exp, times T[0] (the test is on the exponent
+// field).
 __device__ __forceinline__ double exp_table(double x, const double* T) {
-    const float xf = (float)x;
-    if (!(fabsf(xf) <= 700.0f)) return exp(x);
+    const unsigned long long u = (unsigned long long)__double_as_longlong(x);
+    if ((u >> 52 & 0x7ff) >= 1023 + 9) return T[0] * exp(x);  // T[0]: the table's own factor
+    const float xf = f64_to_f32_bits(x);
     const int n = __float2int_rn(xf * 92.332482616893656f);  // 64 / ln 2
-    const double r = fma(-(double)n, 0.010830424696249145, x);  // ln 2 / 64 (exact in float64)
-    const float rf = (float)r;
-    const float q = rf * rf * fmaf(rf, fmaf(rf, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f);
+    const double r = fma(-int_to_f64_bits(n), 0.010830424696249145, x);  // ln 2 / 64 (exact in float64)
+    const float rf = f64_to_f32_bits(r);
+    const float q = rf * rf * fmaf(rf, fmaf(rf, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f);  // >= 0
     const double t = T[n & 63];
-    const double y = fma(t, r + (double)q, t);  // in [1, 2.05): a normal number
+    const double y = fma(t, r + f32_to_f64_bits(q), t);  // in [1, 2.05): a normal number
     return __longlong_as_double(__double_as_longlong(y) + ((long long)(n >> 6) << 52));
 }
 
@@ -732,9 +764,11 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
 // frames (or of a malformed utterance, or after a loss-only forward) is 0.
 __global__ void __launch_bounds__(kRowWarps * 32) f64_grad_kernel(F64Args a) {
     __shared__ double s_exp[64];
+    __shared__ double s_sexp[kRowWarps][64];  // per warp: scale * 2^(j/64) of its current row
     fill_exp_table(s_exp);
     __syncthreads();
     const int lane = threadIdx.x & 31;
+    double* sexp = s_sexp[threadIdx.x >> 5];
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
     const double* lse = ws_at<double>(a.ws, a.L.off_lse);
@@ -764,22 +798,32 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_grad_kernel(F64Args a) {
         }
         const double scale = f64_scale(a, u, b, tl_total);
         const double sh = logits ? lse[row] : 0.0;
+        // scale * exp(x) = exp_table(x) on the table scale * 2^(j/64) when
+        // every result stays a normal number (2^-200 <= |scale| <= 2^200 and
+        // the table's |x| < 512): one multiply a table entry, not an element
+        const int se = (int)((unsigned long long)__double_as_longlong(scale) >> 52 & 0x7ff);
+        const bool folded = se >= 1023 - 200 && se <= 1023 + 200;
+        __syncwarp();
+        sexp[lane] = scale * s_exp[lane];
+        sexp[lane + 32] = scale * s_exp[lane + 32];
+        __syncwarp();
+        auto sexp_of = [&](double v) { return folded ? exp_table(v, sexp) : scale * exp_table(v, s_exp); };
         int c = lane;
         for (; c + 96 < D; c += 128) {
             const double x0 = __ldg(x + c), x1 = __ldg(x + c + 32), x2 = __ldg(x + c + 64), x3 = __ldg(x + c + 96);
-            g[c] = scale * exp_table(x0 - sh, s_exp);
-            g[c + 32] = scale * exp_table(x1 - sh, s_exp);
-            g[c + 64] = scale * exp_table(x2 - sh, s_exp);
-            g[c + 96] = scale * exp_table(x3 - sh, s_exp);
+            g[c] = sexp_of(x0 - sh);
+            g[c + 32] = sexp_of(x1 - sh);
+            g[c + 64] = sexp_of(x2 - sh);
+            g[c + 96] = sexp_of(x3 - sh);
         }
-        for (; c < D; c += 32) g[c] = scale * exp_table(__ldg(x + c) - sh, s_exp);
+        for (; c < D; c += 32) g[c] = sexp_of(__ldg(x + c) - sh);
         if (scale != 0.0) {
             __syncwarp();  // the dense stores land before the class sums rewrite their elements
             const double* er = ent + row * a.L.ecap;
             const int32_t* cl = cls + (size_t)b * a.L.Ep;
             for (int k = lane; k < u.ncls; k += 32) {
                 const int cc = cl[k];
-                g[cc] = fma(scale, exp_table(__ldg(x + cc) - sh, s_exp), er[k]);
+                g[cc] = sexp_of(__ldg(x + cc) - sh) + er[k];
             }
         }
     }

@@ -226,15 +226,17 @@ def test_autograd_wrapper(cuda_device):
     assert_close64(lp.grad.cpu().numpy(), ref_grad, "grad")
 
 
-def test_unnormalised_rows_over_a_wide_range(cuda_device):
+@pytest.mark.parametrize("reduction,grad_loss", [("sum", 1.0), ("mean", -2.5)])
+def test_unnormalised_rows_over_a_wide_range(cuda_device, reduction, grad_loss):
     # raw rows with values in [-720, 5]: the dense exp's table covers
-    # [-700, 700] and hands the rest to the library exp; every element is
-    # compared with the oracle's
-    batch = workloads.make_batch([40, 31], [6, 5], 257, dtype=torch.float64, seed=61, reduction="sum")
+    # |x| < 512 and hands the rest to the library exp, scaled like the table
+    # (the upstream factor folded into it); every element is compared with
+    # the oracle's
+    batch = workloads.make_batch([40, 31], [6, 5], 257, dtype=torch.float64, seed=61, reduction=reduction)
     gen = torch.Generator().manual_seed(62)
     batch.log_probs = torch.rand(batch.log_probs.shape, generator=gen, dtype=torch.float64) * 725.0 - 720.0
-    loss, grad, status = run_f64(batch)
+    loss, grad, status = run_f64(batch, grad_loss=[grad_loss])
     assert status == 0
-    ref_loss, ref_grad, _ = _ref(batch)
+    ref_loss, ref_grad, _ = _ref(batch, grad_loss=[grad_loss])
     assert_close64(loss, ref_loss, "loss")
     assert_close64(grad, ref_grad, "grad")
