@@ -152,10 +152,24 @@ __device__ __forceinline__ X64 x_norm(double m, long long e) {
     return X64{__longlong_as_double((bits & 0x800fffffffffffffll) | (1023ll << 52)), (int)ne};
 }
 
+// m * 2^d for d <= 0, by the exponent field (integer operations: this
+// part's float64 pipe is narrow).  m is a normal number whose exponent field
+// exceeds -d (a mantissa in [1, 4): the result stays normal down to
+// d = -1022), or 0, NaN or infinity, which come back unchanged (NaN and
+// infinity only with d = 0, as the largest term of a sum); terms scaled
+// below 2^-1022 are 0.
+__device__ __forceinline__ double scale_pow2_nonpos(double m, long long d) {
+    const long long bits = __double_as_longlong(m);
+    const long long ex = (bits >> 52) & 0x7ff;
+    if (ex == 0 || ex == 0x7ff) return m;
+    if (ex + d < 1) return 0.0;
+    return __longlong_as_double(bits + (d << 52));
+}
+
 __device__ __forceinline__ X64 x_add3(X64 a, X64 b, X64 c) {
     const int E = max(a.e, max(b.e, c.e));
-    const double m = a.m * pow2_ll((long long)a.e - E) + b.m * pow2_ll((long long)b.e - E) +
-                     c.m * pow2_ll((long long)c.e - E);
+    const double m = scale_pow2_nonpos(a.m, (long long)a.e - E) + scale_pow2_nonpos(b.m, (long long)b.e - E) +
+                     scale_pow2_nonpos(c.m, (long long)c.e - E);
     return x_norm(m, E);
 }
 
@@ -719,7 +733,11 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                     be = x_add3(v0, v1, v2);
                 }
                 gn[k] = x_mul(be, et[k]);
-                const double g = al[k].m * be.m * invz * pow2_ll((long long)al[k].e + be.e - ze);
+                // (mantissa product in [0.25, 4) or 0) * 2^(exponents - ze); a
+                // posterior is at most 1, so the exponent sum is at most ~2
+                const long long d = (long long)al[k].e + be.e - ze;
+                const double gm = al[k].m * be.m * invz;
+                const double g = d <= 0 ? scale_pow2_nonpos(gm, d) : gm * pow2_ll(d);
                 gamma[k] = nan_utt ? qnan : g;
             }
         }
