@@ -99,7 +99,7 @@ typedef enum {
     CTC_PACKED_ERR_INVALID_ARGUMENT = 1, /* a host-checkable argument is wrong */
     CTC_PACKED_ERR_WORKSPACE = 2,        /* workspace NULL or smaller than ctc_packed_workspace_size */
     CTC_PACKED_ERR_CUDA = 3,             /* a CUDA runtime call failed (see cudaGetLastError) */
-    CTC_PACKED_ERR_UNSUPPORTED = 4       /* sizes beyond what the kernels support (D > 1048576, max_target_len > 3839; FSA: D > 16384) */
+    CTC_PACKED_ERR_UNSUPPORTED = 4       /* sizes beyond what the kernels support (D > 1048576, max_target_len > 3839; FSA: D > 16384, or max_states and max_labels beyond shared memory) */
 } ctc_packed_status;
 
 /* Bits of the device status word (ctc_packed_read_status). */
@@ -335,10 +335,13 @@ ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_d
  * scale_b * (exp(lp[t, c]) - sum of the occupancies of frame t's edges with
  * label c), scale_b = grad_loss[b] (0 for an infinite loss), and 0 on rows
  * outside every sequence; the page's gradient convention (the gradient with
- * respect to the logits of a log_softmax).  The recursions run in float32 log
- * space; every sum runs in a fixed order (each sequence's edges are sorted
- * once per forward into per-state and per-label lists), so results are
- * bitwise reproducible.
+ * respect to the logits of a log_softmax).  The recursions carry float32
+ * mantissas with integer exponents (no underflow at any length); every sum
+ * runs in a fixed order (each sequence's edges are sorted once per forward
+ * into per-state and per-label lists), so results are bitwise reproducible.
+ * max_states and max_labels together bound a recursion's shared memory:
+ * about 52 bytes a state and 44 a label (36 and 36 above 2048 states) must
+ * fit in 224 KB, else CTC_PACKED_ERR_UNSUPPORTED (the workspace size is 0).
  *
  * All pointers are device memory; log_probs is 4-byte aligned for every
  * dtype.  Errors the host can see return before

@@ -19,20 +19,24 @@
 //   beta_T(s) = final(s),   beta_t(s) = logsumexp_{e=(s,s',c,w)} w + lp[t, c] + beta_{t+1}(s')
 //   grad[t, c] = scale * (exp(lp[t, c]) - sum_{e with label c} exp(alpha_t(s) + w + lp[t, c] + beta_{t+1}(s') - Z))
 //
-// Every sum runs in a fixed order, so results are bitwise reproducible:
+// The recursions carry every value in extended range, as the CTC chain
+// does: a float mantissa and an int exponent (exp of a log weight or log
+// probability via xp_from_log).  An edge's term is the product of three such
+// values and a sum aligns its terms to the largest exponent, so a frame needs
+// no shift, no exp and no log; Z keeps its exponent, and an occupancy is a
+// product divided by Z, formed directly as a float.  Every sum runs in a
+// fixed order, so results are bitwise reproducible:
 //   index    one CTA per sequence, once per forward: the edges sorted stably
 //            (counting sort; ties keep the edge order) by destination, by
 //            source and by label, as per-state and per-label lists; the
 //            sequence's distinct labels (at most max_labels) in increasing
 //            order, and each edge's slot among them.
 //   forward  one CTA per sequence, a thread per destination state (or a
-//            few): alpha_{t+1}(s') is a running log-sum-exp over the state's
-//            incoming edges in list order.  The label values of frame t + 1
-//            load during frame t; one barrier per frame.  Each frame's
-//            values are shifted by their maximum (the running shift is kept
-//            by one thread, stored as a float pair), so their float32
-//            rounding stays relative to the frame; alpha_t is stored for the
-//            backward with its shift.
+//            few): alpha_{t+1}(s') is the sum over the state's incoming
+//            edges in list order.  The words holding frame t + 1's label
+//            values are copied ahead and converted to extended range by the
+//            threads that copied them during frame t; one barrier per frame.
+//            alpha_t is stored (8 bytes a state) for the backward.
 //   backward one CTA per sequence, a thread per source state: beta_t(s)
 //            over the state's outgoing edges in list order, each edge's
 //            occupancy into a double-buffered per-edge array at the edge's
@@ -50,21 +54,23 @@ namespace ctcp {
 namespace {
 
 constexpr int kIdxThreads = 256;      // threads of the index kernel
-constexpr int kFsaMaxThreads = 512;   // threads of a recursion CTA (states per thread <= 8)
-constexpr int kRing = 4;              // frames of label values (and alpha rows) in flight: kRing - 1 ahead
-constexpr int kFsaSmemBudget = 200 * 1024;  // shared memory of a recursion CTA
+constexpr int kFsaMaxThreads = 512;   // threads of a recursion CTA (states per thread <= 8); the
+                                      // recursions are declared for one CTA an SM: left free, the
+                                      // compiler trades registers for occupancy (40 with spills),
+                                      // and one CTA's frame chain ran 1.9 times slower
+constexpr int kFsaSmemBudget = 200 * 1024;  // shared memory of a recursion CTA, edge lists included
+constexpr int kFsaSmemLimit = 224 * 1024;   // its per-frame buffers alone (larger plans are rejected)
 constexpr int kShortList = 8;         // label lists up to this long are summed by one thread, longer by a warp
 
-// Workspace of the FSA path.  Per sequence: log Z (double) and the number of
-// distinct labels (-1: the sequence was rejected); per frame: the forward
-// values relative to the frame's shift (float) and that shift as an
-// unevaluated float pair hi + lo (about 48 bits: the recursions keep float64
-// arithmetic, slow on this part, out of their per-frame path); per
-// row: the class-sum header and sums read by the gradient stream; per state:
+// Workspace of the FSA path.  Per sequence: log Z (double), Z in extended
+// range, and the number of distinct labels (-1: the sequence was rejected);
+// per frame: the forward values of every state in extended range; per row:
+// the class-sum header and sums read by the gradient stream; per state:
 // offsets of its incoming and outgoing edge lists; per edge: the records of
-// both lists, the label lists and the occupancies of two frames.
+// both lists, each edge's position in label order and the occupancies of two
+// frames.
 struct FsaLayout {
-    size_t off_z, off_nlab, off_coff, off_alpha, off_head, off_ent;
+    size_t off_z, off_nlab, off_zx, off_alpha, off_head, off_ent;
     size_t off_inoff, off_outoff, off_rin, off_rout, off_lpos, off_tmp, off_labs, off_laboff, off_occ, total;
     int cap;       // class sums a row can hold: min(max_labels, D)
     int E_total;   // edges of all sequences (the occupancy buffers' stride)
@@ -78,8 +84,8 @@ __host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int3
     size_t o = 256;  // the status word sits at offset 0, as in the CTC workspace
     L.off_z = o;      o = align_up(o + sizeof(double) * Bn, 256);
     L.off_nlab = o;   o = align_up(o + sizeof(int32_t) * Bn, 256);
-    L.off_coff = o;   o = align_up(o + sizeof(double) * (size_t)T_total, 256);
-    L.off_alpha = o;  o = align_up(o + sizeof(float) * (size_t)T_total * (size_t)max_states, 256);
+    L.off_zx = o;     o = align_up(o + 8 * Bn, 256);
+    L.off_alpha = o;  o = align_up(o + 8 * (size_t)T_total * (size_t)max_states, 256);
     // per row: a header and the row's class sums, in the format the dense
     // gradient stream of the CTC path reads
     L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
@@ -239,58 +245,63 @@ __device__ void place_stable(int E, KeyF key, int* cursor, int* out) {
     }
 }
 
-// Block-wide logsumexp of v[0 .. n) + w[0 .. n), fixed order.
-__device__ float block_lse(const float* v, const float* w, int n, float* red) {
-    float m = -INFINITY;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, v[i] + w[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    m = -INFINITY;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
-    __syncthreads();
-    float s = 0.0f;
-    if (m > -INFINITY)
-        for (int i = threadIdx.x; i < n; i += blockDim.x) s += expf(v[i] + w[i] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-    __syncthreads();
-    s = 0.0f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
-    __syncthreads();
-    return m > -INFINITY ? m + logf(s) : -INFINITY;
+// 8-byte loads and stores of an extended value (its arrays are 8-byte aligned).
+__device__ __forceinline__ XP ld_xp(const XP* p) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    return XP{__uint_as_float(v.x), (int)v.y};
+}
+__device__ __forceinline__ void st_xp(XP* p, XP x) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(__float_as_uint(x.m), (unsigned)x.e);
 }
 
-// Running log-sum-exp (m, s): the sum is s * exp(m); -inf terms are skipped.
-__device__ __forceinline__ void lse_push(float& m, float& s, float v) {
-    if (!(v > -INFINITY)) return;
-    if (v > m) {
-        s = s * expf(m - v) + 1.0f;
-        m = v;
-    } else {
-        s += expf(v - m);
+// exp(v) in extended range; a NaN stays in the mantissa, so every sum it
+// enters is NaN.
+__device__ __forceinline__ XP xp_exp(float v) {
+    XP r = xp_from_log(v);
+    if (v != v) r.m = v;
+    return r;
+}
+
+// Product of three extended values.  A zero product takes the zero exponent,
+// so that no sum aligns on it.
+__device__ __forceinline__ XP xp_mul3(XP a, XP b, XP c) {
+    XP r;
+    r.m = a.m * b.m * c.m;
+    r.e = r.m > 0.0f ? a.e + b.e + c.e : kEZero;
+    return r;
+}
+
+// 2^k as a float for any k: 0 below 2^-126, 2^127 above.
+__device__ __forceinline__ float pow2_any(int k) { return __int_as_float(min(max(127 + k, 0), 254) << 23); }
+
+// Running sum S * 2^E of extended values in a fixed order: the sum and each
+// new term are aligned to the larger exponent (a term 2^126 below it drops
+// out).  S stays finite: every term's mantissa is below 8.
+struct XSum {
+    float S = 0.0f;
+    int E = kEZero;
+    __device__ __forceinline__ void add(XP x) {
+        const int E2 = max(E, x.e);
+        S = fmaf(S, pow2_nonpos(E - E2), x.m * pow2_nonpos(x.e - E2));
+        E = E2;
     }
-}
-__device__ __forceinline__ float lse_value(float m, float s) { return s > 0.0f ? m + logf(s) : -INFINITY; }
+};
 
-// Error-free sum (Knuth's TwoSum): a + b = s + err exactly, in float32.
-__device__ __forceinline__ float two_sum(float a, float b, float& err) {
-    const float s = a + b;
-    const float bb = s - a;
-    err = (a - (s - bb)) + (b - bb);
-    return s;
-}
-
-// Maximum over the warp maxima of the CTA (what the last barrier published),
-// every warp reducing the nw values by shuffles.
-__device__ __forceinline__ float max_of(const float* wmax, int nw) {
-    const int lane = threadIdx.x & 31;
-    float m = lane < nw ? wmax[lane] : -INFINITY;
+// Sum over the CTA of every thread's partial sum: the lanes by a fixed
+// shuffle tree, then the warps in order (every thread gets the result).
+__device__ __forceinline__ XSum block_xsum(XSum a, XP* red) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    return m;
+    for (int o = 16; o > 0; o >>= 1) a.add(XP{__shfl_xor_sync(0xffffffffu, a.S, o), __shfl_xor_sync(0xffffffffu, a.E, o)});
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = XP{a.S, a.E};
+    __syncthreads();
+    XSum r;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r.add(red[i]);
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
 
 }  // namespace
@@ -362,7 +373,8 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     for (int k = threadIdx.x; k < E; k += blockDim.x) lpos[tmp[k]] = k;
     __syncthreads();
 
-    // 2. incoming lists (by destination): records (from, label slot, weight, edge)
+    // 2. incoming lists (by destination): records (from, label slot, exp of
+    //    the weight in extended range: mantissa bits, exponent)
     int* inoff = ws_at<int32_t>(a.ws, a.L.off_inoff) + s0 + b;
     for (int s = threadIdx.x; s < S; s += blockDim.x) cnt[s] = 0;
     __syncthreads();
@@ -373,12 +385,13 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     int4* rin = ws_at<int4>(a.ws, a.L.off_rin) + e0;
     for (int k = threadIdx.x; k < E; k += blockDim.x) {
         const int e = tmp[k];
-        rin[k] = make_int4(ed[3 * e], slot[ed[3 * e + 2]], __float_as_int(ew[e]), e);
+        const XP w = xp_exp(ew[e]);
+        rin[k] = make_int4(ed[3 * e], slot[ed[3 * e + 2]], __float_as_int(w.m), w.e);
     }
     __syncthreads();
 
-    // 3. outgoing lists (by source): records (to, label slot, weight, the
-    //    edge's position in label order)
+    // 3. outgoing lists (by source): records (to, label slot, log weight,
+    //    the edge's position in label order)
     int* outoff = ws_at<int32_t>(a.ws, a.L.off_outoff) + s0 + b;
     for (int s = threadIdx.x; s < S; s += blockDim.x) cnt[s] = 0;
     __syncthreads();
@@ -394,6 +407,11 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     if (threadIdx.x == 0) nlab_out[b] = nlab;
 }
 
+// Frames of label words (and, backward, stored alpha rows) a recursion CTA
+// keeps in flight, ring - 1 ahead of the frame it computes: 4, or 2 for
+// sequences of more than 4 states a thread (their rows would not fit).
+__host__ __device__ constexpr int fsa_ring(int per) { return per > 4 ? 2 : 4; }
+
 // Shared-memory plan of a recursion CTA (see FsaArgs::ecap_smem): the
 // sequence's edge lists when it has at most ecap_smem edges, then the
 // per-frame buffers.
@@ -401,16 +419,16 @@ struct FsaSmem {
     int4* rec;        // edge records of the list (incoming or outgoing), ecap_smem
     int* off;         // list offsets per state, Smax + 1
     float* occ;       // (backward) occupancies of two frames, 2 * ecap_smem
-    float* val;       // alpha or beta of two frames, 2 * Smax
+    XP* val;          // alpha or beta of two frames, 2 * Smax
+    XP* lpx;          // exp of the label values of two frames, 2 * cap
     int* longl;       // (backward) the labels with long edge lists, cap
-    uint32_t* ring;   // words holding the label values of kRing frames, kRing * cap
-    float* aring;     // (backward) stored alpha rows of kRing frames, kRing * Smax
-    float2* cring;    // (backward) the stored rows' shifts of kRing frames (float pairs)
+    uint32_t* ring;   // words holding the label values of `ring` frames, ring * cap
+    XP* aring;        // (backward) stored alpha rows of `ring` frames, ring * Smax
     int* labs;        // the distinct labels, cap
     int* laboff;      // (backward) label list offsets, cap + 1
 };
-__host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Smax, int cap, unsigned char* base,
-                                                FsaSmem* out) {
+__host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Smax, int cap, int ring_frames,
+                                                unsigned char* base, FsaSmem* out) {
     size_t o = 0;
     auto take = [&](size_t bytes, size_t align) {
         o = align_up(o, align);
@@ -421,22 +439,22 @@ __host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Sma
     const size_t rec = take(16 * (size_t)ecap, 16);
     const size_t off = take(4 * ((size_t)Smax + 1), 4);
     const size_t occ = backward ? take(8 * (size_t)ecap, 4) : 0;
-    const size_t val = take(8 * (size_t)Smax, 4);
+    const size_t val = take(16 * (size_t)Smax, 8);
+    const size_t lpx = take(16 * (size_t)cap, 8);
     const size_t longl = backward ? take(4 * (size_t)cap, 4) : 0;
-    const size_t ring = take(4 * (size_t)kRing * cap, 4);
-    const size_t aring = backward ? take(4 * (size_t)kRing * Smax, 4) : 0;
-    const size_t cring = backward ? take(8 * (size_t)kRing, 8) : 0;
+    const size_t ring = take(4 * (size_t)ring_frames * cap, 4);
+    const size_t aring = backward ? take(8 * (size_t)ring_frames * Smax, 8) : 0;
     const size_t labs = take(4 * (size_t)cap, 4);
     const size_t laboff = backward ? take(4 * ((size_t)cap + 1), 4) : 0;
     if (out != nullptr) {
         out->rec = reinterpret_cast<int4*>(base + rec);
         out->off = reinterpret_cast<int*>(base + off);
         out->occ = reinterpret_cast<float*>(base + occ);
-        out->val = reinterpret_cast<float*>(base + val);
+        out->val = reinterpret_cast<XP*>(base + val);
+        out->lpx = reinterpret_cast<XP*>(base + lpx);
         out->longl = reinterpret_cast<int*>(base + longl);
         out->ring = reinterpret_cast<uint32_t*>(base + ring);
-        out->aring = reinterpret_cast<float*>(base + aring);
-        out->cring = reinterpret_cast<float2*>(base + cring);
+        out->aring = reinterpret_cast<XP*>(base + aring);
         out->labs = reinterpret_cast<int*>(base + labs);
         out->laboff = reinterpret_cast<int*>(base + laboff);
     }
@@ -472,16 +490,16 @@ template <int PER, int RE>
 struct EdgeRegs {
     int peer[PER][RE];   // the other state of each edge (source forward, destination backward)
     int slot[PER][RE];   // its label's slot among the sequence's distinct labels
-    float w[PER][RE];    // its log weight
-    int id[PER][RE];     // its edge id (backward: the occupancy's index)
-    int par[PER][RE];    // parity of its label's element in a row starting on a word (2-byte types)
+    XP w[PER][RE];       // exp of its log weight
+    int id[PER][RE];     // (backward) its occupancy's index
     int n[PER];          // edges held (at most RE)
     int k0[PER], k1[PER];  // the rest of the list: entries [k0, k1)
 };
 
-template <int PER, int RE>
-__device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int* off, const int4* rec, int S,
-                                               const int* labs, int base_half) {
+// Forward records hold the weight in extended range, backward ones the log
+// weight and the occupancy's index.
+template <bool BACKWARD, int PER, int RE>
+__device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int* off, const int4* rec, int S) {
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
         const int s = threadIdx.x + k * blockDim.x;
@@ -499,9 +517,13 @@ __device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int*
             const int4 r = j < n ? rec[b0 + j] : make_int4(0, 0, 0, 0);
             er.peer[k][j] = r.x;
             er.slot[k][j] = r.y;
-            er.w[k][j] = __int_as_float(r.z);
-            er.id[k][j] = r.w;
-            er.par[k][j] = (base_half ^ labs[r.y]) & 1;
+            if (BACKWARD) {
+                er.w[k][j] = xp_exp(__int_as_float(r.z));
+                er.id[k][j] = r.w;
+            } else {
+                er.w[k][j] = XP{__int_as_float(r.z), r.w};
+                er.id[k][j] = 0;
+            }
         }
     }
 }
@@ -527,13 +549,23 @@ __device__ __forceinline__ void issue_row(uint32_t* dst, const void* lp, int64_t
     }
 }
 
+// The label values of frame f in extended range, into dst[0 .. nlab): each
+// thread converts the labels whose words it copied (issue_row's mapping), so
+// its own wait for the copies suffices.
+template <int DT>
+__device__ __forceinline__ void convert_row(XP* dst, const uint32_t* lw, const int* labs, int nlab, int flip,
+                                            int base_half) {
+    for (int i = threadIdx.x; i < nlab; i += blockDim.x)
+        st_xp(dst + i, xp_exp(word_to_float<DT>(lw[i], ((base_half ^ labs[i]) & 1) ^ flip)));
+}
+
 template <int DT, int PER>
-__global__ void __launch_bounds__(kFsaMaxThreads) fsa_forward_kernel(FsaArgs a) {
+__global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_forward_kernel(FsaArgs a) {
     constexpr int RE = PER <= 2 ? 3 : (PER == 4 ? 2 : 1);
+    constexpr int RING = fsa_ring(PER);
     extern __shared__ __align__(16) unsigned char fsa_smem[];
-    __shared__ float wmax[2][kFsaMaxThreads / 32];
-    __shared__ float red[kFsaMaxThreads / 32];
-    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
+    __shared__ XP red[kFsaMaxThreads / 32];
+    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
     const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
     if (nlab < 0) return;  // rejected by the index pass (NaN loss written there)
     const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
@@ -542,13 +574,11 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_forward_kernel(FsaArgs a) 
     const int T = a.lengths[b];
     const int Smax = a.max_states, cap = a.L.cap, D = a.D;
     FsaSmem sm;
-    fsa_smem_plan(false, a.ecap_smem, Smax, cap, fsa_smem, &sm);
+    fsa_smem_plan(false, a.ecap_smem, Smax, cap, RING, fsa_smem, &sm);
     const int* inoff_g = ws_at<int32_t>(a.ws, a.L.off_inoff) + s0 + b;
     const int4* rin_g = ws_at<int4>(a.ws, a.L.off_rin) + e0;
     const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
-    double* z_out = ws_at<double>(a.ws, a.L.off_z);
-    float2* coff = ws_at<float2>(a.ws, a.L.off_coff);
-    float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
+    XP* alpha_rows = ws_at<XP>(a.ws, a.L.off_alpha);
     const uintptr_t lp0 = reinterpret_cast<uintptr_t>(a.lp);
     const uintptr_t lp_end = lp0 + (uintptr_t)(a.T_total * (int64_t)D * (DT == 0 ? 4 : 2));
     const int base_half = (int)((lp0 >> 1) & 1);
@@ -562,105 +592,83 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_forward_kernel(FsaArgs a) 
     const int4* rin = local ? sm.rec : rin_g;
     const int* inoff = local ? sm.off : inoff_g;
     for (int i = tid; i < nlab; i += nt) sm.labs[i] = labs_g[i];
-    // label values: the words of frames 0 .. kRing - 2 in flight (thread
-    // i % nt copies label i); a frame's words are read where they land
+    // label words: frames 0 .. RING - 2 in flight (thread i % nt copies and
+    // converts label i)
     auto issue = [&](int f) {
-        if (f < T) issue_row<DT>(sm.ring + (f % kRing) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
+        if (f < T) issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
         cp_async_commit();
     };
-    for (int f = 0; f < kRing - 1; ++f) issue(f);
-    float tm = -INFINITY;
-    for (int s = tid; s < S; s += nt) {
-        const float v = a.start_weight[s0 + s];
-        sm.val[s] = v;
-        tm = fmaxf(tm, v);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-    if ((tid & 31) == 0) wmax[0][tid >> 5] = tm;
-    cp_async_wait<kRing - 2>();
+    for (int f = 0; f < RING - 1; ++f) issue(f);
+    for (int s = tid; s < S; s += nt) st_xp(sm.val + s, xp_exp(a.start_weight[s0 + s]));
+    cp_async_wait<RING - 2>();
+    if (T > 0) convert_row<DT>(sm.lpx, sm.ring, sm.labs, nlab, row_flip(start, D), base_half);
     __syncthreads();
     EdgeRegs<PER, RE> er;
-    load_edge_regs(er, inoff, rin, S, sm.labs, base_half);
-    float c_hi = 0.0f, c_lo = 0.0f;  // the running shift C, a float pair (thread 0 stores it)
-    bool nan_seen = false;  // a NaN edge value: the loss is NaN
+    load_edge_regs<false>(er, inoff, rin, S);
+    bool nan_seen = false;  // a NaN sum: the loss is NaN
     int p = 0;
     for (int t = 0; t < T; ++t) {
-        issue(t + kRing - 1);
-        const float* alp = sm.val + p * Smax;
-        float* alq = sm.val + (p ^ 1) * Smax;
-        const uint32_t* lw = sm.ring + (t % kRing) * cap;  // the frame's label words
-        const int flip = row_flip(start + t, D);
-        // the frame's shift: alpha_t is stored relative to C
-        const float m = max_of(wmax[p], nw);
-        const float sh = (m > -INFINITY && m < INFINITY) ? m : 0.0f;
-        {
-            float e;
-            c_hi = two_sum(c_hi, sh, e);
-            c_lo += e;
-        }
-        if (tid == 0) coff[start + t] = make_float2(c_hi, c_lo);
-        float* row = alpha_rows + (start + t) * (int64_t)Smax;
-        tm = -INFINITY;
+        issue(t + RING - 1);
+        const XP* alp = sm.val + p * Smax;
+        XP* alq = sm.val + (p ^ 1) * Smax;
+        const XP* lx = sm.lpx + (t & 1) * cap;  // the frame's label values
+        XP* row = alpha_rows + (start + t) * (int64_t)Smax;
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const int s = tid + k * nt;
             if (s < S) {
-                row[s] = alp[s] - sh;
-                // the held edges: maximum first, then the sum of exp(v - max)
-                float v[RE], lm = -INFINITY;
+                st_xp(row + s, ld_xp(alp + s));  // alpha_t, read by the backward
+                // alpha_{t+1}(s) = sum over the incoming list, in order, of
+                // alpha_t(from) x exp(weight) x exp(lp[t, label])
+                XSum acc;
 #pragma unroll
-                for (int j = 0; j < RE; ++j) {
-                    v[j] = j < er.n[k] ? alp[er.peer[k][j]] + er.w[k][j] +
-                                             word_to_float<DT>(lw[er.slot[k][j]], er.par[k][j] ^ flip) - sh
-                                       : -INFINITY;
-                    nan_seen |= v[j] != v[j];
-                    lm = fmaxf(lm, v[j]);
-                }
-                float ls = 0.0f;
-                if (lm > -INFINITY) {
-#pragma unroll
-                    for (int j = 0; j < RE; ++j) ls += expf(v[j] - lm);
-                }
-                // the rest of the list, in order
+                for (int j = 0; j < RE; ++j)
+                    if (j < er.n[k]) acc.add(xp_mul3(ld_xp(alp + er.peer[k][j]), er.w[k][j], ld_xp(lx + er.slot[k][j])));
                 for (int kk = er.k0[k]; kk < er.k1[k]; ++kk) {
                     const int4 r = rin[kk];
-                    const float lv = word_to_float<DT>(lw[r.y], ((base_half ^ sm.labs[r.y]) & 1) ^ flip);
-                    const float vv = alp[r.x] - sh + __int_as_float(r.z) + lv;
-                    nan_seen |= vv != vv;
-                    lse_push(lm, ls, vv);
+                    acc.add(xp_mul3(ld_xp(alp + r.x), XP{__int_as_float(r.z), r.w}, ld_xp(lx + r.y)));
                 }
-                const float nv = lse_value(lm, ls);
-                alq[s] = nv;
-                tm = fmaxf(tm, nv);
+                nan_seen |= acc.S != acc.S;
+                st_xp(alq + s, xp_norm(acc.S, acc.E));
             }
         }
-        cp_async_wait<kRing - 2>();
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-        if ((tid & 31) == 0) wmax[p ^ 1][tid >> 5] = tm;
+        cp_async_wait<RING - 2>();
+        if (t + 1 < T)
+            convert_row<DT>(sm.lpx + ((t + 1) & 1) * cap, sm.ring + ((t + 1) % RING) * cap, sm.labs, nlab,
+                            row_flip(start + t + 1, D), base_half);
         __syncthreads();
         p ^= 1;
     }
     cp_async_wait<0>();
-    const float zr = block_lse(sm.val + p * Smax, a.final_weight + s0, S, red);
+    // Z = sum over the states of alpha_T(s) x exp(final(s))
+    XSum zs;
+    for (int s = tid; s < S; s += nt)
+        zs.add(xp_mul3(ld_xp(sm.val + p * Smax + s), xp_exp(a.final_weight[s0 + s]), XP{1.0f, 0}));
+    nan_seen |= zs.S != zs.S;
+    const XSum z = block_xsum(zs, red);
     const bool any_nan = __syncthreads_or(nan_seen) != 0;
     if (tid == 0) {
-        const double C = (double)c_hi + (double)c_lo;
-        const double Z = any_nan ? __longlong_as_double(0x7ff8000000000000ll)
-                                 : (zr > -INFINITY ? C + (double)zr : (double)zr);
-        z_out[b] = Z;
-        float l = (float)-Z;
-        if (a.zero_infinity && Z == -INFINITY) l = 0.0f;
+        const XP zx = any_nan ? XP{0.0f, kEZero} : xp_norm(z.S, z.E);
+        double lz;
+        if (any_nan)
+            lz = __longlong_as_double(0x7ff8000000000000ll);
+        else if (zx.m == 0.0f)
+            lz = -INFINITY;
+        else
+            lz = log((double)zx.m) + (double)zx.e * 0.69314718055994530942;
+        ws_at<double>(a.ws, a.L.off_z)[b] = lz;
+        st_xp(ws_at<XP>(a.ws, a.L.off_zx) + b, zx);
+        float l = (float)-lz;
+        if (a.zero_infinity && lz == -INFINITY) l = 0.0f;
         a.loss[b] = l;
     }
 }
 
 template <int DT, int PER>
-__global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a) {
+__global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs a) {
     constexpr int RE = PER <= 2 ? 3 : (PER == 4 ? 2 : 1);
+    constexpr int RING = fsa_ring(PER);
     extern __shared__ __align__(16) unsigned char fsa_smem[];
-    __shared__ float wmax[2][kFsaMaxThreads / 32];
     const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5, warp = tid >> 5, lane = tid & 31;
     const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
     if (nlab < 0) return;  // the rows keep zero headers: zero gradient
@@ -669,21 +677,27 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a)
     const int64_t start = a.cu[b];
     const int T = a.lengths[b];
     const int Smax = a.max_states, cap = a.L.cap, D = a.D;
-    const double Z = ws_at<double>(a.ws, a.L.off_z)[b];
-    const float2* coff = ws_at<float2>(a.ws, a.L.off_coff);
+    const double lz = ws_at<double>(a.ws, a.L.off_z)[b];
+    RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
     float scale = a.grad_loss[b];
-    if (!(Z > -INFINITY)) scale = 0.0f;  // no path: zero rows (defined only with zero_infinity)
-    // -Z as a float pair, once
-    const float nz_hi = (float)-Z, nz_lo = (float)(-Z - (double)nz_hi);
+    if (!(lz > -INFINITY)) scale = 0.0f;  // no path: zero rows (defined only with zero_infinity)
+    if (scale == 0.0f) {
+        // no occupancy is read: the rows are scale * exp(lp) with no class sums
+        for (int t = tid; t < T; t += nt) head[start + t] = RowHead{0, scale, 1, 0};
+        return;
+    }
+    // an edge's occupancy is alpha_t(s) x (its term) / Z: 1 / Z's mantissa
+    // (in [1, 2)) and its exponent, once
+    const XP zx = ld_xp(ws_at<XP>(a.ws, a.L.off_zx) + b);
+    const float izm = 1.0f / zx.m;
     FsaSmem sm;
-    fsa_smem_plan(true, a.ecap_smem, Smax, cap, fsa_smem, &sm);
+    fsa_smem_plan(true, a.ecap_smem, Smax, cap, RING, fsa_smem, &sm);
     const int* outoff_g = ws_at<int32_t>(a.ws, a.L.off_outoff) + s0 + b;
     const int4* rout_g = ws_at<int4>(a.ws, a.L.off_rout) + e0;
     const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
     const int* laboff_g = ws_at<int32_t>(a.ws, a.L.off_laboff) + (size_t)b * (cap + 1);
     float* occ_g = ws_at<float>(a.ws, a.L.off_occ) + e0;
-    const float* alpha_rows = ws_at<float>(a.ws, a.L.off_alpha);
-    RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
+    const XP* alpha_rows = ws_at<XP>(a.ws, a.L.off_alpha);
     int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
     const uintptr_t lp0 = reinterpret_cast<uintptr_t>(a.lp);
     const uintptr_t lp_end = lp0 + (uintptr_t)(a.T_total * (int64_t)D * (DT == 0 ? 4 : 2));
@@ -693,9 +707,7 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a)
     // memory when they fit
     const bool local = E <= a.ecap_smem;
     if (local) {
-        for (int k = tid; k < E; k += nt) {
-            sm.rec[k] = rout_g[k];
-        }
+        for (int k = tid; k < E; k += nt) sm.rec[k] = rout_g[k];
         for (int s = tid; s <= S; s += nt) sm.off[s] = outoff_g[s];
     }
     const int4* rout = local ? sm.rec : rout_g;
@@ -710,120 +722,72 @@ __global__ void __launch_bounds__(kFsaMaxThreads) fsa_backward_kernel(FsaArgs a)
     // the labels whose lists a warp sums (any order: each sum is one warp's)
     for (int i = tid; i < nlab; i += nt)
         if (sm.laboff[i + 1] - sm.laboff[i] > kShortList) sm.longl[atomicAdd(&s_nlong, 1)] = i;
-    // frame f's label words, its stored alpha row (this thread's states) and
-    // the row's shift (thread 0) are copied kRing - 1 frames ahead
+    // frame f's label words and its stored alpha row (each thread copies its
+    // own states' values) are copied RING - 1 frames ahead
     auto issue = [&](int f) {
         if (f >= 0) {
-            issue_row<DT>(sm.ring + (f % kRing) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
+            issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
             for (int s = tid; s < S; s += nt)
-                cp_async4(smem_addr(sm.aring + (f % kRing) * Smax + s), alpha_rows + (start + f) * (int64_t)Smax + s);
-            if (tid == 0)
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(sm.cring + f % kRing)),
-                             "l"(coff + start + f)
-                             : "memory");
+                cp_async8(smem_addr(sm.aring + (f % RING) * Smax + s), alpha_rows + (start + f) * (int64_t)Smax + s);
         }
         cp_async_commit();
     };
-    for (int j = 0; j < kRing - 1; ++j) issue(T - 1 - j);
-    float tm = -INFINITY;
-    for (int s = tid; s < S; s += nt) {
-        const float v = a.final_weight[s0 + s];
-        sm.val[s] = v;
-        tm = fmaxf(tm, v);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-    if ((tid & 31) == 0) wmax[0][tid >> 5] = tm;
-    cp_async_wait<kRing - 2>();
+    for (int j = 0; j < RING - 1; ++j) issue(T - 1 - j);
+    for (int s = tid; s < S; s += nt) st_xp(sm.val + s, xp_exp(a.final_weight[s0 + s]));
+    cp_async_wait<RING - 2>();
+    if (T > 0)
+        convert_row<DT>(sm.lpx + ((T - 1) & 1) * cap, sm.ring + ((T - 1) % RING) * cap, sm.labs, nlab,
+                        row_flip(start + T - 1, D), base_half);
     __syncthreads();
     const int nlong = s_nlong;
     EdgeRegs<PER, RE> er;
-    load_edge_regs(er, outoff, rout, S, sm.labs, base_half);
-    float dn_hi = 0.0f, dn_lo = 0.0f;  // the running shift Dn, a float pair
+    load_edge_regs<true>(er, outoff, rout, S);
     int p = 0;
     for (int t = T - 1; t >= 0; --t) {
-        issue(t - (kRing - 1));
-        const float* bep = sm.val + p * Smax;
-        float* beq = sm.val + (p ^ 1) * Smax;
-        const uint32_t* lw = sm.ring + (t % kRing) * cap;  // the frame's label words
-        const int flip = row_flip(start + t, D);
-        const float* arow = sm.aring + (t % kRing) * Smax;
+        issue(t - (RING - 1));
+        const XP* bep = sm.val + p * Smax;  // beta_{t+1}
+        XP* beq = sm.val + (p ^ 1) * Smax;
+        const XP* lx = sm.lpx + (t & 1) * cap;  // the frame's label values
+        const XP* arow = sm.aring + (t % RING) * Smax;
         float* occ = occ_base + (size_t)(t & 1) * occ_stride;
-        const float m = max_of(wmax[p], nw);
-        const float sh = (m > -INFINITY && m < INFINITY) ? m : 0.0f;
-        {
-            float e;
-            dn_hi = two_sum(dn_hi, sh, e);  // beta_{t+1} = bep - sh + Dn
-            dn_lo += e;
-        }
-        // occupancy exponent: alpha row + edge value (shifted beta) + this
-        // constant, K = coff_t + Dn - Z, summed as float pairs (the large
-        // parts cancel; K itself is of the order of the frame's spread)
-        float K = 0.0f;
-        if (scale != 0.0f) {
-            const float2 c = sm.cring[t % kRing];
-            float e1, e2;
-            const float s1 = two_sum(c.x, nz_hi, e1);
-            const float s2 = two_sum(s1, dn_hi, e2);
-            K = s2 + (e2 + (e1 + (c.y + nz_lo + dn_lo)));
-        }
-        tm = -INFINITY;
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const int s = tid + k * nt;
             if (s < S) {
-                const float as = arow[s];
-                float v[RE], e[RE], lm = -INFINITY;
+                const XP as = ld_xp(arow + s);
+                const float gm = as.m * izm;
+                const int ge = as.e - zx.e;
+                // beta_t(s) = sum over the outgoing list, in order, of
+                // exp(weight) x exp(lp[t, label]) x beta_{t+1}(to); each
+                // term times alpha_t(s) / Z is the edge's occupancy
+                XSum acc;
 #pragma unroll
                 for (int j = 0; j < RE; ++j) {
-                    v[j] = j < er.n[k] ? er.w[k][j] + word_to_float<DT>(lw[er.slot[k][j]], er.par[k][j] ^ flip) +
-                                             bep[er.peer[k][j]] - sh
-                                       : -INFINITY;
-                    lm = fmaxf(lm, v[j]);
-                }
-                float ls = 0.0f;
-#pragma unroll
-                for (int j = 0; j < RE; ++j) {
-                    e[j] = lm > -INFINITY ? expf(v[j] - lm) : 0.0f;
-                    ls += e[j];
-                }
-                if (scale != 0.0f) {
-                    // occupancy exp(as + v + K) = exp(v - max) * exp(as + max + K)
-                    const float g = lm > -INFINITY ? expf(as + lm + K) : 0.0f;
-#pragma unroll
-                    for (int j = 0; j < RE; ++j) {
-                        if (j < er.n[k]) {
-                            const float o = e[j] * g;
-                            occ[er.id[k][j]] = o > 0.0f ? o : 0.0f;
-                        }
+                    if (j < er.n[k]) {
+                        const XP x = xp_mul3(er.w[k][j], ld_xp(lx + er.slot[k][j]), ld_xp(bep + er.peer[k][j]));
+                        acc.add(x);
+                        occ[er.id[k][j]] = x.m * gm * pow2_any(x.e + ge);
                     }
                 }
-                // the rest of the list, in order
                 for (int kk = er.k0[k]; kk < er.k1[k]; ++kk) {
                     const int4 r = rout[kk];
-                    const float lv = word_to_float<DT>(lw[r.y], ((base_half ^ sm.labs[r.y]) & 1) ^ flip);
-                    const float vv = __int_as_float(r.z) + lv + bep[r.x] - sh;
-                    lse_push(lm, ls, vv);
-                    if (scale != 0.0f) {
-                        const float o = vv > -INFINITY ? expf(as + vv + K) : 0.0f;
-                        occ[r.w] = o > 0.0f ? o : 0.0f;
-                    }
+                    const XP x = xp_mul3(xp_exp(__int_as_float(r.z)), ld_xp(lx + r.y), ld_xp(bep + r.x));
+                    acc.add(x);
+                    occ[r.w] = x.m * gm * pow2_any(x.e + ge);
                 }
-                const float nv = lse_value(lm, ls);
-                beq[s] = nv;
-                tm = fmaxf(tm, nv);
+                st_xp(beq + s, xp_norm(acc.S, acc.E));
             }
         }
-        cp_async_wait<kRing - 2>();
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-        if ((tid & 31) == 0) wmax[p ^ 1][tid >> 5] = tm;
+        cp_async_wait<RING - 2>();
+        if (t > 0)
+            convert_row<DT>(sm.lpx + ((t - 1) & 1) * cap, sm.ring + ((t - 1) % RING) * cap, sm.labs, nlab,
+                            row_flip(start + t - 1, D), base_half);
         __syncthreads();
         // the row's class sums (class, -scale * occupancy), each label's edges
         // in list order; the dense rows are written afterwards by the all-SM
         // gradient stream
         const int64_t row = start + t;
-        const int n = scale != 0.0f ? nlab : 0;
+        const int n = nlab;
         // a label's occupancies are the contiguous range [laboff[i],
         // laboff[i + 1]) in edge order.  Short lists: a thread each, in order
         for (int i = tid; i < n; i += nt) {
@@ -881,6 +845,28 @@ namespace {
 
 bool fsa_valid_dtype(int d) { return d == CTC_PACKED_F32 || d == CTC_PACKED_BF16 || d == CTC_PACKED_F16; }
 
+// Threads of a recursion CTA: a thread per state of the largest sequence, in
+// whole warps, between 64 and 512 (at most 8 states a thread).
+int recursion_threads(int max_states) {
+    int nt = (max_states + 31) / 32 * 32;
+    if (nt < 64) nt = 64;
+    if (nt > kFsaMaxThreads) nt = kFsaMaxThreads;
+    return nt;
+}
+
+// Ring depth of the recursions for sequences of up to max_states states.
+int ring_for(int max_states) {
+    const int nt = recursion_threads(max_states);
+    return fsa_ring((max_states + nt - 1) / nt);
+}
+
+// The backward's per-frame buffers (the larger plan) within a CTA's shared
+// memory: max_states and max_labels bound them together.
+bool fsa_plan_fits(int max_states, int max_labels, int D) {
+    const int cap = max_labels < D ? max_labels : D;
+    return fsa_smem_plan(true, 0, max_states, cap, ring_for(max_states), nullptr, nullptr) <= (size_t)kFsaSmemLimit;
+}
+
 ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_total, int32_t D, const int32_t* cu,
                                  const int32_t* lengths, int32_t B, const int32_t* so, const float* sw,
                                  const float* fw, int32_t S_total, const int32_t* eo, const int32_t* edges,
@@ -889,7 +875,8 @@ ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_tot
     if (!fsa_valid_dtype(dtype) || T_total < 0 || B < 0 || D < 1 || S_total < 0 || E_total < 0)
         return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (max_labels < 1) return CTC_PACKED_ERR_INVALID_ARGUMENT;
-    if (D > kFsaMaxD || T_total > INT32_MAX || max_states < 1 || max_states > kFsaMaxStates)
+    if (D > kFsaMaxD || T_total > INT32_MAX || max_states < 1 || max_states > kFsaMaxStates ||
+        !fsa_plan_fits(max_states, max_labels, D))
         return CTC_PACKED_ERR_UNSUPPORTED;
     if (cu == nullptr || so == nullptr || eo == nullptr) return CTC_PACKED_ERR_INVALID_ARGUMENT;
     if (B > 0 && (lengths == nullptr || sw == nullptr || fw == nullptr)) return CTC_PACKED_ERR_INVALID_ARGUMENT;
@@ -913,22 +900,14 @@ cudaError_t launch_fsa(K kernel, unsigned grid, int threads, size_t smem, cudaSt
     return cudaGetLastError();
 }
 
-// Threads of a recursion CTA: a thread per state of the largest sequence, in
-// whole warps, between 64 and 512 (at most 8 states a thread).
-int recursion_threads(int max_states) {
-    int nt = (max_states + 31) / 32 * 32;
-    if (nt < 64) nt = 64;
-    if (nt > kFsaMaxThreads) nt = kFsaMaxThreads;
-    return nt;
-}
-
 // Edges of one sequence a recursion CTA keeps in shared memory (16 bytes an
-// edge forward; 24 backward: the record and two occupancies): four times the batch's mean per sequence (at least 1024), at
-// most what the budget leaves after the per-frame buffers and at most the
-// batch's edges, so that CTAs of ordinary sequences share an SM.  A sequence
-// with more edges reads its lists from the workspace.
+// edge forward; 24 backward: the record and two occupancies): four times the
+// batch's mean per sequence (at least 1024), at most what the budget leaves
+// after the per-frame buffers and at most the batch's edges, so that CTAs of
+// ordinary sequences share an SM.  A sequence with more edges reads its lists
+// from the workspace.
 int smem_edges(bool backward, int B, int E_total, int max_states, int cap) {
-    const size_t fixed = fsa_smem_plan(backward, 0, max_states, cap, nullptr, nullptr);
+    const size_t fixed = fsa_smem_plan(backward, 0, max_states, cap, ring_for(max_states), nullptr, nullptr);
     const size_t per = backward ? 24 : 16;
     if (fixed + 64 >= (size_t)kFsaSmemBudget) return 0;
     size_t e = ((size_t)kFsaSmemBudget - fixed - 64) / per;
@@ -991,7 +970,7 @@ extern "C" {
 size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t num_states, int32_t num_edges,
                                      int32_t max_states, int32_t max_labels, int32_t D) {
     if (T_total < 0 || B < 0 || num_states < 0 || num_edges < 0 || max_states < 1 || max_states > kFsaMaxStates ||
-        T_total > INT32_MAX || max_labels < 1 || D < 1 || D > kFsaMaxD)
+        T_total > INT32_MAX || max_labels < 1 || D < 1 || D > kFsaMaxD || !fsa_plan_fits(max_states, max_labels, D))
         return 0;
     return fsa_layout(T_total, B, num_states, num_edges, max_states, max_labels, D).total;
 }
@@ -1024,7 +1003,7 @@ ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype
     // 2. per sequence: the forward recursion
     const int nt = recursion_threads(max_states);
     a.ecap_smem = smem_edges(false, B, num_edges, max_states, a.L.cap);
-    const size_t smem = fsa_smem_plan(false, a.ecap_smem, max_states, a.L.cap, nullptr, nullptr);
+    const size_t smem = fsa_smem_plan(false, a.ecap_smem, max_states, a.L.cap, ring_for(max_states), nullptr, nullptr);
     const cudaError_t e = dtype == CTC_PACKED_F32    ? launch_recursion<0, false>(max_states, B, nt, smem, stream, a)
                           : dtype == CTC_PACKED_BF16 ? launch_recursion<1, false>(max_states, B, nt, smem, stream, a)
                                                      : launch_recursion<2, false>(max_states, B, nt, smem, stream, a);
@@ -1065,7 +1044,8 @@ ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtyp
     if (B > 0) {
         const int nt = recursion_threads(max_states);
         a.ecap_smem = smem_edges(true, B, num_edges, max_states, a.L.cap);
-        const size_t smem = fsa_smem_plan(true, a.ecap_smem, max_states, a.L.cap, nullptr, nullptr);
+        const size_t smem =
+            fsa_smem_plan(true, a.ecap_smem, max_states, a.L.cap, ring_for(max_states), nullptr, nullptr);
         const cudaError_t e =
             dtype == CTC_PACKED_F32    ? launch_recursion<0, true>(max_states, B, nt, smem, stream, a)
             : dtype == CTC_PACKED_BF16 ? launch_recursion<1, true>(max_states, B, nt, smem, stream, a)

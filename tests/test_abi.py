@@ -190,8 +190,14 @@ def test_fsa_workspace_size():
     assert f(100, 4, 20, -1, 10, 5, 10) == 0
     assert f(100, 4, 20, 60, 10, 5, 16385) == 0
     n = f(1000, 4, 200, 600, 50, 20, 30)
-    # alpha rows (4 B x states) and class sums (8 B x min(labels, D)) per frame, and per edge two
-    # 16-byte list records and two occupancies at least
-    assert n >= 1000 * 50 * 4 + 1000 * 20 * 8 + 1000 * 8 + 600 * (32 + 8)
+    # alpha rows (8 B x states, extended range) and class sums (8 B x min(labels, D)) per frame, and
+    # per edge two 16-byte list records and two occupancies at least
+    assert n >= 1000 * 50 * 8 + 1000 * 20 * 8 + 1000 * 8 + 600 * (32 + 8)
+    # a recursion's per-frame buffers must fit a CTA's shared memory: about 52 bytes a state and
+    # 44 a label up to 2048 states (36 and 36 above)
+    assert f(1000, 4, 200, 600, 2048, 2000, 16384) > 0
+    assert f(1000, 4, 200, 600, 2048, 3000, 16384) == 0
+    assert f(1000, 4, 200, 600, 4096, 1000, 16384) > 0
+    assert f(1000, 4, 200, 600, 4096, 3000, 16384) == 0
     assert f(1000, 4, 200, 600, 50, 200, 30) < f(1000, 4, 200, 600, 50, 200, 300)  # class sums capped at D
     assert f(1000, 4, 200, 600, 50, 20, 30) < f(1000, 4, 200, 6000, 50, 20, 30)  # edge lists grow with edges

@@ -219,3 +219,22 @@ def test_sequence_beyond_the_shared_memory_lists(cuda_device):
     ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
     assert_loss_close(loss, ref_loss)
     assert_grad_close(grad, ref_grad, torch.float32)
+
+
+@pytest.mark.parametrize("L", [300, 700, 1250])
+def test_many_states_a_thread(cuda_device, L):
+    # CTC lattices of 2L + 2 states (the entry state included): 602 (two
+    # states a thread), 1402 (four) and 2502 (eight, with the two-frame ring
+    # of label words and alpha rows)
+    batch = workloads.make_batch([L + 150, 90], [L, 30], 41, seed=29 + L, repeat_prob=0.1, redraw_infeasible=True,
+                                 reduction="none")
+    offs = np.concatenate([[0], np.cumsum(batch.target_lengths.numpy())])
+    tg = batch.targets.numpy()
+    fsa = workloads.pack_fsas([workloads.ctc_lattice_fsa(tg[offs[b]:offs[b + 1]], batch.blank)
+                               for b in range(batch.B)])
+    assert _max_states(fsa) == 2 * L + 2
+    loss, grad, status, g = _run(batch.log_probs, batch.cu_seqlens, batch.lengths, fsa, _max_states(fsa))
+    assert status == 0
+    ref_loss, ref_grad = _oracle(batch.log_probs, batch.cu_seqlens, batch.lengths, fsa, g)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, torch.float32)
