@@ -6,10 +6,11 @@ path), seeded random FSAs with weights, several start and final states and
 loops, in the three dtypes; a sequence without a path (with and without
 zero_infinity), frameless sequences and gap rows; a large vocabulary; and
 out-of-range FSA data (and more distinct labels than max_labels), which must
-set the status word and a NaN loss; and bitwise reproducibility.  The
-recursions run in float32 log space: losses within 1e-4 relative, float32
-gradients within 2e-5 (on these lengths), half types within one unit in the
-last place plus 1e-3.
+set the status word and a NaN loss; bitwise reproducibility; and lattices
+of 602 to 2502 states (two to eight states a thread).  The recursions carry
+float32 mantissas with integer exponents: losses within 1e-4 relative,
+float32 gradients within 2e-5 (on these lengths), half types within one
+unit in the last place plus 1e-3.
 """
 
 import numpy as np
