@@ -188,60 +188,71 @@ __device__ __forceinline__ X64 x_from_log(double x) {
     return x_norm(exp(r), (long long)k);
 }
 
-// Exact conversions by the numbers' bits, on the integer pipe (this part's
-// float64 pipe is narrow, and its conversions would use it):
-// a float64 in (2^-126, 2^127) to the float32 with its leading 24 bits
-// (truncated; smaller magnitudes give 0) ...
+// A float64 in (2^-126, 2^127) to the float32 with its leading 24 bits
+// (truncated; smaller magnitudes give 0), by the numbers' bits on the integer
+// pipe (this part's float64 pipe is narrow, and its conversions would use it).
 __device__ __forceinline__ float f64_to_f32_bits(double x) {
     const unsigned long long u = (unsigned long long)__double_as_longlong(x);
     const int e = (int)((u >> 52) & 0x7ff) - 896;  // float32 exponent field
     if (e <= 0) return 0.0f;
     return __uint_as_float((unsigned)(u >> 32 & 0x80000000ull) | ((unsigned)e << 23) | (unsigned)(u >> 29 & 0x7fffff));
 }
-// ... a non-negative normal float32 (or 0) to float64, exactly ...
-__device__ __forceinline__ double f32_to_f64_bits(float f) {
-    const unsigned b = __float_as_uint(f);
-    if ((b & 0x7fffffffu) == 0) return 0.0;
-    return __longlong_as_double((long long)((unsigned long long)(b >> 31) << 63 |
-                                            (unsigned long long)((b >> 23 & 0xff) + 896) << 52 |
-                                            (unsigned long long)(b & 0x7fffff) << 29));
-}
-// ... and an int of magnitude below 2^30 to float64, exactly.
-__device__ __forceinline__ double int_to_f64_bits(int n) {
-    if (n == 0) return 0.0;
-    const unsigned a = (unsigned)(n < 0 ? -n : n);
-    const int lz = __clz(a);
-    // the bits below the leading one, moved to the top of the 52-bit field
-    const unsigned long long frac = ((unsigned long long)a << (lz + 21)) & 0xfffffffffffffull;
-    return __longlong_as_double((long long)((unsigned long long)(n < 0) << 63 |
-                                            (unsigned long long)(1023 + 31 - lz) << 52 | frac));
-}
+
+// ln 2 / 64 in units of 2^-53: kLn2o64Hi + kLn2o64Lo / 2^11 (within 2^-12
+// of a unit).
+constexpr long long kLn2o64Hi = 97551793252583ll;
+constexpr long long kLn2o64Lo = 1511;
 
 // exp(x) by Tang's table-driven method (P. T. P. Tang, "Table-driven
 // implementation of the exponential function in IEEE floating-point
 // arithmetic", ACM TOMS 15(2), 1989), shaped for a part with a narrow float64
-// pipe: three float64 operations an element.  x = (64 k + j) ln2/64 + r,
-// with n = 64 k + j = round(x * 64/ln2) taken in float32: a rounding off by
-// one only leaves |r| < ln2/64.  Then r is formed in float64 by one fused
-// multiply-add, and exp(r) = 1 + r + q with q = r^2/2 + r^3/6 + r^4/24 in
-// float32: |q| < 6e-5, so float32 rounds it to within 4e-12, and the dropped
-// r^5/120 is below 1.3e-12.  Finally exp(x) = 2^k * T[j] * (1 + r + q), with
-// T[j] = 2^(j/64) from a table the caller fills (shared memory), and 2^k
-// added to the exponent field.  A table c * 2^(j/64) gives c * exp(x) (the
-// caller keeps c * exp(x) a normal number).  The relative error is below
-// about 1e-11; the gradient it feeds is held to 1e-10.  |x| >= 512, NaN and
-// infinities take the library exp, times T[0] (the test is on the exponent
-// field).
+// pipe: one float64 operation an element, the reduction on the integer pipe.
+// x = (64 k + j) ln2/64 + r, with n = 64 k + j = round(x * 64/ln2) taken in
+// float32: a rounding off by one only leaves |r| < ln2/64.  x and n ln2/64
+// are formed as 64-bit integers in units of 2^-53 (x's bits below 2^-53
+// drop out), so their difference R is r * 2^53 to within a unit.  Then
+// exp(r) = 1 + s, s = r + q, q = r^2/2 + r^3/6 + r^4/24 in float32 from R's
+// leading bits: |q| < 6e-5, so float32 rounds it to within 4e-12, and the
+// dropped r^5/120 is below 1.3e-12.  q joins R in the same units and the
+// sum (below 2^48 in magnitude) becomes a float64 by its bits.  Finally
+// exp(x) = 2^k * T[j] * (1 + s) = fma(T[j], s, T[j]), with T[j] = 2^(j/64)
+// from a table the caller fills (shared memory) and 2^k added to the
+// exponent field.  A table c * 2^(j/64) gives c * exp(x) (the caller keeps
+// c * exp(x) a normal number).  The relative error is below about 1e-11;
+// the gradient it feeds is held to 1e-10.  |x| >= 512, NaN and infinities
+// take the library exp, times T[0] (the test is on the exponent field).
 __device__ __forceinline__ double exp_table(double x, const double* T) {
     const unsigned long long u = (unsigned long long)__double_as_longlong(x);
-    if ((u >> 52 & 0x7ff) >= 1023 + 9) return T[0] * exp(x);  // T[0]: the table's own factor
+    const int ex = (int)(u >> 52 & 0x7ff);
+    if (ex >= 1023 + 9) return T[0] * exp(x);  // T[0]: the table's own factor
+    // x * 2^53: the significand (implicit bit included) moved by ex - 1022
+    // bits, at most 9 to the left (62 bits in all)
+    const long long sig = (long long)((u & 0xfffffffffffffull) | (1ull << 52));
+    const int sh = ex - 1022;
+    long long X = sh >= 0 ? sig << sh : (sh > -64 ? sig >> -sh : 0ll);
+    if (u >> 63) X = -X;
     const float xf = f64_to_f32_bits(x);
     const int n = __float2int_rn(xf * 92.332482616893656f);  // 64 / ln 2
-    const double r = fma(-int_to_f64_bits(n), 0.010830424696249145, x);  // ln 2 / 64 (exact in float64)
-    const float rf = f64_to_f32_bits(r);
+    const long long R = X - ((long long)n * kLn2o64Hi + (((long long)n * kLn2o64Lo + 1024) >> 11));
+    // r in float32 from R's bits down to 2^-37 (|R| < 2^47: 31 bits)
+    const float rf = (float)(int)(R >> 16) * 0x1p-37f;
     const float q = rf * rf * fmaf(rf, fmaf(rf, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f);  // >= 0
+    // q = m 2^(E - 150) in units of 2^-53: m shifted by E - 97 (E <= 113)
+    const unsigned qb = __float_as_uint(q);
+    const int qe = (int)(qb >> 23) - 97;
+    const long long qm = (long long)((qb & 0x7fffffu) | 0x800000u);
+    const long long Q = qb == 0 ? 0ll : (qe >= 0 ? qm << qe : (qe > -32 ? qm >> -qe : 0ll));
+    const long long S = R + Q;
+    // s = S * 2^-53 as a float64 by its bits (at most 48 significant bits: exact)
+    double s = 0.0;
+    if (S != 0) {
+        const unsigned long long A = (unsigned long long)(S < 0 ? -S : S);
+        const int lz = __clzll((long long)A);
+        s = __longlong_as_double((long long)((unsigned long long)(S < 0) << 63 |
+                                             (unsigned long long)(1023 - 53 + 63 - lz) << 52 | ((A << lz) << 1) >> 12));
+    }
     const double t = T[n & 63];
-    const double y = fma(t, r + f32_to_f64_bits(q), t);  // in [1, 2.05): a normal number
+    const double y = fma(t, s, t);  // in [0.98, 2.03) times the table's factor
     return __longlong_as_double(__double_as_longlong(y) + ((long long)(n >> 6) << 52));
 }
 
@@ -778,6 +789,27 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
     }
 }
 
+// scale * exp(x[c] - sh) for the lane's elements c of a row: with FOLDED the
+// table T already holds scale * 2^(j/64); without SHIFT the row is not
+// shifted.
+template <bool SHIFT, bool FOLDED>
+__device__ __forceinline__ void dense_row(double* g, const double* x, int D, int lane, double sh, double scale,
+                                          const double* T) {
+    auto f = [&](double v) {
+        if (SHIFT) v -= sh;
+        return FOLDED ? exp_table(v, T) : scale * exp_table(v, T);
+    };
+    int c = lane;
+    for (; c + 96 < D; c += 128) {
+        const double x0 = __ldg(x + c), x1 = __ldg(x + c + 32), x2 = __ldg(x + c + 64), x3 = __ldg(x + c + 96);
+        g[c] = f(x0);
+        g[c + 32] = f(x1);
+        g[c + 64] = f(x2);
+        g[c + 96] = f(x3);
+    }
+    for (; c < D; c += 32) g[c] = f(__ldg(x + c));
+}
+
 // The dense gradient: one warp per row.  A row outside every utterance's
 // frames (or of a malformed utterance, or after a loss-only forward) is 0.
 __global__ void __launch_bounds__(kRowWarps * 32) f64_grad_kernel(F64Args a) {
@@ -826,15 +858,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_grad_kernel(F64Args a) {
         sexp[lane + 32] = scale * s_exp[lane + 32];
         __syncwarp();
         auto sexp_of = [&](double v) { return folded ? exp_table(v, sexp) : scale * exp_table(v, s_exp); };
-        int c = lane;
-        for (; c + 96 < D; c += 128) {
-            const double x0 = __ldg(x + c), x1 = __ldg(x + c + 32), x2 = __ldg(x + c + 64), x3 = __ldg(x + c + 96);
-            g[c] = sexp_of(x0 - sh);
-            g[c + 32] = sexp_of(x1 - sh);
-            g[c + 64] = sexp_of(x2 - sh);
-            g[c + 96] = sexp_of(x3 - sh);
-        }
-        for (; c < D; c += 32) g[c] = sexp_of(__ldg(x + c) - sh);
+        // the dense pass, its row-uniform choices taken once: log
+        // probabilities need no shift (a float64 subtraction an element)
+        if (logits)
+            folded ? dense_row<true, true>(g, x, D, lane, sh, scale, sexp) : dense_row<true, false>(g, x, D, lane, sh, scale, s_exp);
+        else
+            folded ? dense_row<false, true>(g, x, D, lane, sh, scale, sexp) : dense_row<false, false>(g, x, D, lane, sh, scale, s_exp);
         if (scale != 0.0) {
             __syncwarp();  // the dense stores land before the class sums rewrite their elements
             const double* er = ent + row * a.L.ecap;
