@@ -53,6 +53,12 @@ namespace {
 constexpr int kZeroE = -(1 << 30);  // exponent of zero; values below 2^kZeroE flush to zero
 constexpr int kRowWarps = 8;        // warps (rows) per CTA of the row kernels
 constexpr int kMaxChainThreads = 1024;
+// Frames of a recursion's per-state loads in flight through shared memory
+// (the next frames' emissions; backward also the stored alpha rows), RING - 1
+// ahead of the frame computed: 4 up to 1024 states a CTA (both kernels) and
+// up to 2048 (forward); larger CTAs load one frame ahead into registers
+// (their rings would not fit).
+__host__ __device__ constexpr int f64_ring(bool backward, int per) { return per == 1 || (!backward && per == 2) ? 4 : 0; }
 
 // Extended-range value m * 2^e, m in [1, 2), or zero (m = 0, e = kZeroE);
 // NaN and infinity are carried in m.
@@ -266,6 +272,17 @@ __device__ __forceinline__ X64 ld_em(const EmX* p) {
     return X64{v.x, (int)__double_as_longlong(v.y)};
 }
 
+// 4-, 8- and 16-byte async copies global -> shared.
+__device__ __forceinline__ void cp_async_n4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_n8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_n16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 // ------------------------------------------------------------ helpers
 
 __device__ __forceinline__ int f64_utterance_of_row(const int32_t* cu, int B, int64_t row) {
@@ -466,6 +483,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_emit_kernel(F64Args a) {
 // frame.
 template <int PER>
 __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args a) {
+    constexpr int RING = f64_ring(false, PER);
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_bad;
     const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
@@ -477,6 +495,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
     const int cap = PER * nt;
     double* const mbuf = reinterpret_cast<double*>(smem);         // two buffers of cap mantissas
     int* const ebuf = reinterpret_cast<int*>(mbuf + 2 * cap);      // two buffers of cap exponents
+    EmX* const ring = reinterpret_cast<EmX*>(ebuf + 2 * cap);      // RING frames of the states' emissions
     if (tid == 0) s_bad = 0;
     __syncthreads();
     const int32_t* tg = a.targets + u.toff;
@@ -526,17 +545,41 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
                 ae[s] = v.e;
             }
         }
-        nx[k] = (s < S && T > 1) ? ld_em(em + Ep + ent[k]) : x_zero();
+        if (RING == 0) nx[k] = (s < S && T > 1) ? ld_em(em + Ep + ent[k]) : x_zero();
     }
+    // the states' emissions of frame f into ring slot f % RING (each thread
+    // copies and later reads its own states' entries)
+    auto issue = [&](int f) {
+        if (f < T) {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                if (s < S) cp_async_n16(ring + (f % (RING > 0 ? RING : 1)) * cap + s, em + (size_t)f * Ep + ent[k]);
+            }
+        }
+        cp_async_commit();
+    };
+    if (RING > 0)
+        for (int f = 1; f < RING; ++f) issue(f);
     __syncthreads();
     int p = 0;
     for (int t = 1; t < T; ++t) {
         X64 e_t[PER];
+        if constexpr (RING > 0) {
+            issue(t + RING - 1);
+            cp_async_wait<RING - 1>();  // frame t's entries have landed
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            e_t[k] = nx[k];
-            const int s = tid + k * nt;
-            if (s < S && t + 1 < T) nx[k] = ld_em(em + (size_t)(t + 1) * Ep + ent[k]);
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                e_t[k] = s < S ? ld_em(ring + (t % RING) * cap + s) : x_zero();
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                e_t[k] = nx[k];
+                const int s = tid + k * nt;
+                if (s < S && t + 1 < T) nx[k] = ld_em(em + (size_t)(t + 1) * Ep + ent[k]);
+            }
         }
         const double* mp = mbuf + p * cap;
         const int* ep = ebuf + p * cap;
@@ -561,6 +604,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
         __syncthreads();
         p ^= 1;
     }
+    if (RING > 0) cp_async_wait<0>();
     if (tid == 0) {
         const double* mp = mbuf + p * cap;
         const int* ep = ebuf + p * cap;
@@ -624,6 +668,8 @@ __global__ void __launch_bounds__(256) f64_reduce_kernel(F64Args a) {
 // frame are read between B and the next A.
 template <int PER>
 __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a) {
+    constexpr int RING = f64_ring(true, PER);
+    constexpr int RS = RING > 0 ? RING : 1;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ double s_wsum[kMaxChainThreads / 32];
     __shared__ int s_warp[32];
@@ -638,7 +684,12 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
     if (scale == 0.0) return;  // the row stream writes zeros without class sums
     const int U = u.U, S = 2 * U + 1, T = u.T, Ep = a.L.Ep, Sp = a.L.Sp;
     const int cap = PER * nt;
-    double* gm = reinterpret_cast<double*>(smem);             // g, mantissas
+    // RING frames of the states' emissions and stored alpha rows, then the
+    // per-frame buffers
+    EmX* const rx = reinterpret_cast<EmX*>(smem);
+    double* const rm = reinterpret_cast<double*>(rx + RING * cap);
+    int* const re = reinterpret_cast<int*>(rm + RING * cap);
+    double* gm = reinterpret_cast<double*>(re + RING * cap);  // g, mantissas
     double* gam = gm + cap;                                   // label-state posteriors, U entries
     int* ge = reinterpret_cast<int*>(gam + (U > 0 ? U : 1));  // g, exponents
     int* lab = ge + cap;                                      // the target
@@ -707,25 +758,58 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
         eidx[k] = (s & 1) ? (s >> 1) : U;
         skip2[k] = (s & 1) && s + 2 < S && lab[(s + 2) >> 1] != lab[s >> 1];
     }
-    X64 al[PER], et[PER];
+    // frame f's emissions and stored alpha values of the thread's states
+    // into ring slot f % RING (each thread copies and later reads its own)
+    auto issue = [&](int f) {
+        if (f >= 0) {
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-        const int s = tid + k * nt;
-        al[k] = s < S ? X64{am[(size_t)(T - 1) * Sp + s], ae[(size_t)(T - 1) * Sp + s]} : x_zero();
-        et[k] = s < S ? ld_em(em + (size_t)(T - 1) * Ep + eidx[k]) : x_zero();
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                if (s < S) {
+                    const int q = (f % RS) * cap + s;
+                    cp_async_n16(rx + q, em + (size_t)f * Ep + eidx[k]);
+                    cp_async_n8(rm + q, am + (size_t)f * Sp + s);
+                    cp_async_n4(re + q, ae + (size_t)f * Sp + s);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    X64 al[PER], et[PER];
+    if constexpr (RING > 0) {
+        for (int j = 0; j < RING - 1; ++j) issue(T - 1 - j);
+    } else {
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            al[k] = s < S ? X64{am[(size_t)(T - 1) * Sp + s], ae[(size_t)(T - 1) * Sp + s]} : x_zero();
+            et[k] = s < S ? ld_em(em + (size_t)(T - 1) * Ep + eidx[k]) : x_zero();
+        }
     }
     for (int t = T - 1; t >= 0; --t) {
         X64 gn[PER];
         double gamma[PER];
         X64 al_n[PER], et_n[PER];
+        if constexpr (RING > 0) {
+            issue(t - (RING - 1));
+            cp_async_wait<RING - 1>();  // frame t's values have landed
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int s = tid + k * nt;
-            al_n[k] = x_zero();
-            et_n[k] = x_zero();
-            if (s < S && t > 0) {
-                al_n[k] = X64{am[(size_t)(t - 1) * Sp + s], ae[(size_t)(t - 1) * Sp + s]};
-                et_n[k] = ld_em(em + (size_t)(t - 1) * Ep + eidx[k]);
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                const int q = (t % RS) * cap + s;
+                al[k] = s < S ? X64{rm[q], re[q]} : x_zero();
+                et[k] = s < S ? ld_em(rx + q) : x_zero();
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                al_n[k] = x_zero();
+                et_n[k] = x_zero();
+                if (s < S && t > 0) {
+                    al_n[k] = X64{am[(size_t)(t - 1) * Sp + s], ae[(size_t)(t - 1) * Sp + s]};
+                    et_n[k] = ld_em(em + (size_t)(t - 1) * Ep + eidx[k]);
+                }
             }
         }
 #pragma unroll
@@ -766,8 +850,10 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                     bpart += gamma[k];
                 }
             }
-            al[k] = al_n[k];
-            et[k] = et_n[k];
+            if (RING == 0) {
+                al[k] = al_n[k];
+                et[k] = et_n[k];
+            }
         }
         bpart = warp_sum(bpart);
         if (lane == 0) s_wsum[warp] = bpart;
@@ -787,6 +873,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
             er[ncls - 1] = -scale * P;
         }
     }
+    if (RING > 0) cp_async_wait<0>();
 }
 
 // scale * exp(x[c] - sh) for the lane's elements c of a row: with FOLDED the
@@ -998,7 +1085,8 @@ ctc_packed_status ctc_packed_forward_f64(const double* log_probs, int64_t T_tota
     if (B > 0) {
         int per = 1, nt = 32;
         chain_shape(max_target_len, per, nt);
-        const size_t smem = 2 * (size_t)per * nt * (sizeof(double) + sizeof(int));
+        const size_t cap = (size_t)per * nt;
+        const size_t smem = 2 * cap * (sizeof(double) + sizeof(int)) + (size_t)f64_ring(false, per) * cap * sizeof(EmX);
         cudaError_t e;
         switch (per) {
             case 1: e = launch_chain_kernel(f64_alpha_kernel<1>, (unsigned)B, nt, smem, stream, a); break;
@@ -1041,8 +1129,9 @@ ctc_packed_status ctc_packed_backward_f64(const double* log_probs, int64_t T_tot
         int per = 1, nt = 32;
         chain_shape(max_target_len, per, nt);
         const int U = max_target_len > 0 ? max_target_len : 1;
-        const size_t smem = (size_t)per * nt * (sizeof(double) + sizeof(int)) + sizeof(double) * (size_t)U +
-                            3 * sizeof(int) * (size_t)U;
+        const size_t cap = (size_t)per * nt;
+        const size_t smem = (size_t)f64_ring(true, per) * cap * (sizeof(EmX) + sizeof(double) + sizeof(int)) +
+                            cap * (sizeof(double) + sizeof(int)) + sizeof(double) * (size_t)U + 3 * sizeof(int) * (size_t)U;
         cudaError_t e;
         switch (per) {
             case 1: e = launch_chain_kernel(f64_beta_kernel<1>, (unsigned)B, nt, smem, stream, a); break;
