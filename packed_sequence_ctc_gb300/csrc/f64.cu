@@ -59,6 +59,8 @@ constexpr int kMaxChainThreads = 1024;
 // up to 2048 (forward); larger CTAs load one frame ahead into registers
 // (their rings would not fit).
 __host__ __device__ constexpr int f64_ring(bool backward, int per) { return per == 1 || (!backward && per == 2) ? 4 : 0; }
+// The beta kernel double-buffers its per-frame values up to 4 states a thread.
+__host__ __device__ constexpr bool f64_beta_double_buffered(int per) { return per <= 4; }
 
 // Extended-range value m * 2^e, m in [1, 2), or zero (m = 0, e = kZeroE);
 // NaN and infinity are carried in m.
@@ -670,6 +672,10 @@ template <int PER>
 __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a) {
     constexpr int RING = f64_ring(true, PER);
     constexpr int RS = RING > 0 ? RING : 1;
+    // DB: g and the posteriors double buffered, one barrier a frame (up to
+    // 4096 states a CTA); otherwise one buffer and two barriers
+    constexpr bool DB = f64_beta_double_buffered(PER);
+    constexpr int NB = DB ? 2 : 1;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ double s_wsum[kMaxChainThreads / 32];
     __shared__ int s_warp[32];
@@ -689,10 +695,12 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
     EmX* const rx = reinterpret_cast<EmX*>(smem);
     double* const rm = reinterpret_cast<double*>(rx + RING * cap);
     int* const re = reinterpret_cast<int*>(rm + RING * cap);
-    double* gm = reinterpret_cast<double*>(re + RING * cap);  // g, mantissas
-    double* gam = gm + cap;                                   // label-state posteriors, U entries
-    int* ge = reinterpret_cast<int*>(gam + (U > 0 ? U : 1));  // g, exponents
-    int* lab = ge + cap;                                      // the target
+    const int Uu = U > 0 ? U : 1;
+    double* gm = reinterpret_cast<double*>(re + RING * cap);  // g, mantissas (NB buffers of cap)
+    double* gam = gm + NB * cap;                              // label-state posteriors (NB of Uu)
+    double* gb = gam + NB * Uu;                               // blank-state posteriors (two of U + 1, DB)
+    int* ge = reinterpret_cast<int*>(gb + (DB ? 2 * (U + 1) : 0));  // g, exponents (NB of cap)
+    int* lab = ge + NB * cap;                                 // the target
     int* nxt = lab + U;                                       // next position of the same class, -1: none
     int* rnk = nxt + U;                                       // rank of a first occurrence, -1 otherwise
 
@@ -786,6 +794,31 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
             et[k] = s < S ? ld_em(em + (size_t)(T - 1) * Ep + eidx[k]) : x_zero();
         }
     }
+    // the class sums of frame tt from its label-state posteriors gamr and
+    // (DB) blank-state posteriors gbr: a first occurrence's thread sums its
+    // class's positions in target order; the last warp (the fewest states)
+    // sums the blank class, lane l taking blank states l, l + 32, ..., then a
+    // fixed shuffle tree, then the labels equal to the blank
+    auto class_sums = [&](int tt, const double* gamr, const double* gbr) {
+        double* er = ent + (size_t)tt * a.L.ecap;
+        for (int j = tid; j < U; j += nt) {
+            const int r = rnk[j];
+            if (r < 0) continue;
+            double P = gamr[j];
+            for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gamr[jj];
+            er[r] = -scale * P;
+        }
+        if (warp == nw - 1) {
+            double P = 0.0;
+            for (int i = lane; i <= U; i += 32) P += gbr[i];
+            P = warp_sum(P);
+            if (lane == 0) {
+                for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gamr[jj];
+                er[ncls - 1] = -scale * P;
+            }
+        }
+    };
+    int p = 0;  // DB: g and the posteriors of frame t + 1 are in buffer p
     for (int t = T - 1; t >= 0; --t) {
         X64 gn[PER];
         double gamma[PER];
@@ -812,6 +845,11 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                 }
             }
         }
+        const double* gmp = gm + (DB ? p * cap : 0);  // g of frame t + 1
+        const int* gep = ge + (DB ? p * cap : 0);
+        if constexpr (DB) {
+            if (t + 1 < T) class_sums(t + 1, gam + p * Uu, gb + p * (U + 1));
+        }
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const int s = tid + k * nt;
@@ -822,9 +860,9 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                 if (t == T - 1) {
                     be = s >= S - 2 ? X64{1.0, 0} : x_zero();
                 } else {
-                    const X64 v0{gm[s], ge[s]};
-                    const X64 v1 = s + 1 < S ? X64{gm[s + 1], ge[s + 1]} : x_zero();
-                    const X64 v2 = skip2[k] ? X64{gm[s + 2], ge[s + 2]} : x_zero();
+                    const X64 v0{gmp[s], gep[s]};
+                    const X64 v1 = s + 1 < S ? X64{gmp[s + 1], gep[s + 1]} : x_zero();
+                    const X64 v2 = skip2[k] ? X64{gmp[s + 2], gep[s + 2]} : x_zero();
                     be = x_add3(v0, v1, v2);
                 }
                 gn[k] = x_mul(be, et[k]);
@@ -836,42 +874,74 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                 gamma[k] = nan_utt ? qnan : g;
             }
         }
-        __syncthreads();  // A
-        double bpart = 0.0;
+        if constexpr (DB) {
+            // frame t's values into the other buffers; one barrier
+            double* gmq = gm + (p ^ 1) * cap;
+            int* geq = ge + (p ^ 1) * cap;
+            double* gamq = gam + (p ^ 1) * Uu;
+            double* gbq = gb + (p ^ 1) * (U + 1);
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int s = tid + k * nt;
-            if (s < S) {
-                gm[s] = gn[k].m;
-                ge[s] = gn[k].e;
-                if (s & 1) {
-                    gam[s >> 1] = gamma[k];
-                } else {
-                    bpart += gamma[k];
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                if (s < S) {
+                    gmq[s] = gn[k].m;
+                    geq[s] = gn[k].e;
+                    if (s & 1)
+                        gamq[s >> 1] = gamma[k];
+                    else
+                        gbq[s >> 1] = gamma[k];
                 }
             }
-            if (RING == 0) {
+            __syncthreads();
+            p ^= 1;
+        } else {
+            __syncthreads();  // A
+            double bpart = 0.0;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                if (s < S) {
+                    gm[s] = gn[k].m;
+                    ge[s] = gn[k].e;
+                    if (s & 1) {
+                        gam[s >> 1] = gamma[k];
+                    } else {
+                        bpart += gamma[k];
+                    }
+                }
+                if (RING == 0) {
+                    al[k] = al_n[k];
+                    et[k] = et_n[k];
+                }
+            }
+            bpart = warp_sum(bpart);
+            if (lane == 0) s_wsum[warp] = bpart;
+            __syncthreads();  // B
+            double* er = ent + (size_t)t * a.L.ecap;
+            for (int j = tid; j < U; j += nt) {
+                const int r = rnk[j];
+                if (r < 0) continue;
+                double P = gam[j];
+                for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gam[jj];
+                er[r] = -scale * P;
+            }
+            if (tid == 0) {
+                double P = 0.0;
+                for (int w = 0; w < nw; ++w) P += s_wsum[w];
+                for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gam[jj];
+                er[ncls - 1] = -scale * P;
+            }
+        }
+        if constexpr (DB && RING == 0) {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
                 al[k] = al_n[k];
                 et[k] = et_n[k];
             }
         }
-        bpart = warp_sum(bpart);
-        if (lane == 0) s_wsum[warp] = bpart;
-        __syncthreads();  // B
-        double* er = ent + (size_t)t * a.L.ecap;
-        for (int j = tid; j < U; j += nt) {
-            const int r = rnk[j];
-            if (r < 0) continue;
-            double P = gam[j];
-            for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gam[jj];
-            er[r] = -scale * P;
-        }
-        if (tid == 0) {
-            double P = 0.0;
-            for (int w = 0; w < nw; ++w) P += s_wsum[w];
-            for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gam[jj];
-            er[ncls - 1] = -scale * P;
-        }
+    }
+    if constexpr (DB) {
+        if (T > 0) class_sums(0, gam + p * Uu, gb + p * (U + 1));
     }
     if (RING > 0) cp_async_wait<0>();
 }
@@ -1130,8 +1200,10 @@ ctc_packed_status ctc_packed_backward_f64(const double* log_probs, int64_t T_tot
         chain_shape(max_target_len, per, nt);
         const int U = max_target_len > 0 ? max_target_len : 1;
         const size_t cap = (size_t)per * nt;
+        const size_t nb = f64_beta_double_buffered(per) ? 2 : 1;
         const size_t smem = (size_t)f64_ring(true, per) * cap * (sizeof(EmX) + sizeof(double) + sizeof(int)) +
-                            cap * (sizeof(double) + sizeof(int)) + sizeof(double) * (size_t)U + 3 * sizeof(int) * (size_t)U;
+                            nb * cap * (sizeof(double) + sizeof(int)) + nb * sizeof(double) * (size_t)U +
+                            (nb == 2 ? 2 * sizeof(double) * ((size_t)U + 1) : 0) + 3 * sizeof(int) * (size_t)U;
         cudaError_t e;
         switch (per) {
             case 1: e = launch_chain_kernel(f64_beta_kernel<1>, (unsigned)B, nt, smem, stream, a); break;
