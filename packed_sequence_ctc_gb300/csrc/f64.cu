@@ -196,16 +196,6 @@ __device__ __forceinline__ X64 x_from_log(double x) {
     return x_norm(exp(r), (long long)k);
 }
 
-// A float64 in (2^-126, 2^127) to the float32 with its leading 24 bits
-// (truncated; smaller magnitudes give 0), by the numbers' bits on the integer
-// pipe (this part's float64 pipe is narrow, and its conversions would use it).
-__device__ __forceinline__ float f64_to_f32_bits(double x) {
-    const unsigned long long u = (unsigned long long)__double_as_longlong(x);
-    const int e = (int)((u >> 52) & 0x7ff) - 896;  // float32 exponent field
-    if (e <= 0) return 0.0f;
-    return __uint_as_float((unsigned)(u >> 32 & 0x80000000ull) | ((unsigned)e << 23) | (unsigned)(u >> 29 & 0x7fffff));
-}
-
 // ln 2 / 64 in units of 2^-53: kLn2o64Hi + kLn2o64Lo / 2^11 (within 2^-12
 // of a unit).
 constexpr long long kLn2o64Hi = 97551793252583ll;
@@ -216,16 +206,18 @@ constexpr long long kLn2o64Lo = 1511;
 // arithmetic", ACM TOMS 15(2), 1989), shaped for a part with a narrow float64
 // pipe: one float64 operation an element, the reduction on the integer pipe.
 // x = (64 k + j) ln2/64 + r, with n = 64 k + j = round(x * 64/ln2) taken in
-// float32: a rounding off by one only leaves |r| < ln2/64.  x and n ln2/64
+// float32 from x's fixed-point form below: a rounding off by one only leaves
+// |r| < ln2/64.  x and n ln2/64
 // are formed as 64-bit integers in units of 2^-53 (x's bits below 2^-53
 // drop out), so their difference R is r * 2^53 to within a unit.  Then
 // exp(r) = 1 + s, s = r + q, q = r^2/2 + r^3/6 + r^4/24 in float32 from R's
 // leading bits: |q| < 6e-5, so float32 rounds it to within 4e-12, and the
-// dropped r^5/120 is below 1.3e-12.  q joins R in the same units and the
-// sum (below 2^48 in magnitude) becomes a float64 by its bits.  Finally
-// exp(x) = 2^k * T[j] * (1 + s) = fma(T[j], s, T[j]), with T[j] = 2^(j/64)
-// from a table the caller fills (shared memory) and 2^k added to the
-// exponent field.  A table c * 2^(j/64) gives c * exp(x) (the caller keeps
+// dropped r^5/120 is below 1.3e-12.  q joins R (rounded to 2^-40), and the
+// sum S, |S| < 2^47, is added to the bit pattern of 0.75, which in [0.5, 1)
+// moves by one per 2^-53: that is 0.75 + s exactly.  Finally exp(x) =
+// 2^k * T[j] * (1 + s) = fma(T[j], 0.75 + s, T[j] / 4), with T[j] =
+// 2^(j/64) from a table the caller fills (shared memory), the quarter and
+// 2^k taken on the exponent field.  A table c * 2^(j/64) gives c * exp(x) (the caller keeps
 // c * exp(x) a normal number).  The relative error is below about 1e-11;
 // the gradient it feeds is held to 1e-10.  |x| >= 512, NaN and infinities
 // take the library exp, times T[0] (the test is on the exponent field).
@@ -234,33 +226,27 @@ __device__ __forceinline__ double exp_table(double x, const double* T) {
     const int ex = (int)(u >> 52 & 0x7ff);
     if (ex >= 1023 + 9) return T[0] * exp(x);  // T[0]: the table's own factor
     // x * 2^53: the significand (implicit bit included) moved by ex - 1022
-    // bits, at most 9 to the left (62 bits in all)
-    const long long sig = (long long)((u & 0xfffffffffffffull) | (1ull << 52));
-    const int sh = ex - 1022;
-    long long X = sh >= 0 ? sig << sh : (sh > -64 ? sig >> -sh : 0ll);
+    // bits, at most 9 to the left (62 bits in all): moved 10 left, then
+    // 1032 - ex right
+    const unsigned long long sig = ((u & 0xfffffffffffffull) | (1ull << 52)) << 10;
+    long long X = (long long)(sig >> min(1032 - ex, 63));
     if (u >> 63) X = -X;
-    const float xf = f64_to_f32_bits(x);
-    const int n = __float2int_rn(xf * 92.332482616893656f);  // 64 / ln 2
+    // n from X's high word (|x| < 2^-21 gives 0, as it should)
+    const int n = __float2int_rn((float)(int)(X >> 32) * (92.332482616893656f * 0x1p-21f));  // 64 / ln 2
     const long long R = X - ((long long)n * kLn2o64Hi + (((long long)n * kLn2o64Lo + 1024) >> 11));
     // r in float32 from R's bits down to 2^-37 (|R| < 2^47: 31 bits)
     const float rf = (float)(int)(R >> 16) * 0x1p-37f;
     const float q = rf * rf * fmaf(rf, fmaf(rf, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f);  // >= 0
-    // q = m 2^(E - 150) in units of 2^-53: m shifted by E - 97 (E <= 113)
-    const unsigned qb = __float_as_uint(q);
-    const int qe = (int)(qb >> 23) - 97;
-    const long long qm = (long long)((qb & 0x7fffffu) | 0x800000u);
-    const long long Q = qb == 0 ? 0ll : (qe >= 0 ? qm << qe : (qe > -32 ? qm >> -qe : 0ll));
-    const long long S = R + Q;
-    // s = S * 2^-53 as a float64 by its bits (at most 48 significant bits: exact)
-    double s = 0.0;
-    if (S != 0) {
-        const unsigned long long A = (unsigned long long)(S < 0 ? -S : S);
-        const int lz = __clzll((long long)A);
-        s = __longlong_as_double((long long)((unsigned long long)(S < 0) << 63 |
-                                             (unsigned long long)(1023 - 53 + 63 - lz) << 52 | ((A << lz) << 1) >> 12));
-    }
+    // q in units of 2^-40 (below 2^27: one conversion), then 2^-53
+    const long long S = R + ((long long)__float2int_rn(q * 0x1p40f) << 13);
+    // 0.75 + s by its bits: in [0.5, 1) a float64's bit pattern moves by one
+    // per 2^-53, so adding S to 0.75's pattern is exact; then
+    // T[j] (1 + s) = fma(T[j], 0.75 + s, T[j] / 4), the quarter by the
+    // exponent field (exact)
+    const double s75 = __longlong_as_double(0x3FE8000000000000ll + S);
     const double t = T[n & 63];
-    const double y = fma(t, s, t);  // in [0.98, 2.03) times the table's factor
+    const double t4 = __longlong_as_double(__double_as_longlong(t) - (2ll << 52));
+    const double y = fma(t, s75, t4);  // in [0.98, 2.03) times the table's factor
     return __longlong_as_double(__double_as_longlong(y) + ((long long)(n >> 6) << 52));
 }
 
