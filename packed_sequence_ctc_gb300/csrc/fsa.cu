@@ -126,6 +126,10 @@ struct FsaArgs {
     void* grad;
     void* ws;
     int ecap_smem;  // a recursion CTA keeps a sequence's edge lists in shared memory up to this many edges
+    // a recursion CTA's threads: [0, nst) hold states; [lt0, lt0 + nlt) copy
+    // and convert the label values (its own warps after the state threads
+    // when they fit the CTA, else the state threads themselves)
+    int nst, lt0, nlt;
     FsaLayout L;
 };
 
@@ -499,10 +503,11 @@ struct EdgeRegs {
 // Forward records hold the weight in extended range, backward ones the log
 // weight and the occupancy's index.
 template <bool BACKWARD, int PER, int RE>
-__device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int* off, const int4* rec, int S) {
+__device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int* off, const int4* rec, int S,
+                                               int nst) {
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-        const int s = threadIdx.x + k * blockDim.x;
+        const int s = (int)threadIdx.x < nst ? (int)threadIdx.x + k * nst : S;  // label threads hold none
         int b0 = 0, b1 = 0;
         if (s < S) {
             b0 = off[s];
@@ -533,29 +538,71 @@ __device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int*
 // the buffer's own; `par` is the row-independent part (base ^ label).
 __device__ __forceinline__ int row_flip(int64_t row, int D) { return (int)(row & (int64_t)D) & 1; }
 
-// Starts the copies of the words holding labels labs[0 .. nlab) of row
-// `row` (thread i % nt copies label i).  Only the buffer's last row can hold
-// an element whose word would reach past the buffer.
+// A label thread's labels: li, li + nlt, ... of the sequence's nlab; the
+// first two are held in registers across the frames (each label's byte
+// offset in a row and the parity of its element's half in a 32-bit word),
+// the rest are read from shared memory each frame.
+template <int DT>
+struct LabelLane {
+    int li, nlt, nlab;
+    int n;               // labels held (0, 1 or 2)
+    uint32_t off[2];     // byte offset of label li + j * nlt in a row
+    int par[2];          // parity of its element's half (2-byte types)
+};
+template <int DT>
+__device__ __forceinline__ LabelLane<DT> label_lane(const int* labs, int nlab, int li, int nlt, int base_half) {
+    constexpr int E = DT == 0 ? 4 : 2;
+    LabelLane<DT> L;
+    L.li = li;
+    L.nlt = nlt;
+    L.nlab = nlab;
+    L.n = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = li + j * nlt;
+        const bool on = (unsigned)li < (unsigned)nlt && i < nlab;
+        const int c = on ? labs[i] : 0;
+        L.off[j] = (uint32_t)c * E;
+        L.par[j] = (base_half ^ c) & 1;
+        L.n += on ? 1 : 0;
+    }
+    return L;
+}
+
+// Starts the copies of the words holding the thread's labels of row `row`.
+// Only the buffer's last row can hold an element whose word would reach
+// past the buffer.
 template <int DT>
 __device__ __forceinline__ void issue_row(uint32_t* dst, const void* lp, int64_t row, int D, int64_t T_total,
-                                          const int* labs, int nlab, uintptr_t lp_end) {
+                                          const int* labs, uintptr_t lp_end, const LabelLane<DT>& L) {
     constexpr int E = DT == 0 ? 4 : 2;
+    if (L.n == 0) return;
     if (DT == 0 || row + 1 < T_total) {
         const uintptr_t rp = reinterpret_cast<uintptr_t>(lp) + (uintptr_t)(row * (int64_t)D) * E;
-        for (int i = threadIdx.x; i < nlab; i += blockDim.x)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (j < L.n)
+                cp_async4(smem_addr(dst + L.li + j * L.nlt), reinterpret_cast<const void*>((rp + L.off[j]) & ~uintptr_t(3)));
+        for (int i = L.li + 2 * L.nlt; i < L.nlab; i += L.nlt)
             cp_async4(smem_addr(dst + i), reinterpret_cast<const void*>((rp + (uintptr_t)labs[i] * E) & ~uintptr_t(3)));
     } else {
-        for (int i = threadIdx.x; i < nlab; i += blockDim.x) fetch_word<DT>(dst + i, lp, row * (int64_t)D + labs[i], lp_end);
+        for (int i = L.li; i < L.nlab; i += L.nlt) fetch_word<DT>(dst + i, lp, row * (int64_t)D + labs[i], lp_end);
     }
 }
 
-// The label values of frame f in extended range, into dst[0 .. nlab): each
-// thread converts the labels whose words it copied (issue_row's mapping), so
-// its own wait for the copies suffices.
+// The thread's label values of a frame in extended range, into dst (each
+// label thread converts the labels whose words it copied, so its own wait
+// for the copies suffices).
 template <int DT>
-__device__ __forceinline__ void convert_row(XP* dst, const uint32_t* lw, const int* labs, int nlab, int flip,
-                                            int base_half) {
-    for (int i = threadIdx.x; i < nlab; i += blockDim.x)
+__device__ __forceinline__ void convert_row(XP* dst, const uint32_t* lw, const int* labs, int flip, int base_half,
+                                            const LabelLane<DT>& L) {
+    if (L.n == 0) return;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = L.li + j * L.nlt;
+        if (j < L.n) st_xp(dst + i, xp_exp(word_to_float<DT>(lw[i], L.par[j] ^ flip)));
+    }
+    for (int i = L.li + 2 * L.nlt; i < L.nlab; i += L.nlt)
         st_xp(dst + i, xp_exp(word_to_float<DT>(lw[i], ((base_half ^ labs[i]) & 1) ^ flip)));
 }
 
@@ -566,6 +613,7 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_forward_kernel(FsaArgs 
     extern __shared__ __align__(16) unsigned char fsa_smem[];
     __shared__ XP red[kFsaMaxThreads / 32];
     const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const int nst = a.nst, li = tid - a.lt0, nlt = a.nlt;  // state threads; this label thread
     const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
     if (nlab < 0) return;  // rejected by the index pass (NaN loss written there)
     const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
@@ -591,32 +639,34 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_forward_kernel(FsaArgs 
     }
     const int4* rin = local ? sm.rec : rin_g;
     const int* inoff = local ? sm.off : inoff_g;
-    for (int i = tid; i < nlab; i += nt) sm.labs[i] = labs_g[i];
-    // label words: frames 0 .. RING - 2 in flight (thread i % nt copies and
-    // converts label i)
+    // the label threads load, copy and convert their own labels (no barrier
+    // between): label words of frames 0 .. RING - 2 in flight
+    if ((unsigned)li < (unsigned)nlt)
+        for (int i = li; i < nlab; i += nlt) sm.labs[i] = labs_g[i];
+    const LabelLane<DT> ll = label_lane<DT>(sm.labs, nlab, li, nlt, base_half);
     auto issue = [&](int f) {
-        if (f < T) issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
+        if (f < T) issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, lp_end, ll);
         cp_async_commit();
     };
     for (int f = 0; f < RING - 1; ++f) issue(f);
     for (int s = tid; s < S; s += nt) st_xp(sm.val + s, xp_exp(a.start_weight[s0 + s]));
     cp_async_wait<RING - 2>();
-    if (T > 0) convert_row<DT>(sm.lpx, sm.ring, sm.labs, nlab, row_flip(start, D), base_half);
+    if (T > 0) convert_row<DT>(sm.lpx, sm.ring, sm.labs, row_flip(start, D), base_half, ll);
     __syncthreads();
     EdgeRegs<PER, RE> er;
-    load_edge_regs<false>(er, inoff, rin, S);
+    load_edge_regs<false>(er, inoff, rin, S, nst);
     bool nan_seen = false;  // a NaN sum: the loss is NaN
     int p = 0;
-    for (int t = 0; t < T; ++t) {
+    XP* row = alpha_rows + start * (int64_t)Smax;  // frame t's stored row
+    for (int t = 0; t < T; ++t, row += Smax) {
         issue(t + RING - 1);
         const XP* alp = sm.val + p * Smax;
         XP* alq = sm.val + (p ^ 1) * Smax;
         const XP* lx = sm.lpx + (t & 1) * cap;  // the frame's label values
-        XP* row = alpha_rows + (start + t) * (int64_t)Smax;
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
-            const int s = tid + k * nt;
-            if (s < S) {
+            const int s = tid + k * nst;
+            if (tid < nst && s < S) {
                 st_xp(row + s, ld_xp(alp + s));  // alpha_t, read by the backward
                 // alpha_{t+1}(s) = sum over the incoming list, in order, of
                 // alpha_t(from) x exp(weight) x exp(lp[t, label])
@@ -634,8 +684,8 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_forward_kernel(FsaArgs 
         }
         cp_async_wait<RING - 2>();
         if (t + 1 < T)
-            convert_row<DT>(sm.lpx + ((t + 1) & 1) * cap, sm.ring + ((t + 1) % RING) * cap, sm.labs, nlab,
-                            row_flip(start + t + 1, D), base_half);
+            convert_row<DT>(sm.lpx + ((t + 1) & 1) * cap, sm.ring + ((t + 1) % RING) * cap, sm.labs,
+                            row_flip(start + t + 1, D), base_half, ll);
         __syncthreads();
         p ^= 1;
     }
@@ -669,7 +719,8 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
     constexpr int RE = PER <= 2 ? 3 : (PER == 4 ? 2 : 1);
     constexpr int RING = fsa_ring(PER);
     extern __shared__ __align__(16) unsigned char fsa_smem[];
-    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+    const int nst = a.nst, nws = nst >> 5, li = tid - a.lt0, nlt = a.nlt;  // state threads and warps; label thread
     const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
     if (nlab < 0) return;  // the rows keep zero headers: zero gradient
     const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
@@ -722,13 +773,22 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
     // the labels whose lists a warp sums (any order: each sum is one warp's)
     for (int i = tid; i < nlab; i += nt)
         if (sm.laboff[i + 1] - sm.laboff[i] > kShortList) sm.longl[atomicAdd(&s_nlong, 1)] = i;
-    // frame f's label words and its stored alpha row (each thread copies its
-    // own states' values) are copied RING - 1 frames ahead
+    // frame f's label words (label threads) and its stored alpha row (each
+    // state thread copies its own states' values) are copied RING - 1 frames
+    // ahead
+    const LabelLane<DT> ll = label_lane<DT>(sm.labs, nlab, li, nlt, base_half);
     auto issue = [&](int f) {
         if (f >= 0) {
-            issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, nlab, lp_end);
-            for (int s = tid; s < S; s += nt)
-                cp_async8(smem_addr(sm.aring + (f % RING) * Smax + s), alpha_rows + (start + f) * (int64_t)Smax + s);
+            issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, lp_end, ll);
+            if (tid < nst) {
+#pragma unroll
+                for (int k = 0; k < PER; ++k) {
+                    const int s = tid + k * nst;
+                    if (s < S)
+                        cp_async8(smem_addr(sm.aring + (f % RING) * Smax + s),
+                                  alpha_rows + (start + f) * (int64_t)Smax + s);
+                }
+            }
         }
         cp_async_commit();
     };
@@ -736,12 +796,12 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
     for (int s = tid; s < S; s += nt) st_xp(sm.val + s, xp_exp(a.final_weight[s0 + s]));
     cp_async_wait<RING - 2>();
     if (T > 0)
-        convert_row<DT>(sm.lpx + ((T - 1) & 1) * cap, sm.ring + ((T - 1) % RING) * cap, sm.labs, nlab,
-                        row_flip(start + T - 1, D), base_half);
+        convert_row<DT>(sm.lpx + ((T - 1) & 1) * cap, sm.ring + ((T - 1) % RING) * cap, sm.labs,
+                        row_flip(start + T - 1, D), base_half, ll);
     __syncthreads();
     const int nlong = s_nlong;
     EdgeRegs<PER, RE> er;
-    load_edge_regs<true>(er, outoff, rout, S);
+    load_edge_regs<true>(er, outoff, rout, S, nst);
     int p = 0;
     for (int t = T - 1; t >= 0; --t) {
         issue(t - (RING - 1));
@@ -752,8 +812,8 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
         float* occ = occ_base + (size_t)(t & 1) * occ_stride;
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
-            const int s = tid + k * nt;
-            if (s < S) {
+            const int s = tid + k * nst;
+            if (tid < nst && s < S) {
                 const XP as = ld_xp(arow + s);
                 const float gm = as.m * izm;
                 const int ge = as.e - zx.e;
@@ -780,8 +840,8 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
         }
         cp_async_wait<RING - 2>();
         if (t > 0)
-            convert_row<DT>(sm.lpx + ((t - 1) & 1) * cap, sm.ring + ((t - 1) % RING) * cap, sm.labs, nlab,
-                            row_flip(start + t - 1, D), base_half);
+            convert_row<DT>(sm.lpx + ((t - 1) & 1) * cap, sm.ring + ((t - 1) % RING) * cap, sm.labs,
+                            row_flip(start + t - 1, D), base_half, ll);
         __syncthreads();
         // the row's class sums (class, -scale * occupancy), each label's edges
         // in list order; the dense rows are written afterwards by the all-SM
@@ -800,10 +860,10 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
             ent[row * cap + i] = make_int2(sm.labs[i], __float_as_int(-scale * P));
         }
         // long lists (the blank of a CTC lattice has about two edges per
-        // label): a warp each, from the last warp down (the last warps hold
-        // the fewest states), lane l summing entries l, l + 32, ... in order,
-        // then a fixed shuffle tree
-        for (int q = nw - 1 - warp; q < (n > 0 ? nlong : 0); q += nw) {
+        // label): a state warp each, from the last state warp down (the last
+        // warps hold the fewest states), lane l summing entries l, l + 32, ...
+        // in order, then a fixed shuffle tree
+        for (int q = nws - 1 - warp; warp < nws && q < (n > 0 ? nlong : 0); q += nws) {
             const int i = sm.longl[q];
             const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
             // four independent partial sums per lane (entries l, l + 32, l + 64,
@@ -852,6 +912,26 @@ int recursion_threads(int max_states) {
     if (nt < 64) nt = 64;
     if (nt > kFsaMaxThreads) nt = kFsaMaxThreads;
     return nt;
+}
+
+// Label threads of a recursion CTA: warps of their own after the nst state
+// threads, one per 64 labels (a sequence's distinct labels, at most
+// min(max_labels, D)), as many as fit the CTA's 512 threads; none when not
+// one fits (the state threads then copy and convert the labels).  Sets
+// a.nst, a.lt0, a.nlt and returns the CTA's threads.
+int recursion_geometry(FsaArgs& a, int max_states) {
+    const int nst = recursion_threads(max_states);
+    int nlw = (a.L.cap + 63) / 64;
+    if (nlw > (kFsaMaxThreads - nst) / 32) nlw = (kFsaMaxThreads - nst) / 32;
+    a.nst = nst;
+    if (nlw < 1) {
+        a.lt0 = 0;
+        a.nlt = nst;
+        return nst;
+    }
+    a.lt0 = nst;
+    a.nlt = 32 * nlw;
+    return nst + 32 * nlw;
 }
 
 // Ring depth of the recursions for sequences of up to max_states states.
@@ -919,10 +999,11 @@ int smem_edges(bool backward, int B, int E_total, int max_states, int cap) {
 }
 
 // The forward or backward recursion with PER states a thread: the smallest
-// of 1, 2, 4, 8 that covers max_states with nt threads.
+// of 1, 2, 4, 8 that covers max_states with the a.nst state threads (nt
+// threads in all, the label warps included).
 template <int DT, bool BACKWARD>
 cudaError_t launch_recursion(int max_states, int B, int nt, size_t smem, cudaStream_t s, const FsaArgs& a) {
-    const int per = (max_states + nt - 1) / nt;
+    const int per = (max_states + a.nst - 1) / a.nst;
     if (per <= 1)
         return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 1>, (unsigned)B, nt, smem, s, a)
                         : launch_fsa(fsa_forward_kernel<DT, 1>, (unsigned)B, nt, smem, s, a);
@@ -1001,7 +1082,7 @@ ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype
     if (launch_fsa(fsa_index_kernel, (unsigned)B, kIdxThreads, ismem, stream, a) != cudaSuccess)
         return CTC_PACKED_ERR_CUDA;
     // 2. per sequence: the forward recursion
-    const int nt = recursion_threads(max_states);
+    const int nt = recursion_geometry(a, max_states);
     a.ecap_smem = smem_edges(false, B, num_edges, max_states, a.L.cap);
     const size_t smem = fsa_smem_plan(false, a.ecap_smem, max_states, a.L.cap, ring_for(max_states), nullptr, nullptr);
     const cudaError_t e = dtype == CTC_PACKED_F32    ? launch_recursion<0, false>(max_states, B, nt, smem, stream, a)
@@ -1042,7 +1123,7 @@ ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtyp
         return CTC_PACKED_ERR_CUDA;
     // 2. per sequence: beta, edge occupancies, each row's class sums and header
     if (B > 0) {
-        const int nt = recursion_threads(max_states);
+        const int nt = recursion_geometry(a, max_states);
         a.ecap_smem = smem_edges(true, B, num_edges, max_states, a.L.cap);
         const size_t smem =
             fsa_smem_plan(true, a.ecap_smem, max_states, a.L.cap, ring_for(max_states), nullptr, nullptr);
