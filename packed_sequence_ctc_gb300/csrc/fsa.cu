@@ -849,8 +849,9 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
         const int64_t row = start + t;
         const int n = nlab;
         // a label's occupancies are the contiguous range [laboff[i],
-        // laboff[i + 1]) in edge order.  Short lists: a thread each, in order
-        for (int i = tid; i < n; i += nt) {
+        // laboff[i + 1]) in edge order.  Short lists: a thread each, in order,
+        // the label threads taking their own labels
+        for (int i = li; (unsigned)li < (unsigned)nlt && i < n; i += nlt) {
             const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
             if (k1 - k0 > kShortList) continue;
             float P = 0.0f;
