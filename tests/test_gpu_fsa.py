@@ -6,8 +6,10 @@ path), seeded random FSAs with weights, several start and final states and
 loops, in the three dtypes; a sequence without a path (with and without
 zero_infinity), frameless sequences and gap rows; a large vocabulary; and
 out-of-range FSA data (and more distinct labels than max_labels), which must
-set the status word and a NaN loss; bitwise reproducibility; and lattices
-of 602 to 2502 states (two to eight states a thread).  The recursions carry
+set the status word and a NaN loss; bitwise reproducibility; lattices
+of 602 to 2502 states (two to eight states a thread); and sequences with
+over a thousand distinct labels (more than two a label thread, with and
+without label warps of their own).  The recursions carry
 float32 mantissas with integer exponents: losses within 1e-4 relative,
 float32 gradients within 2e-5 (on these lengths), half types within one
 unit in the last place plus 1e-3.
@@ -239,3 +241,21 @@ def test_many_states_a_thread(cuda_device, L):
     ref_loss, ref_grad = _oracle(batch.log_probs, batch.cu_seqlens, batch.lengths, fsa, g)
     assert_loss_close(loss, ref_loss)
     assert_grad_close(grad, ref_grad, torch.float32)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("S,E,D", [(40, 3000, 1200), (500, 3000, 2000)])
+def test_many_distinct_labels(cuda_device, dtype, S, E, D):
+    # about 1 100 (1 550) distinct labels in one sequence: more than two a
+    # label thread, whether the labels have warps of their own (40 states:
+    # 14 label warps) or the 512 state threads carry them (500 states)
+    lp = torch.log_softmax(torch.randn(70, D, generator=torch.Generator().manual_seed(21)) * 2.0, -1).to(dtype)
+    fsa = workloads.pack_fsas([workloads.random_fsa(S, E, D, seed=61), workloads.random_fsa(7, 40, D, seed=62)])
+    cu = torch.tensor([0, 50, 70], dtype=torch.int32)
+    ln = torch.tensor([50, 20], dtype=torch.int32)
+    assert _max_labels(fsa) > 1024 if S == 500 else _max_labels(fsa) > 2 * 14 * 32
+    loss, grad, status, g = _run(lp, cu, ln, fsa, _max_states(fsa), grad_loss=[0.8, 1.2])
+    assert status == 0
+    ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)
