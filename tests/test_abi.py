@@ -173,6 +173,9 @@ def test_fsa_host_checks_return_before_any_cuda_call(lib):
     assert _fsa_fwd(lib, ms=0) == UNSUPPORTED
     assert _fsa_fwd(lib, ms=4097) == UNSUPPORTED  # more states than a shared-memory row holds
     assert _fsa_fwd(lib, D=16385) == UNSUPPORTED
+    # states and labels whose per-frame shared-memory buffers exceed a CTA's
+    assert _fsa_fwd(lib, ms=4096, ml=3000, D=16384) == UNSUPPORTED
+    assert _fsa_fwd(lib, ms=2048, ml=3000, D=16384) == UNSUPPORTED
     assert _fsa_fwd(lib, ws=None) == WORKSPACE
     assert _fsa_fwd(lib, ws=128) == WORKSPACE  # not 256-byte aligned
     assert _fsa_fwd(lib, wsb=64) == WORKSPACE
