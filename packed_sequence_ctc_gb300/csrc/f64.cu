@@ -139,14 +139,6 @@ struct F64Args {
 
 __device__ __forceinline__ X64 x_zero() { return X64{0.0, kZeroE}; }
 
-// 2^d as a double for d in [-1022, 1023]; 0 below (a term that far below the
-// largest one of a sum is under its last bit).
-__device__ __forceinline__ double pow2_ll(long long d) {
-    if (d < -1022) return 0.0;
-    if (d > 1023) return __longlong_as_double(0x7ff0000000000000ll);
-    return __longlong_as_double((d + 1023) << 52);
-}
-
 // Brings m >= 0 to [1, 2), adjusting e; zero, subnormal results and
 // exponents below kZeroE give zero; NaN and infinity pass through.
 __device__ __forceinline__ X64 x_norm(double m, long long e) {
@@ -646,6 +638,27 @@ __global__ void __launch_bounds__(256) f64_reduce_kernel(F64Args a) {
 
 // ------------------------------------------------------------ backward kernels
 
+// A posterior (a value in [0, 2)) in fixed point,
+// units of 2^-62: its significand moved by its exponent (bits below 2^-62,
+// about 2e-19, drop out).  Class sums of such values are exact integer
+// sums, the same in any order, and convert to float64 once.
+// Here the posterior is m * 2^d with m >= 0 a normal number or 0, taken by
+// its bits (no float64 operation).
+__device__ __forceinline__ long long post_fixed(double m, long long d) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(m);
+    const int ex = (int)(u >> 52);  // m >= 0: no sign bit
+    if (ex == 0) return 0;
+    const unsigned long long sig = (u & 0xfffffffffffffull) | (1ull << 52);
+    // m 2^d = sig 2^(ex - 1075 + d): times 2^62 is sig 2^(ex - 1013 + d)
+    const long long sh = (long long)ex - 1013 + d;
+    return (long long)(sh >= 0 ? sig << sh : (sh > -64 ? sig >> -sh : 0ull));
+}
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 // Backward recursion of one utterance from its last frame, with the
 // posteriors and their class sums.  beta_t(s) excludes frame t's emission,
 // g_t(s) = beta_t(s) * exp(lp[t, l(s)]) is what frame t - 1 reads:
@@ -663,7 +676,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
     constexpr bool DB = f64_beta_double_buffered(PER);
     constexpr int NB = DB ? 2 : 1;
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ double s_wsum[kMaxChainThreads / 32];
+    __shared__ long long s_wsum[kMaxChainThreads / 32];
     __shared__ int s_warp[32];
     __shared__ int s_bfirst;
     const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
@@ -683,8 +696,9 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
     int* const re = reinterpret_cast<int*>(rm + RING * cap);
     const int Uu = U > 0 ? U : 1;
     double* gm = reinterpret_cast<double*>(re + RING * cap);  // g, mantissas (NB buffers of cap)
-    double* gam = gm + NB * cap;                              // label-state posteriors (NB of Uu)
-    double* gb = gam + NB * Uu;                               // blank-state posteriors (two of U + 1, DB)
+    // posteriors in fixed point (post_fixed)
+    long long* gam = reinterpret_cast<long long*>(gm + NB * cap);  // label states (NB of Uu)
+    long long* gb = gam + NB * Uu;                                 // blank states (two of U + 1, DB)
     int* ge = reinterpret_cast<int*>(gb + (DB ? 2 * (U + 1) : 0));  // g, exponents (NB of cap)
     int* lab = ge + NB * cap;                                 // the target
     int* nxt = lab + U;                                       // next position of the same class, -1: none
@@ -780,34 +794,37 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
             et[k] = s < S ? ld_em(em + (size_t)(T - 1) * Ep + eidx[k]) : x_zero();
         }
     }
+    // a class sum P (fixed point) as its gradient entry -scale * P
+    const double nscale = -scale * 0x1p-62;
+    auto entry = [&](long long P) { return nan_utt ? qnan : nscale * __ll2double_rn(P); };
     // the class sums of frame tt from its label-state posteriors gamr and
-    // (DB) blank-state posteriors gbr: a first occurrence's thread sums its
-    // class's positions in target order; the last warp (the fewest states)
-    // sums the blank class, lane l taking blank states l, l + 32, ..., then a
-    // fixed shuffle tree, then the labels equal to the blank
-    auto class_sums = [&](int tt, const double* gamr, const double* gbr) {
+    // (DB) blank-state posteriors gbr, exact integer sums: a first
+    // occurrence's thread sums its class's positions; the last warp (the
+    // fewest states) sums the blank class, lane l taking blank states l,
+    // l + 32, ..., then a shuffle tree, then the labels equal to the blank
+    auto class_sums = [&](int tt, const long long* gamr, const long long* gbr) {
         double* er = ent + (size_t)tt * a.L.ecap;
         for (int j = tid; j < U; j += nt) {
             const int r = rnk[j];
             if (r < 0) continue;
-            double P = gamr[j];
+            long long P = gamr[j];
             for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gamr[jj];
-            er[r] = -scale * P;
+            er[r] = entry(P);
         }
         if (warp == nw - 1) {
-            double P = 0.0;
+            long long P = 0;
             for (int i = lane; i <= U; i += 32) P += gbr[i];
-            P = warp_sum(P);
+            P = warp_sum_ll(P);
             if (lane == 0) {
                 for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gamr[jj];
-                er[ncls - 1] = -scale * P;
+                er[ncls - 1] = entry(P);
             }
         }
     };
     int p = 0;  // DB: g and the posteriors of frame t + 1 are in buffer p
     for (int t = T - 1; t >= 0; --t) {
         X64 gn[PER];
-        double gamma[PER];
+        long long gamma[PER];  // posteriors in fixed point
         X64 al_n[PER], et_n[PER];
         if constexpr (RING > 0) {
             issue(t - (RING - 1));
@@ -840,7 +857,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
         for (int k = 0; k < PER; ++k) {
             const int s = tid + k * nt;
             gn[k] = x_zero();
-            gamma[k] = 0.0;
+            gamma[k] = 0;
             if (s < S) {
                 X64 be;
                 if (t == T - 1) {
@@ -855,17 +872,15 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                 // (mantissa product in [0.25, 4) or 0) * 2^(exponents - ze); a
                 // posterior is at most 1, so the exponent sum is at most ~2
                 const long long d = (long long)al[k].e + be.e - ze;
-                const double gm = al[k].m * be.m * invz;
-                const double g = d <= 0 ? scale_pow2_nonpos(gm, d) : gm * pow2_ll(d);
-                gamma[k] = nan_utt ? qnan : g;
+                gamma[k] = nan_utt ? 0 : post_fixed(al[k].m * be.m * invz, d);  // NaN entries: see entry
             }
         }
         if constexpr (DB) {
             // frame t's values into the other buffers; one barrier
             double* gmq = gm + (p ^ 1) * cap;
             int* geq = ge + (p ^ 1) * cap;
-            double* gamq = gam + (p ^ 1) * Uu;
-            double* gbq = gb + (p ^ 1) * (U + 1);
+            long long* gamq = gam + (p ^ 1) * Uu;
+            long long* gbq = gb + (p ^ 1) * (U + 1);
 #pragma unroll
             for (int k = 0; k < PER; ++k) {
                 const int s = tid + k * nt;
@@ -882,7 +897,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
             p ^= 1;
         } else {
             __syncthreads();  // A
-            double bpart = 0.0;
+            long long bpart = 0;
 #pragma unroll
             for (int k = 0; k < PER; ++k) {
                 const int s = tid + k * nt;
@@ -900,22 +915,22 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                     et[k] = et_n[k];
                 }
             }
-            bpart = warp_sum(bpart);
+            bpart = warp_sum_ll(bpart);
             if (lane == 0) s_wsum[warp] = bpart;
             __syncthreads();  // B
             double* er = ent + (size_t)t * a.L.ecap;
             for (int j = tid; j < U; j += nt) {
                 const int r = rnk[j];
                 if (r < 0) continue;
-                double P = gam[j];
+                long long P = gam[j];
                 for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gam[jj];
-                er[r] = -scale * P;
+                er[r] = entry(P);
             }
             if (tid == 0) {
-                double P = 0.0;
+                long long P = 0;
                 for (int w = 0; w < nw; ++w) P += s_wsum[w];
                 for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gam[jj];
-                er[ncls - 1] = -scale * P;
+                er[ncls - 1] = entry(P);
             }
         }
         if constexpr (DB && RING == 0) {
