@@ -62,16 +62,19 @@ __host__ __device__ constexpr int f64_ring(bool backward, int per) { return per 
 // The beta kernel double-buffers its per-frame values up to 4 states a thread.
 __host__ __device__ constexpr bool f64_beta_double_buffered(int per) { return per <= 4; }
 
-// Extended-range value m * 2^e, m in [1, 2), or zero (m = 0, e = kZeroE);
-// NaN and infinity are carried in m.
+// Extended-range value m * 2^(e - 61): m an integer with its leading one at
+// bit 61 (62 significant bits, carried on the integer pipes: this part's
+// float64 pipe is narrow), or zero (m = 0, e = kZeroE).  NaN and infinite
+// inputs are flagged apart (the utterance's loss is NaN).
 struct X64 {
-    double m;
+    unsigned long long m;
     int e;
 };
+constexpr unsigned long long kXOne = 1ull << 61;  // the mantissa of 1
 
 // Emission entry of the workspace (16 bytes).
 struct EmX {
-    double m;
+    unsigned long long m;
     int32_t e, pad;
 };
 
@@ -137,55 +140,61 @@ struct F64Args {
 
 // ------------------------------------------------------------ extended range
 
-__device__ __forceinline__ X64 x_zero() { return X64{0.0, kZeroE}; }
+__device__ __forceinline__ X64 x_zero() { return X64{0ull, kZeroE}; }
 
-// Brings m >= 0 to [1, 2), adjusting e; zero, subnormal results and
-// exponents below kZeroE give zero; NaN and infinity pass through.
-__device__ __forceinline__ X64 x_norm(double m, long long e) {
-    const long long bits = __double_as_longlong(m);
-    const int be = (int)((bits >> 52) & 0x7ff);
-    if (be == 0x7ff) return X64{m, 0};
-    if (be == 0) return x_zero();
-    const long long ne = e + (be - 1023);
+// m * 2^(e - 61) (m < 2^64) with m's leading one moved to bit 61; exponents
+// below kZeroE give zero, above 2^30 saturate.
+__device__ __forceinline__ X64 x_norm(unsigned long long m, long long e) {
+    if (m == 0) return x_zero();
+    const int sh = __clzll((long long)m) - 2;
+    const unsigned long long mm = sh >= 0 ? m << sh : m >> -sh;
+    const long long ne = e - sh;
     if (ne <= kZeroE) return x_zero();
-    if (ne > (1ll << 30)) return X64{__longlong_as_double(0x7ff0000000000000ll), 0};
-    return X64{__longlong_as_double((bits & 0x800fffffffffffffll) | (1023ll << 52)), (int)ne};
+    return X64{mm, (int)min(ne, (long long)(1 << 30))};
 }
 
-// m * 2^d for d <= 0, by the exponent field (integer operations: this
-// part's float64 pipe is narrow).  m is a normal number whose exponent field
-// exceeds -d (a mantissa in [1, 4): the result stays normal down to
-// d = -1022), or 0, NaN or infinity, which come back unchanged (NaN and
-// infinity only with d = 0, as the largest term of a sum); terms scaled
-// below 2^-1022 are 0.
-__device__ __forceinline__ double scale_pow2_nonpos(double m, long long d) {
-    const long long bits = __double_as_longlong(m);
-    const long long ex = (bits >> 52) & 0x7ff;
-    if (ex == 0 || ex == 0x7ff) return m;
-    if (ex + d < 1) return 0.0;
-    return __longlong_as_double(bits + (d << 52));
-}
-
+// a + b + c: each mantissa shifted to the largest exponent (bits below the
+// 62nd drop out), summed (below 3 * 2^62), renormalised.
 __device__ __forceinline__ X64 x_add3(X64 a, X64 b, X64 c) {
     const int E = max(a.e, max(b.e, c.e));
-    const double m = scale_pow2_nonpos(a.m, (long long)a.e - E) + scale_pow2_nonpos(b.m, (long long)b.e - E) +
-                     scale_pow2_nonpos(c.m, (long long)c.e - E);
-    return x_norm(m, E);
+    auto aligned = [&](X64 x) {
+        const long long d = (long long)E - x.e;
+        return d < 62 ? x.m >> d : 0ull;
+    };
+    return x_norm(aligned(a) + aligned(b) + aligned(c), E);
 }
 
-__device__ __forceinline__ X64 x_mul(X64 a, X64 b) { return x_norm(a.m * b.m, (long long)a.e + b.e); }
+// a * b: the 124-bit product of the mantissas, its leading 62 bits (the
+// high word moved up by 2 or 3 with the low word's top bits).
+__device__ __forceinline__ X64 x_mul(X64 a, X64 b) {
+    const unsigned long long hi = __umul64hi(a.m, b.m), lo = a.m * b.m;
+    if (hi == 0) return x_zero();  // a zero factor: normalised products are at least 2^122
+    const int s = __clzll((long long)hi) - 2;  // 2 or 3
+    const long long e = (long long)a.e + b.e + 3 - s;
+    if (e <= kZeroE) return x_zero();
+    return X64{(hi << s) | (lo >> (64 - s)), (int)min(e, (long long)(1 << 30))};
+}
+
+// A positive normal float64 v times 2^k in extended range, by v's bits.
+__device__ __forceinline__ X64 x_of_double(double v, long long k) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(v);
+    const long long e = (long long)(u >> 52) - 1023 + k;
+    if (e <= kZeroE) return x_zero();
+    return X64{((u & 0xfffffffffffffull) | (1ull << 52)) << 9, (int)min(e, (long long)(1 << 30))};
+}
+
+// The mantissa of a nonzero extended value as a float64 in [1, 2).
+__device__ __forceinline__ double x_mantissa(X64 x) { return __ull2double_rn(x.m) * 0x1p-61; }
 
 // exp(x) in extended range: x = k ln2 + r with k = floor(x log2 e), then
-// exp(r) in [1, 2) up to rounding (renormalised).
+// exp(r) in [1, 2) up to rounding, taken by its bits.  -inf gives zero, and
+// so do NaN and +inf (the caller flags those).
 __device__ __forceinline__ X64 x_from_log(double x) {
-    if (x != x) return X64{x, 0};
-    if (x == -INFINITY) return x_zero();
-    if (x == INFINITY) return X64{x, 0};
+    if (!(x > -INFINITY) || !(x < INFINITY)) return x_zero();
     const double k = floor(x * kLog2eD);
     if (k < (double)kZeroE) return x_zero();
-    if (k > (double)(1 << 30)) return X64{__longlong_as_double(0x7ff0000000000000ll), 0};
     const double r = fma(-k, kLn2D, x);
-    return x_norm(exp(r), (long long)k);
+    return x_of_double(exp(r), (long long)k);
 }
 
 // ln 2 / 64 in units of 2^-53: kLn2o64Hi + kLn2o64Lo / 2^11 (within 2^-12
@@ -248,8 +257,8 @@ __device__ __forceinline__ void fill_exp_table(double* T) {
 }
 
 __device__ __forceinline__ X64 ld_em(const EmX* p) {
-    const double2 v = *reinterpret_cast<const double2*>(p);
-    return X64{v.x, (int)__double_as_longlong(v.y)};
+    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
+    return X64{v.x, (int)(long long)v.y};
 }
 
 // 4-, 8- and 16-byte async copies global -> shared.
@@ -447,10 +456,10 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_emit_kernel(F64Args a) {
             X64 v = x_zero();
             if (c >= 0 && c < D) {
                 const double y = __ldg(x + c) - sh;
-                nan |= y != y;
+                nan |= !(y < INFINITY);  // NaN or +inf: the utterance's loss is NaN
                 v = x_from_log(y);
             }
-            *reinterpret_cast<double2*>(out + k) = make_double2(v.m, __longlong_as_double((long long)v.e));
+            *reinterpret_cast<ulonglong2*>(out + k) = make_ulonglong2(v.m, (unsigned long long)(long long)v.e);
         }
         if (__any_sync(0xffffffffu, nan) && lane == 0) atomicOr(&utt[b].has_nan, 1);
     }
@@ -473,7 +482,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
     if (!u.valid || u.T == 0) return;
     const int U = u.U, S = 2 * U + 1, T = u.T, Ep = a.L.Ep, Sp = a.L.Sp;
     const int cap = PER * nt;
-    double* const mbuf = reinterpret_cast<double*>(smem);         // two buffers of cap mantissas
+    unsigned long long* const mbuf = reinterpret_cast<unsigned long long*>(smem);  // two buffers of cap mantissas
     int* const ebuf = reinterpret_cast<int*>(mbuf + 2 * cap);      // two buffers of cap exponents
     EmX* const ring = reinterpret_cast<EmX*>(ebuf + 2 * cap);      // RING frames of the states' emissions
     if (tid == 0) s_bad = 0;
@@ -506,7 +515,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
         return;
     }
     const EmX* em = ws_at<EmX>(a.ws, a.L.off_em) + (size_t)u.start * Ep;
-    double* am = ws_at<double>(a.ws, a.L.off_am) + (size_t)u.start * Sp;
+    unsigned long long* am = ws_at<unsigned long long>(a.ws, a.L.off_am) + (size_t)u.start * Sp;
     int32_t* ae = ws_at<int32_t>(a.ws, a.L.off_ae) + (size_t)u.start * Sp;
     const bool store = a.need_grad != 0;
 
@@ -561,9 +570,9 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
                 if (s < S && t + 1 < T) nx[k] = ld_em(em + (size_t)(t + 1) * Ep + ent[k]);
             }
         }
-        const double* mp = mbuf + p * cap;
+        const unsigned long long* mp = mbuf + p * cap;
         const int* ep = ebuf + p * cap;
-        double* mq = mbuf + (p ^ 1) * cap;
+        unsigned long long* mq = mbuf + (p ^ 1) * cap;
         int* eq = ebuf + (p ^ 1) * cap;
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
@@ -586,24 +595,25 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
     }
     if (RING > 0) cp_async_wait<0>();
     if (tid == 0) {
-        const double* mp = mbuf + p * cap;
+        const unsigned long long* mp = mbuf + p * cap;
         const int* ep = ebuf + p * cap;
         const X64 last{mp[S - 1], ep[S - 1]};
         const X64 prev = S >= 2 ? X64{mp[S - 2], ep[S - 2]} : x_zero();
         const X64 z = x_add3(last, prev, x_zero());
         const bool has_nan = u.has_nan != 0;  // written by the emission gather
-        double v;
+        double v, zm = 0.0;
         int inf = 0;
-        if (has_nan || z.m != z.m) {
+        if (has_nan) {
             v = __longlong_as_double(0x7ff8000000000000ll);
-        } else if (z.m == 0.0) {
+        } else if (z.m == 0) {
             v = __longlong_as_double(0x7ff0000000000000ll);
             inf = 1;
         } else {
-            v = -(log(z.m) + (double)z.e * kLn2D);
+            zm = x_mantissa(z);
+            v = -(log(zm) + (double)z.e * kLn2D);
         }
         utt[b].nll = v;
-        utt[b].zm = z.m;
+        utt[b].zm = zm;
         utt[b].ze = z.e;
         utt[b].nll_inf = inf;
         if (a.reduction == CTC_PACKED_NONE) a.loss[b] = (a.zero_infinity && inf) ? 0.0 : v;
@@ -638,20 +648,14 @@ __global__ void __launch_bounds__(256) f64_reduce_kernel(F64Args a) {
 
 // ------------------------------------------------------------ backward kernels
 
-// A posterior (a value in [0, 2)) in fixed point,
-// units of 2^-62: its significand moved by its exponent (bits below 2^-62,
-// about 2e-19, drop out).  Class sums of such values are exact integer
-// sums, the same in any order, and convert to float64 once.
-// Here the posterior is m * 2^d with m >= 0 a normal number or 0, taken by
-// its bits (no float64 operation).
-__device__ __forceinline__ long long post_fixed(double m, long long d) {
-    const unsigned long long u = (unsigned long long)__double_as_longlong(m);
-    const int ex = (int)(u >> 52);  // m >= 0: no sign bit
-    if (ex == 0) return 0;
-    const unsigned long long sig = (u & 0xfffffffffffffull) | (1ull << 52);
-    // m 2^d = sig 2^(ex - 1075 + d): times 2^62 is sig 2^(ex - 1013 + d)
-    const long long sh = (long long)ex - 1013 + d;
-    return (long long)(sh >= 0 ? sig << sh : (sh > -64 ? sig >> -sh : 0ull));
+// A posterior (an extended value in [0, 2)) in fixed point, units of 2^-62:
+// its mantissa moved by its exponent (bits below 2^-62, about 2e-19, drop
+// out).  Class sums of such values are exact integer sums, the same in any
+// order, and convert to float64 once.
+__device__ __forceinline__ long long post_fixed(X64 x) {
+    if (x.m == 0) return 0;
+    const long long sh = (long long)x.e + 1;  // m 2^(e - 61) times 2^62
+    return (long long)(sh >= 0 ? x.m << sh : (sh > -64 ? x.m >> -sh : 0ull));
 }
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
 #pragma unroll
@@ -692,10 +696,10 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
     // RING frames of the states' emissions and stored alpha rows, then the
     // per-frame buffers
     EmX* const rx = reinterpret_cast<EmX*>(smem);
-    double* const rm = reinterpret_cast<double*>(rx + RING * cap);
+    unsigned long long* const rm = reinterpret_cast<unsigned long long*>(rx + RING * cap);
     int* const re = reinterpret_cast<int*>(rm + RING * cap);
     const int Uu = U > 0 ? U : 1;
-    double* gm = reinterpret_cast<double*>(re + RING * cap);  // g, mantissas (NB buffers of cap)
+    unsigned long long* gm = reinterpret_cast<unsigned long long*>(re + RING * cap);  // g, mantissas (NB of cap)
     // posteriors in fixed point (post_fixed)
     long long* gam = reinterpret_cast<long long*>(gm + NB * cap);  // label states (NB of Uu)
     long long* gb = gam + NB * Uu;                                 // blank states (two of U + 1, DB)
@@ -751,11 +755,10 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
 
     // 2. the recursion
     const EmX* em = ws_at<EmX>(a.ws, a.L.off_em) + (size_t)u.start * Ep;
-    const double* am = ws_at<double>(a.ws, a.L.off_am) + (size_t)u.start * Sp;
+    const unsigned long long* am = ws_at<unsigned long long>(a.ws, a.L.off_am) + (size_t)u.start * Sp;
     const int32_t* ae = ws_at<int32_t>(a.ws, a.L.off_ae) + (size_t)u.start * Sp;
     double* ent = ws_at<double>(a.ws, a.L.off_ent) + (size_t)u.start * a.L.ecap;
-    const double invz = 1.0 / u.zm;
-    const long long ze = u.ze;
+    const X64 izx = x_of_double(1.0 / u.zm, -(long long)u.ze);  // 1 / Z
     const bool nan_utt = u.has_nan != 0;
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
     int eidx[PER];
@@ -848,7 +851,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                 }
             }
         }
-        const double* gmp = gm + (DB ? p * cap : 0);  // g of frame t + 1
+        const unsigned long long* gmp = gm + (DB ? p * cap : 0);  // g of frame t + 1
         const int* gep = ge + (DB ? p * cap : 0);
         if constexpr (DB) {
             if (t + 1 < T) class_sums(t + 1, gam + p * Uu, gb + p * (U + 1));
@@ -861,7 +864,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
             if (s < S) {
                 X64 be;
                 if (t == T - 1) {
-                    be = s >= S - 2 ? X64{1.0, 0} : x_zero();
+                    be = s >= S - 2 ? X64{kXOne, 0} : x_zero();
                 } else {
                     const X64 v0{gmp[s], gep[s]};
                     const X64 v1 = s + 1 < S ? X64{gmp[s + 1], gep[s + 1]} : x_zero();
@@ -869,15 +872,13 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                     be = x_add3(v0, v1, v2);
                 }
                 gn[k] = x_mul(be, et[k]);
-                // (mantissa product in [0.25, 4) or 0) * 2^(exponents - ze); a
-                // posterior is at most 1, so the exponent sum is at most ~2
-                const long long d = (long long)al[k].e + be.e - ze;
-                gamma[k] = nan_utt ? 0 : post_fixed(al[k].m * be.m * invz, d);  // NaN entries: see entry
+                // the posterior alpha * beta / Z (at most 1) in fixed point
+                gamma[k] = nan_utt ? 0 : post_fixed(x_mul(x_mul(al[k], be), izx));  // NaN entries: see entry
             }
         }
         if constexpr (DB) {
             // frame t's values into the other buffers; one barrier
-            double* gmq = gm + (p ^ 1) * cap;
+            unsigned long long* gmq = gm + (p ^ 1) * cap;
             int* geq = ge + (p ^ 1) * cap;
             long long* gamq = gam + (p ^ 1) * Uu;
             long long* gbq = gb + (p ^ 1) * (U + 1);
