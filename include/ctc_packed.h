@@ -226,9 +226,11 @@ ctc_packed_status ctc_packed_forward_backward(const void* log_probs, ctc_packed_
  *   log_probs, grad_log_probs  8-byte aligned; not overlapping.
  *   loss                       float64 device output: B entries for NONE, 1 otherwise.
  *   grad_loss                  float64 device input: B entries for NONE, 1 otherwise.
- * Precision: probabilities are carried as a float64 mantissa with an int
- * exponent through both recursions, so no state underflows; the loss and
+ * Precision: probabilities are carried as a 62-bit integer mantissa with an
+ * int exponent through both recursions, so no state underflows; the loss and
  * gradient agree with an exact float64 evaluation to about 1e-12 relative.
+ * A NaN or +inf label or blank log probability gives the utterance a NaN
+ * loss (and NaN class entries in its gradient rows).
  * Page "feat(asr): native CTC loss kernel over sequence-packed log
  * probabilities": ctc.py forward_packed serves float64 at float64 precision
  * on a path of its own, and test_ctc_loss.py test_float64_takes_padded_path
