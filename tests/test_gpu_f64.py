@@ -169,6 +169,19 @@ def test_nan_log_probability(cuda_device):
     assert_close64(grad[30:], ref_grad[30:], "grad of the clean utterance")
 
 
+def test_positive_infinite_log_probability(cuda_device):
+    # not a log probability: the utterance's loss is NaN, as with a NaN; the
+    # other utterance is unaffected
+    batch = workloads.make_batch([30, 20], [5, 4], 9, dtype=torch.float64, seed=58, reduction="none")
+    batch.log_probs[7, batch.blank] = float("inf")
+    loss, grad, status = run_f64(batch)
+    assert status == 0
+    assert np.isnan(loss[0])
+    ref_loss, ref_grad, _ = _ref(batch)
+    assert_close64(loss[1:], ref_loss[1:], "loss")
+    assert_close64(grad[30:], ref_grad[30:], "grad of the clean utterance")
+
+
 def test_label_out_of_range_sets_status(cuda_device):
     batch = workloads.make_batch([30, 20], [3, 2], 9, dtype=torch.float64, seed=57, reduction="none",
                                  targets=[[1, 9, 2], [3, 4]])
