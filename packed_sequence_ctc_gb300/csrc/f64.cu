@@ -654,7 +654,10 @@ __global__ void __launch_bounds__(256) f64_reduce_kernel(F64Args a) {
 // order, and convert to float64 once.
 __device__ __forceinline__ long long post_fixed(X64 x) {
     if (x.m == 0) return 0;
-    const long long sh = (long long)x.e + 1;  // m 2^(e - 61) times 2^62
+    // m 2^(e - 61) times 2^62; a posterior is at most 1 (e <= 0), and the
+    // shift is capped at 1 for the undefined rows of an utterance without a
+    // path (Z = 0 and no zero_infinity)
+    const long long sh = min((long long)x.e + 1, 1ll);
     return (long long)(sh >= 0 ? x.m << sh : (sh > -64 ? x.m >> -sh : 0ull));
 }
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
