@@ -660,6 +660,21 @@ __device__ __forceinline__ long long post_fixed(X64 x) {
     const long long sh = min((long long)x.e + 1, 1ll);
     return (long long)(sh >= 0 ? x.m << sh : (sh > -64 ? x.m >> -sh : 0ull));
 }
+// The posterior a * b * c (alpha, beta, 1 / Z) in the same fixed point,
+// without normalising the products: the high word of a.m * b.m (below
+// 2^60), the high word of that times c.m (below 2^58), moved by the
+// exponent sum: a.m b.m c.m 2^(ea + eb + ec - 183) = p 2^(ea + eb + ec - 55)
+// with p the second high word, times 2^62.
+__device__ __forceinline__ long long post_fixed3(X64 a, X64 b, X64 c) {
+    const unsigned long long p = __umul64hi(__umul64hi(a.m, b.m), c.m);
+    if (p == 0) return 0;
+    // a posterior of at most 1 needs a shift of at most 7 (p >= 2^55); the
+    // cap keeps the shift defined on the undefined rows of an utterance
+    // without a path
+    const long long sh = min((long long)a.e + b.e + c.e + 7, 7ll);
+    return (long long)(sh >= 0 ? p << sh : (sh > -64 ? p >> -sh : 0ull));
+}
+
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -876,7 +891,7 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a
                 }
                 gn[k] = x_mul(be, et[k]);
                 // the posterior alpha * beta / Z (at most 1) in fixed point
-                gamma[k] = nan_utt ? 0 : post_fixed(x_mul(x_mul(al[k], be), izx));  // NaN entries: see entry
+                gamma[k] = nan_utt ? 0 : post_fixed3(al[k], be, izx);  // NaN entries: see entry
             }
         }
         if constexpr (DB) {
