@@ -4,7 +4,7 @@ The call must give exactly what a forward followed by a backward gives: the
 same losses and the same gradient bits, on every named workload and on the
 edge cases of the page's test file (test_ctc_loss.py of "feat(asr): native
 CTC loss kernel over sequence-packed log probabilities"), which are also
-checked against the fp64 oracle.  Rows of at least 2 KB take the bulk-copy
+checked against the fp64 oracle.  Rows of at least 4 KB take the bulk-copy
 gradient stream; CTC_PACKED_STREAM=1 sends narrow rows through it as well, so
 the edge cases run there at small sizes too.
 """
@@ -82,7 +82,7 @@ def test_fused_wide_rows_match_oracle(cuda_device, case, reduction):
 def test_fused_narrow_rows_through_the_bulk_copy_stream(cuda_device, case, monkeypatch):
     monkeypatch.setenv("CTC_PACKED_STREAM", "1")
     batch = dict(_wide_cases())[case]
-    # the same utterances with 9 classes: rows far below 2 KB
+    # the same utterances with 9 classes: rows far below 4 KB
     small = workloads.make_batch(batch.lengths.tolist(), batch.target_lengths.tolist(), 9, seed=2,
                                  targets=None, label_high=8, repeat_prob=0.2, dtype=batch.log_probs.dtype,
                                  zero_infinity=batch.zero_infinity)
