@@ -58,12 +58,12 @@ namespace ctcp {
 
 namespace {
 
-template <int P>
+template <int P, int G_>
 struct ChainShape {
-    static constexpr int G = ghost_lanes(P);  // shadow lanes per warp
-    static constexpr int GP = group_pairs(P); // pairs a warp owns
-    static constexpr int F = G * P;           // frames between halo exchanges (8, 4, 4)
-    static constexpr int R = P == 1 ? 8 : 4;  // emission frames in flight per warp
+    static constexpr int G = G_;                 // shadow lanes per warp
+    static constexpr int GP = group_pairs(P, G); // pairs a warp owns
+    static constexpr int F = G * P;              // frames between halo exchanges (8, 8, 4, 4)
+    static constexpr int R = F == 8 ? 8 : 4;     // emission frames in flight per warp
     // extended values per lane and frame in the ring: (label 0, blank), the
     // other labels, padded to 16 bytes
     static constexpr int LW = 2 * ((P + 2) / 2);
@@ -117,9 +117,9 @@ struct ItemCtx {
 // warps of a multi-warp item exchange their edges.
 // CKPT: the checkpoint policy (store_rows > 1) is compiled as a variant of
 // its own, so that the default (every row or none) keeps the plain loop.
-template <int P, int DIR, bool CKPT>
+template <int P, int G, int DIR, bool CKPT>
 __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
-    using S = ChainShape<P>;
+    using S = ChainShape<P, G>;
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     const UttInfo info = ws_at<UttInfo>(a.ws, a.L.off_utt)[b];
     double* nll_out = ws_at<double>(a.ws, a.L.off_nll);
@@ -476,12 +476,12 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     }
 }
 
-template <int P, bool CKPT>
+template <int P, int G, bool CKPT>
 __device__ __forceinline__ void run_item(const ChainArgs& a, int item, const ItemCtx& c) {
     if (item & 1) {
-        run_chain<P, 1, CKPT>(a, item >> 1, c);
+        run_chain<P, G, 1, CKPT>(a, item >> 1, c);
     } else {
-        run_chain<P, 0, CKPT>(a, item >> 1, c);
+        run_chain<P, G, 0, CKPT>(a, item >> 1, c);
     }
 }
 
@@ -493,9 +493,9 @@ __device__ __forceinline__ void run_item(const ChainArgs& a, int item, const Ite
 // workload's 8-warp chains).
 // CKPT: the chains keep only checkpoint rows (store_rows > 1), a kernel of
 // its own so that the default one holds only the plain loop.
-template <int P, int MAXT, bool CKPT>
+template <int P, int G, int MAXT, bool CKPT>
 __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
-    using S = ChainShape<P>;
+    using S = ChainShape<P, G>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_item;
     __shared__ int s_last;
@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
         const int item = queue[k];
         const int U = utt[item >> 1].U;
         const int nw = min(NW, (U + 1 + S::GP - 1) / S::GP);
-        if (warp < nw) run_item<P, CKPT>(a, item, ItemCtx{warp, nw, my_ring, xch, fins, my_stage});
+        if (warp < nw) run_item<P, G, CKPT>(a, item, ItemCtx{warp, nw, my_ring, xch, fins, my_stage});
     }
     // 2. single-warp chains, each warp on its own
     for (;;) {
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
         if (lane == 0) k = (int)atomicAdd(&ctrl->small_head, 1u);
         k = __shfl_sync(0xffffffffu, k, 0);
         if (k >= n_small) break;
-        run_item<P, CKPT>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp, my_stage});
+        run_item<P, G, CKPT>(a, queue[n_big + k], ItemCtx{0, 1, my_ring, xch, fins + 2 * warp, my_stage});
     }
     // 3. (the label analysis of the backward runs in the emission gather's kernel)
     // 4. the last CTA to finish reduces the losses (fixed order: deterministic)
@@ -568,20 +568,22 @@ __global__ void __launch_bounds__(MAXT, 1) chain_kernel(ChainArgs a) {
     }
 }
 
-template __global__ void chain_kernel<1, 256, false>(ChainArgs);
-template __global__ void chain_kernel<1, 512, false>(ChainArgs);
-template __global__ void chain_kernel<2, 512, false>(ChainArgs);
-template __global__ void chain_kernel<2, 1024, false>(ChainArgs);
-template __global__ void chain_kernel<4, 1024, false>(ChainArgs);
-template __global__ void chain_kernel<1, 256, true>(ChainArgs);
-template __global__ void chain_kernel<1, 512, true>(ChainArgs);
-template __global__ void chain_kernel<2, 512, true>(ChainArgs);
-template __global__ void chain_kernel<2, 1024, true>(ChainArgs);
-template __global__ void chain_kernel<4, 1024, true>(ChainArgs);
+template __global__ void chain_kernel<1, 8, 256, false>(ChainArgs);
+template __global__ void chain_kernel<1, 8, 512, false>(ChainArgs);
+template __global__ void chain_kernel<2, 4, 512, false>(ChainArgs);
+template __global__ void chain_kernel<2, 2, 512, false>(ChainArgs);
+template __global__ void chain_kernel<2, 2, 1024, false>(ChainArgs);
+template __global__ void chain_kernel<4, 1, 1024, false>(ChainArgs);
+template __global__ void chain_kernel<1, 8, 256, true>(ChainArgs);
+template __global__ void chain_kernel<1, 8, 512, true>(ChainArgs);
+template __global__ void chain_kernel<2, 4, 512, true>(ChainArgs);
+template __global__ void chain_kernel<2, 2, 512, true>(ChainArgs);
+template __global__ void chain_kernel<2, 2, 1024, true>(ChainArgs);
+template __global__ void chain_kernel<4, 1, 1024, true>(ChainArgs);
 
-template <int P, int MAXT, bool CKPT>
+template <int P, int G, int MAXT, bool CKPT>
 static cudaError_t launch_chain_c(const ChainArgs& a, cudaStream_t s) {
-    using S = ChainShape<P>;
+    using S = ChainShape<P, G>;
     const int nw = a.L.nwo;  // warps for the longest possible target
     const size_t smem = sizeof(XP) * ((size_t)nw * S::R * 32 * S::LW + 2 * (size_t)nw * S::XW + 2 * (size_t)nw) +
                         sizeof(int) * (size_t)nw * S::kStageInts;
@@ -590,11 +592,11 @@ static cudaError_t launch_chain_c(const ChainArgs& a, cudaStream_t s) {
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     // set on every call (on the current device): a cached value could go
     // stale between host threads launching with different sizes
-    e = cudaFuncSetAttribute(chain_kernel<P, MAXT, CKPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(chain_kernel<P, G, MAXT, CKPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P, MAXT, CKPT>, 32 * nw, smem)) !=
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel<P, G, MAXT, CKPT>, 32 * nw, smem)) !=
         cudaSuccess)
         return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -602,22 +604,23 @@ static cudaError_t launch_chain_c(const ChainArgs& a, cudaStream_t s) {
     long long want = 2ll * a.L.B;
     long long grid = (long long)sms * per_sm;
     if (want < grid) grid = want > 0 ? want : 1;
-    return launch_pdl(chain_kernel<P, MAXT, CKPT>, dim3((unsigned)grid), dim3(32 * nw), smem, s, a);
+    return launch_pdl(chain_kernel<P, G, MAXT, CKPT>, dim3((unsigned)grid), dim3(32 * nw), smem, s, a);
 }
 
-template <int P, int MAXT>
+template <int P, int G, int MAXT>
 static cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t s) {
-    return a.store_rows > 1 ? launch_chain_c<P, MAXT, true>(a, s) : launch_chain_c<P, MAXT, false>(a, s);
+    return a.store_rows > 1 ? launch_chain_c<P, G, MAXT, true>(a, s) : launch_chain_c<P, G, MAXT, false>(a, s);
 }
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s) {
     // the smallest thread bound that holds the chain's warps: fewer threads
     // a CTA, more registers a thread
-    switch (pairs_for_max_u(a.L.max_U)) {
-        case 1: return a.L.nwo <= 8 ? launch_chain_t<1, 256>(a, s) : launch_chain_t<1, 512>(a, s);
-        case 2: return a.L.nwo <= 16 ? launch_chain_t<2, 512>(a, s) : launch_chain_t<2, 1024>(a, s);
-        default: return launch_chain_t<4, 1024>(a, s);
-    }
+    int P, G;
+    chain_shape_for_max_u(a.L.max_U, P, G);
+    if (P == 1) return a.L.nwo <= 8 ? launch_chain_t<1, 8, 256>(a, s) : launch_chain_t<1, 8, 512>(a, s);
+    if (P == 2 && G == 4) return launch_chain_t<2, 4, 512>(a, s);
+    if (P == 2) return a.L.nwo <= 16 ? launch_chain_t<2, 2, 512>(a, s) : launch_chain_t<2, 2, 1024>(a, s);
+    return launch_chain_t<4, 1, 1024>(a, s);
 }
 
 }  // namespace ctcp

@@ -99,23 +99,41 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // check (those rows are never consumed).
 constexpr int kEmPad = 8;
 
-// Lanes of a chain warp that shadow the neighbouring warp's edge pairs, so
-// the warp runs ghost_lanes(P) * P frames between two halo exchanges: 8, 4
-// and 4 frames.  (Measured with one pair per lane on the 8193-class
-// workload: 8 shadow lanes beat 4, 2 and 16; fewer frames per exchange pay
-// for more barriers, more shadow lanes for more warps.)
-__host__ __device__ constexpr int ghost_lanes(int P) { return P == 1 ? 8 : P == 2 ? 2 : 1; }
-__host__ __device__ constexpr int group_pairs(int P) { return (32 - ghost_lanes(P)) * P; }
-// State pairs (blank, label) each lane of a chain warp holds, from the target
-// bound; a warp owns group_pairs(P) pairs and at most 32 warps run a chain.
-// One pair per lane up to 16 warps (a chain CTA of at most 512 threads keeps
-// 128 registers a thread), then two pairs per lane (up to 16, then 32
-// warps), then four.
-__host__ __device__ inline int pairs_for_max_u(int max_u) {
+// The shape of a chain: the state pairs (blank, label) each lane holds (P)
+// and the lanes of each warp that shadow the neighbouring warp's edge pairs
+// (G), so that the warp runs G * P frames between two halo exchanges.  A
+// warp owns group_pairs(P, G) pairs and at most 32 warps run a chain.
+__host__ __device__ constexpr int group_pairs(int P, int G) { return (32 - G) * P; }
+// The shape for a target bound:
+//   one pair per lane, 8 shadow lanes, up to 16 warps (a chain CTA of at
+//     most 512 threads keeps 128 registers a thread);
+//   two pairs, 4 shadow lanes (8 frames an exchange), up to 16 warps;
+//   two pairs, 2 shadow lanes (4 frames), up to 32 warps (an 8-frame ring of
+//     32 warps would not fit shared memory);
+//   four pairs, 1 shadow lane.
+// (Measured: with one pair on the 8193-class workload 8 shadow lanes beat 4,
+// 2 and 16; with two pairs on the long-form workload 4 shadow lanes took the
+// forward from 0.910 to 0.853 ms against 2.)
+__host__ __device__ inline void chain_shape_for_max_u(int max_u, int& P, int& G) {
     const int pairs = max_u + 1;
-    if (pairs <= group_pairs(1) * 16) return 1;
-    if (pairs <= group_pairs(2) * 32) return 2;
-    return 4;
+    if (pairs <= group_pairs(1, 8) * 16) {
+        P = 1;
+        G = 8;
+    } else if (pairs <= group_pairs(2, 4) * 16) {
+        P = 2;
+        G = 4;
+    } else if (pairs <= group_pairs(2, 2) * 32) {
+        P = 2;
+        G = 2;
+    } else {
+        P = 4;
+        G = 1;
+    }
+}
+__host__ __device__ inline int pairs_for_max_u(int max_u) {
+    int P, G;
+    chain_shape_for_max_u(max_u, P, G);
+    return P;
 }
 
 __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_t max_U, int32_t D) {
@@ -126,10 +144,11 @@ __host__ __device__ inline Layout make_layout(int64_t T_total, int32_t B, int32_
     L.D = D;
     // a row holds 2 ints per state pair; a lane stores its P pairs as one
     // aligned vector, so the pitch is a multiple of 2P ints (and of 4)
-    const int P = pairs_for_max_u(max_U);
+    int P, G;
+    chain_shape_for_max_u(max_U, P, G);
     L.pitch = (int32_t)align_up((size_t)(2 * (max_U + 1)), (size_t)(2 * P > 4 ? 2 * P : 4));
     L.ecap = (max_U + 1) < D ? (max_U + 1) : D;
-    L.gpairs = group_pairs(P);
+    L.gpairs = group_pairs(P, G);
     {
         const int pairs = max_U + 1;
         const int nw = (pairs + L.gpairs - 1) / L.gpairs;

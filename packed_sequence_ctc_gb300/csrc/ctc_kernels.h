@@ -86,7 +86,7 @@ template <int DT>
 __global__ void lse_kernel(ChainArgs a);
 template <int DT>
 __global__ void emit_kernel(ChainArgs a);
-template <int P, int MAXT, bool CKPT>
+template <int P, int G, int MAXT, bool CKPT>
 __global__ void chain_kernel(ChainArgs a);
 __global__ void post_kernel(GradArgs a);
 template <int DT>
