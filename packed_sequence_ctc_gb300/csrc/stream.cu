@@ -403,11 +403,15 @@ __global__ void __launch_bounds__((32 + kTeamThreads) * kMaxTeams, 1) stream_ker
         {
             const uint32_t sq = smem_addr(sl) + 16u * (uint32_t)qa;
             uint4* gq = reinterpret_cast<uint4*>(gbase) + qa;
+            // streaming stores (evict first): the gradient is not read again
+            // here, and 1.3 GB pass through a 126 MB L2 (measured: the
+            // backward 0.2271 -> 0.2225 ms on the 8193-class workload)
             if (zero) {
-                for (int i = tt; i < nint; i += kTeamThreads) gq[i] = make_uint4(0u, 0u, 0u, 0u);
+                for (int i = tt; i < nint; i += kTeamThreads) __stcs(gq + i, make_uint4(0u, 0u, 0u, 0u));
             } else {
 #pragma unroll 4
-                for (int i = tt; i < nint; i += kTeamThreads) gq[i] = chunk_scaled<DT>(lds128(sq + 16u * (uint32_t)i), s, bias);
+                for (int i = tt; i < nint; i += kTeamThreads)
+                    __stcs(gq + i, chunk_scaled<DT>(lds128(sq + 16u * (uint32_t)i), s, bias));
             }
         }
         // the ragged chunks at the row's ends (and past the buffer's last whole chunk)
