@@ -13,15 +13,17 @@
 // frame, and grad[t, c] = scale * (exp(lp[t, c]) - sum_{s: l(s) = c} gamma_t(s))
 // with gamma_t(s) = alpha_t(s) beta_t(s) / Z.
 //
-// Arithmetic.  A probability is carried in extended range: a float64
-// mantissa m in [1, 2) and an int exponent e, value m * 2^e (zero: m = 0).
-// The recursions then take no exp or log per state and frame, which matters
-// on a part whose float64 rate is a small fraction of its float32 rate: a sum
-// aligns its terms to the largest exponent with exact power-of-two scales and
-// adds them, a product multiplies the mantissas and adds the exponents, and
-// each emission exp(lp[t, c]) is converted once, in a parallel gather.  Every
-// step rounds to float64 (a few ulps per frame), so the loss and gradient
-// keep about 13 significant digits over thousands of frames.
+// Arithmetic.  A probability is carried in extended range: a 62-bit integer
+// mantissa (its leading one at bit 61) and an int exponent (zero: m = 0).
+// The recursions then take no exp, log or float64 operation per state and
+// frame, which matters on a part whose float64 rate is a small fraction of
+// its integer and float32 rates: a sum shifts its terms to the largest
+// exponent and adds them, a product takes the high 62 bits of the mantissa
+// product and adds the exponents, and each emission exp(lp[t, c]) is
+// converted once, in a parallel gather.  Every step keeps 62 bits, so the
+// loss and gradient keep float64's digits over thousands of frames.  The
+// posteriors go to fixed point (units of 2^-62) for the class sums, which
+// are then exact integer sums.
 //
 // Kernels, in stream order.  Forward:
 //   prep    one CTA: utterance checks, target offsets, the losses of
