@@ -34,16 +34,19 @@
 //   forward  one CTA per sequence, a thread per destination state (or a
 //            few): alpha_{t+1}(s') is the sum over the state's incoming
 //            edges in list order.  The words holding frame t + 1's label
-//            values are copied ahead and converted to extended range by the
-//            threads that copied them during frame t; one barrier per frame.
-//            alpha_t is stored (8 bytes a state) for the backward.
+//            values are copied ahead and converted to extended range during
+//            frame t by label threads (warps of their own after the state
+//            threads when they fit the CTA), each converting the words it
+//            copied; one barrier per frame.  alpha_t is stored (8 bytes a
+//            state) for the backward.
 //   backward one CTA per sequence, a thread per source state: beta_t(s)
 //            over the state's outgoing edges in list order, each edge's
 //            occupancy into a double-buffered per-edge array at the edge's
 //            position in label order, then after the frame's barrier the
-//            class sums, each label's contiguous range in order; the dense
-//            rows are written by the CTC path's all-SM gradient stream from
-//            the rows' class sums.
+//            class sums, each label's contiguous range in order (short ones
+//            by the label threads, long ones by state warps); the dense rows
+//            are written by the CTC path's all-SM gradient stream from the
+//            rows' class sums.
 #include <cstdint>
 
 #include "ctc_common.cuh"
