@@ -30,6 +30,7 @@
 //           utterances without frames
 //   lse     (logits) one warp per row: the row's log-sum-exp
 //   emit    one warp per row: exp(lp[t, c]) of the row's labels and blank
+//           (Tang's table-driven exp in float64, see x_from_log)
 //   alpha   one CTA per utterance, a thread per state (or per few): the
 //           forward recursion, one barrier per frame; every alpha row is
 //           stored for the backward, and Z and the nll per utterance
@@ -188,15 +189,32 @@ __device__ __forceinline__ X64 x_of_double(double v, long long k) {
 // The mantissa of a nonzero extended value as a float64 in [1, 2).
 __device__ __forceinline__ double x_mantissa(X64 x) { return __ull2double_rn(x.m) * 0x1p-61; }
 
-// exp(x) in extended range: x = k ln2 + r with k = floor(x log2 e), then
-// exp(r) in [1, 2) up to rounding, taken by its bits.  -inf gives zero, and
-// so do NaN and +inf (the caller flags those).
-__device__ __forceinline__ X64 x_from_log(double x) {
-    if (!(x > -INFINITY) || !(x < INFINITY)) return x_zero();
-    const double k = floor(x * kLog2eD);
-    if (k < (double)kZeroE) return x_zero();
-    const double r = fma(-k, kLn2D, x);
-    return x_of_double(exp(r), (long long)k);
+// exp(x) in extended range by Tang's table-driven method (P. T. P. Tang,
+// ACM TOMS 15(2), 1989) in float64: n = round(x * 64 / ln2) by the
+// 1.5 * 2^52 rounding constant, r = x - n ln2/64 by two fused multiply-adds
+// (ln2/64 as a float64 and its remainder), |r| <= ln2/128; exp(r) - 1 by its
+// Taylor polynomial to r^5 (the next term is below 2^-53 of the result);
+// exp(x) = 2^(n >> 6) * T[n & 63] * (1 + p), T[j] = 2^(j/64) from a table the
+// caller fills.  About ten float64 operations, within about one unit in the
+// last place, the mantissa taken by its bits and the exponent kept apart (no
+// underflow).  -inf gives zero, and so do NaN and +inf (the caller flags
+// those).
+constexpr double kLn2o64D = 0.010830424696249145;     // ln 2 / 64, rounded
+constexpr double kLn2o64LoD = 3.623510646634843e-19;   // ln 2 / 64 minus the above
+constexpr double k64oLn2D = 92.332482616893656;
+__device__ __forceinline__ X64 x_from_log(double x, const double* T) {
+    if (!(x > -1.0e9) || !(x < INFINITY)) return x_zero();  // below 2^kZeroE (or NaN, +-inf)
+    if (x > 1.0e9) x = 1.0e9;                                // saturates (see x_of_double)
+    const double t = fma(x, k64oLn2D, 0x1.8p52);
+    const long long n = __double_as_longlong(t) - __double_as_longlong(0x1.8p52);
+    const double nd = t - 0x1.8p52;
+    const double r = fma(-nd, kLn2o64LoD, fma(-nd, kLn2o64D, x));
+    double q = fma(r, 1.0 / 120.0, 1.0 / 24.0);
+    q = fma(r, q, 1.0 / 6.0);
+    q = fma(r, q, 0.5);
+    const double p = fma(r * r, q, r);
+    const double tj = T[n & 63];
+    return x_of_double(fma(tj, p, tj), n >> 6);
 }
 
 // ln 2 / 64 in units of 2^-53: kLn2o64Hi + kLn2o64Lo / 2^11 (within 2^-12
@@ -437,6 +455,9 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_lse_kernel(F64Args a) {
 // and its blank (entry U).  A label outside [0, D) gets zero here; the
 // recursion rejects the utterance.
 __global__ void __launch_bounds__(kRowWarps * 32) f64_emit_kernel(F64Args a) {
+    __shared__ double s_exp[64];
+    fill_exp_table(s_exp);
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
     EmX* em = ws_at<EmX>(a.ws, a.L.off_em);
@@ -459,7 +480,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_emit_kernel(F64Args a) {
             if (c >= 0 && c < D) {
                 const double y = __ldg(x + c) - sh;
                 nan |= !(y < INFINITY);  // NaN or +inf: the utterance's loss is NaN
-                v = x_from_log(y);
+                v = x_from_log(y, s_exp);
             }
             *reinterpret_cast<ulonglong2*>(out + k) = make_ulonglong2(v.m, (unsigned long long)(long long)v.e);
         }
