@@ -117,7 +117,7 @@ struct ItemCtx {
 // warps of a multi-warp item exchange their edges.
 // CKPT: the checkpoint policy (store_rows > 1) is compiled as a variant of
 // its own, so that the default (every row or none) keeps the plain loop.
-template <int P, int G, int DIR, bool CKPT>
+template <int P, int G, int DIR, bool CKPT, bool STORE>
 __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
     using S = ChainShape<P, G>;
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
@@ -394,14 +394,14 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
             request((base + q + S::R - 1) & (S::R - 1), i0 + q + S::R - 1);
             if (CKPT) {
                 flush_ckpt(i0 + q - 1);
-            } else if (a.store_rows) {
+            } else if (STORE) {
                 flush_row(q);  // frame i0 + q - 1
             }
             step(el, eb);
         }
         renormalise();
         if (multi) exchange((i0 - 1) / S::F);
-        if (!CKPT && a.store_rows) write_rows(i0 - 1, S::F);
+        if (!CKPT && STORE) write_rows(i0 - 1, S::F);
     }
     // the last frames (fewer than F: no exchange needed)
 #pragma unroll 1
@@ -413,14 +413,14 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
         request((slot + S::R - 1) & (S::R - 1), i + S::R - 1);
         if (CKPT) {
             flush_ckpt(i - 1);
-        } else if (a.store_rows) {
+        } else if (STORE) {
             flush_row(i - i0);  // frame i - 1
         }
         step(el, eb);
     }
     if (CKPT) {
         flush_ckpt(T - 1);
-    } else if (a.store_rows) {
+    } else if (STORE) {
         flush_row(T - i0);  // frame T - 1 (T >= 1 for every queued item)
         write_rows(i0 - 1, T - i0 + 1);
     }
@@ -478,10 +478,18 @@ __device__ void run_chain(const ChainArgs& a, int b, const ItemCtx& c) {
 
 template <int P, int G, bool CKPT>
 __device__ __forceinline__ void run_item(const ChainArgs& a, int item, const ItemCtx& c) {
-    if (item & 1) {
-        run_chain<P, G, 1, CKPT>(a, item >> 1, c);
+    if (CKPT || a.store_rows) {
+        if (item & 1) {
+            run_chain<P, G, 1, CKPT, true>(a, item >> 1, c);
+        } else {
+            run_chain<P, G, 0, CKPT, true>(a, item >> 1, c);
+        }
     } else {
-        run_chain<P, G, 0, CKPT>(a, item >> 1, c);
+        if (item & 1) {
+            run_chain<P, G, 1, CKPT, false>(a, item >> 1, c);
+        } else {
+            run_chain<P, G, 0, CKPT, false>(a, item >> 1, c);
+        }
     }
 }
 
