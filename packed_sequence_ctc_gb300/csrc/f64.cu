@@ -9,9 +9,10 @@
 // and float16 only), and test_ctc_loss.py ``test_float64_takes_padded_path``
 // holds that path to 1e-10.  The recursion and gradient are the ones of
 // ctc_loss.py (``_alpha_kernel``, ``_beta_grad_kernel``): alpha over the
-// extended label sequence, beta recomputed in the backward from the last
-// frame, and grad[t, c] = scale * (exp(lp[t, c]) - sum_{s: l(s) = c} gamma_t(s))
-// with gamma_t(s) = alpha_t(s) beta_t(s) / Z.
+// extended label sequence, beta from the last frame (here in the forward
+// call, beside alpha, where the page recomputes it in the backward), and
+// grad[t, c] = scale * (exp(lp[t, c]) - sum_{s: l(s) = c} gamma_t(s)) with
+// gamma_t(s) = alpha_t(s) beta_t(s) / Z.
 //
 // Arithmetic.  A probability is carried in extended range: a 62-bit integer
 // mantissa (its leading one at bit 61) and an int exponent (zero: m = 0).
@@ -31,14 +32,17 @@
 //   lse     (logits) one warp per row: the row's log-sum-exp
 //   emit    one warp per row: exp(lp[t, c]) of the row's labels and blank
 //           (Tang's table-driven exp in float64, see x_from_log)
-//   alpha   one CTA per utterance, a thread per state (or per few): the
-//           forward recursion, one barrier per frame; every alpha row is
-//           stored for the backward, and Z and the nll per utterance
+//   chain   one CTA per utterance and recursion, a thread per state (or per
+//           few), one barrier per frame: the alpha recursion (every alpha
+//           row stored, Z and the nll per utterance) and, when the
+//           gradient's state is kept, the beta recursion at the same time on
+//           CTAs of its own (the label analysis, distinct classes in target
+//           order, then every beta row stored)
 //   reduce  one CTA: the reduced loss in a fixed summation order
 // Backward:
-//   beta    one CTA per utterance: the label analysis (distinct classes in
-//           target order), then the backward recursion from the last frame;
-//           per frame the posteriors and their sum per distinct class
+//   post    a small CTA per row at a time: the row's posteriors from the
+//           two stored rows, summed per distinct class (exact integer sums),
+//           as gradient entries
 //   grad    one warp per row: scale * exp(lp) for every class (a table-driven
 //           exp, see exp_table), then each class sum rewrites its element,
 //           scale * exp(lp) - scale * P
@@ -56,14 +60,10 @@ namespace {
 constexpr int kZeroE = -(1 << 30);  // exponent of zero; values below 2^kZeroE flush to zero
 constexpr int kRowWarps = 8;        // warps (rows) per CTA of the row kernels
 constexpr int kMaxChainThreads = 1024;
-// Frames of a recursion's per-state loads in flight through shared memory
-// (the next frames' emissions; backward also the stored alpha rows), RING - 1
-// ahead of the frame computed: 4 up to 1024 states a CTA (both kernels) and
-// up to 2048 (forward); larger CTAs load one frame ahead into registers
-// (their rings would not fit).
-__host__ __device__ constexpr int f64_ring(bool backward, int per) { return per == 1 || (!backward && per == 2) ? 4 : 0; }
-// The beta kernel double-buffers its per-frame values up to 4 states a thread.
-__host__ __device__ constexpr bool f64_beta_double_buffered(int per) { return per <= 4; }
+// Frames of a recursion's emissions in flight through shared memory, RING - 1
+// ahead of the frame computed: 4 up to 2048 states a CTA; larger CTAs load
+// one frame ahead into registers (their rings would not fit).
+__host__ __device__ constexpr int f64_ring(int per) { return per <= 2 ? 4 : 0; }
 
 // Extended-range value m * 2^(e - 61): m an integer with its leading one at
 // bit 61 (62 significant bits, carried on the integer pipes: this part's
@@ -88,8 +88,10 @@ struct F64Utt {
     int32_t labels_ok;  // every target id in [0, D) (cleared by the alpha recursion)
     int32_t has_nan;    // a label or blank log probability of the utterance is NaN
     int32_t nll_inf;    // no alignment: Z = 0
-    int32_t ncls;       // distinct classes of the target, the blank included (backward)
-    int32_t ze, pad0, pad1;
+    int32_t ncls;       // distinct classes of the target, the blank included (label analysis)
+    int32_t ze;
+    int32_t bfirst;     // first target position whose id is the blank, -1: none (label analysis)
+    int32_t pad1;
     double nll, zm;     // nll, and Z = zm * 2^ze
 };
 static_assert(sizeof(F64Utt) == 64, "utterance record is 64 bytes");
@@ -100,7 +102,8 @@ struct F64Layout {
     int32_t Ep;    // emission entries per row: max_U labels, then the blank
     int32_t Sp;    // stored alpha states per row: 2 max_U + 1, padded to even
     int32_t ecap;  // class sums a row can hold: min(max_U + 1, D)
-    size_t off_ctrl, off_utt, off_lse, off_em, loss_only_total, off_am, off_ae, off_cls, off_ent, total;
+    size_t off_ctrl, off_utt, off_lse, off_em, loss_only_total, off_am, off_ae, off_bm, off_bx, off_lrec, off_cls,
+        off_ent, total;
 };
 
 __host__ __device__ inline F64Layout f64_layout(int64_t T, int32_t B, int32_t max_U, int32_t D) {
@@ -121,6 +124,12 @@ __host__ __device__ inline F64Layout f64_layout(int64_t T, int32_t B, int32_t ma
     // what only the backward reads
     L.off_am = o;   o = align_up(o + sizeof(double) * (size_t)T * (size_t)L.Sp, 256);
     L.off_ae = o;   o = align_up(o + sizeof(int32_t) * (size_t)T * (size_t)L.Sp, 256);
+    // beta_t(s) before frame t's emission, every row (the beta recursion)
+    L.off_bm = o;   o = align_up(o + sizeof(double) * (size_t)T * (size_t)L.Sp, 256);
+    L.off_bx = o;   o = align_up(o + sizeof(int32_t) * (size_t)T * (size_t)L.Sp, 256);
+    // per target position: the rank of a first occurrence (-1 otherwise) and
+    // the next position with the same class (-1: none)
+    L.off_lrec = o; o = align_up(o + sizeof(int2) * (size_t)B * (size_t)L.Ep, 256);
     L.off_cls = o;  o = align_up(o + sizeof(int32_t) * (size_t)B * (size_t)L.Ep, 256);
     L.off_ent = o;  o = align_up(o + sizeof(double) * (size_t)T * (size_t)L.ecap, 256);
     L.total = o;
@@ -281,13 +290,7 @@ __device__ __forceinline__ X64 ld_em(const EmX* p) {
     return X64{v.x, (int)(long long)v.y};
 }
 
-// 4-, 8- and 16-byte async copies global -> shared.
-__device__ __forceinline__ void cp_async_n4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_n8(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
+// 16-byte async copy global -> shared.
 __device__ __forceinline__ void cp_async_n16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
@@ -494,11 +497,11 @@ __global__ void __launch_bounds__(kRowWarps * 32) f64_emit_kernel(F64Args a) {
 // next frame's reads.  The next frame's emissions load during the current
 // frame.
 template <int PER>
-__global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args a) {
-    constexpr int RING = f64_ring(false, PER);
+__device__ __forceinline__ void f64_alpha_chain(const F64Args& a, int b) {
+    constexpr int RING = f64_ring(PER);
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_bad;
-    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = blockDim.x;
     Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
     F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
     const F64Utt u = utt[b];
@@ -643,6 +646,187 @@ __global__ void __launch_bounds__(kMaxChainThreads, 1) f64_alpha_kernel(F64Args 
     }
 }
 
+// Backward recursion of one utterance from its last frame, run by the
+// forward call beside the alpha recursion (on CTAs of its own).  beta_t(s)
+// excludes frame t's emission; g_t(s) = beta_t(s) * exp(lp[t, l(s)]) is what
+// frame t - 1 reads:
+//   beta_{T-1}(s) = 1 for the last two states,
+//   beta_t(s) = g_{t+1}(s) + g_{t+1}(s + 1) + [l(s + 2) != l(s)] g_{t+1}(s + 2).
+// Every beta row is stored for the backward's posteriors; g is double
+// buffered in shared memory, one barrier per frame.  First the label
+// analysis the class sums use: first occurrences ranked in target order,
+// links to the next occurrence, labels equal to the blank joining its class
+// (in shared memory that the recursion reuses afterwards).
+template <int PER>
+__device__ __forceinline__ void f64_beta_chain(const F64Args& a, int b) {
+    constexpr int RING = f64_ring(PER);
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_warp[32];
+    __shared__ int s_bfirst, s_bad;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    const F64Utt u = utt[b];
+    if (!u.valid || u.T == 0) return;
+    const int U = u.U, S = 2 * U + 1, T = u.T, Ep = a.L.Ep, Sp = a.L.Sp;
+    const int cap = PER * nt;
+
+    // 1. label analysis
+    int* const lab = reinterpret_cast<int*>(smem);  // the target
+    int* const nxt = lab + U;                       // next position of the same class, -1: none
+    int* const rnk = nxt + U;                       // rank of a first occurrence, -1 otherwise
+    if (tid == 0) {
+        s_bfirst = -1;
+        s_bad = 0;
+    }
+    __syncthreads();
+    for (int j = tid; j < U; j += nt) {
+        const int c = a.targets[u.toff + j];
+        lab[j] = c;
+        if (c < 0 || c >= a.D) s_bad = 1;
+    }
+    __syncthreads();
+    if (s_bad) return;  // the alpha recursion reports it
+    int running = 0;
+    for (int j0 = 0; j0 < U; j0 += nt) {
+        const int j = j0 + tid;
+        bool first = false;
+        if (j < U) {
+            const int c = lab[j];
+            first = true;
+            for (int k = 0; k < j; ++k)
+                if (lab[k] == c) {
+                    first = false;
+                    break;
+                }
+            int nx = -1;
+            for (int k = j + 1; k < U; ++k)
+                if (lab[k] == c) {
+                    nx = k;
+                    break;
+                }
+            nxt[j] = nx;
+            if (c == a.blank) {
+                if (first) s_bfirst = j;
+                first = false;
+            }
+        }
+        int total;
+        const int pre = f64_block_scan(first ? 1 : 0, s_warp, &total);
+        if (j < U) rnk[j] = first ? running + pre : -1;
+        running += total;
+    }
+    const int ncls = running + 1;
+    int32_t* cls = ws_at<int32_t>(a.ws, a.L.off_cls) + (size_t)b * Ep;
+    int2* lrec = ws_at<int2>(a.ws, a.L.off_lrec) + (size_t)b * Ep;
+    for (int j = tid; j < U; j += nt) {
+        if (rnk[j] >= 0) cls[rnk[j]] = lab[j];
+        lrec[j] = make_int2(rnk[j], nxt[j]);
+    }
+    if (tid == 0) {
+        cls[ncls - 1] = a.blank;
+        utt[b].ncls = ncls;
+        utt[b].bfirst = s_bfirst;
+    }
+    int eidx[PER];
+    bool skip2[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int s = tid + k * nt;
+        eidx[k] = (s & 1) ? (s >> 1) : U;
+        skip2[k] = (s & 1) && s + 2 < S && lab[(s + 2) >> 1] != lab[s >> 1];
+    }
+    __syncthreads();  // the label arrays are read: their shared memory goes to the recursion
+
+    // 2. the recursion
+    unsigned long long* const gbm = reinterpret_cast<unsigned long long*>(smem);  // two buffers of cap mantissas
+    int* const gbe = reinterpret_cast<int*>(gbm + 2 * cap);                         // two buffers of cap exponents
+    EmX* const ring = reinterpret_cast<EmX*>(gbe + 2 * cap);  // RING frames of the states' emissions
+    const EmX* em = ws_at<EmX>(a.ws, a.L.off_em) + (size_t)u.start * Ep;
+    unsigned long long* bm = ws_at<unsigned long long>(a.ws, a.L.off_bm) + (size_t)u.start * Sp;
+    int32_t* bx = ws_at<int32_t>(a.ws, a.L.off_bx) + (size_t)u.start * Sp;
+    // frame f's emissions into ring slot f % RING (each thread copies and
+    // later reads its own states' entries)
+    auto issue = [&](int f) {
+        if (f >= 0) {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                if (s < S) cp_async_n16(ring + (f % (RING > 0 ? RING : 1)) * cap + s, em + (size_t)f * Ep + eidx[k]);
+            }
+        }
+        cp_async_commit();
+    };
+    X64 nx[PER];  // without a ring: the next frame's emissions, loaded a frame ahead
+    if constexpr (RING > 0) {
+        for (int j = 0; j < RING - 1; ++j) issue(T - 1 - j);
+    } else {
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            nx[k] = s < S ? ld_em(em + (size_t)(T - 1) * Ep + eidx[k]) : x_zero();
+        }
+    }
+    int p = 0;  // g of frame t + 1 is in buffer p
+    for (int t = T - 1; t >= 0; --t) {
+        X64 e_t[PER];
+        if constexpr (RING > 0) {
+            issue(t - (RING - 1));
+            cp_async_wait<RING - 1>();  // frame t's entries have landed
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int s = tid + k * nt;
+                e_t[k] = s < S ? ld_em(ring + (t % RING) * cap + s) : x_zero();
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                e_t[k] = nx[k];
+                const int s = tid + k * nt;
+                if (s < S && t > 0) nx[k] = ld_em(em + (size_t)(t - 1) * Ep + eidx[k]);
+            }
+        }
+        const unsigned long long* gmp = gbm + p * cap;
+        const int* gep = gbe + p * cap;
+        unsigned long long* gmq = gbm + (p ^ 1) * cap;
+        int* geq = gbe + (p ^ 1) * cap;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int s = tid + k * nt;
+            if (s < S) {
+                X64 be;
+                if (t == T - 1) {
+                    be = s >= S - 2 ? X64{kXOne, 0} : x_zero();
+                } else {
+                    const X64 v0{gmp[s], gep[s]};
+                    const X64 v1 = s + 1 < S ? X64{gmp[s + 1], gep[s + 1]} : x_zero();
+                    const X64 v2 = skip2[k] ? X64{gmp[s + 2], gep[s + 2]} : x_zero();
+                    be = x_add3(v0, v1, v2);
+                }
+                const X64 g = x_mul(be, e_t[k]);
+                gmq[s] = g.m;
+                geq[s] = g.e;
+                bm[(size_t)t * Sp + s] = be.m;
+                bx[(size_t)t * Sp + s] = be.e;
+            }
+        }
+        __syncthreads();
+        p ^= 1;
+    }
+    if (RING > 0) cp_async_wait<0>();
+}
+
+// The recursions of the forward call: CTA b < B runs utterance b's alpha
+// recursion; with the gradient's state kept, CTA B + b runs its beta
+// recursion at the same time.
+template <int PER>
+__global__ void __launch_bounds__(kMaxChainThreads, 1) f64_chain_kernel(F64Args a) {
+    if ((int)blockIdx.x < a.L.B) {
+        f64_alpha_chain<PER>(a, (int)blockIdx.x);
+    } else {
+        f64_beta_chain<PER>(a, (int)blockIdx.x - a.L.B);
+    }
+}
+
 // The reduced loss (sum, mean, mean_batch, mean_volume) in a fixed order.
 __global__ void __launch_bounds__(256) f64_reduce_kernel(F64Args a) {
     __shared__ double s_red[8];
@@ -704,289 +888,121 @@ __device__ __forceinline__ long long warp_sum_ll(long long v) {
     return v;
 }
 
-// Backward recursion of one utterance from its last frame, with the
-// posteriors and their class sums.  beta_t(s) excludes frame t's emission,
-// g_t(s) = beta_t(s) * exp(lp[t, l(s)]) is what frame t - 1 reads:
-//   beta_{T-1}(s) = 1 for the last two states,
-//   beta_t(s) = g_{t+1}(s) + g_{t+1}(s + 1) + [l(s + 2) != l(s)] g_{t+1}(s + 2).
-// Two barriers per frame: after the reads of g (A), after the writes of g,
-// the label posteriors and the blank partial sums (B); the class sums of the
-// frame are read between B and the next A.
-template <int PER>
-__global__ void __launch_bounds__(kMaxChainThreads, 1) f64_beta_kernel(F64Args a) {
-    constexpr int RING = f64_ring(true, PER);
-    constexpr int RS = RING > 0 ? RING : 1;
-    // DB: g and the posteriors double buffered, one barrier a frame (up to
-    // 4096 states a CTA); otherwise one buffer and two barriers
-    constexpr bool DB = f64_beta_double_buffered(PER);
-    constexpr int NB = DB ? 2 : 1;
+// Posteriors and class sums of each row, from the rows both recursions
+// stored: gamma_t(s) = alpha_t(s) beta_t(s) / Z in fixed point (post_fixed3),
+// summed per distinct class in exact integer arithmetic (so in any order and
+// the same as any other order), each sum written as its gradient entry
+// -scale * P: a first occurrence's thread sums its class's label states along
+// the next-occurrence links; the blank class is the CTA's sum of the blank
+// states plus the labels equal to the blank.  One CTA per row at a time, over
+// a contiguous range of rows (mostly of one utterance, whose links are loaded
+// once).  Rows without class sums (outside every utterance, a malformed or
+// unaligned one, scale 0) are left to the dense pass.  Small CTAs, so that an
+// SM holds many rows in flight: each row's loads wait on DRAM, then its
+// class sums on two barriers (measured on the 8193-class workload: 226 us
+// with 256 threads a CTA).
+constexpr int kPostThreads = 64;
+constexpr int kPostUnroll = 4;  // states a thread loads at once
+__global__ void __launch_bounds__(kPostThreads) f64_post_kernel(F64Args a) {
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ long long s_wsum[kMaxChainThreads / 32];
-    __shared__ int s_warp[32];
-    __shared__ int s_bfirst;
-    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
-    const int nw = nt >> 5;
-    Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
-    F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
-    const F64Utt u = utt[b];
-    if (ctrl->grad_ready == 0 || !u.valid || !u.labels_ok || u.T == 0) return;
-    const double scale = f64_scale(a, u, b, ctrl->tl_total);
-    if (scale == 0.0) return;  // the row stream writes zeros without class sums
-    const int U = u.U, S = 2 * U + 1, T = u.T, Ep = a.L.Ep, Sp = a.L.Sp;
-    const int cap = PER * nt;
-    // RING frames of the states' emissions and stored alpha rows, then the
-    // per-frame buffers
-    EmX* const rx = reinterpret_cast<EmX*>(smem);
-    unsigned long long* const rm = reinterpret_cast<unsigned long long*>(rx + RING * cap);
-    int* const re = reinterpret_cast<int*>(rm + RING * cap);
-    const int Uu = U > 0 ? U : 1;
-    unsigned long long* gm = reinterpret_cast<unsigned long long*>(re + RING * cap);  // g, mantissas (NB of cap)
-    // posteriors in fixed point (post_fixed)
-    long long* gam = reinterpret_cast<long long*>(gm + NB * cap);  // label states (NB of Uu)
-    long long* gb = gam + NB * Uu;                                 // blank states (two of U + 1, DB)
-    int* ge = reinterpret_cast<int*>(gb + (DB ? 2 * (U + 1) : 0));  // g, exponents (NB of cap)
-    int* lab = ge + NB * cap;                                 // the target
-    int* nxt = lab + U;                                       // next position of the same class, -1: none
-    int* rnk = nxt + U;                                       // rank of a first occurrence, -1 otherwise
-
-    // 1. label analysis: first occurrences ranked in target order, links to
-    //    the next occurrence; labels equal to the blank join its class
-    if (tid == 0) s_bfirst = -1;
-    for (int j = tid; j < U; j += nt) lab[j] = a.targets[u.toff + j];
-    __syncthreads();
-    int running = 0;
-    for (int j0 = 0; j0 < U; j0 += nt) {
-        const int j = j0 + tid;
-        bool first = false;
-        if (j < U) {
-            const int c = lab[j];
-            first = true;
-            for (int k = 0; k < j; ++k)
-                if (lab[k] == c) {
-                    first = false;
-                    break;
-                }
-            int nx = -1;
-            for (int k = j + 1; k < U; ++k)
-                if (lab[k] == c) {
-                    nx = k;
-                    break;
-                }
-            nxt[j] = nx;
-            if (c == a.blank) {
-                if (first) s_bfirst = j;
-                first = false;
-            }
-        }
-        int total;
-        const int pre = f64_block_scan(first ? 1 : 0, s_warp, &total);
-        if (j < U) rnk[j] = first ? running + pre : -1;
-        running += total;
-    }
-    const int ncls = running + 1;
-    int32_t* cls = ws_at<int32_t>(a.ws, a.L.off_cls) + (size_t)b * Ep;
-    for (int j = tid; j < U; j += nt)
-        if (rnk[j] >= 0) cls[rnk[j]] = lab[j];
-    if (tid == 0) {
-        cls[ncls - 1] = a.blank;
-        utt[b].ncls = ncls;
-    }
-    __syncthreads();
-    const int bfirst = s_bfirst;
-
-    // 2. the recursion
-    const EmX* em = ws_at<EmX>(a.ws, a.L.off_em) + (size_t)u.start * Ep;
-    const unsigned long long* am = ws_at<unsigned long long>(a.ws, a.L.off_am) + (size_t)u.start * Sp;
-    const int32_t* ae = ws_at<int32_t>(a.ws, a.L.off_ae) + (size_t)u.start * Sp;
-    double* ent = ws_at<double>(a.ws, a.L.off_ent) + (size_t)u.start * a.L.ecap;
-    const X64 izx = x_of_double(1.0 / u.zm, -(long long)u.ze);  // 1 / Z
-    const bool nan_utt = u.has_nan != 0;
+    const int Uc = a.L.max_U > 0 ? a.L.max_U : 1;
+    long long* const gam = reinterpret_cast<long long*>(smem);  // label-state posteriors of the row
+    int2* const lr = reinterpret_cast<int2*>(gam + Uc);         // the utterance's (rank, next) links
+    __shared__ long long s_wsum[kPostThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x, nw = nt >> 5;
+    const Control* ctrl = ws_at<Control>(a.ws, a.L.off_ctrl);
+    const F64Utt* utt = ws_at<F64Utt>(a.ws, a.L.off_utt);
+    if (ctrl->grad_ready == 0) return;  // the dense pass reports it
+    const int tl_total = ctrl->tl_total;
+    const int64_t T_total = a.L.T_total;
+    const int64_t per = (T_total + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = (int64_t)blockIdx.x * per;
+    const int64_t r1 = r0 + per < T_total ? r0 + per : T_total;
+    const int Sp = a.L.Sp;
+    const unsigned long long* am_all = ws_at<unsigned long long>(a.ws, a.L.off_am);
+    const int32_t* ae_all = ws_at<int32_t>(a.ws, a.L.off_ae);
+    const unsigned long long* bm_all = ws_at<unsigned long long>(a.ws, a.L.off_bm);
+    const int32_t* bx_all = ws_at<int32_t>(a.ws, a.L.off_bx);
+    double* ent = ws_at<double>(a.ws, a.L.off_ent);
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
-    int eidx[PER];
-    bool skip2[PER];
+    // the utterance whose record, scale, 1 / Z and links are held (rows of a
+    // CTA's range mostly belong to one)
+    int cur = -1;
+    F64Utt u{};
+    double scale = 0.0;
+    X64 izx = x_zero();
+    for (int64_t row = r0; row < r1; ++row) {
+        const int b = f64_utterance_of_row(a.cu, a.L.B, row);
+        if (b < 0) continue;
+        if (b != cur) {
+            __syncthreads();  // every read of the previous links is done
+            u = utt[b];
+            cur = b;
+            if (!u.valid || !u.labels_ok) continue;
+            scale = f64_scale(a, u, b, tl_total);
+            izx = x_of_double(1.0 / u.zm, -(long long)u.ze);  // 1 / Z
+            const int2* lg = ws_at<int2>(a.ws, a.L.off_lrec) + (size_t)b * a.L.Ep;
+            for (int j = tid; j < u.U; j += nt) lr[j] = lg[j];
+        }
+        const int64_t t = row - u.start;
+        if (!u.valid || !u.labels_ok || t < 0 || t >= u.T || scale == 0.0) continue;
+        const int U = u.U, S = 2 * U + 1;
+        const bool nan_utt = u.has_nan != 0;
+        const unsigned long long* am = am_all + row * Sp;
+        const int32_t* ae = ae_all + row * Sp;
+        const unsigned long long* bm = bm_all + row * Sp;
+        const int32_t* bx = bx_all + row * Sp;
+        long long bpart = 0;
+        // the posterior alpha * beta / Z (at most 1) in fixed point,
+        // kPostUnroll states a thread at a time (their loads in flight
+        // together); NaN entries: see entry
+        for (int s0 = tid; s0 < S; s0 += kPostUnroll * nt) {
+            X64 av[kPostUnroll], bv[kPostUnroll];
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-        const int s = tid + k * nt;
-        eidx[k] = (s & 1) ? (s >> 1) : U;
-        skip2[k] = (s & 1) && s + 2 < S && lab[(s + 2) >> 1] != lab[s >> 1];
-    }
-    // frame f's emissions and stored alpha values of the thread's states
-    // into ring slot f % RING (each thread copies and later reads its own)
-    auto issue = [&](int f) {
-        if (f >= 0) {
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int s = tid + k * nt;
+            for (int q = 0; q < kPostUnroll; ++q) {
+                const int s = s0 + q * nt;
+                av[q] = x_zero();
+                bv[q] = x_zero();
                 if (s < S) {
-                    const int q = (f % RS) * cap + s;
-                    cp_async_n16(rx + q, em + (size_t)f * Ep + eidx[k]);
-                    cp_async_n8(rm + q, am + (size_t)f * Sp + s);
-                    cp_async_n4(re + q, ae + (size_t)f * Sp + s);
+                    av[q] = X64{__ldg(am + s), __ldg(ae + s)};
+                    bv[q] = X64{__ldg(bm + s), __ldg(bx + s)};
                 }
             }
-        }
-        cp_async_commit();
-    };
-    X64 al[PER], et[PER];
-    if constexpr (RING > 0) {
-        for (int j = 0; j < RING - 1; ++j) issue(T - 1 - j);
-    } else {
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int s = tid + k * nt;
-            al[k] = s < S ? X64{am[(size_t)(T - 1) * Sp + s], ae[(size_t)(T - 1) * Sp + s]} : x_zero();
-            et[k] = s < S ? ld_em(em + (size_t)(T - 1) * Ep + eidx[k]) : x_zero();
-        }
-    }
-    // a class sum P (fixed point) as its gradient entry -scale * P
-    const double nscale = -scale * 0x1p-62;
-    auto entry = [&](long long P) { return nan_utt ? qnan : nscale * __ll2double_rn(P); };
-    // the class sums of frame tt from its label-state posteriors gamr and
-    // (DB) blank-state posteriors gbr, exact integer sums: a first
-    // occurrence's thread sums its class's positions; the last warp (the
-    // fewest states) sums the blank class, lane l taking blank states l,
-    // l + 32, ..., then a shuffle tree, then the labels equal to the blank
-    auto class_sums = [&](int tt, const long long* gamr, const long long* gbr) {
-        double* er = ent + (size_t)tt * a.L.ecap;
-        for (int j = tid; j < U; j += nt) {
-            const int r = rnk[j];
-            if (r < 0) continue;
-            long long P = gamr[j];
-            for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gamr[jj];
-            er[r] = entry(P);
-        }
-        if (warp == nw - 1) {
-            long long P = 0;
-            for (int i = lane; i <= U; i += 32) P += gbr[i];
-            P = warp_sum_ll(P);
-            if (lane == 0) {
-                for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gamr[jj];
-                er[ncls - 1] = entry(P);
-            }
-        }
-    };
-    int p = 0;  // DB: g and the posteriors of frame t + 1 are in buffer p
-    for (int t = T - 1; t >= 0; --t) {
-        X64 gn[PER];
-        long long gamma[PER];  // posteriors in fixed point
-        X64 al_n[PER], et_n[PER];
-        if constexpr (RING > 0) {
-            issue(t - (RING - 1));
-            cp_async_wait<RING - 1>();  // frame t's values have landed
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int s = tid + k * nt;
-                const int q = (t % RS) * cap + s;
-                al[k] = s < S ? X64{rm[q], re[q]} : x_zero();
-                et[k] = s < S ? ld_em(rx + q) : x_zero();
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int s = tid + k * nt;
-                al_n[k] = x_zero();
-                et_n[k] = x_zero();
-                if (s < S && t > 0) {
-                    al_n[k] = X64{am[(size_t)(t - 1) * Sp + s], ae[(size_t)(t - 1) * Sp + s]};
-                    et_n[k] = ld_em(em + (size_t)(t - 1) * Ep + eidx[k]);
-                }
-            }
-        }
-        const unsigned long long* gmp = gm + (DB ? p * cap : 0);  // g of frame t + 1
-        const int* gep = ge + (DB ? p * cap : 0);
-        if constexpr (DB) {
-            if (t + 1 < T) class_sums(t + 1, gam + p * Uu, gb + p * (U + 1));
-        }
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int s = tid + k * nt;
-            gn[k] = x_zero();
-            gamma[k] = 0;
-            if (s < S) {
-                X64 be;
-                if (t == T - 1) {
-                    be = s >= S - 2 ? X64{kXOne, 0} : x_zero();
-                } else {
-                    const X64 v0{gmp[s], gep[s]};
-                    const X64 v1 = s + 1 < S ? X64{gmp[s + 1], gep[s + 1]} : x_zero();
-                    const X64 v2 = skip2[k] ? X64{gmp[s + 2], gep[s + 2]} : x_zero();
-                    be = x_add3(v0, v1, v2);
-                }
-                gn[k] = x_mul(be, et[k]);
-                // the posterior alpha * beta / Z (at most 1) in fixed point
-                gamma[k] = nan_utt ? 0 : post_fixed3(al[k], be, izx);  // NaN entries: see entry
-            }
-        }
-        if constexpr (DB) {
-            // frame t's values into the other buffers; one barrier
-            unsigned long long* gmq = gm + (p ^ 1) * cap;
-            int* geq = ge + (p ^ 1) * cap;
-            long long* gamq = gam + (p ^ 1) * Uu;
-            long long* gbq = gb + (p ^ 1) * (U + 1);
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int s = tid + k * nt;
+            for (int q = 0; q < kPostUnroll; ++q) {
+                const int s = s0 + q * nt;
                 if (s < S) {
-                    gmq[s] = gn[k].m;
-                    geq[s] = gn[k].e;
-                    if (s & 1)
-                        gamq[s >> 1] = gamma[k];
-                    else
-                        gbq[s >> 1] = gamma[k];
-                }
-            }
-            __syncthreads();
-            p ^= 1;
-        } else {
-            __syncthreads();  // A
-            long long bpart = 0;
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int s = tid + k * nt;
-                if (s < S) {
-                    gm[s] = gn[k].m;
-                    ge[s] = gn[k].e;
+                    const long long g = nan_utt ? 0 : post_fixed3(av[q], bv[q], izx);
                     if (s & 1) {
-                        gam[s >> 1] = gamma[k];
+                        gam[s >> 1] = g;
                     } else {
-                        bpart += gamma[k];
+                        bpart += g;
                     }
                 }
-                if (RING == 0) {
-                    al[k] = al_n[k];
-                    et[k] = et_n[k];
-                }
-            }
-            bpart = warp_sum_ll(bpart);
-            if (lane == 0) s_wsum[warp] = bpart;
-            __syncthreads();  // B
-            double* er = ent + (size_t)t * a.L.ecap;
-            for (int j = tid; j < U; j += nt) {
-                const int r = rnk[j];
-                if (r < 0) continue;
-                long long P = gam[j];
-                for (int jj = nxt[j]; jj >= 0; jj = nxt[jj]) P += gam[jj];
-                er[r] = entry(P);
-            }
-            if (tid == 0) {
-                long long P = 0;
-                for (int w = 0; w < nw; ++w) P += s_wsum[w];
-                for (int jj = bfirst; jj >= 0; jj = nxt[jj]) P += gam[jj];
-                er[ncls - 1] = entry(P);
             }
         }
-        if constexpr (DB && RING == 0) {
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                al[k] = al_n[k];
-                et[k] = et_n[k];
-            }
+        bpart = warp_sum_ll(bpart);
+        if (lane == 0) s_wsum[warp] = bpart;
+        __syncthreads();
+        // a class sum P (fixed point) as its gradient entry -scale * P
+        const double nscale = -scale * 0x1p-62;
+        auto entry = [&](long long P) { return nan_utt ? qnan : nscale * __ll2double_rn(P); };
+        double* er = ent + row * a.L.ecap;
+        for (int j = tid; j < U; j += nt) {
+            const int r = lr[j].x;
+            if (r < 0) continue;
+            long long P = gam[j];
+            for (int jj = lr[j].y; jj >= 0; jj = lr[jj].y) P += gam[jj];
+            er[r] = entry(P);
         }
+        if (tid == 0) {
+            long long P = 0;
+            for (int w = 0; w < nw; ++w) P += s_wsum[w];
+            for (int jj = u.bfirst; jj >= 0; jj = lr[jj].y) P += gam[jj];
+            er[u.ncls - 1] = entry(P);
+        }
+        __syncthreads();  // gam and s_wsum are free for the next row
     }
-    if constexpr (DB) {
-        if (T > 0) class_sums(0, gam + p * Uu, gb + p * (U + 1));
-    }
-    if (RING > 0) cp_async_wait<0>();
 }
 
 // scale * exp(x[c] - sh) for the lane's elements c of a row: with FOLDED the
@@ -1160,6 +1176,28 @@ cudaError_t launch_rows(K kernel, int64_t rows, cudaStream_t s, const F64Args& a
     return cudaGetLastError();
 }
 
+// The posterior / class-sum kernel: a grid of the SMs times the CTAs an SM
+// holds, each over a contiguous range of rows.
+cudaError_t launch_post(int64_t rows, int32_t max_U, cudaStream_t s, const F64Args& a) {
+    if (rows <= 0) return cudaSuccess;
+    const size_t smem = (size_t)(max_U > 0 ? max_U : 1) * (sizeof(long long) + sizeof(int2));
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(f64_post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+        return e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f64_post_kernel, kPostThreads, smem)) !=
+        cudaSuccess)
+        return e;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = (long long)sms * per_sm;
+    if (rows < grid) grid = rows;
+    f64_post_kernel<<<(unsigned)grid, kPostThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace ctcp {
@@ -1199,13 +1237,19 @@ ctc_packed_status ctc_packed_forward_f64(const double* log_probs, int64_t T_tota
         int per = 1, nt = 32;
         chain_shape(max_target_len, per, nt);
         const size_t cap = (size_t)per * nt;
-        const size_t smem = 2 * cap * (sizeof(double) + sizeof(int)) + (size_t)f64_ring(false, per) * cap * sizeof(EmX);
+        // both recursions: two buffers of state values and the emission ring;
+        // the beta CTAs first hold their label analysis in the same memory
+        size_t smem = 2 * cap * (sizeof(double) + sizeof(int)) + (size_t)f64_ring(per) * cap * sizeof(EmX);
+        const size_t labels = 3 * sizeof(int) * (size_t)max_target_len;
+        if (a.need_grad && labels > smem) smem = labels;
+        // with the gradient's state kept, the beta recursions run beside the alpha ones
+        const unsigned grid = (unsigned)B * (a.need_grad ? 2u : 1u);
         cudaError_t e;
         switch (per) {
-            case 1: e = launch_chain_kernel(f64_alpha_kernel<1>, (unsigned)B, nt, smem, stream, a); break;
-            case 2: e = launch_chain_kernel(f64_alpha_kernel<2>, (unsigned)B, nt, smem, stream, a); break;
-            case 4: e = launch_chain_kernel(f64_alpha_kernel<4>, (unsigned)B, nt, smem, stream, a); break;
-            default: e = launch_chain_kernel(f64_alpha_kernel<8>, (unsigned)B, nt, smem, stream, a); break;
+            case 1: e = launch_chain_kernel(f64_chain_kernel<1>, grid, nt, smem, stream, a); break;
+            case 2: e = launch_chain_kernel(f64_chain_kernel<2>, grid, nt, smem, stream, a); break;
+            case 4: e = launch_chain_kernel(f64_chain_kernel<4>, grid, nt, smem, stream, a); break;
+            default: e = launch_chain_kernel(f64_chain_kernel<8>, grid, nt, smem, stream, a); break;
         }
         if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
         if (reduction != CTC_PACKED_NONE) {
@@ -1238,24 +1282,7 @@ ctc_packed_status ctc_packed_backward_f64(const double* log_probs, int64_t T_tot
                          blank, zero_infinity, (int)reduction, workspace);
     a.grad = grad_log_probs;
     a.grad_loss = grad_loss;
-    if (B > 0) {
-        int per = 1, nt = 32;
-        chain_shape(max_target_len, per, nt);
-        const int U = max_target_len > 0 ? max_target_len : 1;
-        const size_t cap = (size_t)per * nt;
-        const size_t nb = f64_beta_double_buffered(per) ? 2 : 1;
-        const size_t smem = (size_t)f64_ring(true, per) * cap * (sizeof(EmX) + sizeof(double) + sizeof(int)) +
-                            nb * cap * (sizeof(double) + sizeof(int)) + nb * sizeof(double) * (size_t)U +
-                            (nb == 2 ? 2 * sizeof(double) * ((size_t)U + 1) : 0) + 3 * sizeof(int) * (size_t)U;
-        cudaError_t e;
-        switch (per) {
-            case 1: e = launch_chain_kernel(f64_beta_kernel<1>, (unsigned)B, nt, smem, stream, a); break;
-            case 2: e = launch_chain_kernel(f64_beta_kernel<2>, (unsigned)B, nt, smem, stream, a); break;
-            case 4: e = launch_chain_kernel(f64_beta_kernel<4>, (unsigned)B, nt, smem, stream, a); break;
-            default: e = launch_chain_kernel(f64_beta_kernel<8>, (unsigned)B, nt, smem, stream, a); break;
-        }
-        if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
-    }
+    if (B > 0 && launch_post(T_total, max_target_len, stream, a) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     if (launch_rows(f64_grad_kernel, T_total, stream, a) != cudaSuccess) return CTC_PACKED_ERR_CUDA;
     return CTC_PACKED_OK;
 }
