@@ -647,7 +647,7 @@ def run_fsa(args):
         "metric": METRIC, "value": round(batch.frames / (ms / 1e3), 1), "unit": "frames/s", "n_gpus": 1,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
-        "roofline": {"bound": "hbm", "kernel": "fsa_backward_kernel+grad_kernel (the FSA backward call)",
+        "roofline": {"bound": "hbm", "kernel": "fsa_post_kernel+grad_kernel (the FSA backward call)",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": None,
                      "peak_kind": f"{peak_kind} copy bandwidth (burst)", "algorithmic_bytes_per_launch": dense,

@@ -341,20 +341,25 @@ ctc_packed_status ctc_packed_forward_noalloc(const void* log_probs, ctc_packed_d
  * mantissas with integer exponents (no underflow at any length); every sum
  * runs in a fixed order (each sequence's edges are sorted once per forward
  * into per-state and per-label lists), so results are bitwise reproducible.
- * max_states and max_labels together bound a recursion's shared memory:
- * about 52 bytes a state and 44 a label (36 and 36 above 2048 states) must
- * fit in 224 KB, else CTC_PACKED_ERR_UNSUPPORTED (the workspace size is 0).
+ * max_states and max_labels together bound the kernels' shared memory: a
+ * recursion's per-frame buffers (about 20 bytes a state and 36 a label; 28 a
+ * label above 2048 states) and the backward's two stages of a row (32 bytes
+ * a state and 28 a label) must each fit in 224 KB, else
+ * CTC_PACKED_ERR_UNSUPPORTED (the workspace size is 0).
  *
  * All pointers are device memory; log_probs is 4-byte aligned for every
  * dtype.  Errors the host can see return before
  * anything is enqueued; malformed FSA data or lengths set the status word
  * (ctc_packed_read_status works on this workspace) and a NaN loss.  The
  * workspace holds the status word, each sequence's log-sum, its sorted edge
- * lists, every frame's forward values and, after the backward, each row's
- * class sums; it is sized by ctc_packed_fsa_workspace_size with the same
- * num_states and num_edges as the calls.  Pass it unchanged from the forward
- * to the backward.  The backward writes the dense gradient rows with the CTC
- * path's all-SM gradient stream.
+ * lists, every frame's forward and backward values and label values (the
+ * forward runs both recursions of a sequence at the same time) and, after
+ * the backward, each row's class sums; it is sized by
+ * ctc_packed_fsa_workspace_size with the same num_states and num_edges as
+ * the calls.  Pass it unchanged from the forward to the backward.  The
+ * backward forms each row's edge occupancies and class sums from those
+ * values, then writes the dense gradient rows with the CTC path's all-SM
+ * gradient stream.
  */
 size_t ctc_packed_fsa_workspace_size(int64_t T_total, int32_t B, int32_t num_states, int32_t num_edges,
                                      int32_t max_states, int32_t max_labels, int32_t D);

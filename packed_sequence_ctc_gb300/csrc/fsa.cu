@@ -31,22 +31,25 @@
 //            source and by label, as per-state and per-label lists; the
 //            sequence's distinct labels (at most max_labels) in increasing
 //            order, and each edge's slot among them.
-//   forward  one CTA per sequence, a thread per destination state (or a
-//            few): alpha_{t+1}(s') is the sum over the state's incoming
-//            edges in list order.  The words holding frame t + 1's label
+//   chain    (the forward call) 2B CTAs: CTA b runs sequence b's forward
+//            recursion, CTA B + b its backward recursion at the same time.
+//            A thread per state (or a few): alpha_{t+1}(s') is the sum over
+//            the state's incoming edges in list order, beta_t(s) over its
+//            outgoing edges.  The words holding the next frame's label
 //            values are copied ahead and converted to extended range during
-//            frame t by label threads (warps of their own after the state
+//            the frame by label threads (warps of their own after the state
 //            threads when they fit the CTA), each converting the words it
-//            copied; one barrier per frame.  alpha_t is stored (8 bytes a
-//            state) for the backward.
-//   backward one CTA per sequence, a thread per source state: beta_t(s)
-//            over the state's outgoing edges in list order, each edge's
-//            occupancy into a double-buffered per-edge array at the edge's
-//            position in label order, then after the frame's barrier the
-//            class sums, each label's contiguous range in order (short ones
-//            by the label threads, long ones by state warps); the dense rows
-//            are written by the CTC path's all-SM gradient stream from the
-//            rows' class sums.
+//            copied; one barrier per frame.  Every alpha_t and beta_t row is
+//            stored (8 bytes a state), and the backward recursion also keeps
+//            each frame's label values.
+//   post     (the backward call) a CTA per row at a time over a contiguous
+//            range of rows: the row's alpha_t, beta_{t+1} and label values
+//            copied into shared memory (the next row's copies in flight
+//            meanwhile), then each label's class sum over its contiguous
+//            range of edges in label order, each occupancy formed as it is
+//            summed (short lists by a thread, long ones by a warp); the dense
+//            rows are written by the CTC path's all-SM gradient stream from
+//            the rows' class sums.
 #include <cstdint>
 
 #include "ctc_common.cuh"
@@ -67,16 +70,16 @@ constexpr int kShortList = 8;         // label lists up to this long are summed 
 
 // Workspace of the FSA path.  Per sequence: log Z (double), Z in extended
 // range, and the number of distinct labels (-1: the sequence was rejected);
-// per frame: the forward values of every state in extended range; per row:
-// the class-sum header and sums read by the gradient stream; per state:
-// offsets of its incoming and outgoing edge lists; per edge: the records of
-// both lists, each edge's position in label order and the occupancies of two
-// frames.
+// per frame: the forward and backward values of every state in extended
+// range and the frame's label values; per row: the class-sum header and sums
+// read by the gradient stream; per state: offsets of its incoming and
+// outgoing edge lists; per edge: the records of both lists, each edge's
+// position in label order and its record at that position.
 struct FsaLayout {
-    size_t off_z, off_nlab, off_zx, off_alpha, off_head, off_ent;
-    size_t off_inoff, off_outoff, off_rin, off_rout, off_lpos, off_tmp, off_labs, off_laboff, off_occ, total;
+    size_t off_z, off_nlab, off_zx, off_alpha, off_beta, off_lx, off_head, off_ent;
+    size_t off_inoff, off_outoff, off_rin, off_rout, off_rpos, off_lpos, off_tmp, off_labs, off_laboff, total;
     int cap;       // class sums a row can hold: min(max_labels, D)
-    int E_total;   // edges of all sequences (the occupancy buffers' stride)
+    int E_total;   // edges of all sequences
 };
 __host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int32_t S_total, int32_t E_total,
                                                 int32_t max_states, int32_t max_labels, int32_t D) {
@@ -89,6 +92,8 @@ __host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int3
     L.off_nlab = o;   o = align_up(o + sizeof(int32_t) * Bn, 256);
     L.off_zx = o;     o = align_up(o + 8 * Bn, 256);
     L.off_alpha = o;  o = align_up(o + 8 * (size_t)T_total * (size_t)max_states, 256);
+    L.off_beta = o;   o = align_up(o + 8 * (size_t)T_total * (size_t)max_states, 256);
+    L.off_lx = o;     o = align_up(o + 8 * (size_t)T_total * cap, 256);
     // per row: a header and the row's class sums, in the format the dense
     // gradient stream of the CTC path reads
     L.off_head = o;   o = align_up(o + sizeof(RowHead) * (size_t)T_total, 256);
@@ -97,11 +102,11 @@ __host__ __device__ inline FsaLayout fsa_layout(int64_t T_total, int32_t B, int3
     L.off_outoff = o; o = align_up(o + sizeof(int32_t) * ((size_t)S_total + Bn), 256);
     L.off_rin = o;    o = align_up(o + sizeof(int4) * (size_t)E_total, 256);
     L.off_rout = o;   o = align_up(o + sizeof(int4) * (size_t)E_total, 256);
+    L.off_rpos = o;   o = align_up(o + sizeof(int4) * (size_t)E_total, 256);  // records in label order
     L.off_lpos = o;   o = align_up(o + sizeof(int32_t) * (size_t)E_total, 256);  // position in label order
     L.off_tmp = o;    o = align_up(o + sizeof(int32_t) * (size_t)E_total, 256);
     L.off_labs = o;   o = align_up(o + sizeof(int32_t) * Bn * cap, 256);
     L.off_laboff = o; o = align_up(o + sizeof(int32_t) * Bn * (cap + 1), 256);
-    L.off_occ = o;    o = align_up(o + sizeof(float) * 2 * (size_t)E_total, 256);
     L.total = o;
     return L;
 }
@@ -307,10 +312,6 @@ __device__ __forceinline__ XSum block_xsum(XSum a, XP* red) {
     return r;
 }
 
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-
 }  // namespace
 
 // Sorted edge lists of sequence b (see the file comment).  A sequence that
@@ -398,7 +399,8 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     __syncthreads();
 
     // 3. outgoing lists (by source): records (to, label slot, log weight,
-    //    the edge's position in label order)
+    //    the edge's position in label order); and at each position in label
+    //    order the edge's record (from, to, label slot, log weight)
     int* outoff = ws_at<int32_t>(a.ws, a.L.off_outoff) + s0 + b;
     for (int s = threadIdx.x; s < S; s += blockDim.x) cnt[s] = 0;
     __syncthreads();
@@ -407,9 +409,11 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     scan_counts(cnt, S, s_warp, outoff);
     place_stable(E, [&](int e) { return ed[3 * e]; }, cnt, tmp);
     int4* rout = ws_at<int4>(a.ws, a.L.off_rout) + e0;
+    int4* rpos = ws_at<int4>(a.ws, a.L.off_rpos) + e0;
     for (int k = threadIdx.x; k < E; k += blockDim.x) {
         const int e = tmp[k];
         rout[k] = make_int4(ed[3 * e + 1], slot[ed[3 * e + 2]], __float_as_int(ew[e]), lpos[e]);
+        rpos[lpos[e]] = make_int4(ed[3 * e], ed[3 * e + 1], slot[ed[3 * e + 2]], __float_as_int(ew[e]));
     }
     if (threadIdx.x == 0) nlab_out[b] = nlab;
 }
@@ -425,17 +429,13 @@ __host__ __device__ constexpr int fsa_ring(int per) { return per > 4 ? 2 : 4; }
 struct FsaSmem {
     int4* rec;        // edge records of the list (incoming or outgoing), ecap_smem
     int* off;         // list offsets per state, Smax + 1
-    float* occ;       // (backward) occupancies of two frames, 2 * ecap_smem
     XP* val;          // alpha or beta of two frames, 2 * Smax
     XP* lpx;          // exp of the label values of two frames, 2 * cap
-    int* longl;       // (backward) the labels with long edge lists, cap
     uint32_t* ring;   // words holding the label values of `ring` frames, ring * cap
-    XP* aring;        // (backward) stored alpha rows of `ring` frames, ring * Smax
     int* labs;        // the distinct labels, cap
-    int* laboff;      // (backward) label list offsets, cap + 1
 };
-__host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Smax, int cap, int ring_frames,
-                                                unsigned char* base, FsaSmem* out) {
+__host__ __device__ inline size_t fsa_smem_plan(int ecap, int Smax, int cap, int ring_frames, unsigned char* base,
+                                                FsaSmem* out) {
     size_t o = 0;
     auto take = [&](size_t bytes, size_t align) {
         o = align_up(o, align);
@@ -445,25 +445,17 @@ __host__ __device__ inline size_t fsa_smem_plan(bool backward, int ecap, int Sma
     };
     const size_t rec = take(16 * (size_t)ecap, 16);
     const size_t off = take(4 * ((size_t)Smax + 1), 4);
-    const size_t occ = backward ? take(8 * (size_t)ecap, 4) : 0;
     const size_t val = take(16 * (size_t)Smax, 8);
     const size_t lpx = take(16 * (size_t)cap, 8);
-    const size_t longl = backward ? take(4 * (size_t)cap, 4) : 0;
     const size_t ring = take(4 * (size_t)ring_frames * cap, 4);
-    const size_t aring = backward ? take(8 * (size_t)ring_frames * Smax, 8) : 0;
     const size_t labs = take(4 * (size_t)cap, 4);
-    const size_t laboff = backward ? take(4 * ((size_t)cap + 1), 4) : 0;
     if (out != nullptr) {
         out->rec = reinterpret_cast<int4*>(base + rec);
         out->off = reinterpret_cast<int*>(base + off);
-        out->occ = reinterpret_cast<float*>(base + occ);
         out->val = reinterpret_cast<XP*>(base + val);
         out->lpx = reinterpret_cast<XP*>(base + lpx);
-        out->longl = reinterpret_cast<int*>(base + longl);
         out->ring = reinterpret_cast<uint32_t*>(base + ring);
-        out->aring = reinterpret_cast<XP*>(base + aring);
         out->labs = reinterpret_cast<int*>(base + labs);
-        out->laboff = reinterpret_cast<int*>(base + laboff);
     }
     return align_up(o, 16);
 }
@@ -498,13 +490,12 @@ struct EdgeRegs {
     int peer[PER][RE];   // the other state of each edge (source forward, destination backward)
     int slot[PER][RE];   // its label's slot among the sequence's distinct labels
     XP w[PER][RE];       // exp of its log weight
-    int id[PER][RE];     // (backward) its occupancy's index
     int n[PER];          // edges held (at most RE)
     int k0[PER], k1[PER];  // the rest of the list: entries [k0, k1)
 };
 
 // Forward records hold the weight in extended range, backward ones the log
-// weight and the occupancy's index.
+// weight.
 template <bool BACKWARD, int PER, int RE>
 __device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int* off, const int4* rec, int S,
                                                int nst) {
@@ -525,13 +516,7 @@ __device__ __forceinline__ void load_edge_regs(EdgeRegs<PER, RE>& er, const int*
             const int4 r = j < n ? rec[b0 + j] : make_int4(0, 0, 0, 0);
             er.peer[k][j] = r.x;
             er.slot[k][j] = r.y;
-            if (BACKWARD) {
-                er.w[k][j] = xp_exp(__int_as_float(r.z));
-                er.id[k][j] = r.w;
-            } else {
-                er.w[k][j] = XP{__int_as_float(r.z), r.w};
-                er.id[k][j] = 0;
-            }
+            er.w[k][j] = BACKWARD ? xp_exp(__int_as_float(r.z)) : XP{__int_as_float(r.z), r.w};
         }
     }
 }
@@ -609,13 +594,36 @@ __device__ __forceinline__ void convert_row(XP* dst, const uint32_t* lw, const i
         st_xp(dst + i, xp_exp(word_to_float<DT>(lw[i], ((base_half ^ labs[i]) & 1) ^ flip)));
 }
 
+// The same, also keeping the values in the workspace row gdst (the frame's
+// label values, read by the backward's occupancies).
+template <int DT>
+__device__ __forceinline__ void convert_row_keep(XP* dst, XP* gdst, const uint32_t* lw, const int* labs, int flip,
+                                                 int base_half, const LabelLane<DT>& L) {
+    if (L.n == 0) return;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = L.li + j * L.nlt;
+        if (j < L.n) {
+            const XP v = xp_exp(word_to_float<DT>(lw[i], L.par[j] ^ flip));
+            st_xp(dst + i, v);
+            st_xp(gdst + i, v);
+        }
+    }
+    for (int i = L.li + 2 * L.nlt; i < L.nlab; i += L.nlt) {
+        const XP v = xp_exp(word_to_float<DT>(lw[i], ((base_half ^ labs[i]) & 1) ^ flip));
+        st_xp(dst + i, v);
+        st_xp(gdst + i, v);
+    }
+}
+
+// Forward recursion of sequence b (a CTA of fsa_chain_kernel).
 template <int DT, int PER>
-__global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_forward_kernel(FsaArgs a) {
+__device__ __forceinline__ void fsa_alpha_body(const FsaArgs& a, int b) {
     constexpr int RE = PER <= 2 ? 3 : (PER == 4 ? 2 : 1);
     constexpr int RING = fsa_ring(PER);
     extern __shared__ __align__(16) unsigned char fsa_smem[];
     __shared__ XP red[kFsaMaxThreads / 32];
-    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = blockDim.x;
     const int nst = a.nst, li = tid - a.lt0, nlt = a.nlt;  // state threads; this label thread
     const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
     if (nlab < 0) return;  // rejected by the index pass (NaN loss written there)
@@ -625,7 +633,7 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_forward_kernel(FsaArgs 
     const int T = a.lengths[b];
     const int Smax = a.max_states, cap = a.L.cap, D = a.D;
     FsaSmem sm;
-    fsa_smem_plan(false, a.ecap_smem, Smax, cap, RING, fsa_smem, &sm);
+    fsa_smem_plan(a.ecap_smem, Smax, cap, RING, fsa_smem, &sm);
     const int* inoff_g = ws_at<int32_t>(a.ws, a.L.off_inoff) + s0 + b;
     const int4* rin_g = ws_at<int4>(a.ws, a.L.off_rin) + e0;
     const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
@@ -717,48 +725,36 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_forward_kernel(FsaArgs 
     }
 }
 
+// Backward recursion of sequence b (a CTA of fsa_chain_kernel, beside the
+// forward recursion): beta_t(s) over the state's outgoing edges in list
+// order, from beta_T(s) = exp(final(s)) down; every beta_t row and every
+// frame's label values are kept for the backward call's occupancies.
 template <int DT, int PER>
-__global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs a) {
+__device__ __forceinline__ void fsa_beta_body(const FsaArgs& a, int b) {
     constexpr int RE = PER <= 2 ? 3 : (PER == 4 ? 2 : 1);
     constexpr int RING = fsa_ring(PER);
     extern __shared__ __align__(16) unsigned char fsa_smem[];
-    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
-    const int nst = a.nst, nws = nst >> 5, li = tid - a.lt0, nlt = a.nlt;  // state threads and warps; label thread
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int nst = a.nst, li = tid - a.lt0, nlt = a.nlt;  // state threads; this label thread
     const int nlab = ws_at<int32_t>(a.ws, a.L.off_nlab)[b];
-    if (nlab < 0) return;  // the rows keep zero headers: zero gradient
+    if (nlab < 0) return;  // rejected by the index pass
     const int s0 = a.state_offsets[b], S = a.state_offsets[b + 1] - s0;
     const int e0 = a.edge_offsets[b], E = a.edge_offsets[b + 1] - e0;
     const int64_t start = a.cu[b];
     const int T = a.lengths[b];
     const int Smax = a.max_states, cap = a.L.cap, D = a.D;
-    const double lz = ws_at<double>(a.ws, a.L.off_z)[b];
-    RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
-    float scale = a.grad_loss[b];
-    if (!(lz > -INFINITY)) scale = 0.0f;  // no path: zero rows (defined only with zero_infinity)
-    if (scale == 0.0f) {
-        // no occupancy is read: the rows are scale * exp(lp) with no class sums
-        for (int t = tid; t < T; t += nt) head[start + t] = RowHead{0, scale, 1, 0};
-        return;
-    }
-    // an edge's occupancy is alpha_t(s) x (its term) / Z: 1 / Z's mantissa
-    // (in [1, 2)) and its exponent, once
-    const XP zx = ld_xp(ws_at<XP>(a.ws, a.L.off_zx) + b);
-    const float izm = 1.0f / zx.m;
     FsaSmem sm;
-    fsa_smem_plan(true, a.ecap_smem, Smax, cap, RING, fsa_smem, &sm);
+    fsa_smem_plan(a.ecap_smem, Smax, cap, RING, fsa_smem, &sm);
     const int* outoff_g = ws_at<int32_t>(a.ws, a.L.off_outoff) + s0 + b;
     const int4* rout_g = ws_at<int4>(a.ws, a.L.off_rout) + e0;
     const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
-    const int* laboff_g = ws_at<int32_t>(a.ws, a.L.off_laboff) + (size_t)b * (cap + 1);
-    float* occ_g = ws_at<float>(a.ws, a.L.off_occ) + e0;
-    const XP* alpha_rows = ws_at<XP>(a.ws, a.L.off_alpha);
-    int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
+    XP* beta_rows = ws_at<XP>(a.ws, a.L.off_beta);
+    XP* lx_rows = ws_at<XP>(a.ws, a.L.off_lx);
     const uintptr_t lp0 = reinterpret_cast<uintptr_t>(a.lp);
     const uintptr_t lp_end = lp0 + (uintptr_t)(a.T_total * (int64_t)D * (DT == 0 ? 4 : 2));
     const int base_half = (int)((lp0 >> 1) & 1);
 
-    // the sequence's outgoing lists, label lists and occupancies in shared
-    // memory when they fit
+    // the sequence's outgoing lists into shared memory when they fit
     const bool local = E <= a.ecap_smem;
     if (local) {
         for (int k = tid; k < E; k += nt) sm.rec[k] = rout_g[k];
@@ -766,43 +762,22 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
     }
     const int4* rout = local ? sm.rec : rout_g;
     const int* outoff = local ? sm.off : outoff_g;
-    float* occ_base = local ? sm.occ : occ_g;
-    const size_t occ_stride = local ? (size_t)a.ecap_smem : (size_t)a.L.E_total;
-    __shared__ int s_nlong;
-    if (tid == 0) s_nlong = 0;
-    for (int i = tid; i < nlab; i += nt) sm.labs[i] = labs_g[i];
-    for (int i = tid; i <= nlab; i += nt) sm.laboff[i] = laboff_g[i];
-    __syncthreads();
-    // the labels whose lists a warp sums (any order: each sum is one warp's)
-    for (int i = tid; i < nlab; i += nt)
-        if (sm.laboff[i + 1] - sm.laboff[i] > kShortList) sm.longl[atomicAdd(&s_nlong, 1)] = i;
-    // frame f's label words (label threads) and its stored alpha row (each
-    // state thread copies its own states' values) are copied RING - 1 frames
-    // ahead
+    // the label threads load, copy and convert their own labels (no barrier
+    // between): label words of frames T - 1 .. T - RING + 1 in flight
+    if ((unsigned)li < (unsigned)nlt)
+        for (int i = li; i < nlab; i += nlt) sm.labs[i] = labs_g[i];
     const LabelLane<DT> ll = label_lane<DT>(sm.labs, nlab, li, nlt, base_half);
     auto issue = [&](int f) {
-        if (f >= 0) {
-            issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, lp_end, ll);
-            if (tid < nst) {
-#pragma unroll
-                for (int k = 0; k < PER; ++k) {
-                    const int s = tid + k * nst;
-                    if (s < S)
-                        cp_async8(smem_addr(sm.aring + (f % RING) * Smax + s),
-                                  alpha_rows + (start + f) * (int64_t)Smax + s);
-                }
-            }
-        }
+        if (f >= 0) issue_row<DT>(sm.ring + (f % RING) * cap, a.lp, start + f, D, a.T_total, sm.labs, lp_end, ll);
         cp_async_commit();
     };
     for (int j = 0; j < RING - 1; ++j) issue(T - 1 - j);
     for (int s = tid; s < S; s += nt) st_xp(sm.val + s, xp_exp(a.final_weight[s0 + s]));
     cp_async_wait<RING - 2>();
     if (T > 0)
-        convert_row<DT>(sm.lpx + ((T - 1) & 1) * cap, sm.ring + ((T - 1) % RING) * cap, sm.labs,
-                        row_flip(start + T - 1, D), base_half, ll);
+        convert_row_keep<DT>(sm.lpx + ((T - 1) & 1) * cap, lx_rows + (start + T - 1) * (int64_t)cap,
+                             sm.ring + ((T - 1) % RING) * cap, sm.labs, row_flip(start + T - 1, D), base_half, ll);
     __syncthreads();
-    const int nlong = s_nlong;
     EdgeRegs<PER, RE> er;
     load_edge_regs<true>(er, outoff, rout, S, nst);
     int p = 0;
@@ -811,85 +786,246 @@ __global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_backward_kernel(FsaArgs
         const XP* bep = sm.val + p * Smax;  // beta_{t+1}
         XP* beq = sm.val + (p ^ 1) * Smax;
         const XP* lx = sm.lpx + (t & 1) * cap;  // the frame's label values
-        const XP* arow = sm.aring + (t % RING) * Smax;
-        float* occ = occ_base + (size_t)(t & 1) * occ_stride;
+        XP* row = beta_rows + (start + t) * (int64_t)Smax;
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const int s = tid + k * nst;
             if (tid < nst && s < S) {
-                const XP as = ld_xp(arow + s);
-                const float gm = as.m * izm;
-                const int ge = as.e - zx.e;
                 // beta_t(s) = sum over the outgoing list, in order, of
-                // exp(weight) x exp(lp[t, label]) x beta_{t+1}(to); each
-                // term times alpha_t(s) / Z is the edge's occupancy
+                // exp(weight) x exp(lp[t, label]) x beta_{t+1}(to)
                 XSum acc;
 #pragma unroll
-                for (int j = 0; j < RE; ++j) {
-                    if (j < er.n[k]) {
-                        const XP x = xp_mul3(er.w[k][j], ld_xp(lx + er.slot[k][j]), ld_xp(bep + er.peer[k][j]));
-                        acc.add(x);
-                        occ[er.id[k][j]] = x.m * gm * pow2_any(x.e + ge);
-                    }
-                }
+                for (int j = 0; j < RE; ++j)
+                    if (j < er.n[k]) acc.add(xp_mul3(er.w[k][j], ld_xp(lx + er.slot[k][j]), ld_xp(bep + er.peer[k][j])));
                 for (int kk = er.k0[k]; kk < er.k1[k]; ++kk) {
                     const int4 r = rout[kk];
-                    const XP x = xp_mul3(xp_exp(__int_as_float(r.z)), ld_xp(lx + r.y), ld_xp(bep + r.x));
-                    acc.add(x);
-                    occ[r.w] = x.m * gm * pow2_any(x.e + ge);
+                    acc.add(xp_mul3(xp_exp(__int_as_float(r.z)), ld_xp(lx + r.y), ld_xp(bep + r.x)));
                 }
-                st_xp(beq + s, xp_norm(acc.S, acc.E));
+                const XP v = xp_norm(acc.S, acc.E);
+                st_xp(beq + s, v);
+                st_xp(row + s, v);  // beta_t, read by the backward
             }
         }
         cp_async_wait<RING - 2>();
         if (t > 0)
-            convert_row<DT>(sm.lpx + ((t - 1) & 1) * cap, sm.ring + ((t - 1) % RING) * cap, sm.labs,
-                            row_flip(start + t - 1, D), base_half, ll);
+            convert_row_keep<DT>(sm.lpx + ((t - 1) & 1) * cap, lx_rows + (start + t - 1) * (int64_t)cap,
+                                 sm.ring + ((t - 1) % RING) * cap, sm.labs, row_flip(start + t - 1, D), base_half, ll);
         __syncthreads();
-        // the row's class sums (class, -scale * occupancy), each label's edges
-        // in list order; the dense rows are written afterwards by the all-SM
-        // gradient stream
-        const int64_t row = start + t;
-        const int n = nlab;
-        // a label's occupancies are the contiguous range [laboff[i],
-        // laboff[i + 1]) in edge order.  Short lists: a thread each, in order,
-        // the label threads taking their own labels
-        for (int i = li; (unsigned)li < (unsigned)nlt && i < n; i += nlt) {
-            const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
-            if (k1 - k0 > kShortList) continue;
-            float P = 0.0f;
-#pragma unroll
-            for (int j = 0; j < kShortList; ++j)
-                if (k0 + j < k1) P += occ[k0 + j];
-            ent[row * cap + i] = make_int2(sm.labs[i], __float_as_int(-scale * P));
-        }
-        // long lists (the blank of a CTC lattice has about two edges per
-        // label): a state warp each, from the last state warp down (the last
-        // warps hold the fewest states), lane l summing entries l, l + 32, ...
-        // in order, then a fixed shuffle tree
-        for (int q = nws - 1 - warp; warp < nws && q < (n > 0 ? nlong : 0); q += nws) {
-            const int i = sm.longl[q];
-            const int k0 = sm.laboff[i], k1 = sm.laboff[i + 1];
-            // four independent partial sums per lane (entries l, l + 32, l + 64,
-            // l + 96 of each block of 128), combined in a fixed order
-            float P0 = 0.0f, P1 = 0.0f, P2 = 0.0f, P3 = 0.0f;
-            int k = k0 + lane;
-            for (; k + 96 < k1; k += 128) {
-                P0 += occ[k];
-                P1 += occ[k + 32];
-                P2 += occ[k + 64];
-                P3 += occ[k + 96];
-            }
-            for (; k < k1; k += 32) P0 += occ[k];
-            float P = (P0 + P1) + (P2 + P3);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) P += __shfl_xor_sync(0xffffffffu, P, o);
-            if (lane == 0) ent[row * cap + i] = make_int2(sm.labs[i], __float_as_int(-scale * P));
-        }
-        if (tid == 0) head[row] = RowHead{n, scale, 1, 0};
         p ^= 1;
     }
     cp_async_wait<0>();
+}
+
+// The recursions of the forward call: CTA b < B runs sequence b's forward
+// recursion, CTA B + b its backward recursion at the same time.
+template <int DT, int PER>
+__global__ void __launch_bounds__(kFsaMaxThreads, 1) fsa_chain_kernel(FsaArgs a) {
+    if ((int)blockIdx.x < a.B) {
+        fsa_alpha_body<DT, PER>(a, (int)blockIdx.x);
+    } else {
+        fsa_beta_body<DT, PER>(a, (int)blockIdx.x - a.B);
+    }
+}
+
+// Occupancies and class sums of each row, from the rows both recursions
+// kept: edge e = (from, to, label, weight) at frame t has occupancy
+//   alpha_t(from) x exp(weight) x exp(lp[t, label]) x beta_{t+1}(to) / Z,
+// beta_T(to) = exp(final(to)); each label's edges are a contiguous range in
+// label order, summed in that order (up to kShortList by one thread; longer
+// ones by a warp: four lane-strided partial sums, then a fixed shuffle tree),
+// and written as the row's class sums (class, -scale * occupancy) with the
+// row's header.  The dense rows are written afterwards by the all-SM
+// gradient stream.  A CTA takes a contiguous range of rows.
+constexpr int kFsaPostThreads = 128;
+constexpr int kFsaPostBudget = 36 * 1024;  // shared memory a CTA aims at (several CTAs an SM)
+// The sequence whose rows start at or before `row` (the last b with
+// cu[b] <= row; -1 before the first), by binary search.
+__device__ __forceinline__ int fsa_seq_of_row(const int32_t* cu, int B, int64_t row) {
+    int lo = 0, hi = B - 1, ans = -1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] <= row) {
+            ans = mid;
+            lo = mid + 1;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return ans;
+}
+__device__ __forceinline__ XP ldg_xp(const XP* p) {
+    const int2 v = __ldg(reinterpret_cast<const int2*>(p));
+    return XP{__int_as_float(v.x), v.y};
+}
+// Its shared memory: two stages of a row's alpha_t and beta_{t+1} (Smax
+// each) and label values (cap), the next row's copied in while the current
+// one is summed; the sequence's labels, label offsets and long lists (cap);
+// then the sequence's edge records in label order when it has at most
+// a.ecap_smem edges.
+__host__ __device__ inline size_t fsa_post_stage_bytes(int Smax, int cap) { return 16 * (size_t)Smax + 8 * (size_t)cap; }
+__host__ __device__ inline size_t fsa_post_smem(int Smax, int cap, int ecap) {
+    return 2 * fsa_post_stage_bytes(Smax, cap) + 4 * (size_t)cap + 4 * ((size_t)cap + 1) + 4 * (size_t)cap + 16 +
+           16 * (size_t)ecap;
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__global__ void __launch_bounds__(kFsaPostThreads) fsa_post_kernel(FsaArgs a) {
+    extern __shared__ __align__(16) unsigned char fsa_smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = kFsaPostThreads / 32;
+    const int64_t T_total = a.T_total;
+    const int64_t per = (T_total + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = (int64_t)blockIdx.x * per;
+    const int64_t r1 = r0 + per < T_total ? r0 + per : T_total;
+    const int cap = a.L.cap, Smax = a.max_states;
+    // stage q: alpha_t, beta_{t+1} (exp(final) at the last frame), the frame's label values
+    const size_t stage_bytes = fsa_post_stage_bytes(Smax, cap);
+    auto stage_al = [&](int q) { return reinterpret_cast<XP*>(fsa_smem + q * stage_bytes); };
+    auto stage_bn = [&](int q) { return stage_al(q) + Smax; };
+    auto stage_lx = [&](int q) { return stage_al(q) + 2 * Smax; };
+    int* const slabs = reinterpret_cast<int*>(fsa_smem + 2 * stage_bytes);
+    int* const sloff = slabs + cap;
+    int* const slong = sloff + cap + 1;  // the labels whose lists a warp sums
+    int4* const srp = reinterpret_cast<int4*>(fsa_smem + align_up(2 * stage_bytes + 12 * (size_t)cap + 4, 16));
+    __shared__ int s_nlong;
+    const int32_t* nlab_all = ws_at<int32_t>(a.ws, a.L.off_nlab);
+    const double* z_all = ws_at<double>(a.ws, a.L.off_z);
+    const XP* zx_all = ws_at<XP>(a.ws, a.L.off_zx);
+    const XP* alpha_rows = ws_at<XP>(a.ws, a.L.off_alpha);
+    const XP* beta_rows = ws_at<XP>(a.ws, a.L.off_beta);
+    const XP* lx_rows = ws_at<XP>(a.ws, a.L.off_lx);
+    RowHead* head = ws_at<RowHead>(a.ws, a.L.off_head);
+    int2* ent = ws_at<int2>(a.ws, a.L.off_ent);
+    // the sequence whose labels, offsets and records are held
+    int cur = -1, nlab = -1, s0 = 0, S = 0, T = 0, e0 = 0, nlong = 0;
+    int q = 0;          // the stage of the current row
+    bool have = false;  // the current row's copies were started by the row before
+    int64_t start = 0;
+    float scale = 0.0f, izm = 1.0f;
+    XP zx{0.0f, 0};
+    const int4* rpos = nullptr;
+    int b = r0 < r1 ? fsa_seq_of_row(a.cu, a.B, r0) : -1;  // then walked forward: rows only grow
+    for (int64_t row = r0; row < r1; ++row) {
+        while (b + 1 < a.B && (int64_t)a.cu[b + 1] <= row) ++b;
+        if (b < 0) continue;
+        if (b != cur) {
+            __syncthreads();  // every read of the previous sequence's data is done
+            cur = b;
+            nlab = nlab_all[b];
+            if (nlab < 0) continue;  // rejected: its rows keep zero headers
+            s0 = a.state_offsets[b];
+            S = a.state_offsets[b + 1] - s0;
+            e0 = a.edge_offsets[b];
+            const int E = a.edge_offsets[b + 1] - e0;
+            start = a.cu[b];
+            T = a.lengths[b];
+            const double lz = z_all[b];
+            scale = a.grad_loss[b];
+            if (!(lz > -INFINITY)) scale = 0.0f;  // no path: zero rows (defined only with zero_infinity)
+            zx = ldg_xp(zx_all + b);
+            izm = 1.0f / zx.m;
+            const int* labs_g = ws_at<int32_t>(a.ws, a.L.off_labs) + (size_t)b * cap;
+            const int* laboff_g = ws_at<int32_t>(a.ws, a.L.off_laboff) + (size_t)b * (cap + 1);
+            if (tid == 0) s_nlong = 0;
+            __syncthreads();
+            for (int i = tid; i < nlab; i += kFsaPostThreads) slabs[i] = labs_g[i];
+            for (int i = tid; i <= nlab; i += kFsaPostThreads) sloff[i] = laboff_g[i];
+            // (any order: each long list is summed by one warp)
+            for (int i = tid; i < nlab; i += kFsaPostThreads)
+                if (laboff_g[i + 1] - laboff_g[i] > kShortList) slong[atomicAdd(&s_nlong, 1)] = i;
+            const int4* rpos_g = ws_at<int4>(a.ws, a.L.off_rpos) + e0;
+            if (E <= a.ecap_smem) {
+                for (int k = tid; k < E; k += kFsaPostThreads) srp[k] = rpos_g[k];
+                rpos = srp;
+            } else {
+                rpos = rpos_g;
+            }
+        }
+        const int64_t t = row - start;
+        if (nlab < 0 || t < 0 || t >= T) continue;  // a rejected sequence, or a row outside its frames: zero
+        if (scale == 0.0f) {
+            // no occupancy is read: the row is scale * exp(lp) with no class sums
+            if (tid == 0) head[row] = RowHead{0, scale, 1, 0};
+            continue;
+        }
+        // the row's values, staged: copied into stage q (unless the row
+        // before already started that), and the next row of the sequence
+        // copied into the other stage meanwhile
+        __syncthreads();  // every read of the other stage (the row before) is done
+        nlong = s_nlong;
+        const bool last = t + 1 == T;
+        auto copy_row = [&](int64_t rw, int qq) {
+            const XP* al = alpha_rows + rw * Smax;
+            const XP* bn = beta_rows + (rw + 1) * Smax;
+            const XP* lx = lx_rows + rw * cap;
+            const bool lst = rw - start + 1 == T;
+            XP* dal = stage_al(qq);
+            XP* dbn = stage_bn(qq);
+            XP* dlx = stage_lx(qq);
+            for (int st = tid; st < S; st += kFsaPostThreads) {
+                cp_async8(smem_addr(dal + st), al + st);
+                if (!lst) cp_async8(smem_addr(dbn + st), bn + st);
+            }
+            for (int i = tid; i < nlab; i += kFsaPostThreads) cp_async8(smem_addr(dlx + i), lx + i);
+            cp_async_commit();
+        };
+        if (!have) copy_row(row, q);
+        const bool next = row + 1 < r1 && t + 1 < T;  // the same sequence: the same scale, nothing skipped
+        if (next) {
+            copy_row(row + 1, q ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        if (last)
+            for (int st = tid; st < S; st += kFsaPostThreads) stage_bn(q)[st] = xp_exp(__ldg(a.final_weight + s0 + st));
+        __syncthreads();
+        const XP* sal = stage_al(q);
+        const XP* sbn = stage_bn(q);
+        const XP* slx = stage_lx(q);
+        // the occupancy of the edge at label-order position k
+        auto occ = [&](int k) -> float {
+            const int4 r = rpos[k];
+            const XP as = sal[r.x];
+            const float gm = as.m * izm;
+            const int ge = as.e - zx.e;
+            const XP x = xp_mul3(xp_exp(__int_as_float(r.w)), slx[r.z], sbn[r.y]);
+            return x.m * gm * pow2_any(x.e + ge);
+        };
+        // short lists: a thread each, in order (a plain loop: unrolled to
+        // kShortList with predicates it issued every step for lists of two or
+        // three edges)
+        for (int i = tid; i < nlab; i += kFsaPostThreads) {
+            const int k0 = sloff[i], k1 = sloff[i + 1];
+            if (k1 - k0 > kShortList) continue;
+            float P = 0.0f;
+            for (int k = k0; k < k1; ++k) P += occ(k);
+            ent[row * cap + i] = make_int2(slabs[i], __float_as_int(-scale * P));
+        }
+        // long lists: a warp each, lane l summing entries l, l + 32, l + 64,
+        // l + 96 of each block of 128 in four partial sums, combined in a
+        // fixed order, then a fixed shuffle tree
+        for (int h = warp; h < nlong; h += nw) {
+            const int i = slong[h];
+            const int k0 = sloff[i], k1 = sloff[i + 1];
+            float P0 = 0.0f, P1 = 0.0f, P2 = 0.0f, P3 = 0.0f;
+            int k = k0 + lane;
+            for (; k + 96 < k1; k += 128) {
+                P0 += occ(k);
+                P1 += occ(k + 32);
+                P2 += occ(k + 64);
+                P3 += occ(k + 96);
+            }
+            for (; k < k1; k += 32) P0 += occ(k);
+            float P = (P0 + P1) + (P2 + P3);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) P += __shfl_xor_sync(0xffffffffu, P, o);
+            if (lane == 0) ent[row * cap + i] = make_int2(slabs[i], __float_as_int(-scale * P));
+        }
+        if (tid == 0) head[row] = RowHead{nlab, scale, 1, 0};
+        have = next;
+        q ^= 1;
+    }
 }
 
 // Every row's header starts as "not covered, no class sums"; the backward
@@ -944,11 +1080,13 @@ int ring_for(int max_states) {
     return fsa_ring((max_states + nt - 1) / nt);
 }
 
-// The backward's per-frame buffers (the larger plan) within a CTA's shared
-// memory: max_states and max_labels bound them together.
+// A recursion CTA's per-frame buffers, and the row kernel's two stages of
+// a row, each within a CTA's shared memory: max_states and max_labels bound
+// them together.
 bool fsa_plan_fits(int max_states, int max_labels, int D) {
     const int cap = max_labels < D ? max_labels : D;
-    return fsa_smem_plan(true, 0, max_states, cap, ring_for(max_states), nullptr, nullptr) <= (size_t)kFsaSmemLimit;
+    return fsa_smem_plan(0, max_states, cap, ring_for(max_states), nullptr, nullptr) <= (size_t)kFsaSmemLimit &&
+           fsa_post_smem(max_states, cap, 0) <= (size_t)kFsaSmemLimit;
 }
 
 ctc_packed_status fsa_check_args(const void* log_probs, int dtype, int64_t T_total, int32_t D, const int32_t* cu,
@@ -984,17 +1122,15 @@ cudaError_t launch_fsa(K kernel, unsigned grid, int threads, size_t smem, cudaSt
     return cudaGetLastError();
 }
 
-// Edges of one sequence a recursion CTA keeps in shared memory (16 bytes an
-// edge forward; 24 backward: the record and two occupancies): four times the
-// batch's mean per sequence (at least 1024), at most what the budget leaves
-// after the per-frame buffers and at most the batch's edges, so that CTAs of
-// ordinary sequences share an SM.  A sequence with more edges reads its lists
-// from the workspace.
-int smem_edges(bool backward, int B, int E_total, int max_states, int cap) {
-    const size_t fixed = fsa_smem_plan(backward, 0, max_states, cap, ring_for(max_states), nullptr, nullptr);
-    const size_t per = backward ? 24 : 16;
+// Edges of one sequence a recursion CTA keeps in shared memory (a 16-byte
+// record each): four times the batch's mean per sequence (at least 1024), at
+// most what the budget leaves after the per-frame buffers and at most the
+// batch's edges, so that CTAs of ordinary sequences share an SM.  A sequence
+// with more edges reads its lists from the workspace.
+int smem_edges(int B, int E_total, int max_states, int cap) {
+    const size_t fixed = fsa_smem_plan(0, max_states, cap, ring_for(max_states), nullptr, nullptr);
     if (fixed + 64 >= (size_t)kFsaSmemBudget) return 0;
-    size_t e = ((size_t)kFsaSmemBudget - fixed - 64) / per;
+    size_t e = ((size_t)kFsaSmemBudget - fixed - 64) / 16;
     size_t want = 4 * (((size_t)E_total + (size_t)B - 1) / (size_t)(B > 0 ? B : 1));
     if (want < 1024) want = 1024;
     if (e > want) e = want;
@@ -1002,23 +1138,17 @@ int smem_edges(bool backward, int B, int E_total, int max_states, int cap) {
     return (int)e;
 }
 
-// The forward or backward recursion with PER states a thread: the smallest
-// of 1, 2, 4, 8 that covers max_states with the a.nst state threads (nt
-// threads in all, the label warps included).
-template <int DT, bool BACKWARD>
-cudaError_t launch_recursion(int max_states, int B, int nt, size_t smem, cudaStream_t s, const FsaArgs& a) {
+// Both recursions with PER states a thread (2B CTAs: forward, then
+// backward): the smallest of 1, 2, 4, 8 that covers max_states with the
+// a.nst state threads (nt threads in all, the label warps included).
+template <int DT>
+cudaError_t launch_recursions(int max_states, int B, int nt, size_t smem, cudaStream_t s, const FsaArgs& a) {
     const int per = (max_states + a.nst - 1) / a.nst;
-    if (per <= 1)
-        return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 1>, (unsigned)B, nt, smem, s, a)
-                        : launch_fsa(fsa_forward_kernel<DT, 1>, (unsigned)B, nt, smem, s, a);
-    if (per <= 2)
-        return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 2>, (unsigned)B, nt, smem, s, a)
-                        : launch_fsa(fsa_forward_kernel<DT, 2>, (unsigned)B, nt, smem, s, a);
-    if (per <= 4)
-        return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 4>, (unsigned)B, nt, smem, s, a)
-                        : launch_fsa(fsa_forward_kernel<DT, 4>, (unsigned)B, nt, smem, s, a);
-    return BACKWARD ? launch_fsa(fsa_backward_kernel<DT, 8>, (unsigned)B, nt, smem, s, a)
-                    : launch_fsa(fsa_forward_kernel<DT, 8>, (unsigned)B, nt, smem, s, a);
+    const unsigned grid = 2u * (unsigned)B;
+    if (per <= 1) return launch_fsa(fsa_chain_kernel<DT, 1>, grid, nt, smem, s, a);
+    if (per <= 2) return launch_fsa(fsa_chain_kernel<DT, 2>, grid, nt, smem, s, a);
+    if (per <= 4) return launch_fsa(fsa_chain_kernel<DT, 4>, grid, nt, smem, s, a);
+    return launch_fsa(fsa_chain_kernel<DT, 8>, grid, nt, smem, s, a);
 }
 
 FsaArgs make_fsa_args(const void* log_probs, int64_t T_total, int32_t D, const int32_t* cu, const int32_t* lengths,
@@ -1085,13 +1215,14 @@ ctc_packed_status ctc_packed_fsa_forward(const void* log_probs, ctc_packed_dtype
     const size_t ismem = sizeof(int) * ((size_t)(max_states > D ? max_states : D) + (size_t)D);
     if (launch_fsa(fsa_index_kernel, (unsigned)B, kIdxThreads, ismem, stream, a) != cudaSuccess)
         return CTC_PACKED_ERR_CUDA;
-    // 2. per sequence: the forward recursion
+    // 2. per sequence: the forward recursion (the loss) and, beside it, the
+    //    backward recursion (beta rows and label values for the gradient)
     const int nt = recursion_geometry(a, max_states);
-    a.ecap_smem = smem_edges(false, B, num_edges, max_states, a.L.cap);
-    const size_t smem = fsa_smem_plan(false, a.ecap_smem, max_states, a.L.cap, ring_for(max_states), nullptr, nullptr);
-    const cudaError_t e = dtype == CTC_PACKED_F32    ? launch_recursion<0, false>(max_states, B, nt, smem, stream, a)
-                          : dtype == CTC_PACKED_BF16 ? launch_recursion<1, false>(max_states, B, nt, smem, stream, a)
-                                                     : launch_recursion<2, false>(max_states, B, nt, smem, stream, a);
+    a.ecap_smem = smem_edges(B, num_edges, max_states, a.L.cap);
+    const size_t smem = fsa_smem_plan(a.ecap_smem, max_states, a.L.cap, ring_for(max_states), nullptr, nullptr);
+    const cudaError_t e = dtype == CTC_PACKED_F32    ? launch_recursions<0>(max_states, B, nt, smem, stream, a)
+                          : dtype == CTC_PACKED_BF16 ? launch_recursions<1>(max_states, B, nt, smem, stream, a)
+                                                     : launch_recursions<2>(max_states, B, nt, smem, stream, a);
     return e == cudaSuccess ? CTC_PACKED_OK : CTC_PACKED_ERR_CUDA;
 }
 
@@ -1125,17 +1256,27 @@ ctc_packed_status ctc_packed_fsa_backward(const void* log_probs, ctc_packed_dtyp
     const long long hgrid = (T_total + 255) / 256;
     if (launch_fsa(fsa_head_init_kernel, (unsigned)(hgrid < 4096 ? hgrid : 4096), 256, 0, stream, a) != cudaSuccess)
         return CTC_PACKED_ERR_CUDA;
-    // 2. per sequence: beta, edge occupancies, each row's class sums and header
+    // 2. per row: the edge occupancies from the forward's kept rows, each
+    //    row's class sums and header (a contiguous range of rows a CTA)
     if (B > 0) {
-        const int nt = recursion_geometry(a, max_states);
-        a.ecap_smem = smem_edges(true, B, num_edges, max_states, a.L.cap);
-        const size_t smem =
-            fsa_smem_plan(true, a.ecap_smem, max_states, a.L.cap, ring_for(max_states), nullptr, nullptr);
-        const cudaError_t e =
-            dtype == CTC_PACKED_F32    ? launch_recursion<0, true>(max_states, B, nt, smem, stream, a)
-            : dtype == CTC_PACKED_BF16 ? launch_recursion<1, true>(max_states, B, nt, smem, stream, a)
-                                       : launch_recursion<2, true>(max_states, B, nt, smem, stream, a);
-        if (e != cudaSuccess) return CTC_PACKED_ERR_CUDA;
+        // the row staging, and the sequence's edge records up to a share of
+        // an SM's shared memory that leaves room for several CTAs
+        const size_t fixed = fsa_post_smem(max_states, a.L.cap, 0);
+        const size_t room = fixed < (size_t)kFsaPostBudget ? ((size_t)kFsaPostBudget - fixed) / 16 : 0;
+        a.ecap_smem = (int)(room < (size_t)num_edges ? room : (size_t)num_edges);
+        const size_t smem = fsa_post_smem(max_states, a.L.cap, a.ecap_smem);
+        int dev = 0, sms = 0, per_sm = 0;
+        if (cudaFuncSetAttribute(fsa_post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess ||
+            cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fsa_post_kernel, kFsaPostThreads, smem) !=
+                cudaSuccess)
+            return CTC_PACKED_ERR_CUDA;
+        long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
+        if (grid > T_total) grid = T_total;
+        if (launch_fsa(fsa_post_kernel, (unsigned)grid, kFsaPostThreads, smem, stream, a) != cudaSuccess)
+            return CTC_PACKED_ERR_CUDA;
     }
     // 3. the dense rows, scale * exp(lp) + class sums, by the CTC path's
     //    all-SM gradient stream over this workspace's headers and sums

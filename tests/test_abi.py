@@ -174,8 +174,8 @@ def test_fsa_host_checks_return_before_any_cuda_call(lib):
     assert _fsa_fwd(lib, ms=4097) == UNSUPPORTED  # more states than a shared-memory row holds
     assert _fsa_fwd(lib, D=16385) == UNSUPPORTED
     # states and labels whose per-frame shared-memory buffers exceed a CTA's
-    assert _fsa_fwd(lib, ms=4096, ml=3000, D=16384) == UNSUPPORTED
-    assert _fsa_fwd(lib, ms=2048, ml=3000, D=16384) == UNSUPPORTED
+    assert _fsa_fwd(lib, ms=4096, ml=3700, D=16384) == UNSUPPORTED
+    assert _fsa_fwd(lib, ms=2048, ml=5500, D=16384) == UNSUPPORTED
     assert _fsa_fwd(lib, ws=None) == WORKSPACE
     assert _fsa_fwd(lib, ws=128) == WORKSPACE  # not 256-byte aligned
     assert _fsa_fwd(lib, wsb=64) == WORKSPACE
@@ -193,14 +193,15 @@ def test_fsa_workspace_size():
     assert f(100, 4, 20, -1, 10, 5, 10) == 0
     assert f(100, 4, 20, 60, 10, 5, 16385) == 0
     n = f(1000, 4, 200, 600, 50, 20, 30)
-    # alpha rows (8 B x states, extended range) and class sums (8 B x min(labels, D)) per frame, and
-    # per edge two 16-byte list records and two occupancies at least
-    assert n >= 1000 * 50 * 8 + 1000 * 20 * 8 + 1000 * 8 + 600 * (32 + 8)
-    # a recursion's per-frame buffers must fit a CTA's shared memory: about 52 bytes a state and
-    # 44 a label up to 2048 states (36 and 36 above)
-    assert f(1000, 4, 200, 600, 2048, 2000, 16384) > 0
-    assert f(1000, 4, 200, 600, 2048, 3000, 16384) == 0
-    assert f(1000, 4, 200, 600, 4096, 1000, 16384) > 0
-    assert f(1000, 4, 200, 600, 4096, 3000, 16384) == 0
+    # alpha and beta rows (8 B x states each, extended range), label values and class sums (8 B x
+    # min(labels, D) each) per frame, and per edge three 16-byte records and two positions at least
+    assert n >= 1000 * 50 * 16 + 1000 * 20 * 16 + 1000 * 8 + 600 * (48 + 8)
+    # a recursion's per-frame buffers (about 20 bytes a state and 36 a label up to 2048 states, 28
+    # a label above) and the row kernel's two stages of a row (32 bytes a state, 28 a label) must
+    # each fit a CTA's shared memory
+    assert f(1000, 4, 200, 600, 2048, 5000, 16384) > 0
+    assert f(1000, 4, 200, 600, 2048, 5500, 16384) == 0
+    assert f(1000, 4, 200, 600, 4096, 3400, 16384) > 0
+    assert f(1000, 4, 200, 600, 4096, 3600, 16384) == 0
     assert f(1000, 4, 200, 600, 50, 200, 30) < f(1000, 4, 200, 600, 50, 200, 300)  # class sums capped at D
     assert f(1000, 4, 200, 600, 50, 20, 30) < f(1000, 4, 200, 6000, 50, 20, 30)  # edge lists grow with edges
