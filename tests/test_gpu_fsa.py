@@ -259,3 +259,22 @@ def test_many_distinct_labels(cuda_device, dtype, S, E, D):
     ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
     assert_loss_close(loss, ref_loss)
     assert_grad_close(grad, ref_grad, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_sizes_beyond_the_older_shared_memory_limit(cuda_device, dtype):
+    # 2048 states and about 3 100 distinct labels: beyond what the kernels
+    # accepted when the backward recursion formed the occupancies itself
+    # (CTC_PACKED_ERR_UNSUPPORTED then).  At this size the recursions' edge
+    # lists and the row kernel's edge records both stay in the workspace.
+    D = 3500
+    lp = torch.log_softmax(torch.randn(60, D, generator=torch.Generator().manual_seed(23)) * 2.0, -1).to(dtype)
+    fsa = workloads.pack_fsas([workloads.random_fsa(2048, 8000, D, seed=71), workloads.random_fsa(9, 50, D, seed=72)])
+    cu = torch.tensor([0, 40, 60], dtype=torch.int32)
+    ln = torch.tensor([40, 20], dtype=torch.int32)
+    assert _max_states(fsa) == 2048 and _max_labels(fsa) > 3000
+    loss, grad, status, g = _run(lp, cu, ln, fsa, _max_states(fsa), grad_loss=[0.9, 1.1])
+    assert status == 0
+    ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)
