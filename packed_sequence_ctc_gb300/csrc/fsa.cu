@@ -210,24 +210,35 @@ __device__ int fsa_block_scan(int v, int* s_warp, int* total) {
     return prefix;
 }
 
+// The contiguous segment [*b0, *b1) of K entries that this thread scans in
+// turn around one block-wide scan of the segments' totals (a few barriers,
+// not a block scan per blockDim.x entries).
+__device__ __forceinline__ void scan_segment(int K, int* b0, int* b1) {
+    const int seg = (K + (int)blockDim.x - 1) / (int)blockDim.x;
+    *b0 = min((int)threadIdx.x * seg, K);
+    *b1 = min(*b0 + seg, K);
+}
+
 // cnt[0 .. K) becomes the exclusive prefix of itself (also written to
 // off_out[0 .. K] when given, off_out[K] = the total); returns the total.
+// (The block scan's first barrier also orders every thread's earlier reads
+// of cnt before these writes.)
 __device__ int scan_counts(int* cnt, int K, int* s_warp, int* off_out) {
-    int run = 0;
-    for (int k0 = 0; k0 < K; k0 += blockDim.x) {
-        const int k = k0 + threadIdx.x;
-        const int v = k < K ? cnt[k] : 0;
-        int total;
-        const int pre = fsa_block_scan(v, s_warp, &total);
-        if (k < K) {
-            cnt[k] = run + pre;
-            if (off_out != nullptr) off_out[k] = run + pre;
-        }
-        run += total;
+    int b0, b1;
+    scan_segment(K, &b0, &b1);
+    int local = 0;
+    for (int k = b0; k < b1; ++k) local += cnt[k];
+    int total;
+    int run = fsa_block_scan(local, s_warp, &total);
+    for (int k = b0; k < b1; ++k) {
+        const int v = cnt[k];
+        cnt[k] = run;
+        if (off_out != nullptr) off_out[k] = run;
+        run += v;
     }
-    if (off_out != nullptr && threadIdx.x == 0) off_out[K] = run;
+    if (off_out != nullptr && threadIdx.x == 0) off_out[K] = total;
     __syncthreads();
-    return run;
+    return total;
 }
 
 // Places edge e at cursor[key(e)]++ in edge order (a stable counting sort's
@@ -351,13 +362,17 @@ __global__ void __launch_bounds__(kIdxThreads) fsa_index_kernel(FsaArgs a) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) atomicAdd(&cnt[ed[3 * e + 2]], 1);
     __syncthreads();
     int nlab = 0;
-    for (int c0 = 0; c0 < D; c0 += blockDim.x) {
-        const int c = c0 + threadIdx.x;
-        const int f = c < D && cnt[c] > 0 ? 1 : 0;
-        int total;
-        const int pre = fsa_block_scan(f, s_warp, &total);
-        if (c < D) slot[c] = nlab + pre;
-        nlab += total;
+    {
+        int b0, b1;
+        scan_segment(D, &b0, &b1);
+        int local = 0;
+        for (int c = b0; c < b1; ++c) local += cnt[c] > 0 ? 1 : 0;
+        int run = fsa_block_scan(local, s_warp, &nlab);
+        for (int c = b0; c < b1; ++c) {
+            slot[c] = run;
+            run += cnt[c] > 0 ? 1 : 0;
+        }
+        __syncthreads();  // slots are read across the segments below
     }
     if (nlab > cap) {
         if (threadIdx.x == 0) set_status(ws_at<Control>(a.ws, 0), CTC_PACKED_DEV_BAD_FSA);
