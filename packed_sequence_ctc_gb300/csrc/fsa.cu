@@ -310,6 +310,23 @@ struct XSum {
     }
 };
 
+// The sum of a state's held terms (zero where it holds fewer): all aligned
+// at once to their largest exponent and added in list order, as the first
+// value of its running sum.
+template <int N>
+__device__ __forceinline__ XSum xsum_held(const XP (&t)[N]) {
+    int E = t[0].e;
+#pragma unroll
+    for (int j = 1; j < N; ++j) E = max(E, t[j].e);
+    float S = t[0].m * pow2_nonpos(t[0].e - E);
+#pragma unroll
+    for (int j = 1; j < N; ++j) S = fmaf(t[j].m, pow2_nonpos(t[j].e - E), S);
+    XSum r;
+    r.S = S;
+    r.E = E;
+    return r;
+}
+
 // Sum over the CTA of every thread's partial sum: the lanes by a fixed
 // shuffle tree, then the warps in order (every thread gets the result).
 __device__ __forceinline__ XSum block_xsum(XSum a, XP* red) {
@@ -696,10 +713,12 @@ __device__ __forceinline__ void fsa_alpha_body(const FsaArgs& a, int b) {
                 st_xp(row + s, ld_xp(alp + s));  // alpha_t, read by the backward
                 // alpha_{t+1}(s) = sum over the incoming list, in order, of
                 // alpha_t(from) x exp(weight) x exp(lp[t, label])
-                XSum acc;
+                XP hold[RE];
 #pragma unroll
                 for (int j = 0; j < RE; ++j)
-                    if (j < er.n[k]) acc.add(xp_mul3(ld_xp(alp + er.peer[k][j]), er.w[k][j], ld_xp(lx + er.slot[k][j])));
+                    hold[j] = j < er.n[k] ? xp_mul3(ld_xp(alp + er.peer[k][j]), er.w[k][j], ld_xp(lx + er.slot[k][j]))
+                                          : XP{0.0f, kEZero};
+                XSum acc = xsum_held(hold);
                 for (int kk = er.k0[k]; kk < er.k1[k]; ++kk) {
                     const int4 r = rin[kk];
                     acc.add(xp_mul3(ld_xp(alp + r.x), XP{__int_as_float(r.z), r.w}, ld_xp(lx + r.y)));
@@ -808,10 +827,12 @@ __device__ __forceinline__ void fsa_beta_body(const FsaArgs& a, int b) {
             if (tid < nst && s < S) {
                 // beta_t(s) = sum over the outgoing list, in order, of
                 // exp(weight) x exp(lp[t, label]) x beta_{t+1}(to)
-                XSum acc;
+                XP hold[RE];
 #pragma unroll
                 for (int j = 0; j < RE; ++j)
-                    if (j < er.n[k]) acc.add(xp_mul3(er.w[k][j], ld_xp(lx + er.slot[k][j]), ld_xp(bep + er.peer[k][j])));
+                    hold[j] = j < er.n[k] ? xp_mul3(er.w[k][j], ld_xp(lx + er.slot[k][j]), ld_xp(bep + er.peer[k][j]))
+                                          : XP{0.0f, kEZero};
+                XSum acc = xsum_held(hold);
                 for (int kk = er.k0[k]; kk < er.k1[k]; ++kk) {
                     const int4 r = rout[kk];
                     acc.add(xp_mul3(xp_exp(__int_as_float(r.z)), ld_xp(lx + r.y), ld_xp(bep + r.x)));
