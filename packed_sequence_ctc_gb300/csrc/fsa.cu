@@ -1030,8 +1030,13 @@ __global__ void __launch_bounds__(kFsaPostThreads) fsa_post_kernel(FsaArgs a) {
         };
         // short lists: a thread each, in order (a plain loop: unrolled to
         // kShortList with predicates it issued every step for lists of two or
-        // three edges)
-        for (int i = tid; i < nlab; i += kFsaPostThreads) {
+        // three edges).  With fewer long lists than warps and few labels, the
+        // warps that sum the long lists take no short ones (a CTC lattice's
+        // blank list is then the longest single sum of the row); with many
+        // labels every thread takes short lists.
+        const int lw = nlong < nw && nlab <= 2 * (kFsaPostThreads - 32 * nlong) ? nlong : 0;
+        for (int i = tid - 32 * lw; i < nlab; i += kFsaPostThreads - 32 * lw) {
+            if (i < 0) break;
             const int k0 = sloff[i], k1 = sloff[i + 1];
             if (k1 - k0 > kShortList) continue;
             float P = 0.0f;
