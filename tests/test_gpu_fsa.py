@@ -278,3 +278,23 @@ def test_sizes_beyond_the_older_shared_memory_limit(cuda_device, dtype):
     ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
     assert_loss_close(loss, ref_loss)
     assert_grad_close(grad, ref_grad, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
+def test_one_and_two_frame_sequences(cuda_device, dtype):
+    # a sequence of one frame (its only row is its last frame, where the
+    # occupancies take beta_T = exp(final)) and one of two (a 2- and a 3-state
+    # chain: both have a path), beside a longer one, with rows between the
+    # sequences that no sequence covers
+    D = 12
+    lp = torch.log_softmax(torch.randn(30, D, generator=torch.Generator().manual_seed(31)), -1).to(dtype)
+    fsa = workloads.pack_fsas([workloads.random_fsa(2, 6, D, seed=81), workloads.random_fsa(3, 9, D, seed=82),
+                               workloads.random_fsa(6, 18, D, seed=83)])
+    cu = torch.tensor([0, 3, 7, 30], dtype=torch.int32)  # spans of 3, 4 and 23 rows
+    ln = torch.tensor([1, 2, 20], dtype=torch.int32)
+    loss, grad, status, g = _run(lp, cu, ln, fsa, _max_states(fsa), grad_loss=[0.7, 1.3, 0.9])
+    assert status == 0
+    ref_loss, ref_grad = _oracle(lp, cu, ln, fsa, g)
+    assert np.isfinite(ref_loss).all()
+    assert_loss_close(loss, ref_loss)
+    assert_grad_close(grad, ref_grad, dtype)
